@@ -1,0 +1,315 @@
+"""fp64 CPU oracle for the sparsely-gated Mixture-of-Experts forward path.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / ``--impl reference`` legs are the only callers.
+The product library never imports this package and shares no code with it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C, double precision, one loop
+per definition); this module only compiles it with gcc, loads it with ctypes
+and marshals numpy arrays. Each wrapper names the page passage it follows:
+
+* "Outrageously Large Neural Networks: The Sparsely-Gated Mixture-of-Experts
+  Layer" (paper summary), section 3.4: Eq. 4 noisy logits, Eq. 5
+  KeepTopK-softmax, Eqs. 6-7 importance and CV^2, Eqs. 8-10 P(x,i) and load.
+* "Switch Transformer" (abhik.ai), Implementation steps 1-8: fp32 router,
+  argmax gate, capacity, exclusive-cumsum slots, dispatch, ReLU experts,
+  combine with residual, auxiliary loss.
+* "Mixture-of-Experts: Sparse Computation" (cs8803 lesson), Chapters 1, 2, 5.
+
+Parity status: every function is pinned by ``tests/test_oracle_pins.py``
+except the expert FFN's values on random weights, which the pages never print;
+those are pinned only through reductions (dense all-experts sum, the Switch
+page's dispatch/combine einsum algebra, and the E = 1 dense-MLP special case).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+TOPK_SOFTMAX = 0
+SWITCH = 1
+_F32 = 0
+_BF16 = 1
+
+
+def _compile(src: str, out: str) -> None:
+    tmp = out + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so with gcc (OpenMP over tokens)."""
+    stale = (not os.path.exists(_LIB_PATH)) or (
+        os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE))
+    if force or stale:
+        _compile(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return _F32
+    if a.dtype in (np.uint16, np.int16):
+        return _BF16
+    raise TypeError(f"oracle inputs are float32 or bf16 bit patterns, got {a.dtype}")
+
+
+def _f32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float32)
+
+
+class Oracle:
+    """ctypes view of one compiled copy of moe_oracle.c."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.orc_capacity.argtypes = [I, I, I, D, I]
+        lib.orc_capacity.restype = I
+        lib.orc_router.argtypes = [I, I, I, P, I, P, P, P, P, P, P, P]
+        lib.orc_router.restype = I
+        lib.orc_select.argtypes = [I, I, I, I, P, P, P, P, P]
+        lib.orc_select.restype = None
+        lib.orc_gates_given.argtypes = [I, I, I, I, P, P, P]
+        lib.orc_gates_given.restype = None
+        lib.orc_slots.argtypes = [I, I, I, I, P, P, P, P]
+        lib.orc_slots.restype = None
+        lib.orc_layer_out.argtypes = [I, I, I, P, I, P, P, P, P, P, P, P, I, P, I, P]
+        lib.orc_layer_out.restype = I
+        lib.orc_cv2.argtypes = [P, I]
+        lib.orc_cv2.restype = D
+        lib.orc_aux.argtypes = [I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P]
+        lib.orc_aux.restype = None
+        lib.orc_softplus_at.argtypes = [D]
+        lib.orc_softplus_at.restype = D
+        lib.orc_phi_at.argtypes = [D]
+        lib.orc_phi_at.restype = D
+        self.lib = lib
+        self.path = lib_path
+
+    def capacity(self, T: int, E: int, k: int, cf: float, min_cap: int = 1) -> int:
+        """C = max(min_cap, min(T, floor(k*T*cf/E))) (Switch Transformer, step 3)."""
+        return int(self.lib.orc_capacity(T, E, k, float(cf), min_cap))
+
+    def softplus(self, z: float) -> float:
+        return float(self.lib.orc_softplus_at(float(z)))
+
+    def phi(self, u: float) -> float:
+        return float(self.lib.orc_phi_at(float(u)))
+
+    def cv2(self, v) -> float:
+        """Squared coefficient of variation, population std (OLNN Eq. 7)."""
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        return float(self.lib.orc_cv2(_ptr(v), v.size))
+
+    def router(self, x, Wg, Wn=None, noise=None, bias=None):
+        """Clean logits c, noise scale sigma and noisy logits H, each [T,E] fp64,
+        plus a non-finite flag (OLNN Eq. 4; Switch step 1). x is float32 or
+        bf16 bits [T,d]."""
+        x = np.ascontiguousarray(x)
+        T, d = x.shape
+        Wg = _f32(Wg)
+        E = Wg.shape[1]
+        if (Wn is None) != (noise is None):
+            raise ValueError("noise weights and noise come together")
+        Wn, noise, bias = _f32(Wn), _f32(noise), _f32(bias)
+        c = np.empty((T, E), np.float64)
+        s = np.empty((T, E), np.float64)
+        H = np.empty((T, E), np.float64)
+        bad = self.lib.orc_router(T, d, E, _ptr(x), _dtype_code(x), _ptr(Wg), _ptr(Wn),
+                                  _ptr(noise), _ptr(bias), _ptr(c), _ptr(s), _ptr(H))
+        return c, s, H, bool(bad)
+
+    def select(self, H, k: int, mode: int):
+        """Top-k selection and gates (OLNN Eq. 5, or Switch step 2 for
+        mode=SWITCH). Returns idx [T,k] int32, gate [T,k], hk [T] (k-th largest
+        H), hk1 [T] ((k+1)-th largest, -inf when k == E)."""
+        H = np.ascontiguousarray(H, dtype=np.float64)
+        T, E = H.shape
+        if mode == SWITCH and k != 1:
+            raise ValueError("Switch gating is top-1")
+        idx = np.empty((T, k), np.int32)
+        gate = np.empty((T, k), np.float64)
+        hk = np.empty(T, np.float64)
+        hk1 = np.empty(T, np.float64)
+        self.lib.orc_select(T, E, k, mode, _ptr(H), _ptr(idx), _ptr(gate), _ptr(hk), _ptr(hk1))
+        return idx, gate, hk, hk1
+
+    def gates_given(self, H, idx, mode: int):
+        """Gates for a forced expert set idx [T,k] (same formulas as select)."""
+        H = np.ascontiguousarray(H, dtype=np.float64)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, E = H.shape
+        k = idx.shape[1]
+        gate = np.empty((T, k), np.float64)
+        self.lib.orc_gates_given(T, E, k, mode, _ptr(H), _ptr(idx), _ptr(gate))
+        return gate
+
+    def slots(self, idx, E: int, C: int):
+        """Token-order exclusive-cumsum positions, accept mask and pre-capacity
+        counts (Switch steps 3-4). Returns pos [T,k] int32, keep [T,k] uint8,
+        count [E] int32."""
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, k = idx.shape
+        pos = np.empty((T, k), np.int32)
+        keep = np.empty((T, k), np.uint8)
+        count = np.empty(E, np.int32)
+        self.lib.orc_slots(T, k, E, C, _ptr(idx), _ptr(pos), _ptr(keep), _ptr(count))
+        return pos, keep, count
+
+    def layer_out(self, x, idx, gate, keep, W1, W2, b1=None, b2=None, tokens=None):
+        """y_t = x_t + sum over accepted choices of gate * E_e(x_t) for the
+        listed tokens (OLNN MoE output; Switch steps 6-7; lesson Ch. 1).
+        Returns (y [n,d] fp64, any_nonfinite)."""
+        x = np.ascontiguousarray(x)
+        T, d = x.shape
+        W1 = np.ascontiguousarray(W1)
+        W2 = np.ascontiguousarray(W2)
+        d_ff = W1.shape[2]
+        wcode = _dtype_code(W1)
+        if _dtype_code(W2) != wcode:
+            raise TypeError("W1 and W2 share one element type")
+        b1 = None if b1 is None else np.ascontiguousarray(b1)
+        b2 = None if b2 is None else np.ascontiguousarray(b2)
+        for b in (b1, b2):
+            if b is not None and _dtype_code(b) != wcode:
+                raise TypeError("biases share the weights' element type")
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        k = idx.shape[1]
+        gate = np.ascontiguousarray(gate, dtype=np.float64)
+        keep = np.ascontiguousarray(keep, dtype=np.uint8)
+        if tokens is None:
+            tokens = np.arange(T, dtype=np.int32)
+        tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+        y = np.empty((tokens.size, d), np.float64)
+        bad = self.lib.orc_layer_out(d, d_ff, k, _ptr(x), _dtype_code(x), _ptr(idx),
+                                     _ptr(gate), _ptr(keep), _ptr(W1), _ptr(b1), _ptr(W2),
+                                     _ptr(b2), wcode, _ptr(tokens), tokens.size, _ptr(y))
+        return y, bool(bad)
+
+    def aux(self, c, sigma, H, idx, gate, hk, hk1, noisy: bool):
+        """Importance, load, Switch fractions f and mean probabilities Pbar,
+        and out3 = [CV(importance)^2, CV(load)^2, 0.01*E*sum(f*Pbar)]
+        (OLNN Eqs. 6-10; Switch step 8)."""
+        c = np.ascontiguousarray(c, dtype=np.float64)
+        sigma = np.ascontiguousarray(sigma, dtype=np.float64)
+        H = np.ascontiguousarray(H, dtype=np.float64)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        gate = np.ascontiguousarray(gate, dtype=np.float64)
+        hk = np.ascontiguousarray(hk, dtype=np.float64)
+        hk1 = np.ascontiguousarray(hk1, dtype=np.float64)
+        T, E = H.shape
+        k = idx.shape[1]
+        imp = np.empty(E, np.float64)
+        load = np.empty(E, np.float64)
+        f = np.empty(E, np.float64)
+        pbar = np.empty(E, np.float64)
+        out3 = np.empty(3, np.float64)
+        self.lib.orc_aux(T, E, k, _ptr(c), _ptr(sigma), _ptr(H), _ptr(idx), _ptr(gate),
+                         _ptr(hk), _ptr(hk1), int(bool(noisy)), _ptr(imp), _ptr(load),
+                         _ptr(f), _ptr(pbar), _ptr(out3))
+        return dict(importance=imp, load=load, f=f, pbar=pbar, out3=out3)
+
+    def forward(self, inp: dict, tokens=None) -> dict:
+        """The whole forward path on one input set.
+
+        ``inp`` holds numpy arrays and sizes: x, Wg, Wn, noise, bias, W1, b1,
+        W2, b2 (optional ones may be None) and k, cf, min_cap, mode.
+        ``tokens`` lists the rows of y to compute (all by default); gating,
+        slots and the balancing quantities always cover every token, because
+        slot positions depend on all earlier tokens.
+        """
+        x = inp["x"]
+        T = x.shape[0]
+        E = inp["Wg"].shape[1]
+        k = int(inp["k"])
+        mode = int(inp["mode"])
+        c, s, H, bad_h = self.router(x, inp["Wg"], inp.get("Wn"), inp.get("noise"),
+                                     inp.get("bias"))
+        idx, gate, hk, hk1 = self.select(H, k, mode)
+        C = self.capacity(T, E, k, inp["cf"], inp.get("min_cap", 1))
+        pos, keep, count = self.slots(idx, E, C)
+        y, bad_y = self.layer_out(x, idx, gate, keep, inp["W1"], inp["W2"], inp.get("b1"),
+                                  inp.get("b2"), tokens)
+        ax = self.aux(c, s, H, idx, gate, hk, hk1, inp.get("Wn") is not None)
+        return dict(c=c, sigma=s, H=H, idx=idx, gate=gate, hk=hk, hk1=hk1, C=C, pos=pos,
+                    keep=keep, count=count, y=y, nonfinite=bad_h or bad_y, **ax)
+
+
+def default() -> Oracle:
+    """The oracle compiled from moe_oracle.c (built on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def variant(src_path: str, out_dir: str) -> Oracle:
+    """Compile another copy of the oracle source (e.g. one with a planted
+    mistake, for the tests that check the pins catch it) and load it."""
+    out = os.path.join(out_dir, "liboracle_variant_%d.so" % (abs(hash(src_path)) % 10**8))
+    _compile(src_path, out)
+    return Oracle(out)
+
+
+def capacity(*a, **k):
+    return default().capacity(*a, **k)
+
+
+def softplus(z):
+    return default().softplus(z)
+
+
+def phi(u):
+    return default().phi(u)
+
+
+def cv2(v):
+    return default().cv2(v)
+
+
+def router(*a, **k):
+    return default().router(*a, **k)
+
+
+def select(*a, **k):
+    return default().select(*a, **k)
+
+
+def gates_given(*a, **k):
+    return default().gates_given(*a, **k)
+
+
+def slots(*a, **k):
+    return default().slots(*a, **k)
+
+
+def layer_out(*a, **k):
+    return default().layer_out(*a, **k)
+
+
+def aux(*a, **k):
+    return default().aux(*a, **k)
+
+
+def forward(*a, **k):
+    return default().forward(*a, **k)

@@ -1,0 +1,360 @@
+/*
+ * moe_oracle.c -- plain, slow, fp64 CPU oracle for the forward path of the
+ * sparsely-gated Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is compiled into liboracle.so, which only
+ * the tests, the package's smoke check and the benchmark's CPU-baseline leg
+ * load. The product (libmoe.so and its Python binding) never calls it, and it
+ * shares no code, header, table or helper with the CUDA path.
+ *
+ * Every quantity is computed in double precision from the exact values of the
+ * inputs (bf16 and fp32 inputs widen to double without rounding). Nothing is
+ * blocked, fused or reordered beyond what the definitions state; loops follow
+ * the definitions in the order the pages give them.
+ *
+ * Pages cited (by title and section):
+ *  [OLNN]   "Outrageously Large Neural Networks: The Sparsely-Gated
+ *           Mixture-of-Experts Layer" (paper summary), section 3.4
+ *           "Detailed, Sentence-Based Technical Breakdown": the MoE output sum,
+ *           Noisy Top-K Gating steps 1-3 (Eqs. 3-5), Importance / CV^2 (Eqs. 6-7),
+ *           P(x,i) / Load (Eqs. 8-10), zero initialisation.
+ *  [SWITCH] "Switch Transformer" (abhik.ai), Implementation steps 1-8: fp32
+ *           router, argmax gate without renormalisation, capacity with
+ *           floor / T clamp / minimum, exclusive-cumsum slots, accepted vs
+ *           overflow, dispatch, ReLU experts, weighted combine plus residual,
+ *           auxiliary loss alpha*E*sum(f*P).
+ *  [KB]     "Sparsely-Gated MoE" (llm-arch-kb), section 2 "Derivation" and
+ *           section 3 "Reference implementation" (noisy top-K gate).
+ *  [LESSON] "Mixture-of-Experts: Sparse Computation" (cs8803 lesson),
+ *           Chapter 1 (skip experts whose gate is zero), Chapter 2
+ *           (KeepTopK with -inf, softplus), Chapter 5 (CV, load estimator).
+ *
+ * Parity status of each function is stated beside it; the pins live in
+ * tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+#include <stdlib.h>
+
+#define ORC_F32 0  /* array holds IEEE binary32 values */
+#define ORC_BF16 1 /* array holds bfloat16 bit patterns (uint16) */
+
+#define ORC_TOPK_SOFTMAX 0 /* Softmax(KeepTopK(H, k)) */
+#define ORC_SWITCH 1       /* full softmax, argmax, gate = p[argmax] */
+
+/* Exact widening of one input element to double. */
+static double orc_in(const void *base, int dtype, size_t i) {
+  if (dtype == ORC_BF16) {
+    uint16_t h = ((const uint16_t *)base)[i];
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return (double)((const float *)base)[i];
+}
+
+/* Softplus(z) = log(1 + e^z) [OLNN Step 1; LESSON Ch. 2 Part 2], written as
+ * max(z,0) + log1p(exp(-|z|)), which is the same function without overflow. */
+static double orc_softplus(double z) {
+  return (z > 0.0 ? z : 0.0) + log1p(exp(-fabs(z)));
+}
+
+/* Standard normal CDF [OLNN, P(x,i)]: Phi(u) = erfc(-u / sqrt 2) / 2. */
+static double orc_phi(double u) { return 0.5 * erfc(-u / sqrt(2.0)); }
+
+/* Expert capacity [SWITCH step 3], with the top-k factor k:
+ * C = max(min_cap, min(T, floor(k*T*cf / E))). */
+int orc_capacity(int T, int E, int k, double cf, int min_cap) {
+  double raw = floor((double)k * (double)T * cf / (double)E);
+  long c = (long)raw;
+  if (c > T) c = T;
+  if (c < min_cap) c = min_cap;
+  return (int)c;
+}
+
+/*
+ * Router [OLNN Step 1 (Eq. 4); SWITCH step 1; KB section 3]:
+ *   c[t,e]     = sum_i x[t,i] * Wg[i,e] + bias[e]          (clean logit)
+ *   sigma[t,e] = Softplus(sum_i x[t,i] * Wn[i,e])           (noise scale)
+ *   H[t,e]     = c[t,e] + noise[t,e] * sigma[t,e]           (noisy logit)
+ * The StandardNormal() draw of Eq. 4 is the caller's noise[t,e]. With no noise
+ * weights, sigma = 0 and H = c. bias may be NULL (zero). Layouts are row-major:
+ * x [T,d], Wg/Wn [d,E], noise [T,E]. Returns 0, or 1 if any H is not finite
+ * (the Switch page raises on non-finite router logits).
+ */
+int orc_router(int T, int d, int E, const void *x, int x_dtype, const float *Wg,
+               const float *Wn, const float *noise, const float *bias, double *c,
+               double *sigma, double *H) {
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i)
+        acc += orc_in(x, x_dtype, (size_t)t * d + i) * (double)Wg[(size_t)i * E + e];
+      if (bias) acc += (double)bias[e];
+      double s = 0.0, h = acc;
+      if (Wn) {
+        double z = 0.0;
+        for (int i = 0; i < d; ++i)
+          z += orc_in(x, x_dtype, (size_t)t * d + i) * (double)Wn[(size_t)i * E + e];
+        s = orc_softplus(z);
+        h = acc + (double)noise[(size_t)t * E + e] * s;
+      }
+      c[(size_t)t * E + e] = acc;
+      sigma[(size_t)t * E + e] = s;
+      H[(size_t)t * E + e] = h;
+      if (!isfinite(h)) bad = 1;
+    }
+  }
+  return bad;
+}
+
+/* The r-th expert in the order (H descending, index ascending) among those not
+ * yet taken; taken[] marks the ones already chosen. */
+static int orc_next_best(const double *h, int E, const unsigned char *taken) {
+  int best = -1;
+  for (int e = 0; e < E; ++e) {
+    if (taken[e]) continue;
+    if (best < 0 || h[e] > h[best]) best = e; /* strict >: lower index wins ties */
+  }
+  return best;
+}
+
+/*
+ * Gate selection.
+ *  TOPK [OLNN Steps 2-3 (Eq. 5); LESSON Ch. 2 Part 4]: S = the k largest H
+ *    (ties: lower expert index first); G_j = exp(H_{S_j}) / sum_{S} exp(H),
+ *    which is Softmax(KeepTopK(H,k)) restricted to its nonzero entries (the
+ *    -inf entries give exactly 0 and are not stored).
+ *  SWITCH [SWITCH step 2]: k == 1; p = Softmax(H) over all E experts;
+ *    S_0 = argmax p (first on ties); gate = p[S_0], not renormalised.
+ * Outputs per token (row-major): idx [T,k] in H-descending order, gate [T,k],
+ * hk [T] = k-th largest H, hk1 [T] = (k+1)-th largest H (-inf when k == E).
+ */
+void orc_select(int T, int E, int k, int mode, const double *H, int *idx,
+                double *gate, double *hk, double *hk1) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double *h = H + (size_t)t * E;
+    unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+    int kk = k < E ? k + 1 : k;
+    int order[kk];
+    for (int r = 0; r < kk; ++r) {
+      order[r] = orc_next_best(h, E, taken);
+      taken[order[r]] = 1;
+    }
+    free(taken);
+    for (int j = 0; j < k; ++j) idx[(size_t)t * k + j] = order[j];
+    hk[t] = h[order[k - 1]];
+    hk1[t] = (k < E) ? h[order[k]] : -INFINITY;
+    double top = h[order[0]];
+    if (mode == ORC_SWITCH) {
+      double z = 0.0;
+      for (int e = 0; e < E; ++e) z += exp(h[e] - top);
+      gate[(size_t)t * k] = exp(h[order[0]] - top) / z;
+    } else {
+      double z = 0.0;
+      for (int j = 0; j < k; ++j) z += exp(h[order[j]] - top);
+      for (int j = 0; j < k; ++j) gate[(size_t)t * k + j] = exp(h[order[j]] - top) / z;
+    }
+  }
+}
+
+/*
+ * Gates for a given selection (used when a test must accept either side of a
+ * rounding-level near-tie): the same formulas as orc_select, applied to the
+ * expert set idx [T,k] instead of the oracle's own choice.
+ */
+void orc_gates_given(int T, int E, int k, int mode, const double *H, const int *idx,
+                     double *gate) {
+  for (int t = 0; t < T; ++t) {
+    const double *h = H + (size_t)t * E;
+    double top = h[idx[(size_t)t * k]];
+    for (int j = 1; j < k; ++j)
+      if (h[idx[(size_t)t * k + j]] > top) top = h[idx[(size_t)t * k + j]];
+    if (mode == ORC_SWITCH) {
+      double z = 0.0;
+      for (int e = 0; e < E; ++e) z += exp(h[e] - top);
+      gate[(size_t)t * k] = exp(h[idx[(size_t)t * k]] - top) / z;
+    } else {
+      double z = 0.0;
+      for (int j = 0; j < k; ++j) z += exp(h[idx[(size_t)t * k + j]] - top);
+      for (int j = 0; j < k; ++j)
+        gate[(size_t)t * k + j] = exp(h[idx[(size_t)t * k + j]] - top) / z;
+    }
+  }
+}
+
+/*
+ * Slot assignment [SWITCH steps 3-4]: the position of an assignment (t,j) to
+ * expert e is the number of earlier assignments to e, counting tokens in
+ * order (the exclusive cumulative sum of the one-hot choices); an assignment
+ * is accepted iff its position < C. For k > 1 the assignments are taken token
+ * by token, and within a token in choice order (a token never picks one
+ * expert twice, so that inner order does not change any position). count[e]
+ * receives the number of assignments to e before capacity filtering.
+ */
+void orc_slots(int T, int k, int E, int C, const int *idx, int *pos,
+               unsigned char *keep, int *count) {
+  for (int e = 0; e < E; ++e) count[e] = 0;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      int e = idx[(size_t)t * k + j];
+      int p = count[e];
+      count[e] = p + 1;
+      pos[(size_t)t * k + j] = p;
+      keep[(size_t)t * k + j] = (unsigned char)(p < C);
+    }
+}
+
+/*
+ * Layer output for the listed tokens [OLNN, MoE output y = sum_i G_i E_i(x);
+ * LESSON Ch. 1, "wherever G(x)_i = 0 we need not compute E_i(x)"; SWITCH
+ * steps 6-7, residual y = x + branch]:
+ *   y_t = x_t + sum_{j : keep[t,j]} gate[t,j] * E_{idx[t,j]}(x_t),
+ *   E_e(v) = ReLU(v W1[e] + b1[e]) W2[e] + b2[e].
+ * W1 [E,d,d_ff], W2 [E,d_ff,d], b1 [E,d_ff], b2 [E,d] (b1/b2 may be NULL).
+ * A token with no accepted choice returns x_t unchanged. tokens[] lists which
+ * rows to compute; y is [n_tokens, d]. Returns 1 if any y is not finite.
+ */
+int orc_layer_out(int d, int d_ff, int k, const void *x, int x_dtype, const int *idx,
+                  const double *gate, const unsigned char *keep, const void *W1,
+                  const void *b1, const void *W2, const void *b2, int w_dtype,
+                  const int *tokens, int n_tokens, double *y) {
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int n = 0; n < n_tokens; ++n) {
+    int t = tokens[n];
+    double *h = (double *)malloc(sizeof(double) * (size_t)d_ff);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    double *yt = y + (size_t)n * d;
+    for (int i = 0; i < d; ++i) yt[i] = orc_in(x, x_dtype, (size_t)t * d + i);
+    for (int j = 0; j < k; ++j) {
+      if (!keep[(size_t)t * k + j]) continue;
+      int e = idx[(size_t)t * k + j];
+      /* first layer: h_f = ReLU(sum_i x_i W1[e,i,f] + b1[e,f]) */
+      for (int f = 0; f < d_ff; ++f) h[f] = 0.0;
+      for (int i = 0; i < d; ++i) {
+        double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        size_t row = ((size_t)e * d + i) * d_ff;
+        for (int f = 0; f < d_ff; ++f) h[f] += xi * orc_in(W1, w_dtype, row + f);
+      }
+      for (int f = 0; f < d_ff; ++f) {
+        if (b1) h[f] += orc_in(b1, w_dtype, (size_t)e * d_ff + f);
+        if (h[f] < 0.0) h[f] = 0.0;
+      }
+      /* second layer: o_c = sum_f h_f W2[e,f,c] + b2[e,c] */
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int f = 0; f < d_ff; ++f) {
+        size_t row = ((size_t)e * d_ff + f) * d;
+        for (int c = 0; c < d; ++c) o[c] += h[f] * orc_in(W2, w_dtype, row + c);
+      }
+      double g = gate[(size_t)t * k + j];
+      for (int c = 0; c < d; ++c) {
+        double oc = o[c] + (b2 ? orc_in(b2, w_dtype, (size_t)e * d + c) : 0.0);
+        yt[c] += g * oc;
+      }
+    }
+    for (int i = 0; i < d; ++i)
+      if (!isfinite(yt[i])) bad = 1;
+    free(h);
+    free(o);
+  }
+  return bad;
+}
+
+/* CV(v)^2 with the population standard deviation [OLNN Eq. 7; LESSON Ch. 5]:
+ * (1/n) sum (v_i - mean)^2 / mean^2. */
+double orc_cv2(const double *v, int n) {
+  double mean = 0.0;
+  for (int i = 0; i < n; ++i) mean += v[i];
+  mean /= n;
+  double var = 0.0;
+  for (int i = 0; i < n; ++i) var += (v[i] - mean) * (v[i] - mean);
+  var /= n;
+  return var / (mean * mean);
+}
+
+/*
+ * Balancing quantities, all before capacity filtering.
+ *  importance[e] = sum_t G(x_t)_e                    [OLNN Eq. 6]
+ *  load[e]       = sum_t P(x_t, e)                   [OLNN Eqs. 8-10]
+ *     P(x,e) = Phi((c_e - kth_excluding(H, k, e)) / sigma_e), where
+ *     kth_excluding is the k-th largest H among the other experts: hk1 when e
+ *     is one of the chosen k, hk otherwise. With no noise (noisy == 0), or
+ *     where sigma is 0, P is the limit of that probability as sigma -> 0+, the
+ *     indicator that e is chosen. With k == E every expert is always chosen.
+ *  out3[0] = CV(importance)^2, out3[1] = CV(load)^2    [OLNN Eq. 7, Eq. 10]
+ *  out3[2] = 0.01 * E * sum_e f_e * Pbar_e             [SWITCH step 8]
+ *     f_e = fraction of tokens whose first choice is e (hard, pre-capacity),
+ *     Pbar_e = mean over tokens of Softmax(H)_e over all E experts.
+ * f_out and pbar_out ([E] each) may be NULL.
+ */
+void orc_aux(int T, int E, int k, const double *c, const double *sigma, const double *H,
+             const int *idx, const double *gate, const double *hk, const double *hk1,
+             int noisy, double *importance, double *load, double *f_out,
+             double *pbar_out, double *out3) {
+  double *rowmax = (double *)malloc(sizeof(double) * (size_t)T);
+  double *rowsum = (double *)malloc(sizeof(double) * (size_t)T);
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double *h = H + (size_t)t * E;
+    double m = h[0];
+    for (int e = 1; e < E; ++e)
+      if (h[e] > m) m = h[e];
+    double s = 0.0;
+    for (int e = 0; e < E; ++e) s += exp(h[e] - m);
+    rowmax[t] = m;
+    rowsum[t] = s;
+  }
+  double *f = (double *)malloc(sizeof(double) * (size_t)E);
+  double *pbar = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp parallel for schedule(static)
+  for (int e = 0; e < E; ++e) {
+    double imp = 0.0, ld = 0.0, pb = 0.0, first = 0.0;
+    for (int t = 0; t < T; ++t) {
+      int chosen = -1;
+      for (int j = 0; j < k; ++j)
+        if (idx[(size_t)t * k + j] == e) chosen = j;
+      if (chosen >= 0) imp += gate[(size_t)t * k + chosen];
+      if (idx[(size_t)t * k] == e) first += 1.0;
+      double p;
+      if (k == E) {
+        p = 1.0;
+      } else {
+        double s = sigma[(size_t)t * E + e];
+        if (!noisy || s == 0.0) {
+          p = chosen >= 0 ? 1.0 : 0.0;
+        } else {
+          double thr = chosen >= 0 ? hk1[t] : hk[t];
+          p = orc_phi((c[(size_t)t * E + e] - thr) / s);
+        }
+      }
+      ld += p;
+      pb += exp(H[(size_t)t * E + e] - rowmax[t]) / rowsum[t];
+    }
+    importance[e] = imp;
+    load[e] = ld;
+    f[e] = first / T;
+    pbar[e] = pb / T;
+  }
+  double sfp = 0.0;
+  for (int e = 0; e < E; ++e) sfp += f[e] * pbar[e];
+  out3[0] = orc_cv2(importance, E);
+  out3[1] = orc_cv2(load, E);
+  out3[2] = 0.01 * (double)E * sfp;
+  if (f_out) memcpy(f_out, f, sizeof(double) * (size_t)E);
+  if (pbar_out) memcpy(pbar_out, pbar, sizeof(double) * (size_t)E);
+  free(f);
+  free(pbar);
+  free(rowmax);
+  free(rowsum);
+}
+
+/* Exposed for the pins: the scalar building blocks. */
+double orc_softplus_at(double z) { return orc_softplus(z); }
+double orc_phi_at(double u) { return orc_phi(u); }

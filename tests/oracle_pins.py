@@ -1,0 +1,441 @@
+"""Pins of the fp64 oracle to facts the pages and mathematics fix.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError if
+that oracle disagrees with:
+
+* numbers printed on the pages (``tests/golden/lesson_worked_examples.json``),
+* closed forms (capacity, Switch auxiliary loss under uniform and collapsed
+  routing, zero initialisation),
+* independent library routines (numpy matmul / einsum / sort, scipy's normal
+  CDF) on small inputs, and
+* brute force (a Monte-Carlo redraw of one expert's noise for P(x,i)).
+
+``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutations.py``
+runs them on copies of the oracle with planted mistakes and checks that every
+mistake fails at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+from scipy.special import ndtr
+
+from sparsely_gated_mixture_gb300.workloads import bf16_bits_to_f32, f32_to_bf16_bits
+
+TOPK, SWITCH = 0, 1
+_GOLDEN_PATH = os.path.join(os.path.dirname(__file__), "golden", "lesson_worked_examples.json")
+with open(_GOLDEN_PATH) as _f:
+    GOLDEN = json.load(_f)
+
+
+def _dense_gates(idx, gate, E):
+    T, k = idx.shape
+    G = np.zeros((T, E))
+    for t in range(T):
+        for j in range(k):
+            G[t, idx[t, j]] = gate[t, j]
+    return G
+
+
+def _router_for_H(clean, H):
+    """Router inputs whose noisy logits are H: d = E + 1, x = [clean, 1],
+    W_g = [I; 0] and W_noise = [0; ln(e - 1)], so sigma = Softplus(ln(e-1)) = 1
+    and noise = H - clean."""
+    E = len(clean)
+    x = np.array([list(clean) + [1.0]], np.float32)
+    Wg = np.zeros((E + 1, E), np.float32)
+    Wg[:E, :E] = np.eye(E, dtype=np.float32)
+    Wn = np.zeros((E + 1, E), np.float32)
+    Wn[E, :] = math.log(math.e - 1.0)
+    noise = (np.asarray(H, np.float64) - np.asarray(clean, np.float64)).astype(np.float32)[None]
+    return x, Wg, Wn, noise
+
+
+def _ref_order(h, k):
+    """Experts ordered by (H descending, index ascending), first k."""
+    return sorted(range(len(h)), key=lambda e: (-h[e], e))[:k]
+
+
+def _x64(x):
+    return bf16_bits_to_f32(x).astype(np.float64) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+def _ffn_all(X, W1, b1, W2, b2):
+    """E_e(X) for every expert e with numpy matmuls: [E, T, d]."""
+    E = W1.shape[0]
+    out = []
+    for e in range(E):
+        h = X @ _x64(W1[e]) + (0.0 if b1 is None else _x64(b1[e]))
+        h = np.maximum(h, 0.0)
+        out.append(h @ _x64(W2[e]) + (0.0 if b2 is None else _x64(b2[e])))
+    return np.stack(out)
+
+
+# ----------------------------------------------------------------------------- gating
+
+
+def pin_lesson_gates(orc):
+    """The lesson's four-expert worked examples, routed through the router."""
+    for ex in GOLDEN["gating"]:
+        x, Wg, Wn, noise = _router_for_H(ex["clean"], ex["H"])
+        c, s, H, bad = orc.router(x, Wg, Wn, noise)
+        assert not bad
+        np.testing.assert_allclose(c[0], ex["clean"], atol=1e-12)
+        np.testing.assert_allclose(s[0], 1.0, atol=1e-6)
+        np.testing.assert_allclose(H[0], ex["H"], atol=1e-6)
+        idx, gate, _, _ = orc.select(H, ex["k"], TOPK)
+        G = _dense_gates(idx, gate, 4)[0]
+        np.testing.assert_allclose(G, ex["gates"], atol=ex["tol"] + 1e-12, err_msg=ex["source"])
+        assert np.count_nonzero(G) == ex["k"]
+        assert abs(G.sum() - 1.0) < 1e-12
+
+
+def pin_lesson_second_draw(orc):
+    ex = GOLDEN["second_draw"]
+    H = np.array([[1.4, 0.2, 1.5, -1.0]])  # only 1.5 and 1.4 are printed; the rest are lower
+    idx, gate, _, _ = orc.select(H, ex["k"], TOPK)
+    assert list(idx[0]) == ex["top2_experts"]
+    np.testing.assert_allclose(gate[0], ex["gates"], atol=ex["tol"])
+
+
+def pin_zero_init(orc):
+    """W_g = W_noise = 0: clean logits 0, sigma = Softplus(0) = log 2, H = noise*log 2."""
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((5, 7)).astype(np.float32)
+    noise = rng.standard_normal((5, 4)).astype(np.float32)
+    z = np.zeros((7, 4), np.float32)
+    c, s, H, _ = orc.router(x, z, z, noise)
+    assert np.all(c == 0.0)
+    np.testing.assert_allclose(s, math.log(2.0), rtol=1e-15)
+    ex = GOLDEN["zero_init"]
+    assert abs(s[0, 0] - ex["sigma"]) < ex["tol"]
+    np.testing.assert_allclose(H, noise.astype(np.float64) * math.log(2.0), rtol=1e-15)
+
+
+def pin_router_numpy(orc):
+    """Router against numpy's fp64 matmul, with bias and noise, fp32 and bf16 x."""
+    rng = np.random.default_rng(2)
+    T, d, E = 7, 13, 5
+    x32 = rng.standard_normal((T, d)).astype(np.float32)
+    Wg = (rng.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    Wn = (rng.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    noise = rng.standard_normal((T, E)).astype(np.float32)
+    bias = rng.standard_normal(E).astype(np.float32)
+    for x in (x32, f32_to_bf16_bits(x32)):
+        X = _x64(x)
+        c_ref = X @ Wg.astype(np.float64) + bias.astype(np.float64)
+        s_ref = np.logaddexp(0.0, X @ Wn.astype(np.float64))
+        H_ref = c_ref + noise.astype(np.float64) * s_ref
+        c, s, H, _ = orc.router(x, Wg, Wn, noise, bias)
+        np.testing.assert_allclose(c, c_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(s, s_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(H, H_ref, rtol=1e-12, atol=1e-12)
+        c0, s0, H0, _ = orc.router(x, Wg)
+        np.testing.assert_allclose(c0, X @ Wg.astype(np.float64), rtol=1e-12, atol=1e-12)
+        assert np.all(s0 == 0.0) and np.all(H0 == c0)
+
+
+def pin_select_bruteforce(orc):
+    """Top-k order with ties (lower index first), gates, thresholds; Switch."""
+    rng = np.random.default_rng(3)
+    T, E = 60, 6
+    H = np.round(rng.standard_normal((T, E)), 1)  # one decimal: many exact ties
+    H[0] = 0.5  # a row of all-equal logits
+    for k in range(1, E + 1):
+        idx, gate, hk, hk1 = orc.select(H, k, TOPK)
+        for t in range(T):
+            order = _ref_order(list(H[t]), E)
+            assert list(idx[t]) == order[:k], (k, t)
+            w = np.exp(H[t, order[:k]] - H[t, order[0]])
+            np.testing.assert_allclose(gate[t], w / w.sum(), rtol=1e-13)
+            assert hk[t] == H[t, order[k - 1]]
+            assert hk1[t] == (H[t, order[k]] if k < E else -np.inf)
+        G = _dense_gates(idx, gate, E)
+        assert np.all(np.count_nonzero(G, axis=1) == k)
+        np.testing.assert_allclose(G.sum(axis=1), 1.0, rtol=1e-13)
+    idx, gate, _, _ = orc.select(H, 1, SWITCH)
+    p = np.exp(H - H.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    am = np.argmax(H, axis=1)  # numpy: first index on ties
+    assert np.array_equal(idx[:, 0], am)
+    np.testing.assert_allclose(gate[:, 0], p[np.arange(T), am], rtol=1e-13)
+    assert np.all(gate[:, 0] <= 1.0) and np.any(gate[:, 0] < 1.0)  # not renormalised
+
+
+def pin_mask_renormalise(orc):
+    """Softmax(KeepTopK(H)) equals the dense softmax masked to the top k and
+    renormalised (the paper's appendix form, quoted in the lesson's Ch. 2)."""
+    rng = np.random.default_rng(4)
+    H = rng.standard_normal((40, 9)) * 2.0
+    for k in (1, 2, 4, 9):
+        idx, gate, _, _ = orc.select(H, k, TOPK)
+        Gs = np.exp(H - H.max(axis=1, keepdims=True))
+        Gs /= Gs.sum(axis=1, keepdims=True)
+        M = np.zeros_like(H)
+        np.put_along_axis(M, idx.astype(np.int64), 1.0, axis=1)
+        ref = Gs * M / (Gs * M).sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(_dense_gates(idx, gate, 9), ref, rtol=1e-12, atol=1e-15)
+
+
+def pin_gates_given(orc):
+    rng = np.random.default_rng(5)
+    H = rng.standard_normal((20, 7))
+    for k, mode in ((1, SWITCH), (3, TOPK)):
+        idx, gate, _, _ = orc.select(H, k, mode)
+        np.testing.assert_allclose(orc.gates_given(H, idx, mode), gate, rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------- capacity, slots
+
+
+def pin_capacity(orc):
+    cases = [  # (T, E, k, cf, expected): the five measured workloads, then the clamps
+        (8, 3, 1, 1.0, 2), (4096, 16, 4, 2.0, 2048), (16384, 64, 1, 1.25, 320),
+        (8192, 8, 2, 1.25, 2560), (32768, 1024, 4, 1.5, 192),
+        (2, 8, 1, 1.0, 1),  # floor(0.25) = 0 -> minimum 1
+        (4, 1, 1, 2.0, 4),  # floor(8) -> clamped to T
+    ]
+    for T, E, k, cf, want in cases:
+        exact = math.floor(Fraction(k * T) * Fraction(cf) / E)
+        assert max(1, min(T, exact)) == want
+        assert orc.capacity(T, E, k, cf, 1) == want, (T, E, k, cf)
+
+
+def pin_slots_cumsum(orc):
+    """Positions equal the exclusive cumulative sum of one-hot choices in
+    token order (Switch step 3), accept iff position < C (step 4)."""
+    rng = np.random.default_rng(6)
+    T, k, E = 40, 3, 5
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    idx[:10, 0] = 2  # pile onto one expert so that small capacities drop
+    for C in (1, 3, 7, 1000):
+        pos, keep, count = orc.slots(idx, E, C)
+        onehot = np.zeros((T * k, E), np.int64)
+        onehot[np.arange(T * k), idx.reshape(-1)] = 1
+        excl = np.cumsum(onehot, axis=0) - onehot
+        pos_ref = (excl * onehot).sum(axis=1).reshape(T, k)
+        assert np.array_equal(pos, pos_ref)
+        assert np.array_equal(keep.astype(bool), pos_ref < C)
+        assert np.array_equal(count, onehot.sum(axis=0))
+        assert int(keep.sum()) == int(np.minimum(onehot.sum(axis=0), C).sum())
+        taken = {(int(idx[t, j]), int(pos[t, j])) for t in range(T) for j in range(k) if keep[t, j]}
+        assert len(taken) == int(keep.sum())  # each slot holds at most one assignment
+
+
+# ----------------------------------------------------------------------------- expert FFN and combine
+
+
+def _small_case(rng, T, d, E, d_ff, bf16, biases=True):
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    W1 = (rng.standard_normal((E, d, d_ff)) / math.sqrt(d)).astype(np.float32)
+    W2 = (rng.standard_normal((E, d_ff, d)) / math.sqrt(d_ff)).astype(np.float32)
+    b1 = (0.1 * rng.standard_normal((E, d_ff))).astype(np.float32) if biases else None
+    b2 = (0.1 * rng.standard_normal((E, d))).astype(np.float32) if biases else None
+    if bf16:
+        x, W1, W2 = (f32_to_bf16_bits(a) for a in (x, W1, W2))
+        b1 = None if b1 is None else f32_to_bf16_bits(b1)
+        b2 = None if b2 is None else f32_to_bf16_bits(b2)
+    return x, W1, b1, W2, b2
+
+
+def pin_dense_sum(orc):
+    """With nothing dropped, the per-token loop over kept experts equals the
+    dense all-experts sum x + sum_e G_e E_e(x) (the MoE output equation), with
+    G = Softmax(KeepTopK(H)) built independently in numpy."""
+    rng = np.random.default_rng(7)
+    T, d, E, d_ff, k = 6, 5, 4, 7, 2
+    for bf16 in (False, True):
+        x, W1, b1, W2, b2 = _small_case(rng, T, d, E, d_ff, bf16)
+        H = rng.standard_normal((T, E))
+        idx, gate, _, _ = orc.select(H, k, TOPK)
+        keep = np.ones((T, k), np.uint8)
+        y, bad = orc.layer_out(x, idx, gate, keep, W1, W2, b1, b2)
+        assert not bad
+        masked = np.full_like(H, -np.inf)
+        for t in range(T):
+            top = _ref_order(list(H[t]), k)
+            masked[t, top] = H[t, top]
+        G = np.exp(masked - masked.max(axis=1, keepdims=True))
+        G /= G.sum(axis=1, keepdims=True)
+        X = _x64(x)
+        Y = _ffn_all(X, W1, b1, W2, b2)
+        ref = X + np.einsum("te,etd->td", G, Y)
+        np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+def pin_switch_einsum_algebra(orc):
+    """With drops, the output equals the Switch page's dispatch / combine
+    tensor algebra (steps 5-7) evaluated with numpy einsum."""
+    rng = np.random.default_rng(8)
+    T, d, E, d_ff = 10, 4, 3, 6
+    for k in (1, 2):
+        x, W1, b1, W2, b2 = _small_case(rng, T, d, E, d_ff, False)
+        H = rng.standard_normal((T, E))
+        H[:, 1] += 1.5  # overload expert 1
+        mode = SWITCH if k == 1 else TOPK
+        idx, gate, _, _ = orc.select(H, k, mode)
+        C = 3
+        onehot = np.zeros((T * k, E), np.int64)
+        onehot[np.arange(T * k), idx.reshape(-1)] = 1
+        pos = ((np.cumsum(onehot, axis=0) - onehot) * onehot).sum(axis=1).reshape(T, k)
+        keep = (pos < C).astype(np.uint8)
+        assert keep.sum() < T * k  # something overflowed
+        dispatch = np.zeros((T, E, C))
+        combine = np.zeros((T, E, C))
+        for t in range(T):
+            for j in range(k):
+                if keep[t, j]:
+                    dispatch[t, idx[t, j], pos[t, j]] = 1.0
+                    combine[t, idx[t, j], pos[t, j]] = gate[t, j]
+        X = _x64(x)
+        U = np.einsum("tec,td->ecd", dispatch, X)
+        Hh = np.maximum(np.einsum("ecd,edh->ech", U, W1.astype(np.float64)) + b1[:, None, :], 0.0)
+        Z = np.einsum("ech,ehd->ecd", Hh, W2.astype(np.float64)) + b2[:, None, :]
+        ref = X + np.einsum("tec,ecd->td", combine, Z)
+        y, _ = orc.layer_out(x, idx, gate, keep, W1, W2, b1, b2)
+        np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+def pin_dropped_identity(orc):
+    """A token whose choices all overflow leaves the layer unchanged."""
+    rng = np.random.default_rng(9)
+    T, d, E, d_ff = 8, 6, 3, 5
+    x, W1, b1, W2, b2 = _small_case(rng, T, d, E, d_ff, True)
+    H = np.tile([3.0, 0.0, -1.0], (T, 1))
+    idx, gate, _, _ = orc.select(H, 1, SWITCH)
+    pos, keep, _ = orc.slots(idx, E, 2)
+    y, _ = orc.layer_out(x, idx, gate, keep, W1, W2, b1, b2)
+    X = _x64(x)
+    assert np.array_equal(y[2:], X[2:])
+    assert not np.array_equal(y[:2], X[:2])
+
+
+def pin_dense_mlp_special_case(orc):
+    """One expert, top-1 Switch, capacity T: every gate is Softmax over one
+    expert = 1 and the layer is x + a plain two-layer ReLU MLP."""
+    rng = np.random.default_rng(10)
+    T, d, d_ff = 9, 6, 11
+    x, W1, b1, W2, b2 = _small_case(rng, T, d, 1, d_ff, False)
+    Wg = rng.standard_normal((d, 1)).astype(np.float32)
+    c, s, H, _ = orc.router(x, Wg)
+    idx, gate, _, _ = orc.select(H, 1, SWITCH)
+    assert np.all(gate == 1.0)
+    C = orc.capacity(T, 1, 1, 1.0, 1)
+    assert C == T
+    pos, keep, _ = orc.slots(idx, 1, C)
+    y, _ = orc.layer_out(x, idx, gate, keep, W1, W2, b1, b2)
+    X = _x64(x)
+    ref = X + np.maximum(X @ W1[0].astype(np.float64) + b1[0], 0.0) @ W2[0].astype(np.float64) + b2[0]
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- balancing losses
+
+
+def pin_cv(orc):
+    for ex in GOLDEN["cv"]:
+        assert abs(orc.cv2(ex["importance"]) - ex["cv2"]) <= ex["tol"], ex["source"]
+    v = np.array([3.0, 1.0, 4.0, 1.0, 5.0])
+    assert abs(orc.cv2(v) - np.var(v) / np.mean(v) ** 2) < 1e-14
+
+
+def pin_importance_and_noise_free_load(orc):
+    rng = np.random.default_rng(11)
+    T, E, k = 30, 5, 2
+    H = rng.standard_normal((T, E))
+    idx, gate, hk, hk1 = orc.select(H, k, TOPK)
+    zero = np.zeros_like(H)
+    a = orc.aux(H, zero, H, idx, gate, hk, hk1, False)
+    G = _dense_gates(idx, gate, E)
+    np.testing.assert_allclose(a["importance"], G.sum(axis=0), rtol=1e-13)
+    counts = np.bincount(idx.reshape(-1), minlength=E)
+    assert np.array_equal(a["load"], counts.astype(np.float64))
+    np.testing.assert_allclose(a["out3"][0], np.var(a["importance"]) / np.mean(a["importance"]) ** 2,
+                               rtol=1e-12)
+    np.testing.assert_allclose(a["out3"][1], np.var(counts) / np.mean(counts) ** 2, rtol=1e-12)
+    idx, gate, hk, hk1 = orc.select(H, E, TOPK)  # k = E: every expert always chosen
+    a = orc.aux(H, zero + 1.0, H, idx, gate, hk, hk1, True)
+    assert np.all(a["load"] == T) and a["out3"][1] == 0.0
+
+
+def pin_load_lesson_reading(orc):
+    """The lesson's Ch. 5 load example: H = [2.3, 0.8, 0.6, -2.0], clean
+    [2.0, 1.0, 0.5, -0.5], noise scale 1, k = 2. kth_excluding drops the expert
+    and takes the 2nd largest of the rest ([0.6, 0.6, 0.8, 0.8]); P = Phi(clean -
+    kth_excluding), evaluated here with scipy's normal CDF."""
+    Hr = np.array([[2.3, 0.8, 0.6, -2.0]])
+    clean = np.array([[2.0, 1.0, 0.5, -0.5]])
+    idx, gate, hk, hk1 = orc.select(Hr, 2, TOPK)
+    a = orc.aux(clean, np.ones_like(Hr), Hr, idx, gate, hk, hk1, True)
+    kth = np.array([0.6, 0.6, 0.8, 0.8])
+    np.testing.assert_allclose(a["load"], ndtr(clean[0] - kth), rtol=1e-13)
+
+
+def pin_load_monte_carlo(orc):
+    """P(x,i) is the probability that expert i stays in the top k when only
+    its own noise is redrawn: count it by brute force."""
+    rng = np.random.default_rng(12)
+    T, E, k, N = 3, 5, 2, 40000
+    c = rng.standard_normal((T, E))
+    s = 0.3 + rng.random((T, E))
+    n = rng.standard_normal((T, E))
+    H = c + n * s
+    idx, gate, hk, hk1 = orc.select(H, k, TOPK)
+    a = orc.aux(c, s, H, idx, gate, hk, hk1, True)
+    est = np.zeros(E)
+    for t in range(T):
+        for e in range(E):
+            draws = c[t, e] + rng.standard_normal(N) * s[t, e]
+            others = np.delete(H[t], e)
+            beaten_by = (others[None, :] > draws[:, None]).sum(axis=1)
+            est[e] += np.mean(beaten_by < k)
+    tol = 5.0 * math.sqrt(T * 0.25 / N)
+    assert np.all(np.abs(a["load"] - est) < tol), (a["load"], est)
+
+
+def pin_switch_aux_closed_forms(orc):
+    alpha = GOLDEN["switch_aux"]["alpha"]
+    E, m = 4, 3
+    v = np.array([1.0, 0.2, -0.3, 0.7])
+    H = np.stack([np.roll(v, r) for r in range(E)] * m)  # every expert first equally often
+    idx, gate, hk, hk1 = orc.select(H, 1, SWITCH)
+    a = orc.aux(H, np.zeros_like(H), H, idx, gate, hk, hk1, False)
+    np.testing.assert_allclose(a["f"], 1.0 / E, rtol=1e-14)
+    np.testing.assert_allclose(a["pbar"], 1.0 / E, rtol=1e-13)
+    assert abs(a["out3"][2] - alpha) < 1e-14
+    H = np.tile(v, (7, 1))  # collapse: every token picks expert 0 with probability q
+    idx, gate, hk, hk1 = orc.select(H, 1, SWITCH)
+    a = orc.aux(H, np.zeros_like(H), H, idx, gate, hk, hk1, False)
+    q = np.exp(v[0]) / np.exp(v).sum()
+    assert abs(a["out3"][2] - alpha * E * q) < 1e-14
+
+
+# ----------------------------------------------------------------------------- scalars, errors
+
+
+def pin_softplus_phi(orc):
+    for z in np.linspace(-50.0, 50.0, 41):
+        assert abs(orc.softplus(z) - np.logaddexp(0.0, z)) <= 1e-14 * max(1.0, abs(z))
+    assert orc.softplus(-10.0) > 0.0
+    for u in np.linspace(-8.0, 8.0, 33):
+        assert abs(orc.phi(u) - ndtr(u)) < 1e-15
+    assert orc.phi(0.0) == 0.5
+
+
+def pin_nonfinite(orc):
+    x = np.ones((2, 3), np.float32)
+    x[1, 2] = np.inf
+    _, _, _, bad = orc.router(x, np.ones((3, 2), np.float32))
+    assert bad
+    W1 = np.ones((1, 3, 2), np.float32)
+    W1[0, 0, 0] = np.nan
+    y, bad = orc.layer_out(np.ones((1, 3), np.float32), np.zeros((1, 1), np.int32), np.ones((1, 1)),
+                           np.ones((1, 1), np.uint8), W1, np.ones((1, 2, 3), np.float32))
+    assert bad
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,59 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Each mutation is a plausible slip (a flipped tie rule, an off-by-one capacity
+test, a swapped threshold, a dropped term, a transposed operand, the sample
+instead of the population variance, ...). The copy is compiled on the CPU into
+a temporary library; the real oracle is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTATIONS = {
+    "tie_rule_higher_index_wins": ("h[e] > h[best]", "h[e] >= h[best]"),
+    "capacity_test_inclusive": ("(p < C)", "(p <= C)"),
+    "capacity_ceil": ("floor((double)k", "ceil((double)k"),
+    "count_only_kept": ("count[e] = p + 1;", "count[e] = p + (p < C);"),
+    "threshold_swapped": ("chosen >= 0 ? hk1[t] : hk[t]", "chosen >= 0 ? hk[t] : hk1[t]"),
+    "load_sign": ("(c[(size_t)t * E + e] - thr) / s", "(thr - c[(size_t)t * E + e]) / s"),
+    "router_bias_dropped": ("if (bias) acc += (double)bias[e];", ""),
+    "noise_unscaled": ("h = acc + (double)noise[(size_t)t * E + e] * s;",
+                       "h = acc + (double)noise[(size_t)t * E + e];"),
+    "softplus_as_log_exp": ("log1p(exp(-fabs(z)))", "log(exp(-fabs(z)))"),
+    "relu_dropped": ("if (h[f] < 0.0) h[f] = 0.0;", ""),
+    "gate_not_applied": ("yt[c] += g * oc;", "yt[c] += oc;"),
+    "w1_transposed": ("size_t row = ((size_t)e * d + i) * d_ff;\n        for (int f = 0; f < d_ff; ++f) h[f] += xi * orc_in(W1, w_dtype, row + f);",
+                      "for (int f = 0; f < d_ff; ++f) h[f] += xi * orc_in(W1, w_dtype, ((size_t)e * d_ff + f) * d + i);"),
+    "b2_outside_gate": ("double oc = o[c] + (b2 ? orc_in(b2, w_dtype, (size_t)e * d + c) : 0.0);\n        yt[c] += g * oc;",
+                        "double oc = o[c];\n        yt[c] += g * oc + (b2 ? orc_in(b2, w_dtype, (size_t)e * d + c) : 0.0);"),
+    "sample_variance": ("var /= n;", "var /= (n - 1);"),
+    "cv_not_squared": ("return var / (mean * mean);", "return sqrt(var) / mean;"),
+    "switch_gate_renormalised": ("gate[(size_t)t * k] = exp(h[order[0]] - top) / z;\n    } else {",
+                                 "gate[(size_t)t * k] = 1.0;\n    } else {"),
+    "switch_aux_no_E": ("out3[2] = 0.01 * (double)E * sfp;", "out3[2] = 0.01 * sfp;"),
+    "importance_first_choice_only": ("if (chosen >= 0) imp += gate[(size_t)t * k + chosen];",
+                                     "if (chosen == 0) imp += gate[(size_t)t * k + chosen];"),
+    "kplus1_threshold_off_by_one": ("hk1[t] = (k < E) ? h[order[k]] : -INFINITY;",
+                                    "hk1[t] = (k < E) ? h[order[k - 1]] : -INFINITY;"),
+    "phi_argument_unscaled": ("erfc(-u / sqrt(2.0))", "erfc(-u)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mutated = tmp_path / "moe_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    mutant = oracle.variant(str(mutated), str(tmp_path))
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
