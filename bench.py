@@ -1,0 +1,424 @@
+"""Benchmark of the MoE layer forward path on GB300.
+
+One step = one pass of the whole forward path (router + noisy top-k gate,
+capacity and slots, dispatch, both expert layers, combine with residual, and
+the balancing losses) over one batch of synthetic input, through the library's
+C ABI. Default workload: the top-2 large-expert layer (T=8192, d=4096, E=8,
+d_ff=14336, k=2, capacity factor 1.25, noisy gating, bf16), the one the
+expert-GEMM share of bf16 peak is quoted on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Prints one JSON line (rank 0). With N > 1 (torchrun) every rank runs an
+independent replica of the workload on its own GPU (the layer needs no
+exchange between replicas); value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparsely_gated_mixture_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s @1 GB300; expert GEMM % bf16 peak; gate/dispatch HBM %"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(w: wl.Workload, extra: dict) -> dict:
+    cfg = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "d_ff": w.d_ff, "k": w.k,
+           "capacity_factor": w.cf, "gate": w.mode, "noisy": w.noisy, "capacity": w.capacity,
+           "seed": 0}
+    cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = sorted(sm)[len(sm) // 2:] or sm  # the loaded half of the samples
+        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- algorithmic traffic
+
+
+def stage_traffic(w: wl.Workload, accepted: int, experts_used: int) -> dict:
+    """What each stage must move (bytes) or compute (flops) per forward."""
+    s = 2 if w.dtype == "bf16" else 4
+    T, d, E, dff, k = w.T, w.d, w.E, w.d_ff, w.k
+    cols = 2 if w.noisy else 1
+    gate_bytes = T * d * s + cols * d * E * 4 + (T * E * 4 if w.noisy else 0) + T * k * 8 + T * 8
+    dispatch_bytes = T * k * 8 + T * k * 5 + 2 * accepted * d * s + accepted * 8
+    ffn_flops = 4 * d * dff * accepted
+    ffn_bytes = 2 * experts_used * d * dff * s + accepted * d * s + 2 * accepted * dff * s \
+        + accepted * d * 4
+    combine_bytes = accepted * d * 4 + 2 * T * d * s + T * k * 9
+    return {"gate_bytes": gate_bytes, "dispatch_bytes": dispatch_bytes, "ffn_flops": ffn_flops,
+            "ffn_bytes": ffn_bytes, "combine_bytes": combine_bytes,
+            "router_flops": w.router_flops()}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, w: wl.Workload):
+    import torch
+    import torch.distributed as dist
+
+    from sparsely_gated_mixture_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    inp = wl.generate(w, seed=0)
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(a, is_act):
+        if a is None:
+            return None
+        if is_act and w.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    x = to_dev(inp["x"], True)
+    Wg, Wn, noise, bias = (to_dev(inp[k], False) for k in ("Wg", "Wn", "noise", "bias"))
+    W1, W2 = to_dev(inp["W1"], True), to_dev(inp["W2"], True)
+    b1 = b2 = None
+    cfg = B.config_for(w)
+    T, k, E, d, dff = w.T, w.k, w.E, w.d, w.d_ff
+    A = T * k
+    ws = torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    z = dict(device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, **z)
+    gate = torch.empty((T, k), dtype=torch.float32, **z)
+    thr = torch.empty((T, 2), dtype=torch.float32, **z)
+    pos = torch.empty((T, k), dtype=torch.int32, **z)
+    keep = torch.empty((T, k), dtype=torch.uint8, **z)
+    count = torch.empty(E, dtype=torch.int32, **z)
+    offset = torch.empty(E + 1, dtype=torch.int32, **z)
+    xbuf = torch.empty((A, d), dtype=act, **z)
+    row_token = torch.empty(A, dtype=torch.int32, **z)
+    row_gate = torch.empty(A, dtype=torch.float32, **z)
+    hbuf = torch.empty((A, dff), dtype=act, **z)
+    zbuf = torch.empty((A, d), dtype=torch.float32, **z)
+    y = torch.empty((T, d), dtype=act, **z)
+    out3 = torch.zeros(3, dtype=torch.float32, **z)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, **z)
+
+    # One step: the five stage entry points, each bracketed by events on the
+    # launching stream so the expert GEMMs and the HBM stages are timed live.
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        B.moe_gate(cfg, x, Wg, Wn, noise, bias, idx, gate, thr, ws, stream)
+        if ev: ev[1].record(stream)
+        B.moe_dispatch(cfg, idx, gate, x, pos, keep, count, offset, xbuf, row_token, row_gate, ws,
+                       stream)
+        if ev: ev[2].record(stream)
+        B.moe_expert_ffn(cfg, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, ws, stream)
+        if ev: ev[3].record(stream)
+        B.moe_combine(cfg, x, zbuf, pos, keep, idx, offset, y, ws, stream)
+        if ev: ev[4].record(stream)
+        B.moe_aux_loss(cfg, ws, out3, None, None, stream)
+        if ev: ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) during warm-up")
+    accepted = int(keep.sum().item())
+    experts_used = int((torch.minimum(count, torch.tensor(w.capacity, device=dev)) > 0).sum())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush, outside the per-step events
+        step(evs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the timed region")
+    stages = ["gate", "dispatch", "expert_ffn", "combine", "aux_loss"]
+    per = {s: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+           for j, s in enumerate(stages)}
+    step_ms = [sum(per[s][i] for s in stages) for i in range(args.steps)]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # End to end through the public call moe_forward: pinned host inputs copied
+    # in and the result read back, inside the timed region, every step.
+    x_h = torch.empty(x.shape, dtype=x.dtype).pin_memory()
+    x_h.copy_(x.cpu())
+    noise_h = None
+    if noise is not None:
+        noise_h = torch.empty(noise.shape, dtype=noise.dtype).pin_memory()
+        noise_h.copy_(noise.cpu())
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    aux_h = torch.empty(3, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    noise_d = None if noise is None else torch.empty_like(noise)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        if noise_d is not None:
+            noise_d.copy_(noise_h, non_blocking=True)
+        B.moe_forward(cfg, x_d, Wg, Wn, noise_d, bias, W1, b1, W2, b2, y, out3, ws,
+                      stream=stream)
+        y_h.copy_(y, non_blocking=True)
+        aux_h.copy_(out3, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        e2e_step()
+        b_ev.record(stream)
+        b_ev.synchronize()
+        e_ms.append(a_ev.elapsed_time(b_ev))
+    e2e_ms = statistics.mean(e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the e2e region")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+
+    peaks, peak_kind = load_peaks()
+    tr = stage_traffic(w, accepted, experts_used)
+    mean = {s: statistics.mean(v) for s, v in per.items()}
+    ffn_s = mean["expert_ffn"] * 1e-3
+    ffn_tflops = tr["ffn_flops"] / ffn_s / 1e12
+    bw = lambda b, s: b / (mean[s] * 1e-3) / 1e9
+    stage_rep = {
+        "gate": {"ms": mean["gate"], "gbs": bw(tr["gate_bytes"], "gate"),
+                 "hbm_frac": bw(tr["gate_bytes"], "gate") / peaks["hbm_gbs"],
+                 "router_tflops": tr["router_flops"] / (mean["gate"] * 1e-3) / 1e12},
+        "dispatch": {"ms": mean["dispatch"], "gbs": bw(tr["dispatch_bytes"], "dispatch"),
+                     "hbm_frac": bw(tr["dispatch_bytes"], "dispatch") / peaks["hbm_gbs"]},
+        "expert_ffn": {"ms": mean["expert_ffn"], "tflops": ffn_tflops,
+                       "bf16_frac": ffn_tflops / peaks["bf16_tflops"],
+                       "bf16_frac_sustained": ffn_tflops / peaks["bf16_tflops_sustained"]},
+        "combine": {"ms": mean["combine"], "gbs": bw(tr["combine_bytes"], "combine"),
+                    "hbm_frac": bw(tr["combine_bytes"], "combine") / peaks["hbm_gbs"]},
+        "aux_loss": {"ms": mean["aux_loss"]},
+    }
+    tps = world * T / (ms * 1e-3)
+    # router, select, balancing partials, slot histogram / scan / rank, gather,
+    # two expert GEMMs, combine, balancing finalize
+    launches_per_step = 11
+    line = {
+        "metric": METRIC,
+        "value": tps,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, N(0,1) gate noise)",
+        "config": workload_config(w, {"parallelism": "replicas" if world > 1 else "single",
+                                      "l2": "flushed between steps (256 MiB write)",
+                                      "accepted_rows": accepted,
+                                      "dropped_fraction": 1 - accepted / A}),
+        "roofline": {"kernel": "moe_expert_ffn (two grouped GEMM launches)", "bound": "tensor",
+                     "achieved": ffn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ffn_tflops / peaks["bf16_tflops"], "peak_source": peak_kind,
+                     "algorithmic_flops_per_launch": tr["ffn_flops"], "traffic": None},
+        "stages": stage_rep,
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x.numel() * x.element_size()
+                + (0 if noise is None else noise.numel() * 4),
+                "d2h_bytes_per_step": y.numel() * y.element_size() + 12},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_sample)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+
+def cpu_baseline(w: wl.Workload, inp: dict, n_sample: int) -> dict:
+    """The fp64 oracle as it stands on the host cores: the gate, slots and
+    balancing sums over every token, plus the expert loop for n_sample tokens;
+    the full-batch time is extrapolated from the per-token expert cost."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    c, s, H, _ = oracle.router(inp["x"], inp["Wg"], inp["Wn"], inp["noise"], inp["bias"])
+    idx, gate, hk, hk1 = oracle.select(H, w.k, inp["mode"])
+    C = oracle.capacity(w.T, w.E, w.k, w.cf, w.min_cap)
+    pos, keep, _ = oracle.slots(idx, w.E, C)
+    oracle.aux(c, s, H, idx, gate, hk, hk1, w.noisy)
+    t_gate = time.perf_counter() - t0
+    n = min(n_sample, w.T)
+    tokens = np.linspace(0, w.T - 1, n).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.layer_out(inp["x"], idx, gate, keep, inp["W1"], inp["W2"], inp["b1"], inp["b2"], tokens)
+    t_ffn = time.perf_counter() - t0
+    full = t_gate + t_ffn * (w.T / n)
+    return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"gate+slots+aux over all {w.T} tokens ({t_gate:.2f} s) and the expert "
+                      f"loop over {n} evenly spaced tokens ({t_ffn:.2f} s), extrapolated to "
+                      f"{w.T} tokens"}
+
+
+def run_reference(args, w: wl.Workload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    inp = wl.generate(w, seed=0)
+    for _ in range(args.warmup):
+        cpu_baseline(w, inp, max(2, args.cpu_sample // 8))
+    vals = []
+    last = None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        last = cpu_baseline(w, inp, args.cpu_sample)
+        vals.append(last["value"])
+    _ = time.perf_counter() - t0
+    v = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.T / v * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, {"parallelism": "host cores"}),
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="top2_large_experts", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-sample", type=int, default=16,
+                    help="tokens whose expert loop the oracle runs for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    w = wl.WORKLOADS[args.workload]
+    line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

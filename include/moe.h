@@ -1,0 +1,181 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward path of the sparsely-gated
+ * Mixture-of-Experts layer on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer, as the pages state it ("Outrageously Large Neural Networks: The
+ * Sparsely-Gated Mixture-of-Experts Layer", section 3.4; "Switch Transformer",
+ * Implementation steps 1-8): T tokens of width d are routed to k of E experts,
+ * each a ReLU feed-forward network of hidden width d_ff; each expert accepts at
+ * most C = max(min_capacity, min(T, floor(k*T*capacity_factor/E))) of them,
+ * in token order; the output is the input plus the gate-weighted sum of the
+ * accepted experts' outputs; two balancing losses (importance and load) and
+ * the Switch auxiliary loss are reported on the side.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.  Every array argument is a DEVICE pointer owned by the caller, on the
+ *   current CUDA device, row-major and contiguous, 16-byte aligned. The library
+ *   never allocates, frees or copies host<->device (except moe_last_device_status,
+ *   which reads 16 bytes back). Scratch space is the caller's workspace `ws` of
+ *   moe_workspace_size() bytes (256-byte aligned).
+ * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream) and returns without synchronising.
+ * Element types.  cfg->act_dtype (MOE_F32 or MOE_BF16) is the type of x, W1,
+ *   b1, W2, b2, y, xbuf and hbuf. The router weights, router bias, noise,
+ *   gates and zbuf are always fp32.
+ * Errors.  A bad argument returns MOE_ERR_ARG (or MOE_ERR_UNSUPPORTED) before
+ *   anything is enqueued. A failed launch returns MOE_ERR_CUDA. Conditions found
+ *   on the device -- a non-finite router logit, expert output or layer output
+ *   (the Switch page raises on each), an index out of range, or a bounded wait
+ *   that ran out -- are recorded in a status word inside `ws`;
+ *   moe_last_device_status() reads it. moe_gate() and moe_forward() clear it
+ *   when they start.
+ * Determinism.  Indices, slots and drop masks are exact; no floating-point
+ *   atomics are used, so two calls on the same inputs give identical bits.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,         /* invalid argument (sizes, null or misaligned pointer) */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but not handled by this build */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  MOE_ERR_NONFINITE = 4,   /* device: a logit or an output was Inf/NaN */
+  MOE_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel ran out */
+  MOE_ERR_BOUNDS = 6       /* device: an index fell outside its array */
+} moe_status;
+
+typedef enum {
+  MOE_GATE_TOPK_SOFTMAX = 0, /* G = Softmax(KeepTopK(H, k)) ("Outrageously Large", Eq. 5) */
+  MOE_GATE_SWITCH = 1        /* k = 1; p = Softmax(H); gate = p[argmax] ("Switch", step 2) */
+} moe_gate_mode;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+  int32_t T;               /* tokens, >= 1 */
+  int32_t d;               /* token width, >= 1 */
+  int32_t E;               /* experts, >= 1 */
+  int32_t d_ff;            /* expert hidden width, >= 1 */
+  int32_t k;               /* experts per token, 1 <= k <= E (1 for MOE_GATE_SWITCH) */
+  float capacity_factor;   /* > 0 */
+  int32_t min_capacity;    /* >= 1; the Switch page's reduced minimum is 1 */
+  int32_t gate_mode;       /* moe_gate_mode */
+  int32_t act_dtype;       /* moe_dtype */
+} moe_config;
+
+/* Human-readable name of a moe_status value (static string). */
+const char *moe_status_string(int status);
+
+/* Expert capacity C = max(min_capacity, min(T, floor(k*T*capacity_factor/E)))
+ * ("Switch Transformer", step 3, with the top-k factor k). Host only. */
+int moe_capacity(const moe_config *cfg, int32_t *C);
+
+/* Bytes of workspace every entry point below needs for `cfg`. Host only. */
+int moe_workspace_size(const moe_config *cfg, size_t *bytes);
+
+/*
+ * Stages 1-2: router and gate ("Outrageously Large", section 3.4, Eqs. 4-5;
+ * "Switch Transformer", steps 1-2).
+ *   c = x Wg + logit_bias; sigma = Softplus(x Wnoise); H = c + noise * sigma
+ *   TOPK:   expert_idx[t,:] = the k largest H (descending; lower index on
+ *           ties), gate[t,:] = softmax of those k values.
+ *   SWITCH: expert_idx[t,0] = argmax H (first on ties), gate[t,0] = Softmax(H)
+ *           at that expert (not renormalised).
+ * x [T,d] (act_dtype); Wg, Wnoise [d,E] fp32; noise [T,E] fp32 (the
+ * StandardNormal() draws, supplied so runs are deterministic); logit_bias [E]
+ * fp32. Wnoise and noise are both NULL (no noise: sigma = 0, H = c) or both
+ * given; logit_bias may be NULL. Outputs: expert_idx [T,k] int32, gate [T,k]
+ * fp32, thr [T,2] fp32 = (k-th largest H, (k+1)-th largest H or -inf when
+ * k == E). Also leaves in `ws` what moe_aux_loss() reads.
+ */
+int moe_gate(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+             const float *noise, const float *logit_bias, int32_t *expert_idx, float *gate,
+             float *thr, void *ws, moe_stream_t stream);
+
+/*
+ * Stage 3 and dispatch ("Switch Transformer", steps 3-5): positions are
+ * exclusive counts in token order, pos[t,j] = number of assignments (t',j')
+ * before (t,j) in token-major order with the same expert; keep = pos < C.
+ * Inputs: expert_idx [T,k], gate [T,k] from moe_gate, x [T,d].
+ * Outputs: pos [T,k] int32; keep [T,k] uint8; expert_count [E] int32 = choices
+ * per expert before capacity; expert_offset [E+1] int32 = exclusive sum of
+ * min(expert_count, C); rows expert_offset[e] .. expert_offset[e+1]-1 of
+ * xbuf [T*k, d] hold expert e's accepted tokens in token order;
+ * row_token [T*k] int32 = t*k + j of each row; row_gate [T*k] fp32 = its gate.
+ * Rows past expert_offset[E] are not written.
+ */
+int moe_dispatch(const moe_config *cfg, const int32_t *expert_idx, const float *gate,
+                 const void *x, int32_t *pos, uint8_t *keep, int32_t *expert_count,
+                 int32_t *expert_offset, void *xbuf, int32_t *row_token, float *row_gate,
+                 void *ws, moe_stream_t stream);
+
+/*
+ * Stage 4, experts ("Switch Transformer", step 6; "Outrageously Large", the
+ * expert networks E_i): for each expert e and each of its rows r,
+ *   hbuf[r] = ReLU(xbuf[r] W1[e] + b1[e])             (act_dtype)
+ *   zbuf[r] = row_gate[r] * (hbuf[r] W2[e] + b2[e])   (fp32)
+ * W1 [E,d,d_ff], b1 [E,d_ff] (NULL = 0), W2 [E,d_ff,d], b2 [E,d] (NULL = 0);
+ * expert_offset and row_gate as written by moe_dispatch; hbuf [T*k,d_ff],
+ * zbuf [T*k,d]. bf16 runs on the tensor cores with fp32 accumulation.
+ */
+int moe_expert_ffn(const moe_config *cfg, const void *xbuf, const int32_t *expert_offset,
+                   const float *row_gate, const void *W1, const void *b1, const void *W2,
+                   const void *b2, void *hbuf, float *zbuf, void *ws, moe_stream_t stream);
+
+/*
+ * Stage 4, combine ("Switch Transformer", step 7; "Outrageously Large", the
+ * output y = sum_i G(x)_i E_i(x)): y[t] = x[t] + sum over j with keep[t,j] of
+ * zbuf[expert_offset[expert_idx[t,j]] + pos[t,j]], summed in j order in fp32
+ * and rounded once to act_dtype. A token with no accepted choice gets y = x.
+ */
+int moe_combine(const moe_config *cfg, const void *x, const float *zbuf, const int32_t *pos,
+                const uint8_t *keep, const int32_t *expert_idx, const int32_t *expert_offset,
+                void *y, void *ws, moe_stream_t stream);
+
+/*
+ * Stage 5, balancing losses, from what moe_gate() left in `ws` (all before
+ * capacity): importance[e] = sum_t G(x_t)_e ("Outrageously Large", Eq. 6);
+ * load[e] = sum_t P(x_t,e) with P(x,e) = Phi((c_e - kth_excluding(H,k,e)) /
+ * sigma_e) (Eqs. 8-10; the 0/1 indicator of selection when there is no noise);
+ * out3[0] = CV(importance)^2, out3[1] = CV(load)^2 (population std, Eq. 7;
+ * the caller applies its own weights w_importance, w_load); out3[2] =
+ * 0.01 * E * sum_e f_e * Pbar_e with f_e the fraction of tokens whose first
+ * choice is e and Pbar_e the mean of Softmax(H)_e ("Switch Transformer",
+ * step 8). out3 [3] fp32; importance, load [E] fp32, each may be NULL.
+ */
+int moe_aux_loss(const moe_config *cfg, const void *ws, float *out3, float *importance,
+                 float *load, moe_stream_t stream);
+
+/*
+ * Stages 1-5 in one call: moe_gate, moe_dispatch, moe_expert_ffn, moe_combine
+ * and moe_aux_loss, with the intermediate buffers inside `ws`. y [T,d]
+ * (act_dtype), aux_out3 [3] fp32 (may be NULL to skip stage 5), and optionally
+ * (each may be NULL) expert_idx [T,k], gate [T,k], pos [T,k], keep [T,k].
+ */
+int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                const float *noise, const float *logit_bias, const void *W1, const void *b1,
+                const void *W2, const void *b2, void *y, float *aux_out3, int32_t *expert_idx,
+                float *gate, int32_t *pos, uint8_t *keep, void *ws, moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, returns the first device-side error recorded in `ws`
+ * since it was last cleared (MOE_OK if none), writes its detail word (e.g. the
+ * offending flat index) to *detail if non-NULL, and clears it.
+ */
+int moe_last_device_status(void *ws, moe_stream_t stream, int64_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -91,17 +91,21 @@ int orc_router(int T, int d, int E, const void *x, int x_dtype, const float *Wg,
   int bad = 0;
 #pragma omp parallel for schedule(static) reduction(| : bad)
   for (int t = 0; t < T; ++t) {
+    /* acc_c[e] and acc_z[e] each sum x_i * W[i,e] over i = 0..d-1 in order. */
+    double *acc_c = (double *)calloc((size_t)E, sizeof(double));
+    double *acc_z = (double *)calloc((size_t)E, sizeof(double));
+    for (int i = 0; i < d; ++i) {
+      double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+      for (int e = 0; e < E; ++e) acc_c[e] += xi * (double)Wg[(size_t)i * E + e];
+      if (Wn)
+        for (int e = 0; e < E; ++e) acc_z[e] += xi * (double)Wn[(size_t)i * E + e];
+    }
     for (int e = 0; e < E; ++e) {
-      double acc = 0.0;
-      for (int i = 0; i < d; ++i)
-        acc += orc_in(x, x_dtype, (size_t)t * d + i) * (double)Wg[(size_t)i * E + e];
+      double acc = acc_c[e];
       if (bias) acc += (double)bias[e];
       double s = 0.0, h = acc;
       if (Wn) {
-        double z = 0.0;
-        for (int i = 0; i < d; ++i)
-          z += orc_in(x, x_dtype, (size_t)t * d + i) * (double)Wn[(size_t)i * E + e];
-        s = orc_softplus(z);
+        s = orc_softplus(acc_z[e]);
         h = acc + (double)noise[(size_t)t * E + e] * s;
       }
       c[(size_t)t * E + e] = acc;
@@ -109,6 +113,8 @@ int orc_router(int T, int d, int E, const void *x, int x_dtype, const float *Wg,
       H[(size_t)t * E + e] = h;
       if (!isfinite(h)) bad = 1;
     }
+    free(acc_c);
+    free(acc_z);
   }
   return bad;
 }

@@ -1,0 +1,167 @@
+"""ctypes binding of libmoe.so: the C-ABI entry points under the same names.
+
+Argument marshalling only. Arrays are torch CUDA tensors (or None where the C
+signature allows NULL); they pass as raw device pointers, and every step of
+the computation runs in the library's CUDA kernels. A non-zero status raises
+MoEError. Loading fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+MOE_GATE_TOPK_SOFTMAX = 0
+MOE_GATE_SWITCH = 1
+MOE_F32 = 0
+MOE_BF16 = 1
+
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+                4: "MOE_ERR_NONFINITE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_BOUNDS"}
+
+# Every symbol include/moe.h declares.
+EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate", "moe_dispatch",
+           "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
+           "moe_last_device_status")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("d_ff", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
+                ("gate_mode", ctypes.c_int32), ("act_dtype", ctypes.c_int32)]
+
+
+def config(T, d, E, d_ff, k, capacity_factor, gate_mode=MOE_GATE_TOPK_SOFTMAX,
+           act_dtype=MOE_BF16, min_capacity=1) -> moe_config:
+    return moe_config(T, d, E, d_ff, k, capacity_factor, min_capacity, gate_mode, act_dtype)
+
+
+def config_for(w) -> moe_config:
+    """moe_config of a workloads.Workload."""
+    return config(w.T, w.d, w.E, w.d_ff, w.k, w.cf,
+                  MOE_GATE_SWITCH if w.mode == "switch" else MOE_GATE_TOPK_SOFTMAX,
+                  MOE_BF16 if w.dtype == "bf16" else MOE_F32, w.min_cap)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: run the package build first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, CP = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(moe_config)
+            L.moe_status_string.argtypes = [I]
+            L.moe_status_string.restype = ctypes.c_char_p
+            L.moe_capacity.argtypes = [CP, ctypes.POINTER(ctypes.c_int32)]
+            L.moe_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
+            L.moe_gate.argtypes = [CP] + [P] * 10
+            L.moe_dispatch.argtypes = [CP] + [P] * 12
+            L.moe_expert_ffn.argtypes = [CP] + [P] * 11
+            L.moe_combine.argtypes = [CP] + [P] * 9
+            L.moe_aux_loss.argtypes = [CP] + [P] * 5
+            L.moe_forward.argtypes = [CP] + [P] * 17
+            L.moe_last_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int64)]
+            for name in EXPORTS[1:]:
+                getattr(L, name).restype = I
+            _lib = L
+        return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise MoEError(status, where)
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_capacity(cfg: moe_config) -> int:
+    c = ctypes.c_int32()
+    _check(lib().moe_capacity(ctypes.byref(cfg), ctypes.byref(c)), "moe_capacity")
+    return c.value
+
+
+def moe_workspace_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_gate(cfg, x, Wg, Wnoise, noise, logit_bias, expert_idx, gate, thr, ws, stream=None):
+    _check(lib().moe_gate(ctypes.byref(cfg), _p(x), _p(Wg), _p(Wnoise), _p(noise), _p(logit_bias),
+                          _p(expert_idx), _p(gate), _p(thr), _p(ws), _stream(stream)), "moe_gate")
+
+
+def moe_dispatch(cfg, expert_idx, gate, x, pos, keep, expert_count, expert_offset, xbuf,
+                 row_token, row_gate, ws, stream=None):
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _p(expert_idx), _p(gate), _p(x), _p(pos),
+                              _p(keep), _p(expert_count), _p(expert_offset), _p(xbuf),
+                              _p(row_token), _p(row_gate), _p(ws), _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_expert_ffn(cfg, xbuf, expert_offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, ws,
+                   stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), _p(xbuf), _p(expert_offset), _p(row_gate),
+                                _p(W1), _p(b1), _p(W2), _p(b2), _p(hbuf), _p(zbuf), _p(ws),
+                                _stream(stream)), "moe_expert_ffn")
+
+
+def moe_combine(cfg, x, zbuf, pos, keep, expert_idx, expert_offset, y, ws, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(x), _p(zbuf), _p(pos), _p(keep),
+                             _p(expert_idx), _p(expert_offset), _p(y), _p(ws), _stream(stream)),
+           "moe_combine")
+
+
+def moe_aux_loss(cfg, ws, out3, importance=None, load=None, stream=None):
+    _check(lib().moe_aux_loss(ctypes.byref(cfg), _p(ws), _p(out3), _p(importance), _p(load),
+                              _stream(stream)), "moe_aux_loss")
+
+
+def moe_forward(cfg, x, Wg, Wnoise, noise, logit_bias, W1, b1, W2, b2, y, aux_out3, ws,
+                expert_idx=None, gate=None, pos=None, keep=None, stream=None):
+    _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(Wg), _p(Wnoise), _p(noise),
+                             _p(logit_bias), _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(aux_out3),
+                             _p(expert_idx), _p(gate), _p(pos), _p(keep), _p(ws),
+                             _stream(stream)), "moe_forward")
+
+
+def moe_last_device_status(ws, stream=None):
+    """Synchronise, return (status, detail) recorded on the device, and clear it."""
+    det = ctypes.c_int64()
+    st = lib().moe_last_device_status(_p(ws), _stream(stream), ctypes.byref(det))
+    return st, det.value

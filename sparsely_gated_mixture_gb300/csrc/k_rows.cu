@@ -1,0 +1,164 @@
+// Row movement around the experts.
+//   gather  ("Switch Transformer", step 5: dispatch): row r of the packed
+//           buffer receives token row_token[r] / k, so expert e's accepted
+//           tokens sit contiguously, in token order, from offset[e].
+//   combine ("Switch Transformer", step 7; "Outrageously Large", the output
+//           y = sum_i G_i E_i(x), plus the residual): y[t] = x[t] + the kept
+//           gate-weighted expert rows of t, added in choice order in fp32.
+// Both are pure HBM streams: 16-byte vector loads and stores, one warp per row.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRowWarps = 8;
+
+// Gather: copies d elements of `elem` bytes per row, in 16-byte vectors when
+// the row length allows (the library requires 16-byte aligned base pointers).
+template <typename V>
+__global__ void __launch_bounds__(kRowWarps * 32)
+k_gather(int A, int k, int nvec, const V *__restrict__ x, const int32_t *__restrict__ offset_end,
+         const int32_t *__restrict__ row_token, V *__restrict__ xbuf, DeviceStatus *st) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (r >= A || r >= *offset_end) return;
+  const int a = row_token[r];
+  if (a < 0 || a >= A) {
+    if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)r);
+    return;
+  }
+  const int t = a / k;
+  const V *src = x + (size_t)t * nvec;
+  V *dst = xbuf + (size_t)r * nvec;
+  int v = lane;
+  for (; v + 96 < nvec; v += 128) {
+    V a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
+    dst[v] = a0;
+    dst[v + 32] = a1;
+    dst[v + 64] = a2;
+    dst[v + 96] = a3;
+  }
+  for (; v < nvec; v += 32) dst[v] = src[v];
+}
+
+template <typename T>
+struct Act;
+template <>
+struct Act<float> {
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <>
+struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Combine: one warp per token; each lane handles groups of 4 consecutive
+// elements (VEC4) or single elements.
+template <typename T, bool VEC4>
+__global__ void __launch_bounds__(kRowWarps * 32)
+k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__restrict__ zbuf,
+          const int32_t *__restrict__ pos, const uint8_t *__restrict__ keep,
+          const int32_t *__restrict__ idx, const int32_t *__restrict__ offset, T *__restrict__ y,
+          DeviceStatus *st) {
+  constexpr int kMaxK = 16;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  int rows[kMaxK];
+  int nr = 0;
+  for (int j = 0; j < k; ++j) {
+    size_t a = (size_t)t * k + j;
+    if (!keep[a]) continue;
+    int e = idx[a];
+    int r = (e >= 0 && e < E) ? offset[e] + pos[a] : -1;
+    if (r < 0 || e < 0 || e >= E || r >= offset[e + 1]) {
+      if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)a);
+      continue;
+    }
+    rows[nr++] = r;
+  }
+  const T *xr = x + (size_t)t * d;
+  T *yr = y + (size_t)t * d;
+  bool bad = false;
+  if (VEC4) {
+    for (int c = lane * 4; c < d; c += 128) {
+      float acc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = Act<T>::to_f(xr[c + q]);
+      for (int i = 0; i < nr; ++i) {
+        float4 z = *reinterpret_cast<const float4 *>(zbuf + (size_t)rows[i] * d + c);
+        acc[0] += z.x;
+        acc[1] += z.y;
+        acc[2] += z.z;
+        acc[3] += z.w;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        bad |= !isfinite(acc[q]);
+        yr[c + q] = Act<T>::from_f(acc[q]);
+      }
+    }
+  } else {
+    for (int c = lane; c < d; c += 32) {
+      float acc = Act<T>::to_f(xr[c]);
+      for (int i = 0; i < nr; ++i) acc += zbuf[(size_t)rows[i] * d + c];
+      bad |= !isfinite(acc);
+      yr[c] = Act<T>::from_f(acc);
+    }
+  }
+  if (bad) record_error(st, MOE_ERR_NONFINITE, (long long)t);
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,
+                          const int32_t *row_token, void *xbuf, DeviceStatus *st, cudaStream_t s) {
+  const int A = cfg.T * cfg.k;
+  const size_t row_bytes = (size_t)cfg.d * elem_bytes(cfg.act_dtype);
+  dim3 grid((A + kRowWarps - 1) / kRowWarps);
+  const int32_t *end = offset + cfg.E;
+  if (row_bytes % 16 == 0) {
+    k_gather<uint4><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 16),
+                                                    (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
+  } else if (row_bytes % 4 == 0) {
+    k_gather<uint32_t><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 4),
+                                                       (const uint32_t *)x, end, row_token,
+                                                       (uint32_t *)xbuf, st);
+  } else {
+    k_gather<uint16_t><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 2),
+                                                       (const uint16_t *)x, end, row_token,
+                                                       (uint16_t *)xbuf, st);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zbuf,
+                           const int32_t *pos, const uint8_t *keep, const int32_t *idx,
+                           const int32_t *offset, void *y, DeviceStatus *st, cudaStream_t s) {
+  dim3 grid((cfg.T + kRowWarps - 1) / kRowWarps);
+  const bool v4 = cfg.d % 4 == 0;
+  if (cfg.act_dtype == MOE_BF16) {
+    auto xp = (const __nv_bfloat16 *)x;
+    auto yp = (__nv_bfloat16 *)y;
+    if (v4)
+      k_combine<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, s>>>(
+          cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+    else
+      k_combine<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, s>>>(
+          cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+  } else {
+    auto xp = (const float *)x;
+    auto yp = (float *)y;
+    if (v4)
+      k_combine<float, true><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf,
+                                                             pos, keep, idx, offset, yp, st);
+    else
+      k_combine<float, false><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
+                                                              zbuf, pos, keep, idx, offset, yp, st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

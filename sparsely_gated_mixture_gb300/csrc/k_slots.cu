@@ -1,0 +1,177 @@
+// Stage 3: capacity and token-order slot assignment ("Switch Transformer",
+// steps 3-4). The position of assignment a = t*k + j is the number of earlier
+// assignments (in that flat, token-major order) to the same expert: an
+// exclusive cumulative count. It is computed without atomics on the order:
+//   k_slot_hist  -- per chunk of kSlotChunk assignments, count per expert;
+//   k_slot_scan  -- per expert, exclusive sum over chunks (chunk bases), the
+//                   total n_e, min(n_e, C), row offsets and GEMM tile offsets;
+//   k_slot_rank  -- one warp walks each chunk in order, 32 assignments at a
+//                   time: __match_any_sync finds same-expert lanes, the rank
+//                   among them is a popcount, a per-warp counter carries it.
+// Kept assignments (pos < C) get row offset[e] + pos of the packed buffer.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kHistThreads = 256;
+constexpr int kScanThreads = 1024;
+constexpr int kRankWarps = 8;
+
+__global__ void __launch_bounds__(kHistThreads)
+k_slot_hist(int A, int E, const int32_t *__restrict__ idx, int32_t *__restrict__ hist,
+            DeviceStatus *st) {
+  extern __shared__ int32_t sh_hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
+  __syncthreads();
+  const int a0 = blockIdx.x * kSlotChunk;
+  for (int i = threadIdx.x; i < kSlotChunk; i += blockDim.x) {
+    int a = a0 + i;
+    if (a >= A) break;
+    int e = idx[a];
+    if (e < 0 || e >= E) {
+      record_error(st, MOE_ERR_BOUNDS, (long long)a);
+      continue;
+    }
+    atomicAdd(&sh_hist[e], 1);  // integer counts: order does not matter
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = sh_hist[e];
+}
+
+// Exclusive block scan of one int per thread (blockDim.x == kScanThreads).
+__device__ int block_exclusive_scan(int v, int *sh_warp, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = sh_warp[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    sh_warp[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) sh_warp[32] = wi;
+  }
+  __syncthreads();
+  int r = sh_warp[warp] + incl - v;
+  *total = sh_warp[32];
+  __syncthreads();
+  return r;
+}
+
+// One block. Experts are processed kScanThreads at a time; carries join the tiles.
+__global__ void __launch_bounds__(kScanThreads)
+k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
+            int32_t *__restrict__ count, int32_t *__restrict__ offset,
+            int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist) {
+  __shared__ int sh_warp[33];
+  int carry_rows = 0, carry_tiles = 0;
+  for (int e0 = 0; e0 < E; e0 += kScanThreads) {
+    int e = e0 + threadIdx.x;
+    int n = 0;
+    if (e < E) {
+      for (int c = 0; c < n_chunks; ++c) {
+        hist_base[(size_t)c * E + e] = n;
+        n += hist[(size_t)c * E + e];
+      }
+      count[e] = n;
+    }
+    int kept = e < E ? min(n, C) : 0;
+    int tiles = (kept + bm - 1) / bm;
+    int tot_rows, tot_tiles;
+    int off = block_exclusive_scan(kept, sh_warp, &tot_rows);
+    int toff = block_exclusive_scan(tiles, sh_warp, &tot_tiles);
+    if (e < E) {
+      offset[e] = carry_rows + off;
+      mtiles[e] = carry_tiles + toff;
+    }
+    carry_rows += tot_rows;
+    carry_tiles += tot_tiles;
+  }
+  if (threadIdx.x == 0) {
+    offset[E] = carry_rows;
+    mtiles[E] = carry_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(kRankWarps * 32)
+k_slot_rank(int A, int E, int C, int n_chunks, const int32_t *__restrict__ idx,
+            const float *__restrict__ gate, const int32_t *__restrict__ hist_base,
+            const int32_t *__restrict__ offset, int32_t *__restrict__ pos,
+            uint8_t *__restrict__ keep, int32_t *__restrict__ row_token,
+            float *__restrict__ row_gate) {
+  extern __shared__ int32_t sh_cnt[];  // [kRankWarps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunk = blockIdx.x * kRankWarps + warp;
+  if (chunk >= n_chunks) return;  // whole warps leave together; no block barrier below
+  int32_t *cnt = sh_cnt + (size_t)warp * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int a0 = chunk * kSlotChunk;
+  const int a1 = min(A, a0 + kSlotChunk);
+  for (int base = a0; base < a1; base += 32) {
+    int a = base + lane;
+    int e = -1;
+    if (a < a1) {
+      e = idx[a];
+      if (e < 0 || e >= E) e = -1;  // counted as a bounds error by k_slot_hist
+    }
+    unsigned peers = __match_any_sync(0xffffffffu, e);
+    int before = e >= 0 ? cnt[e] : 0;
+    __syncwarp();
+    if (e >= 0 && (peers & lt) == 0) cnt[e] = before + __popc(peers);  // lowest peer updates
+    __syncwarp();
+    if (e >= 0) {
+      int p = hist_base[(size_t)chunk * E + e] + before + __popc(peers & lt);
+      pos[a] = p;
+      bool kp = p < C;
+      keep[a] = kp ? 1 : 0;
+      if (kp) {
+        int r = offset[e] + p;
+        row_token[r] = a;
+        row_gate[r] = gate[a];
+      }
+    } else if (a < a1) {
+      pos[a] = -1;
+      keep[a] = 0;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
+                         int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
+                         int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
+                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s) {
+  const int A = cfg.T * cfg.k;
+  k_slot_hist<<<n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s>>>(A, cfg.E, idx, hist, st);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  k_slot_scan<<<1, kScanThreads, 0, s>>>(cfg.E, C, n_chunks, kTcBM, chunk_base, count, offset,
+                                         mtiles, hist);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  size_t smem = (size_t)kRankWarps * cfg.E * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    err = cudaFuncSetAttribute(k_slot_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (err != cudaSuccess) return err;
+  }
+  int blocks = (n_chunks + kRankWarps - 1) / kRankWarps;
+  k_slot_rank<<<blocks, kRankWarps * 32, smem, s>>>(A, cfg.E, C, n_chunks, idx, gate, chunk_base,
+                                                    offset, pos, keep, row_token, row_gate);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,282 @@
+// C ABI of libmoe.so (declared in include/moe.h): argument checks, the
+// workspace layout and the order of launches. No computation happens here;
+// every stage runs in the kernels of the other translation units.
+#include "moe_internal.cuh"
+
+#include <math.h>
+#include <string.h>
+
+namespace moe {
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+WsLayout ws_layout(const moe_config &cfg) {
+  WsLayout L{};
+  const size_t T = cfg.T, E = cfg.E, k = cfg.k, d = cfg.d, dff = cfg.d_ff;
+  const size_t A = T * k;
+  const size_t eb = elem_bytes(cfg.act_dtype);
+  L.n_chunks = (int)((A + kSlotChunk - 1) / kSlotChunk);
+  L.n_aux_blocks = (int)((T + kAuxTokBlock - 1) / kAuxTokBlock);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(sizeof(DeviceStatus));
+  L.c = take(T * E * 4);
+  L.sigma = take(T * E * 4);
+  L.H = take(T * E * 4);
+  L.rowstat = take(T * 2 * 4);
+  L.hist = take((size_t)L.n_chunks * E * 4);
+  L.chunk_base = take((size_t)L.n_chunks * E * 4);
+  L.count = take(E * 4);
+  L.offset = take((E + 1) * 4);
+  L.mtiles = take((E + 1) * 4);
+  L.partials = take((size_t)L.n_aux_blocks * 4 * E * 4);
+  L.aux_vec = take(4 * E * 4);
+  L.idx = take(A * 4);
+  L.gate = take(A * 4);
+  L.thr = take(T * 2 * 4);
+  L.pos = take(A * 4);
+  L.keep = take(A);
+  L.row_token = take(A * 4);
+  L.row_gate = take(A * 4);
+  L.xbuf = take(A * d * eb);
+  L.hbuf = take(A * dff * eb);
+  L.zbuf = take(A * d * 4);
+  L.total = off;
+  return L;
+}
+
+static int host_capacity(const moe_config &c) {
+  double raw = floor((double)c.k * (double)c.T * (double)c.capacity_factor / (double)c.E);
+  long v = (long)raw;
+  if (v > c.T) v = c.T;
+  if (v < c.min_capacity) v = c.min_capacity;
+  return (int)v;
+}
+
+static int check_cfg(const moe_config *c) {
+  if (!c) return MOE_ERR_ARG;
+  if (c->T < 1 || c->d < 1 || c->E < 1 || c->d_ff < 1 || c->k < 1 || c->k > c->E) return MOE_ERR_ARG;
+  if (!(c->capacity_factor > 0.f) || !isfinite(c->capacity_factor)) return MOE_ERR_ARG;
+  if (c->min_capacity < 1) return MOE_ERR_ARG;
+  if (c->gate_mode != MOE_GATE_TOPK_SOFTMAX && c->gate_mode != MOE_GATE_SWITCH) return MOE_ERR_ARG;
+  if (c->gate_mode == MOE_GATE_SWITCH && c->k != 1) return MOE_ERR_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_ARG;
+  if ((long long)c->T * c->k > 0x7fffffffLL || (long long)c->T * c->E > 0x7fffffffLL)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->E > 1024 || c->k > 16) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Required pointers must be non-null; every given pointer 16-byte aligned.
+#define MOE_REQ(p)                                      \
+  do {                                                  \
+    if (!(p) || !aligned((p), 16)) return MOE_ERR_ARG;  \
+  } while (0)
+#define MOE_OPT(p)                                      \
+  do {                                                  \
+    if ((p) && !aligned((p), 16)) return MOE_ERR_ARG;   \
+  } while (0)
+#define MOE_CUDA(call)                                  \
+  do {                                                  \
+    if ((call) != cudaSuccess) return MOE_ERR_CUDA;     \
+  } while (0)
+
+static int gate_impl(const moe_config &c, const void *x, const float *Wg, const float *Wn,
+                     const float *noise, const float *bias, int32_t *idx, float *gate, float *thr,
+                     void *ws, bool partials, cudaStream_t s) {
+  const WsLayout L = ws_layout(c);
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
+  float *rs = ws_at<float>(ws, L.rowstat);
+  MOE_CUDA(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
+  MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, st, s));
+  MOE_CUDA(launch_select(c, H, idx, gate, thr, rs, st, s));
+  if (partials)
+    MOE_CUDA(launch_aux_partials(c, Wn != nullptr, cc, sg, H, rs, idx, gate, thr,
+                                 ws_at<float>(ws, L.partials), L.n_aux_blocks, s));
+  return MOE_OK;
+}
+
+static int ffn_impl(const moe_config &c, const void *xbuf, const int32_t *offset,
+                    const int32_t *mtiles, const float *row_gate, const void *W1, const void *b1,
+                    const void *W2, const void *b2, void *hbuf, float *zbuf, DeviceStatus *st,
+                    cudaStream_t s) {
+  const int C = host_capacity(c);
+  if (c.act_dtype == MOE_BF16 && ffn_tc_supported(c)) {
+    MOE_CUDA(launch_ffn_tc(c, C, xbuf, offset, mtiles, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+  } else {
+    MOE_CUDA(launch_ffn_simt(c, C, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+  }
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_NONFINITE: return "non-finite router logit or output";
+    case MOE_ERR_TIMEOUT: return "bounded device wait ran out";
+    case MOE_ERR_BOUNDS: return "index out of range";
+    default: return "unknown status";
+  }
+}
+
+int moe_capacity(const moe_config *cfg, int32_t *C) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!C) return MOE_ERR_ARG;
+  *C = host_capacity(*cfg);
+  return MOE_OK;
+}
+
+int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = ws_layout(*cfg).total;
+  return MOE_OK;
+}
+
+int moe_gate(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+             const float *noise, const float *logit_bias, int32_t *expert_idx, float *gate,
+             float *thr, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(Wnoise); MOE_OPT(noise); MOE_OPT(logit_bias);
+  MOE_REQ(expert_idx); MOE_REQ(gate); MOE_REQ(thr);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_ARG;
+  return gate_impl(*cfg, x, Wg, Wnoise, noise, logit_bias, expert_idx, gate, thr, ws, true,
+                   (cudaStream_t)stream);
+}
+
+int moe_dispatch(const moe_config *cfg, const int32_t *expert_idx, const float *gate,
+                 const void *x, int32_t *pos, uint8_t *keep, int32_t *expert_count,
+                 int32_t *expert_offset, void *xbuf, int32_t *row_token, float *row_gate,
+                 void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(expert_idx); MOE_REQ(gate); MOE_REQ(x); MOE_REQ(pos); MOE_REQ(keep);
+  MOE_REQ(expert_count); MOE_REQ(expert_offset); MOE_REQ(xbuf); MOE_REQ(row_token);
+  MOE_REQ(row_gate);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  MOE_CUDA(launch_slots(c, host_capacity(c), expert_idx, gate, ws_at<int32_t>(ws, L.hist),
+                        ws_at<int32_t>(ws, L.chunk_base), expert_count, expert_offset,
+                        ws_at<int32_t>(ws, L.mtiles), pos, keep, row_token, row_gate, L.n_chunks,
+                        st, s));
+  MOE_CUDA(launch_gather(c, x, expert_offset, row_token, xbuf, st, s));
+  return MOE_OK;
+}
+
+int moe_expert_ffn(const moe_config *cfg, const void *xbuf, const int32_t *expert_offset,
+                   const float *row_gate, const void *W1, const void *b1, const void *W2,
+                   const void *b2, void *hbuf, float *zbuf, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(xbuf); MOE_REQ(expert_offset); MOE_REQ(row_gate); MOE_REQ(W1); MOE_OPT(b1);
+  MOE_REQ(W2); MOE_OPT(b2); MOE_REQ(hbuf); MOE_REQ(zbuf);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  return ffn_impl(*cfg, xbuf, expert_offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf,
+                  ws_at<DeviceStatus>(ws, L.status), (cudaStream_t)stream);
+}
+
+int moe_combine(const moe_config *cfg, const void *x, const float *zbuf, const int32_t *pos,
+                const uint8_t *keep, const int32_t *expert_idx, const int32_t *expert_offset,
+                void *y, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(zbuf); MOE_REQ(pos); MOE_REQ(keep); MOE_REQ(expert_idx);
+  MOE_REQ(expert_offset); MOE_REQ(y);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  MOE_CUDA(launch_combine(*cfg, x, zbuf, pos, keep, expert_idx, expert_offset, y,
+                          ws_at<DeviceStatus>(ws, L.status), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_aux_loss(const moe_config *cfg, const void *ws, float *out3, float *importance,
+                 float *load, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(out3); MOE_OPT(importance); MOE_OPT(load);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  void *w = const_cast<void *>(ws);
+  MOE_CUDA(launch_aux_finalize(*cfg, ws_at<float>(w, L.partials), L.n_aux_blocks, out3,
+                               importance, load, ws_at<float>(w, L.aux_vec),
+                               (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                const float *noise, const float *logit_bias, const void *W1, const void *b1,
+                const void *W2, const void *b2, void *y, float *aux_out3, int32_t *expert_idx,
+                float *gate, int32_t *pos, uint8_t *keep, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(Wnoise); MOE_OPT(noise); MOE_OPT(logit_bias);
+  MOE_REQ(W1); MOE_OPT(b1); MOE_REQ(W2); MOE_OPT(b2); MOE_REQ(y); MOE_OPT(aux_out3);
+  MOE_OPT(expert_idx); MOE_OPT(gate); MOE_OPT(pos); MOE_OPT(keep);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  if ((Wnoise == nullptr) != (noise == nullptr)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
+  float *g = gate ? gate : ws_at<float>(ws, L.gate);
+  int32_t *ps = pos ? pos : ws_at<int32_t>(ws, L.pos);
+  uint8_t *kp = keep ? keep : ws_at<uint8_t>(ws, L.keep);
+  float *thr = ws_at<float>(ws, L.thr);
+  int32_t *offset = ws_at<int32_t>(ws, L.offset);
+  int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
+  float *row_gate = ws_at<float>(ws, L.row_gate);
+  void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
+  float *zbuf = ws_at<float>(ws, L.zbuf);
+  r = gate_impl(c, x, Wg, Wnoise, noise, logit_bias, idx, g, thr, ws, aux_out3 != nullptr, s);
+  if (r != MOE_OK) return r;
+  MOE_CUDA(launch_slots(c, host_capacity(c), idx, g, ws_at<int32_t>(ws, L.hist),
+                        ws_at<int32_t>(ws, L.chunk_base), ws_at<int32_t>(ws, L.count), offset,
+                        ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
+                        s));
+  MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
+  r = ffn_impl(c, xbuf, offset, ws_at<int32_t>(ws, L.mtiles), row_gate, W1, b1, W2, b2, hbuf,
+               zbuf, st, s);
+  if (r != MOE_OK) return r;
+  MOE_CUDA(launch_combine(c, x, zbuf, ps, kp, idx, offset, y, st, s));
+  if (aux_out3)
+    MOE_CUDA(launch_aux_finalize(c, ws_at<float>(ws, L.partials), L.n_aux_blocks, aux_out3,
+                                 nullptr, nullptr, ws_at<float>(ws, L.aux_vec), s));
+  return MOE_OK;
+}
+
+int moe_last_device_status(void *ws, moe_stream_t stream, int64_t *detail) {
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  DeviceStatus h{};
+  MOE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  MOE_CUDA(cudaMemcpy(&h, ws, sizeof h, cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(ws, 0, sizeof h));
+  if (detail) *detail = h.detail;
+  return h.code;
+}
+
+}  // extern "C"

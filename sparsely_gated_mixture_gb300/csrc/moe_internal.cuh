@@ -1,0 +1,100 @@
+// Internal declarations shared by the translation units of libmoe.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------------------- tiling constants
+constexpr int kSlotChunk = 512;     // assignments ranked per warp in the slot pass
+constexpr int kAuxTokBlock = 256;   // tokens per partial-sum block of the balancing sums
+constexpr int kTcBM = 128;          // rows per tile of the tensor-core expert GEMM
+constexpr int kSimtBM = 64;         // rows per tile of the CUDA-core expert GEMM
+
+// ----------------------------------------------------------------------------- device status word
+// Lives at offset 0 of the workspace. The first error wins; later ones are dropped.
+struct DeviceStatus {
+  int32_t code;
+  int32_t pad;
+  long long detail;
+};
+
+__device__ __forceinline__ void record_error(DeviceStatus *st, int code, long long detail) {
+  if (atomicCAS(&st->code, 0, code) == 0) {
+    *reinterpret_cast<volatile long long *>(&st->detail) = detail;
+  }
+}
+
+// ----------------------------------------------------------------------------- workspace layout
+struct WsLayout {
+  size_t status;
+  size_t c, sigma, H, rowstat;            // router results kept for the balancing sums
+  size_t hist, chunk_base;                // slot pass: per-chunk per-expert counts and bases
+  size_t count, offset, mtiles;           // per-expert totals, row offsets, GEMM tile prefix
+  size_t partials, aux_vec;               // balancing partial sums and final vectors
+  size_t idx, gate, thr, pos, keep;       // moe_forward's own copies of the gate / slot outputs
+  size_t row_token, row_gate;             // moe_forward's dispatch maps
+  size_t xbuf, hbuf, zbuf;                // moe_forward's expert buffers
+  size_t total;
+  int n_chunks, n_aux_blocks;
+};
+
+WsLayout ws_layout(const moe_config &cfg);
+
+template <typename T>
+inline T *ws_at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+inline int elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+
+// ----------------------------------------------------------------------------- launchers
+// Each returns a cudaError_t from the launch (cudaSuccess if nothing failed).
+
+// k_gate.cu: router GEMM + noise + softplus, selection + softmax, balancing partials.
+cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
+                          const float *noise, const float *bias, float *c, float *sigma, float *H,
+                          DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, float *gate,
+                          float *thr, float *rowstat, DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
+                                const float *sigma, const float *H, const float *rowstat,
+                                const int32_t *idx, const float *gate, const float *thr,
+                                float *partials, int n_blocks, cudaStream_t s);
+cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
+                                float *out3, float *importance, float *load, float *aux_vec,
+                                cudaStream_t s);
+
+// k_slots.cu: capacity, token-order slots, dispatch maps.
+cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
+                         int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
+                         int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
+                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s);
+
+// k_rows.cu: gather of accepted token rows and the combine with the residual.
+cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,
+                          const int32_t *row_token, void *xbuf, DeviceStatus *st,
+                          cudaStream_t s);
+cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zbuf,
+                           const int32_t *pos, const uint8_t *keep, const int32_t *idx,
+                           const int32_t *offset, void *y, DeviceStatus *st, cudaStream_t s);
+
+// k_ffn_simt.cu: CUDA-core grouped expert GEMMs (fp32, and shapes the tensor-core path rejects).
+cudaError_t launch_ffn_simt(const moe_config &cfg, int C, const void *xbuf, const int32_t *offset,
+                            const float *row_gate, const void *W1, const void *b1, const void *W2,
+                            const void *b2, void *hbuf, float *zbuf, DeviceStatus *st,
+                            cudaStream_t s);
+
+// k_ffn_tc.cu: tcgen05 / TMEM / TMA grouped expert GEMMs for bf16.
+bool ffn_tc_supported(const moe_config &cfg);
+cudaError_t launch_ffn_tc(const moe_config &cfg, int C, const void *xbuf, const int32_t *offset,
+                          const int32_t *mtiles, const float *row_gate, const void *W1,
+                          const void *b1, const void *W2, const void *b2, void *hbuf, float *zbuf,
+                          DeviceStatus *st, cudaStream_t s);
+
+}  // namespace moe

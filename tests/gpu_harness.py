@@ -1,0 +1,168 @@
+"""Helpers for the GPU parity tests: move generated inputs to the device, run
+the library through its C ABI, and compare with the oracle under the rules:
+
+* expert indices, slot positions, drop masks, counts and offsets bit-exact,
+  except tokens whose oracle margin between the k-th and (k+1)-th noisy logit
+  (or, for an order swap inside the top k, between the swapped logits) is
+  below TIE_TOL; such tokens are reported, and the GPU's choice is then fed to
+  the oracle for everything downstream;
+* bf16 outputs within 2e-2 * (1 + |ref|); fp32 outputs, gates and balancing
+  losses within 1e-4 relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from sparsely_gated_mixture_gb300 import binding as B
+from sparsely_gated_mixture_gb300 import workloads as wl
+
+TIE_TOL = 1e-6
+BF16_TOL = 2e-2
+F32_RTOL = 1e-4
+
+
+def dev_act(a, dtype: str):
+    if a is None:
+        return None
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def dev_f32(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def to_device(w: wl.Workload, inp: dict) -> dict:
+    dt = w.dtype
+    return dict(x=dev_act(inp["x"], dt), Wg=dev_f32(inp["Wg"]), Wn=dev_f32(inp["Wn"]),
+                noise=dev_f32(inp["noise"]), bias=dev_f32(inp["bias"]), W1=dev_act(inp["W1"], dt),
+                b1=dev_act(inp["b1"], dt), W2=dev_act(inp["W2"], dt), b2=dev_act(inp["b2"], dt))
+
+
+def act_to_f64(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+def act_bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy()
+    return t.view(torch.int32).cpu().numpy()
+
+
+def workspace(cfg) -> torch.Tensor:
+    return torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+
+
+def run_forward(w, d, aux=True, keep_outputs=True):
+    """moe_forward through the C ABI. Returns a dict of host arrays."""
+    cfg = B.config_for(w)
+    T, k, E = w.T, w.k, w.E
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    y = torch.empty((T, w.d), dtype=act, device="cuda")
+    out3 = torch.zeros(3, dtype=torch.float32, device="cuda") if aux else None
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    pos = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    keep = torch.empty((T, k), dtype=torch.uint8, device="cuda")
+    ws = workspace(cfg)
+    B.moe_forward(cfg, d["x"], d["Wg"], d["Wn"], d["noise"], d["bias"], d["W1"], d["b1"], d["W2"],
+                  d["b2"], y, out3, ws, idx, gate, pos, keep)
+    st, det = B.moe_last_device_status(ws)
+    return dict(status=st, detail=det, y=y, out3=None if out3 is None else out3.cpu().numpy(),
+                idx=idx.cpu().numpy(), gate=gate.cpu().numpy(), pos=pos.cpu().numpy(),
+                keep=keep.cpu().numpy(), ws=ws)
+
+
+def run_stages(w, d):
+    """The five stage entry points in turn, keeping every intermediate."""
+    cfg = B.config_for(w)
+    T, k, E = w.T, w.k, w.E
+    A = T * k
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    z = dict(device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, **z)
+    gate = torch.empty((T, k), dtype=torch.float32, **z)
+    thr = torch.empty((T, 2), dtype=torch.float32, **z)
+    ws = workspace(cfg)
+    B.moe_gate(cfg, d["x"], d["Wg"], d["Wn"], d["noise"], d["bias"], idx, gate, thr, ws)
+    pos = torch.empty((T, k), dtype=torch.int32, **z)
+    keep = torch.empty((T, k), dtype=torch.uint8, **z)
+    count = torch.empty(E, dtype=torch.int32, **z)
+    offset = torch.empty(E + 1, dtype=torch.int32, **z)
+    xbuf = torch.empty((A, w.d), dtype=act, **z)
+    row_token = torch.full((A,), -1, dtype=torch.int32, **z)
+    row_gate = torch.empty(A, dtype=torch.float32, **z)
+    B.moe_dispatch(cfg, idx, gate, d["x"], pos, keep, count, offset, xbuf, row_token, row_gate, ws)
+    hbuf = torch.empty((A, w.d_ff), dtype=act, **z)
+    zbuf = torch.empty((A, w.d), dtype=torch.float32, **z)
+    B.moe_expert_ffn(cfg, xbuf, offset, row_gate, d["W1"], d["b1"], d["W2"], d["b2"], hbuf, zbuf, ws)
+    y = torch.empty((T, w.d), dtype=act, **z)
+    B.moe_combine(cfg, d["x"], zbuf, pos, keep, idx, offset, y, ws)
+    out3 = torch.zeros(3, dtype=torch.float32, **z)
+    imp = torch.zeros(E, dtype=torch.float32, **z)
+    load = torch.zeros(E, dtype=torch.float32, **z)
+    B.moe_aux_loss(cfg, ws, out3, imp, load)
+    st, det = B.moe_last_device_status(ws)
+    h = lambda t: t.cpu().numpy()
+    return dict(status=st, detail=det, idx=h(idx), gate=h(gate), thr=h(thr), pos=h(pos),
+                keep=h(keep), count=h(count), offset=h(offset), xbuf=xbuf, row_token=h(row_token),
+                row_gate=h(row_gate), hbuf=hbuf, zbuf=zbuf, y=y, out3=h(out3), importance=h(imp),
+                load=h(load))
+
+
+def oracle_gate(inp):
+    c, s, H, bad = oracle.router(inp["x"], inp["Wg"], inp["Wn"], inp["noise"], inp["bias"])
+    idx, gate, hk, hk1 = oracle.select(H, int(inp["k"]), int(inp["mode"]))
+    return dict(c=c, sigma=s, H=H, idx=idx, gate=gate, hk=hk, hk1=hk1, nonfinite=bad)
+
+
+def reconcile_selection(H, ref_idx, gpu_idx, tol=TIE_TOL):
+    """Tokens where the GPU's expert list differs from the oracle's. Each must
+    be explained by a near-tie: the GPU's list, read in the oracle's fp64 H,
+    must be non-increasing within tol and no unchosen expert may beat its last
+    entry by more than tol. Returns (idx to use downstream, list of tokens,
+    list of unexplained tokens)."""
+    diff = np.nonzero((ref_idx != gpu_idx).any(axis=1))[0]
+    used = ref_idx.copy()
+    ties, bad = [], []
+    E = H.shape[1]
+    for t in diff:
+        g = gpu_idx[t]
+        ok = bool(np.all((g >= 0) & (g < E))) and len(set(g.tolist())) == len(g)
+        if ok:
+            hv = H[t, g]
+            ok = bool(np.all(np.diff(hv) <= tol))
+            rest = np.setdiff1d(np.arange(E), g)
+            if ok and rest.size:
+                ok = bool(H[t, rest].max() <= hv.min() + tol)
+        (ties if ok else bad).append(int(t))
+        if ok:
+            used[t] = g
+    return used, ties, bad
+
+
+def check_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if dtype == "bf16":
+        lim = BF16_TOL * (1.0 + np.abs(ref))
+    else:
+        lim = F32_RTOL * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    worst = np.unravel_index(np.argmax(err - lim), err.shape) if err.size else None
+    assert np.all(err <= lim), (f"{what}: max err {err.max():.3e} at {worst}, "
+                                f"got {got[worst]:.6g} ref {ref[worst]:.6g}")
+    return float(err.max()) if err.size else 0.0
+
+
+def check_rel(got, ref, what, rtol=F32_RTOL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    lim = rtol * np.maximum(np.abs(ref), 1e-30)
+    assert np.all(err <= lim), f"{what}: got {got} ref {ref}"

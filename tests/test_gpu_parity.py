@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.
+
+Small cases span several tiles and a ragged tail and are compared element by
+element; the five measured workloads at full size (the configuration the
+benchmark times) are compared on every index, slot and balancing value and on
+sampled output rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_harness import (TIE_TOL, act_bits, act_to_f64, check_close, check_rel, oracle_gate,
+                         reconcile_selection, run_forward, run_stages, to_device)
+from sparsely_gated_mixture_gb300 import binding as B
+from sparsely_gated_mixture_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+W = wl.WORKLOADS
+
+
+def _compare(w, inp, res, ref_gate, tokens, report):
+    """Checks shared by the stage-wise and forward runs. Returns the
+    reconciled selection for reuse."""
+    T, k, E = w.T, w.k, w.E
+    used, ties, bad = reconcile_selection(ref_gate["H"], ref_gate["idx"], res["idx"])
+    assert not bad, f"expert choices differ beyond near-ties at tokens {bad[:10]}"
+    report["ties"] = ties
+    mode = int(inp["mode"])
+    g_ref = oracle.gates_given(ref_gate["H"], used, mode)
+    err = np.abs(res["gate"] - g_ref)
+    assert np.all(err <= 1e-4 * g_ref + 1e-6), f"gate max err {err.max():.3e}"
+    C = oracle.capacity(T, E, k, w.cf, w.min_cap)
+    pos, keep, count = oracle.slots(used, E, C)
+    assert np.array_equal(res["pos"], pos), "slot positions differ"
+    assert np.array_equal(res["keep"], keep), "drop masks differ"
+    # Output rows: the oracle's per-token loop over accepted experts.
+    y_ref, bad_y = oracle.layer_out(inp["x"], used, g_ref, keep, inp["W1"], inp["W2"], inp["b1"],
+                                    inp["b2"], tokens)
+    assert not bad_y
+    y = act_to_f64(res["y"][torch.as_tensor(tokens, device="cuda").long()])
+    report["y_max_err"] = check_close(y, y_ref, w.dtype, "layer output y")
+    # Tokens with every choice dropped come out bit-identical to their input.
+    drop = np.nonzero(~keep.astype(bool).any(axis=1))[0]
+    report["dropped_tokens"] = int(drop.size)
+    if drop.size:
+        dsel = torch.as_tensor(drop, device="cuda").long()
+        x_bits = inp["x"][drop].view(np.int16) if w.dtype == "bf16" else inp["x"][drop].view(np.int32)
+        assert np.array_equal(act_bits(res["y"][dsel]), x_bits), "dropped token changed"
+    return used, g_ref, pos, keep, count, C
+
+
+def _check_aux(w, inp, ref_gate, used, g_ref, out3, importance=None, load=None):
+    ax = oracle.aux(ref_gate["c"], ref_gate["sigma"], ref_gate["H"], used, g_ref, ref_gate["hk"],
+                    ref_gate["hk1"], inp["Wn"] is not None)
+    check_rel(out3, ax["out3"], "aux out3 [importance CV^2, load CV^2, switch aux]")
+    if importance is not None:
+        check_rel(importance, ax["importance"], "importance")
+        check_rel(load, ax["load"], "load")
+    return ax
+
+
+def check_stages(w, inp, tokens=None):
+    d = to_device(w, inp)
+    res = run_stages(w, d)
+    assert res["status"] == 0, (B.STATUS_NAMES[res["status"]], res["detail"])
+    ref_gate = oracle_gate(inp)
+    if tokens is None:
+        tokens = np.arange(w.T, dtype=np.int32)
+    report = {}
+    used, g_ref, pos, keep, count, C = _compare(w, inp, res, ref_gate, tokens, report)
+    # Gate thresholds, counts, offsets.
+    thr_ref = np.stack([ref_gate["hk"], ref_gate["hk1"]], axis=1)
+    fin = np.isfinite(thr_ref)
+    assert np.array_equal(np.isfinite(res["thr"]), fin)
+    assert np.all(np.abs(res["thr"][fin] - thr_ref[fin]) <= 1e-4 * (1 + np.abs(thr_ref[fin])))
+    assert np.array_equal(res["count"], count)
+    off = np.concatenate([[0], np.cumsum(np.minimum(count, C))]).astype(np.int32)
+    assert np.array_equal(res["offset"], off)
+    # Dispatch: every accepted (t, j) sits at row offset[e] + pos, in token order.
+    a = np.nonzero(keep.reshape(-1))[0]
+    t_of, j_of = a // w.k, a % w.k
+    rows = off[used.reshape(-1)[a]] + pos.reshape(-1)[a]
+    assert np.array_equal(np.sort(rows), np.arange(off[-1]))
+    assert np.array_equal(res["row_token"][rows], a.astype(np.int32))
+    assert np.array_equal(res["row_gate"][rows], res["gate"].reshape(-1)[a])
+    xb = act_bits(res["xbuf"][: off[-1]])
+    x_bits = inp["x"].view(np.int16) if w.dtype == "bf16" else inp["x"].view(np.int32)
+    assert np.array_equal(xb[rows], x_bits[t_of]), "gathered rows differ from their tokens"
+    _check_aux(w, inp, ref_gate, used, g_ref, res["out3"], res["importance"], res["load"])
+    return res, report
+
+
+def check_forward(w, inp, tokens, stages=None):
+    d = to_device(w, inp)
+    res = run_forward(w, d)
+    assert res["status"] == 0, (B.STATUS_NAMES[res["status"]], res["detail"])
+    ref_gate = oracle_gate(inp)
+    report = {}
+    used, g_ref, *_ = _compare(w, inp, res, ref_gate, tokens, report)
+    _check_aux(w, inp, ref_gate, used, g_ref, res["out3"])
+    if stages is not None:
+        assert torch.equal(res["y"], stages["y"]), "moe_forward and the stage calls differ"
+    return res, report
+
+
+SMALL = {
+    "toy": W["switch_top1_toy"],
+    "noisy_top4_e16": W["noisy_top4_e16"].with_(T=517),
+    "zipf_switch_e64": W["switch_top1_zipf_e64"].with_(T=700),
+    "top2_large_dims": W["top2_large_experts"].with_(T=40),
+    "top2_mid": W["top2_large_experts"].with_(T=333, d=512, d_ff=1024),
+    "e1024_top4": W["many_small_experts_e1024"].with_(T=900),
+    "ragged_bf16": wl.Workload("ragged_bf16", T=333, d=72, E=5, d_ff=200, k=3, cf=0.8,
+                               mode=wl.TOPK, dtype="bf16", noisy=True),
+    "ragged_f32": wl.Workload("ragged_f32", T=129, d=36, E=7, d_ff=50, k=2, cf=1.0,
+                              mode=wl.TOPK, dtype="f32", noisy=True),
+    "single_token": wl.Workload("single_token", T=1, d=64, E=4, d_ff=128, k=2, cf=1.0,
+                                mode=wl.TOPK, dtype="bf16", noisy=True),
+    "one_expert_dense": wl.Workload("one_expert_dense", T=130, d=64, E=1, d_ff=192, k=1, cf=1.0,
+                                    mode=wl.SWITCH, dtype="bf16", noisy=False),
+    "k_equals_E": wl.Workload("k_equals_E", T=257, d=128, E=4, d_ff=256, k=4, cf=1.0,
+                              mode=wl.TOPK, dtype="bf16", noisy=True),
+    "heavy_drop": wl.Workload("heavy_drop", T=300, d=128, E=8, d_ff=256, k=2, cf=0.05,
+                              mode=wl.TOPK, dtype="bf16", noisy=True),
+    "switch_f32_noisy": wl.Workload("switch_f32_noisy", T=200, d=24, E=6, d_ff=40, k=1, cf=1.1,
+                                    mode=wl.SWITCH, dtype="f32", noisy=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_parity(name):
+    w = SMALL[name]
+    inp = wl.generate(w, seed=11, biases=name not in ("toy",))
+    stages, rep = check_stages(w, inp)
+    check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
+
+
+def test_toy_zero_bias_exact_workload():
+    """The Switch toy exactly as specified: seed 0, zero biases, no noise."""
+    w = W["switch_top1_toy"]
+    inp = wl.generate(w, seed=0)
+    check_stages(w, inp)
+
+
+def _sample_tokens(T, n, seed):
+    rng = np.random.default_rng(seed)
+    s = set(rng.choice(T, size=min(n, T), replace=False).tolist()) | {0, T - 1}
+    return np.array(sorted(s), dtype=np.int32)
+
+
+@pytest.mark.parametrize("name", sorted(W))
+def test_full_size_sampled(name):
+    """Each measured workload at full size, launched as the benchmark launches
+    it: every index, slot and balancing value, and sampled output rows."""
+    w = W[name]
+    inp = wl.generate(w, seed=0)
+    tokens = _sample_tokens(w.T, 48 if w.d * w.d_ff > 10**7 else 256, seed=1)
+    res, rep = check_forward(w, inp, tokens)
+    print(name, "near-ties:", len(rep["ties"]), "dropped:", rep["dropped_tokens"],
+          "y max err:", rep["y_max_err"])
+
+
+def test_deterministic():
+    w = SMALL["noisy_top4_e16"]
+    inp = wl.generate(w, seed=5)
+    d = to_device(w, inp)
+    a = run_forward(w, d)
+    b = run_forward(w, d)
+    assert torch.equal(a["y"], b["y"])
+    assert np.array_equal(a["out3"], b["out3"])
+    assert np.array_equal(a["pos"], b["pos"])
+
+
+def test_nonfinite_input_reported():
+    w = SMALL["top2_mid"]
+    inp = wl.generate(w, seed=6)
+    inp["x"] = inp["x"].copy()
+    inp["x"][5, 3] = 0x7FC0  # bf16 NaN
+    d = to_device(w, inp)
+    res = run_forward(w, d)
+    assert res["status"] == 4  # MOE_ERR_NONFINITE
+
+
+def test_bad_arguments_rejected_before_launch():
+    w = SMALL["top2_mid"]
+    cfg = B.config_for(w)
+    bad = B.config_for(w.with_(k=9))  # k > E
+    with pytest.raises(B.MoEError) as e:
+        B.moe_workspace_size(bad)
+    assert e.value.status == 1
+    inp = wl.generate(w, seed=7)
+    d = to_device(w, inp)
+    ws = torch.empty(B.moe_workspace_size(cfg) + 256, dtype=torch.uint8, device="cuda")
+    y = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(B.MoEError) as e:  # misaligned workspace
+        B.moe_forward(cfg, d["x"], d["Wg"], d["Wn"], d["noise"], None, d["W1"], None, d["W2"],
+                      None, y, None, ws.data_ptr() + 8)
+    assert e.value.status == 1
+    with pytest.raises(B.MoEError):  # noise weights without noise
+        B.moe_forward(cfg, d["x"], d["Wg"], d["Wn"], None, None, d["W1"], None, d["W2"], None, y,
+                      None, ws)
