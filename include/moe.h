@@ -29,7 +29,9 @@
  *   (the Switch page raises on each), an index out of range, or a bounded wait
  *   that ran out -- are recorded in a status word inside `ws`;
  *   moe_last_device_status() reads it. moe_gate() and moe_forward() clear it
- *   when they start.
+ *   when they start, moe_last_device_status() after reading it; a caller whose
+ *   first call on a fresh workspace is another stage zero-fills the workspace
+ *   (or calls moe_last_device_status) first.
  * Determinism.  Indices, slots and drop masks are exact; no floating-point
  *   atomics are used, so two calls on the same inputs give identical bits.
  */

@@ -55,7 +55,7 @@ def act_bits(t: torch.Tensor) -> np.ndarray:
 
 
 def workspace(cfg) -> torch.Tensor:
-    return torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    return torch.zeros(B.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
 
 
 def run_forward(w, d, aux=True, keep_outputs=True):
