@@ -171,6 +171,34 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
                 float *gate, int32_t *pos, uint8_t *keep, void *ws, moe_stream_t stream);
 
 /*
+ * Allocation-free variant of moe_dispatch. The pages have no counterpart: it
+ * exists for callers that cannot call cudaMalloc where they route tokens --
+ * for example an inference engine's plugin whose enqueue callback must not
+ * allocate, or a runtime that fixes its device memory at start-up -- and so
+ * cannot provide the workspace moe_dispatch needs.
+ *
+ * Same arguments, computation and outputs as moe_dispatch, minus `ws`. Its
+ * scratch is a static device array of MOE_NOALLOC_SCRATCH_BYTES inside
+ * libmoe.so (every GPU that loads the library holds it until the process
+ * exits). The call needs 256 + 2 * ceil(T*k/512) * E * 4 + (E+1) * 4 bytes of
+ * it (each term rounded up to 256) and returns MOE_ERR_UNSUPPORTED, enqueuing
+ * nothing, if that is more. It allocates nothing and frees nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls share the one array: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller. Device-side index errors are not reported here;
+ * an expert index outside [0, E) yields pos = -1 and keep = 0 for that
+ * assignment.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx, const float *gate,
+                         const void *x, int32_t *pos, uint8_t *keep, int32_t *expert_count,
+                         int32_t *expert_offset, void *xbuf, int32_t *row_token,
+                         float *row_gate, moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the first device-side error recorded in `ws`
  * since it was last cleared (MOE_OK if none), writes its detail word (e.g. the
  * offending flat index) to *detail if non-NULL, and clears it.

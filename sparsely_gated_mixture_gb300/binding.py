@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
-           "moe_last_device_status")
+           "moe_last_device_status", "moe_dispatch_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,7 @@ def lib():
             L.moe_aux_loss.argtypes = [CP] + [P] * 5
             L.moe_forward.argtypes = [CP] + [P] * 17
             L.moe_last_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int64)]
+            L.moe_dispatch_noalloc.argtypes = [CP] + [P] * 11
             for name in EXPORTS[1:]:
                 getattr(L, name).restype = I
             _lib = L
@@ -158,6 +159,22 @@ def moe_forward(cfg, x, Wg, Wnoise, noise, logit_bias, W1, b1, W2, b2, y, aux_ou
                              _p(logit_bias), _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(aux_out3),
                              _p(expert_idx), _p(gate), _p(pos), _p(keep), _p(ws),
                              _stream(stream)), "moe_forward")
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def moe_dispatch_noalloc(cfg, expert_idx, gate, x, pos, keep, expert_count, expert_offset, xbuf,
+                         row_token, row_gate, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate
+    device memory; its scratch is the library's static 4 MiB device array."""
+    st = lib().moe_dispatch_noalloc(ctypes.byref(cfg), _p(expert_idx), _p(gate), _p(x), _p(pos),
+                                    _p(keep), _p(expert_count), _p(expert_offset), _p(xbuf),
+                                    _p(row_token), _p(row_gate), _stream(stream))
+    if st == 2:
+        raise MoEError(st, "moe_dispatch_noalloc: these sizes need more scratch than the "
+                           f"library's static {NOALLOC_SCRATCH_BYTES >> 20} MiB array")
+    _check(st, "moe_dispatch_noalloc")
 
 
 def moe_last_device_status(ws, stream=None):

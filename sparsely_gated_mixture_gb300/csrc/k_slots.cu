@@ -11,6 +11,8 @@
 // Kept assignments (pos < C) get row offset[e] + pos of the packed buffer.
 #include "moe_internal.cuh"
 
+#include <mutex>
+
 namespace moe {
 namespace {
 
@@ -175,3 +177,86 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
 }
 
 }  // namespace moe
+
+// ----------------------------------------------------------------------------- allocation-free dispatch
+// moe_dispatch_noalloc: the same slot assignment and gather as moe_dispatch,
+// for callers that cannot give the library a workspace because they may not
+// allocate device memory where they route tokens. Its scratch (the slot pass's
+// histograms and chunk bases, tile offsets and a status word) is this file's
+// own device array, which every GPU that loads the library keeps until exit.
+
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocBytes = MOE_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a stand-in, so the address is looked up once per
+// device, with that device current, and cached.
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+bool aligned16(const void *p) { return p && ((uintptr_t)p % 16) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx,
+                                    const float *gate, const void *x, int32_t *pos,
+                                    uint8_t *keep, int32_t *expert_count, int32_t *expert_offset,
+                                    void *xbuf, int32_t *row_token, float *row_gate,
+                                    moe_stream_t stream) {
+  using namespace moe;
+  int32_t C = 0;
+  int r = moe_capacity(cfg, &C);  // also validates cfg
+  if (r != MOE_OK) return r;
+  const void *ptrs[] = {expert_idx, gate, x, pos, keep, expert_count, expert_offset,
+                        xbuf, row_token, row_gate};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_ARG;
+  const size_t A = (size_t)cfg->T * cfg->k;
+  const size_t n_chunks = (A + kSlotChunk - 1) / kSlotChunk;
+  const size_t E = (size_t)cfg->E;
+  // Scratch layout: status | hist [n_chunks, E] | chunk bases [n_chunks, E] | tile offsets [E+1]
+  const size_t off_hist = 256;
+  const size_t off_base = off_hist + round256(n_chunks * E * 4);
+  const size_t off_tiles = off_base + round256(n_chunks * E * 4);
+  const size_t need = off_tiles + round256((E + 1) * 4);
+  if (need > kNoAllocBytes) return MOE_ERR_UNSUPPORTED;
+  void *scratch = nullptr;
+  r = noalloc_scratch(&scratch);
+  if (r != MOE_OK) return r;
+  char *base = static_cast<char *>(scratch);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = reinterpret_cast<DeviceStatus *>(base);
+  // Only the status word must start at zero; every other scratch word is
+  // written before it is read within one call.
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_slots(*cfg, C, expert_idx, gate, reinterpret_cast<int32_t *>(base + off_hist),
+                   reinterpret_cast<int32_t *>(base + off_base), expert_count, expert_offset,
+                   reinterpret_cast<int32_t *>(base + off_tiles), pos, keep, row_token, row_gate,
+                   (int)n_chunks, st, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_gather(*cfg, x, expert_offset, row_token, xbuf, st, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
