@@ -12,7 +12,10 @@ drawn in the fixed order x, W_g, W_noise, noise, W1, b1, W2, b2:
 * noise ~ N(0, 1) [T, E]           (the StandardNormal() draw of the noisy gate)
 * W1 ~ N(0, 1/d) [E, d, d_ff], W2 ~ N(0, 1/d_ff) [E, d_ff, d]  (N(0, 1/fan_in))
 * b1, b2 zero unless ``biases=True``, then N(0, 0.1^2)
-* the Zipf-skewed workload adds a router bias b_e = 1.5 * ln(1 / (e + 1)).
+* the Zipf-skewed workload adds a router bias b_e = 1.5 * ln(1 / (e + 1)) and
+  draws W_g from N(0, 25/d) (``router_scale`` 5): that logit scale is what
+  makes the stated bias send 15-25% of the tokens past capacity (about 23%);
+  with N(0, 1/d) it would send about 88%.
 
 bf16 workloads round x, W1, W2, b1, b2 from fp32 to bf16 with
 round-to-nearest-even and keep the bit patterns as uint16; both sides of every
@@ -43,6 +46,7 @@ class Workload:
     noisy: bool
     zipf_bias: bool = False
     min_cap: int = 1
+    router_scale: float = 1.0  # W_g ~ N(0, router_scale^2 / d)
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -71,7 +75,7 @@ WORKLOADS = {
         Workload("noisy_top4_e16", T=4096, d=512, E=16, d_ff=1024, k=4, cf=2.0, mode=TOPK,
                  dtype="bf16", noisy=True),
         Workload("switch_top1_zipf_e64", T=16384, d=768, E=64, d_ff=3072, k=1, cf=1.25,
-                 mode=SWITCH, dtype="bf16", noisy=False, zipf_bias=True),
+                 mode=SWITCH, dtype="bf16", noisy=False, zipf_bias=True, router_scale=5.0),
         Workload("top2_large_experts", T=8192, d=4096, E=8, d_ff=14336, k=2, cf=1.25,
                  mode=TOPK, dtype="bf16", noisy=True),
         Workload("many_small_experts_e1024", T=32768, d=512, E=1024, d_ff=1024, k=4, cf=1.5,
@@ -113,7 +117,7 @@ def generate(w: Workload, seed: int = 0, biases: bool = False) -> dict:
     rng = np.random.Generator(np.random.PCG64(seed))
     bf = w.dtype == "bf16"
     x = _normal(rng, (w.T, w.d), 1.0, bf)
-    Wg = _normal(rng, (w.d, w.E), 1.0 / math.sqrt(w.d), False)
+    Wg = _normal(rng, (w.d, w.E), w.router_scale / math.sqrt(w.d), False)
     Wn = noise = None
     if w.noisy:
         Wn = _normal(rng, (w.d, w.E), 1.0 / math.sqrt(w.d), False)
