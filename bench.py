@@ -414,11 +414,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T (smaller cases for profiler captures)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller cases for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = wl.WORKLOADS[args.workload]
     if args.tokens:
         w = w.with_(T=args.tokens)
+    if args.experts:
+        w = w.with_(E=args.experts)
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

@@ -136,6 +136,187 @@ cudaError_t run_router(const moe_config &cfg, const void *x, const float *Wg, co
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------------------- router, vector path
+// The same arithmetic as k_router, laid out for streaming: each warp owns TPW
+// tokens over the whole K range and its lanes split K (lane l takes
+// k = l, l+32, ... of each 256-wide chunk); x rows (16-byte cp.async) and the
+// W chunk (cp.async) are double-buffered in shared memory, so loads of chunk
+// c+1 overlap the FMAs of chunk c. The lanes' partial sums are combined by a
+// fixed xor-butterfly, so results are run-to-run identical.
+constexpr int kRvWarps = 8;
+constexpr int kRvKC = 256;
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename XT, int BE, bool NOISY, int TPW>
+__global__ void __launch_bounds__(kRvWarps * 32)
+k_router_vec(int T, int d, int E, int w16, const XT *__restrict__ x, const float *__restrict__ Wg,
+             const float *__restrict__ Wn, const float *__restrict__ noise,
+             const float *__restrict__ bias, float *__restrict__ c_out, float *__restrict__ s_out,
+             float *__restrict__ H_out, DeviceStatus *st) {
+  constexpr int NC = NOISY ? 2 * BE : BE;  // columns: BE clean, then BE noise
+  constexpr int WP = NC + 4;               // padded W row: conflict-free float4 reads
+  constexpr int VEC = 16 / (int)sizeof(XT);
+  constexpr int TOK = kRvWarps * TPW;
+  extern __shared__ float4 smem4[];
+  float *Ws = reinterpret_cast<float *>(smem4);                  // [2][KC][WP]
+  XT *Xs = reinterpret_cast<XT *>(Ws + 2 * kRvKC * WP);          // [2][warps][TPW][KC]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TOK + warp * TPW;
+  const int e0 = blockIdx.y * BE;
+  const int nchunks = (d + kRvKC - 1) / kRvKC;
+
+  auto stage = [&](int chunk, int buf) {
+    const int k0 = chunk * kRvKC;
+    float *wdst = Ws + (size_t)buf * kRvKC * WP;
+    if (w16) {  // E % 4 == 0: 16-byte pieces of each W row segment
+      constexpr int NV = NC / 4;
+      for (int i = threadIdx.x; i < kRvKC * NV; i += blockDim.x) {
+        const int kk = i / NV, cv = (i % NV) * 4;
+        const int k = k0 + kk, col = cv < BE ? cv : cv - BE, e = e0 + col;
+        const float *src = cv < BE ? Wg : Wn;
+        const bool ok = k < d && e < E;
+        cp_async16(wdst + kk * WP + cv, ok ? src + (size_t)k * E + e : src, ok ? 16 : 0);
+      }
+    } else {
+      for (int i = threadIdx.x; i < kRvKC * NC; i += blockDim.x) {
+        const int kk = i / NC, cv = i % NC;
+        const int k = k0 + kk, col = cv < BE ? cv : cv - BE, e = e0 + col;
+        const float *src = cv < BE ? Wg : Wn;
+        const bool ok = k < d && e < E;
+        cp_async4(wdst + kk * WP + cv, ok ? src + (size_t)k * E + e : src, ok ? 4 : 0);
+      }
+    }
+    XT *xdst = Xs + ((size_t)(buf * kRvWarps + warp) * TPW) * kRvKC;
+    constexpr int NVX = TPW * kRvKC / VEC;
+    for (int v = lane; v < NVX; v += 32) {
+      const int tl = v / (kRvKC / VEC), kv = (v % (kRvKC / VEC)) * VEC;
+      const int t = t0 + tl, k = k0 + kv;
+      const bool ok = t < T && k < d;
+      cp_async16(xdst + tl * kRvKC + kv, ok ? x + (size_t)t * d + k : x, ok ? 16 : 0);
+    }
+    cp_async_commit();
+  };
+
+  float acc[TPW][NC];
+#pragma unroll
+  for (int tl = 0; tl < TPW; ++tl)
+#pragma unroll
+    for (int j = 0; j < NC; ++j) acc[tl][j] = 0.f;
+
+  stage(0, 0);
+  if (nchunks > 1) stage(1, 1);
+  else cp_async_commit();
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int buf = ch & 1;
+    cp_async_wait<1>();
+    __syncthreads();
+    const float *w = Ws + (size_t)buf * kRvKC * WP;
+    const XT *xw = Xs + ((size_t)(buf * kRvWarps + warp) * TPW) * kRvKC;
+#pragma unroll 2
+    for (int j = 0; j < kRvKC / 32; ++j) {
+      const int kk = lane + 32 * j;
+      float xv[TPW];
+#pragma unroll
+      for (int tl = 0; tl < TPW; ++tl) xv[tl] = to_f(xw[tl * kRvKC + kk]);
+      const float4 *wr = reinterpret_cast<const float4 *>(w + kk * WP);
+#pragma unroll
+      for (int c4 = 0; c4 < NC / 4; ++c4) {
+        const float4 wv = wr[c4];
+#pragma unroll
+        for (int tl = 0; tl < TPW; ++tl) {
+          acc[tl][4 * c4 + 0] = fmaf(xv[tl], wv.x, acc[tl][4 * c4 + 0]);
+          acc[tl][4 * c4 + 1] = fmaf(xv[tl], wv.y, acc[tl][4 * c4 + 1]);
+          acc[tl][4 * c4 + 2] = fmaf(xv[tl], wv.z, acc[tl][4 * c4 + 2]);
+          acc[tl][4 * c4 + 3] = fmaf(xv[tl], wv.w, acc[tl][4 * c4 + 3]);
+        }
+      }
+    }
+    __syncthreads();
+    if (ch + 2 < nchunks) stage(ch + 2, buf);
+    else cp_async_commit();  // keep one group per iteration
+  }
+  cp_async_wait<0>();
+  // Fixed butterfly: every lane ends with the full sums.
+#pragma unroll
+  for (int tl = 0; tl < TPW; ++tl)
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int o = 16; o; o >>= 1) acc[tl][j] += __shfl_xor_sync(0xffffffffu, acc[tl][j], o);
+#pragma unroll
+  for (int tl = 0; tl < TPW; ++tl) {
+#pragma unroll
+    for (int el = 0; el < BE; ++el) {
+      if (((tl * BE + el) & 31) != lane) continue;
+      const int t = t0 + tl, e = e0 + el;
+      if (t >= T || e >= E) continue;
+      float cv = acc[tl][el];
+      if (bias) cv += bias[e];
+      float sg = 0.f, h = cv;
+      if (NOISY) {
+        sg = softplus_f(acc[tl][BE + el]);
+        h = fmaf(noise[(size_t)t * E + e], sg, cv);
+      }
+      const size_t o = (size_t)t * E + e;
+      c_out[o] = cv;
+      s_out[o] = sg;
+      H_out[o] = h;
+      if (!isfinite(h)) record_error(st, MOE_ERR_NONFINITE, (long long)o);
+    }
+  }
+}
+
+template <typename XT, int BE, bool NOISY, int TPW>
+cudaError_t run_router_vec(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
+                           const float *noise, const float *bias, float *c, float *s, float *H,
+                           DeviceStatus *st, cudaStream_t stream) {
+  constexpr int NC = NOISY ? 2 * BE : BE;
+  const size_t smem = (size_t)2 * kRvKC * (NC + 4) * 4 +
+                      (size_t)2 * kRvWarps * TPW * kRvKC * sizeof(XT);
+  auto kern = k_router_vec<XT, BE, NOISY, TPW>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((cfg.T + kRvWarps * TPW - 1) / (kRvWarps * TPW), (cfg.E + BE - 1) / BE);
+  kern<<<grid, kRvWarps * 32, smem, stream>>>(cfg.T, cfg.d, cfg.E, cfg.E % 4 == 0 ? 1 : 0,
+                                               static_cast<const XT *>(x), Wg, Wn, noise, bias, c,
+                                               s, H, st);
+  return cudaGetLastError();
+}
+
+template <typename XT, bool NOISY>
+cudaError_t router_vec_dispatch(const moe_config &cfg, const void *x, const float *Wg,
+                                const float *Wn, const float *noise, const float *bias, float *c,
+                                float *s, float *H, DeviceStatus *st, cudaStream_t stream) {
+  if (cfg.E <= 8)
+    return run_router_vec<XT, 8, NOISY, 4>(cfg, x, Wg, Wn, noise, bias, c, s, H, st, stream);
+  if (cfg.E <= 16 || NOISY)
+    return run_router_vec<XT, 16, NOISY, NOISY ? 2 : 4>(cfg, x, Wg, Wn, noise, bias, c, s, H, st,
+                                                          stream);
+  return run_router_vec<XT, 32, NOISY, 2>(cfg, x, Wg, Wn, noise, bias, c, s, H, st, stream);
+}
+
 // ----------------------------------------------------------------------------- selection
 // One warp per token; expert e lives in lane e % 32, slot e / 32.
 template <int VPL>
@@ -215,55 +396,84 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
 }
 
 // ----------------------------------------------------------------------------- balancing partials
-// Thread per expert; tokens of one block walked in order. partials layout:
-// [block][4][E]: importance, load, first-choice count, sum of Softmax(H).
-constexpr int kAuxThreads = 128;
+// Block (token block b, expert chunk): warp w walks tokens t0+w, t0+w+8, ...
+// of the block in order; lane l owns experts chunk0 + l + 32 i. The eight
+// warps' sums are added in warp order, so every partial is run-to-run
+// identical. partials layout: [block][4][E] = importance, load, first-choice
+// count, sum of Softmax(H).
+constexpr int kAuxWarps = 8;
 
-__global__ void __launch_bounds__(kAuxThreads)
-k_aux_partials(int T, int E, int k, int noisy, const float *__restrict__ c,
+template <int VPL>
+__global__ void __launch_bounds__(kAuxWarps * 32)
+k_aux_partials(int T, int E, int k, int tb, int noisy, const float *__restrict__ c,
                const float *__restrict__ sg, const float *__restrict__ H,
                const float *__restrict__ rowstat, const int32_t *__restrict__ idx,
                const float *__restrict__ gate, const float *__restrict__ thr,
                float *__restrict__ partials) {
-  const int e = blockIdx.x * kAuxThreads + threadIdx.x;
-  const int b = blockIdx.y;
-  if (e >= E) return;
-  const int tb = b * kAuxTokBlock, te = min(T, tb + kAuxTokBlock);
-  float imp = 0.f, ld = 0.f, first = 0.f, pb = 0.f;
-  for (int t = tb; t < te; ++t) {
-    int chosen = -1;
-    for (int j = 0; j < k; ++j)
-      if (idx[(size_t)t * k + j] == e) chosen = j;
-    if (chosen >= 0) imp += gate[(size_t)t * k + chosen];
-    if (idx[(size_t)t * k] == e) first += 1.f;
-    size_t o = (size_t)t * E + e;
-    float p;
-    if (k == E) {
-      p = 1.f;
-    } else {
-      float s = noisy ? sg[o] : 0.f;
-      if (s == 0.f) {
-        p = chosen >= 0 ? 1.f : 0.f;
+  constexpr int CH = 32 * VPL;
+  __shared__ float red[kAuxWarps][4][CH];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x, e0 = blockIdx.y * CH;
+  const int t0 = b * tb, t1 = min(T, t0 + tb);
+  float acc[4][VPL];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[q][i] = 0.f;
+  for (int t = t0 + warp; t < t1; t += kAuxWarps) {
+    const float th0 = thr[2 * (size_t)t], th1 = thr[2 * (size_t)t + 1];
+    const float mx = rowstat[2 * (size_t)t], se = rowstat[2 * (size_t)t + 1];
+    const int first = idx[(size_t)t * k];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = e0 + lane + 32 * i;
+      if (e >= E) continue;
+      int chosen = -1;
+      for (int j = 0; j < k; ++j)
+        if (idx[(size_t)t * k + j] == e) chosen = j;
+      const size_t o = (size_t)t * E + e;
+      if (chosen >= 0) acc[0][i] += gate[(size_t)t * k + chosen];
+      float p;
+      if (k == E) {
+        p = 1.f;
       } else {
-        float th = chosen >= 0 ? thr[2 * (size_t)t + 1] : thr[2 * (size_t)t];
-        float u = (c[o] - th) / s;
-        p = 0.5f * erfcf(-u * 0.70710678118654752f);
+        const float s = noisy ? sg[o] : 0.f;
+        if (s == 0.f) {
+          p = chosen >= 0 ? 1.f : 0.f;
+        } else {
+          const float u = (c[o] - (chosen >= 0 ? th1 : th0)) / s;
+          p = 0.5f * erfcf(-u * 0.70710678118654752f);
+        }
       }
+      acc[1][i] += p;
+      if (first == e) acc[2][i] += 1.f;
+      acc[3][i] += expf(H[o] - mx) / se;
     }
-    ld += p;
-    pb += expf(H[o] - rowstat[2 * (size_t)t]) / rowstat[2 * (size_t)t + 1];
   }
-  float *out = partials + (size_t)b * 4 * E;
-  out[e] = imp;
-  out[E + e] = ld;
-  out[2 * E + e] = first;
-  out[3 * E + e] = pb;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) red[warp][q][lane + 32 * i] = acc[q][i];
+  __syncthreads();
+  for (int v = threadIdx.x; v < 4 * CH; v += blockDim.x) {
+    const int q = v / CH, el = v % CH, e = e0 + el;
+    if (e >= E) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAuxWarps; ++w) sum += red[w][q][el];
+    partials[((size_t)b * 4 + q) * E + e] = sum;
+  }
 }
 
+// Finalize, one launch. Each warp sums one expert's partials over the token
+// blocks (lane l takes blocks l, l+32, ... in order, then a fixed xor
+// butterfly; fp64), writing aux_vec [4][E] = importance, load, f, Pbar. The
+// block that finishes last (a ticket in the status word, reset by that block)
+// then computes CV^2 of importance and load (population variance) and the
+// Switch loss 0.01 * E * sum(f * Pbar) in a fixed order.
 constexpr int kFinThreads = 256;
 
 __device__ double block_sum_fixed(double v, double *sh) {
-  // Fixed-shape tree: identical order on every run.
   sh[threadIdx.x] = v;
   __syncthreads();
   for (int s = kFinThreads / 2; s > 0; s >>= 1) {
@@ -275,49 +485,58 @@ __device__ double block_sum_fixed(double v, double *sh) {
   return r;
 }
 
-// One block: sums the partials over token blocks in order (fp64), then CV^2 and
-// the Switch loss. aux_vec: [4][E] fp32 copies (importance, load, f, Pbar).
 __global__ void __launch_bounds__(kFinThreads)
-k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float *__restrict__ out3,
-               float *__restrict__ importance, float *__restrict__ load,
-               float *__restrict__ aux_vec) {
+k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials,
+               double *__restrict__ aux_vec, float *__restrict__ importance,
+               float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
   __shared__ double sh[kFinThreads];
-  double s_imp = 0, s_ld = 0, s_fp = 0;
-  for (int e = threadIdx.x; e < E; e += kFinThreads) {
-    double a = 0, l = 0, f = 0, p = 0;
-    for (int b = 0; b < nb; ++b) {
+  __shared__ int last;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
+  if (e < E) {
+    double v[4] = {0, 0, 0, 0};
+    for (int b = lane; b < nb; b += 32) {
       const float *q = partials + (size_t)b * 4 * E;
-      a += q[e];
-      l += q[E + e];
-      f += q[2 * E + e];
-      p += q[3 * E + e];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] += q[(size_t)i * E + e];
     }
-    f /= T;
-    p /= T;
-    aux_vec[e] = (float)a;
-    aux_vec[E + e] = (float)l;
-    aux_vec[2 * E + e] = (float)f;
-    aux_vec[3 * E + e] = (float)p;
-    if (importance) importance[e] = (float)a;
-    if (load) load[e] = (float)l;
-    s_imp += a;
-    s_ld += l;
-    s_fp += f * p;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    if (lane == 0) {
+      aux_vec[e] = v[0];
+      aux_vec[E + e] = v[1];
+      aux_vec[2 * E + e] = v[2] / T;
+      aux_vec[3 * E + e] = v[3] / T;
+      if (importance) importance[e] = (float)v[0];
+      if (load) load[e] = (float)v[1];
+    }
   }
-  double m_imp = block_sum_fixed(s_imp, sh) / E;
-  double m_ld = block_sum_fixed(s_ld, sh) / E;
-  double fp = block_sum_fixed(s_fp, sh);
-  // Second pass for the variances, re-summing the same partials in the same order.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned ticket = atomicAdd(reinterpret_cast<unsigned *>(&st->aux_ticket), 1u);
+    last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const volatile double *av = aux_vec;
+  double s_imp = 0, s_ld = 0, s_fp = 0;
+  for (int i = threadIdx.x; i < E; i += kFinThreads) {
+    s_imp += av[i];
+    s_ld += av[E + i];
+    s_fp += av[2 * E + i] * av[3 * E + i];
+  }
+  const double m_imp = block_sum_fixed(s_imp, sh) / E;
+  const double m_ld = block_sum_fixed(s_ld, sh) / E;
+  const double fp = block_sum_fixed(s_fp, sh);
   double v_imp = 0, v_ld = 0;
-  for (int e = threadIdx.x; e < E; e += kFinThreads) {
-    double a = 0, l = 0;
-    for (int b = 0; b < nb; ++b) {
-      const float *q = partials + (size_t)b * 4 * E;
-      a += q[e];
-      l += q[E + e];
-    }
-    v_imp += (a - m_imp) * (a - m_imp);
-    v_ld += (l - m_ld) * (l - m_ld);
+  for (int i = threadIdx.x; i < E; i += kFinThreads) {
+    const double a = av[i] - m_imp, l = av[E + i] - m_ld;
+    v_imp += a * a;
+    v_ld += l * l;
   }
   v_imp = block_sum_fixed(v_imp, sh) / E;
   v_ld = block_sum_fixed(v_ld, sh) / E;
@@ -325,6 +544,7 @@ k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float *
     out3[0] = (float)(v_imp / (m_imp * m_imp));
     out3[1] = (float)(v_ld / (m_ld * m_ld));
     out3[2] = (float)(0.01 * E * fp);
+    st->aux_ticket = 0;  // ready for the next call
   }
 }
 
@@ -334,6 +554,20 @@ cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg,
                           const float *noise, const float *bias, float *c, float *sigma, float *H,
                           DeviceStatus *st, cudaStream_t s) {
   const bool noisy = Wn != nullptr;
+  // Vector path: whole 16-byte pieces of every x row, and a small expert count
+  // (beyond it the per-block W traffic of this layout grows with E).
+  const bool vec = cfg.E <= 64 &&
+                   (cfg.act_dtype == MOE_BF16 ? cfg.d % 8 == 0 : cfg.d % 4 == 0);
+  if (vec) {
+    if (cfg.act_dtype == MOE_BF16)
+      return noisy ? router_vec_dispatch<__nv_bfloat16, true>(cfg, x, Wg, Wn, noise, bias, c,
+                                                              sigma, H, st, s)
+                   : router_vec_dispatch<__nv_bfloat16, false>(cfg, x, Wg, Wn, noise, bias, c,
+                                                               sigma, H, st, s);
+    return noisy ? router_vec_dispatch<float, true>(cfg, x, Wg, Wn, noise, bias, c, sigma, H, st, s)
+                 : router_vec_dispatch<float, false>(cfg, x, Wg, Wn, noise, bias, c, sigma, H, st,
+                                                     s);
+  }
   if (cfg.E <= 8)
     return noisy ? run_router<8, true>(cfg, x, Wg, Wn, noise, bias, c, sigma, H, st, s)
                  : run_router<8, false>(cfg, x, Wg, Wn, noise, bias, c, sigma, H, st, s);
@@ -363,21 +597,32 @@ cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, f
   return cudaGetLastError();
 }
 
+int aux_token_block(int E) { return E <= 64 ? 64 : (E <= 256 ? 256 : 512); }
+
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
                                 const float *sigma, const float *H, const float *rowstat,
                                 const int32_t *idx, const float *gate, const float *thr,
                                 float *partials, int n_blocks, cudaStream_t s) {
-  dim3 grid((cfg.E + kAuxThreads - 1) / kAuxThreads, n_blocks);
-  k_aux_partials<<<grid, kAuxThreads, 0, s>>>(cfg.T, cfg.E, cfg.k, noisy ? 1 : 0, c, sigma, H,
-                                              rowstat, idx, gate, thr, partials);
+  const int tb = aux_token_block(cfg.E);
+  const int vpl = cfg.E <= 32 ? 1 : (cfg.E <= 64 ? 2 : (cfg.E <= 128 ? 4 : 8));
+  dim3 grid(n_blocks, (cfg.E + 32 * vpl - 1) / (32 * vpl));
+#define MOE_AUXP(V)                                                                           \
+  k_aux_partials<V><<<grid, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, tb, noisy ? 1 : 0, c, \
+                                                     sigma, H, rowstat, idx, gate, thr, partials)
+  if (vpl == 1) MOE_AUXP(1);
+  else if (vpl == 2) MOE_AUXP(2);
+  else if (vpl == 4) MOE_AUXP(4);
+  else MOE_AUXP(8);
+#undef MOE_AUXP
   return cudaGetLastError();
 }
 
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
-                                float *out3, float *importance, float *load, float *aux_vec,
-                                cudaStream_t s) {
-  k_aux_finalize<<<1, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials, out3, importance,
-                                           load, aux_vec);
+                                float *out3, float *importance, float *load, double *aux_vec,
+                                DeviceStatus *st, cudaStream_t s) {
+  const int per_block = kFinThreads / 32;
+  k_aux_finalize<<<(cfg.E + per_block - 1) / per_block, kFinThreads, 0, s>>>(
+      cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
   return cudaGetLastError();
 }
 

@@ -111,6 +111,64 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
   if (bad) record_error(st, MOE_ERR_NONFINITE, (long long)t);
 }
 
+// Combine for bf16 rows with d % 8 == 0: each lane handles 8 consecutive
+// elements per step (one 16-byte load of x and of y, two of each kept Z row),
+// two steps in flight.
+__global__ void __launch_bounds__(kRowWarps * 32)
+k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ x,
+                 const float *__restrict__ zbuf, const int32_t *__restrict__ pos,
+                 const uint8_t *__restrict__ keep, const int32_t *__restrict__ idx,
+                 const int32_t *__restrict__ offset, __nv_bfloat16 *__restrict__ y,
+                 DeviceStatus *st) {
+  constexpr int kMaxK = 16;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= Tn) return;
+  int rows[kMaxK];
+  int nr = 0;
+  for (int j = 0; j < k; ++j) {
+    const size_t a = (size_t)t * k + j;
+    if (!keep[a]) continue;
+    const int e = idx[a];
+    const int r = (e >= 0 && e < E) ? offset[e] + pos[a] : -1;
+    if (r < 0 || r >= offset[e + 1]) {
+      if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)a);
+      continue;
+    }
+    rows[nr++] = r;
+  }
+  const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+  uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)t * d);
+  const int nv = d / 8;
+  bool bad = false;
+  for (int v = lane; v < nv; v += 32) {
+    const uint4 xv = xr[v];
+    const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = __bfloat1622float2(xb[q]);
+      acc[2 * q] = f.x;
+      acc[2 * q + 1] = f.y;
+    }
+    for (int i = 0; i < nr; ++i) {
+      const float4 *zr = reinterpret_cast<const float4 *>(zbuf + (size_t)rows[i] * d) + 2 * v;
+      const float4 z0 = zr[0], z1 = zr[1];
+      acc[0] += z0.x; acc[1] += z0.y; acc[2] += z0.z; acc[3] += z0.w;
+      acc[4] += z1.x; acc[5] += z1.y; acc[6] += z1.z; acc[7] += z1.w;
+    }
+    uint4 out;
+    __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      bad |= !isfinite(acc[2 * q]) || !isfinite(acc[2 * q + 1]);
+      ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    }
+    yr[v] = out;
+  }
+  if (bad) record_error(st, MOE_ERR_NONFINITE, (long long)t);
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,
@@ -142,7 +200,10 @@ cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zb
   if (cfg.act_dtype == MOE_BF16) {
     auto xp = (const __nv_bfloat16 *)x;
     auto yp = (__nv_bfloat16 *)y;
-    if (v4)
+    if (cfg.d % 8 == 0)
+      k_combine_bf16x8<<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos,
+                                                       keep, idx, offset, yp, st);
+    else if (v4)
       k_combine<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, s>>>(
           cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
     else

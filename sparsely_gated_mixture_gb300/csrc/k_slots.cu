@@ -105,47 +105,72 @@ k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
   }
 }
 
+// One block per chunk. Warp w ranks its 64 assignments in order (two rounds
+// of 32: __match_any_sync groups equal experts, a popcount gives the rank,
+// a per-warp counter carries it); an exclusive scan over the warps' counts
+// then gives each warp its base, in warp order.
+constexpr int kRankPerWarp = kSlotChunk / kRankWarps;
+
 __global__ void __launch_bounds__(kRankWarps * 32)
-k_slot_rank(int A, int E, int C, int n_chunks, const int32_t *__restrict__ idx,
-            const float *__restrict__ gate, const int32_t *__restrict__ hist_base,
-            const int32_t *__restrict__ offset, int32_t *__restrict__ pos,
-            uint8_t *__restrict__ keep, int32_t *__restrict__ row_token,
+k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *__restrict__ gate,
+            const int32_t *__restrict__ hist_base, const int32_t *__restrict__ offset,
+            int32_t *__restrict__ pos, uint8_t *__restrict__ keep, int32_t *__restrict__ row_token,
             float *__restrict__ row_gate) {
   extern __shared__ int32_t sh_cnt[];  // [kRankWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int chunk = blockIdx.x * kRankWarps + warp;
-  if (chunk >= n_chunks) return;  // whole warps leave together; no block barrier below
+  const int chunk = blockIdx.x;
+  for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) sh_cnt[i] = 0;
+  __syncthreads();
   int32_t *cnt = sh_cnt + (size_t)warp * E;
-  for (int e = lane; e < E; e += 32) cnt[e] = 0;
-  __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
-  const int a0 = chunk * kSlotChunk;
-  const int a1 = min(A, a0 + kSlotChunk);
-  for (int base = a0; base < a1; base += 32) {
-    int a = base + lane;
+  const int a0 = chunk * kSlotChunk + warp * kRankPerWarp;
+  constexpr int R = kRankPerWarp / 32;
+  int ee[R], rk[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int a = a0 + 32 * r + lane;
     int e = -1;
-    if (a < a1) {
+    if (a < A) {
       e = idx[a];
       if (e < 0 || e >= E) e = -1;  // counted as a bounds error by k_slot_hist
     }
-    unsigned peers = __match_any_sync(0xffffffffu, e);
-    int before = e >= 0 ? cnt[e] : 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int before = e >= 0 ? cnt[e] : 0;
     __syncwarp();
     if (e >= 0 && (peers & lt) == 0) cnt[e] = before + __popc(peers);  // lowest peer updates
     __syncwarp();
-    if (e >= 0) {
-      int p = hist_base[(size_t)chunk * E + e] + before + __popc(peers & lt);
-      pos[a] = p;
-      bool kp = p < C;
-      keep[a] = kp ? 1 : 0;
-      if (kp) {
-        int r = offset[e] + p;
-        row_token[r] = a;
-        row_gate[r] = gate[a];
-      }
-    } else if (a < a1) {
+    ee[r] = e;
+    rk[r] = before + __popc(peers & lt);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kRankWarps; ++w) {
+      const int v = sh_cnt[w * E + e];
+      sh_cnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int a = a0 + 32 * r + lane;
+    if (a >= A) continue;
+    const int e = ee[r];
+    if (e < 0) {
       pos[a] = -1;
       keep[a] = 0;
+      continue;
+    }
+    const int p = hist_base[(size_t)chunk * E + e] + cnt[e] + rk[r];
+    pos[a] = p;
+    const bool kp = p < C;
+    keep[a] = kp ? 1 : 0;
+    if (kp) {
+      const int row = offset[e] + p;
+      row_token[row] = a;
+      row_gate[row] = gate[a];
     }
   }
 }
@@ -170,9 +195,8 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
                                (int)smem);
     if (err != cudaSuccess) return err;
   }
-  int blocks = (n_chunks + kRankWarps - 1) / kRankWarps;
-  k_slot_rank<<<blocks, kRankWarps * 32, smem, s>>>(A, cfg.E, C, n_chunks, idx, gate, chunk_base,
-                                                    offset, pos, keep, row_token, row_gate);
+  k_slot_rank<<<n_chunks, kRankWarps * 32, smem, s>>>(A, cfg.E, C, idx, gate, chunk_base, offset,
+                                                      pos, keep, row_token, row_gate);
   return cudaGetLastError();
 }
 

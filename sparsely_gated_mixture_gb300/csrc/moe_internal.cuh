@@ -12,7 +12,6 @@ namespace moe {
 
 // ----------------------------------------------------------------------------- tiling constants
 constexpr int kSlotChunk = 512;     // assignments ranked per warp in the slot pass
-constexpr int kAuxTokBlock = 256;   // tokens per partial-sum block of the balancing sums
 constexpr int kTcBM = 128;          // rows per tile of the tensor-core expert GEMM
 constexpr int kSimtBM = 64;         // rows per tile of the CUDA-core expert GEMM
 
@@ -20,7 +19,7 @@ constexpr int kSimtBM = 64;         // rows per tile of the CUDA-core expert GEM
 // Lives at offset 0 of the workspace. The first error wins; later ones are dropped.
 struct DeviceStatus {
   int32_t code;
-  int32_t pad;
+  uint32_t aux_ticket;  // blocks of the balancing finalize that are done (reset by the last)
   long long detail;
 };
 
@@ -67,8 +66,9 @@ cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *
                                 const int32_t *idx, const float *gate, const float *thr,
                                 float *partials, int n_blocks, cudaStream_t s);
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
-                                float *out3, float *importance, float *load, float *aux_vec,
-                                cudaStream_t s);
+                                float *out3, float *importance, float *load, double *aux_vec,
+                                DeviceStatus *st, cudaStream_t s);
+int aux_token_block(int E);  // tokens per partial-sum block of the balancing sums
 
 // k_slots.cu: capacity, token-order slots, dispatch maps.
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
