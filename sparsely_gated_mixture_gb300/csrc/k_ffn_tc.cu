@@ -22,9 +22,9 @@
 // past the limit the CTA records MOE_ERR_TIMEOUT, stops issuing, waits
 // (bounded) for its copies and MMAs in flight, frees TMEM and returns.
 #include "moe_internal.cuh"
+#include "tc_ptx.cuh"
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include <stdlib.h>
 
 namespace moe {
 namespace {
@@ -38,7 +38,6 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BK * BN * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;     // two accumulators
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 struct Params {
   int K, N, E, n_blocks;
@@ -48,92 +47,6 @@ struct Params {
   void *out;              // layer 1: bf16 [rows, N]; layer 2: fp32 [rows, N]
   DeviceStatus *st;
 };
-
-// ----------------------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait. Returns false if this CTA is aborting (limit reached here or
-// elsewhere in the CTA); the first thread to run out records the error.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          DeviceStatus *st, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        record_error(st, MOE_ERR_TIMEOUT, (long long)where);
-        return false;
-      }
-    }
-  }
-}
-
-// Wait used while draining after an abort: bounded, no abort check.
-__device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), version 1.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
 // B MN-major, M = 128, N = 256.
@@ -147,27 +60,6 @@ __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, ui
       "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // ----------------------------------------------------------------------------- tile map
 struct TileMap {
   int *start;  // shared [E+1]: first tile of each expert
@@ -404,6 +296,301 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
   }
 }
 
+// ----------------------------------------------------------------------------- CTA-pair variant
+// Same GEMM with tcgen05.mma.cta_group::2: a cluster of two CTAs on two SMs
+// computes a 256-row x 256-column tile. Each CTA loads its own 128 rows of A
+// and half (128 columns) of the B tile, so each SM takes in 32 KB per K step
+// instead of 48 KB for the same MMA work; the even CTA of the pair issues the
+// MMAs, which read B from both CTAs' shared memory and write each CTA's rows
+// to that CTA's TMEM. The odd CTA's TMA completions are counted on the even
+// CTA's "full" barriers; the MMA commits arrive (multicast) on both CTAs'
+// "empty" and "accumulator full" barriers; both CTAs' epilogues arrive on the
+// even CTA's "accumulator empty" barriers.
+constexpr int P_STAGES = 6;
+constexpr int P_BN_HALF = BN / 2;               // B columns held per CTA
+constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int P_B_BYTES = BK * P_BN_HALF * 2;   // 16 KB
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+// kind::f16, fp32 accumulate, bf16 A/B, A K-major, B MN-major, M = 256, N = 256.
+constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                                ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster_addr, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(bar_cluster_addr), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(kIdescPair), "r"(acc)
+      : "memory");
+}
+// Arrives on the barrier at this offset in every CTA of `mask` (bit = cluster rank).
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask = 0x3) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+template <int LAYER>
+__global__ void __launch_bounds__(kThreads, 1)
+k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + P_STAGES * P_A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES);
+  uint64_t *full = bars, *empty = bars + P_STAGES;
+  uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *tile_start = reinterpret_cast<int *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's expect_tx arrival
+      mbar_init(&empty[s], 1);  // one multicast commit per use
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {  // expert tile prefix: ceil(rows_e / 256) * n_blocks tiles each
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < p.E) {
+        const int rows = p.offset[e + 1] - p.offset[e];
+        t = (rows + 2 * BM - 1) / (2 * BM) * p.n_blocks;
+      }
+      int incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < p.E) tile_start[e] = carry + incl - t;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[p.E] = carry;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[p.E];
+  const int num_kb = p.K / BK;
+
+  auto locate = [&](int tile, int &e, int &pm, int &nb, int &row0, int &rows) {
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_start[mid] <= tile) lo = mid;
+      else hi = mid;
+    }
+    e = lo;
+    row0 = p.offset[e];
+    rows = p.offset[e + 1] - row0;
+    const int mt = (rows + 2 * BM - 1) / (2 * BM);
+    const int local = tile - tile_start[e];
+    nb = local / mt;
+    pm = local % mt;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // --------------------------------------------------------- producer (both CTAs)
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs) {
+        int e, pm, nb, row0, rows;
+        locate(tile, e, pm, nb, row0, rows);
+        const int arow = row0 + pm * 2 * BM + (int)rank * BM;
+        const int ncol = nb * BN + (int)rank * P_BN_HALF;
+        const int brow = e * p.K;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 11)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = mapa(smem_u32(&full[s]), 0);
+          if (leader) mbar_expect_tx(&full[s], 2 * P_STAGE_BYTES);
+          tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kb * BK, arow);
+#pragma unroll
+          for (int j = 0; j < P_BN_HALF / 64; ++j)
+            tma_load_2d_pair(sB + s * P_B_BYTES + j * (BK * 128), &tmB, full_leader,
+                             ncol + j * 64, brow + kb * BK);
+        }
+      }
+      // This CTA's copies have landed once the MMAs that read them are done.
+      const uint32_t issued = it;
+      for (uint32_t q = issued > (uint32_t)P_STAGES ? issued - P_STAGES : 0; q < issued; ++q)
+        mbar_drain(&empty[q % P_STAGES], (q / P_STAGES) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // --------------------------------------------------------- MMA issuer (even CTA)
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 12)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 13)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * P_A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * P_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc(b0 + kk * 2048, BK * 128, 1024);
+            umma_pair(tmem_d, ad, bd, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit_pair(&empty[s]);
+        }
+        if (ok) umma_commit_pair(&acc_full[buf]);
+      }
+      umma_commit_pair(drain, 0x1);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int r_in_tile = quad * 32 + lane;
+    const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
+    int local = 0;
+    for (int tile = pair; tile < total_tiles; tile += n_pairs, ++local) {
+      int e, pm, nb, row0, rows;
+      locate(tile, e, pm, nb, row0, rows);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
+                                                           p.st, 14));
+      if (!ready) break;
+      tc_fence_after();
+      const int m = pm * 2 * BM + (int)rank * BM + r_in_tile;
+      const bool valid = m < rows;
+      const size_t r = (size_t)row0 + m;
+      const float g = (LAYER == 2 && valid) ? p.row_gate[r] : 1.f;
+      bool bad = false;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n = nb * BN + c * 32;
+        uint32_t v[32];
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c * 32);
+        tmem_ld32(taddr, v);
+        if (!valid || n >= p.N) continue;
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          f[j] = __uint_as_float(v[j]);
+          if (p.bias) f[j] += __bfloat162float(p.bias[(size_t)e * p.N + n + j]);
+        }
+        if (LAYER == 1) {
+          __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(fmaxf(f[2 * j], 0.f), fmaxf(f[2 * j + 1], 0.f));
+            packed[j] = *reinterpret_cast<uint32_t *>(&h2);
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            reinterpret_cast<uint4 *>(o)[q] =
+                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        } else {
+          float *o = static_cast<float *>(p.out) + r * p.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            f[j] *= g;
+            bad |= !isfinite(f[j]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4 *>(o)[q] =
+                make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+        }
+      }
+      if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every MMA reading either CTA's memory and every TMEM read are done
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
 // ----------------------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -443,6 +630,8 @@ int sm_count() {
   return n;
 }
 
+namespace {
+
 constexpr size_t smem_bytes(int E) {
   return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 8 + (size_t)(E + 1) * 4;
 }
@@ -458,6 +647,70 @@ cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const Param
   return cudaGetLastError();
 }
 
+constexpr size_t smem_bytes_pair(int E) {
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5) * 8 + 8 +
+         (size_t)(E + 1) * 4;
+}
+
+cudaLaunchAttribute pair_cluster_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 2;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  return a;
+}
+
+// Clusters of two that can be resident at once (0 if the device cannot host one).
+int pair_clusters(size_t smem) {
+  static int cached = -1;
+  if (cached >= 0) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sm_count() / 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1] = {pair_cluster_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaFuncSetAttribute(k_ffn_tc_pair<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_ffn_tc_pair<1>, &cfg) != cudaSuccess)
+    n = 0;
+  cached = n;
+  return n;
+}
+
+template <int LAYER>
+cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const Params &p,
+                              int clusters, cudaStream_t s) {
+  const size_t smem = smem_bytes_pair(p.E);
+  cudaError_t err = cudaFuncSetAttribute(
+      k_ffn_tc_pair<LAYER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pair_cluster_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_ffn_tc_pair<LAYER>, a, b, p);
+}
+
+// Clusters available to the CTA-pair kernel, or 0 when the one-CTA kernel must
+// run (MOE_FFN_TC_VARIANT=single asks for it; so does a device without room).
+int pair_clusters_for(int E) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char *v = getenv("MOE_FFN_TC_VARIANT");
+    forced = (v && v[0] == 's') ? 0 : 1;
+  }
+  if (!forced || smem_bytes_pair(E) > 227 * 1024) return 0;
+  return pair_clusters(smem_bytes_pair(E));
+}
+
 }  // namespace
 
 bool ffn_tc_supported(const moe_config &c) {
@@ -469,7 +722,6 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
                           const int32_t *mtiles, const float *row_gate, const void *W1,
                           const void *b1, const void *W2, const void *b2, void *hbuf, float *zbuf,
                           DeviceStatus *st, cudaStream_t s) {
-  (void)C;
   (void)mtiles;
   const uint64_t A = (uint64_t)c.T * c.k;
   CUtensorMap ta1, tb1, ta2, tb2;
@@ -478,11 +730,20 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
     return cudaErrorInvalidValue;
   Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b1), hbuf, st};
-  cudaError_t err = launch_layer<1>(ta1, tb1, p1, s);
-  if (err != cudaSuccess) return err;
   Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b2), zbuf, st};
-  return launch_layer<2>(ta2, tb2, p2, s);
+  // Per layer: the CTA pair pays off for long K and enough 256-row tiles to
+  // fill several waves; otherwise the one-CTA kernel's finer tiles win.
+  const long rows = (long)c.T * c.k < (long)c.E * C ? (long)c.T * c.k : (long)c.E * C;
+  const int clusters = pair_clusters_for(c.E);
+  auto pair_for = [&](int K, int N) {
+    return clusters > 0 && K >= 2048 && (rows / 256) * ((N + BN - 1) / BN) >= 4L * clusters;
+  };
+  cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, p1, clusters, s)
+                                          : launch_layer<1>(ta1, tb1, p1, s);
+  if (err != cudaSuccess) return err;
+  return pair_for(c.d_ff, c.d) ? launch_layer_pair<2>(ta2, tb2, p2, clusters, s)
+                               : launch_layer<2>(ta2, tb2, p2, s);
 }
 
 }  // namespace moe

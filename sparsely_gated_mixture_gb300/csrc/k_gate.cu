@@ -11,6 +11,7 @@
 #include "moe_internal.cuh"
 
 #include <math.h>
+#include <stdlib.h>
 
 namespace moe {
 namespace {
@@ -552,8 +553,16 @@ k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials,
 
 cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
                           const float *noise, const float *bias, float *c, float *sigma, float *H,
-                          DeviceStatus *st, cudaStream_t s) {
+                          void *bsplit, DeviceStatus *st, cudaStream_t s) {
   const bool noisy = Wn != nullptr;
+  // bf16 tokens: the tensor-core router (MOE_ROUTER=simt selects the CUDA-core kernels).
+  static int force_simt = -1;
+  if (force_simt < 0) {
+    const char *v = getenv("MOE_ROUTER");
+    force_simt = (v && v[0] == 's') ? 1 : 0;
+  }
+  if (!force_simt && router_tc_supported(cfg))
+    return launch_router_tc(cfg, x, Wg, Wn, noise, bias, c, sigma, H, bsplit, st, s);
   // Vector path: whole 16-byte pieces of every x row, and a small expert count
   // (beyond it the per-block W traffic of this layout grows with E).
   const bool vec = cfg.E <= 64 &&

@@ -1,0 +1,335 @@
+// Stage 1 router on the tensor cores ("Outrageously Large", Noisy Top-K
+// Gating step 1, Eq. 4; "Switch Transformer", step 1: the router is fp32).
+//
+// x is bf16, so every product x_i * W[i,e] is exact once W is written as the
+// sum of three bf16 pieces: hi = bf16(W), mid = bf16(W - hi), lo = bf16(W -
+// hi - mid), with W = hi + mid + lo exactly (each piece carries 8 of fp32's
+// 24 significand bits; the differences are exact in fp32). The router is then
+// three bf16 GEMMs, x * hi + x * mid + x * lo, accumulated in fp32 in TMEM:
+// the fp32 router's arithmetic at the tensor cores' rate.
+//
+// k_router_split builds the pieces, transposed so that each B row is one
+// output column (K contiguous): columns 2e and 2e+1 are expert e's clean and
+// noise logits (noisy gate) or column e is expert e (no noise), each plane
+// padded with zero rows to a whole number of column tiles.
+// k_router_tc is one persistent CTA per SM: a TMA warp loads x [128 tokens x
+// 64 K] and the three [BNR columns x 64 K] B pieces per stage, one lane
+// issues 3 x 4 tcgen05.mma (M=128, N=BNR, K=16, both operands K-major,
+// 128B swizzle) into one of two TMEM accumulators, and four epilogue warps
+// turn each token's row into c = acc + b, sigma = Softplus(z) and
+// H = c + noise * sigma, written as fp32 [T, E].
+#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int RBM = 128, RBK = 64, kRThreads = 192;
+
+struct RParams {
+  int T, d, E, noisy, NC, NCP, n_blocks;
+  const float *noise, *bias;
+  float *c_out, *s_out, *H_out;
+  DeviceStatus *st;
+};
+
+__device__ __forceinline__ float softplus_r(float z) {
+  return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
+}
+
+// grid (ceil(d/32), ceil(NCP/32)), block (32, 8): a 32 x 32 transpose tile.
+__global__ void k_router_split(int d, int E, int noisy, int NC, int NCP,
+                               const float *__restrict__ Wg, const float *__restrict__ Wn,
+                               __nv_bfloat16 *__restrict__ B) {
+  __shared__ float tile[32][33];
+  const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int k = k0 + r, n = n0 + threadIdx.x;
+    float w = 0.f;
+    if (k < d && n < NC) {
+      const int e = noisy ? n >> 1 : n;
+      const float *src = (noisy && (n & 1)) ? Wn : Wg;
+      w = src[(size_t)k * E + e];
+    }
+    tile[r][threadIdx.x] = w;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int n = n0 + r, k = k0 + threadIdx.x;
+    if (n >= NCP || k >= d) continue;
+    const float w = tile[threadIdx.x][r];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    B[((size_t)0 * NCP + n) * d + k] = hi;
+    B[((size_t)1 * NCP + n) * d + k] = mid;
+    B[((size_t)2 * NCP + n) * d + k] = lo;
+  }
+}
+
+template <int BNR>
+struct RCfg {
+  static constexpr int A_BYTES = RBM * RBK * 2;  // 16 KB
+  static constexpr int P_BYTES = BNR * RBK * 2;  // one piece
+  static constexpr int STAGE = A_BYTES + 3 * P_BYTES;
+  static constexpr int FIT = 200 * 1024 / STAGE;
+  static constexpr int STAGES = FIT > 8 ? 8 : (FIT < 2 ? 2 : FIT);
+  static constexpr int TMEM_COLS = 2 * BNR < 32 ? 32 : 2 * BNR;
+  // kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = BNR.
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                    ((uint32_t)(BNR >> 3) << 17) | ((uint32_t)(RBM >> 4) << 24);
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (2 * STAGES + 5) * 8 + 8;
+};
+
+template <int BNR>
+__device__ __forceinline__ void umma_r(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(RCfg<BNR>::IDESC), "r"(acc)
+      : "memory");
+}
+
+// Epilogue for `count` accumulator columns of token t starting at column n.
+__device__ __forceinline__ void router_cols(const RParams &p, int t, int n, const uint32_t *v,
+                                            int count) {
+  if (p.noisy) {
+    for (int j = 0; j + 1 < count; j += 2) {
+      const int e = (n + j) >> 1;
+      if (e >= p.E) break;
+      float c = __uint_as_float(v[j]);
+      if (p.bias) c += p.bias[e];
+      const float sg = softplus_r(__uint_as_float(v[j + 1]));
+      const size_t o = (size_t)t * p.E + e;
+      const float h = fmaf(p.noise[o], sg, c);
+      p.c_out[o] = c;
+      p.s_out[o] = sg;
+      p.H_out[o] = h;
+      if (!isfinite(h)) record_error(p.st, MOE_ERR_NONFINITE, (long long)o);
+    }
+  } else {
+    for (int j = 0; j < count; ++j) {
+      const int e = n + j;
+      if (e >= p.E) break;
+      float c = __uint_as_float(v[j]);
+      if (p.bias) c += p.bias[e];
+      const size_t o = (size_t)t * p.E + e;
+      p.c_out[o] = c;
+      p.s_out[o] = 0.f;
+      p.H_out[o] = c;
+      if (!isfinite(c)) record_error(p.st, MOE_ERR_NONFINITE, (long long)o);
+    }
+  }
+}
+
+template <int BNR>
+__global__ void __launch_bounds__(kRThreads, 1)
+k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            const RParams p) {
+  using C = RCfg<BNR>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE);
+  uint64_t *full = bars, *empty = bars + C::STAGES;
+  uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int m_blocks = (p.T + RBM - 1) / RBM;
+  const int total = m_blocks * p.n_blocks;
+  const int num_kb = (p.d + RBK - 1) / RBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 21)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = smem + s * C::STAGE;
+          mbar_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(st, &tmA, &full[s], kb * RBK, mb * RBM);
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+            tma_load_2d(st + C::A_BYTES + q * C::P_BYTES, &tmB, &full[s], kb * RBK,
+                        q * p.NCP + nb * BNR);
+        }
+      }
+      const uint32_t issued = it;
+      for (uint32_t q = issued > (uint32_t)C::STAGES ? issued - C::STAGES : 0; q < issued; ++q)
+        mbar_drain(&full[q % C::STAGES], (q / C::STAGES) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 22)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BNR);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 23)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < RBK / 16; ++kk) {
+            const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              const uint64_t bd = sdesc(a0 + C::A_BYTES + q * C::P_BYTES + kk * 32, 16, 1024);
+              umma_r<BNR>(tmem_d, ad, bd, (kb | kk | q) ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&acc_full[buf]);
+      }
+      umma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    const int quad = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
+                                                           p.st, 24));
+      if (!ready) break;
+      tc_fence_after();
+      const int t = mb * RBM + quad * 32 + lane;
+      const uint32_t lane_addr =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BNR);
+      if (BNR == 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_addr, v);
+        if (t < p.T) router_cols(p, t, nb * BNR, v, 16);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BNR / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + (uint32_t)(c * 32), v);
+          const int n = nb * BNR + c * 32;
+          if (t < p.T && n < p.NC) router_cols(p, t, n, v, 32);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+int tile_cols(int NC) {
+  return NC <= 16 ? 16 : NC <= 32 ? 32 : NC <= 64 ? 64 : NC <= 128 ? 128 : 256;
+}
+
+template <int BNR>
+cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float *Wn,
+                const float *noise, const float *bias, float *cc, float *sg, float *H,
+                void *bsplit, DeviceStatus *st, cudaStream_t s) {
+  const int noisy = Wn != nullptr;
+  const int NC = noisy ? 2 * c.E : c.E;
+  const int n_blocks = (NC + BNR - 1) / BNR;
+  const int NCP = n_blocks * BNR;
+  dim3 sg_grid((c.d + 31) / 32, (NCP + 31) / 32);
+  k_router_split<<<sg_grid, dim3(32, 8), 0, s>>>(c.d, c.E, noisy, NC, NCP, Wg, Wn,
+                                                 static_cast<__nv_bfloat16 *>(bsplit));
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, x, (uint64_t)c.T, (uint64_t)c.d, RBM) ||
+      !make_map(&tb, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, BNR))
+    return cudaErrorInvalidValue;
+  RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, noise, bias, cc, sg, H, st};
+  const size_t smem = RCfg<BNR>::SMEM;
+  err = cudaFuncSetAttribute(k_router_tc<BNR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (err != cudaSuccess) return err;
+  const int tiles = ((c.T + RBM - 1) / RBM) * n_blocks;
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k_router_tc<BNR><<<grid, kRThreads, smem, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool router_tc_supported(const moe_config &c) {
+  return c.act_dtype == MOE_BF16 && c.d % 8 == 0 && encode_fn() != nullptr;
+}
+
+size_t router_tc_split_bytes(const moe_config &c) {
+  const int NC = 2 * c.E;  // the noisy layout is the larger one
+  const int BNR = tile_cols(NC);
+  const size_t NCP = (size_t)((NC + BNR - 1) / BNR) * BNR;
+  return 3 * NCP * (size_t)c.d * 2;
+}
+
+cudaError_t launch_router_tc(const moe_config &c, const void *x, const float *Wg, const float *Wn,
+                             const float *noise, const float *bias, float *cc, float *sg, float *H,
+                             void *bsplit, DeviceStatus *st, cudaStream_t s) {
+  switch (tile_cols(Wn ? 2 * c.E : c.E)) {
+    case 16: return run<16>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    case 32: return run<32>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    case 64: return run<64>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    case 128: return run<128>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    default: return run<256>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+  }
+}
+
+}  // namespace moe

@@ -28,6 +28,7 @@ WsLayout ws_layout(const moe_config &cfg) {
   L.sigma = take(T * E * 4);
   L.H = take(T * E * 4);
   L.rowstat = take(T * 2 * 4);
+  L.bsplit = take(router_tc_split_bytes(cfg));
   L.hist = take((size_t)L.n_chunks * E * 4);
   L.chunk_base = take((size_t)L.n_chunks * E * 4);
   L.count = take(E * 4);
@@ -95,7 +96,7 @@ static int gate_impl(const moe_config &c, const void *x, const float *Wg, const 
   float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
   float *rs = ws_at<float>(ws, L.rowstat);
   MOE_CUDA(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
-  MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, st, s));
+  MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, ws_at<char>(ws, L.bsplit), st, s));
   MOE_CUDA(launch_select(c, H, idx, gate, thr, rs, st, s));
   if (partials)
     MOE_CUDA(launch_aux_partials(c, Wn != nullptr, cc, sg, H, rs, idx, gate, thr,

@@ -33,6 +33,7 @@ __device__ __forceinline__ void record_error(DeviceStatus *st, int code, long lo
 struct WsLayout {
   size_t status;
   size_t c, sigma, H, rowstat;            // router results kept for the balancing sums
+  size_t bsplit;                          // router weights as three bf16 pieces (tensor-core router)
   size_t hist, chunk_base;                // slot pass: per-chunk per-expert counts and bases
   size_t count, offset, mtiles;           // per-expert totals, row offsets, GEMM tile prefix
   size_t partials, aux_vec;               // balancing partial sums and final vectors
@@ -58,7 +59,7 @@ inline int elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
 // k_gate.cu: router GEMM + noise + softplus, selection + softmax, balancing partials.
 cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
                           const float *noise, const float *bias, float *c, float *sigma, float *H,
-                          DeviceStatus *st, cudaStream_t s);
+                          void *bsplit, DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, float *gate,
                           float *thr, float *rowstat, DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
@@ -69,6 +70,13 @@ cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, in
                                 float *out3, float *importance, float *load, double *aux_vec,
                                 DeviceStatus *st, cudaStream_t s);
 int aux_token_block(int E);  // tokens per partial-sum block of the balancing sums
+
+// k_router_tc.cu: the router as three bf16 tensor-core GEMMs (exact split of W).
+bool router_tc_supported(const moe_config &cfg);
+size_t router_tc_split_bytes(const moe_config &cfg);
+cudaError_t launch_router_tc(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
+                             const float *noise, const float *bias, float *c, float *sigma,
+                             float *H, void *bsplit, DeviceStatus *st, cudaStream_t s);
 
 // k_slots.cu: capacity, token-order slots, dispatch maps.
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
