@@ -403,6 +403,7 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
 // identical. partials layout: [block][4][E] = importance, load, first-choice
 // count, sum of Softmax(H).
 constexpr int kAuxWarps = 8;
+constexpr int kAuxMaxK = 16;
 
 template <int VPL>
 __global__ void __launch_bounds__(kAuxWarps * 32)
@@ -422,33 +423,50 @@ k_aux_partials(int T, int E, int k, int tb, int noisy, const float *__restrict__
 #pragma unroll
     for (int i = 0; i < VPL; ++i) acc[q][i] = 0.f;
   for (int t = t0 + warp; t < t1; t += kAuxWarps) {
+    // All of this token's loads first, so they are in flight together.
     const float th0 = thr[2 * (size_t)t], th1 = thr[2 * (size_t)t + 1];
-    const float mx = rowstat[2 * (size_t)t], se = rowstat[2 * (size_t)t + 1];
-    const int first = idx[(size_t)t * k];
+    const float mx = rowstat[2 * (size_t)t], inv_se = 1.f / rowstat[2 * (size_t)t + 1];
+    int chosen_e[kAuxMaxK];
+    float chosen_g[kAuxMaxK];
+#pragma unroll
+    for (int j = 0; j < kAuxMaxK; ++j) {
+      chosen_e[j] = j < k ? idx[(size_t)t * k + j] : -1;
+      chosen_g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
+    }
+    float cv[VPL], sv[VPL], hv[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = e0 + lane + 32 * i;
+      const size_t o = (size_t)t * E + (e < E ? e : 0);
+      hv[i] = H[o];
+      cv[i] = noisy ? c[o] : 0.f;
+      sv[i] = noisy ? sg[o] : 0.f;
+    }
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = e0 + lane + 32 * i;
       if (e >= E) continue;
-      int chosen = -1;
-      for (int j = 0; j < k; ++j)
-        if (idx[(size_t)t * k + j] == e) chosen = j;
-      const size_t o = (size_t)t * E + e;
-      if (chosen >= 0) acc[0][i] += gate[(size_t)t * k + chosen];
+      float g = 0.f;
+      bool in = false;
+#pragma unroll
+      for (int j = 0; j < kAuxMaxK; ++j)
+        if (chosen_e[j] == e) {
+          in = true;
+          g = chosen_g[j];
+        }
+      acc[0][i] += g;
       float p;
       if (k == E) {
         p = 1.f;
+      } else if (sv[i] == 0.f) {
+        p = in ? 1.f : 0.f;
       } else {
-        const float s = noisy ? sg[o] : 0.f;
-        if (s == 0.f) {
-          p = chosen >= 0 ? 1.f : 0.f;
-        } else {
-          const float u = (c[o] - (chosen >= 0 ? th1 : th0)) / s;
-          p = 0.5f * erfcf(-u * 0.70710678118654752f);
-        }
+        const float u = (cv[i] - (in ? th1 : th0)) / sv[i];
+        p = 0.5f * erfcf(-u * 0.70710678118654752f);
       }
       acc[1][i] += p;
-      if (first == e) acc[2][i] += 1.f;
-      acc[3][i] += expf(H[o] - mx) / se;
+      if (chosen_e[0] == e) acc[2][i] += 1.f;
+      acc[3][i] += expf(hv[i] - mx) * inv_se;
     }
   }
 #pragma unroll
@@ -606,7 +624,7 @@ cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, f
   return cudaGetLastError();
 }
 
-int aux_token_block(int E) { return E <= 64 ? 64 : (E <= 256 ? 256 : 512); }
+int aux_token_block(int E) { return E <= 64 ? 64 : (E <= 256 ? 128 : 256); }
 
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
                                 const float *sigma, const float *H, const float *rowstat,

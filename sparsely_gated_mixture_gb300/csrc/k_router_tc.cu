@@ -13,18 +13,21 @@
 // noise logits (noisy gate) or column e is expert e (no noise), each plane
 // padded with zero rows to a whole number of column tiles.
 // k_router_tc is one persistent CTA per SM: a TMA warp loads x [128 tokens x
-// 64 K] and the three [BNR columns x 64 K] B pieces per stage, one lane
-// issues 3 x 4 tcgen05.mma (M=128, N=BNR, K=16, both operands K-major,
-// 128B swizzle) into one of two TMEM accumulators, and four epilogue warps
-// turn each token's row into c = acc + b, sigma = Softplus(z) and
-// H = c + noise * sigma, written as fp32 [T, E].
+// 64 K] and the three [BNR columns x 64 K] B pieces per stage (BNR <= 64),
+// one lane issues 3 x 4 tcgen05.mma (M=128, N=BNR, K=16, both operands
+// K-major, 128B swizzle) into one of two TMEM accumulators, and eight epilogue
+// warps (two per TMEM lane quadrant) turn each token's columns into c = acc + b, sigma = Softplus(z) and
+// H = c + noise * sigma, staged in shared memory so that noise is read and
+// c, sigma, H [T, E] fp32 are written a row segment at a time.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int RBM = 128, RBK = 64, kRThreads = 192;
+constexpr int RBM = 128, RBK = 64;
+constexpr int kREpiWarps = 8;  // two per TMEM lane quadrant, alternating 16-column chunks
+constexpr int kRThreads = 64 + 32 * kREpiWarps;
 
 struct RParams {
   int T, d, E, noisy, NC, NCP, n_blocks;
@@ -69,18 +72,25 @@ __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP,
   }
 }
 
+// Epilogue staging: per epilogue warp, three [32 rows x 16 experts] fp32
+// tiles (c, sigma, H out), columns XOR-swizzled by row to spread banks.
+constexpr int kEpiTile = 32 * 16;
+constexpr int EPI_BYTES = kREpiWarps * 3 * kEpiTile * 4;  // 8 warps x 3 tiles = 48 KB
+
 template <int BNR>
 struct RCfg {
   static constexpr int A_BYTES = RBM * RBK * 2;  // 16 KB
   static constexpr int P_BYTES = BNR * RBK * 2;  // one piece
   static constexpr int STAGE = A_BYTES + 3 * P_BYTES;
-  static constexpr int FIT = 200 * 1024 / STAGE;
-  static constexpr int STAGES = FIT > 8 ? 8 : (FIT < 2 ? 2 : FIT);
+  static constexpr int FIT = (227 * 1024 - 1024 - EPI_BYTES - 256) / STAGE;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
   static constexpr int TMEM_COLS = 2 * BNR < 32 ? 32 : 2 * BNR;
   // kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = BNR.
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                                     ((uint32_t)(BNR >> 3) << 17) | ((uint32_t)(RBM >> 4) << 24);
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + (2 * STAGES + 5) * 8 + 8;
+  static constexpr size_t SMEM =
+      1024 + (size_t)STAGES * STAGE + EPI_BYTES + (2 * STAGES + 5) * 8 + 8;
+  static_assert(STAGES >= 2, "router tile too wide for two pipeline stages");
 };
 
 template <int BNR>
@@ -92,35 +102,61 @@ __device__ __forceinline__ void umma_r(uint32_t tmem_d, uint64_t a, uint64_t b, 
       : "memory");
 }
 
-// Epilogue for `count` accumulator columns of token t starting at column n.
-__device__ __forceinline__ void router_cols(const RParams &p, int t, int n, const uint32_t *v,
-                                            int count) {
-  if (p.noisy) {
-    for (int j = 0; j + 1 < count; j += 2) {
-      const int e = (n + j) >> 1;
-      if (e >= p.E) break;
-      float c = __uint_as_float(v[j]);
-      if (p.bias) c += p.bias[e];
-      const float sg = softplus_r(__uint_as_float(v[j + 1]));
-      const size_t o = (size_t)t * p.E + e;
-      const float h = fmaf(p.noise[o], sg, c);
-      p.c_out[o] = c;
-      p.s_out[o] = sg;
+// Epilogue for up to 16 experts e0 .. e0+ne-1 of the warp's 32 tokens t0 ..
+// t0+31. Lane l holds token t0+l's clean logits cv[], noise logits zv[] and
+// noise draws nz[] (noisy gate) in registers; c, sigma and H go through the
+// warp's staging tiles so that each store instruction writes two tokens'
+// 16-expert row segments.
+__device__ __forceinline__ int swz(int row, int col) { return row * 16 + (col ^ (row & 15)); }
+
+__device__ __forceinline__ void router_rows(const RParams &p, int t0, int e0, int ne,
+                                            const float *cv, const float *zv, const float *nz,
+                                            float *stg) {
+  const int lane = threadIdx.x & 31;
+  float *sc = stg, *ss = stg + kEpiTile, *sh = stg + 2 * kEpiTile;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float c = cv[j];
+    if (p.bias && j < ne) c += p.bias[e0 + j];
+    float sg = 0.f, h = c;
+    if (p.noisy && j < 8) {
+      sg = softplus_r(zv[j]);
+      h = fmaf(nz[j], sg, c);
+    }
+    sc[swz(lane, j)] = c;
+    ss[swz(lane, j)] = sg;
+    sh[swz(lane, j)] = h;
+  }
+  __syncwarp();
+  const int half = lane >> 4, col = lane & 15;
+  bool bad = false;
+#pragma unroll 4
+  for (int r = 0; r < 32; r += 2) {
+    const int row = r + half, t = t0 + row;
+    if (t < p.T && col < ne) {
+      const size_t o = (size_t)t * p.E + e0 + col;
+      const float h = sh[swz(row, col)];
+      p.c_out[o] = sc[swz(row, col)];
+      p.s_out[o] = ss[swz(row, col)];
       p.H_out[o] = h;
-      if (!isfinite(h)) record_error(p.st, MOE_ERR_NONFINITE, (long long)o);
+      bad |= !isfinite(h);
     }
+  }
+  if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)t0);
+  __syncwarp();
+}
+
+// Token t's noise draws for experts e0 .. e0+7 (zero past E or T).
+__device__ __forceinline__ void load_noise8(const RParams &p, int t, int e0, float *nz) {
+  if (t < p.T && (p.E & 3) == 0 && e0 + 8 <= p.E) {
+    const float4 *src = reinterpret_cast<const float4 *>(p.noise + (size_t)t * p.E + e0);
+    const float4 a = src[0], b = src[1];
+    nz[0] = a.x; nz[1] = a.y; nz[2] = a.z; nz[3] = a.w;
+    nz[4] = b.x; nz[5] = b.y; nz[6] = b.z; nz[7] = b.w;
   } else {
-    for (int j = 0; j < count; ++j) {
-      const int e = n + j;
-      if (e >= p.E) break;
-      float c = __uint_as_float(v[j]);
-      if (p.bias) c += p.bias[e];
-      const size_t o = (size_t)t * p.E + e;
-      p.c_out[o] = c;
-      p.s_out[o] = 0.f;
-      p.H_out[o] = c;
-      if (!isfinite(c)) record_error(p.st, MOE_ERR_NONFINITE, (long long)o);
-    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      nz[j] = (t < p.T && e0 + j < p.E) ? p.noise[(size_t)t * p.E + e0 + j] : 0.f;
   }
 }
 
@@ -132,7 +168,8 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE);
+  float *staging = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE + EPI_BYTES);
   uint64_t *full = bars, *empty = bars + C::STAGES;
   uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -146,7 +183,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], kREpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -234,7 +271,8 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     __syncwarp();
   } else {
-    const int quad = warp & 3;
+    const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
+    const int sub = (warp - 2) >> 2;    // this warp's chunks: sub, sub+2, ...
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
@@ -244,21 +282,47 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                                            p.st, 24));
       if (!ready) break;
       tc_fence_after();
-      const int t = mb * RBM + quad * 32 + lane;
+      const int t0 = mb * RBM + quad * 32;
       const uint32_t lane_addr =
           tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BNR);
-      if (BNR == 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_addr, v);
-        if (t < p.T) router_cols(p, t, nb * BNR, v, 16);
-      } else {
+      float *stg = staging + (size_t)(warp - 2) * 3 * kEpiTile;
+      const int t = t0 + lane;
+      const int nchunks = (min(p.NC - nb * BNR, BNR) + 15) / 16;
+      // 16 columns at a time: 8 experts (noisy, clean/noise pairs) or 16.
+      // The next chunk's noise is loaded while this one is computed.
+      float nz_next[8];
+      if (p.noisy && sub < nchunks) load_noise8(p, t, (nb * BNR + sub * 16) >> 1, nz_next);
 #pragma unroll 1
-        for (int c = 0; c < BNR / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + (uint32_t)(c * 32), v);
-          const int n = nb * BNR + c * 32;
-          if (t < p.T && n < p.NC) router_cols(p, t, n, v, 32);
+      for (int c16 = sub; c16 < nchunks; c16 += 2) {
+        const int n = nb * BNR + c16 * 16;
+        float nz[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) nz[j] = nz_next[j];
+        if (p.noisy && c16 + 2 < nchunks) load_noise8(p, t, (n + 32) >> 1, nz_next);
+        uint32_t v[16];
+        tmem_ld16(lane_addr + (uint32_t)(c16 * 16), v);
+        float cv[16], zv[16];
+        int e0, ne;
+        if (p.noisy) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            cv[j] = __uint_as_float(v[2 * j]);
+            zv[j] = __uint_as_float(v[2 * j + 1]);
+          }
+#pragma unroll
+          for (int j = 8; j < 16; ++j) cv[j] = zv[j] = 0.f;
+          e0 = n >> 1;
+          ne = p.E - e0 < 8 ? p.E - e0 : 8;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            cv[j] = __uint_as_float(v[j]);
+            zv[j] = 0.f;
+          }
+          e0 = n;
+          ne = p.E - e0 < 16 ? p.E - e0 : 16;
         }
+        router_rows(p, t0, e0, ne, cv, zv, nz, stg);
       }
       tc_fence_before();
       __syncwarp();
@@ -275,9 +339,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   }
 }
 
-int tile_cols(int NC) {
-  return NC <= 16 ? 16 : NC <= 32 ? 32 : NC <= 64 ? 64 : NC <= 128 ? 128 : 256;
-}
+int tile_cols(int NC) { return NC <= 16 ? 16 : NC <= 32 ? 32 : 64; }
 
 template <int BNR>
 cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float *Wn,
@@ -326,9 +388,7 @@ cudaError_t launch_router_tc(const moe_config &c, const void *x, const float *Wg
   switch (tile_cols(Wn ? 2 * c.E : c.E)) {
     case 16: return run<16>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
     case 32: return run<32>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
-    case 64: return run<64>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
-    case 128: return run<128>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
-    default: return run<256>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    default: return run<64>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
   }
 }
 
