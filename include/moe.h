@@ -31,7 +31,12 @@
  *   moe_last_device_status() reads it. moe_gate() and moe_forward() clear it
  *   when they start, moe_last_device_status() after reading it; a caller whose
  *   first call on a fresh workspace is another stage zero-fills the workspace
- *   (or calls moe_last_device_status) first.
+ *   (or calls moe_last_device_status) first. Each bounded wait inside the
+ *   tensor-core kernels gives up after 2 s, or after MOE_WAIT_LIMIT_NS
+ *   nanoseconds if that environment variable is set when the call is made
+ *   (a diagnostic: 0 makes the first wait that is not already satisfied run
+ *   out); the kernel then records MOE_ERR_TIMEOUT, finishes its copies and
+ *   MMAs in flight and returns, leaving the CUDA context usable.
  * Determinism.  Indices, slots and drop masks are exact; no floating-point
  *   atomics are used, so two calls on the same inputs give identical bits.
  */

@@ -46,6 +46,7 @@ struct Params {
   const __nv_bfloat16 *bias;  // [E, N] or null
   void *out;              // layer 1: bf16 [rows, N]; layer 2: fp32 [rows, N]
   DeviceStatus *st;
+  unsigned long long wait_ns;  // bounded-wait limit
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -166,7 +167,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 1)) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 1, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -193,13 +194,13 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 2)) break;
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 2, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BN);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 3)) {
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 3, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -233,7 +234,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       const uint32_t use = (uint32_t)(local >> 1);
       // Warp-uniform decision before the warp-collective TMEM loads.
       const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
-                                                           p.st, 4));
+                                                           p.st, 4, p.wait_ns));
       if (!ready) break;
       tc_fence_after();
       const int m = mb * BM + r_in_tile;
@@ -457,7 +458,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 11)) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 11, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -485,13 +486,13 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       for (int tile = pair; ok && tile < total_tiles; tile += n_pairs, ++local) {
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 12)) break;
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 12, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BN);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 13)) {
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 13, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -525,7 +526,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
       const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
-                                                           p.st, 14));
+                                                           p.st, 14, p.wait_ns));
       if (!ready) break;
       tc_fence_after();
       const int m = pm * 2 * BM + (int)rank * BM + r_in_tile;
@@ -617,6 +618,12 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+unsigned long long wait_limit_ns() {
+  const char *v = getenv("MOE_WAIT_LIMIT_NS");
+  if (v && *v) return strtoull(v, nullptr, 10);
+  return 2000000000ull;
 }
 
 int sm_count() {
@@ -729,9 +736,9 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
       !make_map(&ta2, hbuf, A, c.d_ff, BM) || !make_map(&tb2, W2, (uint64_t)c.E * c.d_ff, c.d, BK))
     return cudaErrorInvalidValue;
   Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, offset, row_gate,
-            static_cast<const __nv_bfloat16 *>(b1), hbuf, st};
+            static_cast<const __nv_bfloat16 *>(b1), hbuf, st, wait_limit_ns()};
   Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, offset, row_gate,
-            static_cast<const __nv_bfloat16 *>(b2), zbuf, st};
+            static_cast<const __nv_bfloat16 *>(b2), zbuf, st, wait_limit_ns()};
   // Per layer: the CTA pair pays off for long K and enough 256-row tiles to
   // fill several waves; otherwise the one-CTA kernel's finer tiles win.
   const long rows = (long)c.T * c.k < (long)c.E * C ? (long)c.T * c.k : (long)c.E * C;

@@ -34,6 +34,7 @@ struct RParams {
   const float *noise, *bias;
   float *c_out, *s_out, *H_out;
   DeviceStatus *st;
+  unsigned long long wait_ns;  // bounded-wait limit
 };
 
 __device__ __forceinline__ float softplus_r(float z) {
@@ -215,7 +216,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 21)) {
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 21, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -241,13 +242,13 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
-        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 22)) break;
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 22, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BNR);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 23)) {
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 23, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -279,7 +280,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
       const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
-                                                           p.st, 24));
+                                                           p.st, 24, p.wait_ns));
       if (!ready) break;
       tc_fence_after();
       const int t0 = mb * RBM + quad * 32;
@@ -358,7 +359,8 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   if (!make_map(&ta, x, (uint64_t)c.T, (uint64_t)c.d, RBM) ||
       !make_map(&tb, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, BNR))
     return cudaErrorInvalidValue;
-  RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, noise, bias, cc, sg, H, st};
+  RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, noise, bias, cc, sg, H, st,
+            wait_limit_ns()};
   const size_t smem = RCfg<BNR>::SMEM;
   err = cudaFuncSetAttribute(k_router_tc<BNR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);

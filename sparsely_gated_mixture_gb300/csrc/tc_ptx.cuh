@@ -16,10 +16,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64 cols], 128B swizzle.
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 int sm_count();
+// Limit of every bounded mbarrier wait, in ns: MOE_WAIT_LIMIT_NS if set (read
+// at each launch, so a test can shorten it to force the timeout path), else 2 s.
+unsigned long long wait_limit_ns();
 
 namespace {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long kDrainLimitNs = 2000000000ull;  // 2 s per drain wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -55,19 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Bounded wait. Returns false if this CTA is aborting (limit reached here or
 // elsewhere in the CTA); the first thread to run out records the error.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          DeviceStatus *st, int where) {
+                                          DeviceStatus *st, int where,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        record_error(st, MOE_ERR_TIMEOUT, (long long)where);
-        return false;
-      }
+  for (;;) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 >= limit_ns) {
+      *abort_flag = 1;
+      record_error(st, MOE_ERR_TIMEOUT, (long long)where);
+      return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
   }
 }
 
@@ -75,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
+    if (globaltimer() - t0 > kDrainLimitNs) return;
   }
 }
 
