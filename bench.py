@@ -36,6 +36,26 @@ from sparsely_gated_mixture_gb300 import workloads as wl  # noqa: E402
 METRIC = "MoE layer fwd tokens/s @1 GB300; expert GEMM % bf16 peak; gate/dispatch HBM %"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+# DRAM bytes (read + write) of the expert FFN stage per step, from one ncu
+# capture (profiles/expert_ffn_tc_pair_top2_large_experts.md), valid only for
+# the kernel source it was taken on (hash of k_ffn_tc.cu + tc_ptx.cuh).
+FFN_TRAFFIC = {"top2_large_experts": {"bytes": 5272459264, "source": "538ca832aa8ddec3"}}
+
+
+def ffn_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("k_ffn_tc.cu", "tc_ptx.cuh"):
+        with open(os.path.join(ROOT, "sparsely_gated_mixture_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(w) -> int | None:
+    rec = FFN_TRAFFIC.get(w.name)
+    if rec is None or w != wl.WORKLOADS.get(w.name) or rec["source"] != ffn_source_hash():
+        return None
+    return rec["bytes"]
 
 
 def load_peaks():
@@ -307,9 +327,10 @@ def run_ours(args, w: wl.Workload):
         "aux_loss": {"ms": mean["aux_loss"]},
     }
     tps = world * T / (ms * 1e-3)
-    # router, select, balancing partials, slot histogram / scan / rank, gather,
-    # two expert GEMMs, combine, balancing finalize
-    launches_per_step = 11
+    # router (plus the weight split that feeds the tensor-core router for bf16
+    # tokens), select, balancing partials, slot histogram / scan / rank,
+    # gather, two expert GEMMs, combine, balancing finalize
+    launches_per_step = 12 if (w.dtype == "bf16" and w.d % 8 == 0) else 11
     line = {
         "metric": METRIC,
         "value": tps,
@@ -330,7 +351,8 @@ def run_ours(args, w: wl.Workload):
         "roofline": {"kernel": "moe_expert_ffn (two grouped GEMM launches)", "bound": "tensor",
                      "achieved": ffn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": ffn_tflops / peaks["bf16_tflops"], "peak_source": peak_kind,
-                     "algorithmic_flops_per_launch": tr["ffn_flops"], "traffic": None},
+                     "algorithmic_flops_per_launch": tr["ffn_flops"],
+                     "algorithmic_bytes": tr["ffn_bytes"], "traffic": measured_traffic(w)},
         "stages": stage_rep,
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x.numel() * x.element_size()
