@@ -319,46 +319,34 @@ cudaError_t router_vec_dispatch(const moe_config &cfg, const void *x, const floa
 }
 
 // ----------------------------------------------------------------------------- selection
-// One warp per token; expert e lives in lane e % 32, slot e / 32.
+// One warp per token; expert e lives in lane e % 32, slot e / 32. On return
+// every lane holds the same results: topv/topi = the k+1 (k if k == E) largest
+// values in (value desc, index asc) order, mx = max, se = sum of exp(v - mx).
+// A NaN never wins; if only NaNs remain a round yields E (out of range),
+// which the consumers reject. The router has already flagged the NaN.
 template <int VPL>
-__global__ void __launch_bounds__(256)
-k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__restrict__ idx,
-         float *__restrict__ gate, float *__restrict__ thr, float *__restrict__ rowstat) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float *h = H + (size_t)t * E;
-  float v[VPL];
-  float mx = -INFINITY;
+__device__ __forceinline__ void warp_topk(const float (&v)[VPL], int E, int k, int lane,
+                                          float *topv, int *topi, float &mx, float &se) {
+  mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    int e = lane + 32 * i;
-    v[i] = e < E ? h[e] : -INFINITY;
-    mx = fmaxf(mx, v[i]);
-  }
+  for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, v[i]);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float se = 0.f;
+  se = 0.f;
 #pragma unroll
   for (int i = 0; i < VPL; ++i)
     if (lane + 32 * i < E) se += expf(v[i] - mx);
 #pragma unroll
   for (int o = 16; o; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
-
-  // Rounds of warp-wide argmax in (value desc, index asc) order. A NaN never
-  // wins; if only NaNs remain the round yields E (out of range), which the
-  // consumers reject. The router has already flagged the NaN.
   uint32_t taken = 0;
   const int rounds = k < E ? k + 1 : k;
-  float topv[kMaxK + 1];
-  int topi[kMaxK + 1];
   for (int r = 0; r < rounds; ++r) {
     float bv = -INFINITY;
     int bi = E;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      int e = lane + 32 * i;
-      bool ok = e < E && !((taken >> i) & 1u);
+      const int e = lane + 32 * i;
+      const bool ok = e < E && !((taken >> i) & 1u);
       if (ok && (v[i] > bv || (v[i] == bv && e < bi))) {
         bv = v[i];
         bi = e;
@@ -366,8 +354,8 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
       if (ov > bv || (ov == bv && oi < bi)) {
         bv = ov;
         bi = oi;
@@ -377,17 +365,39 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
     topv[r] = bv;
     topi[r] = bi;
   }
+}
+
+// The gate of choice j (TOPK: softmax over the kept k; SWITCH: the full
+// softmax at the argmax).
+__device__ __forceinline__ float gate_of(int j, int k, int mode, const float *topv, float mx,
+                                         float se) {
+  if (mode == MOE_GATE_SWITCH) return expf(topv[0] - mx) / se;
+  float z = 0.f;
+  for (int q = 0; q < k; ++q) z += expf(topv[q] - topv[0]);
+  return expf(topv[j] - topv[0]) / z;
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256)
+k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__restrict__ idx,
+         float *__restrict__ gate, float *__restrict__ thr, float *__restrict__ rowstat) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float *h = H + (size_t)t * E;
+  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? h[e] : -INFINITY;
+  }
+  float topv[kMaxK + 1], mx, se;
+  int topi[kMaxK + 1];
+  warp_topk<VPL>(v, E, k, lane, topv, topi, mx, se);
   if (lane == 0) {
-    if (mode == MOE_GATE_SWITCH) {
-      idx[t] = topi[0];
-      gate[t] = expf(topv[0] - mx) / se;
-    } else {
-      float z = 0.f;
-      for (int j = 0; j < k; ++j) z += expf(topv[j] - topv[0]);
-      for (int j = 0; j < k; ++j) {
-        idx[(size_t)t * k + j] = topi[j];
-        gate[(size_t)t * k + j] = expf(topv[j] - topv[0]) / z;
-      }
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = topi[j];
+      gate[(size_t)t * k + j] = gate_of(j, k, mode, topv, mx, se);
     }
     thr[2 * (size_t)t] = topv[k - 1];
     thr[2 * (size_t)t + 1] = k < E ? topv[k] : -INFINITY;
@@ -484,53 +494,158 @@ k_aux_partials(int T, int E, int k, int tb, int noisy, const float *__restrict__
   }
 }
 
-// Finalize, one launch. Each warp sums one expert's partials over the token
-// blocks (lane l takes blocks l, l+32, ... in order, then a fixed xor
-// butterfly; fp64), writing aux_vec [4][E] = importance, load, f, Pbar. The
-// block that finishes last (a ticket in the status word, reset by that block)
-// then computes CV^2 of importance and load (population variance) and the
-// Switch loss 0.01 * E * sum(f * Pbar) in a fixed order.
+// Selection and balancing partials in one pass, for E <= 256: the warp that
+// selects token t's experts goes on to add t's contributions to the expert
+// sums its lanes own, so H, the chosen experts and the gates are read once.
+// Token order, warp order and the block sums are those of k_aux_partials, so
+// the partials are bit-identical to the two-kernel path.
+template <int VPL>
+__global__ void __launch_bounds__(kAuxWarps * 32)
+k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__restrict__ c,
+             const float *__restrict__ sg, const float *__restrict__ H,
+             int32_t *__restrict__ idx, float *__restrict__ gate, float *__restrict__ thr,
+             float *__restrict__ rowstat, float *__restrict__ partials) {
+  constexpr int CH = 32 * VPL;
+  __shared__ float red[kAuxWarps][4][CH];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  const int t0 = b * tb, t1 = min(T, t0 + tb);
+  float acc[4][VPL];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) acc[q][i] = 0.f;
+  for (int t = t0 + warp; t < t1; t += kAuxWarps) {
+    float v[VPL], cv[VPL], sv[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      const size_t o = (size_t)t * E + (e < E ? e : 0);
+      v[i] = e < E ? H[o] : -INFINITY;
+      cv[i] = noisy ? c[o] : 0.f;
+      sv[i] = noisy ? sg[o] : 0.f;
+    }
+    float topv[kMaxK + 1], mx, se;
+    int topi[kMaxK + 1];
+    warp_topk<VPL>(v, E, k, lane, topv, topi, mx, se);
+    float g[kMaxK];
+    for (int j = 0; j < k; ++j) g[j] = gate_of(j, k, mode, topv, mx, se);
+    const float th0 = topv[k - 1], th1 = k < E ? topv[k] : -INFINITY;
+    if (lane == 0) {
+      for (int j = 0; j < k; ++j) {
+        idx[(size_t)t * k + j] = topi[j];
+        gate[(size_t)t * k + j] = g[j];
+      }
+      thr[2 * (size_t)t] = th0;
+      thr[2 * (size_t)t + 1] = th1;
+      rowstat[2 * (size_t)t] = mx;
+      rowstat[2 * (size_t)t + 1] = se;
+    }
+    const float inv_se = 1.f / se;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= E) continue;
+      float gi = 0.f;
+      bool in = false;
+      for (int j = 0; j < k; ++j)
+        if (topi[j] == e) {
+          in = true;
+          gi = g[j];
+        }
+      acc[0][i] += gi;
+      float p;
+      if (k == E) {
+        p = 1.f;
+      } else if (sv[i] == 0.f) {
+        p = in ? 1.f : 0.f;
+      } else {
+        const float u = (cv[i] - (in ? th1 : th0)) / sv[i];
+        p = 0.5f * erfcf(-u * 0.70710678118654752f);
+      }
+      acc[1][i] += p;
+      if (topi[0] == e) acc[2][i] += 1.f;
+      acc[3][i] += expf(v[i] - mx) * inv_se;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) red[warp][q][lane + 32 * i] = acc[q][i];
+  __syncthreads();
+  for (int vv = threadIdx.x; vv < 4 * CH; vv += blockDim.x) {
+    const int q = vv / CH, e = vv % CH;
+    if (e >= E) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAuxWarps; ++w) sum += red[w][q][e];
+    partials[((size_t)b * 4 + q) * E + e] = sum;
+  }
+}
+
+// Finalize, one launch. A block (E <= 256) or a warp sums each expert's
+// partials over the token blocks (thread j takes blocks j, j+G, ... in order;
+// fp64; then a fixed butterfly), writing aux_vec [4][E] = importance, load,
+// f, Pbar. The block that
+// finishes last (a ticket in the status word, reset by that block) then
+// computes CV^2 of importance and load (population variance) and the Switch
+// loss 0.01 * E * sum(f * Pbar) in a fixed order.
 constexpr int kFinThreads = 256;
 
+// Sum over the block in a fixed order (xor butterfly in each warp, then the
+// warp totals in warp order): identical on every run.
 __device__ double block_sum_fixed(double v, double *sh) {
-  sh[threadIdx.x] = v;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[warp] = v;
   __syncthreads();
-  for (int s = kFinThreads / 2; s > 0; s >>= 1) {
-    if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
-    __syncthreads();
-  }
-  double r = sh[0];
+  double r = 0;
+#pragma unroll
+  for (int w = 0; w < kFinThreads / 32; ++w) r += sh[w];
   __syncthreads();
   return r;
 }
 
+// G threads sum one expert's partials: the whole block (G = 256, few experts)
+// or one warp (G = 32, eight experts per block).
+template <int G>
 __global__ void __launch_bounds__(kFinThreads)
 k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials,
                double *__restrict__ aux_vec, float *__restrict__ importance,
                float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
   __shared__ double sh[kFinThreads];
   __shared__ int last;
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * (kFinThreads / 32) + (threadIdx.x >> 5);
+  constexpr int PER = kFinThreads / G;  // experts per block
+  const int e = blockIdx.x * PER + threadIdx.x / G;
+  const int j = threadIdx.x % G;
+  double v[4] = {0, 0, 0, 0};
   if (e < E) {
-    double v[4] = {0, 0, 0, 0};
-    for (int b = lane; b < nb; b += 32) {
-      const float *q = partials + (size_t)b * 4 * E;
+    for (int b = j; b < nb; b += G) {
+      const float *q = partials + (size_t)b * 4 * E + e;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] += q[(size_t)i * E + e];
+      for (int i = 0; i < 4; ++i) v[i] += q[(size_t)i * E];
     }
+  }
+  double tot[4];
+  if (G == kFinThreads) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) tot[i] = block_sum_fixed(v[i], sh);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
       for (int o = 16; o; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
-    if (lane == 0) {
-      aux_vec[e] = v[0];
-      aux_vec[E + e] = v[1];
-      aux_vec[2 * E + e] = v[2] / T;
-      aux_vec[3 * E + e] = v[3] / T;
-      if (importance) importance[e] = (float)v[0];
-      if (load) load[e] = (float)v[1];
+      tot[i] = v[i];
     }
+  }
+  if (j == 0 && e < E) {
+    aux_vec[e] = tot[0];
+    aux_vec[E + e] = tot[1];
+    aux_vec[2 * E + e] = tot[2] / T;
+    aux_vec[3 * E + e] = tot[3] / T;
+    if (importance) importance[e] = (float)tot[0];
+    if (load) load[e] = (float)tot[1];
   }
   __threadfence();
   __syncthreads();
@@ -624,7 +739,10 @@ cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, f
   return cudaGetLastError();
 }
 
-int aux_token_block(int E) { return E <= 64 ? 64 : (E <= 256 ? 128 : 256); }
+// Tokens per partial-sum block: small blocks (two tokens per warp) where the
+// fused selection kernel runs (two tokens per warp), so it has enough CTAs;
+// larger ones for E > 256.
+int aux_token_block(int E) { return E <= 256 ? 16 : 256; }
 
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
                                 const float *sigma, const float *H, const float *rowstat,
@@ -644,12 +762,34 @@ cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *
   return cudaGetLastError();
 }
 
+cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c, const float *sigma,
+                              const float *H, int32_t *idx, float *gate, float *thr,
+                              float *rowstat, float *partials, int n_blocks, cudaStream_t s) {
+  const int tb = aux_token_block(cfg.E);
+  const int vpl = cfg.E <= 32 ? 1 : (cfg.E <= 64 ? 2 : (cfg.E <= 128 ? 4 : 8));
+#define MOE_SELAUX(V)                                                                           \
+  k_select_aux<V><<<n_blocks, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, cfg.gate_mode, tb,   \
+                                                       noisy ? 1 : 0, c, sigma, H, idx, gate, thr, \
+                                                       rowstat, partials)
+  if (vpl == 1) MOE_SELAUX(1);
+  else if (vpl == 2) MOE_SELAUX(2);
+  else if (vpl == 4) MOE_SELAUX(4);
+  else MOE_SELAUX(8);
+#undef MOE_SELAUX
+  return cudaGetLastError();
+}
+
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
                                 float *out3, float *importance, float *load, double *aux_vec,
                                 DeviceStatus *st, cudaStream_t s) {
-  const int per_block = kFinThreads / 32;
-  k_aux_finalize<<<(cfg.E + per_block - 1) / per_block, kFinThreads, 0, s>>>(
-      cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
+  // Many partial rows (16-token blocks, E <= 256): a block per expert; few
+  // (256-token blocks): a warp per expert.
+  if (cfg.E <= 256)
+    k_aux_finalize<kFinThreads><<<cfg.E, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials,
+                                                              aux_vec, importance, load, out3, st);
+  else
+    k_aux_finalize<32><<<(cfg.E + 7) / 8, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials,
+                                                               aux_vec, importance, load, out3, st);
   return cudaGetLastError();
 }
 

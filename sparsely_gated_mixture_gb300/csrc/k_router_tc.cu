@@ -10,12 +10,14 @@
 //
 // k_router_split builds the pieces, transposed so that each B row is one
 // output column (K contiguous): columns 2e and 2e+1 are expert e's clean and
-// noise logits (noisy gate) or column e is expert e (no noise), each plane
-// padded with zero rows to a whole number of column tiles.
+// noise logits (noisy gate) or column e is expert e (no noise); each block of
+// BNR columns holds its hi, mid and lo rows back to back, and the columns are
+// padded with zero rows to a whole number of blocks.
 // k_router_tc is one persistent CTA per SM: a TMA warp loads x [128 tokens x
-// 64 K] and the three [BNR columns x 64 K] B pieces per stage (BNR <= 64),
-// one lane issues 3 x 4 tcgen05.mma (M=128, N=BNR, K=16, both operands
-// K-major, 128B swizzle) into one of two TMEM accumulators, and eight epilogue
+// 64 K] and the [3*BNR rows x 64 K] B box (the three pieces) per stage
+// (BNR <= 64), one lane issues 4 tcgen05.mma (M=128, N=3*BNR, K=16, both
+// operands K-major, 128B swizzle) into one of two TMEM accumulators, whose
+// three BNR-wide sections are summed per column, and eight epilogue
 // warps (two per TMEM lane quadrant) turn each token's columns into c = acc + b, sigma = Softplus(z) and
 // H = c + noise * sigma, staged in shared memory so that noise is read and
 // c, sigma, H [T, E] fp32 are written a row segment at a time.
@@ -42,7 +44,10 @@ __device__ __forceinline__ float softplus_r(float z) {
 }
 
 // grid (ceil(d/32), ceil(NCP/32)), block (32, 8): a 32 x 32 transpose tile.
-__global__ void k_router_split(int d, int E, int noisy, int NC, int NCP,
+// Output rows are grouped per column block of BNR: block b holds hi rows,
+// then mid rows, then lo rows of its BNR columns, so one TMA box of 3*BNR rows
+// brings all three pieces of a block.
+__global__ void k_router_split(int d, int E, int noisy, int NC, int NCP, int BNR,
                                const float *__restrict__ Wg, const float *__restrict__ Wn,
                                __nv_bfloat16 *__restrict__ B) {
   __shared__ float tile[32][33];
@@ -67,9 +72,10 @@ __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP,
     const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
     const float r2 = r1 - __bfloat162float(mid);
     const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-    B[((size_t)0 * NCP + n) * d + k] = hi;
-    B[((size_t)1 * NCP + n) * d + k] = mid;
-    B[((size_t)2 * NCP + n) * d + k] = lo;
+    const size_t row0 = (size_t)(n / BNR) * 3 * BNR + (n % BNR);
+    B[(row0 + 0 * (size_t)BNR) * d + k] = hi;
+    B[(row0 + 1 * (size_t)BNR) * d + k] = mid;
+    B[(row0 + 2 * (size_t)BNR) * d + k] = lo;
   }
 }
 
@@ -81,14 +87,15 @@ constexpr int EPI_BYTES = kREpiWarps * 3 * kEpiTile * 4;  // 8 warps x 3 tiles =
 template <int BNR>
 struct RCfg {
   static constexpr int A_BYTES = RBM * RBK * 2;  // 16 KB
-  static constexpr int P_BYTES = BNR * RBK * 2;  // one piece
-  static constexpr int STAGE = A_BYTES + 3 * P_BYTES;
+  static constexpr int NB = 3 * BNR;              // MMA N: the three pieces side by side
+  static constexpr int B_BYTES = NB * RBK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int FIT = (227 * 1024 - 1024 - EPI_BYTES - 256) / STAGE;
   static constexpr int STAGES = FIT > 8 ? 8 : FIT;
-  static constexpr int TMEM_COLS = 2 * BNR < 32 ? 32 : 2 * BNR;
-  // kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = BNR.
+  static constexpr int TMEM_COLS = 2 * NB <= 64 ? 64 : (2 * NB <= 128 ? 128 : (2 * NB <= 256 ? 256 : 512));
+  // kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 128, N = 3*BNR.
   static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
-                                    ((uint32_t)(BNR >> 3) << 17) | ((uint32_t)(RBM >> 4) << 24);
+                                    ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(RBM >> 4) << 24);
   static constexpr size_t SMEM =
       1024 + (size_t)STAGES * STAGE + EPI_BYTES + (2 * STAGES + 5) * 8 + 8;
   static_assert(STAGES >= 2, "router tile too wide for two pipeline stages");
@@ -223,10 +230,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           uint8_t *st = smem + s * C::STAGE;
           mbar_expect_tx(&full[s], C::STAGE);
           tma_load_2d(st, &tmA, &full[s], kb * RBK, mb * RBM);
-#pragma unroll
-          for (int q = 0; q < 3; ++q)
-            tma_load_2d(st + C::A_BYTES + q * C::P_BYTES, &tmB, &full[s], kb * RBK,
-                        q * p.NCP + nb * BNR);
+          tma_load_2d(st + C::A_BYTES, &tmB, &full[s], kb * RBK, nb * C::NB);
         }
       }
       const uint32_t issued = it;
@@ -244,7 +248,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const uint32_t use = (uint32_t)(local >> 1);
         if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 22, p.wait_ns)) break;
         tc_fence_after();
-        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BNR);
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * C::NB);
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (it / C::STAGES) & 1u;
@@ -257,11 +261,8 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
           for (int kk = 0; kk < RBK / 16; ++kk) {
             const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-              const uint64_t bd = sdesc(a0 + C::A_BYTES + q * C::P_BYTES + kk * 32, 16, 1024);
-              umma_r<BNR>(tmem_d, ad, bd, (kb | kk | q) ? 1u : 0u);
-            }
+            const uint64_t bd = sdesc(a0 + C::A_BYTES + kk * 32, 16, 1024);
+            umma_r<BNR>(tmem_d, ad, bd, (kb | kk) ? 1u : 0u);
           }
           umma_commit(&empty[s]);
         }
@@ -285,7 +286,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_fence_after();
       const int t0 = mb * RBM + quad * 32;
       const uint32_t lane_addr =
-          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BNR);
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * C::NB);
       float *stg = staging + (size_t)(warp - 2) * 3 * kEpiTile;
       const int t = t0 + lane;
       const int nchunks = (min(p.NC - nb * BNR, BNR) + 15) / 16;
@@ -300,15 +301,23 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
         for (int j = 0; j < 8; ++j) nz[j] = nz_next[j];
         if (p.noisy && c16 + 2 < nchunks) load_noise8(p, t, (n + 32) >> 1, nz_next);
-        uint32_t v[16];
-        tmem_ld16(lane_addr + (uint32_t)(c16 * 16), v);
+        // Column j of the block is hi[j] + (mid[j] + lo[j]), from the three
+        // BNR-wide sections of the accumulator.
+        uint32_t vh[16], vm[16], vl[16];
+        tmem_ld16(lane_addr + (uint32_t)(c16 * 16), vh);
+        tmem_ld16(lane_addr + (uint32_t)(BNR + c16 * 16), vm);
+        tmem_ld16(lane_addr + (uint32_t)(2 * BNR + c16 * 16), vl);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
         float cv[16], zv[16];
         int e0, ne;
         if (p.noisy) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            cv[j] = __uint_as_float(v[2 * j]);
-            zv[j] = __uint_as_float(v[2 * j + 1]);
+            cv[j] = v[2 * j];
+            zv[j] = v[2 * j + 1];
           }
 #pragma unroll
           for (int j = 8; j < 16; ++j) cv[j] = zv[j] = 0.f;
@@ -317,7 +326,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            cv[j] = __uint_as_float(v[j]);
+            cv[j] = v[j];
             zv[j] = 0.f;
           }
           e0 = n;
@@ -351,13 +360,13 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   const int n_blocks = (NC + BNR - 1) / BNR;
   const int NCP = n_blocks * BNR;
   dim3 sg_grid((c.d + 31) / 32, (NCP + 31) / 32);
-  k_router_split<<<sg_grid, dim3(32, 8), 0, s>>>(c.d, c.E, noisy, NC, NCP, Wg, Wn,
+  k_router_split<<<sg_grid, dim3(32, 8), 0, s>>>(c.d, c.E, noisy, NC, NCP, BNR, Wg, Wn,
                                                  static_cast<__nv_bfloat16 *>(bsplit));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb;
   if (!make_map(&ta, x, (uint64_t)c.T, (uint64_t)c.d, RBM) ||
-      !make_map(&tb, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, BNR))
+      !make_map(&tb, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, 3 * BNR))
     return cudaErrorInvalidValue;
   RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, noise, bias, cc, sg, H, st,
             wait_limit_ns()};

@@ -111,9 +111,11 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
   if (bad) record_error(st, MOE_ERR_NONFINITE, (long long)t);
 }
 
-// Combine for bf16 rows with d % 8 == 0: each lane handles 8 consecutive
-// elements per step (one 16-byte load of x and of y, two of each kept Z row),
-// two steps in flight.
+// Combine for bf16 rows with d % 8 == 0: each lane handles NG groups of 8
+// consecutive elements per step (16-byte loads of x and y, 32 bytes of each
+// kept Z row per group), with every load of the step issued first; two groups
+// when k <= 2, one when k <= 4 (register budget).
+template <int KM, int NG>  // at most KM choices per token; NG 8-element groups per lane-step
 __global__ void __launch_bounds__(kRowWarps * 32)
 k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ x,
                  const float *__restrict__ zbuf, const int32_t *__restrict__ pos,
@@ -141,30 +143,54 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
   uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)t * d);
   const int nv = d / 8;
   bool bad = false;
-  for (int v = lane; v < nv; v += 32) {
-    const uint4 xv = xr[v];
-    const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xv);
-    float acc[8];
+  // NG 8-element groups per lane per step, all loads issued before the sums.
+  for (int v0 = lane; v0 < nv; v0 += 32 * NG) {
+    const int v1 = v0 + 32;
+    const bool has1 = NG > 1 && v1 < nv;
+    const uint4 xv0 = xr[v0];
+    const uint4 xv1 = has1 ? xr[v1] : make_uint4(0, 0, 0, 0);
+    float4 z[KM][2 * NG];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f = __bfloat1622float2(xb[q]);
-      acc[2 * q] = f.x;
-      acc[2 * q + 1] = f.y;
+    for (int i = 0; i < KM; ++i) {
+      if (i >= nr) break;
+      const float4 *zr = reinterpret_cast<const float4 *>(zbuf + (size_t)rows[i] * d);
+      z[i][0] = zr[2 * v0];
+      z[i][1] = zr[2 * v0 + 1];
+      if constexpr (NG > 1) {
+        if (has1) {
+          z[i][2] = zr[2 * v1];
+          z[i][3] = zr[2 * v1 + 1];
+        }
+      }
     }
-    for (int i = 0; i < nr; ++i) {
-      const float4 *zr = reinterpret_cast<const float4 *>(zbuf + (size_t)rows[i] * d) + 2 * v;
-      const float4 z0 = zr[0], z1 = zr[1];
-      acc[0] += z0.x; acc[1] += z0.y; acc[2] += z0.z; acc[3] += z0.w;
-      acc[4] += z1.x; acc[5] += z1.y; acc[6] += z1.z; acc[7] += z1.w;
-    }
-    uint4 out;
-    __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&out);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      bad |= !isfinite(acc[2 * q]) || !isfinite(acc[2 * q + 1]);
-      ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    for (int h = 0; h < NG; ++h) {
+      if (h == 1 && !has1) break;
+      const uint4 xv = h ? xv1 : xv0;
+      const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&xv);
+      float acc[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(xb[q]);
+        acc[2 * q] = f.x;
+        acc[2 * q + 1] = f.y;
+      }
+#pragma unroll
+      for (int i = 0; i < KM; ++i) {
+        if (i >= nr) break;
+        const float4 a0 = z[i][2 * h], a1 = z[i][2 * h + 1];
+        acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+        acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
+      }
+      uint4 out;
+      __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&out);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        bad |= !isfinite(acc[2 * q]) || !isfinite(acc[2 * q + 1]);
+        ob[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+      }
+      yr[h ? v1 : v0] = out;
     }
-    yr[v] = out;
   }
   if (bad) record_error(st, MOE_ERR_NONFINITE, (long long)t);
 }
@@ -200,10 +226,14 @@ cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zb
   if (cfg.act_dtype == MOE_BF16) {
     auto xp = (const __nv_bfloat16 *)x;
     auto yp = (__nv_bfloat16 *)y;
-    if (cfg.d % 8 == 0)
-      k_combine_bf16x8<<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos,
-                                                       keep, idx, offset, yp, st);
-    else if (v4)
+    if (cfg.d % 8 == 0 && cfg.k <= 4) {
+      if (cfg.k <= 2)
+        k_combine_bf16x8<2, 2><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
+                                                               zbuf, pos, keep, idx, offset, yp, st);
+      else
+        k_combine_bf16x8<4, 1><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
+                                                               zbuf, pos, keep, idx, offset, yp, st);
+    } else if (v4)
       k_combine<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, s>>>(
           cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
     else

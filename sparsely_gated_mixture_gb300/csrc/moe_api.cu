@@ -97,10 +97,15 @@ static int gate_impl(const moe_config &c, const void *x, const float *Wg, const 
   float *rs = ws_at<float>(ws, L.rowstat);
   MOE_CUDA(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
   MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, ws_at<char>(ws, L.bsplit), st, s));
-  MOE_CUDA(launch_select(c, H, idx, gate, thr, rs, st, s));
-  if (partials)
-    MOE_CUDA(launch_aux_partials(c, Wn != nullptr, cc, sg, H, rs, idx, gate, thr,
-                                 ws_at<float>(ws, L.partials), L.n_aux_blocks, s));
+  if (partials && c.E <= 256) {
+    MOE_CUDA(launch_select_aux(c, Wn != nullptr, cc, sg, H, idx, gate, thr, rs,
+                               ws_at<float>(ws, L.partials), L.n_aux_blocks, s));
+  } else {
+    MOE_CUDA(launch_select(c, H, idx, gate, thr, rs, st, s));
+    if (partials)
+      MOE_CUDA(launch_aux_partials(c, Wn != nullptr, cc, sg, H, rs, idx, gate, thr,
+                                   ws_at<float>(ws, L.partials), L.n_aux_blocks, s));
+  }
   return MOE_OK;
 }
 

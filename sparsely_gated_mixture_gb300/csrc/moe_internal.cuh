@@ -70,6 +70,10 @@ cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, in
                                 float *out3, float *importance, float *load, double *aux_vec,
                                 DeviceStatus *st, cudaStream_t s);
 int aux_token_block(int E);  // tokens per partial-sum block of the balancing sums
+// Selection and balancing partials in one kernel (E <= 256).
+cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c, const float *sigma,
+                              const float *H, int32_t *idx, float *gate, float *thr,
+                              float *rowstat, float *partials, int n_blocks, cudaStream_t s);
 
 // k_router_tc.cu: the router as three bf16 tensor-core GEMMs (exact split of W).
 bool router_tc_supported(const moe_config &cfg);
