@@ -13,6 +13,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <type_traits>
+
 namespace moe {
 namespace {
 
@@ -320,13 +322,15 @@ cudaError_t router_vec_dispatch(const moe_config &cfg, const void *x, const floa
 
 // ----------------------------------------------------------------------------- selection
 // One warp per token; expert e lives in lane e % 32, slot e / 32. On return
-// every lane holds the same results: topv/topi = the k+1 (k if k == E) largest
-// values in (value desc, index asc) order, mx = max, se = sum of exp(v - mx).
-// A NaN never wins; if only NaNs remain a round yields E (out of range),
-// which the consumers reject. The router has already flagged the NaN.
+// lane r (r < k+1, or k if k == E) holds the r-th pick (myv, myi) of the k+1
+// largest values in (value desc, index asc) order, and every lane holds
+// mx = max and se = sum of exp(v - mx). Results stay in registers: a pick is
+// read from its lane with a shuffle. A NaN never wins; if only NaNs remain a
+// round yields E (out of range), which the consumers reject. The router has
+// already flagged the NaN.
 template <int VPL>
 __device__ __forceinline__ void warp_topk(const float (&v)[VPL], int E, int k, int lane,
-                                          float *topv, int *topi, float &mx, float &se) {
+                                          float &myv, int &myi, float &mx, float &se) {
   mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) mx = fmaxf(mx, v[i]);
@@ -362,25 +366,137 @@ __device__ __forceinline__ void warp_topk(const float (&v)[VPL], int E, int k, i
       }
     }
     if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    topv[r] = bv;
-    topi[r] = bi;
+    if (lane == r) {
+      myv = bv;
+      myi = bi;
+    }
   }
 }
 
-// The gate of choice j (TOPK: softmax over the kept k; SWITCH: the full
-// softmax at the argmax).
-__device__ __forceinline__ float gate_of(int j, int k, int mode, const float *topv, float mx,
-                                         float se) {
-  if (mode == MOE_GATE_SWITCH) return expf(topv[0] - mx) / se;
+// The same results as warp_topk, for wide rows (VPL >= 16), by a threshold:
+// tau = the R-th largest of the 32 lanes' maxima (R = rounds). R distinct
+// values are >= tau, so the R-th largest value overall is >= tau and every
+// member of the top R is a candidate (value >= tau). The candidates (rarely
+// more than a handful) are packed into the warp's 32-entry scratch, one per
+// lane, and R rounds of a warp arg-max pick them in (value desc, index asc)
+// order. Returns false, having written nothing, when tau is -inf or there are
+// more than 32 candidates (heavy ties); the caller then runs warp_topk. se is
+// summed with the fast exponential here (relative error ~1e-6).
+template <int VPL>
+__device__ __forceinline__ bool warp_topk_thresh(const float (&v)[VPL], int E, int k, int lane,
+                                                 float2 *scratch, float &myv, int &myi,
+                                                 float &mx, float &se) {
+  float m = -INFINITY;  // fmaxf drops NaN
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) m = fmaxf(m, v[i]);
+  mx = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const int rounds = k < E ? k + 1 : k;
+  float cur = m, tau = -INFINITY;
+  for (int r = 0; r < rounds; ++r) {
+    float w = cur;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+    tau = w;
+    const unsigned hit = __ballot_sync(0xffffffffu, cur == w);
+    if (lane == __ffs(hit) - 1) cur = -INFINITY;
+  }
+  if (tau == -INFINITY) return false;
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) n += (lane + 32 * i < E && v[i] >= tau) ? 1 : 0;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total > 32) return false;
+  se = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) se += __expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+  int o = incl - n;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && v[i] >= tau) scratch[o++] = make_float2(v[i], __int_as_float(e));
+  }
+  __syncwarp();
+  float cv = -INFINITY;
+  int ci = E;
+  if (lane < total) {
+    const float2 q = scratch[lane];
+    cv = q.x;
+    ci = __float_as_int(q.y);
+  }
+  __syncwarp();  // scratch is free for the warp's next token
+  for (int r = 0; r < rounds; ++r) {
+    float bv = cv;
+    int bi = ci;
+#pragma unroll
+    for (int o2 = 16; o2; o2 >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o2);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o2);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == r) {
+      myv = bv;
+      myi = bi;
+    }
+    if (ci == bi) {
+      cv = -INFINITY;
+      ci = E;
+    }
+  }
+  return true;
+}
+
+// The gate held by lane j < k (TOPK: softmax over the kept k, the
+// normaliser summed in pick order; SWITCH: the full-softmax probability of the
+// argmax). Every lane takes part; lanes >= k get 0.
+__device__ __forceinline__ float warp_gate(float myv, int k, int mode, float mx, float se,
+                                           int lane) {
+  const float v0 = __shfl_sync(0xffffffffu, myv, 0);
+  if (mode == MOE_GATE_SWITCH) return lane == 0 ? expf(v0 - mx) / se : 0.f;
+  const float ej = lane < k ? expf(myv - v0) : 0.f;
   float z = 0.f;
-  for (int q = 0; q < k; ++q) z += expf(topv[q] - topv[0]);
-  return expf(topv[j] - topv[0]) / z;
+  for (int q = 0; q < k; ++q) z += __shfl_sync(0xffffffffu, ej, q);
+  return lane < k ? ej / z : 0.f;
+}
+
+// Token t's selection outputs: the k picks and gates from lanes 0..k-1, the
+// thresholds (k-th and (k+1)-th values) and the row statistics from lane 0.
+__device__ __forceinline__ void store_selection(size_t t, int E, int k, int lane, float myv,
+                                                int myi, float g, float th0, float th1, float mx,
+                                                float se, int32_t *__restrict__ idx,
+                                                float *__restrict__ gate, float *__restrict__ thr,
+                                                float *__restrict__ rowstat) {
+  if (lane < k) {
+    idx[t * k + lane] = myi;
+    gate[t * k + lane] = g;
+  }
+  if (lane == 0) {
+    thr[2 * t] = th0;
+    thr[2 * t + 1] = th1;
+    rowstat[2 * t] = mx;
+    rowstat[2 * t + 1] = se;
+  }
 }
 
 template <int VPL>
 __global__ void __launch_bounds__(256)
 k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__restrict__ idx,
          float *__restrict__ gate, float *__restrict__ thr, float *__restrict__ rowstat) {
+  __shared__ float2 scratch[8][32];
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -391,106 +507,157 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
     const int e = lane + 32 * i;
     v[i] = e < E ? h[e] : -INFINITY;
   }
-  float topv[kMaxK + 1], mx, se;
-  int topi[kMaxK + 1];
-  warp_topk<VPL>(v, E, k, lane, topv, topi, mx, se);
-  if (lane == 0) {
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = topi[j];
-      gate[(size_t)t * k + j] = gate_of(j, k, mode, topv, mx, se);
-    }
-    thr[2 * (size_t)t] = topv[k - 1];
-    thr[2 * (size_t)t + 1] = k < E ? topv[k] : -INFINITY;
-    rowstat[2 * (size_t)t] = mx;
-    rowstat[2 * (size_t)t + 1] = se;
-  }
+  float myv = -INFINITY, mx, se;
+  int myi = E;
+  if (VPL < 16 ||
+      !warp_topk_thresh<VPL>(v, E, k, lane, scratch[threadIdx.x >> 5], myv, myi, mx, se))
+    warp_topk<VPL>(v, E, k, lane, myv, myi, mx, se);
+  const float g = warp_gate(myv, k, mode, mx, se, lane);
+  const float th0 = __shfl_sync(0xffffffffu, myv, k - 1);
+  const float thk = __shfl_sync(0xffffffffu, myv, k & 31);
+  store_selection(t, E, k, lane, myv, myi, g, th0, k < E ? thk : -INFINITY, mx, se, idx, gate, thr,
+                  rowstat);
+}
+
+// Phi(u), the standard normal CDF, as erfc(-u / sqrt 2) / 2. erfc(z), z >= 0,
+// is the Chebyshev-fitted form of Numerical Recipes (Press et al., 2nd ed.,
+// section 6.2, "erfcc"): t exp(-z^2 + P(t)), t = 1 / (1 + z/2), P of degree 9,
+// fractional error below 1.2e-7 for every z; erfc(-z) = 2 - erfc(z). In fp32,
+// with z^2 compensated and the fast exponential, the relative error is about
+// 1e-6 wherever Phi > 1e-7, far inside the tolerance of the balancing sums.
+__device__ __forceinline__ float normal_cdf(float u) {
+  const float w = -u * 0.70710678118654752f;
+  const float z = fabsf(w);
+  const float t = __fdividef(1.f, fmaf(0.5f, z, 1.f));
+  float p = 0.17087277f;
+  p = fmaf(t, p, -0.82215223f);
+  p = fmaf(t, p, 1.48851587f);
+  p = fmaf(t, p, -1.13520398f);
+  p = fmaf(t, p, 0.27886807f);
+  p = fmaf(t, p, -0.18628806f);
+  p = fmaf(t, p, 0.09678418f);
+  p = fmaf(t, p, 0.37409196f);
+  p = fmaf(t, p, 1.00002368f);
+  p = fmaf(t, p, -1.26551223f);
+  const float zz = z * z;
+  const float ez = fmaf(z, z, -zz);  // z^2 = zz + ez exactly
+  const float half_erfc = 0.5f * t * __expf((p - zz) - ez);
+  return w >= 0.f ? half_erfc : 1.f - half_erfc;
 }
 
 // ----------------------------------------------------------------------------- balancing partials
-// Block (token block b, expert chunk): warp w walks tokens t0+w, t0+w+8, ...
-// of the block in order; lane l owns experts chunk0 + l + 32 i. The eight
-// warps' sums are added in warp order, so every partial is run-to-run
-// identical. partials layout: [block][4][E] = importance, load, first-choice
-// count, sum of Softmax(H).
+// Partials layout: [token block][4][E] = importance, load, first-choice count,
+// sum of Softmax(H), each a sum over the block's tokens.
 constexpr int kAuxWarps = 8;
-constexpr int kAuxMaxK = 16;
 
-template <int VPL>
-__global__ void __launch_bounds__(kAuxWarps * 32)
-k_aux_partials(int T, int E, int k, int tb, int noisy, const float *__restrict__ c,
-               const float *__restrict__ sg, const float *__restrict__ H,
-               const float *__restrict__ rowstat, const int32_t *__restrict__ idx,
-               const float *__restrict__ gate, const float *__restrict__ thr,
-               float *__restrict__ partials) {
-  constexpr int CH = 32 * VPL;
-  __shared__ float red[kAuxWarps][4][CH];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.x, e0 = blockIdx.y * CH;
-  const int t0 = b * tb, t1 = min(T, t0 + tb);
-  float acc[4][VPL];
+// E > 256: the column form. Partial row b covers the contiguous tokens
+// [b T / P, (b+1) T / P), P = aux_rows(T, E): at most kColRows, one wave of
+// four blocks on each of 152 SMs, so every block has an equal share. Thread j
+// owns V consecutive experts (e0 = chunk start + V j) and walks its block's
+// tokens in order, so each sum runs in one thread in token order (identical on
+// every run). The per-token scalars (thresholds, row max, 1 / sum of
+// exponentials, chosen experts and gates) are staged in shared memory kColTB
+// tokens at a time; the c, sigma and H loads are coalesced across the block
+// (V = 4: one 16-byte load each).
+constexpr int kColThreads = 256;
+constexpr int kColTB = 64;
+constexpr int kColU = 2;  // tokens whose loads are in flight together
+constexpr int kColRows = 4 * 152;
+
+template <int V, int KM>  // KM >= k
+__global__ void __launch_bounds__(kColThreads, 4)
+k_aux_cols(int T, int E, int k, int noisy, int P, const float *__restrict__ c,
+           const float *__restrict__ sg, const float *__restrict__ H,
+           const float *__restrict__ rowstat, const int32_t *__restrict__ idx,
+           const float *__restrict__ gate, const float *__restrict__ thr,
+           float *__restrict__ partials) {
+  using VT = typename std::conditional<V == 4, float4, float>::type;
+  __shared__ float4 s_tok[kColTB];  // th0, th1, mx, 1/se
+  __shared__ int s_idx[kColTB][KM];
+  __shared__ float s_g[kColTB][KM];
+  const int b = blockIdx.x;
+  const int tb0 = (int)((long long)b * T / P), tb1 = (int)((long long)(b + 1) * T / P);
+  const int e0 = blockIdx.y * (kColThreads * V) + threadIdx.x * V;
+  const bool active = e0 < E;
+  float imp[V], ld[V], fc[V], ps[V];
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) acc[q][i] = 0.f;
-  for (int t = t0 + warp; t < t1; t += kAuxWarps) {
-    // All of this token's loads first, so they are in flight together.
-    const float th0 = thr[2 * (size_t)t], th1 = thr[2 * (size_t)t + 1];
-    const float mx = rowstat[2 * (size_t)t], inv_se = 1.f / rowstat[2 * (size_t)t + 1];
-    int chosen_e[kAuxMaxK];
-    float chosen_g[kAuxMaxK];
-#pragma unroll
-    for (int j = 0; j < kAuxMaxK; ++j) {
-      chosen_e[j] = j < k ? idx[(size_t)t * k + j] : -1;
-      chosen_g[j] = j < k ? gate[(size_t)t * k + j] : 0.f;
+  for (int q = 0; q < V; ++q) imp[q] = ld[q] = fc[q] = ps[q] = 0.f;
+  for (int t0 = tb0; t0 < tb1; t0 += kColTB) {
+    const int nt = min(kColTB, tb1 - t0);
+    __syncthreads();  // the previous chunk's scalars are no longer read
+    for (int i = threadIdx.x; i < nt; i += kColThreads) {
+      const size_t t = (size_t)t0 + i;
+      s_tok[i] = make_float4(thr[2 * t], thr[2 * t + 1], rowstat[2 * t], 1.f / rowstat[2 * t + 1]);
     }
-    float cv[VPL], sv[VPL], hv[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = e0 + lane + 32 * i;
-      const size_t o = (size_t)t * E + (e < E ? e : 0);
-      hv[i] = H[o];
-      cv[i] = noisy ? c[o] : 0.f;
-      sv[i] = noisy ? sg[o] : 0.f;
+    for (int i = threadIdx.x; i < nt * k; i += kColThreads) {
+      s_idx[i / k][i % k] = idx[(size_t)t0 * k + i];
+      s_g[i / k][i % k] = gate[(size_t)t0 * k + i];
     }
+    __syncthreads();
+    if (!active) continue;
+    for (int tt0 = 0; tt0 < nt; tt0 += kColU) {
+      VT hv[kColU], cv[kColU], sv[kColU];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = e0 + lane + 32 * i;
-      if (e >= E) continue;
-      float g = 0.f;
-      bool in = false;
-#pragma unroll
-      for (int j = 0; j < kAuxMaxK; ++j)
-        if (chosen_e[j] == e) {
-          in = true;
-          g = chosen_g[j];
+      for (int u = 0; u < kColU; ++u) {
+        const int tt = min(tt0 + u, nt - 1);  // a repeated row past the end is loaded, not used
+        const size_t o = ((size_t)t0 + tt) * E + e0;
+        hv[u] = *reinterpret_cast<const VT *>(H + o);
+        if (noisy) {
+          cv[u] = *reinterpret_cast<const VT *>(c + o);
+          sv[u] = *reinterpret_cast<const VT *>(sg + o);
         }
-      acc[0][i] += g;
-      float p;
-      if (k == E) {
-        p = 1.f;
-      } else if (sv[i] == 0.f) {
-        p = in ? 1.f : 0.f;
-      } else {
-        const float u = (cv[i] - (in ? th1 : th0)) / sv[i];
-        p = 0.5f * erfcf(-u * 0.70710678118654752f);
       }
-      acc[1][i] += p;
-      if (chosen_e[0] == e) acc[2][i] += 1.f;
-      acc[3][i] += expf(hv[i] - mx) * inv_se;
+#pragma unroll
+      for (int u = 0; u < kColU; ++u) {
+        const int tt = tt0 + u;
+        if (tt >= nt) break;
+        const float4 sc = s_tok[tt];
+        unsigned in = 0;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          if (j >= k) break;
+          const unsigned rel = (unsigned)(s_idx[tt][j] - e0);
+          if (rel < (unsigned)V) {
+            in |= 1u << rel;
+            const float g = s_g[tt][j];
+#pragma unroll
+            for (int q = 0; q < V; ++q)
+              if (rel == (unsigned)q) {
+                imp[q] += g;
+                if (j == 0) fc[q] += 1.f;
+              }
+          }
+        }
+        const float *h = reinterpret_cast<const float *>(&hv[u]);
+        const float *cc = reinterpret_cast<const float *>(&cv[u]);
+        const float *ss = reinterpret_cast<const float *>(&sv[u]);
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+          const bool isin = (in >> q) & 1u;
+          float p;
+          if (k == E) {
+            p = 1.f;
+          } else if (!noisy || ss[q] == 0.f) {
+            p = isin ? 1.f : 0.f;
+          } else {
+            p = normal_cdf(__fdividef(cc[q] - (isin ? sc.y : sc.x), ss[q]));
+          }
+          ld[q] += p;
+          ps[q] += __expf(h[q] - sc.z) * sc.w;
+        }
+      }
     }
   }
+  if (!active) return;
+  float *out = partials + (size_t)b * 4 * E + e0;
+  const float *acc[4] = {imp, ld, fc, ps};
 #pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int a = 0; a < 4; ++a) {
+    VT r;
+    float *rp = reinterpret_cast<float *>(&r);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) red[warp][q][lane + 32 * i] = acc[q][i];
-  __syncthreads();
-  for (int v = threadIdx.x; v < 4 * CH; v += blockDim.x) {
-    const int q = v / CH, el = v % CH, e = e0 + el;
-    if (e >= E) continue;
-    float sum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kAuxWarps; ++w) sum += red[w][q][el];
-    partials[((size_t)b * 4 + q) * E + e] = sum;
+    for (int q = 0; q < V; ++q) rp[q] = acc[a][q];
+    *reinterpret_cast<VT *>(out + (size_t)a * E) = r;
   }
 }
 
@@ -499,7 +666,7 @@ k_aux_partials(int T, int E, int k, int tb, int noisy, const float *__restrict__
 // sums its lanes own, so H, the chosen experts and the gates are read once.
 // Token order, warp order and the block sums are those of k_aux_partials, so
 // the partials are bit-identical to the two-kernel path.
-template <int VPL>
+template <int VPL, int KM>  // KM >= k: the chosen list kept in registers
 __global__ void __launch_bounds__(kAuxWarps * 32)
 k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__restrict__ c,
              const float *__restrict__ sg, const float *__restrict__ H,
@@ -525,21 +692,21 @@ k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__re
       cv[i] = noisy ? c[o] : 0.f;
       sv[i] = noisy ? sg[o] : 0.f;
     }
-    float topv[kMaxK + 1], mx, se;
-    int topi[kMaxK + 1];
-    warp_topk<VPL>(v, E, k, lane, topv, topi, mx, se);
-    float g[kMaxK];
-    for (int j = 0; j < k; ++j) g[j] = gate_of(j, k, mode, topv, mx, se);
-    const float th0 = topv[k - 1], th1 = k < E ? topv[k] : -INFINITY;
-    if (lane == 0) {
-      for (int j = 0; j < k; ++j) {
-        idx[(size_t)t * k + j] = topi[j];
-        gate[(size_t)t * k + j] = g[j];
-      }
-      thr[2 * (size_t)t] = th0;
-      thr[2 * (size_t)t + 1] = th1;
-      rowstat[2 * (size_t)t] = mx;
-      rowstat[2 * (size_t)t + 1] = se;
+    float myv = -INFINITY, mx, se;
+    int myi = E;
+    warp_topk<VPL>(v, E, k, lane, myv, myi, mx, se);
+    const float g = warp_gate(myv, k, mode, mx, se, lane);
+    const float th0 = __shfl_sync(0xffffffffu, myv, k - 1);
+    const float thk = __shfl_sync(0xffffffffu, myv, k & 31);
+    const float th1 = k < E ? thk : -INFINITY;
+    store_selection(t, E, k, lane, myv, myi, g, th0, th1, mx, se, idx, gate, thr, rowstat);
+    int ce[KM];
+    float cg[KM];
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      ce[j] = __shfl_sync(0xffffffffu, myi, j);
+      cg[j] = __shfl_sync(0xffffffffu, g, j);
+      if (j >= k) ce[j] = -1;
     }
     const float inv_se = 1.f / se;
 #pragma unroll
@@ -548,10 +715,11 @@ k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__re
       if (e >= E) continue;
       float gi = 0.f;
       bool in = false;
-      for (int j = 0; j < k; ++j)
-        if (topi[j] == e) {
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        if (ce[j] == e) {
           in = true;
-          gi = g[j];
+          gi = cg[j];
         }
       acc[0][i] += gi;
       float p;
@@ -560,11 +728,10 @@ k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__re
       } else if (sv[i] == 0.f) {
         p = in ? 1.f : 0.f;
       } else {
-        const float u = (cv[i] - (in ? th1 : th0)) / sv[i];
-        p = 0.5f * erfcf(-u * 0.70710678118654752f);
+        p = normal_cdf(__fdividef(cv[i] - (in ? th1 : th0), sv[i]));
       }
       acc[1][i] += p;
-      if (topi[0] == e) acc[2][i] += 1.f;
+      if (ce[0] == e) acc[2][i] += 1.f;
       acc[3][i] += expf(v[i] - mx) * inv_se;
     }
   }
@@ -583,103 +750,186 @@ k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__re
   }
 }
 
-// Finalize, one launch. A block (E <= 256) or a warp sums each expert's
-// partials over the token blocks (thread j takes blocks j, j+G, ... in order;
-// fp64; then a fixed butterfly), writing aux_vec [4][E] = importance, load,
-// f, Pbar. The block that
-// finishes last (a ticket in the status word, reset by that block) then
-// computes CV^2 of importance and load (population variance) and the Switch
-// loss 0.01 * E * sum(f * Pbar) in a fixed order.
+// Finalize, one launch: each expert's partials are summed over the partial
+// rows in a fixed order (fp64), writing aux_vec [4][E] = importance, load, f,
+// Pbar; the last block to finish then forms the three losses (finish_aux).
 constexpr int kFinThreads = 256;
 
 // Sum over the block in a fixed order (xor butterfly in each warp, then the
 // warp totals in warp order): identical on every run.
-__device__ double block_sum_fixed(double v, double *sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  double r = 0;
-#pragma unroll
-  for (int w = 0; w < kFinThreads / 32; ++w) r += sh[w];
-  __syncthreads();
-  return r;
+// Double-float ("ff") arithmetic: a value is hi + lo with |lo| <= ulp(hi)/2,
+// about 44 significant bits from fp32 operations alone (the fp64 pipe of this
+// part is narrow). Sums use Knuth's TwoSum, products Dekker's TwoProduct via
+// FMA (Knuth, TAOCP vol. 2, 4.2.2; Dekker 1971); for a fixed order of
+// operations every result is run-to-run identical.
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const float s = a.hi + b.hi;
+  const float v = s - a.hi;
+  const float e = (a.hi - (s - v)) + (b.hi - v);  // a.hi + b.hi = s + e exactly
+  const float t = e + (a.lo + b.lo);
+  const float hi = s + t;
+  return {hi, t - (hi - s)};
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = a.hi * b.hi;
+  const float e = fmaf(a.hi, b.hi, -p);  // a.hi * b.hi = p + e exactly
+  const float t = e + (a.hi * b.lo + a.lo * b.hi);
+  const float hi = p + t;
+  return {hi, t - (hi - p)};
+}
+__device__ __forceinline__ double ff_to_d(ff a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ ff d_to_ff(double x) {
+  const float h = (float)x;
+  return {h, (float)(x - (double)h)};
+}
+__device__ __forceinline__ ff ff_ld(const float2 *p) {
+  const float2 v = __ldcg(p);  // written by other blocks of this launch: read at L2
+  return {v.x, v.y};
 }
 
-// G threads sum one expert's partials: the whole block (G = 256, few experts)
-// or one warp (G = 32, eight experts per block).
-template <int G>
-__global__ void __launch_bounds__(kFinThreads)
-k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials,
-               double *__restrict__ aux_vec, float *__restrict__ importance,
-               float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
-  __shared__ double sh[kFinThreads];
+// N sums over the block at once: a fixed xor butterfly in each warp, then the
+// warp totals in warp order by N threads, shared back. sh holds >= 33 N.
+template <int N>
+__device__ void block_sum_ff(ff (&v)[N], ff *sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+      v[i] = ff_add(v[i], ff{__shfl_xor_sync(0xffffffffu, v[i].hi, o),
+                             __shfl_xor_sync(0xffffffffu, v[i].lo, o)});
+  if (lane == 0)
+#pragma unroll
+    for (int i = 0; i < N; ++i) sh[warp * N + i] = v[i];
+  __syncthreads();
+  if (threadIdx.x < N) {
+    ff r{0.f, 0.f};
+    for (int w = 0; w < nw; ++w) r = ff_add(r, sh[w * N + threadIdx.x]);
+    sh[32 * N + threadIdx.x] = r;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = sh[32 * N + i];
+  __syncthreads();
+}
+
+// Expert e's totals (importance, load, f, Pbar) into aux [4][E] as ff, and the
+// optional fp32 copies of importance and load.
+__device__ __forceinline__ void store_expert_totals(int T, int E, int e, int q, ff tot,
+                                                    float2 *__restrict__ aux,
+                                                    float *__restrict__ importance,
+                                                    float *__restrict__ load) {
+  const ff v = q >= 2 ? d_to_ff(ff_to_d(tot) / T) : tot;
+  aux[(size_t)q * E + e] = make_float2(v.hi, v.lo);
+  const float f32 = (float)ff_to_d(tot);
+  if (q == 0 && importance) importance[e] = f32;
+  if (q == 1 && load) load[e] = f32;
+}
+
+// Run by every block of a finalize launch once its aux entries are written:
+// the block that finishes last (a ticket in the status word, reset by that
+// block) computes CV^2 of importance and load (population variance, two
+// passes) and the Switch loss 0.01 * E * sum(f * Pbar), in ff with a fixed
+// order, the last few scalar steps in fp64.
+__device__ void finish_aux(int E, const float2 *__restrict__ aux, float *__restrict__ out3,
+                           DeviceStatus *st, ff *sh) {
   __shared__ int last;
-  constexpr int PER = kFinThreads / G;  // experts per block
-  const int e = blockIdx.x * PER + threadIdx.x / G;
-  const int j = threadIdx.x % G;
-  double v[4] = {0, 0, 0, 0};
-  if (e < E) {
-    for (int b = j; b < nb; b += G) {
-      const float *q = partials + (size_t)b * 4 * E + e;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] += q[(size_t)i * E];
-    }
-  }
-  double tot[4];
-  if (G == kFinThreads) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tot[i] = block_sum_fixed(v[i], sh);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
-      tot[i] = v[i];
-    }
-  }
-  if (j == 0 && e < E) {
-    aux_vec[e] = tot[0];
-    aux_vec[E + e] = tot[1];
-    aux_vec[2 * E + e] = tot[2] / T;
-    aux_vec[3 * E + e] = tot[3] / T;
-    if (importance) importance[e] = (float)tot[0];
-    if (load) load[e] = (float)tot[1];
-  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned ticket = atomicAdd(reinterpret_cast<unsigned *>(&st->aux_ticket), 1u);
-    last = ticket == gridDim.x - 1;
+    last = ticket == gridDim.x * gridDim.y - 1;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const volatile double *av = aux_vec;
-  double s_imp = 0, s_ld = 0, s_fp = 0;
-  for (int i = threadIdx.x; i < E; i += kFinThreads) {
-    s_imp += av[i];
-    s_ld += av[E + i];
-    s_fp += av[2 * E + i] * av[3 * E + i];
+  ff s3[3] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    s3[0] = ff_add(s3[0], ff_ld(aux + i));
+    s3[1] = ff_add(s3[1], ff_ld(aux + E + i));
+    s3[2] = ff_add(s3[2], ff_mul(ff_ld(aux + 2 * E + i), ff_ld(aux + 3 * E + i)));
   }
-  const double m_imp = block_sum_fixed(s_imp, sh) / E;
-  const double m_ld = block_sum_fixed(s_ld, sh) / E;
-  const double fp = block_sum_fixed(s_fp, sh);
-  double v_imp = 0, v_ld = 0;
-  for (int i = threadIdx.x; i < E; i += kFinThreads) {
-    const double a = av[i] - m_imp, l = av[E + i] - m_ld;
-    v_imp += a * a;
-    v_ld += l * l;
+  block_sum_ff<3>(s3, sh);
+  const double m_imp = ff_to_d(s3[0]) / E, m_ld = ff_to_d(s3[1]) / E;
+  const ff nm_imp = d_to_ff(-m_imp), nm_ld = d_to_ff(-m_ld);
+  ff v2[2] = {{0.f, 0.f}, {0.f, 0.f}};
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const ff a = ff_add(ff_ld(aux + i), nm_imp), l = ff_add(ff_ld(aux + E + i), nm_ld);
+    v2[0] = ff_add(v2[0], ff_mul(a, a));
+    v2[1] = ff_add(v2[1], ff_mul(l, l));
   }
-  v_imp = block_sum_fixed(v_imp, sh) / E;
-  v_ld = block_sum_fixed(v_ld, sh) / E;
+  block_sum_ff<2>(v2, sh);
   if (threadIdx.x == 0) {
+    const double v_imp = ff_to_d(v2[0]) / E, v_ld = ff_to_d(v2[1]) / E;
     out3[0] = (float)(v_imp / (m_imp * m_imp));
     out3[1] = (float)(v_ld / (m_ld * m_ld));
-    out3[2] = (float)(0.01 * E * fp);
+    out3[2] = (float)(0.01 * E * ff_to_d(s3[2]));
     st->aux_ticket = 0;  // ready for the next call
   }
+}
+
+// E <= 256: a block per expert; thread j takes rows j, j+256, ... in order,
+// then a fixed butterfly.
+__global__ void __launch_bounds__(kFinThreads)
+k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float2 *__restrict__ aux,
+               float *__restrict__ importance, float *__restrict__ load,
+               float *__restrict__ out3, DeviceStatus *st) {
+  __shared__ ff sh[kFinThreads];
+  const int e = blockIdx.x;
+  ff tot[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+  for (int b = threadIdx.x; b < nb; b += kFinThreads) {
+    const float *q = partials + (size_t)b * 4 * E + e;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tot[i] = ff_add(tot[i], ff{q[(size_t)i * E], 0.f});
+  }
+  block_sum_ff<4>(tot, sh);
+  if (threadIdx.x < 4) store_expert_totals(T, E, e, threadIdx.x, tot[threadIdx.x], aux,
+                                           importance, load);
+  finish_aux(E, aux, out3, st, sh);
+}
+
+// E > 256: block (32-expert group, quantity q). Lane l takes expert
+// 32 group + l and warp w the partial rows w, w+16, ... in order, so the row
+// reads are coalesced and kFinBatch of them are in flight at once; the
+// sixteen warp sums are added in warp order.
+constexpr int kFinColThreads = 512;
+constexpr int kFinBatch = 16;
+
+__global__ void __launch_bounds__(kFinColThreads)
+k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
+                    float2 *__restrict__ aux, float *__restrict__ importance,
+                    float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
+  __shared__ ff sh[kFinColThreads];
+  constexpr int NW = kFinColThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane, q = blockIdx.y;
+  ff v{0.f, 0.f};
+  if (e < E) {
+    const float *p = partials + (size_t)q * E + e;
+    for (int b0 = warp; b0 < nb; b0 += NW * kFinBatch) {
+      float r[kFinBatch];
+#pragma unroll
+      for (int u = 0; u < kFinBatch; ++u) {
+        const int b = b0 + u * NW;
+        r[u] = b < nb ? p[(size_t)b * 4 * E] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kFinBatch; ++u) v = ff_add(v, ff{r[u], 0.f});
+    }
+  }
+  sh[threadIdx.x] = v;
+  __syncthreads();
+  if (warp == 0 && e < E) {
+    ff tot{0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot = ff_add(tot, sh[w * 32 + lane]);
+    store_expert_totals(T, E, e, q, tot, aux, importance, load);
+  }
+  __syncthreads();
+  finish_aux(E, aux, out3, st, sh);
 }
 
 }  // namespace
@@ -739,57 +989,72 @@ cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, f
   return cudaGetLastError();
 }
 
-// Tokens per partial-sum block: small blocks (two tokens per warp) where the
-// fused selection kernel runs (two tokens per warp), so it has enough CTAs;
-// larger ones for E > 256.
-int aux_token_block(int E) { return E <= 256 ? 16 : 256; }
+// Partial rows of the balancing sums: one per 16 tokens (two per warp) where
+// the fused selection kernel runs (E <= 256), so it has enough CTAs; for the
+// column kernel the same, capped at one wave of its blocks.
+int aux_rows(int T, int E) {
+  const int r = (T + 15) / 16;
+  return E <= 256 ? r : (r < kColRows ? r : kColRows);
+}
 
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
                                 const float *sigma, const float *H, const float *rowstat,
                                 const int32_t *idx, const float *gate, const float *thr,
                                 float *partials, int n_blocks, cudaStream_t s) {
-  const int tb = aux_token_block(cfg.E);
-  const int vpl = cfg.E <= 32 ? 1 : (cfg.E <= 64 ? 2 : (cfg.E <= 128 ? 4 : 8));
-  dim3 grid(n_blocks, (cfg.E + 32 * vpl - 1) / (32 * vpl));
-#define MOE_AUXP(V)                                                                           \
-  k_aux_partials<V><<<grid, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, tb, noisy ? 1 : 0, c, \
-                                                     sigma, H, rowstat, idx, gate, thr, partials)
-  if (vpl == 1) MOE_AUXP(1);
-  else if (vpl == 2) MOE_AUXP(2);
-  else if (vpl == 4) MOE_AUXP(4);
-  else MOE_AUXP(8);
-#undef MOE_AUXP
+  const bool v4 = cfg.E % 4 == 0;
+  const int per = kColThreads * (v4 ? 4 : 1);
+  dim3 grid(n_blocks, (cfg.E + per - 1) / per);
+#define MOE_COLS(V, KM)                                                                       \
+  k_aux_cols<V, KM><<<grid, kColThreads, 0, s>>>(cfg.T, cfg.E, cfg.k, noisy ? 1 : 0, n_blocks, \
+                                                 c, sigma, H, rowstat, idx, gate, thr, partials)
+  if (v4) {
+    if (cfg.k <= 4) MOE_COLS(4, 4);
+    else MOE_COLS(4, kMaxK);
+  } else {
+    if (cfg.k <= 4) MOE_COLS(1, 4);
+    else MOE_COLS(1, kMaxK);
+  }
+#undef MOE_COLS
   return cudaGetLastError();
 }
 
 cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c, const float *sigma,
                               const float *H, int32_t *idx, float *gate, float *thr,
                               float *rowstat, float *partials, int n_blocks, cudaStream_t s) {
-  const int tb = aux_token_block(cfg.E);
+  const int tb = 16;  // tokens per partial row (aux_rows)
   const int vpl = cfg.E <= 32 ? 1 : (cfg.E <= 64 ? 2 : (cfg.E <= 128 ? 4 : 8));
-#define MOE_SELAUX(V)                                                                           \
-  k_select_aux<V><<<n_blocks, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, cfg.gate_mode, tb,   \
-                                                       noisy ? 1 : 0, c, sigma, H, idx, gate, thr, \
-                                                       rowstat, partials)
+#define MOE_SELAUX_K(V, KM)                                                                   \
+  k_select_aux<V, KM><<<n_blocks, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, cfg.gate_mode, tb, \
+                                                           noisy ? 1 : 0, c, sigma, H, idx, gate,  \
+                                                           thr, rowstat, partials)
+#define MOE_SELAUX(V)                 \
+  do {                                \
+    if (cfg.k <= 2)                   \
+      MOE_SELAUX_K(V, 2);             \
+    else if (cfg.k <= 4)              \
+      MOE_SELAUX_K(V, 4);             \
+    else                              \
+      MOE_SELAUX_K(V, kMaxK);         \
+  } while (0)
   if (vpl == 1) MOE_SELAUX(1);
   else if (vpl == 2) MOE_SELAUX(2);
   else if (vpl == 4) MOE_SELAUX(4);
   else MOE_SELAUX(8);
 #undef MOE_SELAUX
+#undef MOE_SELAUX_K
   return cudaGetLastError();
 }
 
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
-                                float *out3, float *importance, float *load, double *aux_vec,
+                                float *out3, float *importance, float *load, float2 *aux_vec,
                                 DeviceStatus *st, cudaStream_t s) {
-  // Many partial rows (16-token blocks, E <= 256): a block per expert; few
-  // (256-token blocks): a warp per expert.
+  // E <= 256: a block per expert; beyond: the column form.
   if (cfg.E <= 256)
-    k_aux_finalize<kFinThreads><<<cfg.E, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials,
-                                                              aux_vec, importance, load, out3, st);
+    k_aux_finalize<<<cfg.E, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials, aux_vec,
+                                                 importance, load, out3, st);
   else
-    k_aux_finalize<32><<<(cfg.E + 7) / 8, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials,
-                                                               aux_vec, importance, load, out3, st);
+    k_aux_finalize_cols<<<dim3((cfg.E + 31) / 32, 4), kFinColThreads, 0, s>>>(
+        cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
   return cudaGetLastError();
 }
 

@@ -3,8 +3,9 @@
 // assignments (in that flat, token-major order) to the same expert: an
 // exclusive cumulative count. It is computed without atomics on the order:
 //   k_slot_hist  -- per chunk of kSlotChunk assignments, count per expert;
-//   k_slot_scan  -- per expert, exclusive sum over chunks (chunk bases), the
-//                   total n_e, min(n_e, C), row offsets and GEMM tile offsets;
+//   k_slot_scan  -- per expert, exclusive sum over chunks (chunk bases) and
+//                   the total n_e; the last block to finish then scans
+//                   min(n_e, C) into row offsets and GEMM tile offsets;
 //   k_slot_rank  -- one warp walks each chunk in order, 32 assignments at a
 //                   time: __match_any_sync finds same-expert lanes, the rank
 //                   among them is a popcount, a per-warp counter carries it.
@@ -18,12 +19,14 @@ namespace {
 
 constexpr int kHistThreads = 256;
 constexpr int kScanThreads = 1024;
+constexpr int kScanBatch = 16;
 constexpr int kRankWarps = 8;
 
 __global__ void __launch_bounds__(kHistThreads)
 k_slot_hist(int A, int E, const int32_t *__restrict__ idx, int32_t *__restrict__ hist,
             DeviceStatus *st) {
   extern __shared__ int32_t sh_hist[];
+  if (blockIdx.x == 0 && threadIdx.x == 0) st->slot_ticket = 0;  // for k_slot_scan, next in order
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
   __syncthreads();
   const int a0 = blockIdx.x * kSlotChunk;
@@ -70,31 +73,65 @@ __device__ int block_exclusive_scan(int v, int *sh_warp, int *total) {
   return r;
 }
 
-// One block. Experts are processed kScanThreads at a time; carries join the tiles.
+// Block per 32 experts: lane l takes expert 32 blockIdx.x + l, warp w the
+// chunk segment [w S, (w+1) S), S = ceil(n_chunks / 32), so hist rows are read
+// coalesced. Segment totals are added across warps in shared memory, giving
+// each warp its base; the warp then writes its chunks' bases. The block that
+// finishes last (a ticket in the status word) scans min(n_e, C) and the tile
+// counts over all experts, kScanThreads at a time, into offset and mtiles.
 __global__ void __launch_bounds__(kScanThreads)
 k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
             int32_t *__restrict__ count, int32_t *__restrict__ offset,
-            int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist) {
+            int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist, DeviceStatus *st) {
+  constexpr int NW = kScanThreads / 32;
+  __shared__ int seg[NW][33];
   __shared__ int sh_warp[33];
+  __shared__ int last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int S = (n_chunks + NW - 1) / NW;
+  const int c0 = min(n_chunks, warp * S), c1 = min(n_chunks, c0 + S);
+  int tot = 0;
+  if (e < E) {
+    for (int cb = c0; cb < c1; cb += kScanBatch) {
+      int h[kScanBatch];
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u)
+        h[u] = cb + u < c1 ? hist[(size_t)(cb + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) tot += h[u];
+    }
+  }
+  seg[warp][lane] = tot;
+  __syncthreads();
+  int n = 0;
+  for (int w = 0; w < warp; ++w) n += seg[w][lane];
+  if (e < E) {
+    for (int c = c0; c < c1; ++c) {  // hist rows are L2-resident by now
+      const int h = hist[(size_t)c * E + e];
+      hist_base[(size_t)c * E + e] = n;
+      n += h;
+    }
+    if (warp == NW - 1) count[e] = n;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&st->slot_ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const volatile int32_t *cnt = count;
   int carry_rows = 0, carry_tiles = 0;
   for (int e0 = 0; e0 < E; e0 += kScanThreads) {
-    int e = e0 + threadIdx.x;
-    int n = 0;
-    if (e < E) {
-      for (int c = 0; c < n_chunks; ++c) {
-        hist_base[(size_t)c * E + e] = n;
-        n += hist[(size_t)c * E + e];
-      }
-      count[e] = n;
-    }
-    int kept = e < E ? min(n, C) : 0;
-    int tiles = (kept + bm - 1) / bm;
+    const int ee = e0 + threadIdx.x;
+    const int kept = ee < E ? min(cnt[ee], C) : 0;
+    const int tiles = (kept + bm - 1) / bm;
     int tot_rows, tot_tiles;
-    int off = block_exclusive_scan(kept, sh_warp, &tot_rows);
-    int toff = block_exclusive_scan(tiles, sh_warp, &tot_tiles);
-    if (e < E) {
-      offset[e] = carry_rows + off;
-      mtiles[e] = carry_tiles + toff;
+    const int off = block_exclusive_scan(kept, sh_warp, &tot_rows);
+    const int toff = block_exclusive_scan(tiles, sh_warp, &tot_tiles);
+    if (ee < E) {
+      offset[ee] = carry_rows + off;
+      mtiles[ee] = carry_tiles + toff;
     }
     carry_rows += tot_rows;
     carry_tiles += tot_tiles;
@@ -102,6 +139,7 @@ k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
   if (threadIdx.x == 0) {
     offset[E] = carry_rows;
     mtiles[E] = carry_tiles;
+    st->slot_ticket = 0;
   }
 }
 
@@ -185,8 +223,8 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
   k_slot_hist<<<n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s>>>(A, cfg.E, idx, hist, st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  k_slot_scan<<<1, kScanThreads, 0, s>>>(cfg.E, C, n_chunks, kTcBM, chunk_base, count, offset,
-                                         mtiles, hist);
+  k_slot_scan<<<(cfg.E + 31) / 32, kScanThreads, 0, s>>>(cfg.E, C, n_chunks, kTcBM, chunk_base,
+                                                         count, offset, mtiles, hist, st);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   size_t smem = (size_t)kRankWarps * cfg.E * sizeof(int32_t);

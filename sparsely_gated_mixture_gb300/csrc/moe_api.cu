@@ -16,7 +16,7 @@ WsLayout ws_layout(const moe_config &cfg) {
   const size_t A = T * k;
   const size_t eb = elem_bytes(cfg.act_dtype);
   L.n_chunks = (int)((A + kSlotChunk - 1) / kSlotChunk);
-  L.n_aux_blocks = (int)((T + aux_token_block(cfg.E) - 1) / aux_token_block(cfg.E));
+  L.n_aux_blocks = aux_rows((int)T, (int)cfg.E);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -228,7 +228,7 @@ int moe_aux_loss(const moe_config *cfg, const void *ws, float *out3, float *impo
   const WsLayout L = ws_layout(*cfg);
   void *w = const_cast<void *>(ws);
   MOE_CUDA(launch_aux_finalize(*cfg, ws_at<float>(w, L.partials), L.n_aux_blocks, out3,
-                               importance, load, ws_at<double>(w, L.aux_vec),
+                               importance, load, ws_at<float2>(w, L.aux_vec),
                                ws_at<DeviceStatus>(w, L.status), (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -271,7 +271,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
   MOE_CUDA(launch_combine(c, x, zbuf, ps, kp, idx, offset, y, st, s));
   if (aux_out3)
     MOE_CUDA(launch_aux_finalize(c, ws_at<float>(ws, L.partials), L.n_aux_blocks, aux_out3,
-                                 nullptr, nullptr, ws_at<double>(ws, L.aux_vec), st, s));
+                                 nullptr, nullptr, ws_at<float2>(ws, L.aux_vec), st, s));
   return MOE_OK;
 }
 

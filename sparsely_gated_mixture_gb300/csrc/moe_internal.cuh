@@ -21,6 +21,8 @@ struct DeviceStatus {
   int32_t code;
   uint32_t aux_ticket;  // blocks of the balancing finalize that are done (reset by the last)
   long long detail;
+  uint32_t slot_ticket;  // blocks of the slot scan that are done (zeroed by the histogram pass)
+  uint32_t reserved;
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus *st, int code, long long detail) {
@@ -67,9 +69,9 @@ cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *
                                 const int32_t *idx, const float *gate, const float *thr,
                                 float *partials, int n_blocks, cudaStream_t s);
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
-                                float *out3, float *importance, float *load, double *aux_vec,
+                                float *out3, float *importance, float *load, float2 *aux_vec,
                                 DeviceStatus *st, cudaStream_t s);
-int aux_token_block(int E);  // tokens per partial-sum block of the balancing sums
+int aux_rows(int T, int E);  // partial rows of the balancing sums
 // Selection and balancing partials in one kernel (E <= 256).
 cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c, const float *sigma,
                               const float *H, int32_t *idx, float *gate, float *thr,

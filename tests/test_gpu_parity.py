@@ -202,3 +202,40 @@ def test_bad_arguments_rejected_before_launch():
     with pytest.raises(B.MoEError):  # noise weights without noise
         B.moe_forward(cfg, d["x"], d["Wg"], d["Wn"], None, None, d["W1"], None, d["W2"], None, y,
                       None, ws)
+
+
+WIDE = {
+    # E = 301: one expert per thread in the column sums, 16 values per lane in
+    # the selection; k = 5 takes the long chosen-list form.
+    "e301_k5": wl.Workload("e301_k5", T=333, d=64, E=301, d_ff=64, k=5, cf=1.0, mode=wl.TOPK,
+                           dtype="bf16", noisy=True),
+    "e1024_switch": wl.Workload("e1024_switch", T=300, d=128, E=1024, d_ff=64, k=1, cf=1.0,
+                                mode=wl.SWITCH, dtype="bf16", noisy=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WIDE))
+def test_wide_router_parity(name):
+    w = WIDE[name]
+    inp = wl.generate(w, seed=13, biases=True)
+    stages, _ = check_stages(w, inp)
+    check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
+
+
+@pytest.mark.parametrize("levels", [0, 3])
+def test_tied_logits_wide(levels):
+    """Exact ties in wide rows: a zero clean router with a bias on a coarse
+    grid, so every token's logits are the bias. levels = 0 ties all 1024
+    experts (more candidates than a warp holds); levels = 3 leaves a few
+    dozen experts tied at the top. Ties are broken by the lower index on both
+    sides, so the choices must match exactly."""
+    w = wl.Workload("tied_e1024", T=200, d=64, E=1024, d_ff=64, k=4, cf=2.0, mode=wl.TOPK,
+                    dtype="bf16", noisy=False)
+    inp = wl.generate(w, seed=17)
+    inp["Wg"] = np.zeros_like(inp["Wg"])
+    rng = np.random.default_rng(3)
+    inp["bias"] = (np.round(rng.standard_normal(w.E) * levels) if levels else
+                   np.zeros(w.E)).astype(np.float32)
+    res, _ = check_stages(w, inp)
+    ref = oracle_gate(inp)
+    assert np.array_equal(res["idx"], ref["idx"])
