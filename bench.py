@@ -346,6 +346,8 @@ def run_ours(args, w: wl.Workload):
         "dispatch": {"ms": mean["dispatch"], "gbs": bw(tr["dispatch_bytes"], "dispatch"),
                      "hbm_frac": bw(tr["dispatch_bytes"], "dispatch") / peaks["hbm_gbs"]},
         "expert_ffn": {"ms": mean["expert_ffn"], "tflops": ffn_tflops,
+                       "gbs": tr["ffn_bytes"] / ffn_s / 1e9,
+                       "hbm_frac": tr["ffn_bytes"] / ffn_s / 1e9 / peaks["hbm_gbs"],
                        "bf16_frac": ffn_tflops / peaks["bf16_tflops"],
                        "bf16_frac_sustained": ffn_tflops / peaks["bf16_tflops_sustained"]},
         "combine": {"ms": mean["combine"], "gbs": bw(tr["combine_bytes"], "combine"),
@@ -354,9 +356,26 @@ def run_ours(args, w: wl.Workload):
     }
     tps = world * T / (ms * 1e-3)
     # router (plus the weight split that feeds the tensor-core router for bf16
-    # tokens), select, balancing partials, slot histogram / scan / rank,
-    # gather, two expert GEMMs, combine, balancing finalize
-    launches_per_step = 12 if (w.dtype == "bf16" and w.d % 8 == 0) else 11
+    # tokens), selection with the balancing partials (one fused kernel up to
+    # 256 experts, two beyond), slot histogram / scan / rank, gather, two
+    # expert GEMMs, combine, balancing finalize
+    launches_per_step = ((2 if (w.dtype == "bf16" and w.d % 8 == 0) else 1)
+                         + (1 if w.E <= 256 else 2) + 3 + 1 + 2 + 1 + 1)
+    # The expert GEMMs' roofline is whichever bound is the tighter for this
+    # layer: the bf16 tensor rate, or HBM for the weights and activations they
+    # must stream (many small experts).
+    t_flops = tr["ffn_flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = tr["ffn_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    roof = {"kernel": "moe_expert_ffn (two grouped GEMM launches)"}
+    if t_bytes > t_flops:
+        ffn_gbs = tr["ffn_bytes"] / ffn_s / 1e9
+        roof.update({"bound": "hbm", "achieved": ffn_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ffn_gbs / peaks["hbm_gbs"]})
+    else:
+        roof.update({"bound": "tensor", "achieved": ffn_tflops, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": ffn_tflops / peaks["bf16_tflops"]})
+    roof.update({"peak_source": peak_kind, "algorithmic_flops_per_launch": tr["ffn_flops"],
+                 "algorithmic_bytes": tr["ffn_bytes"], "traffic": measured_traffic(w)})
     line = {
         "metric": METRIC,
         "value": tps,
@@ -374,11 +393,7 @@ def run_ours(args, w: wl.Workload):
                                       "l2": "flushed between steps (256 MiB write)",
                                       "accepted_rows": accepted,
                                       "dropped_fraction": 1 - accepted / A}),
-        "roofline": {"kernel": "moe_expert_ffn (two grouped GEMM launches)", "bound": "tensor",
-                     "achieved": ffn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": ffn_tflops / peaks["bf16_tflops"], "peak_source": peak_kind,
-                     "algorithmic_flops_per_launch": tr["ffn_flops"],
-                     "algorithmic_bytes": tr["ffn_bytes"], "traffic": measured_traffic(w)},
+        "roofline": roof,
         "stages": stage_rep,
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "overlap": "copies of steps i+1 and i-1 overlap the compute of step i",

@@ -18,9 +18,12 @@
 // (BNR <= 64), one lane issues 4 tcgen05.mma (M=128, N=3*BNR, K=16, both
 // operands K-major, 128B swizzle) into one of two TMEM accumulators, whose
 // three BNR-wide sections are summed per column, and eight epilogue
-// warps (two per TMEM lane quadrant) turn each token's columns into c = acc + b, sigma = Softplus(z) and
-// H = c + noise * sigma, staged in shared memory so that noise is read and
-// c, sigma, H [T, E] fp32 are written a row segment at a time.
+// warps (two per TMEM lane quadrant) turn each token's columns into
+// c = acc + b, sigma = Softplus(z) and H = c + noise * sigma, 16 experts at a
+// time: the [32 tokens x 16 experts] fp32 tiles of c, sigma and H go to
+// shared memory (64-byte swizzle) and out with one TMA store each (only H
+// without the noise term, where c = H and sigma = 0). Rows of E floats that
+// are not 16-byte multiples (E % 4 != 0) take a staged store per row segment.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -32,15 +35,61 @@ constexpr int kREpiWarps = 8;  // two per TMEM lane quadrant, alternating 16-col
 constexpr int kRThreads = 64 + 32 * kREpiWarps;
 
 struct RParams {
-  int T, d, E, noisy, NC, NCP, n_blocks;
+  int T, d, E, noisy, NC, NCP, n_blocks, tma_out;
   const float *noise, *bias;
   float *c_out, *s_out, *H_out;
   DeviceStatus *st;
   unsigned long long wait_ns;  // bounded-wait limit
 };
 
+// Softplus(z) = max(z, 0) + log1p(t), t = exp(-|z|) in (0, 1]. log1p(t) is
+// 2 atanh(s) with s = t / (2 + t) in [0, 1/3], summed as the odd series
+// 2 s (1 + s^2/3 + s^4/5 + ... + s^12/13): the truncation is below 2^-26
+// relative, and in fp32 the result matches log1pf(expf(-|z|)) to within a few
+// ulps (max 3.4 vs 3.0 ulps of Softplus against the exact value).
 __device__ __forceinline__ float softplus_r(float z) {
-  return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
+  const float t = expf(-fabsf(z));
+  const float sv = __fdividef(t, 2.f + t);
+  const float s2 = sv * sv;
+  float q = 1.f / 13.f;
+  q = fmaf(s2, q, 1.f / 11.f);
+  q = fmaf(s2, q, 1.f / 9.f);
+  q = fmaf(s2, q, 1.f / 7.f);
+  q = fmaf(s2, q, 1.f / 5.f);
+  q = fmaf(s2, q, 1.f / 3.f);
+  q = fmaf(s2, q, 1.f);
+  return fmaxf(z, 0.0f) + 2.f * sv * q;
+}
+
+// TMA store of a shared-memory tile, and the bulk-group bookkeeping around it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
+                                             int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   (uint64_t)map),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Row l of a [32 x 16] fp32 tile in the 64-byte swizzle of the TMA store:
+// 16-byte chunk q of row l sits at chunk q ^ ((l >> 1) & 3).
+__device__ __forceinline__ void tile_row_store(float *tile, int l, const float *v) {
+  float4 *row = reinterpret_cast<float4 *>(tile + l * 16);
+  const int x = (l >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    row[q ^ x] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 // grid (ceil(d/32), ceil(NCP/32)), block (32, 8): a 32 x 32 transpose tile.
@@ -168,10 +217,69 @@ __device__ __forceinline__ void load_noise8(const RParams &p, int t, int e0, flo
   }
 }
 
+// Token t's noise draws for experts e0 .. e0+15 (zero past E or T).
+__device__ __forceinline__ void load_noise16(const RParams &p, int t, int e0, float *nz) {
+  if (t < p.T && (p.E & 3) == 0 && e0 + 16 <= p.E) {
+    const float4 *src = reinterpret_cast<const float4 *>(p.noise + (size_t)t * p.E + e0);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 a = src[q];
+      nz[4 * q] = a.x;
+      nz[4 * q + 1] = a.y;
+      nz[4 * q + 2] = a.z;
+      nz[4 * q + 3] = a.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      nz[j] = (t < p.T && e0 + j < p.E) ? p.noise[(size_t)t * p.E + e0 + j] : 0.f;
+  }
+}
+
+// One unit of the TMA-store epilogue: experts e0 .. e0+15 of tokens t0 .. t0+31
+// (lane l = token t0 + l). cv holds the clean logits and zv the noise logits
+// on entry; both are overwritten (c, then sigma, then H), each tile written to
+// shared memory as soon as it is ready.
+__device__ __forceinline__ void router_unit_tma(const RParams &p, const CUtensorMap *mc,
+                                                const CUtensorMap *ms, const CUtensorMap *mh,
+                                                int t0, int e0, float *cv, float *zv,
+                                                const float *nz, float *stg) {
+  const int lane = threadIdx.x & 31;
+  float *sc = stg, *ss = stg + kEpiTile, *sh = stg + 2 * kEpiTile;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
+  if (p.noisy) {
+    tile_row_store(sc, lane, cv);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      zv[j] = softplus_r(zv[j]);
+      cv[j] = fmaf(nz[j], zv[j], cv[j]);
+    }
+    tile_row_store(ss, lane, zv);
+  }
+  tile_row_store(sh, lane, cv);
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
+  if (bad && t0 + lane < p.T) record_error(p.st, MOE_ERR_NONFINITE, (long long)(t0 + lane));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(mh, sh, e0, t0);
+    if (p.noisy) {
+      tma_store_2d(mc, sc, e0, t0);
+      tma_store_2d(ms, ss, e0, t0);
+    }
+    bulk_commit();
+  }
+}
+
 template <int BNR>
 __global__ void __launch_bounds__(kRThreads, 1)
 k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const RParams p) {
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+            const __grid_constant__ CUtensorMap tmH, const RParams p) {
   using C = RCfg<BNR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -289,7 +397,56 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * C::NB);
       float *stg = staging + (size_t)(warp - 2) * 3 * kEpiTile;
       const int t = t0 + lane;
-      const int nchunks = (min(p.NC - nb * BNR, BNR) + 15) / 16;
+      const int ncols = min(p.NC - nb * BNR, BNR);
+      if (p.tma_out) {
+        // Units of 16 experts: 32 columns (clean/noise pairs) or 16. The
+        // next unit's noise is loaded while this one is computed.
+        const int upc = p.noisy ? 32 : 16;
+        const int nunits = (ncols + upc - 1) / upc;
+        const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first expert of the block
+        float nz_next[16];
+        if (p.noisy && sub < nunits) load_noise16(p, t, eb + sub * 16, nz_next);
+#pragma unroll 1
+        for (int u = sub; u < nunits; u += 2) {
+          float nz[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) nz[j] = nz_next[j];
+          if (p.noisy && u + 2 < nunits) load_noise16(p, t, eb + (u + 2) * 16, nz_next);
+          float cv[16], zv[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cv[j] = zv[j] = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int col = u * upc + hh * 16;
+            if ((hh == 1 && !p.noisy) || col >= ncols) continue;  // warp-uniform
+            uint32_t vh[16], vm[16], vl[16];
+            tmem_ld16(lane_addr + (uint32_t)col, vh);
+            tmem_ld16(lane_addr + (uint32_t)(BNR + col), vm);
+            tmem_ld16(lane_addr + (uint32_t)(2 * BNR + col), vl);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float v =
+                  __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
+              if (p.noisy) {
+                if (j & 1)
+                  zv[hh * 8 + (j >> 1)] = v;
+                else
+                  cv[hh * 8 + (j >> 1)] = v;
+              } else {
+                cv[j] = v;
+              }
+            }
+          }
+          if (lane == 0) bulk_wait_read_all();  // the last unit's stores have read the tiles
+          __syncwarp();
+          router_unit_tma(p, &tmC, &tmS, &tmH, t0, eb + u * 16, cv, zv, nz, stg);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        continue;
+      }
+      const int nchunks = (ncols + 15) / 16;
       // 16 columns at a time: 8 experts (noisy, clean/noise pairs) or 16.
       // The next chunk's noise is loaded while this one is computed.
       float nz_next[8];
@@ -339,6 +496,7 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
   }
+  if (warp >= 2 && lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -350,6 +508,20 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 }
 
 int tile_cols(int NC) { return NC <= 16 ? 16 : NC <= 32 ? 32 : 64; }
+
+// 2-D fp32 tensor [T, E] (E contiguous, E % 4 == 0), box [32 tokens, 16
+// experts], 64-byte swizzle: the router's output tiles.
+bool make_out_map(CUtensorMap *m, float *base, int T, int E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)E * 4};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 template <int BNR>
 cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float *Wn,
@@ -364,11 +536,16 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
                                                  static_cast<__nv_bfloat16 *>(bsplit));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc, ts, th;
   if (!make_map(&ta, x, (uint64_t)c.T, (uint64_t)c.d, RBM) ||
       !make_map(&tb, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, 3 * BNR))
     return cudaErrorInvalidValue;
-  RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, noise, bias, cc, sg, H, st,
+  // The TMA-store epilogue needs 16-byte rows and 16-byte-aligned outputs.
+  const bool tma_out = c.E % 4 == 0 && (uintptr_t)cc % 16 == 0 && (uintptr_t)sg % 16 == 0 &&
+                       (uintptr_t)H % 16 == 0 && make_out_map(&tc, cc, c.T, c.E) &&
+                       make_out_map(&ts, sg, c.T, c.E) && make_out_map(&th, H, c.T, c.E);
+  if (!tma_out) th = ts = tc = ta;  // unused
+  RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, tma_out ? 1 : 0, noise, bias, cc, sg, H, st,
             wait_limit_ns()};
   const size_t smem = RCfg<BNR>::SMEM;
   err = cudaFuncSetAttribute(k_router_tc<BNR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -376,7 +553,7 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   if (err != cudaSuccess) return err;
   const int tiles = ((c.T + RBM - 1) / RBM) * n_blocks;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_router_tc<BNR><<<grid, kRThreads, smem, s>>>(ta, tb, p);
+  k_router_tc<BNR><<<grid, kRThreads, smem, s>>>(ta, tb, tc, ts, th, p);
   return cudaGetLastError();
 }
 
