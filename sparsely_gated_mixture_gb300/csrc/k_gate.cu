@@ -664,8 +664,9 @@ k_aux_cols(int T, int E, int k, int noisy, int P, const float *__restrict__ c,
 // Selection and balancing partials in one pass, for E <= 256: the warp that
 // selects token t's experts goes on to add t's contributions to the expert
 // sums its lanes own, so H, the chosen experts and the gates are read once.
-// Token order, warp order and the block sums are those of k_aux_partials, so
-// the partials are bit-identical to the two-kernel path.
+// Block b covers tokens [16 b, 16 b + 16); warp w takes tokens t0+w, t0+w+8
+// in order and the eight warps' sums are added in warp order, so every
+// partial is run-to-run identical.
 template <int VPL, int KM>  // KM >= k: the chosen list kept in registers
 __global__ void __launch_bounds__(kAuxWarps * 32)
 k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__restrict__ c,
