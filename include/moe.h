@@ -16,10 +16,14 @@
  * Memory.  Every array argument is a DEVICE pointer owned by the caller, on the
  *   current CUDA device, row-major and contiguous, 16-byte aligned. The library
  *   never allocates, frees or copies host<->device (except moe_last_device_status,
- *   which reads 16 bytes back). Scratch space is the caller's workspace `ws` of
- *   moe_workspace_size() bytes (256-byte aligned).
+ *   which reads the 24-byte status word back). Scratch space is the caller's
+ *   workspace `ws` of moe_workspace_size() bytes (256-byte aligned).
  * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
- *   default stream) and returns without synchronising.
+ *   default stream) and returns without synchronising. moe_forward() runs the
+ *   balancing-loss finalize on a side stream of its own, forked from `stream`
+ *   after the gate and joined back before it returns (so later work on
+ *   `stream`, and stream capture, see one ordered forward); the side stream and
+ *   its two events are created once per device on first use and kept.
  * Element types.  cfg->act_dtype (MOE_F32 or MOE_BF16) is the type of x, W1,
  *   b1, W2, b2, y, xbuf and hbuf. The router weights, router bias, noise,
  *   gates and zbuf are always fp32.

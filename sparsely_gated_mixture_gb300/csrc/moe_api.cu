@@ -3,6 +3,8 @@
 // every stage runs in the kernels of the other translation units.
 #include "moe_internal.cuh"
 
+#include <mutex>
+
 #include <math.h>
 #include <string.h>
 
@@ -120,6 +122,39 @@ static int ffn_impl(const moe_config &c, const void *xbuf, const int32_t *offset
     MOE_CUDA(launch_ffn_simt(c, C, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
   }
   return MOE_OK;
+}
+
+// One side stream (non-blocking) and a fork / join event pair per device,
+// made on first use and kept; the lock is held while a call enqueues on them,
+// so calls from several host threads do not interleave their records.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kSideMaxDevices = 64;
+static std::mutex g_side_mu;
+static SideStream g_side[kSideMaxDevices];
+static bool g_side_failed[kSideMaxDevices] = {};
+
+static SideStream *side_stream(std::unique_lock<std::mutex> &lock) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideMaxDevices) return nullptr;
+  lock = std::unique_lock<std::mutex>(g_side_mu);
+  SideStream &ss = g_side[dev];
+  if (!ss.s && !g_side_failed[dev]) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      g_side_failed[dev] = true;
+      ss = SideStream{};
+      cudaGetLastError();
+    }
+  }
+  if (!ss.s) {
+    lock.unlock();
+    return nullptr;
+  }
+  return &ss;
 }
 
 }  // namespace moe
@@ -260,6 +295,22 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
   float *zbuf = ws_at<float>(ws, L.zbuf);
   r = gate_impl(c, x, Wg, Wnoise, noise, logit_bias, idx, g, thr, ws, aux_out3 != nullptr, s);
   if (r != MOE_OK) return r;
+  // The balancing finalize needs only the gate's partial sums: it runs on the
+  // side stream beside dispatch, the expert GEMMs and combine (on `stream`
+  // itself if no side stream could be made).
+  SideStream *side = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  if (aux_out3) {
+    side = side_stream(side_lock);
+    cudaStream_t fs = s;
+    if (side) {
+      MOE_CUDA(cudaEventRecord(side->fork, s));
+      MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+      fs = side->s;
+    }
+    MOE_CUDA(launch_aux_finalize(c, ws_at<float>(ws, L.partials), L.n_aux_blocks, aux_out3,
+                                 nullptr, nullptr, ws_at<float2>(ws, L.aux_vec), st, fs));
+  }
   MOE_CUDA(launch_slots(c, host_capacity(c), idx, g, ws_at<int32_t>(ws, L.hist),
                         ws_at<int32_t>(ws, L.chunk_base), ws_at<int32_t>(ws, L.count), offset,
                         ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
@@ -269,9 +320,11 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
                zbuf, st, s);
   if (r != MOE_OK) return r;
   MOE_CUDA(launch_combine(c, x, zbuf, ps, kp, idx, offset, y, st, s));
-  if (aux_out3)
-    MOE_CUDA(launch_aux_finalize(c, ws_at<float>(ws, L.partials), L.n_aux_blocks, aux_out3,
-                                 nullptr, nullptr, ws_at<float2>(ws, L.aux_vec), st, s));
+  if (side) {
+    // Join: work enqueued on `stream` after this call also waits for the losses.
+    MOE_CUDA(cudaEventRecord(side->join, side->s));
+    MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+  }
   return MOE_OK;
 }
 
