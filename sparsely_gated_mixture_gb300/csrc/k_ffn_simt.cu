@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(kThreads)
 k_ffn_simt(int K, int N, const T *__restrict__ Ain, const int32_t *__restrict__ offset,
            const float *__restrict__ row_gate, const T *__restrict__ W, const T *__restrict__ bias,
            void *__restrict__ out, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN];
   const int e = blockIdx.z;
@@ -97,13 +99,13 @@ cudaError_t run(const moe_config &cfg, int C, const void *xbuf, const int32_t *o
                 const void *b2, void *hbuf, float *zbuf, DeviceStatus *st, cudaStream_t s) {
   const int mt = (C + BM - 1) / BM;
   dim3 g1((cfg.d_ff + BN - 1) / BN, mt, cfg.E);
-  k_ffn_simt<T, 1><<<g1, kThreads, 0, s>>>(cfg.d, cfg.d_ff, (const T *)xbuf, offset, row_gate,
-                                           (const T *)W1, (const T *)b1, hbuf, st);
+  launch_pdl_c(kPdlGemm, k_ffn_simt<T, 1>, g1, kThreads, 0, s, cfg.d, cfg.d_ff, (const T *)xbuf,
+      offset, row_gate, (const T *)W1, (const T *)b1, hbuf, st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   dim3 g2((cfg.d + BN - 1) / BN, mt, cfg.E);
-  k_ffn_simt<T, 2><<<g2, kThreads, 0, s>>>(cfg.d_ff, cfg.d, (const T *)hbuf, offset, row_gate,
-                                           (const T *)W2, (const T *)b2, zbuf, st);
+  launch_pdl_c(kPdlGemm, k_ffn_simt<T, 2>, g2, kThreads, 0, s, cfg.d_ff, cfg.d, (const T *)hbuf,
+      offset, row_gate, (const T *)W2, (const T *)b2, zbuf, st);
   return cudaGetLastError();
 }
 

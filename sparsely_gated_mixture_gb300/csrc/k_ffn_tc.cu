@@ -87,6 +87,7 @@ template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
          const Params p) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzle atoms.
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -185,6 +186,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
         mbar_drain(&full[q % STAGES], (q / STAGES) & 1u);
     }
     __syncwarp();
+    pdl_trigger();  // all loads issued: the next kernel may be scheduled
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------- MMA issuer
@@ -222,6 +224,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       mbar_drain(drain, 0);
     }
     __syncwarp();
+    pdl_trigger();
   } else {
     // ----------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
@@ -286,6 +289,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    pdl_trigger();
   }
   tc_fence_before();
   __syncthreads();
@@ -362,6 +366,7 @@ template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const Params p) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -477,6 +482,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         mbar_drain(&empty[q % P_STAGES], (q / P_STAGES) & 1u);
     }
     __syncwarp();
+    pdl_trigger();  // all loads issued: the next kernel may be scheduled
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // --------------------------------------------------------- MMA issuer (even CTA)
@@ -513,6 +519,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       mbar_drain(drain, 0);
     }
     __syncwarp();
+    pdl_trigger();
   } else {
     // ------------------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;
@@ -579,6 +586,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
+    pdl_trigger();
   }
   tc_fence_before();
   cluster_sync_all();  // every MMA reading either CTA's memory and every TMEM read are done
@@ -650,7 +658,7 @@ cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const Param
   cudaError_t err = cudaFuncSetAttribute(k_ffn_tc<LAYER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  k_ffn_tc<LAYER><<<sm_count(), kThreads, smem, s>>>(a, b, p);
+  launch_pdl_c(kPdlGemm, k_ffn_tc<LAYER>, sm_count(), kThreads, smem, s, a, b, p);
   return cudaGetLastError();
 }
 
@@ -700,9 +708,11 @@ cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1] = {pair_cluster_attr()};
+  cudaLaunchAttribute attr[2] = {pair_cluster_attr(), {}};
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled(kPdlGemm) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k_ffn_tc_pair<LAYER>, a, b, p);
 }
 

@@ -42,6 +42,8 @@ k_router(int T, int d, int E, const void *__restrict__ x, int xdtype, const floa
          const float *__restrict__ Wn, const float *__restrict__ noise,
          const float *__restrict__ bias, float *__restrict__ c_out, float *__restrict__ s_out,
          float *__restrict__ H_out, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float4 smem4[];
   float *smem = reinterpret_cast<float *>(smem4);
   float *xs = smem;                                  // [kRtTok][kRtXPitch]
@@ -134,8 +136,8 @@ cudaError_t run_router(const moe_config &cfg, const void *x, const float *Wg, co
                                          (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((cfg.T + kRtTok - 1) / kRtTok, (cfg.E + BE - 1) / BE);
-  kern<<<grid, kRtWarps * 32, smem, stream>>>(cfg.T, cfg.d, cfg.E, x, cfg.act_dtype, Wg, Wn, noise,
-                                               bias, c, s, H, st);
+  launch_pdl(kern, grid, kRtWarps * 32, smem, stream, cfg.T, cfg.d, cfg.E, x, cfg.act_dtype, Wg, Wn,
+      noise, bias, c, s, H, st);
   return cudaGetLastError();
 }
 
@@ -177,6 +179,8 @@ k_router_vec(int T, int d, int E, int w16, const XT *__restrict__ x, const float
              const float *__restrict__ Wn, const float *__restrict__ noise,
              const float *__restrict__ bias, float *__restrict__ c_out, float *__restrict__ s_out,
              float *__restrict__ H_out, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NC = NOISY ? 2 * BE : BE;  // columns: BE clean, then BE noise
   constexpr int WP = NC + 4;               // padded W row: conflict-free float4 reads
   constexpr int VEC = 16 / (int)sizeof(XT);
@@ -302,9 +306,8 @@ cudaError_t run_router_vec(const moe_config &cfg, const void *x, const float *Wg
                                          (int)smem);
   if (err != cudaSuccess) return err;
   dim3 grid((cfg.T + kRvWarps * TPW - 1) / (kRvWarps * TPW), (cfg.E + BE - 1) / BE);
-  kern<<<grid, kRvWarps * 32, smem, stream>>>(cfg.T, cfg.d, cfg.E, cfg.E % 4 == 0 ? 1 : 0,
-                                               static_cast<const XT *>(x), Wg, Wn, noise, bias, c,
-                                               s, H, st);
+  launch_pdl(kern, grid, kRvWarps * 32, smem, stream, cfg.T, cfg.d, cfg.E, cfg.E % 4 == 0 ? 1 : 0,
+      static_cast<const XT *>(x), Wg, Wn, noise, bias, c, s, H, st);
   return cudaGetLastError();
 }
 
@@ -496,6 +499,8 @@ template <int VPL>
 __global__ void __launch_bounds__(256)
 k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__restrict__ idx,
          float *__restrict__ gate, float *__restrict__ thr, float *__restrict__ rowstat) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float2 scratch[8][32];
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -571,6 +576,8 @@ k_aux_cols(int T, int E, int k, int noisy, int P, const float *__restrict__ c,
            const float *__restrict__ rowstat, const int32_t *__restrict__ idx,
            const float *__restrict__ gate, const float *__restrict__ thr,
            float *__restrict__ partials) {
+  pdl_wait();
+  pdl_trigger();
   using VT = typename std::conditional<V == 4, float4, float>::type;
   __shared__ float4 s_tok[kColTB];  // th0, th1, mx, 1/se
   __shared__ int s_idx[kColTB][KM];
@@ -673,6 +680,8 @@ k_select_aux(int T, int E, int k, int mode, int tb, int noisy, const float *__re
              const float *__restrict__ sg, const float *__restrict__ H,
              int32_t *__restrict__ idx, float *__restrict__ gate, float *__restrict__ thr,
              float *__restrict__ rowstat, float *__restrict__ partials) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int CH = 32 * VPL;
   __shared__ float red[kAuxWarps][4][CH];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -878,6 +887,8 @@ __global__ void __launch_bounds__(kFinThreads)
 k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float2 *__restrict__ aux,
                float *__restrict__ importance, float *__restrict__ load,
                float *__restrict__ out3, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ ff sh[kFinThreads];
   const int e = blockIdx.x;
   ff tot[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -903,6 +914,8 @@ __global__ void __launch_bounds__(kFinColThreads)
 k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
                     float2 *__restrict__ aux, float *__restrict__ importance,
                     float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ ff sh[kFinColThreads];
   constexpr int NW = kFinColThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -978,8 +991,8 @@ cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, f
   dim3 grid((cfg.T + warps - 1) / warps);
   int vpl = (cfg.E + 31) / 32;
 #define MOE_SEL(V)                                                                          \
-  k_select<V><<<grid, warps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, cfg.gate_mode, H, idx, gate, \
-                                          thr, rowstat)
+  launch_pdl(k_select<V>, grid, warps * 32, 0, s, cfg.T, cfg.E, cfg.k, cfg.gate_mode, H, idx,      \
+      gate, thr, rowstat)
   if (vpl <= 1) MOE_SEL(1);
   else if (vpl <= 2) MOE_SEL(2);
   else if (vpl <= 4) MOE_SEL(4);
@@ -1006,8 +1019,8 @@ cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *
   const int per = kColThreads * (v4 ? 4 : 1);
   dim3 grid(n_blocks, (cfg.E + per - 1) / per);
 #define MOE_COLS(V, KM)                                                                       \
-  k_aux_cols<V, KM><<<grid, kColThreads, 0, s>>>(cfg.T, cfg.E, cfg.k, noisy ? 1 : 0, n_blocks, \
-                                                 c, sigma, H, rowstat, idx, gate, thr, partials)
+  launch_pdl(k_aux_cols<V, KM>, grid, kColThreads, 0, s, cfg.T, cfg.E, cfg.k, noisy ? 1 : 0,       \
+      n_blocks, c, sigma, H, rowstat, idx, gate, thr, partials)
   if (v4) {
     if (cfg.k <= 4) MOE_COLS(4, 4);
     else MOE_COLS(4, kMaxK);
@@ -1025,9 +1038,8 @@ cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c,
   const int tb = 16;  // tokens per partial row (aux_rows)
   const int vpl = cfg.E <= 32 ? 1 : (cfg.E <= 64 ? 2 : (cfg.E <= 128 ? 4 : 8));
 #define MOE_SELAUX_K(V, KM)                                                                   \
-  k_select_aux<V, KM><<<n_blocks, kAuxWarps * 32, 0, s>>>(cfg.T, cfg.E, cfg.k, cfg.gate_mode, tb, \
-                                                           noisy ? 1 : 0, c, sigma, H, idx, gate,  \
-                                                           thr, rowstat, partials)
+  launch_pdl(k_select_aux<V, KM>, n_blocks, kAuxWarps * 32, 0, s, cfg.T, cfg.E, cfg.k,             \
+      cfg.gate_mode, tb, noisy ? 1 : 0, c, sigma, H, idx, gate, thr, rowstat, partials)
 #define MOE_SELAUX(V)                 \
   do {                                \
     if (cfg.k <= 2)                   \
@@ -1051,11 +1063,11 @@ cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, in
                                 DeviceStatus *st, cudaStream_t s) {
   // E <= 256: a block per expert; beyond: the column form.
   if (cfg.E <= 256)
-    k_aux_finalize<<<cfg.E, kFinThreads, 0, s>>>(cfg.T, cfg.E, n_blocks, partials, aux_vec,
-                                                 importance, load, out3, st);
+    launch_pdl_c(kPdlFinalize, k_aux_finalize, cfg.E, kFinThreads, 0, s, cfg.T, cfg.E, n_blocks,
+        partials, aux_vec, importance, load, out3, st);
   else
-    k_aux_finalize_cols<<<dim3((cfg.E + 31) / 32, 4), kFinColThreads, 0, s>>>(
-        cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
+    launch_pdl_c(kPdlFinalize, k_aux_finalize_cols, dim3((cfg.E + 31) / 32, 4), kFinColThreads, 0,
+        s, cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
   return cudaGetLastError();
 }
 

@@ -99,6 +99,8 @@ __device__ __forceinline__ void tile_row_store(float *tile, int l, const float *
 __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP, int BNR,
                                const float *__restrict__ Wg, const float *__restrict__ Wn,
                                __nv_bfloat16 *__restrict__ B) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[32][33];
   const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += 8) {
@@ -315,6 +317,8 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // barriers and TMEM are set up; now the inputs may be read
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const int m_blocks = (p.T + RBM - 1) / RBM;
   const int total = m_blocks * p.n_blocks;
@@ -532,8 +536,8 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   const int n_blocks = (NC + BNR - 1) / BNR;
   const int NCP = n_blocks * BNR;
   dim3 sg_grid((c.d + 31) / 32, (NCP + 31) / 32);
-  k_router_split<<<sg_grid, dim3(32, 8), 0, s>>>(c.d, c.E, noisy, NC, NCP, BNR, Wg, Wn,
-                                                 static_cast<__nv_bfloat16 *>(bsplit));
+  launch_pdl(k_router_split, sg_grid, dim3(32, 8), 0, s, c.d, c.E, noisy, NC, NCP, BNR, Wg, Wn,
+      static_cast<__nv_bfloat16 *>(bsplit));
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb, tc, ts, th;
@@ -553,7 +557,7 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   if (err != cudaSuccess) return err;
   const int tiles = ((c.T + RBM - 1) / RBM) * n_blocks;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  k_router_tc<BNR><<<grid, kRThreads, smem, s>>>(ta, tb, tc, ts, th, p);
+  launch_pdl(k_router_tc<BNR>, grid, kRThreads, smem, s, ta, tb, tc, ts, th, p);
   return cudaGetLastError();
 }
 

@@ -19,6 +19,8 @@ template <typename V>
 __global__ void __launch_bounds__(kRowWarps * 32)
 k_gather(int A, int k, int nvec, const V *__restrict__ x, const int32_t *__restrict__ offset_end,
          const int32_t *__restrict__ row_token, V *__restrict__ xbuf, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (r >= A || r >= *offset_end) return;
@@ -62,6 +64,8 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
           const int32_t *__restrict__ pos, const uint8_t *__restrict__ keep,
           const int32_t *__restrict__ idx, const int32_t *__restrict__ offset, T *__restrict__ y,
           DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kMaxK = 16;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -122,6 +126,8 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
                  const uint8_t *__restrict__ keep, const int32_t *__restrict__ idx,
                  const int32_t *__restrict__ offset, __nv_bfloat16 *__restrict__ y,
                  DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kMaxK = 16;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
@@ -204,16 +210,14 @@ cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *o
   dim3 grid((A + kRowWarps - 1) / kRowWarps);
   const int32_t *end = offset + cfg.E;
   if (row_bytes % 16 == 0) {
-    k_gather<uint4><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 16),
-                                                    (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
+    launch_pdl(k_gather<uint4>, grid, kRowWarps * 32, 0, s, A, cfg.k, (int)(row_bytes / 16),
+        (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
   } else if (row_bytes % 4 == 0) {
-    k_gather<uint32_t><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 4),
-                                                       (const uint32_t *)x, end, row_token,
-                                                       (uint32_t *)xbuf, st);
+    launch_pdl(k_gather<uint32_t>, grid, kRowWarps * 32, 0, s, A, cfg.k, (int)(row_bytes / 4),
+        (const uint32_t *)x, end, row_token, (uint32_t *)xbuf, st);
   } else {
-    k_gather<uint16_t><<<grid, kRowWarps * 32, 0, s>>>(A, cfg.k, (int)(row_bytes / 2),
-                                                       (const uint16_t *)x, end, row_token,
-                                                       (uint16_t *)xbuf, st);
+    launch_pdl(k_gather<uint16_t>, grid, kRowWarps * 32, 0, s, A, cfg.k, (int)(row_bytes / 2),
+        (const uint16_t *)x, end, row_token, (uint16_t *)xbuf, st);
   }
   return cudaGetLastError();
 }
@@ -228,26 +232,26 @@ cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zb
     auto yp = (__nv_bfloat16 *)y;
     if (cfg.d % 8 == 0 && cfg.k <= 4) {
       if (cfg.k <= 2)
-        k_combine_bf16x8<2, 2><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
-                                                               zbuf, pos, keep, idx, offset, yp, st);
+        launch_pdl_c(kPdlCombine, k_combine_bf16x8<2, 2>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
+            cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
       else
-        k_combine_bf16x8<4, 1><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
-                                                               zbuf, pos, keep, idx, offset, yp, st);
+        launch_pdl_c(kPdlCombine, k_combine_bf16x8<4, 1>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
+            cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
     } else if (v4)
-      k_combine<__nv_bfloat16, true><<<grid, kRowWarps * 32, 0, s>>>(
-          cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+      launch_pdl_c(kPdlCombine, k_combine<__nv_bfloat16, true>, grid, kRowWarps * 32, 0, s, cfg.T,
+          cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
     else
-      k_combine<__nv_bfloat16, false><<<grid, kRowWarps * 32, 0, s>>>(
-          cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+      launch_pdl_c(kPdlCombine, k_combine<__nv_bfloat16, false>, grid, kRowWarps * 32, 0, s, cfg.T,
+          cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
   } else {
     auto xp = (const float *)x;
     auto yp = (float *)y;
     if (v4)
-      k_combine<float, true><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp, zbuf,
-                                                             pos, keep, idx, offset, yp, st);
+      launch_pdl_c(kPdlCombine, k_combine<float, true>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
+          cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
     else
-      k_combine<float, false><<<grid, kRowWarps * 32, 0, s>>>(cfg.T, cfg.d, cfg.E, cfg.k, xp,
-                                                              zbuf, pos, keep, idx, offset, yp, st);
+      launch_pdl_c(kPdlCombine, k_combine<float, false>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
+          cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
   }
   return cudaGetLastError();
 }

@@ -25,6 +25,8 @@ constexpr int kRankWarps = 8;
 __global__ void __launch_bounds__(kHistThreads)
 k_slot_hist(int A, int E, const int32_t *__restrict__ idx, int32_t *__restrict__ hist,
             DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t sh_hist[];
   if (blockIdx.x == 0 && threadIdx.x == 0) st->slot_ticket = 0;  // for k_slot_scan, next in order
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh_hist[e] = 0;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(kScanThreads)
 k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
             int32_t *__restrict__ count, int32_t *__restrict__ offset,
             int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NW = kScanThreads / 32;
   __shared__ int seg[NW][33];
   __shared__ int sh_warp[33];
@@ -154,6 +158,8 @@ k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *_
             const int32_t *__restrict__ hist_base, const int32_t *__restrict__ offset,
             int32_t *__restrict__ pos, uint8_t *__restrict__ keep, int32_t *__restrict__ row_token,
             float *__restrict__ row_gate) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t sh_cnt[];  // [kRankWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int chunk = blockIdx.x;
@@ -220,11 +226,12 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
                          int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
                          float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s) {
   const int A = cfg.T * cfg.k;
-  k_slot_hist<<<n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s>>>(A, cfg.E, idx, hist, st);
+  launch_pdl(k_slot_hist, n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s, A, cfg.E, idx, hist,
+      st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  k_slot_scan<<<(cfg.E + 31) / 32, kScanThreads, 0, s>>>(cfg.E, C, n_chunks, kTcBM, chunk_base,
-                                                         count, offset, mtiles, hist, st);
+  launch_pdl(k_slot_scan, (cfg.E + 31) / 32, kScanThreads, 0, s, cfg.E, C, n_chunks, kTcBM,
+      chunk_base, count, offset, mtiles, hist, st);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   size_t smem = (size_t)kRankWarps * cfg.E * sizeof(int32_t);
@@ -233,8 +240,8 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
                                (int)smem);
     if (err != cudaSuccess) return err;
   }
-  k_slot_rank<<<n_chunks, kRankWarps * 32, smem, s>>>(A, cfg.E, C, idx, gate, chunk_base, offset,
-                                                      pos, keep, row_token, row_gate);
+  launch_pdl(k_slot_rank, n_chunks, kRankWarps * 32, smem, s, A, cfg.E, C, idx, gate, chunk_base,
+      offset, pos, keep, row_token, row_gate);
   return cudaGetLastError();
 }
 

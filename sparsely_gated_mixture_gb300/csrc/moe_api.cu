@@ -6,11 +6,20 @@
 #include <mutex>
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 namespace moe {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool pdl_enabled(int cls) {
+  static const unsigned mask = [] {
+    const char *v = getenv("MOE_PDL_MASK");
+    return v && *v ? (unsigned)strtoul(v, nullptr, 0) : ~0u;
+  }();
+  return (mask >> cls) & 1u;
+}
 
 WsLayout ws_layout(const moe_config &cfg) {
   WsLayout L{};

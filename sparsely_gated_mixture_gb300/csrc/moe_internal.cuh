@@ -6,9 +6,52 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
+
+// ----------------------------------------------------------------------------- dependent launch
+// Every kernel of the library is launched with programmatic dependent launch:
+// it may become resident while the previous kernel on the stream drains, and
+// it calls pdl_wait() before touching global memory that earlier work writes
+// or reads (the wait returns once the previous grid has completed and its
+// writes are visible), then pdl_trigger() so the next kernel can be scheduled
+// early. A kernel whose predecessor is not a kernel (a memset, an event wait)
+// starts in stream order and its wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch classes for the PDL switch: the environment variable MOE_PDL_MASK
+// (read once; default all) keeps the attribute for the classes whose bit is
+// set, so each kind of edge can be compared with plain stream order.
+enum PdlClass { kPdlOther = 0, kPdlGemm = 1, kPdlCombine = 2, kPdlFinalize = 3 };
+bool pdl_enabled(int cls = kPdlOther);
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl_c(int cls, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                                size_t smem, cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled(cls) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+  return launch_pdl_c(kPdlOther, kernel, grid, block, smem, s, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------- tiling constants
 constexpr int kSlotChunk = 512;     // assignments ranked per warp in the slot pass
