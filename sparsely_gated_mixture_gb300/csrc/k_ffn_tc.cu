@@ -44,9 +44,10 @@ struct Params {
   const int32_t *offset;  // [E+1] packed-row offsets
   const float *row_gate;  // layer 2 only
   const __nv_bfloat16 *bias;  // [E, N] or null
-  void *out;              // layer 1: bf16 [rows, N]; layer 2: fp32 [rows, N]
+  void *out;              // layer 1: bf16 [rows, N]; layer 2: fp32 (or bf16) [rows, N]
   DeviceStatus *st;
   unsigned long long wait_ns;  // bounded-wait limit
+  int z_bf16;                  // layer 2 writes Z in bf16
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -272,16 +273,30 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             reinterpret_cast<uint4 *>(o)[q] =
                 make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
         } else {
-          float *o = static_cast<float *>(p.out) + r * p.N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             f[j] *= g;
             bad |= !isfinite(f[j]);
           }
+          if (p.z_bf16) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
+            uint32_t packed[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4 *>(o)[q] =
-                make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+              packed[j] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                           packed[4 * q + 2], packed[4 * q + 3]);
+          } else {
+            float *o = static_cast<float *>(p.out) + r * p.N + n;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4 *>(o)[q] =
+                  make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+          }
         }
       }
       if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)r);
@@ -569,16 +584,30 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             reinterpret_cast<uint4 *>(o)[q] =
                 make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
         } else {
-          float *o = static_cast<float *>(p.out) + r * p.N + n;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             f[j] *= g;
             bad |= !isfinite(f[j]);
           }
+          if (p.z_bf16) {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
+            uint32_t packed[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4 *>(o)[q] =
-                make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+              packed[j] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                           packed[4 * q + 2], packed[4 * q + 3]);
+          } else {
+            float *o = static_cast<float *>(p.out) + r * p.N + n;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4 *>(o)[q] =
+                  make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+          }
         }
       }
       if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)r);
@@ -737,8 +766,8 @@ bool ffn_tc_supported(const moe_config &c) {
 
 cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const int32_t *offset,
                           const int32_t *mtiles, const float *row_gate, const void *W1,
-                          const void *b1, const void *W2, const void *b2, void *hbuf, float *zbuf,
-                          DeviceStatus *st, cudaStream_t s) {
+                          const void *b1, const void *W2, const void *b2, void *hbuf, void *zbuf,
+                          bool z_bf16, DeviceStatus *st, cudaStream_t s) {
   (void)mtiles;
   const uint64_t A = (uint64_t)c.T * c.k;
   CUtensorMap ta1, tb1, ta2, tb2;
@@ -748,7 +777,7 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
   Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b1), hbuf, st, wait_limit_ns()};
   Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, offset, row_gate,
-            static_cast<const __nv_bfloat16 *>(b2), zbuf, st, wait_limit_ns()};
+            static_cast<const __nv_bfloat16 *>(b2), zbuf, st, wait_limit_ns(), z_bf16 ? 1 : 0};
   // Per layer: the CTA pair pays off for long K and enough 256-row tiles to
   // fill several waves; otherwise the one-CTA kernel's finer tiles win.
   const long rows = (long)c.T * c.k < (long)c.E * C ? (long)c.T * c.k : (long)c.E * C;

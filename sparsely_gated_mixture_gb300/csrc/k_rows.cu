@@ -116,13 +116,14 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
 }
 
 // Combine for bf16 rows with d % 8 == 0: each lane handles NG groups of 8
-// consecutive elements per step (16-byte loads of x and y, 32 bytes of each
-// kept Z row per group), with every load of the step issued first; two groups
-// when k <= 2, one when k <= 4 (register budget).
-template <int KM, int NG>  // at most KM choices per token; NG 8-element groups per lane-step
+// consecutive elements per step (16-byte loads of x and y; 32 bytes of each
+// kept Z row per group, or 16 when Z is bf16 (ZB)), with every load of the
+// step issued first; two groups when k <= 2, one when k <= 4 (register
+// budget). The sum runs in fp32 in choice order either way.
+template <int KM, int NG, bool ZB>  // at most KM choices per token; NG groups per lane-step
 __global__ void __launch_bounds__(kRowWarps * 32)
 k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ x,
-                 const float *__restrict__ zbuf, const int32_t *__restrict__ pos,
+                 const void *__restrict__ zbuf, const int32_t *__restrict__ pos,
                  const uint8_t *__restrict__ keep, const int32_t *__restrict__ idx,
                  const int32_t *__restrict__ offset, __nv_bfloat16 *__restrict__ y,
                  DeviceStatus *st) {
@@ -159,13 +160,30 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
 #pragma unroll
     for (int i = 0; i < KM; ++i) {
       if (i >= nr) break;
-      const float4 *zr = reinterpret_cast<const float4 *>(zbuf + (size_t)rows[i] * d);
-      z[i][0] = zr[2 * v0];
-      z[i][1] = zr[2 * v0 + 1];
-      if constexpr (NG > 1) {
-        if (has1) {
-          z[i][2] = zr[2 * v1];
-          z[i][3] = zr[2 * v1 + 1];
+      if constexpr (ZB) {
+        const uint4 *zr =
+            reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(zbuf) +
+                                            (size_t)rows[i] * d);
+#pragma unroll
+        for (int h = 0; h < NG; ++h) {
+          if (h == 1 && !has1) break;
+          const uint4 zv = zr[h ? v1 : v0];
+          const __nv_bfloat162 *zb = reinterpret_cast<const __nv_bfloat162 *>(&zv);
+          const float2 f0 = __bfloat1622float2(zb[0]), f1 = __bfloat1622float2(zb[1]);
+          const float2 f2 = __bfloat1622float2(zb[2]), f3 = __bfloat1622float2(zb[3]);
+          z[i][2 * h] = make_float4(f0.x, f0.y, f1.x, f1.y);
+          z[i][2 * h + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
+        }
+      } else {
+        const float4 *zr = reinterpret_cast<const float4 *>(static_cast<const float *>(zbuf) +
+                                                            (size_t)rows[i] * d);
+        z[i][0] = zr[2 * v0];
+        z[i][1] = zr[2 * v0 + 1];
+        if constexpr (NG > 1) {
+          if (has1) {
+            z[i][2] = zr[2 * v1];
+            z[i][3] = zr[2 * v1 + 1];
+          }
         }
       }
     }
@@ -222,7 +240,7 @@ cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *o
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zbuf,
+cudaError_t launch_combine(const moe_config &cfg, const void *x, const void *zbuf, bool z_bf16,
                            const int32_t *pos, const uint8_t *keep, const int32_t *idx,
                            const int32_t *offset, void *y, DeviceStatus *st, cudaStream_t s) {
   dim3 grid((cfg.T + kRowWarps - 1) / kRowWarps);
@@ -231,27 +249,36 @@ cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zb
     auto xp = (const __nv_bfloat16 *)x;
     auto yp = (__nv_bfloat16 *)y;
     if (cfg.d % 8 == 0 && cfg.k <= 4) {
-      if (cfg.k <= 2)
-        launch_pdl_c(kPdlCombine, k_combine_bf16x8<2, 2>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
-            cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
-      else
-        launch_pdl_c(kPdlCombine, k_combine_bf16x8<4, 1>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
-            cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+#define MOE_COMB(KM, NG, ZB)                                                                       \
+  launch_pdl_c(kPdlCombine, k_combine_bf16x8<KM, NG, ZB>, grid, kRowWarps * 32, 0, s, cfg.T,       \
+      cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st)
+      if (cfg.k <= 2) {
+        if (z_bf16) MOE_COMB(2, 2, true);
+        else MOE_COMB(2, 2, false);
+      } else {
+        if (z_bf16) MOE_COMB(4, 1, true);
+        else MOE_COMB(4, 1, false);
+      }
+#undef MOE_COMB
+    } else if (z_bf16) {
+      return cudaErrorInvalidValue;  // bf16 Z is only produced for this form
     } else if (v4)
       launch_pdl_c(kPdlCombine, k_combine<__nv_bfloat16, true>, grid, kRowWarps * 32, 0, s, cfg.T,
-          cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+          cfg.d, cfg.E, cfg.k, xp, (const float *)zbuf, pos, keep, idx, offset, yp, st);
     else
       launch_pdl_c(kPdlCombine, k_combine<__nv_bfloat16, false>, grid, kRowWarps * 32, 0, s, cfg.T,
-          cfg.d, cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+          cfg.d, cfg.E, cfg.k, xp, (const float *)zbuf, pos, keep, idx, offset, yp, st);
   } else {
+    if (z_bf16) return cudaErrorInvalidValue;
     auto xp = (const float *)x;
     auto yp = (float *)y;
+    auto zf = (const float *)zbuf;
     if (v4)
       launch_pdl_c(kPdlCombine, k_combine<float, true>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
-          cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+          cfg.E, cfg.k, xp, zf, pos, keep, idx, offset, yp, st);
     else
       launch_pdl_c(kPdlCombine, k_combine<float, false>, grid, kRowWarps * 32, 0, s, cfg.T, cfg.d,
-          cfg.E, cfg.k, xp, zbuf, pos, keep, idx, offset, yp, st);
+          cfg.E, cfg.k, xp, zf, pos, keep, idx, offset, yp, st);
   }
   return cudaGetLastError();
 }

@@ -120,15 +120,26 @@ static int gate_impl(const moe_config &c, const void *x, const float *Wg, const 
   return MOE_OK;
 }
 
+// Inside moe_forward the expert outputs Z stay in bf16 when the layer runs on
+// the tensor cores and combines 16 bytes at a time (the stage calls keep the
+// fp32 zbuf of their contract): half the Z traffic, one more bf16 rounding per
+// expert term before the fp32 combine.
+static bool forward_z_bf16(const moe_config &c) {
+  return c.act_dtype == MOE_BF16 && ffn_tc_supported(c) && c.d % 8 == 0 && c.k <= 4;
+}
+
 static int ffn_impl(const moe_config &c, const void *xbuf, const int32_t *offset,
                     const int32_t *mtiles, const float *row_gate, const void *W1, const void *b1,
-                    const void *W2, const void *b2, void *hbuf, float *zbuf, DeviceStatus *st,
-                    cudaStream_t s) {
+                    const void *W2, const void *b2, void *hbuf, void *zbuf, bool z_bf16,
+                    DeviceStatus *st, cudaStream_t s) {
   const int C = host_capacity(c);
   if (c.act_dtype == MOE_BF16 && ffn_tc_supported(c)) {
-    MOE_CUDA(launch_ffn_tc(c, C, xbuf, offset, mtiles, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+    MOE_CUDA(launch_ffn_tc(c, C, xbuf, offset, mtiles, row_gate, W1, b1, W2, b2, hbuf, zbuf,
+                           z_bf16, st, s));
   } else {
-    MOE_CUDA(launch_ffn_simt(c, C, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+    if (z_bf16) return MOE_ERR_UNSUPPORTED;
+    MOE_CUDA(launch_ffn_simt(c, C, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf,
+                             static_cast<float *>(zbuf), st, s));
   }
   return MOE_OK;
 }
@@ -245,7 +256,7 @@ int moe_expert_ffn(const moe_config *cfg, const void *xbuf, const int32_t *exper
   MOE_REQ(W2); MOE_OPT(b2); MOE_REQ(hbuf); MOE_REQ(zbuf);
   if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
   const WsLayout L = ws_layout(*cfg);
-  return ffn_impl(*cfg, xbuf, expert_offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf,
+  return ffn_impl(*cfg, xbuf, expert_offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf, false,
                   ws_at<DeviceStatus>(ws, L.status), (cudaStream_t)stream);
 }
 
@@ -258,7 +269,7 @@ int moe_combine(const moe_config *cfg, const void *x, const float *zbuf, const i
   MOE_REQ(expert_offset); MOE_REQ(y);
   if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
   const WsLayout L = ws_layout(*cfg);
-  MOE_CUDA(launch_combine(*cfg, x, zbuf, pos, keep, expert_idx, expert_offset, y,
+  MOE_CUDA(launch_combine(*cfg, x, zbuf, false, pos, keep, expert_idx, expert_offset, y,
                           ws_at<DeviceStatus>(ws, L.status), (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -325,10 +336,11 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
                         ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
                         s));
   MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
+  const bool z_bf16 = forward_z_bf16(c);
   r = ffn_impl(c, xbuf, offset, ws_at<int32_t>(ws, L.mtiles), row_gate, W1, b1, W2, b2, hbuf,
-               zbuf, st, s);
+               zbuf, z_bf16, st, s);
   if (r != MOE_OK) return r;
-  MOE_CUDA(launch_combine(c, x, zbuf, ps, kp, idx, offset, y, st, s));
+  MOE_CUDA(launch_combine(c, x, zbuf, z_bf16, ps, kp, idx, offset, y, st, s));
   if (side) {
     // Join: work enqueued on `stream` after this call also waits for the losses.
     MOE_CUDA(cudaEventRecord(side->join, side->s));

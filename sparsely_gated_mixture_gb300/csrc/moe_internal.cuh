@@ -137,7 +137,7 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
 cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,
                           const int32_t *row_token, void *xbuf, DeviceStatus *st,
                           cudaStream_t s);
-cudaError_t launch_combine(const moe_config &cfg, const void *x, const float *zbuf,
+cudaError_t launch_combine(const moe_config &cfg, const void *x, const void *zbuf, bool z_bf16,
                            const int32_t *pos, const uint8_t *keep, const int32_t *idx,
                            const int32_t *offset, void *y, DeviceStatus *st, cudaStream_t s);
 
@@ -151,7 +151,8 @@ cudaError_t launch_ffn_simt(const moe_config &cfg, int C, const void *xbuf, cons
 bool ffn_tc_supported(const moe_config &cfg);
 cudaError_t launch_ffn_tc(const moe_config &cfg, int C, const void *xbuf, const int32_t *offset,
                           const int32_t *mtiles, const float *row_gate, const void *W1,
-                          const void *b1, const void *W2, const void *b2, void *hbuf, float *zbuf,
-                          DeviceStatus *st, cudaStream_t s);
+                          const void *b1, const void *W2, const void *b2, void *hbuf, void *zbuf,
+                          bool z_bf16, DeviceStatus *st,
+                          cudaStream_t s);  // z_bf16: Z in bf16 (else fp32)
 
 }  // namespace moe

@@ -102,7 +102,14 @@ def check_forward(w, inp, tokens, stages=None):
     used, g_ref, *_ = _compare(w, inp, res, ref_gate, tokens, report)
     _check_aux(w, inp, ref_gate, used, g_ref, res["out3"])
     if stages is not None:
-        assert torch.equal(res["y"], stages["y"]), "moe_forward and the stage calls differ"
+        if w.dtype == "bf16":
+            # moe_forward may keep the expert outputs in bf16 where the stage
+            # calls keep fp32 (one more rounding per term); both are checked
+            # against the oracle above, and against each other here.
+            check_close(act_to_f64(res["y"]), act_to_f64(stages["y"]), w.dtype,
+                        "moe_forward against the stage calls")
+        else:
+            assert torch.equal(res["y"], stages["y"]), "moe_forward and the stage calls differ"
     return res, report
 
 
