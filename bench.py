@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) of the expert FFN stage per step, from one ncu
 # capture (profiles/expert_ffn_tc_pair_top2_large_experts.md), valid only for
 # the kernel source it was taken on (hash of k_ffn_tc.cu + tc_ptx.cuh).
-FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4196312832, "source": "a7cea8e015e15c83"}}
+FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4142578176, "source": "c415a17f27aa098b"}}
 
 
 def ffn_source_hash() -> str:

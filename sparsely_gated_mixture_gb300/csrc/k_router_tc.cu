@@ -388,6 +388,8 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
     const int sub = (warp - 2) >> 2;    // this warp's chunks: sub, sub+2, ...
     int local = 0;
+    float nz_next[16];  // noise of this warp's next unit (TMA-store epilogue)
+    int nz_tile = -1;   // the tile whose first unit nz_next already holds
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
       const int buf = local & 1;
@@ -403,19 +405,32 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const int t = t0 + lane;
       const int ncols = min(p.NC - nb * BNR, BNR);
       if (p.tma_out) {
-        // Units of 16 experts: 32 columns (clean/noise pairs) or 16. The
-        // next unit's noise is loaded while this one is computed.
+        // Units of 16 experts: 32 columns (clean/noise pairs) or 16. The next
+        // unit's noise is loaded while this one is computed; after this
+        // warp's last unit of the tile, its first unit of the CTA's next tile,
+        // so the load overlaps the wait for the next accumulator.
         const int upc = p.noisy ? 32 : 16;
         const int nunits = (ncols + upc - 1) / upc;
         const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first expert of the block
-        float nz_next[16];
-        if (p.noisy && sub < nunits) load_noise16(p, t, eb + sub * 16, nz_next);
+        if (p.noisy && sub < nunits && nz_tile != tile) load_noise16(p, t, eb + sub * 16, nz_next);
 #pragma unroll 1
         for (int u = sub; u < nunits; u += 2) {
           float nz[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) nz[j] = nz_next[j];
-          if (p.noisy && u + 2 < nunits) load_noise16(p, t, eb + (u + 2) * 16, nz_next);
+          if (p.noisy) {
+            if (u + 2 < nunits) {
+              load_noise16(p, t, eb + (u + 2) * 16, nz_next);
+            } else if (tile + (int)gridDim.x < total) {
+              const int nt = tile + gridDim.x;
+              const int nmb = nt / p.n_blocks, nnb = nt % p.n_blocks;
+              const int nncols = min(p.NC - nnb * BNR, BNR);
+              if (sub < (nncols + upc - 1) / upc) {
+                load_noise16(p, nmb * RBM + quad * 32 + lane, ((nnb * BNR) >> 1) + sub * 16, nz_next);
+                nz_tile = nt;
+              }
+            }
+          }
           float cv[16], zv[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) cv[j] = zv[j] = 0.f;
