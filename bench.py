@@ -76,6 +76,24 @@ def dist_env():
     return rank, world, local
 
 
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """A per-rank time made the job's: the maximum over all ranks (the job
+    ends with its slowest replica). Needs an initialised process group when
+    world > 1."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def workload_config(w: wl.Workload, extra: dict) -> dict:
     cfg = {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "d_ff": w.d_ff, "k": w.k,
            "capacity_factor": w.cf, "gate": w.mode, "noisy": w.noisy, "capacity": w.capacity,
@@ -271,10 +289,7 @@ def run_ours(args, w: wl.Workload):
            for j, s in enumerate(stages)}
     stage_sum_ms = statistics.mean(sum(per[s][i] for s in stages) for i in range(args.steps))
     ms = statistics.mean(fevs[i][0].elapsed_time(fevs[i][1]) for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(ms, world, dev)
 
     # End to end through the public call moe_forward, as a user streaming
     # batches from the host would run it: every step copies its x and noise in
@@ -337,10 +352,7 @@ def run_ours(args, w: wl.Workload):
     b_ev.record(copy_s)
     torch.cuda.synchronize()
     e2e_ms = a_ev.elapsed_time(b_ev) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank_ms(e2e_ms, world, dev)
     st, det = B.moe_last_device_status(ws, stream)
     if st != 0:
         raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the e2e region")
@@ -371,7 +383,7 @@ def run_ours(args, w: wl.Workload):
                     "hbm_frac": bw(tr["combine_bytes"], "combine") / peaks["hbm_gbs"]},
         "aux_loss": {"ms": mean["aux_loss"]},
     }
-    tps = world * T / (ms * 1e-3)
+    tps = job_tokens_per_s(world, T, ms)
     # router (plus the weight split that feeds the tensor-core router for bf16
     # tokens), selection with the balancing partials (one fused kernel up to
     # 256 experts, two beyond), slot histogram / scan / rank, gather, two
@@ -413,7 +425,8 @@ def run_ours(args, w: wl.Workload):
         "roofline": roof,
         "stages": stage_rep,
         "stage_sum_ms": stage_sum_ms,
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
                 "overlap": "copies of steps i+1 and i-1 overlap the compute of step i",
                 "h2d_bytes_per_step": x.numel() * x.element_size()
                 + (0 if noise is None else noise.numel() * 4),
