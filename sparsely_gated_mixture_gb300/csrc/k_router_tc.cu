@@ -19,11 +19,13 @@
 // operands K-major, 128B swizzle) into one of two TMEM accumulators, whose
 // three BNR-wide sections are summed per column, and eight epilogue
 // warps (two per TMEM lane quadrant) turn each token's columns into
-// c = acc + b, sigma = Softplus(z) and H = c + noise * sigma, 16 experts at a
-// time: the [32 tokens x 16 experts] fp32 tiles of c, sigma and H go to
-// shared memory (64-byte swizzle) and out with one TMA store each (only H
-// without the noise term, where c = H and sigma = 0). Rows of E floats that
-// are not 16-byte multiples (E % 4 != 0) take a staged store per row segment.
+// c = acc + b, sigma = Softplus(z) and H = c + noise * sigma, 16 accumulator
+// columns at a time: 8 experts with the noise term (clean/noise pairs), whose
+// [32 tokens x 8 experts] fp32 tiles of c, sigma and H go to shared memory
+// (32-byte swizzle) and out with one TMA store each; 16 experts without it,
+// where only H is written ([32 x 16], 64-byte swizzle; c = H, sigma = 0). Rows
+// of E floats that are not 16-byte multiples (E % 4 != 0) take a staged store
+// per row segment, on one warp per quadrant.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -31,7 +33,7 @@ namespace moe {
 namespace {
 
 constexpr int RBM = 128, RBK = 64;
-constexpr int kREpiWarps = 8;  // two per TMEM lane quadrant, alternating 16-column chunks
+constexpr int kREpiWarps = 8;  // two per TMEM lane quadrant, taking 16-column units in turn
 constexpr int kRThreads = 64 + 32 * kREpiWarps;
 
 struct RParams {
@@ -82,6 +84,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Row l of a [32 x 8] fp32 tile in the 32-byte swizzle of the TMA store:
+// 16-byte chunk q of row l sits at chunk q ^ ((l >> 2) & 1).
+__device__ __forceinline__ void tile_row_store8(float *tile, int l, const float *v) {
+  float4 *row = reinterpret_cast<float4 *>(tile + l * 8);
+  const int x = (l >> 2) & 1;
+  row[x] = make_float4(v[0], v[1], v[2], v[3]);
+  row[1 ^ x] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 // Row l of a [32 x 16] fp32 tile in the 64-byte swizzle of the TMA store:
 // 16-byte chunk q of row l sits at chunk q ^ ((l >> 1) & 3).
 __device__ __forceinline__ void tile_row_store(float *tile, int l, const float *v) {
@@ -130,10 +141,15 @@ __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP, int BNR
   }
 }
 
-// Epilogue staging: per epilogue warp, three [32 rows x 16 experts] fp32
-// tiles (c, sigma, H out), columns XOR-swizzled by row to spread banks.
+// Epilogue staging, 24 KB (kept small so that more pipeline stages fit:
+// the mainloop is bound by how many bytes are in flight). TMA-store path: per
+// epilogue warp 3 KB, three [32 x 8] fp32 tiles (c, sigma, H) or one [32 x 16]
+// H tile. Row-segment path: per warp of the first of each quadrant, 6 KB,
+// three [32 rows x 16 experts] tiles with columns XOR-swizzled by row.
 constexpr int kEpiTile = 32 * 16;
-constexpr int EPI_BYTES = kREpiWarps * 3 * kEpiTile * 4;  // 8 warps x 3 tiles = 48 KB
+constexpr int kEpiWarpFloats = 3 * 32 * 8;  // TMA-store path, per warp
+constexpr int EPI_BYTES = 4 * 3 * kEpiTile * 4;
+static_assert(kREpiWarps * kEpiWarpFloats * 4 <= EPI_BYTES, "staging");
 
 template <int BNR>
 struct RCfg {
@@ -219,48 +235,50 @@ __device__ __forceinline__ void load_noise8(const RParams &p, int t, int e0, flo
   }
 }
 
-// Token t's noise draws for experts e0 .. e0+15 (zero past E or T).
-__device__ __forceinline__ void load_noise16(const RParams &p, int t, int e0, float *nz) {
-  if (t < p.T && (p.E & 3) == 0 && e0 + 16 <= p.E) {
-    const float4 *src = reinterpret_cast<const float4 *>(p.noise + (size_t)t * p.E + e0);
+// One unit of the TMA-store epilogue with the noise term: experts e0 .. e0+7
+// of tokens t0 .. t0+31 (lane l = token t0 + l). cv holds the clean logits and
+// zv the noise logits on entry; both are overwritten (c, then sigma, then H),
+// each [32 x 8] tile written to shared memory as soon as it is ready.
+__device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtensorMap *mc,
+                                                  const CUtensorMap *ms, const CUtensorMap *mh,
+                                                  int t0, int e0, float *cv, float *zv,
+                                                  const float *nz, float *stg) {
+  const int lane = threadIdx.x & 31;
+  float *sc = stg, *ss = stg + 256, *sh = stg + 512;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 a = src[q];
-      nz[4 * q] = a.x;
-      nz[4 * q + 1] = a.y;
-      nz[4 * q + 2] = a.z;
-      nz[4 * q + 3] = a.w;
-    }
-  } else {
+  for (int j = 0; j < 8; ++j)
+    if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
+  tile_row_store8(sc, lane, cv);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      nz[j] = (t < p.T && e0 + j < p.E) ? p.noise[(size_t)t * p.E + e0 + j] : 0.f;
+  for (int j = 0; j < 8; ++j) {
+    zv[j] = softplus_r(zv[j]);
+    cv[j] = fmaf(nz[j], zv[j], cv[j]);
+  }
+  tile_row_store8(ss, lane, zv);
+  tile_row_store8(sh, lane, cv);
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
+  if (bad && t0 + lane < p.T) record_error(p.st, MOE_ERR_NONFINITE, (long long)(t0 + lane));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(mh, sh, e0, t0);
+    tma_store_2d(mc, sc, e0, t0);
+    tma_store_2d(ms, ss, e0, t0);
+    bulk_commit();
   }
 }
 
-// One unit of the TMA-store epilogue: experts e0 .. e0+15 of tokens t0 .. t0+31
-// (lane l = token t0 + l). cv holds the clean logits and zv the noise logits
-// on entry; both are overwritten (c, then sigma, then H), each tile written to
-// shared memory as soon as it is ready.
-__device__ __forceinline__ void router_unit_tma(const RParams &p, const CUtensorMap *mc,
-                                                const CUtensorMap *ms, const CUtensorMap *mh,
-                                                int t0, int e0, float *cv, float *zv,
-                                                const float *nz, float *stg) {
+// One unit without the noise term: H = c for experts e0 .. e0+15, one
+// [32 x 16] tile.
+__device__ __forceinline__ void router_unit_clean(const RParams &p, const CUtensorMap *mh, int t0,
+                                                  int e0, float *cv, float *stg) {
   const int lane = threadIdx.x & 31;
-  float *sc = stg, *ss = stg + kEpiTile, *sh = stg + 2 * kEpiTile;
 #pragma unroll
   for (int j = 0; j < 16; ++j)
     if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
-  if (p.noisy) {
-    tile_row_store(sc, lane, cv);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      zv[j] = softplus_r(zv[j]);
-      cv[j] = fmaf(nz[j], zv[j], cv[j]);
-    }
-    tile_row_store(ss, lane, zv);
-  }
-  tile_row_store(sh, lane, cv);
+  tile_row_store(stg, lane, cv);
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < 16; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
@@ -268,11 +286,7 @@ __device__ __forceinline__ void router_unit_tma(const RParams &p, const CUtensor
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(mh, sh, e0, t0);
-    if (p.noisy) {
-      tma_store_2d(mc, sc, e0, t0);
-      tma_store_2d(ms, ss, e0, t0);
-    }
+    tma_store_2d(mh, stg, e0, t0);
     bulk_commit();
   }
 }
@@ -386,9 +400,9 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncwarp();
   } else {
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
-    const int sub = (warp - 2) >> 2;    // this warp's chunks: sub, sub+2, ...
+    const int sub = (warp - 2) >> 2;    // this warp's units: sub, sub+2, ...
     int local = 0;
-    float nz_next[16];  // noise of this warp's next unit (TMA-store epilogue)
+    float nz_next[8];   // noise of this warp's next unit
     int nz_tile = -1;   // the tile whose first unit nz_next already holds
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
       const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
@@ -401,82 +415,79 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const int t0 = mb * RBM + quad * 32;
       const uint32_t lane_addr =
           tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * C::NB);
-      float *stg = staging + (size_t)(warp - 2) * 3 * kEpiTile;
       const int t = t0 + lane;
       const int ncols = min(p.NC - nb * BNR, BNR);
       if (p.tma_out) {
-        // Units of 16 experts: 32 columns (clean/noise pairs) or 16. The next
+        // Units of 16 accumulator columns (8 experts with the noise term, 16
+        // without), dealt to the quadrant's two warps in turn. The next
         // unit's noise is loaded while this one is computed; after this
         // warp's last unit of the tile, its first unit of the CTA's next tile,
         // so the load overlaps the wait for the next accumulator.
-        const int upc = p.noisy ? 32 : 16;
-        const int nunits = (ncols + upc - 1) / upc;
+        float *stg = staging + (size_t)(warp - 2) * kEpiWarpFloats;
+        const int nunits = (ncols + 15) / 16;
+        const int epu = p.noisy ? 8 : 16;  // experts per unit
         const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first expert of the block
-        if (p.noisy && sub < nunits && nz_tile != tile) load_noise16(p, t, eb + sub * 16, nz_next);
+        if (p.noisy && sub < nunits && nz_tile != tile) load_noise8(p, t, eb + sub * 8, nz_next);
 #pragma unroll 1
         for (int u = sub; u < nunits; u += 2) {
-          float nz[16];
+          float nz[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) nz[j] = nz_next[j];
+          for (int j = 0; j < 8; ++j) nz[j] = nz_next[j];
           if (p.noisy) {
             if (u + 2 < nunits) {
-              load_noise16(p, t, eb + (u + 2) * 16, nz_next);
+              load_noise8(p, t, eb + (u + 2) * 8, nz_next);
             } else if (tile + (int)gridDim.x < total) {
               const int nt = tile + gridDim.x;
               const int nmb = nt / p.n_blocks, nnb = nt % p.n_blocks;
               const int nncols = min(p.NC - nnb * BNR, BNR);
-              if (sub < (nncols + upc - 1) / upc) {
-                load_noise16(p, nmb * RBM + quad * 32 + lane, ((nnb * BNR) >> 1) + sub * 16, nz_next);
+              if (sub < (nncols + 15) / 16) {
+                load_noise8(p, nmb * RBM + quad * 32 + lane, ((nnb * BNR) >> 1) + sub * 8,
+                            nz_next);
                 nz_tile = nt;
               }
             }
           }
-          float cv[16], zv[16];
+          uint32_t vh[16], vm[16], vl[16];
+          tmem_ld16(lane_addr + (uint32_t)(u * 16), vh);
+          tmem_ld16(lane_addr + (uint32_t)(BNR + u * 16), vm);
+          tmem_ld16(lane_addr + (uint32_t)(2 * BNR + u * 16), vl);
+          float v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cv[j] = zv[j] = 0.f;
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int col = u * upc + hh * 16;
-            if ((hh == 1 && !p.noisy) || col >= ncols) continue;  // warp-uniform
-            uint32_t vh[16], vm[16], vl[16];
-            tmem_ld16(lane_addr + (uint32_t)col, vh);
-            tmem_ld16(lane_addr + (uint32_t)(BNR + col), vm);
-            tmem_ld16(lane_addr + (uint32_t)(2 * BNR + col), vl);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float v =
-                  __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
-              if (p.noisy) {
-                if (j & 1)
-                  zv[hh * 8 + (j >> 1)] = v;
-                else
-                  cv[hh * 8 + (j >> 1)] = v;
-              } else {
-                cv[j] = v;
-              }
-            }
-          }
+          for (int j = 0; j < 16; ++j)
+            v[j] = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
           if (lane == 0) bulk_wait_read_all();  // the last unit's stores have read the tiles
           __syncwarp();
-          router_unit_tma(p, &tmC, &tmS, &tmH, t0, eb + u * 16, cv, zv, nz, stg);
+          if (p.noisy) {
+            float cv[8], zv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              cv[j] = v[2 * j];
+              zv[j] = v[2 * j + 1];
+            }
+            router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg);
+          } else {
+            router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         continue;
       }
-      const int nchunks = (ncols + 15) / 16;
+      // Row-segment path: the first warp of each quadrant, 16 columns at a
+      // time.
+      float *stg = staging + (size_t)(warp - 2) * 3 * kEpiTile;
+      const int nchunks = sub == 0 ? (ncols + 15) / 16 : 0;
       // 16 columns at a time: 8 experts (noisy, clean/noise pairs) or 16.
       // The next chunk's noise is loaded while this one is computed.
-      float nz_next[8];
-      if (p.noisy && sub < nchunks) load_noise8(p, t, (nb * BNR + sub * 16) >> 1, nz_next);
+      if (p.noisy && nchunks > 0) load_noise8(p, t, (nb * BNR) >> 1, nz_next);
 #pragma unroll 1
-      for (int c16 = sub; c16 < nchunks; c16 += 2) {
+      for (int c16 = 0; c16 < nchunks; ++c16) {
         const int n = nb * BNR + c16 * 16;
         float nz[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) nz[j] = nz_next[j];
-        if (p.noisy && c16 + 2 < nchunks) load_noise8(p, t, (n + 32) >> 1, nz_next);
+        if (p.noisy && c16 + 1 < nchunks) load_noise8(p, t, (n + 16) >> 1, nz_next);
         // Column j of the block is hi[j] + (mid[j] + lo[j]), from the three
         // BNR-wide sections of the accumulator.
         uint32_t vh[16], vm[16], vl[16];
@@ -528,17 +539,19 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
 int tile_cols(int NC) { return NC <= 16 ? 16 : NC <= 32 ? 32 : 64; }
 
-// 2-D fp32 tensor [T, E] (E contiguous, E % 4 == 0), box [32 tokens, 16
-// experts], 64-byte swizzle: the router's output tiles.
-bool make_out_map(CUtensorMap *m, float *base, int T, int E) {
+// 2-D fp32 tensor [T, E] (E contiguous, E % 4 == 0): the router's output
+// tiles, box [32 tokens, 8 experts] in the 32-byte swizzle (noise term) or
+// [32 tokens, 16 experts] in the 64-byte swizzle (without).
+bool make_out_map(CUtensorMap *m, float *base, int T, int E, bool noisy) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)T};
   cuuint64_t strides[1] = {(cuuint64_t)E * 4};
-  cuuint32_t box[2] = {16, 32};
+  cuuint32_t box[2] = {noisy ? 8u : 16u, 32};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            noisy ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -561,8 +574,9 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
     return cudaErrorInvalidValue;
   // The TMA-store epilogue needs 16-byte rows and 16-byte-aligned outputs.
   const bool tma_out = c.E % 4 == 0 && (uintptr_t)cc % 16 == 0 && (uintptr_t)sg % 16 == 0 &&
-                       (uintptr_t)H % 16 == 0 && make_out_map(&tc, cc, c.T, c.E) &&
-                       make_out_map(&ts, sg, c.T, c.E) && make_out_map(&th, H, c.T, c.E);
+                       (uintptr_t)H % 16 == 0 && make_out_map(&tc, cc, c.T, c.E, noisy) &&
+                       make_out_map(&ts, sg, c.T, c.E, noisy) &&
+                       make_out_map(&th, H, c.T, c.E, noisy);
   if (!tma_out) th = ts = tc = ta;  // unused
   RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, tma_out ? 1 : 0, noise, bias, cc, sg, H, st,
             wait_limit_ns()};
