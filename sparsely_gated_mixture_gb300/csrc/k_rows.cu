@@ -58,6 +58,39 @@ struct Act<__nv_bfloat16> {
 
 // Combine: one warp per token; each lane handles groups of 4 consecutive
 // elements (VEC4) or single elements.
+// The packed rows of token t's kept choices, in choice order, on every lane:
+// lane j < k resolves choice j (keep, expert, slot -> row offset[e] + pos) so
+// the k lookups run side by side, then the rows are read from the lanes in
+// order. Returns their number; a bad index is recorded (MOE_ERR_BOUNDS) and
+// skipped.
+template <int KM>
+__device__ __forceinline__ int token_rows(int t, int k, int E, const uint8_t *__restrict__ keep,
+                                          const int32_t *__restrict__ idx,
+                                          const int32_t *__restrict__ pos,
+                                          const int32_t *__restrict__ offset, DeviceStatus *st,
+                                          int lane, int (&rows)[KM]) {
+  int r = -1;
+  if (lane < k) {
+    const size_t a = (size_t)t * k + lane;
+    if (keep[a]) {
+      const int e = idx[a];
+      const int rr = (e >= 0 && e < E) ? offset[e] + pos[a] : -1;
+      if (rr < 0 || rr >= offset[e + 1])
+        record_error(st, MOE_ERR_BOUNDS, (long long)a);
+      else
+        r = rr;
+    }
+  }
+  int nr = 0;
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    if (j >= k) break;
+    const int rj = __shfl_sync(0xffffffffu, r, j);
+    if (rj >= 0) rows[nr++] = rj;
+  }
+  return nr;
+}
+
 template <typename T, bool VEC4>
 __global__ void __launch_bounds__(kRowWarps * 32)
 k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__restrict__ zbuf,
@@ -71,18 +104,7 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
   int rows[kMaxK];
-  int nr = 0;
-  for (int j = 0; j < k; ++j) {
-    size_t a = (size_t)t * k + j;
-    if (!keep[a]) continue;
-    int e = idx[a];
-    int r = (e >= 0 && e < E) ? offset[e] + pos[a] : -1;
-    if (r < 0 || e < 0 || e >= E || r >= offset[e + 1]) {
-      if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)a);
-      continue;
-    }
-    rows[nr++] = r;
-  }
+  const int nr = token_rows<kMaxK>(t, k, E, keep, idx, pos, offset, st, lane, rows);
   const T *xr = x + (size_t)t * d;
   T *yr = y + (size_t)t * d;
   bool bad = false;
@@ -118,8 +140,8 @@ k_combine(int Tn, int d, int E, int k, const T *__restrict__ x, const float *__r
 // Combine for bf16 rows with d % 8 == 0: each lane handles NG groups of 8
 // consecutive elements per step (16-byte loads of x and y; 32 bytes of each
 // kept Z row per group, or 16 when Z is bf16 (ZB)), with every load of the
-// step issued first; two groups when k <= 2, one when k <= 4 (register
-// budget). The sum runs in fp32 in choice order either way.
+// step issued first; two groups when k <= 2 or Z is bf16, one for fp32 Z with
+// k <= 4 (register budget). The sum runs in fp32 in choice order either way.
 template <int KM, int NG, bool ZB>  // at most KM choices per token; NG groups per lane-step
 __global__ void __launch_bounds__(kRowWarps * 32)
 k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ x,
@@ -129,23 +151,11 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
                  DeviceStatus *st) {
   pdl_wait();
   pdl_trigger();
-  constexpr int kMaxK = 16;
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= Tn) return;
-  int rows[kMaxK];
-  int nr = 0;
-  for (int j = 0; j < k; ++j) {
-    const size_t a = (size_t)t * k + j;
-    if (!keep[a]) continue;
-    const int e = idx[a];
-    const int r = (e >= 0 && e < E) ? offset[e] + pos[a] : -1;
-    if (r < 0 || r >= offset[e + 1]) {
-      if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)a);
-      continue;
-    }
-    rows[nr++] = r;
-  }
+  int rows[KM];
+  const int nr = token_rows<KM>(t, k, E, keep, idx, pos, offset, st, lane, rows);
   const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
   uint4 *yr = reinterpret_cast<uint4 *>(y + (size_t)t * d);
   const int nv = d / 8;
@@ -156,7 +166,9 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
     const bool has1 = NG > 1 && v1 < nv;
     const uint4 xv0 = xr[v0];
     const uint4 xv1 = has1 ? xr[v1] : make_uint4(0, 0, 0, 0);
-    float4 z[KM][2 * NG];
+    // Z of each kept row: raw bf16 (16 bytes per group) or fp32 (32 bytes).
+    uint4 zb[ZB ? KM : 1][NG];
+    float4 zf[ZB ? 1 : KM][2 * NG];
 #pragma unroll
     for (int i = 0; i < KM; ++i) {
       if (i >= nr) break;
@@ -164,25 +176,18 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
         const uint4 *zr =
             reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(zbuf) +
                                             (size_t)rows[i] * d);
-#pragma unroll
-        for (int h = 0; h < NG; ++h) {
-          if (h == 1 && !has1) break;
-          const uint4 zv = zr[h ? v1 : v0];
-          const __nv_bfloat162 *zb = reinterpret_cast<const __nv_bfloat162 *>(&zv);
-          const float2 f0 = __bfloat1622float2(zb[0]), f1 = __bfloat1622float2(zb[1]);
-          const float2 f2 = __bfloat1622float2(zb[2]), f3 = __bfloat1622float2(zb[3]);
-          z[i][2 * h] = make_float4(f0.x, f0.y, f1.x, f1.y);
-          z[i][2 * h + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
-        }
+        zb[i][0] = zr[v0];
+        if constexpr (NG > 1)
+          if (has1) zb[i][1] = zr[v1];
       } else {
         const float4 *zr = reinterpret_cast<const float4 *>(static_cast<const float *>(zbuf) +
                                                             (size_t)rows[i] * d);
-        z[i][0] = zr[2 * v0];
-        z[i][1] = zr[2 * v0 + 1];
+        zf[i][0] = zr[2 * v0];
+        zf[i][1] = zr[2 * v0 + 1];
         if constexpr (NG > 1) {
           if (has1) {
-            z[i][2] = zr[2 * v1];
-            z[i][3] = zr[2 * v1 + 1];
+            zf[i][2] = zr[2 * v1];
+            zf[i][3] = zr[2 * v1 + 1];
           }
         }
       }
@@ -202,9 +207,19 @@ k_combine_bf16x8(int Tn, int d, int E, int k, const __nv_bfloat16 *__restrict__ 
 #pragma unroll
       for (int i = 0; i < KM; ++i) {
         if (i >= nr) break;
-        const float4 a0 = z[i][2 * h], a1 = z[i][2 * h + 1];
-        acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
-        acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
+        if constexpr (ZB) {
+          const __nv_bfloat162 *z2 = reinterpret_cast<const __nv_bfloat162 *>(&zb[i][h]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(z2[q]);
+            acc[2 * q] += f.x;
+            acc[2 * q + 1] += f.y;
+          }
+        } else {
+          const float4 a0 = zf[i][2 * h], a1 = zf[i][2 * h + 1];
+          acc[0] += a0.x; acc[1] += a0.y; acc[2] += a0.z; acc[3] += a0.w;
+          acc[4] += a1.x; acc[5] += a1.y; acc[6] += a1.z; acc[7] += a1.w;
+        }
       }
       uint4 out;
       __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&out);
@@ -256,7 +271,7 @@ cudaError_t launch_combine(const moe_config &cfg, const void *x, const void *zbu
         if (z_bf16) MOE_COMB(2, 2, true);
         else MOE_COMB(2, 2, false);
       } else {
-        if (z_bf16) MOE_COMB(4, 1, true);
+        if (z_bf16) MOE_COMB(4, 2, true);  // raw bf16 Z leaves room for two groups
         else MOE_COMB(4, 1, false);
       }
 #undef MOE_COMB
