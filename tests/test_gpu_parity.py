@@ -246,3 +246,34 @@ def test_tied_logits_wide(levels):
     res, _ = check_stages(w, inp)
     ref = oracle_gate(inp)
     assert np.array_equal(res["idx"], ref["idx"])
+
+
+CLEAN_TOPK = {
+    # Top-k without the noise term: the router writes H alone, the load sum is
+    # the pre-capacity count; E = 32 takes the fused selection, E = 512 the
+    # column sums.
+    "clean_top2_e32": wl.Workload("clean_top2_e32", T=300, d=128, E=32, d_ff=64, k=2, cf=1.0,
+                                  mode=wl.TOPK, dtype="bf16", noisy=False),
+    "clean_top3_e512": wl.Workload("clean_top3_e512", T=300, d=64, E=512, d_ff=64, k=3,
+                                   cf=1.5, mode=wl.TOPK, dtype="bf16", noisy=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CLEAN_TOPK))
+def test_clean_topk_parity(name):
+    w = CLEAN_TOPK[name]
+    inp = wl.generate(w, seed=23, biases=True)
+    stages, _ = check_stages(w, inp)
+    check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
+
+
+@pytest.mark.parametrize("E", [64, 512])
+def test_router_bias_with_noise(E):
+    """A router logit bias together with the noise term (c = x Wg + b, then
+    H = c + n sigma), on the fused (E = 64) and column (E = 512) paths."""
+    w = wl.Workload(f"noisy_bias_e{E}", T=400, d=128, E=E, d_ff=64, k=2, cf=1.25, mode=wl.TOPK,
+                    dtype="bf16", noisy=True)
+    inp = wl.generate(w, seed=29, biases=True)
+    inp["bias"] = (np.random.default_rng(5).standard_normal(E) * 0.5).astype(np.float32)
+    stages, _ = check_stages(w, inp)
+    check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
