@@ -42,7 +42,7 @@ NOMINAL_HBM_GBS = 8000.0  # the part's nominal HBM3e rate, reported beside the m
 # DRAM bytes (read + write) of the expert FFN stage per step, from one ncu
 # capture (profiles/expert_ffn_tc_pair_top2_large_experts.md), valid only for
 # the kernel source it was taken on (hash of k_ffn_tc.cu + tc_ptx.cuh).
-FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4142578176, "source": "c415a17f27aa098b"}}
+FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4150121984, "source": "d1d148fb66506d6d"}}
 
 
 def ffn_source_hash() -> str:

@@ -26,6 +26,8 @@
 
 #include <stdlib.h>
 
+#include <mutex>
+
 namespace moe {
 namespace {
 
@@ -630,16 +632,17 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 }  // namespace
 
 // ----------------------------------------------------------------------------- host side
+// Looked up once; a function-local static with an initializer is thread-safe.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -664,13 +667,12 @@ unsigned long long wait_limit_ns() {
 }
 
 int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
+  static const int n = [] {
+    int dev = 0, m = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
+    cudaDeviceGetAttribute(&m, cudaDevAttrMultiProcessorCount, dev);
+    return m > 0 ? m : 1;
+  }();
   return n;
 }
 
@@ -706,9 +708,18 @@ cudaLaunchAttribute pair_cluster_attr() {
 }
 
 // Clusters of two that can be resident at once (0 if the device cannot host one).
+// The answer depends on the shared-memory size (it grows with E), so it is kept
+// per size, under a lock, in a small table; a full table means no caching.
+std::mutex g_pair_mu;
+
 int pair_clusters(size_t smem) {
-  static int cached = -1;
-  if (cached >= 0) return cached;
+  constexpr int kSlots = 16;
+  static size_t keys[kSlots];
+  static int vals[kSlots];
+  static int used = 0;
+  std::lock_guard<std::mutex> lock(g_pair_mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == smem) return vals[i];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sm_count() / 2));
   cfg.blockDim = dim3(kThreads);
@@ -721,7 +732,11 @@ int pair_clusters(size_t smem) {
                            (int)smem) != cudaSuccess ||
       cudaOccupancyMaxActiveClusters(&n, k_ffn_tc_pair<1>, &cfg) != cudaSuccess)
     n = 0;
-  cached = n;
+  if (used < kSlots) {
+    keys[used] = smem;
+    vals[used] = n;
+    ++used;
+  }
   return n;
 }
 
@@ -748,12 +763,11 @@ cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const 
 // Clusters available to the CTA-pair kernel, or 0 when the one-CTA kernel must
 // run (MOE_FFN_TC_VARIANT=single asks for it; so does a device without room).
 int pair_clusters_for(int E) {
-  static int forced = -1;
-  if (forced < 0) {
+  static const bool single = [] {
     const char *v = getenv("MOE_FFN_TC_VARIANT");
-    forced = (v && v[0] == 's') ? 0 : 1;
-  }
-  if (!forced || smem_bytes_pair(E) > 227 * 1024) return 0;
+    return v && v[0] == 's';
+  }();
+  if (single || smem_bytes_pair(E) > 227 * 1024) return 0;
   return pair_clusters(smem_bytes_pair(E));
 }
 

@@ -953,11 +953,10 @@ cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg,
                           void *bsplit, DeviceStatus *st, cudaStream_t s) {
   const bool noisy = Wn != nullptr;
   // bf16 tokens: the tensor-core router (MOE_ROUTER=simt selects the CUDA-core kernels).
-  static int force_simt = -1;
-  if (force_simt < 0) {
+  static const bool force_simt = [] {
     const char *v = getenv("MOE_ROUTER");
-    force_simt = (v && v[0] == 's') ? 1 : 0;
-  }
+    return v && v[0] == 's';
+  }();
   if (!force_simt && router_tc_supported(cfg))
     return launch_router_tc(cfg, x, Wg, Wn, noise, bias, c, sigma, H, bsplit, st, s);
   // Vector path: whole 16-byte pieces of every x row, and a small expert count
