@@ -9,6 +9,7 @@
 // Balancing sums (Eqs. 6-10; Switch step 8): per-block partial sums in token
 // order, finished in fp64 by one block, so results are run-to-run identical.
 #include "moe_internal.cuh"
+#include "gate_math.cuh"
 
 #include <math.h>
 #include <stdlib.h>
@@ -524,32 +525,6 @@ k_select(int T, int E, int k, int mode, const float *__restrict__ H, int32_t *__
                   rowstat);
 }
 
-// Phi(u), the standard normal CDF, as erfc(-u / sqrt 2) / 2. erfc(z), z >= 0,
-// is the Chebyshev-fitted form of Numerical Recipes (Press et al., 2nd ed.,
-// section 6.2, "erfcc"): t exp(-z^2 + P(t)), t = 1 / (1 + z/2), P of degree 9,
-// fractional error below 1.2e-7 for every z; erfc(-z) = 2 - erfc(z). In fp32,
-// with z^2 compensated and the fast exponential, the relative error is about
-// 1e-6 wherever Phi > 1e-7, far inside the tolerance of the balancing sums.
-__device__ __forceinline__ float normal_cdf(float u) {
-  const float w = -u * 0.70710678118654752f;
-  const float z = fabsf(w);
-  const float t = __fdividef(1.f, fmaf(0.5f, z, 1.f));
-  float p = 0.17087277f;
-  p = fmaf(t, p, -0.82215223f);
-  p = fmaf(t, p, 1.48851587f);
-  p = fmaf(t, p, -1.13520398f);
-  p = fmaf(t, p, 0.27886807f);
-  p = fmaf(t, p, -0.18628806f);
-  p = fmaf(t, p, 0.09678418f);
-  p = fmaf(t, p, 0.37409196f);
-  p = fmaf(t, p, 1.00002368f);
-  p = fmaf(t, p, -1.26551223f);
-  const float zz = z * z;
-  const float ez = fmaf(z, z, -zz);  // z^2 = zz + ez exactly
-  const float half_erfc = 0.5f * t * __expf((p - zz) - ez);
-  return w >= 0.f ? half_erfc : 1.f - half_erfc;
-}
-
 // ----------------------------------------------------------------------------- balancing partials
 // Partials layout: [token block][4][E] = importance, load, first-choice count,
 // sum of Softmax(H), each a sum over the block's tokens.
@@ -950,15 +925,18 @@ k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
 
 cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
                           const float *noise, const float *bias, float *c, float *sigma, float *H,
-                          void *bsplit, DeviceStatus *st, cudaStream_t s) {
+                          void *bsplit, DeviceStatus *st, cudaStream_t s,
+                          const RouterSelect *sel, bool *selected) {
   const bool noisy = Wn != nullptr;
+  if (selected) *selected = false;
   // bf16 tokens: the tensor-core router (MOE_ROUTER=simt selects the CUDA-core kernels).
   static const bool force_simt = [] {
     const char *v = getenv("MOE_ROUTER");
     return v && v[0] == 's';
   }();
   if (!force_simt && router_tc_supported(cfg))
-    return launch_router_tc(cfg, x, Wg, Wn, noise, bias, c, sigma, H, bsplit, st, s);
+    return launch_router_tc(cfg, x, Wg, Wn, noise, bias, c, sigma, H, bsplit, st, s, sel,
+                            selected);
   // Vector path: whole 16-byte pieces of every x row, and a small expert count
   // (beyond it the per-block W traffic of this layout grows with E).
   const bool vec = cfg.E <= 64 &&

@@ -26,8 +26,11 @@
 // where only H is written ([32 x 16], 64-byte swizzle; c = H, sigma = 0). Rows
 // of E floats that are not 16-byte multiples (E % 4 != 0) take a staged store
 // per row segment, on one warp per quadrant.
+#include "gate_math.cuh"
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
+
+#include <stdlib.h>
 
 namespace moe {
 namespace {
@@ -42,6 +45,11 @@ struct RParams {
   float *c_out, *s_out, *H_out;
   DeviceStatus *st;
   unsigned long long wait_ns;  // bounded-wait limit
+  // Fused selection (one column block, one tile per CTA): k, gate mode and
+  // the selection outputs; partials may be null (no balancing sums).
+  int fused, k, mode;
+  int32_t *idx;
+  float *gate, *thr, *rowstat, *partials;
 };
 
 // Softplus(z) = max(z, 0) + log1p(t), t = exp(-|z|) in (0, 1]. log1p(t) is
@@ -239,16 +247,24 @@ __device__ __forceinline__ void load_noise8(const RParams &p, int t, int e0, flo
 // of tokens t0 .. t0+31 (lane l = token t0 + l). cv holds the clean logits and
 // zv the noise logits on entry; both are overwritten (c, then sigma, then H),
 // each [32 x 8] tile written to shared memory as soon as it is ready.
+// With fused selection, row points at this lane's token row in the shared
+// row buffers (c, sigma and H planes, plane stride ps floats); else null.
 __device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtensorMap *mc,
                                                   const CUtensorMap *ms, const CUtensorMap *mh,
                                                   int t0, int e0, float *cv, float *zv,
-                                                  const float *nz, float *stg) {
+                                                  const float *nz, float *stg, float *row,
+                                                  int ps) {
   const int lane = threadIdx.x & 31;
   float *sc = stg, *ss = stg + 256, *sh = stg + 512;
 #pragma unroll
   for (int j = 0; j < 8; ++j)
     if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
   tile_row_store8(sc, lane, cv);
+  if (row) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (e0 + j < p.E) row[ps + e0 + j] = cv[j];
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     zv[j] = softplus_r(zv[j]);
@@ -256,6 +272,14 @@ __device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtens
   }
   tile_row_store8(ss, lane, zv);
   tile_row_store8(sh, lane, cv);
+  if (row) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (e0 + j < p.E) {
+        row[e0 + j] = cv[j];
+        row[2 * ps + e0 + j] = zv[j];
+      }
+  }
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
@@ -273,12 +297,17 @@ __device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtens
 // One unit without the noise term: H = c for experts e0 .. e0+15, one
 // [32 x 16] tile.
 __device__ __forceinline__ void router_unit_clean(const RParams &p, const CUtensorMap *mh, int t0,
-                                                  int e0, float *cv, float *stg) {
+                                                  int e0, float *cv, float *stg, float *row) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < 16; ++j)
     if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
   tile_row_store(stg, lane, cv);
+  if (row) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (e0 + j < p.E) row[e0 + j] = cv[j];
+  }
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < 16; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
@@ -291,7 +320,231 @@ __device__ __forceinline__ void router_unit_clean(const RParams &p, const CUtens
   }
 }
 
-template <int BNR>
+// ----------------------------------------------------------------------------- fused selection
+// When one column block holds every expert of a token (one tile per row
+// block) and each CTA takes one tile, the epilogue also selects
+// ("Outrageously Large", Eq. 5 and the load estimator of Appendix A;
+// "Switch Transformer", step 2): the units leave the tile's c, sigma and H
+// rows in shared memory (the pipeline stages, free once the CTA's only
+// accumulator is full), a thread per token keeps its k + 1 largest H in
+// registers (value descending, lower index first on ties; a NaN never
+// enters) and writes the picks, gates, thresholds and row statistics, and a
+// thread per (16-token group, expert) adds the group's balancing terms in
+// token order into the partial row of those 16 tokens.
+constexpr int kFuseMaxK = 8;
+
+struct FuseSmem {
+  float *h, *c, *s;  // [RBM][E + 1] planes (c and s with the noise term only)
+  int ps;            // plane stride in floats
+  float4 *sc;        // [RBM] k-th and (k+1)-th largest H, row max, 1 / sum of exp
+  int *ci;           // [RBM][kFuseMaxK] chosen experts
+  float *cg;         // [RBM][kFuseMaxK] their gates
+  float *se;         // [RBM] sum of exp(H - max)
+  float *run;        // [runs][groups x E][4] balancing sums of token runs (256 x 4 at most)
+};
+
+__host__ __device__ constexpr size_t fuse_bytes(int E, int noisy) {
+  return (size_t)(noisy ? 3 : 1) * RBM * (E + 1) * 4 + 16 + (size_t)RBM * 16 +
+         (size_t)RBM * kFuseMaxK * 8 + (size_t)RBM * 4 + 32 * kREpiWarps * 16;
+}
+
+__device__ __forceinline__ FuseSmem fuse_smem(uint8_t *base, int E, int noisy) {
+  FuseSmem f;
+  f.ps = RBM * (E + 1);
+  f.h = reinterpret_cast<float *>(base);
+  f.c = noisy ? f.h + f.ps : nullptr;
+  f.s = noisy ? f.h + 2 * f.ps : nullptr;
+  const uintptr_t end = reinterpret_cast<uintptr_t>(f.h + (size_t)(noisy ? 3 : 1) * f.ps);
+  f.sc = reinterpret_cast<float4 *>((end + 15) & ~uintptr_t(15));
+  f.ci = reinterpret_cast<int *>(f.sc + RBM);
+  f.cg = reinterpret_cast<float *>(f.ci + RBM * kFuseMaxK);
+  f.se = f.cg + RBM * kFuseMaxK;
+  f.run = f.se + RBM;
+  return f;
+}
+
+// Barrier 1 over the epilogue warps only (the TMA and MMA warps never join it).
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kREpiWarps) : "memory");
+}
+// The same barrier, returning whether v held on every epilogue thread.
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, 1, %2, q;\n"
+      " selp.u32 %0, 1, 0, a;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(32 * kREpiWarps)
+      : "memory");
+  return r != 0;
+}
+
+// et = epilogue thread 0..255; mb = the tile's row block. Every epilogue
+// thread calls this (it holds the barriers). Threads 0..127 keep the picks of
+// token et, threads 128..255 sum exp(H - max) of token et - 128 meanwhile;
+// the balancing sums of a (16-token group, expert) are split into S runs of
+// 16/S tokens so that every thread takes part, each run's terms unrolled so
+// that their exponentials overlap, and the runs added in order.
+template <int KM>  // KM >= k
+__device__ __forceinline__ void fused_select(const RParams &p, const FuseSmem &f, int mb, int et) {
+  const int E = p.E, rs = E + 1, k = p.k;
+  const int ntok = min(RBM, p.T - mb * RBM);
+  epi_sync();  // every unit's rows are in shared memory
+  float lv[KM + 1];
+  int li[KM + 1];
+  if (et < ntok) {
+    const float *h = f.h + et * rs;
+#pragma unroll
+    for (int j = 0; j <= KM; ++j) {
+      lv[j] = -INFINITY;
+      li[j] = E;
+    }
+    for (int e = 0; e < E; ++e) {
+      float v = h[e];
+      int i = e;
+#pragma unroll
+      for (int j = 0; j <= KM; ++j) {
+        // Slots 0..k ordered by (value descending, index ascending); an
+        // empty slot is (-inf, E). The entry carried down (the new one, or
+        // one it displaced) goes before any equal value of higher index. A
+        // NaN compares false and never enters.
+        const bool take = j <= k && (v > lv[j] || (v == lv[j] && i < li[j]));
+        const float tv = lv[j];
+        const int ti = li[j];
+        lv[j] = take ? v : tv;
+        li[j] = take ? i : ti;
+        v = take ? tv : v;
+        i = take ? ti : i;
+      }
+    }
+  } else if (et >= RBM && et - RBM < ntok) {
+    const float *h = f.h + (et - RBM) * rs;
+    float mx = -INFINITY;  // fmaxf drops NaN, as the picks do: mx = the first pick
+    for (int e = 0; e < E; ++e) mx = fmaxf(mx, h[e]);
+    float se = 0.f;
+#pragma unroll 2
+    for (int e = 0; e < E; ++e) se += expf(h[e] - mx);
+    f.se[et - RBM] = se;
+  }
+  epi_sync();  // the sums of exponentials are in shared memory
+  if (et < ntok) {
+    const size_t t = (size_t)mb * RBM + et;
+    const float mx = lv[0], se = f.se[et];
+    float g[KM];
+    if (p.mode == MOE_GATE_SWITCH) {
+      g[0] = expf(lv[0] - mx) / se;
+#pragma unroll
+      for (int j = 1; j < KM; ++j) g[j] = 0.f;
+    } else {
+      float z = 0.f;
+#pragma unroll
+      for (int j = 0; j < KM; ++j) {
+        g[j] = j < k ? expf(lv[j] - lv[0]) : 0.f;
+        z += g[j];  // in pick order; the terms past k are zero
+      }
+      const float iz = 1.f / z;
+#pragma unroll
+      for (int j = 0; j < KM; ++j) g[j] *= iz;
+    }
+    float th0 = lv[0], th1 = lv[1];
+#pragma unroll
+    for (int j = 1; j <= KM; ++j) {
+      if (j == k - 1) th0 = lv[j];
+      if (j == k) th1 = lv[j];
+    }
+    if (k >= E) th1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) {
+        p.idx[t * k + j] = li[j];
+        p.gate[t * k + j] = g[j];
+        f.ci[et * kFuseMaxK + j] = li[j];
+        f.cg[et * kFuseMaxK + j] = g[j];
+      }
+    p.thr[2 * t] = th0;
+    p.thr[2 * t + 1] = th1;
+    p.rowstat[2 * t] = mx;
+    p.rowstat[2 * t + 1] = se;
+    f.sc[et] = make_float4(th0, th1, mx, 1.f / se);
+  }
+  epi_sync();  // the token scalars are in shared memory
+  if (!p.partials) return;
+  const int ngroups = (ntok + 15) / 16;
+  const int owners = ngroups * E;
+  int S = 1;  // runs per (group, expert), the same for every tile of the launch
+  while (S < 8 && 8 * E * S * 2 <= 32 * kREpiWarps) S *= 2;
+  const int L = 16 / S;
+  for (int i = et; i < owners * S; i += 32 * kREpiWarps) {
+    const int sl = i / owners, o = i - sl * owners;  // consecutive threads: consecutive experts
+    const int gi = o / E, e = o - gi * E;
+    const int t0 = gi * 16 + sl * L;
+    const int n = min(L, ntok - t0);
+    float imp = 0.f, ld = 0.f, fc = 0.f, pb = 0.f;
+#pragma unroll 2
+    for (int u = 0; u < 16; ++u) {
+      if (u >= n) break;
+      const int tt = t0 + u;
+      const float4 sc = f.sc[tt];
+      const int *ci = f.ci + tt * kFuseMaxK;
+      const float *cg = f.cg + tt * kFuseMaxK;
+      bool in = false;
+      float gv = 0.f;
+#pragma unroll
+      for (int j = 0; j < KM; ++j)
+        if (j < k && ci[j] == e) {
+          in = true;
+          gv = cg[j];
+        }
+      imp += gv;
+      const float sv = f.s ? f.s[tt * rs + e] : 0.f;
+      float pr;
+      if (k == E) {
+        pr = 1.f;
+      } else if (sv == 0.f) {
+        pr = in ? 1.f : 0.f;
+      } else {
+        pr = normal_cdf(__fdividef(f.c[tt * rs + e] - (in ? sc.y : sc.x), sv));
+      }
+      ld += pr;
+      if (ci[0] == e) fc += 1.f;
+      pb += expf(f.h[tt * rs + e] - sc.z) * sc.w;
+    }
+    if (S == 1) {
+      float *out = p.partials + ((size_t)mb * (RBM / 16) + gi) * 4 * E + e;
+      out[0] = imp;
+      out[E] = ld;
+      out[2 * E] = fc;
+      out[3 * E] = pb;
+    } else {
+      float *r = f.run + ((size_t)sl * owners + o) * 4;
+      r[0] = imp;
+      r[1] = ld;
+      r[2] = fc;
+      r[3] = pb;
+    }
+  }
+  if (S == 1) return;
+  epi_sync();  // every run's sums are in shared memory
+  for (int o = et; o < owners; o += 32 * kREpiWarps) {
+    const int gi = o / E, e = o - gi * E;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sl = 0; sl < S; ++sl) {
+      const float *r = f.run + ((size_t)sl * owners + o) * 4;
+      acc.x += r[0];
+      acc.y += r[1];
+      acc.z += r[2];
+      acc.w += r[3];
+    }
+    float *out = p.partials + ((size_t)mb * (RBM / 16) + gi) * 4 * E + e;
+    out[0] = acc.x;
+    out[E] = acc.y;
+    out[2 * E] = acc.z;
+    out[3 * E] = acc.w;
+  }
+}
+
+// KMF = 0: no fused selection; else the pick list length of fused_select.
+template <int BNR, int KMF>
 __global__ void __launch_bounds__(kRThreads, 1)
 k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
@@ -408,8 +661,9 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
-      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
-                                                           p.st, 24, p.wait_ns));
+      bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
+                                                     p.st, 24, p.wait_ns));
+      if (KMF > 0) ready = epi_all(ready);  // the fused phase's barriers need all warps
       if (!ready) break;
       tc_fence_after();
       const int t0 = mb * RBM + quad * 32;
@@ -425,6 +679,13 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // so the load overlaps the wait for the next accumulator.
         float *stg = staging + (size_t)(warp - 2) * kEpiWarpFloats;
         const int nunits = (ncols + 15) / 16;
+        float *row = nullptr;  // this lane's token row in the fused-selection buffers
+        FuseSmem fs{};
+        if (KMF > 0) {
+          fence_proxy_async_smem();  // the stages' last MMA reads are complete (acc_full)
+          fs = fuse_smem(smem, p.E, p.noisy);
+          row = fs.h + (quad * 32 + lane) * (p.E + 1);
+        }
         const int epu = p.noisy ? 8 : 16;  // experts per unit
         const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first expert of the block
         if (p.noisy && sub < nunits && nz_tile != tile) load_noise8(p, t, eb + sub * 8, nz_next);
@@ -464,14 +725,16 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               cv[j] = v[2 * j];
               zv[j] = v[2 * j + 1];
             }
-            router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg);
+            router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg, row,
+                              fs.ps);
           } else {
-            router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg);
+            router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg, row);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        if constexpr (KMF > 0) fused_select<KMF>(p, fs, mb, threadIdx.x - 64);
         continue;
       }
       // Row-segment path: the first warp of each quadrant, 16 columns at a
@@ -558,7 +821,8 @@ bool make_out_map(CUtensorMap *m, float *base, int T, int E, bool noisy) {
 template <int BNR>
 cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float *Wn,
                 const float *noise, const float *bias, float *cc, float *sg, float *H,
-                void *bsplit, DeviceStatus *st, cudaStream_t s) {
+                void *bsplit, DeviceStatus *st, cudaStream_t s, const RouterSelect *sel,
+                bool *selected) {
   const int noisy = Wn != nullptr;
   const int NC = noisy ? 2 * c.E : c.E;
   const int n_blocks = (NC + BNR - 1) / BNR;
@@ -578,16 +842,33 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
                        make_out_map(&ts, sg, c.T, c.E, noisy) &&
                        make_out_map(&th, H, c.T, c.E, noisy);
   if (!tma_out) th = ts = tc = ta;  // unused
+  // Fused selection: one column block, the TMA-store epilogue, k <= 8, and
+  // one tile per CTA (its pipeline stages then hold the selection buffers).
+  // MOE_ROUTER_SELECT=separate keeps the selection kernels instead.
+  static const bool separate = [] {
+    const char *v = getenv("MOE_ROUTER_SELECT");
+    return v && v[0] == 's';
+  }();
+  const bool fuse = !separate && sel != nullptr && tma_out && n_blocks == 1 && c.k <= kFuseMaxK &&
+                    fuse_bytes(c.E, noisy) <= (size_t)RCfg<BNR>::STAGES * RCfg<BNR>::STAGE;
   RParams p{c.T, c.d, c.E, noisy, NC, NCP, n_blocks, tma_out ? 1 : 0, noise, bias, cc, sg, H, st,
-            wait_limit_ns()};
+            wait_limit_ns(), fuse ? 1 : 0, c.k, c.gate_mode,
+            fuse ? sel->idx : nullptr, fuse ? sel->gate : nullptr, fuse ? sel->thr : nullptr,
+            fuse ? sel->rowstat : nullptr, fuse ? sel->partials : nullptr};
   const size_t smem = RCfg<BNR>::SMEM;
-  err = cudaFuncSetAttribute(k_router_tc<BNR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-  if (err != cudaSuccess) return err;
   const int tiles = ((c.T + RBM - 1) / RBM) * n_blocks;
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  launch_pdl(k_router_tc<BNR>, grid, kRThreads, smem, s, ta, tb, tc, ts, th, p);
-  return cudaGetLastError();
+  const int grid = fuse || tiles < sm_count() ? tiles : sm_count();
+  const int kmf = !fuse ? 0 : c.k <= 2 ? 2 : c.k <= 4 ? 4 : kFuseMaxK;
+  auto kernel = kmf == 0 ? k_router_tc<BNR, 0>
+              : kmf == 2 ? k_router_tc<BNR, 2>
+              : kmf == 4 ? k_router_tc<BNR, 4>
+                         : k_router_tc<BNR, kFuseMaxK>;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  launch_pdl(kernel, grid, kRThreads, smem, s, ta, tb, tc, ts, th, p);
+  err = cudaGetLastError();
+  if (err == cudaSuccess && selected) *selected = fuse;
+  return err;
 }
 
 }  // namespace
@@ -605,11 +886,12 @@ size_t router_tc_split_bytes(const moe_config &c) {
 
 cudaError_t launch_router_tc(const moe_config &c, const void *x, const float *Wg, const float *Wn,
                              const float *noise, const float *bias, float *cc, float *sg, float *H,
-                             void *bsplit, DeviceStatus *st, cudaStream_t s) {
+                             void *bsplit, DeviceStatus *st, cudaStream_t s,
+                             const RouterSelect *sel, bool *selected) {
   switch (tile_cols(Wn ? 2 * c.E : c.E)) {
-    case 16: return run<16>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
-    case 32: return run<32>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
-    default: return run<64>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s);
+    case 16: return run<16>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s, sel, selected);
+    case 32: return run<32>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s, sel, selected);
+    default: return run<64>(c, x, Wg, Wn, noise, bias, cc, sg, H, bsplit, st, s, sel, selected);
   }
 }
 

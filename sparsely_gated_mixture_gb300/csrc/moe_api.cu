@@ -107,7 +107,12 @@ static int gate_impl(const moe_config &c, const void *x, const float *Wg, const 
   float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
   float *rs = ws_at<float>(ws, L.rowstat);
   MOE_CUDA(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
-  MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, ws_at<char>(ws, L.bsplit), st, s));
+  float *part = ws_at<float>(ws, L.partials);
+  const RouterSelect sel{idx, gate, thr, rs, partials ? part : nullptr};
+  bool selected = false;
+  MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, ws_at<char>(ws, L.bsplit), st, s,
+                         &sel, &selected));
+  if (selected) return MOE_OK;  // the router's epilogue selected (and summed) itself
   if (partials && c.E <= 256) {
     MOE_CUDA(launch_select_aux(c, Wn != nullptr, cc, sg, H, idx, gate, thr, rs,
                                ws_at<float>(ws, L.partials), L.n_aux_blocks, s));

@@ -101,10 +101,23 @@ inline int elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
 // ----------------------------------------------------------------------------- launchers
 // Each returns a cudaError_t from the launch (cudaSuccess if nothing failed).
 
+// Selection outputs the tensor-core router can produce in its own epilogue
+// when one tile holds every expert of a row: expert_idx [T,k], gate [T,k],
+// thr [T,2], rowstat [T,2] (row max, sum of exp(H - max)) and, when partials
+// is not null, the balancing partial rows (one per 16 tokens, aux_rows).
+struct RouterSelect {
+  int32_t *idx;
+  float *gate, *thr, *rowstat, *partials;
+};
+
 // k_gate.cu: router GEMM + noise + softplus, selection + softmax, balancing partials.
+// With `sel` given, *selected tells whether the router also wrote the
+// selection outputs (and the partials, if asked for); otherwise the caller
+// launches the selection kernels.
 cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
                           const float *noise, const float *bias, float *c, float *sigma, float *H,
-                          void *bsplit, DeviceStatus *st, cudaStream_t s);
+                          void *bsplit, DeviceStatus *st, cudaStream_t s,
+                          const RouterSelect *sel = nullptr, bool *selected = nullptr);
 cudaError_t launch_select(const moe_config &cfg, const float *H, int32_t *idx, float *gate,
                           float *thr, float *rowstat, DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *c,
@@ -125,7 +138,8 @@ bool router_tc_supported(const moe_config &cfg);
 size_t router_tc_split_bytes(const moe_config &cfg);
 cudaError_t launch_router_tc(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
                              const float *noise, const float *bias, float *c, float *sigma,
-                             float *H, void *bsplit, DeviceStatus *st, cudaStream_t s);
+                             float *H, void *bsplit, DeviceStatus *st, cudaStream_t s,
+                             const RouterSelect *sel, bool *selected);
 
 // k_slots.cu: capacity, token-order slots, dispatch maps.
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,

@@ -277,3 +277,55 @@ def test_router_bias_with_noise(E):
     inp["bias"] = (np.random.default_rng(5).standard_normal(E) * 0.5).astype(np.float32)
     stages, _ = check_stages(w, inp)
     check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
+
+
+FUSED = {
+    # The tensor-core router selects in its own epilogue when every expert of
+    # a token sits in one 64-column block (E <= 32 with the noise term, 64
+    # without) and k <= 8: the longest pick lists, k = E, and a grid of more
+    # row blocks than SMs (one tile per CTA, several waves).
+    "fused_noisy_e32_k5": wl.Workload("fused_noisy_e32_k5", T=300, d=128, E=32, d_ff=64, k=5,
+                                      cf=1.0, mode=wl.TOPK, dtype="bf16", noisy=True),
+    "fused_clean_e64_k8": wl.Workload("fused_clean_e64_k8", T=257, d=64, E=64, d_ff=64, k=8,
+                                      cf=1.25, mode=wl.TOPK, dtype="bf16", noisy=False),
+    "fused_k_equals_E8": wl.Workload("fused_k_equals_E8", T=200, d=64, E=8, d_ff=64, k=8, cf=1.0,
+                                     mode=wl.TOPK, dtype="bf16", noisy=True),
+    "fused_switch_noisy_e16": wl.Workload("fused_switch_noisy_e16", T=333, d=96, E=16, d_ff=64,
+                                          k=1, cf=1.0, mode=wl.SWITCH, dtype="bf16", noisy=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FUSED))
+def test_fused_selection_parity(name):
+    w = FUSED[name]
+    inp = wl.generate(w, seed=31, biases=True)
+    stages, _ = check_stages(w, inp)
+    check_forward(w, inp, np.arange(w.T, dtype=np.int32), stages)
+
+
+def test_fused_selection_many_waves():
+    """153 row blocks of 128 tokens (one more than the SMs), the last ragged:
+    every index, slot and balancing value, and sampled rows."""
+    w = wl.Workload("fused_waves", T=152 * 128 + 77, d=64, E=8, d_ff=64, k=2, cf=1.25,
+                    mode=wl.TOPK, dtype="bf16", noisy=True)
+    inp = wl.generate(w, seed=37, biases=True)
+    tokens = _sample_tokens(w.T, 512, seed=2)
+    check_stages(w, inp, tokens)
+    check_forward(w, inp, tokens)
+
+
+@pytest.mark.parametrize("E,levels", [(16, 0), (16, 2), (64, 0), (64, 3)])
+def test_tied_logits_fused(E, levels):
+    """Exact ties on the fused selection: a zero clean router with a bias on a
+    coarse grid (levels = 0: every expert tied), so the picks, thresholds and
+    gates must match the oracle's lower-index-first order exactly."""
+    w = wl.Workload(f"tied_fused_e{E}", T=200, d=64, E=E, d_ff=64, k=4, cf=2.0, mode=wl.TOPK,
+                    dtype="bf16", noisy=False)
+    inp = wl.generate(w, seed=19)
+    inp["Wg"] = np.zeros_like(inp["Wg"])
+    rng = np.random.default_rng(4)
+    inp["bias"] = (np.round(rng.standard_normal(w.E) * levels) if levels else
+                   np.zeros(w.E)).astype(np.float32)
+    res, _ = check_stages(w, inp)
+    ref = oracle_gate(inp)
+    assert np.array_equal(res["idx"], ref["idx"])
