@@ -416,10 +416,10 @@ def run_ours(args, w: wl.Workload):
     # tokens), selection with the balancing partials (one fused kernel up to
     # 256 experts, two beyond), slot histogram / scan / rank, gather, two
     # expert GEMMs, combine, balancing finalize
-    # Router (split + tensor-core kernel for bf16), selection (none when the
-    # tensor-core router selects in its own epilogue: bf16, d % 8 == 0, every
-    # expert in one 64-column block, E % 4 == 0, k <= 8), three slot kernels,
-    # gather, two GEMMs, combine, finalize.
+    # Router (weight split + tensor-core kernel for bf16), selection (none
+    # when the tensor-core router selects in its own epilogue: bf16,
+    # d % 8 == 0, every expert in one 64-column block, E % 4 == 0, k <= 8),
+    # three slot kernels, gather, two GEMMs, combine, finalize.
     tc_router = w.dtype == "bf16" and w.d % 8 == 0
     fused_sel = (tc_router and (2 * w.E if w.noisy else w.E) <= 64 and w.E % 4 == 0
                  and w.k <= 8)

@@ -934,9 +934,15 @@ cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg,
     const char *v = getenv("MOE_ROUTER");
     return v && v[0] == 's';
   }();
+  // The tensor-core router's first kernel clears the status word; the
+  // CUDA-core routers start from a cleared one.
   if (!force_simt && router_tc_supported(cfg))
     return launch_router_tc(cfg, x, Wg, Wn, noise, bias, c, sigma, H, bsplit, st, s, sel,
                             selected);
+  {
+    const cudaError_t err = cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s);
+    if (err != cudaSuccess) return err;
+  }
   // Vector path: whole 16-byte pieces of every x row, and a small expert count
   // (beyond it the per-block W traffic of this layout grows with E).
   const bool vec = cfg.E <= 64 &&

@@ -115,11 +115,20 @@ __device__ __forceinline__ void tile_row_store(float *tile, int l, const float *
 // Output rows are grouped per column block of BNR: block b holds hi rows,
 // then mid rows, then lo rows of its BNR columns, so one TMA box of 3*BNR rows
 // brings all three pieces of a block.
+// It runs first in the gate, so it also clears the status word (after its
+// dependent-launch wait, before any later kernel can record an error).
 __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP, int BNR,
                                const float *__restrict__ Wg, const float *__restrict__ Wn,
-                               __nv_bfloat16 *__restrict__ B) {
+                               __nv_bfloat16 *__restrict__ B, DeviceStatus *st) {
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) {
+    st->code = 0;
+    st->aux_ticket = 0;
+    st->detail = 0;
+    st->slot_ticket = 0;
+    st->reserved = 0;
+  }
   __shared__ float tile[32][33];
   const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += 8) {
@@ -829,7 +838,7 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   const int NCP = n_blocks * BNR;
   dim3 sg_grid((c.d + 31) / 32, (NCP + 31) / 32);
   launch_pdl(k_router_split, sg_grid, dim3(32, 8), 0, s, c.d, c.E, noisy, NC, NCP, BNR, Wg, Wn,
-      static_cast<__nv_bfloat16 *>(bsplit));
+      static_cast<__nv_bfloat16 *>(bsplit), st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   CUtensorMap ta, tb, tc, ts, th;

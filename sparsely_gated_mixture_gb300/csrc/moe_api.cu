@@ -106,8 +106,7 @@ static int gate_impl(const moe_config &c, const void *x, const float *Wg, const 
   DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
   float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
   float *rs = ws_at<float>(ws, L.rowstat);
-  MOE_CUDA(cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s));
-  float *part = ws_at<float>(ws, L.partials);
+  float *part = ws_at<float>(ws, L.partials);  // launch_router clears the status word first
   const RouterSelect sel{idx, gate, thr, rs, partials ? part : nullptr};
   bool selected = false;
   MOE_CUDA(launch_router(c, x, Wg, Wn, noise, bias, cc, sg, H, ws_at<char>(ws, L.bsplit), st, s,
