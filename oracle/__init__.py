@@ -15,6 +15,8 @@ and marshals numpy arrays. Each wrapper names the page passage it follows:
   argmax gate, capacity, exclusive-cumsum slots, dispatch, ReLU experts,
   combine with residual, auxiliary loss.
 * "Mixture-of-Experts: Sparse Computation" (cs8803 lesson), Chapters 1, 2, 5.
+* The paper summary's "Hierarchical Mixture-of-Experts" section: the two-level
+  gate, y_H, Importance_H and Load_H (``hier_*``).
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 except the expert FFN's values on random weights, which the pages never print;
@@ -102,6 +104,10 @@ class Oracle:
         lib.orc_softplus_at.restype = D
         lib.orc_phi_at.argtypes = [D]
         lib.orc_phi_at.restype = D
+        lib.orc_hier_select.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P]
+        lib.orc_hier_select.restype = None
+        lib.orc_hier_aux.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P]
+        lib.orc_hier_aux.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -254,6 +260,81 @@ class Oracle:
                     keep=keep, count=count, y=y, nonfinite=bad_h or bad_y, **ax)
 
 
+    # ------------------------------------------------------------ hierarchical
+    def hier_select(self, idx_p, g_p, Hs, a: int, b: int, ks: int):
+        """Two-level selection (OLNN "Hierarchical Mixture-of-Experts"): for
+        each primary pick (group i) the top-ks softmax of the secondary logits
+        of group i. Returns flat idx [T, kp*ks] (i*b + j), product gates
+        [T, kp*ks], and the in-group thresholds hks, hk1s [T, kp]."""
+        idx_p = np.ascontiguousarray(idx_p, dtype=np.int32)
+        g_p = np.ascontiguousarray(g_p, dtype=np.float64)
+        Hs = np.ascontiguousarray(Hs, dtype=np.float64)
+        T, kp = idx_p.shape
+        if Hs.shape != (T, a * b):
+            raise ValueError("secondary logits are [T, a*b]")
+        k = kp * ks
+        idx = np.empty((T, k), np.int32)
+        gate = np.empty((T, k), np.float64)
+        hks = np.empty((T, kp), np.float64)
+        hk1s = np.empty((T, kp), np.float64)
+        self.lib.orc_hier_select(T, a, b, kp, ks, _ptr(idx_p), _ptr(g_p), _ptr(Hs), _ptr(idx),
+                                 _ptr(gate), _ptr(hks), _ptr(hk1s))
+        return idx, gate, hks, hk1s
+
+    def hier_aux(self, idx_p, cs, ss, idx, gate, hks, hk1s, load_p, a: int, b: int, ks: int,
+                 noisy: bool):
+        """Importance_H, |X^(i)|, the in-group secondary loads, Load_H and
+        out2 = [CV(Importance_H)^2, CV(Load_H)^2] (OLNN "Hierarchical
+        Mixture-of-Experts"; Load_H is 0 for a group no token picked)."""
+        idx_p = np.ascontiguousarray(idx_p, dtype=np.int32)
+        T, kp = idx_p.shape
+        E = a * b
+        args = [np.ascontiguousarray(v, dtype=np.float64) for v in (cs, ss)]
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        gate = np.ascontiguousarray(gate, dtype=np.float64)
+        hks = np.ascontiguousarray(hks, dtype=np.float64)
+        hk1s = np.ascontiguousarray(hk1s, dtype=np.float64)
+        load_p = np.ascontiguousarray(load_p, dtype=np.float64)
+        imp = np.empty(E, np.float64)
+        loadsec = np.empty(E, np.float64)
+        count = np.empty(a, np.int32)
+        load_H = np.empty(E, np.float64)
+        out2 = np.empty(2, np.float64)
+        self.lib.orc_hier_aux(T, a, b, kp, ks, _ptr(idx_p), _ptr(args[0]), _ptr(args[1]),
+                              _ptr(idx), _ptr(gate), _ptr(hks), _ptr(hk1s), int(bool(noisy)),
+                              _ptr(load_p), _ptr(imp), _ptr(loadsec), _ptr(count),
+                              _ptr(load_H), _ptr(out2))
+        return dict(importance_H=imp, loadsec=loadsec, count=count, load_H=load_H, out2=out2)
+
+    def hier_forward(self, inp: dict, tokens=None) -> dict:
+        """The hierarchical layer y_H = x + sum_i sum_j G_p(x)_i G_i(x)_j
+        E_ij(x) with the flat path's capacity and slot rules over the a*b
+        experts (k = kp*ks choices per token, in primary-then-secondary pick
+        order). ``inp``: x, Wp, Wpn, noise_p (primary gate over a groups), Ws,
+        Wsn, noise_s (secondary gates, [d, a*b]: group i's columns i*b ..
+        i*b+b-1), W1, b1, W2, b2 over the a*b experts, a, b, kp, ks, cf,
+        min_cap."""
+        x = inp["x"]
+        T = x.shape[0]
+        a, b, kp, ks = (int(inp[n]) for n in ("a", "b", "kp", "ks"))
+        cp, sp, Hp, bad_p = self.router(x, inp["Wp"], inp.get("Wpn"), inp.get("noise_p"))
+        idx_p, g_p, hkp, hk1p = self.select(Hp, kp, TOPK_SOFTMAX)
+        ax_p = self.aux(cp, sp, Hp, idx_p, g_p, hkp, hk1p, inp.get("Wpn") is not None)
+        cs, ss, Hs, bad_s = self.router(x, inp["Ws"], inp.get("Wsn"), inp.get("noise_s"))
+        idx, gate, hks, hk1s = self.hier_select(idx_p, g_p, Hs, a, b, ks)
+        E, k = a * b, kp * ks
+        C = self.capacity(T, E, k, inp["cf"], inp.get("min_cap", 1))
+        pos, keep, count = self.slots(idx, E, C)
+        y, bad_y = self.layer_out(x, idx, gate, keep, inp["W1"], inp["W2"], inp.get("b1"),
+                                  inp.get("b2"), tokens)
+        hx = self.hier_aux(idx_p, cs, ss, idx, gate, hks, hk1s, ax_p["load"], a, b, ks,
+                           inp.get("Wsn") is not None)
+        return dict(cp=cp, sp=sp, Hp=Hp, idx_p=idx_p, g_p=g_p, load_p=ax_p["load"], cs=cs, ss=ss,
+                    Hs=Hs, idx=idx, gate=gate, hks=hks, hk1s=hk1s, C=C, pos=pos, keep=keep,
+                    expert_count=count, y=y, nonfinite=bad_p or bad_s or bad_y,
+                    group_count=hx.pop("count"), **hx)
+
+
 def default() -> Oracle:
     """The oracle compiled from moe_oracle.c (built on first use)."""
     global _default
@@ -313,3 +394,15 @@ def aux(*a, **k):
 
 def forward(*a, **k):
     return default().forward(*a, **k)
+
+
+def hier_select(*a, **k):
+    return default().hier_select(*a, **k)
+
+
+def hier_aux(*a, **k):
+    return default().hier_aux(*a, **k)
+
+
+def hier_forward(*a, **k):
+    return default().hier_forward(*a, **k)

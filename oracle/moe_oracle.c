@@ -361,6 +361,98 @@ void orc_aux(int T, int E, int k, const double *c, const double *sigma, const do
   free(rowsum);
 }
 
+/*
+ * Hierarchical gate [OLNN, "Hierarchical Mixture-of-Experts"; LESSON Ch. 5]:
+ * a groups of b experts, flat expert i*b + j. The primary gate has picked the
+ * groups idx_p [T,kp] with gates g_p [T,kp] (orc_select over the a primary
+ * logits). The secondary gate of group i is the top-ks softmax of the
+ * secondary noisy logits Hs[t, i*b .. i*b + b - 1], chosen exactly as
+ * orc_select chooses (H descending, lower index first). For token t and
+ * primary pick q (group i) with secondary picks j_0..j_{ks-1}:
+ *   idx[t, q*ks + r]  = i*b + j_r
+ *   gate[t, q*ks + r] = g_p[t,q] * G_i(x_t)_{j_r}      (the product in y_H)
+ *   hks[t,q], hk1s[t,q] = the ks-th and (ks+1)-th largest secondary logit
+ *                         inside group i (-inf when ks == b).
+ */
+void orc_hier_select(int T, int a, int b, int kp, int ks, const int *idx_p, const double *g_p,
+                     const double *Hs, int *idx, double *gate, double *hks, double *hk1s) {
+  (void)a;
+  const int k = kp * ks;
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    int sidx[ks];
+    double sg[ks];
+    for (int q = 0; q < kp; ++q) {
+      const int i = idx_p[(size_t)t * kp + q];
+      const double *h = Hs + (size_t)t * a * b + (size_t)i * b;
+      orc_select(1, b, ks, ORC_TOPK_SOFTMAX, h, sidx, sg, &hks[(size_t)t * kp + q],
+                 &hk1s[(size_t)t * kp + q]);
+      for (int r = 0; r < ks; ++r) {
+        idx[(size_t)t * k + q * ks + r] = i * b + sidx[r];
+        gate[(size_t)t * k + q * ks + r] = g_p[(size_t)t * kp + q] * sg[r];
+      }
+    }
+  }
+}
+
+/*
+ * Hierarchical balancing quantities [OLNN, "Hierarchical Mixture-of-Experts":
+ * Importance_H and Load_H], before capacity:
+ *  imp_H[i*b+j]   = sum_t G_p(x_t)_i * G_i(x_t)_j (the product gates)
+ *  count[i]       = |X^(i)|, the tokens whose primary picks include group i
+ *  loadsec[i*b+j] = Load_i(X^(i))_j = sum over t in X^(i) of P_i(x_t, j), the
+ *                   smooth load of group i's secondary gate over X^(i):
+ *                   Phi((cs - kth_excluding) / ss), kth_excluding = hk1s when
+ *                   j is among the group's ks picks for t, hks otherwise; the
+ *                   pick indicator without noise (or where ss is 0); 1 when
+ *                   ks == b
+ *  load_H[i*b+j]  = load_p[i] * loadsec[i*b+j] / count[i]  (load_p = the
+ *                   primary gate's Load over the whole batch), and 0 where
+ *                   count[i] == 0 (the quotient is undefined there)
+ *  out2 = [CV(imp_H)^2, CV(load_H)^2]                    [OLNN Eq. 7]
+ */
+void orc_hier_aux(int T, int a, int b, int kp, int ks, const int *idx_p, const double *cs,
+                  const double *ss, const int *idx, const double *gate, const double *hks,
+                  const double *hk1s, int noisy, const double *load_p, double *imp_H,
+                  double *loadsec, int *count, double *load_H, double *out2) {
+  const int E = a * b, k = kp * ks;
+  for (int e = 0; e < E; ++e) imp_H[e] = loadsec[e] = 0.0;
+  for (int i = 0; i < a; ++i) count[i] = 0;
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < k; ++c) imp_H[idx[(size_t)t * k + c]] += gate[(size_t)t * k + c];
+    for (int q = 0; q < kp; ++q) {
+      const int i = idx_p[(size_t)t * kp + q];
+      count[i] += 1;
+      for (int j = 0; j < b; ++j) {
+        const int e = i * b + j;
+        int chosen = 0;
+        for (int r = 0; r < ks; ++r)
+          if (idx[(size_t)t * k + q * ks + r] == e) chosen = 1;
+        double p;
+        if (ks == b) {
+          p = 1.0;
+        } else {
+          const double s = ss[(size_t)t * E + e];
+          if (!noisy || s == 0.0) {
+            p = chosen ? 1.0 : 0.0;
+          } else {
+            const double thr = chosen ? hk1s[(size_t)t * kp + q] : hks[(size_t)t * kp + q];
+            p = orc_phi((cs[(size_t)t * E + e] - thr) / s);
+          }
+        }
+        loadsec[e] += p;
+      }
+    }
+  }
+  for (int i = 0; i < a; ++i)
+    for (int j = 0; j < b; ++j) {
+      const int e = i * b + j;
+      load_H[e] = count[i] > 0 ? load_p[i] * loadsec[e] / (double)count[i] : 0.0;
+    }
+  out2[0] = orc_cv2(imp_H, E);
+  out2[1] = orc_cv2(load_H, E);
+}
+
 /* Exposed for the pins: the scalar building blocks. */
 double orc_softplus_at(double z) { return orc_softplus(z); }
 double orc_phi_at(double u) { return orc_phi(u); }

@@ -20,6 +20,12 @@ drawn in the fixed order x, W_g, W_noise, noise, W1, b1, W2, b2:
 bf16 workloads round x, W1, W2, b1, b2 from fp32 to bf16 with
 round-to-nearest-even and keep the bit patterns as uint16; both sides of every
 comparison receive those same bits.
+
+Hierarchical layers (``HierWorkload``, a groups of b experts) draw, in order:
+x; W_p, W_pnoise ~ N(0, 1/d) [d, a] and noise_p ~ N(0, 1) [T, a] for the
+primary gate; W_s, W_snoise ~ N(0, 1/d) [d, a*b] and noise_s ~ N(0, 1)
+[T, a*b] for the secondary gates (group i owns columns i*b .. i*b+b-1); then
+W1, b1, W2, b2 over the a*b experts as above.
 """
 from __future__ import annotations
 
@@ -83,6 +89,57 @@ WORKLOADS = {
     ]
 }
 
+
+@dataclasses.dataclass(frozen=True)
+class HierWorkload:
+    """A hierarchical layer: a groups of b experts, kp groups then ks experts
+    in each picked group, so k = kp * ks choices per token over a*b experts."""
+    name: str
+    T: int
+    d: int
+    a: int
+    b: int
+    kp: int
+    ks: int
+    d_ff: int
+    cf: float
+    dtype: str
+    noisy: bool
+    min_cap: int = 1
+
+    def with_(self, **kw) -> "HierWorkload":
+        return dataclasses.replace(self, **kw)
+
+    @property
+    def E(self) -> int:
+        return self.a * self.b
+
+    @property
+    def k(self) -> int:
+        return self.kp * self.ks
+
+    @property
+    def capacity(self) -> int:
+        c = math.floor(self.k * self.T * self.cf / self.E)
+        return max(self.min_cap, min(self.T, c))
+
+    def expert_flops(self, accepted: int) -> int:
+        return 4 * self.d * self.d_ff * accepted
+
+    def router_flops(self) -> int:
+        cols = (2 if self.noisy else 1) * (self.a + self.a * self.b)
+        return 2 * self.T * self.d * cols
+
+
+# The many-small-experts layer as 16 groups of 64 experts, two of each.
+HIER_WORKLOADS = {
+    w.name: w
+    for w in [
+        HierWorkload("hier_16x64_e1024", T=32768, d=512, a=16, b=64, kp=2, ks=2, d_ff=1024,
+                     cf=1.5, dtype="bf16", noisy=True),
+    ]
+}
+
 _CHUNK = 1 << 24
 
 
@@ -132,3 +189,30 @@ def generate(w: Workload, seed: int = 0, biases: bool = False) -> dict:
     return dict(x=x, Wg=Wg, Wn=Wn, noise=noise, bias=bias, W1=W1, b1=b1, W2=W2, b2=b2,
                 k=w.k, cf=w.cf, min_cap=w.min_cap, mode=1 if w.mode == SWITCH else 0,
                 T=w.T, d=w.d, E=w.E, d_ff=w.d_ff)
+
+
+def generate_hier(w: HierWorkload, seed: int = 0, biases: bool = False) -> dict:
+    """Draw one input set for the hierarchical layer ``w`` (same conventions as
+    ``generate``)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bf = w.dtype == "bf16"
+    E = w.a * w.b
+    x = _normal(rng, (w.T, w.d), 1.0, bf)
+    sd = 1.0 / math.sqrt(w.d)
+    Wp = _normal(rng, (w.d, w.a), sd, False)
+    Wpn = noise_p = None
+    if w.noisy:
+        Wpn = _normal(rng, (w.d, w.a), sd, False)
+        noise_p = _normal(rng, (w.T, w.a), 1.0, False)
+    Ws = _normal(rng, (w.d, E), sd, False)
+    Wsn = noise_s = None
+    if w.noisy:
+        Wsn = _normal(rng, (w.d, E), sd, False)
+        noise_s = _normal(rng, (w.T, E), 1.0, False)
+    W1 = _normal(rng, (E, w.d, w.d_ff), 1.0 / math.sqrt(w.d), bf)
+    b1 = _normal(rng, (E, w.d_ff), 0.1, bf) if biases else None
+    W2 = _normal(rng, (E, w.d_ff, w.d), 1.0 / math.sqrt(w.d_ff), bf)
+    b2 = _normal(rng, (E, w.d), 0.1, bf) if biases else None
+    return dict(x=x, Wp=Wp, Wpn=Wpn, noise_p=noise_p, Ws=Ws, Wsn=Wsn, noise_s=noise_s, W1=W1,
+                b1=b1, W2=W2, b2=b2, a=w.a, b=w.b, kp=w.kp, ks=w.ks, cf=w.cf,
+                min_cap=w.min_cap, T=w.T, d=w.d, d_ff=w.d_ff)

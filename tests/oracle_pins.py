@@ -438,4 +438,165 @@ def pin_nonfinite(orc):
     assert bad
 
 
+# ----------------------------------------------------------------------------- hierarchical
+
+
+def _hier_case(rng, T, d, a, b, d_ff, noisy=True):
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    sd = 1.0 / math.sqrt(d)
+    E = a * b
+    inp = dict(x=x, Wp=(rng.standard_normal((d, a)) * sd).astype(np.float32),
+               Ws=(rng.standard_normal((d, E)) * sd).astype(np.float32),
+               Wpn=None, noise_p=None, Wsn=None, noise_s=None)
+    if noisy:
+        inp.update(Wpn=(rng.standard_normal((d, a)) * sd).astype(np.float32),
+                   noise_p=rng.standard_normal((T, a)).astype(np.float32),
+                   Wsn=(rng.standard_normal((d, E)) * sd).astype(np.float32),
+                   noise_s=rng.standard_normal((T, E)).astype(np.float32))
+    _, W1, b1, W2, b2 = _small_case(rng, T, d, E, d_ff, False)
+    inp.update(W1=W1, b1=b1, W2=W2, b2=b2, a=a, b=b, cf=float(E), min_cap=1)
+    return inp
+
+
+def _np_logits(X, W, Wn, noise):
+    """c, sigma, H of a noisy gate in numpy (OLNN Eq. 4)."""
+    c = X @ W.astype(np.float64)
+    if Wn is None:
+        return c, np.zeros_like(c), c
+    s = np.logaddexp(0.0, X @ Wn.astype(np.float64))
+    return c, s, c + noise.astype(np.float64) * s
+
+
+def _np_topk_gate(h, k):
+    """Dense Softmax(KeepTopK(h, k)) and the ordered picks."""
+    top = _ref_order(list(h), k)
+    g = np.zeros(len(h))
+    ex = np.exp(h[top] - h[top[0]])
+    g[top] = ex / ex.sum()
+    return g, top
+
+
+def _np_smooth_load(c, s, h, k, members=None):
+    """sum over rows of P(x, e) = Phi((c_e - kth_excluding(h, k, e)) / s_e)
+    (OLNN Eqs. 8-9), computed row by row in numpy/scipy; rows limited to
+    ``members`` when given."""
+    T, E = h.shape
+    out = np.zeros(E)
+    for t in range(T) if members is None else members:
+        for e in range(E):
+            others = np.sort(np.delete(h[t], e))[::-1]
+            if k >= E:
+                out[e] += 1.0
+            elif s[t, e] == 0.0:
+                out[e] += 1.0 if e in _ref_order(list(h[t]), k) else 0.0
+            else:
+                out[e] += ndtr((c[t, e] - others[k - 1]) / s[t, e])
+    return out
+
+
+def pin_hier_dense_formula(orc):
+    """The hierarchical layer against its definition written out densely in
+    numpy on a tiny case (OLNN "Hierarchical Mixture-of-Experts"):
+    y_H = x + sum_i sum_j G_p(x)_i G_i(x)_j E_ij(x), Importance_H = sum of the
+    products, Load_H = Load_p(X)_i Load_i(X^(i))_j / |X^(i)|, with every gate
+    a noisy top-k softmax and every load the smooth estimator, and nothing
+    dropped (capacity T)."""
+    rng = np.random.default_rng(41)
+    T, d, a, b, kp, ks, d_ff = 9, 6, 3, 4, 2, 2, 5
+    inp = _hier_case(rng, T, d, a, b, d_ff)
+    inp.update(kp=kp, ks=ks)
+    r = orc.hier_forward(inp)
+    X = _x64(inp["x"])
+    cp, sp, Hp = _np_logits(X, inp["Wp"], inp["Wpn"], inp["noise_p"])
+    cs, ss, Hs = _np_logits(X, inp["Ws"], inp["Wsn"], inp["noise_s"])
+    Y = _ffn_all(X, inp["W1"], inp["b1"], inp["W2"], inp["b2"])
+    y_ref = X.copy()
+    imp = np.zeros(a * b)
+    members = [[] for _ in range(a)]
+    for t in range(T):
+        gp, picks = _np_topk_gate(Hp[t], kp)
+        for i in picks:
+            members[i].append(t)
+            gi, _ = _np_topk_gate(Hs[t, i * b:(i + 1) * b], ks)
+            for j in range(b):
+                w = gp[i] * gi[j]
+                y_ref[t] += w * Y[i * b + j, t]
+                imp[i * b + j] += w
+    np.testing.assert_allclose(r["y"], y_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(r["importance_H"], imp, rtol=1e-12, atol=1e-14)
+    load_p = _np_smooth_load(cp, sp, Hp, kp)
+    load_H = np.zeros(a * b)
+    for i in range(a):
+        sec = _np_smooth_load(cs[:, i * b:(i + 1) * b], ss[:, i * b:(i + 1) * b],
+                              Hs[:, i * b:(i + 1) * b], ks, members[i])
+        if members[i]:
+            load_H[i * b:(i + 1) * b] = load_p[i] * sec / len(members[i])
+    assert list(r["group_count"]) == [len(m) for m in members]
+    np.testing.assert_allclose(r["load_H"], load_H, rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(r["out2"], [np.var(imp) / np.mean(imp) ** 2,
+                                           np.var(load_H) / np.mean(load_H) ** 2], rtol=1e-10)
+
+
+def pin_hier_one_group_is_flat(orc):
+    """a = 1, kp = 1: the primary gate is 1 for every token, so the layer,
+    Importance_H and Load_H are the flat layer's over the b experts."""
+    rng = np.random.default_rng(43)
+    T, d, b, ks, d_ff = 20, 7, 6, 2, 4
+    inp = _hier_case(rng, T, d, 1, b, d_ff)
+    inp.update(kp=1, ks=ks, cf=1.0)
+    r = orc.hier_forward(inp)
+    flat = orc.forward(dict(x=inp["x"], Wg=inp["Ws"], Wn=inp["Wsn"], noise=inp["noise_s"],
+                            bias=None, W1=inp["W1"], b1=inp["b1"], W2=inp["W2"], b2=inp["b2"],
+                            k=ks, cf=1.0, min_cap=1, mode=TOPK))
+    assert np.array_equal(r["idx"], flat["idx"]) and np.array_equal(r["keep"], flat["keep"])
+    np.testing.assert_allclose(r["gate"], flat["gate"], rtol=1e-14)
+    np.testing.assert_allclose(r["y"], flat["y"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["importance_H"], flat["importance"], rtol=1e-13)
+    np.testing.assert_allclose(r["load_H"], flat["load"], rtol=1e-12)
+    np.testing.assert_allclose(r["out2"], flat["out3"][:2], rtol=1e-10)
+
+
+def pin_hier_single_expert_groups(orc):
+    """b = 1, ks = 1: every secondary gate is 1, so the layer is the flat
+    layer over the a groups; Importance_H is the primary importance and
+    Load_H the primary load wherever the group was picked."""
+    rng = np.random.default_rng(47)
+    T, d, a, kp, d_ff = 40, 5, 4, 2, 3
+    inp = _hier_case(rng, T, d, a, 1, d_ff)
+    inp.update(kp=kp, ks=1, cf=2.0)
+    r = orc.hier_forward(inp)
+    flat = orc.forward(dict(x=inp["x"], Wg=inp["Wp"], Wn=inp["Wpn"], noise=inp["noise_p"],
+                            bias=None, W1=inp["W1"], b1=inp["b1"], W2=inp["W2"], b2=inp["b2"],
+                            k=kp, cf=2.0, min_cap=1, mode=TOPK))
+    assert np.array_equal(r["idx"], flat["idx"])
+    np.testing.assert_allclose(r["y"], flat["y"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(r["importance_H"], flat["importance"], rtol=1e-13)
+    assert np.all(r["group_count"] > 0)
+    np.testing.assert_allclose(r["load_H"], flat["load"], rtol=1e-12)
+
+
+def pin_hier_empty_group_guard(orc):
+    """A group that no token's primary gate picks has |X^(i)| = 0, and its
+    Load_H entries are 0 (the quotient is undefined there); the product gates
+    of every token sum to 1, so Importance_H sums to T."""
+    rng = np.random.default_rng(53)
+    T, d, a, b, kp, ks, d_ff = 25, 3, 3, 4, 2, 2, 3
+    inp = _hier_case(rng, T, d, a, b, d_ff, noisy=False)
+    x = inp["x"].copy()
+    x[:, 0] = 1.0
+    inp["x"] = x
+    Wp = np.zeros((d, a), np.float32)
+    Wp[0] = [5.0, 4.0, -10.0]  # group 2 is always the lowest of the three
+    inp.update(Wp=Wp, kp=kp, ks=ks)
+    r = orc.hier_forward(inp)
+    assert list(r["group_count"]) == [T, T, 0]
+    assert np.all(r["load_H"][2 * b:] == 0.0)
+    assert np.all(np.isfinite(r["load_H"]))
+    np.testing.assert_allclose(r["importance_H"].sum(), T, rtol=1e-13)
+    # noise-free: Load_H of a picked group is the in-group pick count (the
+    # primary load of a group picked by every token is T = |X^(i)|)
+    cnt = np.bincount(r["idx"].reshape(-1), minlength=a * b).astype(np.float64)
+    np.testing.assert_allclose(r["load_H"][:2 * b], cnt[:2 * b], rtol=1e-13)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

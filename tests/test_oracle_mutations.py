@@ -39,6 +39,20 @@ MUTATIONS = {
     "kplus1_threshold_off_by_one": ("hk1[t] = (k < E) ? h[order[k]] : -INFINITY;",
                                     "hk1[t] = (k < E) ? h[order[k - 1]] : -INFINITY;"),
     "phi_argument_unscaled": ("erfc(-u / sqrt(2.0))", "erfc(-u)"),
+    "hier_gate_not_product": ("gate[(size_t)t * k + q * ks + r] = g_p[(size_t)t * kp + q] * sg[r];",
+                              "gate[(size_t)t * k + q * ks + r] = sg[r];"),
+    "hier_index_not_offset": ("idx[(size_t)t * k + q * ks + r] = i * b + sidx[r];",
+                              "idx[(size_t)t * k + q * ks + r] = sidx[r];"),
+    "hier_guard_missing": ("count[i] > 0 ? load_p[i] * loadsec[e] / (double)count[i] : 0.0",
+                           "load_p[i] * loadsec[e] / (double)count[i]"),
+    "hier_load_not_normalised": ("count[i] > 0 ? load_p[i] * loadsec[e] / (double)count[i] : 0.0",
+                                 "count[i] > 0 ? load_p[i] * loadsec[e] : 0.0"),
+    "hier_primary_load_dropped": ("count[i] > 0 ? load_p[i] * loadsec[e] / (double)count[i] : 0.0",
+                                  "count[i] > 0 ? loadsec[e] / (double)count[i] : 0.0"),
+    "hier_threshold_swapped": ("chosen ? hk1s[(size_t)t * kp + q] : hks[(size_t)t * kp + q]",
+                               "chosen ? hks[(size_t)t * kp + q] : hk1s[(size_t)t * kp + q]"),
+    "hier_secondary_load_dropped": ("      count[i] += 1;\n      for (int j = 0; j < b; ++j) {",
+                                       "      count[i] += 1;\n      for (int j = 0; j < b && 0; ++j) {"),
 }
 
 
