@@ -412,10 +412,6 @@ def run_ours(args, w: wl.Workload):
         "aux_loss": {"ms": mean["aux_loss"]},
     }
     tps = job_tokens_per_s(world, T, ms)
-    # router (plus the weight split that feeds the tensor-core router for bf16
-    # tokens), selection with the balancing partials (one fused kernel up to
-    # 256 experts, two beyond), slot histogram / scan / rank, gather, two
-    # expert GEMMs, combine, balancing finalize
     # Router (weight split + tensor-core kernel for bf16), selection (none
     # when the tensor-core router selects in its own epilogue: bf16,
     # d % 8 == 0, every expert in one 64-column block, E % 4 == 0, k <= 8),
@@ -481,6 +477,252 @@ def run_ours(args, w: wl.Workload):
     return line
 
 
+# ----------------------------------------------------------------------------- hierarchical layer
+
+
+def run_hier(args, w: wl.HierWorkload):
+    """The hierarchical layer: the value is moe_forward_hier over resident
+    inputs (median of the timed steps, L2 flushed before each); the expert
+    GEMMs, dispatch and combine are also timed through the stage calls on the
+    layer's own routing (its flat choices over the a*b experts), interleaved."""
+    import torch
+    import torch.distributed as dist
+
+    from sparsely_gated_mixture_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    inp = wl.generate_hier(w, seed=0)
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(a, is_act=False):
+        if a is None:
+            return None
+        if is_act and w.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    x = to_dev(inp["x"], True)
+    Wp, Wpn, noise_p, Ws, Wsn, noise_s = (to_dev(inp[n]) for n in
+                                          ("Wp", "Wpn", "noise_p", "Ws", "Wsn", "noise_s"))
+    W1, W2 = to_dev(inp["W1"], True), to_dev(inp["W2"], True)
+    hcfg = B.hier_config_for(w)
+    fcfg = B.config(w.T, w.d, w.E, w.d_ff, w.k, w.cf, B.MOE_GATE_TOPK_SOFTMAX,
+                    B.MOE_BF16 if w.dtype == "bf16" else B.MOE_F32, w.min_cap)
+    T, k, E, d, dff = w.T, w.k, w.E, w.d, w.d_ff
+    A = T * k
+    z = dict(device=dev)
+    ws = torch.empty(B.moe_hier_workspace_size(hcfg), dtype=torch.uint8, **z)
+    ws_f = torch.empty(B.moe_workspace_size(fcfg), dtype=torch.uint8, **z)
+    idx = torch.empty((T, k), dtype=torch.int32, **z)
+    gate = torch.empty((T, k), dtype=torch.float32, **z)
+    pos = torch.empty((T, k), dtype=torch.int32, **z)
+    keep = torch.empty((T, k), dtype=torch.uint8, **z)
+    count = torch.empty(E, dtype=torch.int32, **z)
+    offset = torch.empty(E + 1, dtype=torch.int32, **z)
+    xbuf = torch.empty((A, d), dtype=act, **z)
+    row_token = torch.empty(A, dtype=torch.int32, **z)
+    row_gate = torch.empty(A, dtype=torch.float32, **z)
+    hbuf = torch.empty((A, dff), dtype=act, **z)
+    zbuf = torch.empty((A, d), dtype=torch.float32, **z)
+    y = torch.empty((T, d), dtype=act, **z)
+    y2 = torch.empty_like(y)
+    out2 = torch.zeros(2, dtype=torch.float32, **z)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, **z)
+
+    def fwd(xx=x, npp=noise_p, nss=noise_s, yy=y, oo=out2, with_choices=True):
+        B.moe_forward_hier(hcfg, xx, Wp, Wpn, npp, Ws, Wsn, nss, W1, None, W2, None, yy, oo, ws,
+                           idx if with_choices else None, gate if with_choices else None,
+                           stream=stream)
+
+    def stages(ev):
+        ev[0].record(stream)
+        B.moe_dispatch(fcfg, idx, gate, x, pos, keep, count, offset, xbuf, row_token, row_gate,
+                       ws_f, stream)
+        ev[1].record(stream)
+        B.moe_expert_ffn(fcfg, xbuf, offset, row_gate, W1, None, W2, None, hbuf, zbuf, ws_f,
+                         stream)
+        ev[2].record(stream)
+        B.moe_combine(fcfg, x, zbuf, pos, keep, idx, offset, y2, ws_f, stream)
+        ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        stages([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) during warm-up")
+    accepted = int(keep.sum().item())
+    experts_used = int((torch.minimum(count, torch.tensor(w.capacity, device=dev)) > 0).sum())
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()
+        fevs[i][0].record(stream)
+        fwd()
+        fevs[i][1].record(stream)
+        flush.zero_()
+        stages(sevs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the timed region")
+    ms = slowest_rank_ms(statistics.median(f[0].elapsed_time(f[1]) for f in fevs), world, dev)
+    names = ["dispatch", "expert_ffn", "combine"]
+    mean = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in sevs)
+            for j, n in enumerate(names)}
+
+    # End to end: x and both noise tensors in from pinned host memory, y and
+    # the two losses back, every step inside the timed region (copies on
+    # their own streams, overlapping the neighbouring steps' compute).
+    hosts = [t.cpu().pin_memory() for t in (x, noise_p, noise_s) if t is not None]
+    devs = [[torch.empty_like(t) for t in (x, noise_p, noise_s) if t is not None]
+            for _ in range(2)]
+    y_d = [torch.empty_like(y) for _ in range(2)]
+    o_d = [torch.empty(2, dtype=torch.float32, **z) for _ in range(2)]
+    y_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+    o_h = [torch.empty(2, dtype=torch.float32).pin_memory() for _ in range(2)]
+    up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    fwd_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def h2d(i):
+        b = i % 2
+        with torch.cuda.stream(up_s):
+            if i >= 2:
+                up_s.wait_event(fwd_done[b])
+            for dd, hh in zip(devs[b], hosts):
+                dd.copy_(hh, non_blocking=True)
+            h2d_done[b].record(up_s)
+
+    def step_e2e(i):
+        b = i % 2
+        stream.wait_event(h2d_done[b])
+        if i >= 2:
+            stream.wait_event(d2h_done[b])
+        dv = list(devs[b])
+        xx = dv.pop(0)
+        npp = dv.pop(0) if noise_p is not None else None
+        nss = dv.pop(0) if noise_s is not None else None
+        fwd(xx, npp, nss, y_d[b], o_d[b], with_choices=False)
+        fwd_done[b].record(stream)
+        with torch.cuda.stream(down_s):
+            down_s.wait_event(fwd_done[b])
+            y_h[b].copy_(y_d[b], non_blocking=True)
+            o_h[b].copy_(o_d[b], non_blocking=True)
+            d2h_done[b].record(down_s)
+
+    def run_e2e(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d(i + 1)
+            step_e2e(i)
+
+    run_e2e(max(3, args.warmup))
+    torch.cuda.synchronize()
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
+    up_s.wait_stream(stream)
+    run_e2e(args.steps)
+    stream.wait_stream(up_s)
+    stream.wait_stream(down_s)
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(a_ev.elapsed_time(b_ev) / args.steps, world, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    peaks, peak_kind = load_peaks()
+    s = 2 if w.dtype == "bf16" else 4
+    ffn_flops = 4 * d * dff * accepted
+    ffn_bytes = (2 * experts_used * d * dff * s + accepted * d * s + 2 * accepted * dff * s
+                 + accepted * d * 4)
+    ffn_s = mean["expert_ffn"] * 1e-3
+    t_flops = ffn_flops / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = ffn_bytes / (peaks["hbm_gbs"] * 1e9)
+    roof = {"kernel": "moe_expert_ffn (two grouped GEMM launches) on the layer's routing"}
+    if t_bytes > t_flops:
+        gbs = ffn_bytes / ffn_s / 1e9
+        roof.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"]})
+    else:
+        tf = ffn_flops / ffn_s / 1e12
+        roof.update({"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]})
+    roof.update({"peak_source": peak_kind, "algorithmic_flops_per_launch": ffn_flops,
+                 "algorithmic_bytes": ffn_bytes, "traffic": None})
+    tc = w.dtype == "bf16" and w.d % 8 == 0
+    # primary gate (split + router with fused selection, or + selection),
+    # primary finalize, secondary split + router, two-level selection,
+    # finalize, tail; three slot kernels, gather, two GEMMs, combine
+    prim_fused = tc and (2 * w.a if w.noisy else w.a) <= 64 and w.a % 4 == 0 and w.kp <= 8
+    launches = ((2 if tc else 1) + (0 if prim_fused else 1) + 1 + (2 if tc else 1) + 1 + 1 + 1
+                + 3 + 1 + 2 + 1)
+    line = {
+        "metric": "hierarchical MoE layer fwd tokens/s @1 GB300",
+        "value": job_tokens_per_s(world, T, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights, N(0,1) gate noise)",
+        "config": {"workload": w.name, "T": T, "d": d, "groups": w.a, "experts_per_group": w.b,
+                   "k_primary": w.kp, "k_secondary": w.ks, "d_ff": dff, "capacity_factor": w.cf,
+                   "noisy": w.noisy, "capacity": w.capacity, "seed": 0,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write)", "accepted_rows": accepted,
+                   "dropped_fraction": 1 - accepted / A},
+        "roofline": roof,
+        "stages": {n: {"ms": mean[n]} for n in names},
+        "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hosts),
+                "d2h_bytes_per_step": y.numel() * y.element_size() + 8},
+        "gpu_launches": (launches + 1 + 2 + 1) * args.steps,  # forward + stage calls
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_hier(w, inp, args.cpu_sample)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def cpu_baseline_hier(w: wl.HierWorkload, inp: dict, n_sample: int) -> dict:
+    """The oracle's hierarchical layer on the host cores: both gates, the
+    two-level selection, slots and losses over every token, the expert loop
+    for n_sample tokens, extrapolated."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    n = min(n_sample, w.T)
+    tokens = np.linspace(0, w.T - 1, n).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.hier_forward(inp, tokens=tokens[:0])
+    t_gate = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.hier_forward(inp, tokens=tokens)
+    t_all = time.perf_counter() - t0
+    t_ffn = max(t_all - t_gate, 1e-9)
+    full = t_gate + t_ffn * (w.T / n)
+    return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"gates, selection, slots and losses over all {w.T} tokens "
+                      f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens, "
+                      f"extrapolated to {w.T} tokens"}
+
+
 # ----------------------------------------------------------------------------- oracle timing
 
 
@@ -537,13 +779,38 @@ def run_reference(args, w: wl.Workload):
     }
 
 
+def run_reference_hier(args, w: wl.HierWorkload):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    inp = wl.generate_hier(w, seed=0)
+    cpu_baseline_hier(w, inp, 2)
+    vals, last = [], None
+    for _ in range(args.steps):
+        last = cpu_baseline_hier(w, inp, args.cpu_sample)
+        vals.append(last["value"])
+    v = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": "hierarchical MoE layer fwd tokens/s @1 GB300", "value": v,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": w.T / v * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "parallelism": "host cores"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="top2_large_experts", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default="top2_large_experts",
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.HIER_WORKLOADS))
     ap.add_argument("--cpu-sample", type=int, default=16,
                     help="tokens whose expert loop the oracle runs for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -553,6 +820,14 @@ def main():
                     help="override E (smaller cases for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    if args.workload in wl.HIER_WORKLOADS:
+        w = wl.HIER_WORKLOADS[args.workload]
+        if args.tokens:
+            w = w.with_(T=args.tokens)
+        line = (run_reference_hier(args, w) if args.impl == "reference" else run_hier(args, w))
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     w = wl.WORKLOADS[args.workload]
     if args.tokens:
         w = w.with_(T=args.tokens)

@@ -208,6 +208,54 @@ int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx, const
                          float *row_gate, moe_stream_t stream);
 
 /*
+ * Hierarchical layer ("Outrageously Large Neural Networks", Hierarchical
+ * Mixture-of-Experts): a groups of b experts, flat expert i*b + j. A primary
+ * noisy top-k gate over the a groups picks k_primary groups; in each picked
+ * group i a secondary noisy top-k gate over its b experts picks
+ * k_secondary; the output is y_H = x + sum_i sum_j G_primary(x)_i G_i(x)_j
+ * E_ij(x), with capacity and token-order slots over the a*b experts exactly as
+ * in moe_forward (k = k_primary * k_secondary choices per token, in primary
+ * pick order, then secondary pick order).
+ */
+typedef struct {
+  int32_t T;               /* tokens, >= 1 */
+  int32_t d;               /* token width, >= 1 */
+  int32_t a;               /* groups, >= 1 */
+  int32_t b;               /* experts per group, >= 1; a * b <= 1024 */
+  int32_t k_primary;       /* groups per token, 1 <= k_primary <= min(a, 8) */
+  int32_t k_secondary;     /* experts per picked group, 1 <= k_secondary <= min(b, 8) */
+  int32_t d_ff;            /* expert hidden width, >= 1 */
+  float capacity_factor;   /* > 0; C = max(min_capacity, min(T, floor(k*T*cf/(a*b)))) */
+  int32_t min_capacity;    /* >= 1 */
+  int32_t act_dtype;       /* moe_dtype */
+} moe_hier_config;
+
+/* Bytes of workspace moe_forward_hier needs for `cfg`. Host only. */
+int moe_hier_workspace_size(const moe_hier_config *cfg, size_t *bytes);
+
+/*
+ * The hierarchical layer in one call. Primary gate: Wp, Wp_noise [d,a] fp32,
+ * noise_p [T,a] fp32; secondary gates: Ws, Ws_noise [d,a*b] fp32 (group i owns
+ * columns i*b .. i*b+b-1), noise_s [T,a*b] fp32; each noise pair is both given
+ * or both NULL (that gate without noise). Experts: W1 [a*b,d,d_ff], b1
+ * [a*b,d_ff], W2 [a*b,d_ff,d], b2 [a*b,d] as in moe_forward (biases may be
+ * NULL). Outputs: y [T,d] (act_dtype); aux_out2 [2] fp32 or NULL =
+ * [CV(Importance_H)^2, CV(Load_H)^2] with Importance_H[i*b+j] = sum_x
+ * G_primary(x)_i G_i(x)_j and Load_H[i*b+j] = Load_primary(X)_i *
+ * Load_i(X^(i))_j / |X^(i)| (X^(i): the tokens whose primary gate picked
+ * group i; Load_H is 0 for a group no token picked); optionally (each may be
+ * NULL) expert_idx [T,k] (flat i*b + j), gate [T,k] (the products), pos and
+ * keep [T,k]. Device-side errors go to the status word at the start of `ws`
+ * (moe_last_device_status reads it); the call clears it first.
+ */
+int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
+                     const float *Wp_noise, const float *noise_p, const float *Ws,
+                     const float *Ws_noise, const float *noise_s, const void *W1, const void *b1,
+                     const void *W2, const void *b2, void *y, float *aux_out2,
+                     int32_t *expert_idx, float *gate, int32_t *pos, uint8_t *keep, void *ws,
+                     moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the first device-side error recorded in `ws`
  * since it was last cleared (MOE_OK if none), writes its detail word (e.g. the
  * offending flat index) to *detail if non-NULL, and clears it.

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
-           "moe_last_device_status", "moe_dispatch_noalloc")
+           "moe_last_device_status", "moe_dispatch_noalloc", "moe_hier_workspace_size",
+           "moe_forward_hier")
 
 
 class MoEError(RuntimeError):
@@ -53,6 +54,20 @@ def config_for(w) -> moe_config:
                   MOE_BF16 if w.dtype == "bf16" else MOE_F32, w.min_cap)
 
 
+class moe_hier_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("a", ctypes.c_int32),
+                ("b", ctypes.c_int32), ("k_primary", ctypes.c_int32),
+                ("k_secondary", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float), ("min_capacity", ctypes.c_int32),
+                ("act_dtype", ctypes.c_int32)]
+
+
+def hier_config_for(w) -> moe_hier_config:
+    """moe_hier_config of a workloads.HierWorkload."""
+    return moe_hier_config(w.T, w.d, w.a, w.b, w.kp, w.ks, w.d_ff, w.cf, w.min_cap,
+                           MOE_BF16 if w.dtype == "bf16" else MOE_F32)
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -78,6 +93,9 @@ def lib():
             L.moe_forward.argtypes = [CP] + [P] * 17
             L.moe_last_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int64)]
             L.moe_dispatch_noalloc.argtypes = [CP] + [P] * 11
+            HP = ctypes.POINTER(moe_hier_config)
+            L.moe_hier_workspace_size.argtypes = [HP, ctypes.POINTER(ctypes.c_size_t)]
+            L.moe_forward_hier.argtypes = [HP] + [P] * 19
             for name in EXPORTS[1:]:
                 getattr(L, name).restype = I
             _lib = L
@@ -159,6 +177,21 @@ def moe_forward(cfg, x, Wg, Wnoise, noise, logit_bias, W1, b1, W2, b2, y, aux_ou
                              _p(logit_bias), _p(W1), _p(b1), _p(W2), _p(b2), _p(y), _p(aux_out3),
                              _p(expert_idx), _p(gate), _p(pos), _p(keep), _p(ws),
                              _stream(stream)), "moe_forward")
+
+
+def moe_hier_workspace_size(cfg: moe_hier_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_hier_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_hier_workspace_size")
+    return n.value
+
+
+def moe_forward_hier(cfg, x, Wp, Wp_noise, noise_p, Ws, Ws_noise, noise_s, W1, b1, W2, b2, y,
+                     aux_out2, ws, expert_idx=None, gate=None, pos=None, keep=None, stream=None):
+    _check(lib().moe_forward_hier(ctypes.byref(cfg), _p(x), _p(Wp), _p(Wp_noise), _p(noise_p),
+                                  _p(Ws), _p(Ws_noise), _p(noise_s), _p(W1), _p(b1), _p(W2),
+                                  _p(b2), _p(y), _p(aux_out2), _p(expert_idx), _p(gate), _p(pos),
+                                  _p(keep), _p(ws), _stream(stream)), "moe_forward_hier")
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

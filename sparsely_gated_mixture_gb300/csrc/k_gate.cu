@@ -921,6 +921,201 @@ k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
   finish_aux(E, aux, out3, st, sh);
 }
 
+// ----------------------------------------------------------------------------- hierarchical gate
+// "Outrageously Large", Hierarchical Mixture-of-Experts: a groups of b
+// experts (flat expert i*b + j). The primary gate (the flat gate over a
+// groups) has picked groups idx_p [T,kp] with gates g_p [T,kp]; here each
+// picked group's secondary gate takes the top ks of its b secondary noisy
+// logits (warp_topk: value descending, lower index first) with a softmax over
+// them, and token t's choice q*ks + r is expert i*b + j_r with gate
+// g_p[t,q] * G_i(x_t)_{j_r}.
+//
+// Balancing partials, one row per block of kHierTok tokens, for the finalize:
+// [0] Importance_H (sum of the product gates), [1] the in-group smooth load
+// Load_i(X^(i))_j (P_i(x, j) = Phi((c - kth_excluding) / sigma) inside the
+// group, summed over the tokens that picked group i; the pick indicator
+// without noise; 1 when ks == b), [2] |X^(i)| at j = 0 of each group (0
+// elsewhere), [3] 0. A warp takes whole groups and its lanes the group's
+// experts, walking the block's tokens in order, so every sum has one fixed
+// order and the loads of a token's group row are coalesced.
+constexpr int kHierTokMax = 64;  // tokens per block and per partial row (64, or 32: hier_tokens)
+constexpr int kHierWarps = 8;
+constexpr int kHierMaxKp = 8;    // largest primary k
+
+// Tokens per block: 64, or 32 when the block's P buffer ([tokens][kp][b]
+// floats, kp*b <= a*b <= 1024) would pass 128 KB at 64.
+__host__ __device__ inline int hier_tokens(int kp, int b) { return kp * b <= 512 ? 64 : 32; }
+
+template <int VPL, int KMS>  // b <= 32 * VPL, ks <= KMS
+__global__ void __launch_bounds__(kHierWarps * 32)
+k_hier_select(int T, int a, int b, int kp, int ks, int noisy, const int32_t *__restrict__ idx_p,
+              const float *__restrict__ g_p, const float *__restrict__ cs,
+              const float *__restrict__ ss, const float *__restrict__ Hs,
+              int32_t *__restrict__ idx, float *__restrict__ gate, float *__restrict__ partials,
+              DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_grp[kHierTokMax][kHierMaxKp];        // picked group, or -1
+  __shared__ float s_gp[kHierTokMax][kHierMaxKp];       // its primary gate
+  __shared__ int s_pick[kHierTokMax][kHierMaxKp][KMS];  // in-group picks
+  __shared__ float s_gate[kHierTokMax][kHierMaxKp][KMS];  // their product gates
+  extern __shared__ float s_P[];                        // [tokens][kp][b]: P_i(x_t, j)
+  const int E = a * b, k = kp * ks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int TB = hier_tokens(kp, b);
+  const int t0 = blockIdx.x * TB, nt = min(TB, T - t0);
+  const bool sums = partials != nullptr;
+  for (int u = threadIdx.x; u < nt * kp; u += blockDim.x) {  // the block's primary picks
+    const int i = idx_p[(size_t)t0 * kp + u];
+    s_grp[u / kp][u % kp] = (i >= 0 && i < a) ? i : -1;
+    s_gp[u / kp][u % kp] = g_p[(size_t)t0 * kp + u];
+  }
+  __syncthreads();
+  for (int pr = warp; pr < nt * kp; pr += kHierWarps) {
+    const int tt = pr / kp, q = pr - tt * kp;
+    const size_t t = (size_t)t0 + tt;
+    const int i = s_grp[tt][q];
+    if (i < 0) {  // the primary gate flagged a NaN row, or a bad index
+      if (lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)t);
+      if (lane < ks) {
+        idx[t * k + q * ks + lane] = E;  // out of range: the slot pass rejects it
+        gate[t * k + q * ks + lane] = 0.f;
+      }
+      continue;
+    }
+    // The group's row of H, c and sigma, loaded together (one trip).
+    const size_t o = t * E + (size_t)i * b;
+    float v[VPL], cv[VPL], sv[VPL];
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) {
+      const int j = lane + 32 * m;
+      v[m] = j < b ? Hs[o + j] : -INFINITY;
+      cv[m] = (sums && noisy && j < b) ? cs[o + j] : 0.f;
+      sv[m] = (sums && noisy && j < b) ? ss[o + j] : 0.f;
+    }
+    float myv = -INFINITY, mx, se;
+    int myi = b;
+    warp_topk<VPL>(v, b, ks, lane, myv, myi, mx, se);
+    const float gs = warp_gate(myv, ks, MOE_GATE_TOPK_SOFTMAX, mx, se, lane);
+    const float th0 = __shfl_sync(0xffffffffu, myv, ks - 1);
+    const float thk = __shfl_sync(0xffffffffu, myv, ks & 31);
+    const float th1 = ks < b ? thk : -INFINITY;
+    const float gp = s_gp[tt][q];
+    if (lane < ks) {
+      const float g = gp * gs;
+      idx[t * k + q * ks + lane] = myi < b ? i * b + myi : E;
+      gate[t * k + q * ks + lane] = g;
+      s_pick[tt][q][lane] = myi;
+      s_gate[tt][q][lane] = g;
+    }
+    if (!sums) continue;
+    // P_i(x_t, j) for the group's experts: Phi((c - kth_excluding) / sigma),
+    // kth_excluding = the (ks+1)-th in-group logit for a pick, else the ks-th.
+    int pk[KMS];
+#pragma unroll
+    for (int r = 0; r < KMS; ++r) pk[r] = __shfl_sync(0xffffffffu, myi, r);
+    float *P = s_P + ((size_t)tt * kp + q) * b;
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) {
+      const int j = lane + 32 * m;
+      if (j >= b) break;
+      bool in = false;
+#pragma unroll
+      for (int r = 0; r < KMS; ++r) in |= r < ks && pk[r] == j;
+      float p;
+      if (ks == b) p = 1.f;
+      else if (sv[m] == 0.f) p = in ? 1.f : 0.f;
+      else p = normal_cdf(__fdividef(cv[m] - (in ? th1 : th0), sv[m]));
+      P[j] = p;
+    }
+  }
+  if (!sums) return;
+  __syncthreads();
+  // Per group (a warp) and expert (a lane): the block's tokens in order.
+  float *row = partials + (size_t)blockIdx.x * 4 * E;
+  for (int i = warp; i < a; i += kHierWarps) {
+    float imp[VPL], ld[VPL];
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) imp[m] = ld[m] = 0.f;
+    float cnt = 0.f;
+    for (int tt = 0; tt < nt; ++tt) {
+      for (int q = 0; q < kp; ++q) {
+        if (s_grp[tt][q] != i) continue;
+        cnt += 1.f;
+        const float *P = s_P + ((size_t)tt * kp + q) * b;
+#pragma unroll
+        for (int m = 0; m < VPL; ++m) {
+          const int j = lane + 32 * m;
+          if (j >= b) break;
+          float gv = 0.f;
+#pragma unroll
+          for (int r = 0; r < KMS; ++r)
+            if (r < ks && s_pick[tt][q][r] == j) gv = s_gate[tt][q][r];
+          imp[m] += gv;
+          ld[m] += P[j];
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < VPL; ++m) {
+      const int j = lane + 32 * m;
+      if (j >= b) break;
+      const int e = i * b + j;
+      row[e] = imp[m];
+      row[E + e] = ld[m];
+      row[2 * E + e] = j == 0 ? cnt : 0.f;
+      row[3 * E + e] = 0.f;
+    }
+  }
+}
+
+// The hierarchical losses from the two finalizes' sums (one block, a thread
+// per flat expert): Load_H[i*b+j] = Load_p[i] * Load_i(X^(i))_j / |X^(i)|,
+// 0 where |X^(i)| = 0 (in fp32, about 1e-7 relative); out2 =
+// [CV(Importance_H)^2, CV(Load_H)^2] with the population variance, the means
+// and squared deviations summed in double-float in a fixed order (as the flat
+// finalize does). |X^(i)| comes back from the finalize as a mean over T and
+// is restored to the integer count. Also carries an error the primary gate
+// recorded in its own status word over to the layer's status word.
+constexpr int kHierTailThreads = 1024;
+
+__global__ void __launch_bounds__(kHierTailThreads)
+k_hier_tail(int T, int a, int b, const float2 *__restrict__ aux_s, const float2 *__restrict__ aux_p,
+            float *__restrict__ out2, DeviceStatus *st, const DeviceStatus *st_p) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ ff sh[32 * 2 + 2];
+  const int E = a * b, e = threadIdx.x;
+  if (threadIdx.x == 0 && st->code == 0 && st_p->code != 0) {
+    st->detail = st_p->detail;
+    st->code = st_p->code;
+  }
+  if (!out2) return;
+  ff imp{0.f, 0.f}, lh{0.f, 0.f};
+  if (e < E) {
+    const int i = e / b;
+    imp = ff_ld(aux_s + e);
+    const float2 al = aux_s[E + e], ac = aux_s[2 * E + i * b], ap = aux_p[a + i];
+    const float cnt = (float)rint(((double)ac.x + (double)ac.y) * T);
+    lh.hi = cnt > 0.f ? (ap.x + ap.y) * (al.x + al.y) / cnt : 0.f;
+  }
+  ff m2[2] = {imp, lh};
+  block_sum_ff<2>(m2, sh);
+  const double m_imp = ff_to_d(m2[0]) / E, m_ld = ff_to_d(m2[1]) / E;
+  ff v2[2] = {{0.f, 0.f}, {0.f, 0.f}};
+  if (e < E) {
+    const ff di = ff_add(imp, d_to_ff(-m_imp)), dl = ff_add(lh, d_to_ff(-m_ld));
+    v2[0] = ff_mul(di, di);
+    v2[1] = ff_mul(dl, dl);
+  }
+  block_sum_ff<2>(v2, sh);
+  if (threadIdx.x == 0) {
+    const double v_imp = ff_to_d(v2[0]) / E, v_ld = ff_to_d(v2[1]) / E;
+    out2[0] = (float)(v_imp / (m_imp * m_imp));
+    out2[1] = (float)(v_ld / (m_ld * m_ld));
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_router(const moe_config &cfg, const void *x, const float *Wg, const float *Wn,
@@ -1051,6 +1246,57 @@ cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, in
   else
     launch_pdl_c(kPdlFinalize, k_aux_finalize_cols, dim3((cfg.E + 31) / 32, 4), kFinColThreads, 0,
         s, cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hier_select(int T, int a, int b, int kp, int ks, bool noisy,
+                               const int32_t *idx_p, const float *g_p, const float *cs,
+                               const float *ss, const float *Hs, int32_t *idx, float *gate,
+                               float *partials, DeviceStatus *st, cudaStream_t s) {
+  if (kp > kHierMaxKp || ks > 8 || kp * b > 1024) return cudaErrorInvalidValue;
+  const int TB = hier_tokens(kp, b);
+  const dim3 grid((T + TB - 1) / TB);
+  const size_t dsm = partials ? (size_t)TB * kp * b * 4 : 0;
+  const int vpl = (b + 31) / 32;
+#define MOE_HIER_K(V, KM)                                                                     \
+  do {                                                                                         \
+    cudaError_t e_ = cudaFuncSetAttribute(k_hier_select<V, KM>,                               \
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,         \
+                                          (int)dsm);                                           \
+    if (e_ != cudaSuccess) return e_;                                                          \
+    launch_pdl(k_hier_select<V, KM>, grid, kHierWarps * 32, dsm, s, T, a, b, kp, ks,          \
+               noisy ? 1 : 0, idx_p, g_p, cs, ss, Hs, idx, gate, partials, st);                \
+  } while (0)
+#define MOE_HIER(V)               \
+  do {                            \
+    if (ks <= 2)                  \
+      MOE_HIER_K(V, 2);           \
+    else if (ks <= 4)             \
+      MOE_HIER_K(V, 4);           \
+    else                          \
+      MOE_HIER_K(V, 8);           \
+  } while (0)
+  if (vpl <= 1) MOE_HIER(1);
+  else if (vpl <= 2) MOE_HIER(2);
+  else if (vpl <= 4) MOE_HIER(4);
+  else if (vpl <= 8) MOE_HIER(8);
+  else if (vpl <= 16) MOE_HIER(16);
+  else MOE_HIER(32);
+#undef MOE_HIER
+#undef MOE_HIER_K
+  return cudaGetLastError();
+}
+
+int hier_rows(int T, int kp, int b) {
+  const int TB = hier_tokens(kp, b);
+  return (T + TB - 1) / TB;
+}
+
+cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const float2 *aux_p,
+                             float *out2, DeviceStatus *st, const DeviceStatus *st_p,
+                             cudaStream_t s) {
+  if (a * b > kHierTailThreads) return cudaErrorInvalidValue;
+  launch_pdl(k_hier_tail, 1, kHierTailThreads, 0, s, T, a, b, aux_s, aux_p, out2, st, st_p);
   return cudaGetLastError();
 }
 

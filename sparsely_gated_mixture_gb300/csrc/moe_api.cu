@@ -148,6 +148,89 @@ static int ffn_impl(const moe_config &c, const void *xbuf, const int32_t *offset
   return MOE_OK;
 }
 
+// Stages 3-4 of the forward from a selection: slots and dispatch, the expert
+// GEMMs, combine (the intermediate buffers in `ws` laid out by L).
+static int expert_path(const moe_config &c, const WsLayout &L, void *ws, const void *x,
+                       const int32_t *idx, const float *g, int32_t *ps, uint8_t *kp,
+                       const void *W1, const void *b1, const void *W2, const void *b2, void *y,
+                       DeviceStatus *st, cudaStream_t s) {
+  int32_t *offset = ws_at<int32_t>(ws, L.offset);
+  int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
+  float *row_gate = ws_at<float>(ws, L.row_gate);
+  void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
+  float *zbuf = ws_at<float>(ws, L.zbuf);
+  MOE_CUDA(launch_slots(c, host_capacity(c), idx, g, ws_at<int32_t>(ws, L.hist),
+                        ws_at<int32_t>(ws, L.chunk_base), ws_at<int32_t>(ws, L.count), offset,
+                        ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
+                        s));
+  MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
+  const bool z_bf16 = forward_z_bf16(c);
+  const int r = ffn_impl(c, xbuf, offset, ws_at<int32_t>(ws, L.mtiles), row_gate, W1, b1, W2,
+                         b2, hbuf, zbuf, z_bf16, st, s);
+  if (r != MOE_OK) return r;
+  MOE_CUDA(launch_combine(c, x, zbuf, z_bf16, ps, kp, idx, offset, y, st, s));
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------------------------- hierarchical layer
+// The secondary side is a flat layer over the a*b experts with k = kp*ks; the
+// primary gate is a flat gate over the a groups. The workspace holds the
+// flat layout of the former (status word first), then the latter's, then the
+// hierarchical partial rows and the finalizes' scratch outputs.
+static moe_config hier_secondary(const moe_hier_config &h) {
+  moe_config c{};
+  c.T = h.T;
+  c.d = h.d;
+  c.E = h.a * h.b;
+  c.d_ff = h.d_ff;
+  c.k = h.k_primary * h.k_secondary;
+  c.capacity_factor = h.capacity_factor;
+  c.min_capacity = h.min_capacity;
+  c.gate_mode = MOE_GATE_TOPK_SOFTMAX;
+  c.act_dtype = h.act_dtype;
+  return c;
+}
+
+static moe_config hier_primary(const moe_hier_config &h) {
+  moe_config c = hier_secondary(h);
+  c.E = h.a;
+  c.k = h.k_primary;
+  return c;
+}
+
+struct HierLayout {
+  WsLayout Ls, Lp;
+  size_t off_p, parts, scratch, total;
+  int rows;
+};
+
+static HierLayout hier_layout(const moe_hier_config &h) {
+  HierLayout H;
+  H.Ls = ws_layout(hier_secondary(h));
+  H.Lp = ws_layout(hier_primary(h));
+  H.rows = hier_rows(h.T, h.k_primary, h.b);
+  size_t off = align_up(H.Ls.total, 256);
+  H.off_p = off;
+  off = align_up(off + H.Lp.total, 256);
+  H.parts = off;
+  off = align_up(off + (size_t)H.rows * 4 * (size_t)h.a * h.b * 4, 256);
+  H.scratch = off;  // two finalize outputs of 3 floats
+  H.total = align_up(off + 64, 256);
+  return H;
+}
+
+static int check_hier(const moe_hier_config *h) {
+  if (!h) return MOE_ERR_ARG;
+  if (h->a < 1 || h->b < 1 || h->k_primary < 1 || h->k_secondary < 1 ||
+      h->k_primary > h->a || h->k_secondary > h->b)
+    return MOE_ERR_ARG;
+  if (h->k_primary > 8 || h->k_secondary > 8 || (long long)h->a * h->b > 1024)
+    return MOE_ERR_UNSUPPORTED;
+  const moe_config cs = hier_secondary(*h), cp = hier_primary(*h);
+  const int r = check_cfg(&cs);
+  return r != MOE_OK ? r : check_cfg(&cp);
+}
+
 // One side stream (non-blocking) and a fork / join event pair per device,
 // made on first use and kept; the lock is held while a call enqueues on them,
 // so calls from several host threads do not interleave their records.
@@ -312,11 +395,6 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
   int32_t *ps = pos ? pos : ws_at<int32_t>(ws, L.pos);
   uint8_t *kp = keep ? keep : ws_at<uint8_t>(ws, L.keep);
   float *thr = ws_at<float>(ws, L.thr);
-  int32_t *offset = ws_at<int32_t>(ws, L.offset);
-  int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
-  float *row_gate = ws_at<float>(ws, L.row_gate);
-  void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
-  float *zbuf = ws_at<float>(ws, L.zbuf);
   r = gate_impl(c, x, Wg, Wnoise, noise, logit_bias, idx, g, thr, ws, aux_out3 != nullptr, s);
   if (r != MOE_OK) return r;
   // The balancing finalize needs only the gate's partial sums: it runs on the
@@ -335,22 +413,80 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
     MOE_CUDA(launch_aux_finalize(c, ws_at<float>(ws, L.partials), L.n_aux_blocks, aux_out3,
                                  nullptr, nullptr, ws_at<float2>(ws, L.aux_vec), st, fs));
   }
-  MOE_CUDA(launch_slots(c, host_capacity(c), idx, g, ws_at<int32_t>(ws, L.hist),
-                        ws_at<int32_t>(ws, L.chunk_base), ws_at<int32_t>(ws, L.count), offset,
-                        ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
-                        s));
-  MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
-  const bool z_bf16 = forward_z_bf16(c);
-  r = ffn_impl(c, xbuf, offset, ws_at<int32_t>(ws, L.mtiles), row_gate, W1, b1, W2, b2, hbuf,
-               zbuf, z_bf16, st, s);
+  r = expert_path(c, L, ws, x, idx, g, ps, kp, W1, b1, W2, b2, y, st, s);
   if (r != MOE_OK) return r;
-  MOE_CUDA(launch_combine(c, x, zbuf, z_bf16, ps, kp, idx, offset, y, st, s));
   if (side) {
     // Join: work enqueued on `stream` after this call also waits for the losses.
     MOE_CUDA(cudaEventRecord(side->join, side->s));
     MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   }
   return MOE_OK;
+}
+
+int moe_hier_workspace_size(const moe_hier_config *cfg, size_t *bytes) {
+  const int r = check_hier(cfg);
+  if (r != MOE_OK) return r;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = hier_layout(*cfg).total;
+  return MOE_OK;
+}
+
+int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
+                     const float *Wp_noise, const float *noise_p, const float *Ws,
+                     const float *Ws_noise, const float *noise_s, const void *W1, const void *b1,
+                     const void *W2, const void *b2, void *y, float *aux_out2,
+                     int32_t *expert_idx, float *gate, int32_t *pos, uint8_t *keep, void *ws,
+                     moe_stream_t stream) {
+  int r = check_hier(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wp); MOE_OPT(Wp_noise); MOE_OPT(noise_p); MOE_REQ(Ws);
+  MOE_OPT(Ws_noise); MOE_OPT(noise_s); MOE_REQ(W1); MOE_OPT(b1); MOE_REQ(W2); MOE_OPT(b2);
+  MOE_REQ(y); MOE_OPT(aux_out2); MOE_OPT(expert_idx); MOE_OPT(gate); MOE_OPT(pos); MOE_OPT(keep);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  if ((Wp_noise == nullptr) != (noise_p == nullptr) ||
+      (Ws_noise == nullptr) != (noise_s == nullptr))
+    return MOE_ERR_ARG;
+  const moe_hier_config &h = *cfg;
+  const moe_config cs = hier_secondary(h), cp = hier_primary(h);
+  const HierLayout HL = hier_layout(h);
+  const WsLayout &L = HL.Ls, &Lp = HL.Lp;
+  cudaStream_t s = (cudaStream_t)stream;
+  void *wsp = ws_at<char>(ws, HL.off_p);
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  DeviceStatus *st_p = ws_at<DeviceStatus>(wsp, Lp.status);
+  float *scratch = ws_at<float>(ws, HL.scratch);
+  // 1. The primary gate: the flat gate over the a groups (picks, gates and,
+  //    for the losses, its balancing sums: Load_primary).
+  int32_t *idx_p = ws_at<int32_t>(wsp, Lp.idx);
+  float *g_p = ws_at<float>(wsp, Lp.gate);
+  r = gate_impl(cp, x, Wp, Wp_noise, noise_p, nullptr, idx_p, g_p, ws_at<float>(wsp, Lp.thr), wsp,
+                aux_out2 != nullptr, s);
+  if (r != MOE_OK) return r;
+  if (aux_out2)
+    MOE_CUDA(launch_aux_finalize(cp, ws_at<float>(wsp, Lp.partials), Lp.n_aux_blocks, scratch,
+                                 nullptr, nullptr, ws_at<float2>(wsp, Lp.aux_vec), st_p, s));
+  // 2. The secondary logits over all a*b experts (this clears the layer's
+  //    status word first).
+  float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
+  MOE_CUDA(launch_router(cs, x, Ws, Ws_noise, noise_s, nullptr, cc, sg, H,
+                         ws_at<char>(ws, L.bsplit), st, s));
+  // 3. The two-level selection and the hierarchical partial rows.
+  int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
+  float *g = gate ? gate : ws_at<float>(ws, L.gate);
+  int32_t *ps = pos ? pos : ws_at<int32_t>(ws, L.pos);
+  uint8_t *kp = keep ? keep : ws_at<uint8_t>(ws, L.keep);
+  float *parts = aux_out2 ? ws_at<float>(ws, HL.parts) : nullptr;
+  MOE_CUDA(launch_hier_select(h.T, h.a, h.b, h.k_primary, h.k_secondary, Ws_noise != nullptr,
+                              idx_p, g_p, cc, sg, H, idx, g, parts, st, s));
+  // 4. Importance_H and the in-group loads summed over the rows, then Load_H
+  //    and the two CV^2 (the tail also carries a primary-gate error over).
+  if (aux_out2)
+    MOE_CUDA(launch_aux_finalize(cs, parts, HL.rows, scratch + 4, nullptr, nullptr,
+                                 ws_at<float2>(ws, L.aux_vec), st, s));
+  MOE_CUDA(launch_hier_tail(h.T, h.a, h.b, ws_at<float2>(ws, L.aux_vec),
+                            ws_at<float2>(wsp, Lp.aux_vec), aux_out2, st, st_p, s));
+  // 5. Capacity, dispatch, the experts and the combine over the a*b experts.
+  return expert_path(cs, L, ws, x, idx, g, ps, kp, W1, b1, W2, b2, y, st, s);
 }
 
 int moe_last_device_status(void *ws, moe_stream_t stream, int64_t *detail) {

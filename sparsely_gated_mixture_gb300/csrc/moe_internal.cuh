@@ -133,6 +133,18 @@ cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c,
                               const float *H, int32_t *idx, float *gate, float *thr,
                               float *rowstat, float *partials, int n_blocks, cudaStream_t s);
 
+// Hierarchical gate (k_gate.cu): two-level selection with the balancing
+// partial rows (hier_rows(T, kp, b) rows of [4][a*b]), and the losses from the
+// finalizes' sums.
+cudaError_t launch_hier_select(int T, int a, int b, int kp, int ks, bool noisy,
+                               const int32_t *idx_p, const float *g_p, const float *cs,
+                               const float *ss, const float *Hs, int32_t *idx, float *gate,
+                               float *partials, DeviceStatus *st, cudaStream_t s);
+int hier_rows(int T, int kp, int b);
+cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const float2 *aux_p,
+                             float *out2, DeviceStatus *st, const DeviceStatus *st_p,
+                             cudaStream_t s);
+
 // k_router_tc.cu: the router as three bf16 tensor-core GEMMs (exact split of W).
 bool router_tc_supported(const moe_config &cfg);
 size_t router_tc_split_bytes(const moe_config &cfg);

@@ -166,3 +166,95 @@ def check_rel(got, ref, what, rtol=F32_RTOL):
     err = np.abs(got - ref)
     lim = rtol * np.maximum(np.abs(ref), 1e-30)
     assert np.all(err <= lim), f"{what}: got {got} ref {ref}"
+
+
+# ----------------------------------------------------------------------------- hierarchical layer
+
+
+def hier_to_device(w, inp: dict) -> dict:
+    dt = w.dtype
+    return dict(x=dev_act(inp["x"], dt), Wp=dev_f32(inp["Wp"]), Wpn=dev_f32(inp["Wpn"]),
+                noise_p=dev_f32(inp["noise_p"]), Ws=dev_f32(inp["Ws"]), Wsn=dev_f32(inp["Wsn"]),
+                noise_s=dev_f32(inp["noise_s"]), W1=dev_act(inp["W1"], dt),
+                b1=dev_act(inp["b1"], dt), W2=dev_act(inp["W2"], dt), b2=dev_act(inp["b2"], dt))
+
+
+def run_hier_forward(w, d, aux=True):
+    """moe_forward_hier through the C ABI. Returns host arrays (y on device)."""
+    cfg = B.hier_config_for(w)
+    T, k = w.T, w.k
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    y = torch.empty((T, w.d), dtype=act, device="cuda")
+    out2 = torch.zeros(2, dtype=torch.float32, device="cuda") if aux else None
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    pos = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    keep = torch.empty((T, k), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(B.moe_hier_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    B.moe_forward_hier(cfg, d["x"], d["Wp"], d["Wpn"], d["noise_p"], d["Ws"], d["Wsn"],
+                       d["noise_s"], d["W1"], d["b1"], d["W2"], d["b2"], y, out2, ws, idx, gate,
+                       pos, keep)
+    st, det = B.moe_last_device_status(ws)
+    return dict(status=st, detail=det, y=y, out2=None if out2 is None else out2.cpu().numpy(),
+                idx=idx.cpu().numpy(), gate=gate.cpu().numpy(), pos=pos.cpu().numpy(),
+                keep=keep.cpu().numpy())
+
+
+def _group_rows(Hs, groups, b):
+    """Hs[t, groups[t]*b .. groups[t]*b + b - 1] for every t: [T, b]."""
+    T = Hs.shape[0]
+    cols = groups[:, None].astype(np.int64) * b + np.arange(b)[None, :]
+    return Hs[np.arange(T)[:, None], cols]
+
+
+def reconcile_hier(ref, gpu_idx, a, b, kp, ks, tol=TIE_TOL):
+    """The GPU's flat choices against the oracle's, level by level: its
+    primary list (idx // b every ks choices) must match or be a near-tie in
+    the oracle's fp64 primary logits, and in each picked group its secondary
+    list must match the oracle's selection in that group or be a near-tie in
+    the oracle's secondary logits. Returns (choices to use downstream, tied
+    tokens, unexplained tokens)."""
+    T = gpu_idx.shape[0]
+    idx_p_gpu = (gpu_idx[:, ::ks] // b).astype(np.int32)
+    used_p, ties_p, bad_p = reconcile_selection(ref["Hp"], ref["idx_p"], idx_p_gpu, tol)
+    used = np.empty_like(gpu_idx)
+    ties, bad = set(ties_p), set(bad_p)
+    for q in range(kp):
+        groups = used_p[:, q]
+        sub = _group_rows(ref["Hs"], groups, b)
+        own, _, _, _ = oracle.select(sub, ks, oracle.TOPK_SOFTMAX)
+        loc = gpu_idx[:, q * ks:(q + 1) * ks] - groups[:, None] * b
+        u, t_s, b_s = reconcile_selection(sub, own, loc.astype(np.int32), tol)
+        used[:, q * ks:(q + 1) * ks] = u + groups[:, None] * b
+        ties |= set(t_s)
+        bad |= set(b_s)
+    return used.astype(np.int32), sorted(ties), sorted(bad)
+
+
+def hier_given(inp, ref, used, w, tokens):
+    """The oracle's gates, slots, output rows and hierarchical losses for the
+    flat choices ``used`` (its own where the GPU agreed)."""
+    a, b, kp, ks = w.a, w.b, w.kp, w.ks
+    T, E, k = w.T, w.E, w.k
+    idx_p = (used[:, ::ks] // b).astype(np.int32)
+    g_p = oracle.gates_given(ref["Hp"], idx_p, oracle.TOPK_SOFTMAX)
+    _, _, hkp, hk1p = oracle.select(ref["Hp"], kp, oracle.TOPK_SOFTMAX)
+    load_p = oracle.aux(ref["cp"], ref["sp"], ref["Hp"], idx_p, g_p, hkp, hk1p,
+                        inp["Wpn"] is not None)["load"]
+    gate = np.empty((T, k), np.float64)
+    hks = np.empty((T, kp), np.float64)
+    hk1s = np.empty((T, kp), np.float64)
+    for q in range(kp):
+        sub = _group_rows(ref["Hs"], idx_p[:, q], b)
+        loc = (used[:, q * ks:(q + 1) * ks] - idx_p[:, q:q + 1] * b).astype(np.int32)
+        gate[:, q * ks:(q + 1) * ks] = g_p[:, q:q + 1] * oracle.gates_given(
+            sub, loc, oracle.TOPK_SOFTMAX)
+        _, _, hks[:, q], hk1s[:, q] = oracle.select(sub, ks, oracle.TOPK_SOFTMAX)
+    hx = oracle.hier_aux(idx_p, ref["cs"], ref["ss"], used, gate, hks, hk1s, load_p, a, b, ks,
+                         inp["Wsn"] is not None)
+    C = oracle.capacity(T, E, k, w.cf, w.min_cap)
+    pos, keep, _ = oracle.slots(used, E, C)
+    y, bad = oracle.layer_out(inp["x"], used, gate, keep, inp["W1"], inp["W2"], inp["b1"],
+                              inp["b2"], tokens)
+    assert not bad
+    return dict(gate=gate, pos=pos, keep=keep, y=y, **hx)
