@@ -17,6 +17,9 @@ and marshals numpy arrays. Each wrapper names the page passage it follows:
 * "Mixture-of-Experts: Sparse Computation" (cs8803 lesson), Chapters 1, 2, 5.
 * The paper summary's "Hierarchical Mixture-of-Experts" section: the two-level
   gate, y_H, Importance_H and Load_H (``hier_*``).
+* Its "Strictly Balanced Gating (Batchwise Mask)" section (and the Lesson's
+  Ch. 2 mask form, Ch. 4): the batchwise and threshold masks, the
+  renormalised gate and L_batchwise (``bal_*``).
 
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 except the expert FFN's values on random weights, which the pages never print;
@@ -108,6 +111,12 @@ class Oracle:
         lib.orc_hier_select.restype = None
         lib.orc_hier_aux.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P]
         lib.orc_hier_aux.restype = None
+        lib.orc_softmax_rows.argtypes = [I, I, P, P]
+        lib.orc_softmax_rows.restype = None
+        lib.orc_bal_gate.argtypes = [I, I, I, I, P, P, P, P]
+        lib.orc_bal_gate.restype = None
+        lib.orc_bal_loss.argtypes = [I, I, P, P, P]
+        lib.orc_bal_loss.restype = D
         self.lib = lib
         self.path = lib_path
 
@@ -335,6 +344,66 @@ class Oracle:
                     group_count=hx.pop("count"), **hx)
 
 
+    # ------------------------------------------------------------ strictly balanced
+    def softmax_dense(self, H):
+        """G_sigma = Softmax(H) over all experts, row by row (OLNN's plain
+        softmax gate)."""
+        H = np.ascontiguousarray(H, dtype=np.float64)
+        T, E = H.shape
+        P = np.empty((T, E), np.float64)
+        self.lib.orc_softmax_rows(T, E, _ptr(H), _ptr(P))
+        return P
+
+    def bal_gate(self, P, m: int, thr=None, mode: int = 0):
+        """Batchwise (mode 0: top m tokens per expert) or threshold (mode 1:
+        P > thr) mask and the renormalised gate (OLNN, Strictly Balanced
+        Gating). Returns mask [T,E] uint8, gate [T,E]."""
+        P = np.ascontiguousarray(P, dtype=np.float64)
+        T, E = P.shape
+        thr = None if thr is None else np.ascontiguousarray(thr, dtype=np.float32)
+        if mode == 1 and thr is None:
+            raise ValueError("the threshold mask needs thresholds")
+        mask = np.empty((T, E), np.uint8)
+        gate = np.empty((T, E), np.float64)
+        self.lib.orc_bal_gate(T, E, int(m), int(mode), _ptr(P), _ptr(thr), _ptr(mask),
+                              _ptr(gate))
+        return mask, gate
+
+    def bal_loss(self, P, mask_batch, thr) -> float:
+        """L_batchwise (OLNN, Strictly Balanced Gating)."""
+        P = np.ascontiguousarray(P, dtype=np.float64)
+        T, E = P.shape
+        mask_batch = np.ascontiguousarray(mask_batch, dtype=np.uint8)
+        thr = np.ascontiguousarray(thr, dtype=np.float32)
+        return float(self.lib.orc_bal_loss(T, E, _ptr(P), _ptr(mask_batch), _ptr(thr)))
+
+    def bal_forward(self, inp: dict, tokens=None) -> dict:
+        """The strictly balanced layer: clean router logits H = x W_g (+ b),
+        P = Softmax(H), the batchwise mask with m = max(1, min(T, floor(k*T/E)))
+        (or the threshold mask when ``inp['mode_bal'] == 1``), the renormalised
+        gates, y = x + sum over picked experts of gate * E_i(x) (no capacity:
+        the mask fixes every expert's rows), and L_batchwise when thresholds
+        are given."""
+        x = inp["x"]
+        T = x.shape[0]
+        E = inp["Wg"].shape[1]
+        k = int(inp["k"])
+        mode = int(inp.get("mode_bal", 0))
+        m = max(1, min(T, (k * T) // E))
+        c, s, H, bad_h = self.router(x, inp["Wg"], None, None, inp.get("bias"))
+        P = self.softmax_dense(H)
+        thr = inp.get("thr")
+        mask, gate = self.bal_gate(P, m, thr, mode)
+        idx = np.tile(np.arange(E, dtype=np.int32), (T, 1))
+        y, bad_y = self.layer_out(x, idx, gate, mask, inp["W1"], inp["W2"], inp.get("b1"),
+                                  inp.get("b2"), tokens)
+        out = dict(H=H, P=P, m=m, mask=mask, gate=gate, y=y, nonfinite=bad_h or bad_y)
+        if thr is not None:
+            mb = mask if mode == 0 else self.bal_gate(P, m, None, 0)[0]
+            out["loss"] = self.bal_loss(P, mb, thr)
+        return out
+
+
 def default() -> Oracle:
     """The oracle compiled from moe_oracle.c (built on first use)."""
     global _default
@@ -406,3 +475,19 @@ def hier_aux(*a, **k):
 
 def hier_forward(*a, **k):
     return default().hier_forward(*a, **k)
+
+
+def softmax_dense(*a, **k):
+    return default().softmax_dense(*a, **k)
+
+
+def bal_gate(*a, **k):
+    return default().bal_gate(*a, **k)
+
+
+def bal_loss(*a, **k):
+    return default().bal_loss(*a, **k)
+
+
+def bal_forward(*a, **k):
+    return default().bal_forward(*a, **k)

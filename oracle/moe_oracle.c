@@ -453,6 +453,80 @@ void orc_hier_aux(int T, int a, int b, int kp, int ks, const int *idx_p, const d
   out2[1] = orc_cv2(load_H, E);
 }
 
+/* The plain softmax gate G_sigma = Softmax(H) over all E experts, row by row
+ * [OLNN Step 1 of the gate; LESSON Ch. 2]: exp(H - max) / sum exp(H - max). */
+void orc_softmax_rows(int T, int E, const double *H, double *P) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    const double *h = H + (size_t)t * E;
+    double mx = h[0];
+    for (int e = 1; e < E; ++e)
+      if (h[e] > mx) mx = h[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp(h[e] - mx);
+    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e] - mx) / z;
+  }
+}
+
+/*
+ * Strictly balanced gating [OLNN, "Strictly Balanced Gating (Batchwise
+ * Mask)"; LESSON Ch. 2 mask form and Ch. 4]: P = G_sigma(x) = Softmax(x W_g)
+ * over all E experts (dense), one row per token.
+ *  mask[t,i] (batchwise, mode 0): 1 iff token t is among the m tokens with the
+ *     largest P[.,i] (P descending, lower token index first on ties), so
+ *     every expert gets exactly m tokens.
+ *  mask[t,i] (threshold, mode 1): 1 iff P[t,i] > thr[i].
+ *  gate[t,i] = P[t,i] mask[t,i] / sum_j P[t,j] mask[t,j] (the mask form of
+ *     the gate, renormalised over the token's own picks); 0 for a token no
+ *     expert picked.
+ */
+void orc_bal_gate(int T, int E, int m, int mode, const double *P, const float *thr,
+                  unsigned char *mask, double *gate) {
+  memset(mask, 0, (size_t)T * E);
+  if (mode == 0) {
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < E; ++i) {
+      unsigned char *taken = (unsigned char *)calloc((size_t)T, 1);
+      for (int r = 0; r < m && r < T; ++r) {
+        int best = -1;
+        for (int t = 0; t < T; ++t) {
+          if (taken[t]) continue;
+          if (best < 0 || P[(size_t)t * E + i] > P[(size_t)best * E + i]) best = t;
+        }
+        taken[best] = 1;
+        mask[(size_t)best * E + i] = 1;
+      }
+      free(taken);
+    }
+  } else {
+    for (size_t u = 0; u < (size_t)T * E; ++u) mask[u] = P[u] > (double)thr[u % E] ? 1 : 0;
+  }
+  for (int t = 0; t < T; ++t) {
+    double z = 0.0;
+    for (int i = 0; i < E; ++i)
+      if (mask[(size_t)t * E + i]) z += P[(size_t)t * E + i];
+    for (int i = 0; i < E; ++i)
+      gate[(size_t)t * E + i] = mask[(size_t)t * E + i] ? P[(size_t)t * E + i] / z : 0.0;
+  }
+}
+
+/*
+ * L_batchwise(X, T, m) = sum_t sum_i (M_threshold(x_t, thr)_i - M_batchwise(X, m)_{t,i})
+ *                        * (X_{t,i} - thr_i)            [OLNN, Strictly Balanced Gating]
+ * with X = P (the dense softmax gate) and M_batchwise the mode-0 mask.
+ */
+double orc_bal_loss(int T, int E, const double *P, const unsigned char *mask_batch,
+                    const float *thr) {
+  double s = 0.0;
+  for (int t = 0; t < T; ++t)
+    for (int i = 0; i < E; ++i) {
+      const double x = P[(size_t)t * E + i], th = (double)thr[i];
+      const double mt = x > th ? 1.0 : 0.0;
+      s += (mt - (double)mask_batch[(size_t)t * E + i]) * (x - th);
+    }
+  return s;
+}
+
 /* Exposed for the pins: the scalar building blocks. */
 double orc_softplus_at(double z) { return orc_softplus(z); }
 double orc_phi_at(double u) { return orc_phi(u); }

@@ -599,4 +599,95 @@ def pin_hier_empty_group_guard(orc):
     np.testing.assert_allclose(r["load_H"][:2 * b], cnt[:2 * b], rtol=1e-13)
 
 
+# ----------------------------------------------------------------------------- strictly balanced
+
+
+def pin_softmax_rows(orc):
+    """The plain softmax gate against scipy's softmax, including logits large
+    enough to overflow exp without the max shift."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(71)
+    H = rng.standard_normal((6, 9)) * 3.0
+    H[2] += 900.0
+    np.testing.assert_allclose(orc.softmax_dense(H), softmax(H, axis=1), rtol=1e-13, atol=1e-300)
+
+
+def _bal_ref_mask(P, m):
+    T, E = P.shape
+    M = np.zeros((T, E), np.uint8)
+    for i in range(E):
+        for t in sorted(range(T), key=lambda u: (-P[u, i], u))[:m]:
+            M[t, i] = 1
+    return M
+
+
+def pin_bal_batchwise_bruteforce(orc):
+    """The batchwise mask: per expert the m tokens with the largest dense gate
+    (Python sort by (-P, token), ties included); every expert exactly m; gates
+    P * M renormalised per token, 0 for a token no expert took."""
+    rng = np.random.default_rng(73)
+    T, E, m = 11, 5, 4
+    P = rng.random((T, E))
+    P /= P.sum(axis=1, keepdims=True)
+    top = -np.sort(-P[:, 1])
+    P[3, 1] = P[7, 1] = P[9, 1] = top[2]  # a three-way tie across the m-th place
+    P[0, 2] = P[10, 2] = -np.sort(-P[:, 2])[m - 1]
+    mask, gate = orc.bal_gate(P, m)
+    ref = _bal_ref_mask(P, m)
+    assert np.array_equal(mask, ref)
+    assert np.all(mask.sum(axis=0) == m)
+    z = (P * ref).sum(axis=1, keepdims=True)
+    g_ref = np.where(ref == 1, P / np.where(z > 0, z, 1.0), 0.0)
+    np.testing.assert_allclose(gate, g_ref, rtol=1e-14, atol=0)
+    assert np.all(gate[ref.sum(axis=1) == 0] == 0.0)
+
+
+def pin_bal_threshold_mask_and_loss(orc):
+    """The threshold mask P > T_i and L_batchwise: with each T_i between the
+    m-th and (m+1)-th largest P of its column both masks agree and the loss
+    is exactly 0; lowering one threshold past one more token adds exactly
+    P - T_i for that token; P equal to its threshold is not taken."""
+    rng = np.random.default_rng(79)
+    T, E, m = 12, 4, 3
+    H = rng.standard_normal((T, E))
+    P = orc.softmax_dense(H)
+    mb, _ = orc.bal_gate(P, m)
+    srt = -np.sort(-P, axis=0)
+    thr = ((srt[m - 1] + srt[m]) / 2).astype(np.float32)
+    mt, _ = orc.bal_gate(P, m, thr, 1)
+    assert np.array_equal(mt, (P > thr.astype(np.float64)[None, :]).astype(np.uint8))
+    assert np.array_equal(mt, mb)
+    assert orc.bal_loss(P, mb, thr) == 0.0
+    thr2 = thr.copy()
+    thr2[1] = np.float32((srt[m, 1] + srt[m + 1, 1]) / 2)
+    extra = np.nonzero((P[:, 1] > thr2[1]) & (mb[:, 1] == 0))[0]
+    assert extra.size == 1
+    want = sum((float(P[t, i] > thr2[i]) - mb[t, i]) * (P[t, i] - float(thr2[i]))
+               for t in range(T) for i in range(E))
+    np.testing.assert_allclose(orc.bal_loss(P, mb, thr2), want, rtol=1e-13)
+    assert orc.bal_loss(P, mb, thr2) > 0.0
+    half = orc.softmax_dense(np.zeros((1, 2)))  # exactly 0.5 each
+    mh, _ = orc.bal_gate(half, 1, np.array([0.5, 0.25], np.float32), 1)
+    assert list(mh[0]) == [0, 1]
+
+
+def pin_bal_every_token_is_dense(orc):
+    """m = T (k = E): every expert takes every token, the gate is the dense
+    softmax itself, and the layer is the dense soft mixture x + sum_i
+    G_sigma(x)_i E_i(x) (numpy)."""
+    rng = np.random.default_rng(83)
+    T, d, E, d_ff = 7, 5, 3, 4
+    x, W1, b1, W2, b2 = _small_case(rng, T, d, E, d_ff, False)
+    Wg = (rng.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    r = orc.bal_forward(dict(x=x, Wg=Wg, W1=W1, b1=b1, W2=W2, b2=b2, k=E))
+    assert r["m"] == T and np.all(r["mask"] == 1)
+    X = _x64(x)
+    H = X @ Wg.astype(np.float64)
+    G = np.exp(H - H.max(axis=1, keepdims=True))
+    G /= G.sum(axis=1, keepdims=True)
+    np.testing.assert_allclose(r["gate"], G, rtol=1e-13)
+    ref = X + np.einsum("te,etd->td", G, _ffn_all(X, W1, b1, W2, b2))
+    np.testing.assert_allclose(r["y"], ref, rtol=1e-11, atol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

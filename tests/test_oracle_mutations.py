@@ -51,6 +51,16 @@ MUTATIONS = {
                                   "count[i] > 0 ? loadsec[e] / (double)count[i] : 0.0"),
     "hier_threshold_swapped": ("chosen ? hk1s[(size_t)t * kp + q] : hks[(size_t)t * kp + q]",
                                "chosen ? hks[(size_t)t * kp + q] : hk1s[(size_t)t * kp + q]"),
+    "bal_tie_higher_token_wins": ("if (best < 0 || P[(size_t)t * E + i] > P[(size_t)best * E + i]) best = t;",
+                                  "if (best < 0 || P[(size_t)t * E + i] >= P[(size_t)best * E + i]) best = t;"),
+    "bal_gate_not_renormalised": ("mask[(size_t)t * E + i] ? P[(size_t)t * E + i] / z : 0.0;",
+                                  "mask[(size_t)t * E + i] ? P[(size_t)t * E + i] : 0.0;"),
+    "bal_threshold_inclusive": ("mask[u] = P[u] > (double)thr[u % E] ? 1 : 0;",
+                                "mask[u] = P[u] >= (double)thr[u % E] ? 1 : 0;"),
+    "bal_loss_sign": ("s += (mt - (double)mask_batch[(size_t)t * E + i]) * (x - th);",
+                      "s += ((double)mask_batch[(size_t)t * E + i] - mt) * (x - th);"),
+    "softmax_no_max_shift": ("for (int e = 0; e < E; ++e) z += exp(h[e] - mx);\n    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e] - mx) / z;",
+                             "for (int e = 0; e < E; ++e) z += exp(h[e]);\n    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e]) / z;"),
     "hier_secondary_load_dropped": ("      count[i] += 1;\n      for (int j = 0; j < b; ++j) {",
                                        "      count[i] += 1;\n      for (int j = 0; j < b && 0; ++j) {"),
 }
