@@ -700,6 +700,207 @@ def run_hier(args, w: wl.HierWorkload):
     return line
 
 
+def run_balanced(args, w: wl.Workload):
+    """Strictly balanced gating: the value is moe_forward_balanced over
+    resident inputs (median of the timed steps, L2 flushed before each); the
+    expert GEMMs are also timed through moe_expert_ffn on the same row layout
+    (m rows for every expert), interleaved."""
+    import torch
+    import torch.distributed as dist
+
+    from sparsely_gated_mixture_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    inp = wl.generate(w, seed=0)
+    act = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(a, is_act=False):
+        if a is None:
+            return None
+        if is_act and w.dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    x = to_dev(inp["x"], True)
+    Wg = to_dev(inp["Wg"])
+    W1, W2 = to_dev(inp["W1"], True), to_dev(inp["W2"], True)
+    cfg = B.config_for(w)
+    T, E, d, dff = w.T, w.E, w.d, w.d_ff
+    m = max(1, min(T, (w.k * T) // E))
+    R = E * m
+    z = dict(device=dev)
+    ws = torch.empty(B.moe_balanced_workspace_size(cfg), dtype=torch.uint8, **z)
+    ws_f = torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, **z)
+    y = torch.empty((T, d), dtype=act, **z)
+    offset = torch.arange(0, (E + 1) * m, m, dtype=torch.int32, **z)
+    xbuf = torch.randn((R, d), **z).to(act)
+    row_gate = torch.ones(R, dtype=torch.float32, **z)
+    hbuf = torch.empty((R, dff), dtype=act, **z)
+    zbuf = torch.empty((R, d), dtype=torch.float32, **z)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, **z)
+
+    def fwd(xx=x, yy=y):
+        B.moe_forward_balanced(cfg, xx, Wg, None, None, W1, None, W2, None, yy, None, None, ws,
+                               stream)
+
+    def ffn():
+        B.moe_expert_ffn(cfg, xbuf, offset, row_gate, W1, None, W2, None, hbuf, zbuf, ws_f,
+                         stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        ffn()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) during warm-up")
+    fe = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()
+        fe[i][0].record(stream)
+        fwd()
+        fe[i][1].record(stream)
+        flush.zero_()
+        fe[i][2].record(stream)
+        ffn()
+        fe[i][3].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the timed region")
+    ms = slowest_rank_ms(statistics.median(e[0].elapsed_time(e[1]) for e in fe), world, dev)
+    ffn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in fe)
+
+    # End to end: x in from pinned host memory and y back, every step.
+    x_h = x.cpu().pin_memory()
+    x_d = [torch.empty_like(x) for _ in range(2)]
+    y_d = [torch.empty_like(y) for _ in range(2)]
+    y_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for _ in range(2)]
+    up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    fwd_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def h2d(i):
+        b = i % 2
+        with torch.cuda.stream(up_s):
+            if i >= 2:
+                up_s.wait_event(fwd_done[b])
+            x_d[b].copy_(x_h, non_blocking=True)
+            h2d_done[b].record(up_s)
+
+    def step_e2e(i):
+        b = i % 2
+        stream.wait_event(h2d_done[b])
+        if i >= 2:
+            stream.wait_event(d2h_done[b])
+        fwd(x_d[b], y_d[b])
+        fwd_done[b].record(stream)
+        with torch.cuda.stream(down_s):
+            down_s.wait_event(fwd_done[b])
+            y_h[b].copy_(y_d[b], non_blocking=True)
+            d2h_done[b].record(down_s)
+
+    def run_e2e(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d(i + 1)
+            step_e2e(i)
+
+    run_e2e(max(3, args.warmup))
+    torch.cuda.synchronize()
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
+    up_s.wait_stream(stream)
+    run_e2e(args.steps)
+    stream.wait_stream(up_s)
+    stream.wait_stream(down_s)
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(a_ev.elapsed_time(b_ev) / args.steps, world, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    peaks, peak_kind = load_peaks()
+    sb = 2 if w.dtype == "bf16" else 4
+    ffn_flops = 4 * d * dff * R
+    ffn_bytes = 2 * E * d * dff * sb + R * d * sb + 2 * R * dff * sb + R * d * 4
+    ffn_s = ffn_ms * 1e-3
+    roof = {"kernel": "moe_expert_ffn (two grouped GEMM launches), m rows per expert"}
+    if ffn_bytes / (peaks["hbm_gbs"] * 1e9) > ffn_flops / (peaks["bf16_tflops"] * 1e12):
+        gbs = ffn_bytes / ffn_s / 1e9
+        roof.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"]})
+    else:
+        tf = ffn_flops / ffn_s / 1e12
+        roof.update({"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"]})
+    roof.update({"peak_source": peak_kind, "algorithmic_flops_per_launch": ffn_flops,
+                 "algorithmic_bytes": ffn_bytes, "traffic": None})
+    tc = w.dtype == "bf16" and w.d % 8 == 0
+    # router (split + tensor-core kernel), mask memset, softmax, select,
+    # token gates, gather, two GEMMs, combine
+    launches = (2 if tc else 1) + 3 + 1 + 2 + 1
+    line = {
+        "metric": "strictly balanced MoE layer fwd tokens/s @1 GB300",
+        "value": job_tokens_per_s(world, T, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "T": T, "d": d, "E": E, "d_ff": dff, "k": w.k,
+                   "rows_per_expert": m, "gate": "batchwise mask", "seed": 0,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": roof,
+        "stages": {"expert_ffn": {"ms": ffn_ms}},
+        "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "gpu_launches": (launches + 2) * args.steps,  # forward + the timed GEMMs
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bal(w, inp, args.cpu_sample)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int) -> dict:
+    """The oracle's balanced layer on the host cores: router, softmax and the
+    batchwise mask over every token, the expert loop for n_sample tokens,
+    extrapolated."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    n = min(n_sample, w.T)
+    tokens = np.linspace(0, w.T - 1, n).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.bal_forward(inp, tokens=tokens[:0])
+    t_gate = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.bal_forward(inp, tokens=tokens)
+    t_ffn = max(time.perf_counter() - t0 - t_gate, 1e-9)
+    full = t_gate + t_ffn * (w.T / n)
+    return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"router, softmax and batchwise mask over all {w.T} tokens "
+                      f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens, "
+                      f"extrapolated to {w.T} tokens"}
+
+
 def cpu_baseline_hier(w: wl.HierWorkload, inp: dict, n_sample: int) -> dict:
     """The oracle's hierarchical layer on the host cores: both gates, the
     two-level selection, slots and losses over every token, the expert loop
@@ -810,7 +1011,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="top2_large_experts",
-                    choices=sorted(wl.WORKLOADS) + sorted(wl.HIER_WORKLOADS))
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.HIER_WORKLOADS)
+                    + sorted(wl.BAL_WORKLOADS))
     ap.add_argument("--cpu-sample", type=int, default=16,
                     help="tokens whose expert loop the oracle runs for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -825,6 +1027,31 @@ def main():
         if args.tokens:
             w = w.with_(T=args.tokens)
         line = (run_reference_hier(args, w) if args.impl == "reference" else run_hier(args, w))
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if args.workload in wl.BAL_WORKLOADS:
+        w = wl.BAL_WORKLOADS[args.workload]
+        if args.tokens:
+            w = w.with_(T=args.tokens)
+        if args.impl == "reference":
+            rank, world, _ = dist_env()
+            if rank == 0:
+                inp = wl.generate(w, seed=0)
+                vals = [cpu_baseline_bal(w, inp, args.cpu_sample) for _ in range(args.steps)]
+                v = statistics.mean(x["value"] for x in vals)
+                print(json.dumps({
+                    "impl": "reference", "metric": "strictly balanced MoE layer fwd tokens/s "
+                    "@1 GB300", "value": v, "unit": "tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.T / v * 1e3,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": w.name, "T": w.T, "parallelism": "host cores"},
+                    "cpu_baseline": dict(vals[-1], value=v),
+                    "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        line = run_balanced(args, w)
         if line is not None:
             print(json.dumps(line), flush=True)
         return

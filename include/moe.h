@@ -256,6 +256,28 @@ int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
                      moe_stream_t stream);
 
 /*
+ * Strictly balanced gating ("Outrageously Large Neural Networks", Strictly
+ * Balanced Gating (Batchwise Mask); the mask form of the gate). P =
+ * Softmax(x Wg + logit_bias) over all E experts (dense, fp32, no noise); each
+ * expert takes the m = max(1, min(T, floor(k*T/E))) tokens with the largest P
+ * for it (lower token index first on ties), so every expert processes exactly
+ * m rows and there is no capacity; a token's gate on a picked expert is P
+ * renormalised over its own picks; y = x + sum over the picks of gate *
+ * E_i(x) (a token no expert took keeps only the residual). Uses T, d, E, d_ff,
+ * k and act_dtype of cfg (capacity_factor, min_capacity and gate_mode are not
+ * used). thresholds [E] fp32 or NULL: the per-expert T_i of the threshold mask
+ * P > T_i; loss_out [1] fp32 or NULL (needs thresholds) = L_batchwise = sum_t
+ * sum_i (1[P > T_i] - M_batchwise[t,i]) * (P[t,i] - T_i). mask_out [T][ceil(E/32)]
+ * uint32 or NULL: bit (i % 32) of word i / 32 of token t's row is
+ * M_batchwise[t,i]. The status word at the start of `ws` is cleared first.
+ */
+int moe_balanced_workspace_size(const moe_config *cfg, size_t *bytes);
+int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
+                         const float *logit_bias, const float *thresholds, const void *W1,
+                         const void *b1, const void *W2, const void *b2, void *y,
+                         float *loss_out, uint32_t *mask_out, void *ws, moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the first device-side error recorded in `ws`
  * since it was last cleared (MOE_OK if none), writes its detail word (e.g. the
  * offending flat index) to *detail if non-NULL, and clears it.

@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
            "moe_last_device_status", "moe_dispatch_noalloc", "moe_hier_workspace_size",
-           "moe_forward_hier")
+           "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced")
 
 
 class MoEError(RuntimeError):
@@ -96,6 +96,8 @@ def lib():
             HP = ctypes.POINTER(moe_hier_config)
             L.moe_hier_workspace_size.argtypes = [HP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_hier.argtypes = [HP] + [P] * 19
+            L.moe_balanced_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
+            L.moe_forward_balanced.argtypes = [CP] + [P] * 13
             for name in EXPORTS[1:]:
                 getattr(L, name).restype = I
             _lib = L
@@ -192,6 +194,21 @@ def moe_forward_hier(cfg, x, Wp, Wp_noise, noise_p, Ws, Ws_noise, noise_s, W1, b
                                   _p(Ws), _p(Ws_noise), _p(noise_s), _p(W1), _p(b1), _p(W2),
                                   _p(b2), _p(y), _p(aux_out2), _p(expert_idx), _p(gate), _p(pos),
                                   _p(keep), _p(ws), _stream(stream)), "moe_forward_hier")
+
+
+def moe_balanced_workspace_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_balanced_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_balanced_workspace_size")
+    return n.value
+
+
+def moe_forward_balanced(cfg, x, Wg, logit_bias, thresholds, W1, b1, W2, b2, y, loss_out,
+                         mask_out, ws, stream=None):
+    _check(lib().moe_forward_balanced(ctypes.byref(cfg), _p(x), _p(Wg), _p(logit_bias),
+                                      _p(thresholds), _p(W1), _p(b1), _p(W2), _p(b2), _p(y),
+                                      _p(loss_out), _p(mask_out), _p(ws), _stream(stream)),
+           "moe_forward_balanced")
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

@@ -231,6 +231,46 @@ static int check_hier(const moe_hier_config *h) {
   return r != MOE_OK ? r : check_cfg(&cp);
 }
 
+// ----------------------------------------------------------------------------- balanced gating
+struct BalLayout {
+  size_t status, c, sigma, H, bsplit, PT, mask, row_token, row_p, row_gate, offset, trows, npick,
+      xbuf, hbuf, zbuf, loss, total;
+  int m;
+};
+
+static BalLayout bal_layout(const moe_config &cfg) {
+  BalLayout L{};
+  const size_t T = cfg.T, E = cfg.E, d = cfg.d, dff = cfg.d_ff;
+  const size_t eb = elem_bytes(cfg.act_dtype);
+  L.m = balanced_m(cfg);
+  const size_t R = E * (size_t)L.m, W = (E + 31) / 32;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.status = take(sizeof(DeviceStatus));
+  L.c = take(T * E * 4);
+  L.sigma = take(T * E * 4);
+  L.H = take(T * E * 4);
+  L.bsplit = take(router_tc_split_bytes(cfg));
+  L.PT = take(E * T * 4);
+  L.mask = take(T * W * 4);
+  L.row_token = take(R * 4);
+  L.row_p = take(R * 4);
+  L.row_gate = take(R * 4);
+  L.offset = take((E + 1) * 4);
+  L.trows = take(T * kBalKeepRows * 4);
+  L.npick = take(T * 4);
+  L.xbuf = take(R * d * eb);
+  L.hbuf = take(R * dff * eb);
+  L.zbuf = take(R * d * 4);
+  L.loss = take(E * 8);
+  L.total = off;
+  return L;
+}
+
 // One side stream (non-blocking) and a fork / join event pair per device,
 // made on first use and kept; the lock is held while a call enqueues on them,
 // so calls from several host threads do not interleave their records.
@@ -487,6 +527,59 @@ int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
                             ws_at<float2>(wsp, Lp.aux_vec), aux_out2, st, st_p, s));
   // 5. Capacity, dispatch, the experts and the combine over the a*b experts.
   return expert_path(cs, L, ws, x, idx, g, ps, kp, W1, b1, W2, b2, y, st, s);
+}
+
+int moe_balanced_workspace_size(const moe_config *cfg, size_t *bytes) {
+  const int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = bal_layout(*cfg).total;
+  return MOE_OK;
+}
+
+int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
+                         const float *logit_bias, const float *thresholds, const void *W1,
+                         const void *b1, const void *W2, const void *b2, void *y,
+                         float *loss_out, uint32_t *mask_out, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(logit_bias); MOE_OPT(thresholds); MOE_REQ(W1); MOE_OPT(b1);
+  MOE_REQ(W2); MOE_OPT(b2); MOE_REQ(y); MOE_OPT(loss_out); MOE_OPT(mask_out);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  if (loss_out && !thresholds) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  const BalLayout L = bal_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  float *H = ws_at<float>(ws, L.H);
+  // 1. Clean router logits (this clears the status word first).
+  MOE_CUDA(launch_router(c, x, Wg, nullptr, nullptr, logit_bias, ws_at<float>(ws, L.c),
+                         ws_at<float>(ws, L.sigma), H, ws_at<char>(ws, L.bsplit), st, s));
+  // 2. Dense softmax, the batchwise mask (m rows per expert, token order),
+  //    the renormalised gates and the L_batchwise terms.
+  uint32_t *mask = mask_out ? mask_out : ws_at<uint32_t>(ws, L.mask);
+  int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
+  float *row_gate = ws_at<float>(ws, L.row_gate);
+  int32_t *offset = ws_at<int32_t>(ws, L.offset);
+  double *loss = ws_at<double>(ws, L.loss);
+  int32_t *trows = ws_at<int32_t>(ws, L.trows), *npick = ws_at<int32_t>(ws, L.npick);
+  MOE_CUDA(launch_bal_gate(c, L.m, H, loss_out ? thresholds : nullptr, ws_at<float>(ws, L.PT),
+                           row_token, ws_at<float>(ws, L.row_p), row_gate, offset, mask, trows,
+                           npick, loss, st, s));
+  // 3. The expert rows through the flat gather and expert GEMMs (fp32 Z).
+  void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
+  float *zbuf = ws_at<float>(ws, L.zbuf);
+  MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
+  if (c.act_dtype == MOE_BF16 && ffn_tc_supported(c)) {
+    MOE_CUDA(launch_ffn_tc(c, L.m, xbuf, offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf,
+                           false, st, s));
+  } else {
+    MOE_CUDA(launch_ffn_simt(c, L.m, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+  }
+  // 4. y = x + the picks' outputs, and the loss.
+  MOE_CUDA(launch_bal_combine(c, L.m, x, zbuf, mask, row_token, trows, npick, y, st, s));
+  if (loss_out) MOE_CUDA(launch_bal_loss(c.E, loss, loss_out, s));
+  return MOE_OK;
 }
 
 int moe_last_device_status(void *ws, moe_stream_t stream, int64_t *detail) {

@@ -145,6 +145,19 @@ cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const flo
                              float *out2, DeviceStatus *st, const DeviceStatus *st_p,
                              cudaStream_t s);
 
+// k_balanced.cu: strictly balanced gating (batchwise mask). m rows per expert.
+int balanced_m(const moe_config &c);
+constexpr int kBalKeepRows = 8;  // rows kept per token for the combine
+cudaError_t launch_bal_gate(const moe_config &c, int m, const float *H, const float *thr,
+                            float *PT, int32_t *row_token, float *row_p, float *row_gate,
+                            int32_t *offset, uint32_t *mask, int32_t *trows, int32_t *npick,
+                            double *loss_part, DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_bal_combine(const moe_config &c, int m, const void *x, const float *zbuf,
+                               const uint32_t *mask, const int32_t *row_token,
+                               const int32_t *trows, const int32_t *npick, void *y,
+                               DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_bal_loss(int E, const double *loss_part, float *out, cudaStream_t s);
+
 // k_router_tc.cu: the router as three bf16 tensor-core GEMMs (exact split of W).
 bool router_tc_supported(const moe_config &cfg);
 size_t router_tc_split_bytes(const moe_config &cfg);

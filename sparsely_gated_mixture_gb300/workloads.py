@@ -140,6 +140,16 @@ HIER_WORKLOADS = {
     ]
 }
 
+# Strictly balanced gating (batchwise mask): clean router, m = k*T/E rows per
+# expert; the large-expert layer's widths at 64 experts.
+BAL_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("balanced_top2_e64", T=16384, d=1024, E=64, d_ff=4096, k=2, cf=1.0, mode=TOPK,
+                 dtype="bf16", noisy=False),
+    ]
+}
+
 _CHUNK = 1 << 24
 
 
