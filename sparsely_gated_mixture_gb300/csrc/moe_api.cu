@@ -552,6 +552,15 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
   cudaStream_t s = (cudaStream_t)stream;
   DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
   float *H = ws_at<float>(ws, L.H);
+  // The E*m expert rows exceed T*k when k*T < E (m is at least 1): the row
+  // kernels and GEMMs bound their packed buffers by T*k rows and find a row's
+  // token as (its key) / k, so they get a k that covers every row; rows key
+  // their token t as t*kr.
+  moe_config cr = c;
+  {
+    const long long need = ((long long)c.E * L.m + c.T - 1) / c.T;
+    if (need > cr.k) cr.k = (int)need;
+  }
   // 1. Clean router logits (this clears the status word first).
   MOE_CUDA(launch_router(c, x, Wg, nullptr, nullptr, logit_bias, ws_at<float>(ws, L.c),
                          ws_at<float>(ws, L.sigma), H, ws_at<char>(ws, L.bsplit), st, s));
@@ -563,21 +572,21 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
   int32_t *offset = ws_at<int32_t>(ws, L.offset);
   double *loss = ws_at<double>(ws, L.loss);
   int32_t *trows = ws_at<int32_t>(ws, L.trows), *npick = ws_at<int32_t>(ws, L.npick);
-  MOE_CUDA(launch_bal_gate(c, L.m, H, loss_out ? thresholds : nullptr, ws_at<float>(ws, L.PT),
+  MOE_CUDA(launch_bal_gate(cr, L.m, H, loss_out ? thresholds : nullptr, ws_at<float>(ws, L.PT),
                            row_token, ws_at<float>(ws, L.row_p), row_gate, offset, mask, trows,
                            npick, loss, st, s));
   // 3. The expert rows through the flat gather and expert GEMMs (fp32 Z).
   void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
   float *zbuf = ws_at<float>(ws, L.zbuf);
-  MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
+  MOE_CUDA(launch_gather(cr, x, offset, row_token, xbuf, st, s));
   if (c.act_dtype == MOE_BF16 && ffn_tc_supported(c)) {
-    MOE_CUDA(launch_ffn_tc(c, L.m, xbuf, offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf,
+    MOE_CUDA(launch_ffn_tc(cr, L.m, xbuf, offset, nullptr, row_gate, W1, b1, W2, b2, hbuf, zbuf,
                            false, st, s));
   } else {
-    MOE_CUDA(launch_ffn_simt(c, L.m, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
+    MOE_CUDA(launch_ffn_simt(cr, L.m, xbuf, offset, row_gate, W1, b1, W2, b2, hbuf, zbuf, st, s));
   }
   // 4. y = x + the picks' outputs, and the loss.
-  MOE_CUDA(launch_bal_combine(c, L.m, x, zbuf, mask, row_token, trows, npick, y, st, s));
+  MOE_CUDA(launch_bal_combine(cr, L.m, x, zbuf, mask, row_token, trows, npick, y, st, s));
   if (loss_out) MOE_CUDA(launch_bal_loss(c.E, loss, loss_out, s));
   return MOE_OK;
 }

@@ -102,6 +102,12 @@ SMALL = {
     "bal_k_equals_E": _w("bal_k_equals_E", 130, 64, 4, 64, 4),
     "bal_ragged_f32": _w("bal_ragged_f32", 129, 36, 7, 50, 2, dtype="f32"),
     "bal_e40_d72": _w("bal_e40_d72", 300, 72, 40, 64, 3),
+    # edge cases: one token (m = 1), m = 1 with many tokens, a ragged tail
+    # of the 1024-token select chunks, more than 32 experts per mask word set
+    "bal_single_token": _w("bal_single_token", 1, 64, 4, 64, 2),
+    "bal_m1": _w("bal_m1", 100, 64, 64, 64, 1),
+    "bal_ragged_chunks": _w("bal_ragged_chunks", 2049, 64, 8, 64, 2),
+    "bal_e100_k8": _w("bal_e100_k8", 400, 64, 100, 64, 8),
 }
 
 

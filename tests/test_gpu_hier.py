@@ -56,6 +56,19 @@ SMALL = {
 }
 
 
+EDGE = {
+    # one token; the largest k (k_p * k_s = 16); noise on the primary gate
+    # only is covered by hier_clean_8x8's counterpart below
+    "hier_single_token": HW("hier_single_token", T=1, d=64, a=4, b=8, kp=2, ks=2, d_ff=64,
+                            cf=1.0, dtype="bf16", noisy=True),
+    "hier_k16": HW("hier_k16", T=200, d=64, a=8, b=16, kp=4, ks=4, d_ff=64, cf=1.0,
+                   dtype="bf16", noisy=True),
+    "hier_kp_equals_a": HW("hier_kp_equals_a", T=150, d=64, a=3, b=8, kp=3, ks=2, d_ff=64,
+                           cf=1.0, dtype="bf16", noisy=True),
+}
+SMALL.update(EDGE)
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_hier_small_parity(name):
     w = SMALL[name]
