@@ -10,7 +10,7 @@
 //                  (three digit passes over the fp32 bit patterns, which
 //                  order like the values for P >= 0), then one pass in token
 //                  order that takes every larger value and the first ties,
-//                  writes the expert's rows (token, P) in token order, sets
+//                  writes the expert's rows (their tokens) in token order, sets
 //                  the token's bit in the mask, adds the expert's
 //                  L_batchwise terms, and writes the row offsets e*m;
 //   k_bal_tokens   a warp per token: the sum of P over its picks (expert
@@ -119,7 +119,7 @@ __device__ int block_scan_excl(int v, int *sh, int *total) {
 __global__ void __launch_bounds__(kSelThreads)
 k_bal_select(int T, int E, int k, int m, const float *__restrict__ PT,
              const float *__restrict__ thr, int32_t *__restrict__ row_token,
-             float *__restrict__ row_p, int32_t *__restrict__ offset, uint32_t *__restrict__ mask,
+             int32_t *__restrict__ offset, uint32_t *__restrict__ mask,
              double *__restrict__ loss_part, DeviceStatus *st) {
   pdl_wait();
   pdl_trigger();
@@ -179,7 +179,6 @@ k_bal_select(int T, int E, int k, int m, const float *__restrict__ PT,
       if (pos < m) {
         const size_t row = (size_t)e * m + pos;
         row_token[row] = t * k;
-        row_p[row] = __uint_as_float(u);
         atomicOr(&mask[(size_t)t * W + (e >> 5)], 1u << (e & 31));
       } else {
         record_error(st, MOE_ERR_BOUNDS, (long long)e);
@@ -355,15 +354,15 @@ int balanced_m(const moe_config &c) {
 }
 
 cudaError_t launch_bal_gate(const moe_config &c, int m, const float *H, const float *thr,
-                            float *PT, int32_t *row_token, float *row_p, float *row_gate,
-                            int32_t *offset, uint32_t *mask, int32_t *trows, int32_t *npick,
-                            double *loss_part, DeviceStatus *st, cudaStream_t s) {
+                            float *PT, int32_t *row_token, float *row_gate, int32_t *offset,
+                            uint32_t *mask, int32_t *trows, int32_t *npick, double *loss_part,
+                            DeviceStatus *st, cudaStream_t s) {
   const int W = (c.E + 31) / 32;
   cudaError_t err = cudaMemsetAsync(mask, 0, (size_t)c.T * W * 4, s);
   if (err != cudaSuccess) return err;
   launch_pdl(k_bal_softmax, (c.T + kBalTok - 1) / kBalTok, 256, 0, s, c.T, c.E, H, PT);
   launch_pdl(k_bal_select, c.E, kSelThreads, 0, s, c.T, c.E, c.k, m, (const float *)PT, thr,
-      row_token, row_p, offset, mask, loss_part, st);
+      row_token, offset, mask, loss_part, st);
   launch_pdl(k_bal_tokens, (c.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s, c.T, c.E,
       c.k, m, (const float *)PT, (const uint32_t *)mask, (const int32_t *)row_token, row_gate,
       trows, npick, st);

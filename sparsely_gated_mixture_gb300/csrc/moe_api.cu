@@ -233,8 +233,8 @@ static int check_hier(const moe_hier_config *h) {
 
 // ----------------------------------------------------------------------------- balanced gating
 struct BalLayout {
-  size_t status, c, sigma, H, bsplit, PT, mask, row_token, row_p, row_gate, offset, trows, npick,
-      xbuf, hbuf, zbuf, loss, total;
+  size_t status, c, sigma, H, bsplit, PT, mask, row_token, row_gate, offset, trows, npick, xbuf,
+      hbuf, zbuf, loss, total;
   int m;
 };
 
@@ -258,7 +258,6 @@ static BalLayout bal_layout(const moe_config &cfg) {
   L.PT = take(E * T * 4);
   L.mask = take(T * W * 4);
   L.row_token = take(R * 4);
-  L.row_p = take(R * 4);
   L.row_gate = take(R * 4);
   L.offset = take((E + 1) * 4);
   L.trows = take(T * kBalKeepRows * 4);
@@ -573,8 +572,7 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
   double *loss = ws_at<double>(ws, L.loss);
   int32_t *trows = ws_at<int32_t>(ws, L.trows), *npick = ws_at<int32_t>(ws, L.npick);
   MOE_CUDA(launch_bal_gate(cr, L.m, H, loss_out ? thresholds : nullptr, ws_at<float>(ws, L.PT),
-                           row_token, ws_at<float>(ws, L.row_p), row_gate, offset, mask, trows,
-                           npick, loss, st, s));
+                           row_token, row_gate, offset, mask, trows, npick, loss, st, s));
   // 3. The expert rows through the flat gather and expert GEMMs (fp32 Z).
   void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
   float *zbuf = ws_at<float>(ws, L.zbuf);

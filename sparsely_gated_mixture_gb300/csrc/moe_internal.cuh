@@ -149,9 +149,9 @@ cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const flo
 int balanced_m(const moe_config &c);
 constexpr int kBalKeepRows = 8;  // rows kept per token for the combine
 cudaError_t launch_bal_gate(const moe_config &c, int m, const float *H, const float *thr,
-                            float *PT, int32_t *row_token, float *row_p, float *row_gate,
-                            int32_t *offset, uint32_t *mask, int32_t *trows, int32_t *npick,
-                            double *loss_part, DeviceStatus *st, cudaStream_t s);
+                            float *PT, int32_t *row_token, float *row_gate, int32_t *offset,
+                            uint32_t *mask, int32_t *trows, int32_t *npick, double *loss_part,
+                            DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_bal_combine(const moe_config &c, int m, const void *x, const float *zbuf,
                                const uint32_t *mask, const int32_t *row_token,
                                const int32_t *trows, const int32_t *npick, void *y,
