@@ -111,6 +111,8 @@ class Oracle:
         lib.orc_hier_select.restype = None
         lib.orc_hier_aux.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P]
         lib.orc_hier_aux.restype = None
+        lib.orc_bal_rows.argtypes = [ctypes.c_longlong, I, I]
+        lib.orc_bal_rows.restype = I
         lib.orc_softmax_rows.argtypes = [I, I, P, P]
         lib.orc_softmax_rows.restype = None
         lib.orc_bal_gate.argtypes = [I, I, I, I, P, P, P, P]
@@ -354,6 +356,11 @@ class Oracle:
         self.lib.orc_softmax_rows(T, E, _ptr(H), _ptr(P))
         return P
 
+    def bal_rows(self, T: int, k: int, E: int) -> int:
+        """m = max(1, min(T, floor(k T / E))), the batchwise mask's rows per
+        expert (OLNN, Strictly Balanced Gating: m = k|X|/n)."""
+        return int(self.lib.orc_bal_rows(int(T), int(k), int(E)))
+
     def bal_gate(self, P, m: int, thr=None, mode: int = 0):
         """Batchwise (mode 0: top m tokens per expert) or threshold (mode 1:
         P > thr) mask and the renormalised gate (OLNN, Strictly Balanced
@@ -389,7 +396,7 @@ class Oracle:
         E = inp["Wg"].shape[1]
         k = int(inp["k"])
         mode = int(inp.get("mode_bal", 0))
-        m = max(1, min(T, (k * T) // E))
+        m = self.bal_rows(T, k, E)
         c, s, H, bad_h = self.router(x, inp["Wg"], None, None, inp.get("bias"))
         P = self.softmax_dense(H)
         thr = inp.get("thr")
@@ -491,3 +498,7 @@ def bal_loss(*a, **k):
 
 def bal_forward(*a, **k):
     return default().bal_forward(*a, **k)
+
+
+def bal_rows(*a, **k):
+    return default().bal_rows(*a, **k)

@@ -468,6 +468,16 @@ void orc_softmax_rows(int T, int E, const double *H, double *P) {
   }
 }
 
+/* Rows per expert of the batchwise mask, m = k |X| / n [OLNN, Strictly
+ * Balanced Gating; LESSON Ch. 4]: the expected k T / E taken as a whole
+ * number of tokens, floor(k T / E), at least 1 and at most T. */
+int orc_bal_rows(long long T, int k, int E) {
+  long long m = (long long)k * T / E;
+  if (m < 1) m = 1;
+  if (m > T) m = T;
+  return (int)m;
+}
+
 /*
  * Strictly balanced gating [OLNN, "Strictly Balanced Gating (Batchwise
  * Mask)"; LESSON Ch. 2 mask form and Ch. 4]: P = G_sigma(x) = Softmax(x W_g)

@@ -621,6 +621,17 @@ def _bal_ref_mask(P, m):
     return M
 
 
+def pin_bal_rows_lesson(orc):
+    """The lesson's translation-scale pooling example (golden fixture): k = 2,
+    n = 512 experts, 16,000 words on one GPU give 62.5 per expert (a mask
+    takes whole tokens: 62), and pooled over 64 GPUs exactly 4,000; plus the
+    clamps to 1 and to T."""
+    for ex in GOLDEN["batchwise_rows"]:
+        m = orc.bal_rows(ex["T"], ex["k"], ex["E"])
+        assert m == math.floor(ex["per_expert"]), (ex["source"], m)
+    assert orc.bal_rows(3, 1, 8) == 1 and orc.bal_rows(5, 8, 4) == 5
+
+
 def pin_bal_batchwise_bruteforce(orc):
     """The batchwise mask: per expert the m tokens with the largest dense gate
     (Python sort by (-P, token), ties included); every expert exactly m; gates

@@ -85,3 +85,60 @@ def test_null_and_misaligned_pointers_rejected_on_host(lib):
                         None) == 1
     # misaligned workspace
     assert lib.moe_aux_loss(ctypes.byref(cfg), fake + 16, fake, None, None, None) == 1
+
+
+# ----------------------------------------------------------------------------- widened layers
+
+
+def _hier(**kw):
+    base = dict(T=64, d=32, a=4, b=8, k_primary=2, k_secondary=2, d_ff=64, capacity_factor=1.0,
+                min_capacity=1, act_dtype=B.MOE_BF16)
+    base.update(kw)
+    return B.moe_hier_config(*(base[f] for f, _ in B.moe_hier_config._fields_))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), 0), (dict(k_primary=5), 1), (dict(k_secondary=9), 1), (dict(a=0), 1),
+    (dict(k_primary=0), 1), (dict(a=9, k_primary=9), 2), (dict(b=16, k_secondary=9), 2),
+    (dict(a=33, b=32), 2), (dict(k_primary=4, k_secondary=8, b=8), 2), (dict(T=0), 1),
+    (dict(capacity_factor=0.0), 1), (dict(act_dtype=7), 1)])
+def test_hier_config_checks(lib, kw, status):
+    n = ctypes.c_size_t()
+    assert lib.moe_hier_workspace_size(ctypes.byref(_hier(**kw)), ctypes.byref(n)) == status
+    if status == 0:
+        assert n.value > 0
+
+
+def test_hier_pointers_rejected_on_host(lib):
+    cfg = _hier()
+    f = 1 << 20  # never dereferenced: the checks fail first
+    args = [f, f, None, None, f, None, None, f, None, f, None, f, None, None, None, None, None, f,
+            None]
+    bad = list(args)
+    bad[0] = None  # x
+    assert lib.moe_forward_hier(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[1] = f + 4  # misaligned Wp
+    assert lib.moe_forward_hier(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[2] = f  # primary noise weights without noise
+    assert lib.moe_forward_hier(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[17] = f + 64  # workspace not 256-byte aligned
+    assert lib.moe_forward_hier(ctypes.byref(cfg), *bad) == 1
+
+
+def test_balanced_checks_on_host(lib):
+    cfg = B.config(64, 32, 16, 64, 2, 1.0)
+    n = ctypes.c_size_t()
+    assert lib.moe_balanced_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == 0
+    assert n.value > 0
+    bad_cfg = B.config(64, 32, 16, 64, 17, 1.0)
+    assert lib.moe_balanced_workspace_size(ctypes.byref(bad_cfg), ctypes.byref(n)) == 1
+    f = 1 << 20
+    # loss requested without thresholds
+    assert lib.moe_forward_balanced(ctypes.byref(cfg), f, f, None, None, f, None, f, None, f, f,
+                                    None, f, None) == 1
+    # NULL Wg
+    assert lib.moe_forward_balanced(ctypes.byref(cfg), f, None, None, None, f, None, f, None, f,
+                                    None, None, f, None) == 1

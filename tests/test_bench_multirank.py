@@ -68,3 +68,19 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2
     assert rec["value"] > 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("workload", ["hier_16x64_e1024", "balanced_top2_e64"])
+def test_reference_arm_widened_workloads(workload):
+    """The oracle legs of the hierarchical and balanced workloads (reduced T)
+    print one well-formed JSON line on one rank."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+           "--warmup", "1", "--cpu-sample", "2", "--tokens", "256", "--workload", workload]
+    p = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["config"]["workload"] == workload
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0

@@ -59,6 +59,8 @@ MUTATIONS = {
                                 "mask[u] = P[u] >= (double)thr[u % E] ? 1 : 0;"),
     "bal_loss_sign": ("s += (mt - (double)mask_batch[(size_t)t * E + i]) * (x - th);",
                       "s += ((double)mask_batch[(size_t)t * E + i] - mt) * (x - th);"),
+    "bal_rows_rounded_up": ("long long m = (long long)k * T / E;",
+                            "long long m = ((long long)k * T + E - 1) / E;"),
     "softmax_no_max_shift": ("for (int e = 0; e < E; ++e) z += exp(h[e] - mx);\n    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e] - mx) / z;",
                              "for (int e = 0; e < E; ++e) z += exp(h[e]);\n    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e]) / z;"),
     "hier_secondary_load_dropped": ("      count[i] += 1;\n      for (int j = 0; j < b; ++j) {",
