@@ -951,6 +951,7 @@ __global__ void __launch_bounds__(kHierWarps * 32)
 k_hier_select(int T, int a, int b, int kp, int ks, int noisy, const int32_t *__restrict__ idx_p,
               const float *__restrict__ g_p, const float *__restrict__ cs,
               const float *__restrict__ ss, const float *__restrict__ Hs,
+              const int32_t *__restrict__ poff, const int32_t *__restrict__ pos_p,
               int32_t *__restrict__ idx, float *__restrict__ gate, float *__restrict__ partials,
               DeviceStatus *st) {
   pdl_wait();
@@ -983,8 +984,9 @@ k_hier_select(int T, int a, int b, int kp, int ks, int noisy, const int32_t *__r
       }
       continue;
     }
-    // The group's row of H, c and sigma, loaded together (one trip).
-    const size_t o = t * E + (size_t)i * b;
+    // The group's row of H, c and sigma, loaded together (one trip): in the
+    // dense [T][a*b] layout, or the grouped router's compact row.
+    const size_t o = poff ? ((size_t)poff[i] + pos_p[t * kp + q]) * b : t * E + (size_t)i * b;
     float v[VPL], cv[VPL], sv[VPL];
 #pragma unroll
     for (int m = 0; m < VPL; ++m) {
@@ -1251,7 +1253,8 @@ cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, in
 
 cudaError_t launch_hier_select(int T, int a, int b, int kp, int ks, bool noisy,
                                const int32_t *idx_p, const float *g_p, const float *cs,
-                               const float *ss, const float *Hs, int32_t *idx, float *gate,
+                               const float *ss, const float *Hs, const int32_t *poff,
+                               const int32_t *pos_p, int32_t *idx, float *gate,
                                float *partials, DeviceStatus *st, cudaStream_t s) {
   if (kp > kHierMaxKp || ks > 8 || kp * b > 1024) return cudaErrorInvalidValue;
   const int TB = hier_tokens(kp, b);
@@ -1265,7 +1268,7 @@ cudaError_t launch_hier_select(int T, int a, int b, int kp, int ks, bool noisy,
                                           (int)dsm);                                           \
     if (e_ != cudaSuccess) return e_;                                                          \
     launch_pdl(k_hier_select<V, KM>, grid, kHierWarps * 32, dsm, s, T, a, b, kp, ks,          \
-               noisy ? 1 : 0, idx_p, g_p, cs, ss, Hs, idx, gate, partials, st);                \
+               noisy ? 1 : 0, idx_p, g_p, cs, ss, Hs, poff, pos_p, idx, gate, partials, st);  \
   } while (0)
 #define MOE_HIER(V)               \
   do {                            \

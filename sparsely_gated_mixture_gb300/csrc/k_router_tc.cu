@@ -809,6 +809,241 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   }
 }
 
+// ----------------------------------------------------------------------------- grouped form
+// The hierarchical layer's secondary gates, only where they are used: the
+// (token, primary pick) pairs come packed by group (xg: group i's tokens in
+// rows goff[i] .. goff[i+1]-1, as the slot pass and gather lay them out), and
+// group i's rows meet only group i's weight columns (n-blocks i*nbg ..
+// i*nbg+nbg-1 of the split weights). A tile is (group, 128-row block,
+// n-block). Outputs c, sigma, H [rows][b] are written at padded row offsets
+// poff[i] = sum over earlier groups of their row blocks * 128, so a ragged
+// tail's rows land in its own group's padding (never read), not in the next
+// group's rows. A row's noise is noise[t][i*b + j] with t its packed token.
+struct GParams {
+  int a, nbg, kp, noise_stride;
+  const int32_t *goff;    // [a+1] exact packed-row offsets of the groups
+  const int32_t *grow;    // [rows] packed row -> t * kp + q
+  int32_t *poff_out;      // [a+1] padded output offsets (written by block 0)
+};
+
+__device__ __forceinline__ void load_noise8_g(const RParams &p, int t, size_t e0, float *nz) {
+  if (t < 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) nz[j] = 0.f;
+    return;
+  }
+  const float4 *src = reinterpret_cast<const float4 *>(p.noise + (size_t)t * p.d + e0);
+  const float4 u = src[0], v = src[1];
+  nz[0] = u.x; nz[1] = u.y; nz[2] = u.z; nz[3] = u.w;
+  nz[4] = v.x; nz[5] = v.y; nz[6] = v.z; nz[7] = v.w;
+}
+
+// p: T = output rows (padded), E = b, d = the noise row stride (a*b; the K
+// width is in gd), noise / noisy as usual, no bias, tma_out set.
+template <int BNR>
+__global__ void __launch_bounds__(kRThreads, 1)
+k_router_grp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+             const __grid_constant__ CUtensorMap tmH, const RParams p, const GParams g, int gd) {
+  using C = RCfg<BNR>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  float *staging = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE + EPI_BYTES);
+  uint64_t *full = bars, *empty = bars + C::STAGES;
+  uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *gtile = const_cast<int *>(reinterpret_cast<volatile int *>(abort_flag + 1));  // [a+1]
+  int *gpoff = gtile + g.a + 1;                                                      // [a+1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kREpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();  // the group offsets come from the slot pass
+  pdl_trigger();
+  if (threadIdx.x == 0) {  // tile and padded-row prefixes over the groups
+    int tiles = 0, rows = 0;
+    for (int i = 0; i < g.a; ++i) {
+      gtile[i] = tiles;
+      gpoff[i] = rows;
+      const int mt = (g.goff[i + 1] - g.goff[i] + RBM - 1) / RBM;
+      tiles += mt * g.nbg;
+      rows += mt * RBM;
+    }
+    gtile[g.a] = tiles;
+    gpoff[g.a] = rows;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= g.a; i += blockDim.x) g.poff_out[i] = gpoff[i];
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = gtile[g.a];
+  const int num_kb = (gd + RBK - 1) / RBK;
+  // tile -> (group, row block, n-block in the group)
+  auto locate = [&](int tile, int &gi, int &mb, int &nb) {
+    int lo = 0, hi = g.a - 1;
+    while (lo < hi) {  // the last group whose first tile is <= tile
+      const int mid = (lo + hi + 1) >> 1;
+      if (gtile[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    gi = lo;
+    const int local = tile - gtile[lo];
+    mb = local / g.nbg;
+    nb = local - mb * g.nbg;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+        int gi, mb, nb;
+        locate(tile, gi, mb, nb);
+        const int row0 = g.goff[gi] + mb * RBM, n_abs = gi * g.nbg + nb;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 31, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = smem + s * C::STAGE;
+          mbar_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(st, &tmA, &full[s], kb * RBK, row0);
+          tma_load_2d(st + C::A_BYTES, &tmB, &full[s], kb * RBK, n_abs * C::NB);
+        }
+      }
+      const uint32_t issued = it;
+      for (uint32_t q = issued > (uint32_t)C::STAGES ? issued - C::STAGES : 0; q < issued; ++q)
+        mbar_drain(&full[q % C::STAGES], (q / C::STAGES) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 32, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * C::NB);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 33, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < RBK / 16; ++kk) {
+            const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc(a0 + C::A_BYTES + kk * 32, 16, 1024);
+            umma_r<BNR>(tmem_d, ad, bd, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&acc_full[buf]);
+      }
+      umma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    const int quad = warp & 3;
+    const int sub = (warp - 2) >> 2;
+    int local = 0;
+    float *stg = staging + (size_t)(warp - 2) * kEpiWarpFloats;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+      int gi, mb, nb;
+      locate(tile, gi, mb, nb);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
+                                                           p.st, 34, p.wait_ns));
+      if (!ready) break;
+      tc_fence_after();
+      const int cnt = g.goff[gi + 1] - g.goff[gi];
+      const int lrow = mb * RBM + quad * 32 + lane;  // row within the group
+      int t = -1;                                     // this lane's token, if a real row
+      if (lrow < cnt) t = g.grow[g.goff[gi] + lrow] / g.kp;
+      const int t0 = gpoff[gi] + mb * RBM + quad * 32;  // output row of lane 0
+      const uint32_t lane_addr =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * C::NB);
+      const int nunits = BNR / 16;  // the group's blocks are whole (checked on the host)
+      const int epu = p.noisy ? 8 : 16;
+      const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first in-group expert
+#pragma unroll 1
+      for (int u = sub; u < nunits; u += 2) {
+        float nz[8];
+        if (p.noisy) load_noise8_g(p, t, (size_t)gi * p.E + eb + u * 8, nz);
+        uint32_t vh[16], vm[16], vl[16];
+        tmem_ld16(lane_addr + (uint32_t)(u * 16), vh);
+        tmem_ld16(lane_addr + (uint32_t)(BNR + u * 16), vm);
+        tmem_ld16(lane_addr + (uint32_t)(2 * BNR + u * 16), vl);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        if (p.noisy) {
+          float cv[8], zv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            cv[j] = v[2 * j];
+            zv[j] = v[2 * j + 1];
+          }
+          router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg, nullptr, 0);
+        } else {
+          router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg, nullptr);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  if (warp >= 2 && lane == 0) bulk_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
 int tile_cols(int NC) { return NC <= 16 ? 16 : NC <= 32 ? 32 : 64; }
 
 // 2-D fp32 tensor [T, E] (E contiguous, E % 4 == 0): the router's output
@@ -880,7 +1115,57 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
   return err;
 }
 
+template <int BNR>
+cudaError_t run_grp(const GroupedRouter &r, DeviceStatus *st, cudaStream_t s) {
+  const int noisy = r.Wn != nullptr;
+  const int ncg = (noisy ? 2 : 1) * r.b;  // a group's output columns
+  const int NC = r.a * ncg, n_blocks = NC / BNR;
+  dim3 sg_grid((r.d + 31) / 32, (NC + 31) / 32);
+  launch_pdl(k_router_split, sg_grid, dim3(32, 8), 0, s, r.d, r.a * r.b, noisy, NC, NC, BNR, r.Wg,
+      r.Wn, static_cast<__nv_bfloat16 *>(r.bsplit), st);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  CUtensorMap ta, tb, tc, ts, th;
+  const int rows_pad = r.T * r.kp + r.a * RBM;
+  if (!make_map(&ta, r.xg, (uint64_t)r.T * r.kp, (uint64_t)r.d, RBM) ||
+      !make_map(&tb, r.bsplit, (uint64_t)3 * NC, (uint64_t)r.d, 3 * BNR) ||
+      !make_out_map(&th, r.H, rows_pad, r.b, noisy))
+    return cudaErrorInvalidValue;
+  if (noisy) {
+    if (!make_out_map(&tc, r.c, rows_pad, r.b, true) ||
+        !make_out_map(&ts, r.sigma, rows_pad, r.b, true))
+      return cudaErrorInvalidValue;
+  } else {
+    tc = ts = th;
+  }
+  RParams p{rows_pad, r.a * r.b, r.b, noisy, NC, NC, n_blocks, 1, r.noise, nullptr, r.c, r.sigma,
+            r.H, st, wait_limit_ns(), 0, 0, 0, nullptr, nullptr, nullptr, nullptr, nullptr};
+  GParams g{r.a, ncg / BNR, r.kp, r.a * r.b, r.goff, r.grow, r.poff};
+  const size_t smem = RCfg<BNR>::SMEM + (size_t)8 * (r.a + 1);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  err = cudaFuncSetAttribute(k_router_grp<BNR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (err != cudaSuccess) return err;
+  const long max_tiles = ((long)r.T * r.kp / RBM + r.a) * (ncg / BNR);
+  const int grid = max_tiles < sm_count() ? (int)max_tiles : sm_count();
+  launch_pdl(k_router_grp<BNR>, grid, kRThreads, smem, s, ta, tb, tc, ts, th, p, g, r.d);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+bool router_grouped_supported(int d, int b, bool noisy, bool bf16) {
+  const int ncg = (noisy ? 2 : 1) * b;
+  return bf16 && d % 8 == 0 && b % 4 == 0 && (ncg == 16 || ncg == 32 || ncg % 64 == 0) &&
+         encode_fn() != nullptr;
+}
+
+cudaError_t launch_router_grouped(const GroupedRouter &r, DeviceStatus *st, cudaStream_t s) {
+  const int ncg = (r.Wn ? 2 : 1) * r.b;
+  if (ncg == 16) return run_grp<16>(r, st, s);
+  if (ncg == 32) return run_grp<32>(r, st, s);
+  return run_grp<64>(r, st, s);
+}
 
 bool router_tc_supported(const moe_config &c) {
   return c.act_dtype == MOE_BF16 && c.d % 8 == 0 && encode_fn() != nullptr;

@@ -200,7 +200,7 @@ static moe_config hier_primary(const moe_hier_config &h) {
 
 struct HierLayout {
   WsLayout Ls, Lp;
-  size_t off_p, parts, scratch, total;
+  size_t off_p, parts, scratch, gc, gs, gH, gpoff, total;
   int rows;
 };
 
@@ -215,7 +215,17 @@ static HierLayout hier_layout(const moe_hier_config &h) {
   H.parts = off;
   off = align_up(off + (size_t)H.rows * 4 * (size_t)h.a * h.b * 4, 256);
   H.scratch = off;  // two finalize outputs of 3 floats
-  H.total = align_up(off + 64, 256);
+  off = align_up(off + 64, 256);
+  // The grouped router's compact outputs: [T*kp + a*128 padded rows][b].
+  const size_t grows = (size_t)h.T * h.k_primary + (size_t)h.a * 128;
+  H.gc = off;
+  off = align_up(off + grows * h.b * 4, 256);
+  H.gs = off;
+  off = align_up(off + grows * h.b * 4, 256);
+  H.gH = off;
+  off = align_up(off + grows * h.b * 4, 256);
+  H.gpoff = off;
+  H.total = align_up(off + (size_t)(h.a + 1) * 4, 256);
   return H;
 }
 
@@ -504,11 +514,44 @@ int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
   if (aux_out2)
     MOE_CUDA(launch_aux_finalize(cp, ws_at<float>(wsp, Lp.partials), Lp.n_aux_blocks, scratch,
                                  nullptr, nullptr, ws_at<float2>(wsp, Lp.aux_vec), st_p, s));
-  // 2. The secondary logits over all a*b experts (this clears the layer's
-  //    status word first).
-  float *cc = ws_at<float>(ws, L.c), *sg = ws_at<float>(ws, L.sigma), *H = ws_at<float>(ws, L.H);
-  MOE_CUDA(launch_router(cs, x, Ws, Ws_noise, noise_s, nullptr, cc, sg, H,
-                         ws_at<char>(ws, L.bsplit), st, s));
+  // 2. The secondary logits (the router's first kernel clears the layer's
+  //    status word). Grouped: only for the (token, primary pick) pairs -- the
+  //    pairs packed by group with the flat slot pass (capacity T, so nothing
+  //    drops; its status goes to the primary word) and gather, then the
+  //    grouped router on each group's rows and weight columns. Otherwise the
+  //    dense router over all a*b experts of every token.
+  const bool bf16 = h.act_dtype == MOE_BF16;
+  const bool grouped = router_grouped_supported(h.d, h.b, Ws_noise != nullptr, bf16);
+  float *cc, *sg, *H;
+  const int32_t *gpoff = nullptr, *pos_p = nullptr;
+  if (grouped) {
+    moe_config cpc = cp;
+    cpc.capacity_factor = (float)h.a;  // C = T: every (token, pick) pair is kept
+    const int32_t *goff = ws_at<int32_t>(wsp, Lp.offset);
+    MOE_CUDA(launch_slots(cpc, h.T, idx_p, g_p, ws_at<int32_t>(wsp, Lp.hist),
+                          ws_at<int32_t>(wsp, Lp.chunk_base), ws_at<int32_t>(wsp, Lp.count),
+                          ws_at<int32_t>(wsp, Lp.offset), ws_at<int32_t>(wsp, Lp.mtiles),
+                          ws_at<int32_t>(wsp, Lp.pos), ws_at<uint8_t>(wsp, Lp.keep),
+                          ws_at<int32_t>(wsp, Lp.row_token), ws_at<float>(wsp, Lp.row_gate),
+                          Lp.n_chunks, st_p, s));
+    MOE_CUDA(launch_gather(cpc, x, goff, ws_at<int32_t>(wsp, Lp.row_token),
+                           ws_at<char>(wsp, Lp.xbuf), st_p, s));
+    cc = ws_at<float>(ws, HL.gc);
+    sg = ws_at<float>(ws, HL.gs);
+    H = ws_at<float>(ws, HL.gH);
+    gpoff = ws_at<int32_t>(ws, HL.gpoff);
+    pos_p = ws_at<int32_t>(wsp, Lp.pos);
+    const GroupedRouter gr{h.T, h.d, h.a, h.b, h.k_primary, ws_at<char>(wsp, Lp.xbuf), goff,
+                           ws_at<int32_t>(wsp, Lp.row_token), Ws, Ws_noise, noise_s, cc, sg, H,
+                           ws_at<int32_t>(ws, HL.gpoff), ws_at<char>(ws, L.bsplit)};
+    MOE_CUDA(launch_router_grouped(gr, st, s));
+  } else {
+    cc = ws_at<float>(ws, L.c);
+    sg = ws_at<float>(ws, L.sigma);
+    H = ws_at<float>(ws, L.H);
+    MOE_CUDA(launch_router(cs, x, Ws, Ws_noise, noise_s, nullptr, cc, sg, H,
+                           ws_at<char>(ws, L.bsplit), st, s));
+  }
   // 3. The two-level selection and the hierarchical partial rows.
   int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
   float *g = gate ? gate : ws_at<float>(ws, L.gate);
@@ -516,7 +559,7 @@ int moe_forward_hier(const moe_hier_config *cfg, const void *x, const float *Wp,
   uint8_t *kp = keep ? keep : ws_at<uint8_t>(ws, L.keep);
   float *parts = aux_out2 ? ws_at<float>(ws, HL.parts) : nullptr;
   MOE_CUDA(launch_hier_select(h.T, h.a, h.b, h.k_primary, h.k_secondary, Ws_noise != nullptr,
-                              idx_p, g_p, cc, sg, H, idx, g, parts, st, s));
+                              idx_p, g_p, cc, sg, H, gpoff, pos_p, idx, g, parts, st, s));
   // 4. Importance_H and the in-group loads summed over the rows, then Load_H
   //    and the two CV^2 (the tail also carries a primary-gate error over).
   if (aux_out2)

@@ -136,9 +136,12 @@ cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c,
 // Hierarchical gate (k_gate.cu): two-level selection with the balancing
 // partial rows (hier_rows(T, kp, b) rows of [4][a*b]), and the losses from the
 // finalizes' sums.
+// With poff and pos_p given, the secondary logits are the grouped router's
+// compact rows: (t, q) at row poff[group] + pos_p[t*kp + q], stride b.
 cudaError_t launch_hier_select(int T, int a, int b, int kp, int ks, bool noisy,
                                const int32_t *idx_p, const float *g_p, const float *cs,
-                               const float *ss, const float *Hs, int32_t *idx, float *gate,
+                               const float *ss, const float *Hs, const int32_t *poff,
+                               const int32_t *pos_p, int32_t *idx, float *gate,
                                float *partials, DeviceStatus *st, cudaStream_t s);
 int hier_rows(int T, int kp, int b);
 cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const float2 *aux_p,
@@ -157,6 +160,24 @@ cudaError_t launch_bal_combine(const moe_config &c, int m, const void *x, const 
                                const int32_t *trows, const int32_t *npick, void *y,
                                DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_bal_loss(int E, const double *loss_part, float *out, cudaStream_t s);
+
+// k_router_tc.cu, grouped form: the hierarchical layer's secondary logits for
+// the (token, primary pick) pairs only. xg holds group i's tokens in rows
+// goff[i] .. goff[i+1]-1 (grow: packed row -> t*kp + q); Wg, Wn [d, a*b];
+// noise [T, a*b]; outputs c, sigma, H [T*kp + a*128][b] at the padded row
+// offsets written to poff [a+1]. Supported when a group's columns fill whole
+// blocks (2b or b in {16, 32} or a multiple of 64), b % 4 == 0, bf16 x.
+struct GroupedRouter {
+  int T, d, a, b, kp;
+  const void *xg;
+  const int32_t *goff, *grow;
+  const float *Wg, *Wn, *noise;
+  float *c, *sigma, *H;
+  int32_t *poff;
+  void *bsplit;
+};
+bool router_grouped_supported(int d, int b, bool noisy, bool bf16);
+cudaError_t launch_router_grouped(const GroupedRouter &r, DeviceStatus *st, cudaStream_t s);
 
 // k_router_tc.cu: the router as three bf16 tensor-core GEMMs (exact split of W).
 bool router_tc_supported(const moe_config &cfg);
