@@ -666,11 +666,15 @@ def run_hier(args, w: wl.HierWorkload):
                  "algorithmic_bytes": ffn_bytes, "traffic": None})
     tc = w.dtype == "bf16" and w.d % 8 == 0
     # primary gate (split + router with fused selection, or + selection),
-    # primary finalize, secondary split + router, two-level selection,
-    # finalize, tail; three slot kernels, gather, two GEMMs, combine
+    # primary finalize; the secondary logits: grouped (three slot kernels and
+    # a gather packing the pairs by group, split + grouped router) or dense
+    # (split + router); two-level selection, finalize, tail; three slot
+    # kernels, gather, two GEMMs, combine
     prim_fused = tc and (2 * w.a if w.noisy else w.a) <= 64 and w.a % 4 == 0 and w.kp <= 8
-    launches = ((2 if tc else 1) + (0 if prim_fused else 1) + 1 + (2 if tc else 1) + 1 + 1 + 1
-                + 3 + 1 + 2 + 1)
+    ncg = (2 if w.noisy else 1) * w.b
+    grouped = tc and w.b % 4 == 0 and (ncg in (16, 32) or ncg % 64 == 0)
+    launches = ((2 if tc else 1) + (0 if prim_fused else 1) + 1
+                + (3 + 1 + 2 if grouped else (2 if tc else 1)) + 1 + 1 + 1 + 3 + 1 + 2 + 1)
     line = {
         "metric": "hierarchical MoE layer fwd tokens/s @1 GB300",
         "value": job_tokens_per_s(world, T, ms), "unit": "tokens/s", "n_gpus": world,

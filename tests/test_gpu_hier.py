@@ -65,6 +65,12 @@ EDGE = {
                    dtype="bf16", noisy=True),
     "hier_kp_equals_a": HW("hier_kp_equals_a", T=150, d=64, a=3, b=8, kp=3, ks=2, d_ff=64,
                            cf=1.0, dtype="bf16", noisy=True),
+    # the grouped secondary router without noise (16 columns per group), and
+    # with a group spanning three 64-column blocks
+    "hier_grouped_clean_b16": HW("hier_grouped_clean_b16", T=300, d=64, a=6, b=16, kp=2, ks=3,
+                                 d_ff=64, cf=1.0, dtype="bf16", noisy=False),
+    "hier_grouped_b96": HW("hier_grouped_b96", T=400, d=128, a=4, b=96, kp=2, ks=4, d_ff=64,
+                           cf=1.25, dtype="bf16", noisy=True),
 }
 SMALL.update(EDGE)
 
