@@ -21,6 +21,9 @@ and marshals numpy arrays. Each wrapper names the page passage it follows:
   Ch. 2 mask form, Ch. 4): the batchwise and threshold masks, the
   renormalised gate and L_batchwise (``bal_*``).
 
+* Its section 3.4 "Training the gating network" and the Switch page's step 8:
+  the backward of the layer (``backward``, ``loss``).
+
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 except the expert FFN's values on random weights, which the pages never print;
 those are pinned only through reductions (dense all-experts sum, the Switch
@@ -119,6 +122,9 @@ class Oracle:
         lib.orc_bal_gate.restype = None
         lib.orc_bal_loss.argtypes = [I, I, P, P, P]
         lib.orc_bal_loss.restype = D
+        lib.orc_backward.argtypes = [I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, P, I,
+                                     P, D, D, D, P, P, P, P, P, P, P, P]
+        lib.orc_backward.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -270,6 +276,56 @@ class Oracle:
         return dict(c=c, sigma=s, H=H, idx=idx, gate=gate, hk=hk, hk1=hk1, C=C, pos=pos,
                     keep=keep, count=count, y=y, nonfinite=bad_h or bad_y, **ax)
 
+    def loss(self, inp: dict, dy, w_imp: float = 0.0, w_load: float = 0.0,
+             w_aux: float = 0.0) -> float:
+        """The scalar the backward differentiates: sum <dy, y> + w_imp
+        CV(Importance)^2 + w_load CV(Load)^2 + w_aux * (Switch auxiliary loss)."""
+        fw = self.forward(inp)
+        o3 = fw["out3"]
+        return float(np.sum(np.asarray(dy, np.float64) * fw["y"]) + w_imp * o3[0] +
+                     w_load * o3[1] + w_aux * o3[2])
+
+    def backward(self, inp: dict, dy, w_imp: float = 0.0, w_load: float = 0.0,
+                 w_aux: float = 0.0) -> dict:
+        """Gradients of ``loss`` with the forward's discrete choices (top-k,
+        capacity, ReLU pattern) held fixed (OLNN section 3.4, "Training the
+        gating network"; Switch step 8). Returns fp64 dx, dWg, dWn, dbias, dW1, db1, dW2, db2;
+        dWn and dbias are None without noise weights or router bias, db1 and
+        db2 are the gradients at a zero bias when b1 or b2 is None."""
+        x = np.ascontiguousarray(inp["x"])
+        T, d = x.shape
+        Wg = _f32(inp["Wg"])
+        E = Wg.shape[1]
+        Wn, noise, bias = _f32(inp.get("Wn")), _f32(inp.get("noise")), _f32(inp.get("bias"))
+        if (Wn is None) != (noise is None):
+            raise ValueError("noise weights and noise come together")
+        W1 = np.ascontiguousarray(inp["W1"])
+        W2 = np.ascontiguousarray(inp["W2"])
+        d_ff = W1.shape[2]
+        wcode = _dtype_code(W1)
+        b1 = None if inp.get("b1") is None else np.ascontiguousarray(inp["b1"])
+        b2 = None if inp.get("b2") is None else np.ascontiguousarray(inp["b2"])
+        for a in (W2, b1, b2):
+            if a is not None and _dtype_code(a) != wcode:
+                raise TypeError("expert weights and biases share one element type")
+        k, mode = int(inp["k"]), int(inp["mode"])
+        if mode == SWITCH and k != 1:
+            raise ValueError("Switch gating is top-1")
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        if dy.shape != (T, d):
+            raise ValueError("dy is [T, d]")
+        g = dict(dx=np.empty((T, d)), dWg=np.empty((d, E)),
+                 dWn=None if Wn is None else np.empty((d, E)),
+                 dbias=None if bias is None else np.empty(E),
+                 dW1=np.empty((E, d, d_ff)), db1=np.empty((E, d_ff)),
+                 dW2=np.empty((E, d_ff, d)), db2=np.empty((E, d)))
+        self.lib.orc_backward(T, d, E, d_ff, k, mode, float(inp["cf"]), int(inp.get("min_cap", 1)),
+                              _ptr(x), _dtype_code(x), _ptr(Wg), _ptr(Wn), _ptr(noise),
+                              _ptr(bias), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), wcode,
+                              _ptr(dy), float(w_imp), float(w_load), float(w_aux),
+                              *[_ptr(g[n]) for n in ("dx", "dWg", "dWn", "dbias", "dW1", "db1",
+                                                      "dW2", "db2")])
+        return g
 
     # ------------------------------------------------------------ hierarchical
     def hier_select(self, idx_p, g_p, Hs, a: int, b: int, ks: int):
@@ -470,6 +526,14 @@ def aux(*a, **k):
 
 def forward(*a, **k):
     return default().forward(*a, **k)
+
+
+def loss(*a, **k):
+    return default().loss(*a, **k)
+
+
+def backward(*a, **k):
+    return default().backward(*a, **k)
 
 
 def hier_select(*a, **k):

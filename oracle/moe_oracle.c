@@ -537,6 +537,225 @@ double orc_bal_loss(int T, int E, const double *P, const unsigned char *mask_bat
   return s;
 }
 
+/*
+ * Backward of the layer [OLNN section 3.4, "Training the gating network":
+ * plain back-propagation, gradients reach W_g through the selected softmax
+ * gates and W_noise through the load estimator; SWITCH step 8: f is built
+ * from integer decisions and carries no gradient, P and the selected gate
+ * do]. Parity: pinned by central finite differences of the forward, by the
+ * one-expert dense-MLP closed form and by the logit-shift invariance.
+ * For an upstream gradient dy [T,d] and loss weights w_imp, w_load, w_aux,
+ * the scalar is
+ *   L = sum_t <dy_t, y_t> + w_imp CV(Importance)^2 + w_load CV(Load)^2
+ *       + w_aux * switch_aux,
+ * differentiated as written, with the forward's own choices fixed (top-k,
+ * capacity and the ReLU pattern are piecewise constant):
+ *  - y_t = x_t + sum over kept choices of g * U_e(x_t), U_e(x) = ReLU(x W1_e
+ *    + b1_e) W2_e + b2_e: the residual, the expert MLP and dg = <dy_t, U>;
+ *  - TOPK gates: the softmax over the kept k, dH_Sj = G_j (dG_j - sum_l G_l
+ *    dG_l); SWITCH: g = p[argmax] of the full softmax over E; Importance
+ *    (pre-capacity) adds its CV^2 gradient to every selected choice's dG;
+ *  - Load_e = sum_t Phi((c - thr)/sigma): through c, sigma and thr, where
+ *    thr is the value H of the token's (k+1)-th pick (for a chosen e) or
+ *    k-th pick (otherwise), so its gradient goes to that expert's H; no
+ *    gradient where the load is an indicator (no noise, sigma = 0, k = E);
+ *  - switch_aux = 0.01 E sum_e f_e Pbar_e: through Pbar (Softmax(H) over all
+ *    E, averaged over tokens); f (hard first choices) is constant;
+ *  - H = c + n sigma, sigma = Softplus(z), c = x Wg + b, z = x Wn.
+ * Outputs (fp64, overwritten): dx [T,d], dWg [d,E], dWn [d,E] (when Wn),
+ * dbias [E] (when bias), dW1 [E,d,d_ff], db1 [E,d_ff], dW2 [E,d_ff,d],
+ * db2 [E,d].
+ */
+void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int min_cap,
+                  const void *x, int x_dtype, const float *Wg, const float *Wn,
+                  const float *noise, const float *bias, const void *W1, const void *b1,
+                  const void *W2, const void *b2, int w_dtype, const double *dy, double w_imp,
+                  double w_load, double w_aux, double *dx, double *dWg, double *dWn,
+                  double *dbias, double *dW1, double *db1, double *dW2, double *db2) {
+  const size_t TE = (size_t)T * E;
+  double *c = (double *)malloc(sizeof(double) * TE), *sg = (double *)malloc(sizeof(double) * TE);
+  double *H = (double *)malloc(sizeof(double) * TE), *zn = (double *)calloc(TE, sizeof(double));
+  orc_router(T, d, E, x, x_dtype, Wg, Wn, noise, bias, c, sg, H);
+  if (Wn)
+    for (int t = 0; t < T; ++t)
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        for (int e = 0; e < E; ++e) zn[(size_t)t * E + e] += xi * (double)Wn[(size_t)i * E + e];
+      }
+  int *idx = (int *)malloc(sizeof(int) * (size_t)T * k);
+  double *gate = (double *)malloc(sizeof(double) * (size_t)T * k);
+  double *hk = (double *)malloc(sizeof(double) * T), *hk1 = (double *)malloc(sizeof(double) * T);
+  orc_select(T, E, k, mode, H, idx, gate, hk, hk1);
+  const int C = orc_capacity(T, E, k, cf, min_cap);
+  int *pos = (int *)malloc(sizeof(int) * (size_t)T * k), *cnt = (int *)malloc(sizeof(int) * E);
+  unsigned char *keep = (unsigned char *)malloc((size_t)T * k);
+  orc_slots(T, k, E, C, idx, pos, keep, cnt);
+  /* The (k+1)-th pick of each token (the threshold's owner for chosen experts). */
+  int *kth1 = (int *)malloc(sizeof(int) * T);
+  for (int t = 0; t < T; ++t) {
+    kth1[t] = -1;
+    if (k < E) {
+      const double *h = H + (size_t)t * E;
+      double best = -INFINITY;
+      for (int e = 0; e < E; ++e) {
+        int chosen = 0;
+        for (int j = 0; j < k; ++j) chosen |= idx[(size_t)t * k + j] == e;
+        if (!chosen && (kth1[t] < 0 || h[e] > best)) {
+          best = h[e];
+          kth1[t] = e;
+        }
+      }
+    }
+  }
+  memset(dx, 0, sizeof(double) * (size_t)T * d);
+  memset(dWg, 0, sizeof(double) * (size_t)d * E);
+  if (dWn) memset(dWn, 0, sizeof(double) * (size_t)d * E);
+  if (dbias) memset(dbias, 0, sizeof(double) * E);
+  memset(dW1, 0, sizeof(double) * (size_t)E * d * d_ff);
+  memset(db1, 0, sizeof(double) * (size_t)E * d_ff);
+  memset(dW2, 0, sizeof(double) * (size_t)E * d_ff * d);
+  memset(db2, 0, sizeof(double) * (size_t)E * d);
+  double *dg = (double *)calloc((size_t)T * k, sizeof(double));
+  double *pre = (double *)malloc(sizeof(double) * d_ff), *hh = (double *)malloc(sizeof(double) * d_ff);
+  double *U = (double *)malloc(sizeof(double) * d), *dpre = (double *)malloc(sizeof(double) * d_ff);
+  /* Residual and the expert path (sequential: the weight gradients sum over tokens). */
+  for (int t = 0; t < T; ++t) {
+    for (int i = 0; i < d; ++i) dx[(size_t)t * d + i] += dy[(size_t)t * d + i];
+    for (int j = 0; j < k; ++j) {
+      if (!keep[(size_t)t * k + j]) continue;
+      const int e = idx[(size_t)t * k + j];
+      const double g = gate[(size_t)t * k + j];
+      for (int f = 0; f < d_ff; ++f) pre[f] = b1 ? orc_in(b1, w_dtype, (size_t)e * d_ff + f) : 0.0;
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        for (int f = 0; f < d_ff; ++f) pre[f] += xi * orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f);
+      }
+      for (int f = 0; f < d_ff; ++f) hh[f] = pre[f] > 0.0 ? pre[f] : 0.0;
+      for (int cc = 0; cc < d; ++cc) U[cc] = b2 ? orc_in(b2, w_dtype, (size_t)e * d + cc) : 0.0;
+      for (int f = 0; f < d_ff; ++f)
+        for (int cc = 0; cc < d; ++cc) U[cc] += hh[f] * orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc);
+      double s = 0.0;
+      for (int cc = 0; cc < d; ++cc) s += dy[(size_t)t * d + cc] * U[cc];
+      dg[(size_t)t * k + j] = s;
+      /* dU = g dy_t */
+      for (int cc = 0; cc < d; ++cc) db2[(size_t)e * d + cc] += g * dy[(size_t)t * d + cc];
+      for (int f = 0; f < d_ff; ++f) {
+        double dh = 0.0;
+        for (int cc = 0; cc < d; ++cc) {
+          const double du = g * dy[(size_t)t * d + cc];
+          dW2[((size_t)e * d_ff + f) * d + cc] += hh[f] * du;
+          dh += orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc) * du;
+        }
+        dpre[f] = pre[f] > 0.0 ? dh : 0.0;
+        db1[(size_t)e * d_ff + f] += dpre[f];
+      }
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        double acc = 0.0;
+        for (int f = 0; f < d_ff; ++f) {
+          dW1[((size_t)e * d + i) * d_ff + f] += xi * dpre[f];
+          acc += orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f) * dpre[f];
+        }
+        dx[(size_t)t * d + i] += acc;
+      }
+    }
+  }
+  /* Balancing sums and the gradients of their CV^2. */
+  double *imp = (double *)malloc(sizeof(double) * E), *load = (double *)malloc(sizeof(double) * E);
+  double *f = (double *)malloc(sizeof(double) * E), *pbar = (double *)malloc(sizeof(double) * E);
+  double out3[3];
+  orc_aux(T, E, k, c, sg, H, idx, gate, hk, hk1, Wn != NULL, imp, load, f, pbar, out3);
+  double *dimp = (double *)malloc(sizeof(double) * E), *dload = (double *)malloc(sizeof(double) * E);
+  {
+    double *v[2] = {imp, load}, *dv[2] = {dimp, dload}, w[2] = {w_imp, w_load};
+    for (int q = 0; q < 2; ++q) {
+      double m = 0.0, var = 0.0;
+      for (int e = 0; e < E; ++e) m += v[q][e];
+      m /= E;
+      for (int e = 0; e < E; ++e) var += (v[q][e] - m) * (v[q][e] - m);
+      var /= E;
+      /* d/dv_e [var / m^2] = 2 (v_e - m) / (E m^2) - 2 var / (E m^3) */
+      for (int e = 0; e < E; ++e)
+        dv[q][e] = w[q] * (2.0 * (v[q][e] - m) / (E * m * m) - 2.0 * var / (E * m * m * m));
+    }
+  }
+  double *dH = (double *)calloc(TE, sizeof(double)), *dc = (double *)calloc(TE, sizeof(double));
+  double *dsg = (double *)calloc(TE, sizeof(double));
+  double *p = (double *)malloc(sizeof(double) * E);
+  for (int t = 0; t < T; ++t) {
+    const double *h = H + (size_t)t * E;
+    double mx = h[0];
+    for (int e = 1; e < E; ++e)
+      if (h[e] > mx) mx = h[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp(h[e] - mx);
+    for (int e = 0; e < E; ++e) p[e] = exp(h[e] - mx) / z;
+    /* dL/dp_e from the Switch loss (Pbar = mean of p) and, in SWITCH mode, the gate. */
+    double dp[E];
+    for (int e = 0; e < E; ++e) dp[e] = w_aux * 0.01 * E * f[e] / T;
+    if (mode == ORC_SWITCH) {
+      const int e0 = idx[(size_t)t * k];
+      dp[e0] += dg[(size_t)t * k] + dimp[e0];
+    } else {
+      /* the kept-k softmax: dH_Sj = G_j (dG_j - sum_l G_l dG_l) */
+      double dG[k], sum = 0.0;
+      for (int j = 0; j < k; ++j) {
+        dG[j] = dg[(size_t)t * k + j] + dimp[idx[(size_t)t * k + j]];
+        sum += gate[(size_t)t * k + j] * dG[j];
+      }
+      for (int j = 0; j < k; ++j)
+        dH[(size_t)t * E + idx[(size_t)t * k + j]] += gate[(size_t)t * k + j] * (dG[j] - sum);
+    }
+    double pd = 0.0;
+    for (int e = 0; e < E; ++e) pd += p[e] * dp[e];
+    for (int e = 0; e < E; ++e) dH[(size_t)t * E + e] += p[e] * (dp[e] - pd);
+    /* Load: P = Phi((c - thr) / sigma) */
+    if (Wn && k < E) {
+      for (int e = 0; e < E; ++e) {
+        const double s = sg[(size_t)t * E + e];
+        if (s == 0.0) continue;
+        int chosen = 0;
+        for (int j = 0; j < k; ++j) chosen |= idx[(size_t)t * k + j] == e;
+        const int owner = chosen ? kth1[t] : idx[(size_t)t * k + k - 1];
+        const double thr = chosen ? hk1[t] : hk[t];
+        const double ce = c[(size_t)t * E + e], u = (ce - thr) / s;
+        const double phi = exp(-0.5 * u * u) / sqrt(2.0 * acos(-1.0)); /* the N(0,1) density */
+        const double g = dload[e] * phi / s;
+        dc[(size_t)t * E + e] += g;
+        dsg[(size_t)t * E + e] -= g * u;
+        dH[(size_t)t * E + owner] -= g;
+      }
+    }
+  }
+  /* H = c + n sigma; sigma = Softplus(z); c = x Wg + b; z = x Wn. */
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      const size_t u = (size_t)t * E + e;
+      dc[u] += dH[u];
+      if (Wn) dsg[u] += (double)noise[u] * dH[u];
+    }
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      const size_t u = (size_t)t * E + e;
+      const double dz = Wn ? dsg[u] / (1.0 + exp(-zn[u])) : 0.0;
+      if (dbias) dbias[e] += dc[u];
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        dWg[(size_t)i * E + e] += xi * dc[u];
+        dx[(size_t)t * d + i] += (double)Wg[(size_t)i * E + e] * dc[u];
+        if (Wn) {
+          dWn[(size_t)i * E + e] += xi * dz;
+          dx[(size_t)t * d + i] += (double)Wn[(size_t)i * E + e] * dz;
+        }
+      }
+    }
+  }
+  free(c); free(sg); free(H); free(zn); free(idx); free(gate); free(hk); free(hk1);
+  free(pos); free(cnt); free(keep); free(kth1); free(dg); free(pre); free(hh); free(U);
+  free(dpre); free(imp); free(load); free(f); free(pbar); free(dimp); free(dload);
+  free(dH); free(dc); free(dsg); free(p);
+}
+
 /* Exposed for the pins: the scalar building blocks. */
 double orc_softplus_at(double z) { return orc_softplus(z); }
 double orc_phi_at(double u) { return orc_phi(u); }

@@ -701,4 +701,115 @@ def pin_bal_every_token_is_dense(orc):
     np.testing.assert_allclose(r["y"], ref, rtol=1e-11, atol=1e-12)
 
 
+
+# ----------------------------------------------------------------------------- backward
+
+
+def _grad_case(seed, T, d, E, d_ff, k, cf, mode, noisy, router_bias=True, biases=True):
+    """fp32 inputs for the gradient pins: every weight is an fp32 value, so a
+    step of 2^-12 on any entry below 2^11 in magnitude is exact."""
+    rng = np.random.default_rng(seed)
+    f = lambda *sh, sd=1.0: (rng.standard_normal(sh) * sd).astype(np.float32)
+    inp = dict(x=f(T, d), Wg=f(d, E, sd=1 / math.sqrt(d)), k=k, cf=cf, min_cap=1, mode=mode,
+               W1=f(E, d, d_ff, sd=1 / math.sqrt(d)), W2=f(E, d_ff, d, sd=1 / math.sqrt(d_ff)))
+    inp["Wn"] = f(d, E, sd=1 / math.sqrt(d)) if noisy else None
+    inp["noise"] = f(T, E) if noisy else None
+    inp["bias"] = f(E, sd=0.3) if router_bias else None
+    inp["b1"] = f(E, d_ff, sd=0.1) if biases else None
+    inp["b2"] = f(E, d, sd=0.1) if biases else None
+    dy = rng.standard_normal((T, d))
+    return inp, dy
+
+
+_GRAD_OF = dict(x="dx", Wg="dWg", Wn="dWn", bias="dbias", W1="dW1", b1="db1", W2="dW2", b2="db2")
+
+
+def _finite_difference_check(orc, inp, dy, w, per_param, seed):
+    """Central differences of the forward's scalar loss on sampled entries of
+    every input. The forward's discrete choices (top-k, capacity, ReLU) make
+    the loss piecewise smooth; an entry whose one-sided differences disagree
+    sits on a kink and is skipped (at most a few of them)."""
+    g = orc.backward(inp, dy, *w)
+    L0 = orc.loss(inp, dy, *w)
+    eps = 2.0 ** -12
+    rng = np.random.default_rng(seed)
+    checked = skipped = 0
+    for name, gname in _GRAD_OF.items():
+        a = inp.get(name)
+        if a is None:
+            continue
+        for _ in range(per_param):
+            i = tuple(int(rng.integers(0, n)) for n in a.shape)
+            v = a[i]
+            a[i] = v + np.float32(eps)
+            Lp = orc.loss(inp, dy, *w)
+            a[i] = v - np.float32(eps)
+            Lm = orc.loss(inp, dy, *w)
+            a[i] = v
+            up, down = (Lp - L0) / eps, (L0 - Lm) / eps
+            if abs(up - down) > 1e-3 * (abs(up) + abs(down)) + 1e-6:
+                skipped += 1
+                continue
+            fd = (Lp - Lm) / (2 * eps)
+            assert abs(g[gname][i] - fd) <= 1e-5 * abs(fd) + 1e-7, (name, i, g[gname][i], fd)
+            checked += 1
+    assert skipped <= max(2, checked // 10), (checked, skipped)
+
+
+def pin_backward_finite_differences(orc):
+    """The backward equals central differences of the forward's loss, for
+    noisy top-k with capacity drops and all three balancing terms, clean and
+    noisy Switch top-1 with the auxiliary loss, and k = E (no load gradient)."""
+    cases = [
+        (_grad_case(101, 12, 6, 5, 7, 2, 0.8, TOPK, True), (0.7, 0.9, 0.4)),
+        (_grad_case(102, 10, 5, 4, 6, 1, 0.9, SWITCH, False), (0.3, 0.2, 0.8)),
+        (_grad_case(103, 10, 5, 4, 6, 1, 0.9, SWITCH, True), (0.3, 0.6, 0.8)),
+        (_grad_case(104, 9, 5, 6, 4, 3, 2.0, TOPK, True, router_bias=False, biases=False),
+         (1.0, 1.0, 1.0)),
+        (_grad_case(105, 8, 4, 3, 5, 3, 2.0, TOPK, True), (1.0, 1.0, 1.0)),
+    ]
+    for n, ((inp, dy), w) in enumerate(cases):
+        fw = orc.forward(inp)
+        if n == 0:  # the case must exercise capacity drops
+            assert fw["keep"].min() == 0 and fw["keep"].max() == 1
+        _finite_difference_check(orc, inp, dy, w, 12, 200 + n)
+
+
+def pin_backward_dense_mlp(orc):
+    """One expert: every gate is 1, the balancing terms are constant, and the
+    gradients are those of x + ReLU(x W1 + b1) W2 + b2 in matrix form (numpy);
+    the router weights get none."""
+    for mode in (TOPK, SWITCH):
+        inp, dy = _grad_case(110 + mode, 9, 6, 1, 11, 1, 1.0, mode, True)
+        g = orc.backward(inp, dy, 0.5, 0.5, 0.5)
+        X = inp["x"].astype(np.float64)
+        W1, W2 = inp["W1"][0].astype(np.float64), inp["W2"][0].astype(np.float64)
+        pre = X @ W1 + inp["b1"][0]
+        h = np.maximum(pre, 0.0)
+        dpre = (dy @ W2.T) * (pre > 0)
+        np.testing.assert_allclose(g["dW2"][0], h.T @ dy, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["db2"][0], dy.sum(0), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["dW1"][0], X.T @ dpre, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["db1"][0], dpre.sum(0), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(g["dx"], dy + dpre @ W1.T, rtol=1e-12, atol=1e-12)
+        for name in ("dWg", "dWn", "dbias"):
+            assert np.all(g[name] == 0.0), name
+
+
+def pin_backward_logit_shift_invariance(orc):
+    """Adding one constant to every expert's router logit of a token changes
+    neither the gates, the selection, the load estimator's arguments c - thr
+    nor the full softmax, so the gradient summed over experts vanishes: for
+    the router bias and for every row of W_g."""
+    for seed, (T, d, E, d_ff, k, cf, mode, noisy) in enumerate(
+            [(12, 6, 5, 7, 2, 0.8, TOPK, True), (10, 5, 4, 6, 1, 0.9, SWITCH, True)]):
+        inp, dy = _grad_case(120 + seed, T, d, E, d_ff, k, cf, mode, noisy)
+        g = orc.backward(inp, dy, 0.7, 0.9, 0.4)
+        scale = np.abs(g["dbias"]).sum()
+        assert scale > 1e-3
+        assert abs(g["dbias"].sum()) <= 1e-12 * scale + 1e-15
+        rows = g["dWg"].sum(axis=1)
+        assert np.all(np.abs(rows) <= 1e-12 * np.abs(g["dWg"]).sum(axis=1) + 1e-15)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -65,6 +65,21 @@ MUTATIONS = {
                              "for (int e = 0; e < E; ++e) z += exp(h[e]);\n    for (int e = 0; e < E; ++e) P[(size_t)t * E + e] = exp(h[e]) / z;"),
     "hier_secondary_load_dropped": ("      count[i] += 1;\n      for (int j = 0; j < b; ++j) {",
                                        "      count[i] += 1;\n      for (int j = 0; j < b && 0; ++j) {"),
+    "bwd_residual_dropped": ("for (int i = 0; i < d; ++i) dx[(size_t)t * d + i] += dy[(size_t)t * d + i];", ""),
+    "bwd_relu_mask_dropped": ("dpre[f] = pre[f] > 0.0 ? dh : 0.0;", "dpre[f] = dh;"),
+    "bwd_dropped_choices_trained": ("if (!keep[(size_t)t * k + j]) continue;\n      const int e = idx[(size_t)t * k + j];\n      const double g",
+                                    "const int e = idx[(size_t)t * k + j];\n      const double g"),
+    "bwd_w2_transposed": ("dh += orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc) * du;",
+                          "dh += orc_in(W2, w_dtype, ((size_t)e * d + cc) * d_ff + f) * du;"),
+    "bwd_softmax_jacobian_sign": ("gate[(size_t)t * k + j] * (dG[j] - sum);",
+                                  "gate[(size_t)t * k + j] * (dG[j] + sum);"),
+    "bwd_threshold_owner_dropped": ("dH[(size_t)t * E + owner] -= g;", ""),
+    "bwd_cv2_mean_term_dropped": (" - 2.0 * var / (E * m * m * m));", ");"),
+    "bwd_softplus_slope_dropped": ("dsg[u] / (1.0 + exp(-zn[u]))", "dsg[u]"),
+    "bwd_noise_scale_dropped": ("dsg[u] += (double)noise[u] * dH[u];", "dsg[u] += dH[u];"),
+    "bwd_aux_not_averaged": ("w_aux * 0.01 * E * f[e] / T;", "w_aux * 0.01 * E * f[e];"),
+    "bwd_importance_only_kept": ("dG[j] = dg[(size_t)t * k + j] + dimp[idx[(size_t)t * k + j]];",
+                                 "dG[j] = dg[(size_t)t * k + j] + (dg[(size_t)t * k + j] != 0.0 ? dimp[idx[(size_t)t * k + j]] : 0.0);"),
 }
 
 
