@@ -564,14 +564,17 @@ double orc_bal_loss(int T, int E, const double *P, const unsigned char *mask_bat
  *  - H = c + n sigma, sigma = Softplus(z), c = x Wg + b, z = x Wn.
  * Outputs (fp64, overwritten): dx [T,d], dWg [d,E], dWn [d,E] (when Wn),
  * dbias [E] (when bias), dW1 [E,d,d_ff], db1 [E,d_ff], dW2 [E,d_ff,d],
- * db2 [E,d].
+ * db2 [E,d], and (when not NULL) dgate [T,k] = dL/dgate[t,j], the gradient
+ * reaching each selected gate value: <dy_t, U> for a kept choice plus the
+ * Importance term for every selected one.
  */
 void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int min_cap,
                   const void *x, int x_dtype, const float *Wg, const float *Wn,
                   const float *noise, const float *bias, const void *W1, const void *b1,
                   const void *W2, const void *b2, int w_dtype, const double *dy, double w_imp,
                   double w_load, double w_aux, double *dx, double *dWg, double *dWn,
-                  double *dbias, double *dW1, double *db1, double *dW2, double *db2) {
+                  double *dbias, double *dW1, double *db1, double *dW2, double *db2,
+                  double *dgate) {
   const size_t TE = (size_t)T * E;
   double *c = (double *)malloc(sizeof(double) * TE), *sg = (double *)malloc(sizeof(double) * TE);
   double *H = (double *)malloc(sizeof(double) * TE), *zn = (double *)calloc(TE, sizeof(double));
@@ -696,12 +699,14 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
     if (mode == ORC_SWITCH) {
       const int e0 = idx[(size_t)t * k];
       dp[e0] += dg[(size_t)t * k] + dimp[e0];
+      if (dgate) dgate[(size_t)t * k] = dg[(size_t)t * k] + dimp[e0];
     } else {
       /* the kept-k softmax: dH_Sj = G_j (dG_j - sum_l G_l dG_l) */
       double dG[k], sum = 0.0;
       for (int j = 0; j < k; ++j) {
         dG[j] = dg[(size_t)t * k + j] + dimp[idx[(size_t)t * k + j]];
         sum += gate[(size_t)t * k + j] * dG[j];
+        if (dgate) dgate[(size_t)t * k + j] = dG[j];
       }
       for (int j = 0; j < k; ++j)
         dH[(size_t)t * E + idx[(size_t)t * k + j]] += gate[(size_t)t * k + j] * (dG[j] - sum);

@@ -812,4 +812,35 @@ def pin_backward_logit_shift_invariance(orc):
         assert np.all(np.abs(rows) <= 1e-12 * np.abs(g["dWg"]).sum(axis=1) + 1e-15)
 
 
+
+def pin_backward_dgate(orc):
+    """dL/dgate of a selected choice: <dy_t, E_e(x_t)> (numpy expert) when it
+    is kept, 0 when it overflowed, plus w_imp times the derivative of
+    CV(Importance)^2 in that expert's importance (central differences of the
+    pinned CV^2), which is the same for every choice of one expert."""
+    inp, dy = _grad_case(130, 12, 6, 5, 7, 2, 0.8, TOPK, True)
+    fw = orc.forward(inp)
+    assert fw["keep"].min() == 0
+    X = inp["x"].astype(np.float64)
+    U = _ffn_all(X, inp["W1"], inp["b1"], inp["W2"], inp["b2"])  # [E, T, d]
+    g0 = orc.backward(inp, dy, 0.0, 0.0, 0.0)["dgate"]
+    for t in range(X.shape[0]):
+        for j in range(2):
+            e = fw["idx"][t, j]
+            want = float(dy[t] @ U[e, t]) if fw["keep"][t, j] else 0.0
+            assert abs(g0[t, j] - want) <= 1e-12 * (1 + abs(want)), (t, j)
+    w = 0.7
+    g1 = orc.backward(inp, dy, w, 0.0, 0.0)["dgate"]
+    imp = fw["importance"]
+    h = 1e-6
+    for e in range(imp.size):
+        up, dn = imp.copy(), imp.copy()
+        up[e] += h
+        dn[e] -= h
+        want = w * (orc.cv2(up) - orc.cv2(dn)) / (2 * h)
+        sel = fw["idx"] == e
+        if sel.any():
+            np.testing.assert_allclose((g1 - g0)[sel], want, rtol=1e-6, atol=1e-9)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
