@@ -278,6 +278,65 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
                          float *loss_out, uint32_t *mask_out, void *ws, moe_stream_t stream);
 
 /*
+ * Backward of the flat layer ("Outrageously Large Neural Networks", section
+ * 3.4, "Training the gating network": plain back-propagation, gradients reach
+ * W_g through the selected softmax gates and W_noise through the smooth load
+ * estimator; "Switch Transformer", step 8: f carries no gradient, P and the
+ * selected gate do). The gradients of
+ *   L = sum_t <dy_t, y_t> + w_importance * CV(Importance)^2
+ *       + w_load * CV(Load)^2 + w_aux * 0.01 * E * sum_e f_e Pbar_e
+ * with the forward's discrete choices held fixed (the top-k set, capacity
+ * drops, the ReLU pattern): through the residual, the kept experts (dgrad and
+ * wgrad of both layers), the kept top-k softmax (or the full softmax at the
+ * Switch argmax), Importance (every selected choice, before capacity), the
+ * load estimator P = Phi((c - thr) / sigma) (into c, sigma and the expert
+ * whose noisy logit is thr; none without noise or when k = E), the Switch
+ * loss's Pbar, sigma = Softplus(x W_noise) and c = x W_g + b.
+ *
+ * Precondition: `ws` holds the state the last moe_forward left in it for the
+ * same cfg and inputs (x, Wg, Wnoise, noise, logit_bias, W1, b1, W2, b2), and
+ * expert_idx, gate, pos, keep are the pointers given to that call (NULL where
+ * it got NULL); that call had aux_out3 non-NULL if any loss weight here is
+ * nonzero (the backward reads its balancing totals). The call may overwrite
+ * `ws` rows past the forward's last expert row; it leaves the forward's other
+ * results unchanged, so it may be repeated with another dy.
+ * Supported: act_dtype MOE_BF16 with d and d_ff multiples of 64 (the
+ * tensor-core path); else MOE_ERR_UNSUPPORTED.
+ * Inputs: dy [T,d] bf16. Outputs (fp32 unless stated): dx [T,d] bf16; dWg
+ * [d,E]; dWnoise [d,E] (required iff Wnoise is given); dlogit_bias [E] (may
+ * be NULL); dW1 [E,d,d_ff]; db1 [E,d_ff] (may be NULL); dW2 [E,d_ff,d]; db2
+ * [E,d] (may be NULL); dgate [T,k] (may be NULL) = dL/dgate of each selected
+ * gate value (<dy_t, U_e(x_t)> for a kept choice plus the Importance term).
+ * bws is the backward's own workspace, moe_backward_workspace_size bytes,
+ * 256-byte aligned. Device-side errors (a non-finite gradient, a bounded wait
+ * that ran out) go to the status word of `ws`.
+ */
+int moe_backward_workspace_size(const moe_config *cfg, size_t *bytes);
+int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                 const float *noise, const void *W1, const void *W2, const void *b2,
+                 const int32_t *expert_idx, const float *gate, const int32_t *pos,
+                 const uint8_t *keep, const void *dy, float w_importance, float w_load,
+                 float w_aux, void *dx, float *dWg, float *dWnoise, float *dlogit_bias,
+                 float *dW1, float *db1, float *dW2, float *db2, float *dgate, void *ws,
+                 void *bws, moe_stream_t stream);
+
+/*
+ * The gate's share of the backward, from given gate gradients: dgate [T,k]
+ * fp32 = dL/dgate of each selected gate value (Importance term included) for
+ * the selection expert_idx / gate (NULL: the copies in `ws`) of the last
+ * moe_gate or moe_forward on `ws`; the load and Switch terms are added with
+ * weights w_load, w_aux (these need the balancing totals of moe_aux_loss or
+ * of moe_forward with aux_out3). Outputs: dWg [d,E], dWnoise [d,E] (iff
+ * Wnoise), dlogit_bias [E] (may be NULL), dx_gate [T,d] (may be NULL): the
+ * router's share of dx, all fp32. x [T,d] bf16; bws as for moe_backward.
+ */
+int moe_gate_backward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                      const float *noise, const int32_t *expert_idx, const float *gate,
+                      const float *dgate, float w_load, float w_aux, float *dWg, float *dWnoise,
+                      float *dlogit_bias, float *dx_gate, void *ws, void *bws,
+                      moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the first device-side error recorded in `ws`
  * since it was last cleared (MOE_OK if none), writes its detail word (e.g. the
  * offending flat index) to *detail if non-NULL, and clears it.

@@ -123,7 +123,7 @@ class Oracle:
         lib.orc_bal_loss.argtypes = [I, I, P, P, P]
         lib.orc_bal_loss.restype = D
         lib.orc_backward.argtypes = [I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, P, I,
-                                     P, D, D, D, P, P, P, P, P, P, P, P, P]
+                                     P, D, D, D, P, P, P, P, P, P, P, P, P, P, P]
         lib.orc_backward.restype = None
         self.lib = lib
         self.path = lib_path
@@ -290,7 +290,8 @@ class Oracle:
         """Gradients of ``loss`` with the forward's discrete choices (top-k,
         capacity, ReLU pattern) held fixed (OLNN section 3.4, "Training the
         gating network"; Switch step 8). Returns fp64 dx, dWg, dWn, dbias, dW1, db1, dW2, db2,
-        dgate [T,k] (dL/dgate of each selected gate value);
+        dgate [T,k] (dL/dgate of each selected gate value), dc and dz [T,E]
+        (dL/dc of the clean logits, dL/dz of z = x W_noise);
         dWn and dbias are None without noise weights or router bias, db1 and
         db2 are the gradients at a zero bias when b1 or b2 is None."""
         x = np.ascontiguousarray(inp["x"])
@@ -319,13 +320,14 @@ class Oracle:
                  dWn=None if Wn is None else np.empty((d, E)),
                  dbias=None if bias is None else np.empty(E),
                  dW1=np.empty((E, d, d_ff)), db1=np.empty((E, d_ff)),
-                 dW2=np.empty((E, d_ff, d)), db2=np.empty((E, d)), dgate=np.empty((T, k)))
+                 dW2=np.empty((E, d_ff, d)), db2=np.empty((E, d)), dgate=np.empty((T, k)),
+                 dc=np.empty((T, E)), dz=np.empty((T, E)))
         self.lib.orc_backward(T, d, E, d_ff, k, mode, float(inp["cf"]), int(inp.get("min_cap", 1)),
                               _ptr(x), _dtype_code(x), _ptr(Wg), _ptr(Wn), _ptr(noise),
                               _ptr(bias), _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), wcode,
                               _ptr(dy), float(w_imp), float(w_load), float(w_aux),
                               *[_ptr(g[n]) for n in ("dx", "dWg", "dWn", "dbias", "dW1", "db1",
-                                                      "dW2", "db2", "dgate")])
+                                                      "dW2", "db2", "dgate", "dc", "dz")])
         return g
 
     # ------------------------------------------------------------ hierarchical

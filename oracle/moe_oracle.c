@@ -566,7 +566,9 @@ double orc_bal_loss(int T, int E, const double *P, const unsigned char *mask_bat
  * dbias [E] (when bias), dW1 [E,d,d_ff], db1 [E,d_ff], dW2 [E,d_ff,d],
  * db2 [E,d], and (when not NULL) dgate [T,k] = dL/dgate[t,j], the gradient
  * reaching each selected gate value: <dy_t, U> for a kept choice plus the
- * Importance term for every selected one.
+ * Importance term for every selected one; dc_out, dz_out [T,E] (when not
+ * NULL) = dL/dc and dL/dz, the gradients of the clean logit c = x W_g + b and
+ * of z = x W_noise (0 without noise weights).
  */
 void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int min_cap,
                   const void *x, int x_dtype, const float *Wg, const float *Wn,
@@ -574,7 +576,7 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
                   const void *W2, const void *b2, int w_dtype, const double *dy, double w_imp,
                   double w_load, double w_aux, double *dx, double *dWg, double *dWn,
                   double *dbias, double *dW1, double *db1, double *dW2, double *db2,
-                  double *dgate) {
+                  double *dgate, double *dc_out, double *dz_out) {
   const size_t TE = (size_t)T * E;
   double *c = (double *)malloc(sizeof(double) * TE), *sg = (double *)malloc(sizeof(double) * TE);
   double *H = (double *)malloc(sizeof(double) * TE), *zn = (double *)calloc(TE, sizeof(double));
@@ -743,6 +745,8 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
     for (int e = 0; e < E; ++e) {
       const size_t u = (size_t)t * E + e;
       const double dz = Wn ? dsg[u] / (1.0 + exp(-zn[u])) : 0.0;
+      if (dc_out) dc_out[u] = dc[u];
+      if (dz_out) dz_out[u] = dz;
       if (dbias) dbias[e] += dc[u];
       for (int i = 0; i < d; ++i) {
         const double xi = orc_in(x, x_dtype, (size_t)t * d + i);

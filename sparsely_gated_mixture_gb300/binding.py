@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate", "moe_dispatch",
            "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
            "moe_last_device_status", "moe_dispatch_noalloc", "moe_hier_workspace_size",
-           "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced")
+           "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced",
+           "moe_backward_workspace_size", "moe_backward", "moe_gate_backward")
 
 
 class MoEError(RuntimeError):
@@ -98,6 +99,10 @@ def lib():
             L.moe_forward_hier.argtypes = [HP] + [P] * 19
             L.moe_balanced_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_balanced.argtypes = [CP] + [P] * 13
+            L.moe_backward_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
+            F = ctypes.c_float
+            L.moe_backward.argtypes = [CP] + [P] * 12 + [F, F, F] + [P] * 12
+            L.moe_gate_backward.argtypes = [CP] + [P] * 7 + [F, F] + [P] * 7
             for name in EXPORTS[1:]:
                 getattr(L, name).restype = I
             _lib = L
@@ -209,6 +214,33 @@ def moe_forward_balanced(cfg, x, Wg, logit_bias, thresholds, W1, b1, W2, b2, y, 
                                       _p(thresholds), _p(W1), _p(b1), _p(W2), _p(b2), _p(y),
                                       _p(loss_out), _p(mask_out), _p(ws), _stream(stream)),
            "moe_forward_balanced")
+
+
+def moe_backward_workspace_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_backward(cfg, x, Wg, Wnoise, noise, W1, W2, b2, expert_idx, gate, pos, keep, dy,
+                 w_importance, w_load, w_aux, dx, dWg, dWnoise, dlogit_bias, dW1, db1, dW2, db2,
+                 dgate, ws, bws, stream=None):
+    _check(lib().moe_backward(ctypes.byref(cfg), _p(x), _p(Wg), _p(Wnoise), _p(noise), _p(W1),
+                              _p(W2), _p(b2), _p(expert_idx), _p(gate), _p(pos), _p(keep), _p(dy),
+                              float(w_importance), float(w_load), float(w_aux), _p(dx), _p(dWg),
+                              _p(dWnoise), _p(dlogit_bias), _p(dW1), _p(db1), _p(dW2), _p(db2),
+                              _p(dgate), _p(ws), _p(bws), _stream(stream)),
+           "moe_backward")
+
+
+def moe_gate_backward(cfg, x, Wg, Wnoise, noise, expert_idx, gate, dgate, w_load, w_aux, dWg,
+                      dWnoise, dlogit_bias, dx_gate, ws, bws, stream=None):
+    _check(lib().moe_gate_backward(ctypes.byref(cfg), _p(x), _p(Wg), _p(Wnoise), _p(noise),
+                                   _p(expert_idx), _p(gate), _p(dgate), float(w_load),
+                                   float(w_aux), _p(dWg), _p(dWnoise), _p(dlogit_bias),
+                                   _p(dx_gate), _p(ws), _p(bws), _stream(stream)),
+           "moe_gate_backward")
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

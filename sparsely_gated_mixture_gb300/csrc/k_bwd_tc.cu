@@ -1,0 +1,424 @@
+// Backward of the expert networks on the 5th-generation tensor cores
+// ("Outrageously Large Neural Networks", section 3.4: the experts and the
+// gate are trained by plain back-propagation; "Switch Transformer", step 6:
+// each expert owns W1 [d, d_ff] and W2 [d_ff, d]). One grouped-GEMM kernel in
+// three modes over the rows each expert received in the forward:
+//
+//   dgrad through W2 (mode 0):  D = dY_rows W2[e]^T           [rows, d_ff]
+//       epilogue: dgate partial <D_r, h_r> per 256-column block, and
+//       dpre_r = g_r * D_r * [h_r > 0] in bf16 (pad rows written as zero)
+//   dgrad through W1 (mode 1):  dX_rows = dpre_rows W1[e]^T   [rows, d]   (fp32)
+//   weight gradient  (mode 2):  dW[e] = A_rows^T B_rows       [M, N]      (fp32)
+//       dW2: A = h rows, B = g * dY rows;  dW1: A = x rows, B = dpre rows
+//
+// The backward's own row buffers (dY, g*dY, dpre, dX) give each expert a
+// block of rows padded to a multiple of 64 (at least 64), pad rows zero, at
+// the offsets poff[e]. The weight-gradient mode runs its K loop over those
+// padded rows: the pad rows of B are zero, so whatever A holds there (the
+// next expert's rows, or rows the caller zeroed past the last one) adds
+// nothing, and no K tail needs masking.
+//
+// Operand layouts (bf16, 128-byte swizzle, as the forward kernel):
+//   modes 0, 1: A K-major [128 rows x 64 K]; B K-major [256 rows x 64 K]: the
+//               weight's own rows (W2[e] is [d_ff, d]: row f holds K = d
+//               contiguous values; W1[e] is [d, d_ff]: row i holds d_ff).
+//   mode 2:     A MN-major (M contiguous) as two [64 K x 64 M] boxes, B
+//               MN-major as four [64 K x 64 N] boxes; the instruction
+//               descriptor's transpose bits select MN-major for both.
+// Warp roles, the 4-stage ring, two TMEM accumulators and the bounded waits
+// are those of the forward kernel: warp 0 TMA producer, warp 1 TMEM owner and
+// MMA issuer, warps 2-5 epilogue.
+#include "moe_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kTcBM;  // 128 rows (TMEM lanes)
+constexpr int BN = 256;    // accumulator columns per tile
+constexpr int BK = 64;     // K per stage
+constexpr int STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BK * BN * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+
+struct BParams {
+  int mode;
+  int K;          // modes 0, 1: reduction length
+  int N;          // output columns
+  int M;          // mode 2: output rows per expert
+  int E, n_blocks, m_blocks;
+  const int32_t *offset;  // [E+1] the forward's packed row offsets
+  const int32_t *poff;    // [E+1] padded row offsets
+  const float *row_gate;  // mode 0: [packed rows]
+  const __nv_bfloat16 *hbuf;  // mode 0: [packed rows, N]
+  void *out;      // mode 0: bf16 [padded rows, N]; mode 1: fp32 [padded rows, N];
+                  // mode 2: fp32 [E, M, N]
+  float *dgpart;  // mode 0: [padded rows, n_blocks]
+  DeviceStatus *st;
+  unsigned long long wait_ns;
+};
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = 128,
+// N = 256; bits 15 / 16 select MN-major A / B.
+template <int MODE>
+__host__ __device__ constexpr uint32_t bwd_idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((MODE == 2 ? 1u : 0u) << 15) |
+         ((MODE == 2 ? 1u : 0u) << 16) | ((uint32_t)(BN >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+template <int MODE>
+__device__ __forceinline__ void umma_b(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(bwd_idesc<MODE>()), "r"(acc)
+      : "memory");
+}
+
+// Tile -> (expert, m block, n block), the expert's first padded row, its
+// padded and real row counts, and the number of K blocks.
+struct BTile {
+  int e, mb, nb, prow0, prows, rows, num_kb;
+};
+
+template <int MODE>
+__device__ __forceinline__ BTile locate(const BParams &p, const int *start, int tile) {
+  BTile t;
+  if (MODE == 2) {
+    const int per = p.m_blocks * p.n_blocks;
+    t.e = tile / per;
+    const int local = tile - t.e * per;
+    t.nb = local / p.m_blocks;
+    t.mb = local - t.nb * p.m_blocks;
+  } else {
+    int lo = 0, hi = p.E;  // largest e with start[e] <= tile
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (start[mid] <= tile) lo = mid;
+      else hi = mid;
+    }
+    t.e = lo;
+  }
+  t.prow0 = p.poff[t.e];
+  t.prows = p.poff[t.e + 1] - t.prow0;
+  t.rows = p.offset[t.e + 1] - p.offset[t.e];
+  if (MODE != 2) {
+    const int mt = (t.prows + BM - 1) / BM;
+    const int local = tile - start[t.e];
+    t.nb = local / mt;
+    t.mb = local - t.nb * mt;
+    t.num_kb = p.K / BK;
+  } else {
+    t.num_kb = t.prows / BK;
+  }
+  return t;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+k_bwd_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+         const BParams p) {
+  pdl_wait();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint64_t *full = bars, *empty = bars + STAGES;
+  uint64_t *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *tile_start = reinterpret_cast<int *>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // Dgrad modes: tile prefix over experts, ceil(padded rows / BM) * n_blocks each.
+  if (MODE != 2 && warp == 2) {
+    int carry = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < p.E) t = (p.poff[e + 1] - p.poff[e] + BM - 1) / BM * p.n_blocks;
+      int incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < p.E) tile_start[e] = carry + incl - t;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) tile_start[p.E] = carry;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = MODE == 2 ? p.E * p.m_blocks * p.n_blocks : tile_start[p.E];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------- producer
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const BTile t = locate<MODE>(p, tile_start, tile);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 31, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], STAGE_BYTES);
+          if (MODE != 2) {
+            tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * BK, t.prow0 + t.mb * BM);
+            tma_load_2d(sB + s * B_BYTES, &tmB, &full[s], kb * BK, t.e * p.N + t.nb * BN);
+          } else {
+            const int arow = p.offset[t.e] + kb * BK, brow = t.prow0 + kb * BK;
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j)
+              tma_load_2d(sA + s * A_BYTES + j * (BK * 128), &tmA, &full[s], t.mb * BM + j * 64,
+                          arow);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(sB + s * B_BYTES + j * (BK * 128), &tmB, &full[s], t.nb * BN + j * 64,
+                          brow);
+          }
+        }
+      }
+      const uint32_t issued = it;
+      for (uint32_t q = issued > (uint32_t)STAGES ? issued - STAGES : 0; q < issued; ++q)
+        mbar_drain(&full[q % STAGES], (q / STAGES) & 1u);
+    }
+    __syncwarp();
+    pdl_trigger();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------- MMA issuer
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++local) {
+        const BTile t = locate<MODE>(p, tile_start, tile);
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 32, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 33, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            uint64_t ad, bd;
+            if (MODE != 2) {
+              ad = sdesc(a0 + kk * 32, 16, 1024);
+              bd = sdesc(b0 + kk * 32, 16, 1024);
+            } else {
+              ad = sdesc(a0 + kk * 2048, BK * 128, 1024);
+              bd = sdesc(b0 + kk * 2048, BK * 128, 1024);
+            }
+            umma_b<MODE>(tmem_d, ad, bd, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&acc_full[buf]);
+      }
+      umma_commit(drain);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+    pdl_trigger();
+  } else {
+    // ----------------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int r_in_tile = quad * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
+      const BTile t = locate<MODE>(p, tile_start, tile);
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
+                                                           p.st, 34, p.wait_ns));
+      if (!ready) break;
+      tc_fence_after();
+      const int m = t.mb * BM + r_in_tile;
+      // Rows this lane writes: mode 0 every padded row of the expert (pad rows
+      // as zero), mode 1 the real rows, mode 2 the output rows m < M.
+      const bool valid = MODE == 0 ? m < t.prows : (MODE == 1 ? m < t.rows : m < p.M);
+      const bool real = m < t.rows;
+      const size_t pr = (size_t)t.prow0 + m;
+      const size_t q = (size_t)p.offset[t.e] + m;
+      const float g = (MODE == 0 && valid && real) ? p.row_gate[q] : 0.f;
+      float part = 0.f;
+      bool bad = false;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n = t.nb * BN + c * 32;
+        uint32_t v[32];
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c * 32);
+        tmem_ld32(taddr, v);  // warp-collective
+        if (!valid || n >= p.N) continue;
+        if (MODE == 0) {
+          float h[32];
+          if (real) {
+            const uint4 *hp = reinterpret_cast<const uint4 *>(p.hbuf + q * p.N + n);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const uint4 u = hp[w];
+              const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&uu[j]);
+                h[8 * w + 2 * j] = __low2float(b2);
+                h[8 * w + 2 * j + 1] = __high2float(b2);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = 0.f;
+          }
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float d0 = __uint_as_float(v[2 * j]), d1 = __uint_as_float(v[2 * j + 1]);
+            part = fmaf(d0, h[2 * j], part);
+            part = fmaf(d1, h[2 * j + 1], part);
+            const float p0 = h[2 * j] > 0.f ? g * d0 : 0.f;
+            const float p1 = h[2 * j + 1] > 0.f ? g * d1 : 0.f;
+            bad |= !isfinite(p0) || !isfinite(p1);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            packed[j] = *reinterpret_cast<uint32_t *>(&b2);
+          }
+          uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + pr * p.N + n);
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            o[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
+                              packed[4 * w + 3]);
+        } else {
+          float f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            f[j] = __uint_as_float(v[j]);
+            bad |= !isfinite(f[j]);
+          }
+          float *o = MODE == 1
+                         ? static_cast<float *>(p.out) + pr * p.N + n
+                         : static_cast<float *>(p.out) + ((size_t)t.e * p.M + m) * p.N + n;
+#pragma unroll
+          for (int w = 0; w < 8; ++w)
+            reinterpret_cast<float4 *>(o)[w] =
+                make_float4(f[4 * w], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+        }
+      }
+      if (MODE == 0 && valid) p.dgpart[pr * p.n_blocks + t.nb] = part;
+      if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)(MODE == 2 ? m : (long long)pr));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+    pdl_trigger();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+constexpr size_t bwd_smem_bytes(int E) {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 8 + (size_t)(E + 1) * 4;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap &a, const CUtensorMap &b, const BParams &p,
+                        cudaStream_t s) {
+  const size_t smem = bwd_smem_bytes(p.E);
+  cudaError_t err = cudaFuncSetAttribute(k_bwd_tc<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  launch_pdl_c(kPdlGemm, k_bwd_tc<MODE>, sm_count(), kThreads, smem, s, a, b, p);
+  return cudaGetLastError();
+}
+
+// 2-D bf16 tensor [rows, cols], box [box_rows, 64 cols], 128B swizzle (make_map).
+
+}  // namespace
+
+bool bwd_tc_supported(const moe_config &c) {
+  return c.act_dtype == MOE_BF16 && c.d % 64 == 0 && c.d_ff % 64 == 0 &&
+         bwd_smem_bytes(c.E) <= 227 * 1024 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  BParams p{};
+  p.mode = g.mode;
+  p.K = g.K;
+  p.N = g.N;
+  p.M = g.M;
+  p.E = g.E;
+  p.n_blocks = (g.N + BN - 1) / BN;
+  p.m_blocks = (g.M + BM - 1) / BM;
+  p.offset = g.offset;
+  p.poff = g.poff;
+  p.row_gate = g.row_gate;
+  p.hbuf = static_cast<const __nv_bfloat16 *>(g.hbuf);
+  p.out = g.out;
+  p.dgpart = g.dgpart;
+  p.st = st;
+  p.wait_ns = wait_limit_ns();
+  if (g.mode == 2) {
+    // A: the forward's packed rows [a_rows, M]; B: padded rows [b_rows, N].
+    if (!make_map(&ta, g.A, (uint64_t)g.a_rows, (uint64_t)g.M, 64) ||
+        !make_map(&tb, g.B, (uint64_t)g.b_rows, (uint64_t)g.N, 64))
+      return cudaErrorInvalidValue;
+    return launch_mode<2>(ta, tb, p, s);
+  }
+  // A: padded rows [a_rows, K]; B: the weight as [E*N rows, K].
+  if (!make_map(&ta, g.A, (uint64_t)g.a_rows, (uint64_t)g.K, BM) ||
+      !make_map(&tb, g.B, (uint64_t)g.E * g.N, (uint64_t)g.K, BN))
+    return cudaErrorInvalidValue;
+  return g.mode == 0 ? launch_mode<0>(ta, tb, p, s) : launch_mode<1>(ta, tb, p, s);
+}
+
+}  // namespace moe

@@ -280,6 +280,49 @@ static BalLayout bal_layout(const moe_config &cfg) {
   return L;
 }
 
+// ----------------------------------------------------------------------------- backward
+struct BwdLayout {
+  size_t poff, dY, dU, dP, dX, dgpart, dg, coef, dc, dz, dxr, rpart, bpart, cpart, total;
+  long long P_max;  // padded rows: T*k + 64*E bounds sum_e max(64, roundup(rows_e, 64))
+  int n_blocks2, chunks;
+};
+
+static BwdLayout bwd_layout(const moe_config &cfg) {
+  BwdLayout L{};
+  const size_t T = cfg.T, E = cfg.E, k = cfg.k, d = cfg.d, dff = cfg.d_ff;
+  L.P_max = (long long)T * k + (long long)kBwdRowPad * E;
+  const size_t P = (size_t)L.P_max;
+  L.n_blocks2 = (int)((dff + 255) / 256);
+  // Router-gradient partials: sized for the larger of the clean (E columns)
+  // and noisy (2E) cases, so the size does not depend on the noise arguments.
+  const size_t rp_c = (size_t)xtd_splits(cfg.T, cfg.d, cfg.E) * E;
+  const size_t rp_n = (size_t)xtd_splits(cfg.T, cfg.d, 2 * cfg.E) * 2 * E;
+  const size_t rp = rp_c > rp_n ? rp_c : rp_n;
+  L.chunks = colsum_chunks(host_capacity(cfg));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.poff = take((E + 1) * 4);
+  L.dY = take(P * d * 2);
+  L.dU = take(P * d * 2);
+  L.dP = take(P * dff * 2);
+  L.dX = take(P * d * 4);
+  L.dgpart = take(P * L.n_blocks2 * 4);
+  L.dg = take(T * k * 4);
+  L.coef = take(3 * E * 4);
+  L.dc = take(T * E * 4);
+  L.dz = take(T * E * 4);
+  L.dxr = take(T * d * 4);
+  L.rpart = take(rp * d * 4);
+  L.bpart = take(rp * 4);
+  L.cpart = take((size_t)L.chunks * E * (d > dff ? d : dff) * 4);
+  L.total = off;
+  return L;
+}
+
 // One side stream (non-blocking) and a fork / join event pair per device,
 // made on first use and kept; the lock is held while a call enqueues on them,
 // so calls from several host threads do not interleave their records.
@@ -629,6 +672,133 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
   // 4. y = x + the picks' outputs, and the loss.
   MOE_CUDA(launch_bal_combine(cr, L.m, x, zbuf, mask, row_token, trows, npick, y, st, s));
   if (loss_out) MOE_CUDA(launch_bal_loss(c.E, loss, loss_out, s));
+  return MOE_OK;
+}
+
+int moe_backward_workspace_size(const moe_config *cfg, size_t *bytes) {
+  const int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+// The gate's backward from the total gate gradients (dg_total) or from the
+// kept choices' <dy, U> plus the Importance term (coef), then the router's
+// weight gradients and its share of dx.
+static int gate_bwd_impl(const moe_config &c, const WsLayout &L, const BwdLayout &B, void *ws,
+                         void *bws, const void *x, const float *Wg, const float *Wn,
+                         const float *noise, const int32_t *idx, const float *g,
+                         const uint8_t *kp, const float *dg, bool dg_total, float w_imp,
+                         float w_load, float w_aux, float *dgate_out, float *dWg, float *dWn,
+                         float *dbias, float *dxr, cudaStream_t s) {
+  const bool noisy = Wn != nullptr;
+  const bool load_on = noisy && c.k < c.E && w_load != 0.f;
+  const bool aux_on = w_aux != 0.f;
+  float *coef = ws_at<float>(bws, B.coef);
+  MOE_CUDA(launch_bwd_coef(c, ws_at<float2>(ws, L.aux_vec), w_imp, w_load, w_aux, coef, s));
+  float *dc = ws_at<float>(bws, B.dc), *dz = ws_at<float>(bws, B.dz);
+  MOE_CUDA(launch_bwd_gate(c, noisy, load_on, aux_on, dg_total, ws_at<float>(ws, L.H),
+                           ws_at<float>(ws, L.c), ws_at<float>(ws, L.sigma), noise,
+                           ws_at<float>(ws, L.rowstat), ws_at<float>(ws, L.thr), idx, g, kp, dg,
+                           coef, dgate_out, dc, noisy ? dz : nullptr, s));
+  MOE_CUDA(launch_bwd_router(c, noisy, x, Wg, Wn, dc, noisy ? dz : nullptr,
+                             ws_at<float>(bws, B.rpart), ws_at<float>(bws, B.bpart), dWg, dWn,
+                             dbias, dxr, s));
+  return MOE_OK;
+}
+
+int moe_gate_backward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                      const float *noise, const int32_t *expert_idx, const float *gate,
+                      const float *dgate, float w_load, float w_aux, float *dWg, float *dWnoise,
+                      float *dlogit_bias, float *dx_gate, void *ws, void *bws,
+                      moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(Wnoise); MOE_OPT(noise); MOE_OPT(expert_idx); MOE_OPT(gate);
+  MOE_REQ(dgate); MOE_REQ(dWg); MOE_OPT(dWnoise); MOE_OPT(dlogit_bias); MOE_OPT(dx_gate);
+  if (!ws || !aligned(ws, 256) || !bws || !aligned(bws, 256)) return MOE_ERR_ARG;
+  if ((Wnoise == nullptr) != (noise == nullptr) || (Wnoise == nullptr) != (dWnoise == nullptr))
+    return MOE_ERR_ARG;
+  if (!isfinite(w_load) || !isfinite(w_aux)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  if (c.act_dtype != MOE_BF16 || c.d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(c);
+  const BwdLayout B = bwd_layout(c);
+  const int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
+  const float *g = gate ? gate : ws_at<float>(ws, L.gate);
+  return gate_bwd_impl(c, L, B, ws, bws, x, Wg, Wnoise, noise, idx, g, nullptr, dgate, true, 0.f,
+                       w_load, w_aux, nullptr, dWg, dWnoise, dlogit_bias, dx_gate,
+                       (cudaStream_t)stream);
+}
+
+int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
+                 const float *noise, const void *W1, const void *W2, const void *b2,
+                 const int32_t *expert_idx, const float *gate, const int32_t *pos,
+                 const uint8_t *keep, const void *dy, float w_importance, float w_load,
+                 float w_aux, void *dx, float *dWg, float *dWnoise, float *dlogit_bias,
+                 float *dW1, float *db1, float *dW2, float *db2, float *dgate, void *ws,
+                 void *bws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(Wnoise); MOE_OPT(noise); MOE_REQ(W1); MOE_REQ(W2);
+  MOE_OPT(b2); MOE_OPT(expert_idx); MOE_OPT(gate); MOE_OPT(pos); MOE_OPT(keep); MOE_REQ(dy);
+  MOE_REQ(dx); MOE_REQ(dWg); MOE_OPT(dWnoise); MOE_OPT(dlogit_bias); MOE_REQ(dW1); MOE_OPT(db1);
+  MOE_REQ(dW2); MOE_OPT(db2); MOE_OPT(dgate);
+  if (!ws || !aligned(ws, 256) || !bws || !aligned(bws, 256)) return MOE_ERR_ARG;
+  if ((Wnoise == nullptr) != (noise == nullptr) || (Wnoise == nullptr) != (dWnoise == nullptr))
+    return MOE_ERR_ARG;
+  if (!isfinite(w_importance) || !isfinite(w_load) || !isfinite(w_aux)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  if (!bwd_tc_supported(c)) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(c);
+  const BwdLayout B = bwd_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  const int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
+  const float *g = gate ? gate : ws_at<float>(ws, L.gate);
+  const int32_t *ps = pos ? pos : ws_at<int32_t>(ws, L.pos);
+  const uint8_t *kp = keep ? keep : ws_at<uint8_t>(ws, L.keep);
+  const int32_t *offset = ws_at<int32_t>(ws, L.offset);
+  const int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
+  const float *row_gate = ws_at<float>(ws, L.row_gate);
+  void *xbuf = ws_at<char>(ws, L.xbuf), *hbuf = ws_at<char>(ws, L.hbuf);
+  int32_t *poff = ws_at<int32_t>(bws, B.poff);
+  void *dY = ws_at<char>(bws, B.dY), *dU = ws_at<char>(bws, B.dU), *dP = ws_at<char>(bws, B.dP);
+  float *dX = ws_at<float>(bws, B.dX), *dgpart = ws_at<float>(bws, B.dgpart);
+  float *dg = ws_at<float>(bws, B.dg), *dxr = ws_at<float>(bws, B.dxr);
+  const long long A_rows = (long long)c.T * c.k;
+  // 1. Padded row blocks, finite K tails, the dy rows (plain and gate-scaled).
+  MOE_CUDA(launch_bwd_offsets(c.E, offset, poff, s));
+  MOE_CUDA(launch_bwd_tail_zero(c, offset, xbuf, hbuf, s));
+  MOE_CUDA(launch_bwd_gather(c, B.P_max, offset, poff, row_token, row_gate, dy, dY, dU, s));
+  // 2. Through W2: D = dY W2^T, the gate partials <D, h> and dpre = g D [h > 0];
+  //    through W1: dX = dpre W1^T.
+  BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, dY, W2, offset, poff, row_gate, hbuf, dP, dgpart};
+  MOE_CUDA(launch_bwd_gemm(g0, st, s));
+  BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
+             nullptr};
+  MOE_CUDA(launch_bwd_gemm(g1, st, s));
+  // 3. Weight gradients: dW2[e] = h^T (g dY), dW1[e] = x^T dpre; bias gradients.
+  BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, hbuf, dU, offset, poff, nullptr, nullptr,
+             dW2, nullptr};
+  MOE_CUDA(launch_bwd_gemm(g2, st, s));
+  BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, xbuf, dP, offset, poff, nullptr, nullptr,
+             dW1, nullptr};
+  MOE_CUDA(launch_bwd_gemm(g3, st, s));
+  float *cpart = ws_at<float>(bws, B.cpart);
+  if (db2)
+    MOE_CUDA(launch_bwd_colsum(c, c.d, B.chunks, offset, poff, row_gate, dY, cpart, db2, s));
+  if (db1)
+    MOE_CUDA(launch_bwd_colsum(c, c.d_ff, B.chunks, offset, poff, nullptr, dP, cpart, db1, s));
+  // 4. The gate: <dy, U> per kept choice, then the gate, load and Switch terms,
+  //    the router's weight gradients and its share of dx.
+  MOE_CUDA(launch_bwd_dg(c, B.n_blocks2, offset, poff, row_token, dgpart, dy, b2, dg, s));
+  r = gate_bwd_impl(c, L, B, ws, bws, x, Wg, Wnoise, noise, idx, g, kp, dg, false, w_importance,
+                    w_load, w_aux, dgate, dWg, dWnoise, dlogit_bias, dxr, s);
+  if (r != MOE_OK) return r;
+  // 5. dx = dy + the router's share + the kept experts' rows.
+  MOE_CUDA(launch_bwd_dx(c, idx, ps, kp, poff, dX, dxr, dy, dx, s));
   return MOE_OK;
 }
 

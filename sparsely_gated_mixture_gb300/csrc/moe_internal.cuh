@@ -215,4 +215,60 @@ cudaError_t launch_ffn_tc(const moe_config &cfg, int C, const void *xbuf, const 
                           bool z_bf16, DeviceStatus *st,
                           cudaStream_t s);  // z_bf16: Z in bf16 (else fp32)
 
+// ----------------------------------------------------------------------------- backward
+// Padded row blocks of the backward's row buffers: each expert's rows start at
+// poff[e] and take max(64, roundup(rows, 64)) rows, pad rows zero.
+constexpr int kBwdRowPad = 64;
+
+// k_bwd_tc.cu: the expert backward GEMMs on tcgen05. mode 0: D = dY W2^T with
+// the dgate partials and dpre (A = dY rows [a_rows, K = d], B = W2 as
+// [E*N, K], N = d_ff); mode 1: dX = dpre W1^T (A = dpre rows [a_rows, K =
+// d_ff], B = W1 as [E*N, K], N = d); mode 2: out[e] = A^T B over the padded
+// rows (A: the forward's packed rows [a_rows, M], B: padded rows [b_rows, N]).
+struct BwdGemm {
+  int mode, K, N, M, E;
+  long long a_rows, b_rows;
+  const void *A, *B;
+  const int32_t *offset, *poff;
+  const float *row_gate;
+  const void *hbuf;
+  void *out;
+  float *dgpart;
+};
+bool bwd_tc_supported(const moe_config &cfg);
+cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s);
+
+// k_bwd.cu: the CUDA-core kernels of the backward.
+int sm_count();  // multiprocessors of the current device (k_ffn_tc.cu)
+int xtd_splits(int T, int d, int NC);
+int colsum_chunks(int C);
+cudaError_t launch_bwd_offsets(int E, const int32_t *offset, int32_t *poff, cudaStream_t s);
+cudaError_t launch_bwd_tail_zero(const moe_config &c, const int32_t *offset, void *xbuf,
+                                 void *hbuf, cudaStream_t s);
+cudaError_t launch_bwd_gather(const moe_config &c, long long P_max, const int32_t *offset,
+                              const int32_t *poff, const int32_t *row_token,
+                              const float *row_gate, const void *dy, void *dY, void *dU,
+                              cudaStream_t s);
+cudaError_t launch_bwd_dg(const moe_config &c, int n_blocks, const int32_t *offset,
+                          const int32_t *poff, const int32_t *row_token, const float *dgpart,
+                          const void *dy, const void *b2, float *dg, cudaStream_t s);
+cudaError_t launch_bwd_coef(const moe_config &c, const float2 *aux_vec, float w_imp,
+                            float w_load, float w_aux, float *coef, cudaStream_t s);
+cudaError_t launch_bwd_gate(const moe_config &c, bool noisy, bool load_on, bool aux_on,
+                            bool dg_total, const float *H, const float *cc, const float *sigma,
+                            const float *noise, const float *rowstat, const float *thr,
+                            const int32_t *idx, const float *gate, const uint8_t *keep,
+                            const float *dg, const float *coef, float *dgate_out, float *dc,
+                            float *dz, cudaStream_t s);
+cudaError_t launch_bwd_router(const moe_config &c, bool noisy, const void *x, const float *Wg,
+                              const float *Wn, const float *dc, const float *dz, float *part,
+                              float *bpart, float *dWg, float *dWn, float *dbias, float *dxr,
+                              cudaStream_t s);
+cudaError_t launch_bwd_colsum(const moe_config &c, int cols, int chunks, const int32_t *offset,
+                              const int32_t *poff, const float *row_gate, const void *src,
+                              float *part, float *out, cudaStream_t s);
+cudaError_t launch_bwd_dx(const moe_config &c, const int32_t *idx, const int32_t *pos,
+                          const uint8_t *keep, const int32_t *poff, const float *dX,
+                          const float *dxr, const void *dy, void *dx, cudaStream_t s);
+
 }  // namespace moe

@@ -21,6 +21,9 @@ bf16 workloads round x, W1, W2, b1, b2 from fp32 to bf16 with
 round-to-nearest-even and keep the bit patterns as uint16; both sides of every
 comparison receive those same bits.
 
+The backward's upstream gradient dy ~ N(0, 1) [T, d] comes from a separate
+stream (``generate_dy``), rounded like x.
+
 Hierarchical layers (``HierWorkload``, a groups of b experts) draw, in order:
 x; W_p, W_pnoise ~ N(0, 1/d) [d, a] and noise_p ~ N(0, 1) [T, a] for the
 primary gate; W_s, W_snoise ~ N(0, 1/d) [d, a*b] and noise_s ~ N(0, 1)
@@ -199,6 +202,14 @@ def generate(w: Workload, seed: int = 0, biases: bool = False) -> dict:
     return dict(x=x, Wg=Wg, Wn=Wn, noise=noise, bias=bias, W1=W1, b1=b1, W2=W2, b2=b2,
                 k=w.k, cf=w.cf, min_cap=w.min_cap, mode=1 if w.mode == SWITCH else 0,
                 T=w.T, d=w.d, E=w.E, d_ff=w.d_ff)
+
+
+def generate_dy(w, seed: int = 0) -> np.ndarray:
+    """The upstream gradient for the backward: dy ~ N(0, 1) [T, d], drawn
+    from its own PCG64 stream (seed + 7919) and rounded to bf16 (uint16 bits)
+    for bf16 layers."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    return _normal(rng, (w.T, w.d), 1.0, w.dtype == "bf16")
 
 
 def generate_hier(w: HierWorkload, seed: int = 0, biases: bool = False) -> dict:

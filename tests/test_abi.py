@@ -142,3 +142,35 @@ def test_balanced_checks_on_host(lib):
     # NULL Wg
     assert lib.moe_forward_balanced(ctypes.byref(cfg), f, None, None, None, f, None, f, None, f,
                                     None, None, f, None) == 1
+
+
+def test_backward_checks_on_host(lib):
+    cfg = B.config(64, 64, 8, 128, 2, 1.25)
+    assert B.moe_backward_workspace_size(cfg) > 0
+    f = 1 << 20  # never dereferenced: the checks fail first
+    F = ctypes.c_float
+    #       x  Wg Wn    noise W1 W2 b2    idx   gate  pos   keep  dy
+    args = [f, f, None, None, f, f, None, None, None, None, None, f,
+            F(0.0), F(0.0), F(0.0),
+            #  dx dWg dWn  dbias dW1 db1  dW2 db2   dgate ws  bws stream
+            f, f, None, None, f, None, f, None, None, f, f, None]
+    bad = list(args)
+    bad[11] = None  # dy
+    assert lib.moe_backward(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[2], bad[3] = f, f  # noise weights without their gradient
+    assert lib.moe_backward(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[12] = F(float("nan"))  # loss weight
+    assert lib.moe_backward(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[25] = f + 16  # backward workspace not 256-byte aligned
+    assert lib.moe_backward(ctypes.byref(cfg), *bad) == 1
+    f32 = B.config(64, 64, 8, 128, 2, 1.25, act_dtype=B.MOE_F32)  # fp32: no backward yet
+    assert lib.moe_backward(ctypes.byref(f32), *args) == 2
+    #        x  Wg Wn    noise idx   gate  dgate wl      wa      dWg dWn   db    dxg   ws bws st
+    gargs = [f, f, None, None, None, None, f, F(0.0), F(0.0), f, None, None, None, f, f, None]
+    assert lib.moe_gate_backward(ctypes.byref(f32), *gargs) == 2
+    bad = list(gargs)
+    bad[6] = None  # dgate
+    assert lib.moe_gate_backward(ctypes.byref(cfg), *bad) == 1
