@@ -883,6 +883,196 @@ def run_balanced(args, w: wl.Workload):
     return line
 
 
+def fwd_launches(w: wl.Workload) -> int:
+    """Kernels one moe_forward launches (with the balancing losses)."""
+    tc_router = w.dtype == "bf16" and w.d % 8 == 0
+    fused_sel = (tc_router and (2 * w.E if w.noisy else w.E) <= 64 and w.E % 4 == 0
+                 and w.k <= 8)
+    return ((2 if tc_router else 1) + (0 if fused_sel else (1 if w.E <= 256 else 2))
+            + 3 + 1 + 2 + 1 + 1)
+
+
+# moe_backward: padded offsets, tail zero, dy gather, four expert GEMMs, two
+# bias column sums (two kernels each), dgate, loss coefficients, gate
+# backward, router weight gradients (two kernels) and dx share, dx.
+BWD_LAUNCHES = 18
+# Tokens of the oracle's backward in the CPU baseline: it zeroes and fills
+# fp64 weight gradients of the full layer, several seconds at the large-expert
+# widths, plus seconds per token.
+BWD_CPU_SAMPLE = 2
+
+
+def run_backward(args, w: wl.Workload):
+    """Training step of the layer: moe_forward (with the balancing losses)
+    then moe_backward (dy, loss weights 0.01 each), inputs resident, L2
+    flushed before each step; the two halves are also timed apart."""
+    import torch
+    import torch.distributed as dist
+
+    from sparsely_gated_mixture_gb300 import binding as B
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    if w.dtype != "bf16":
+        raise SystemExit("the backward runs on bf16 layers")
+    inp = wl.generate(w, seed=0, biases=True)
+    dy_bits = wl.generate_dy(w, 0)
+
+    def to_dev(a, is_act=False):
+        if a is None:
+            return None
+        if is_act:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    x, dy = to_dev(inp["x"], True), to_dev(dy_bits, True)
+    Wg, Wn, noise, bias = (to_dev(inp[n]) for n in ("Wg", "Wn", "noise", "bias"))
+    W1, b1, W2, b2 = (to_dev(inp[n], True) for n in ("W1", "b1", "W2", "b2"))
+    cfg = B.config_for(w)
+    T, E, d, dff, k = w.T, w.E, w.d, w.d_ff, w.k
+    z = dict(device=dev)
+    ws = torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, **z)
+    bws = torch.empty(B.moe_backward_workspace_size(cfg), dtype=torch.uint8, **z)
+    y = torch.empty((T, d), dtype=torch.bfloat16, **z)
+    out3 = torch.empty(3, dtype=torch.float32, **z)
+    keep = torch.empty((T, k), dtype=torch.uint8, **z)
+    f = lambda *sh: torch.empty(sh, dtype=torch.float32, **z)
+    grads = [torch.empty((T, d), dtype=torch.bfloat16, **z), f(d, E), f(d, E) if w.noisy else None,
+             f(E) if bias is not None else None, f(E, d, dff), f(E, dff), f(E, dff, d), f(E, d),
+             None]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, **z)
+    wts = (0.01, 0.01, 0.01)
+
+    def fwd(xx=x):
+        B.moe_forward(cfg, xx, Wg, Wn, noise, bias, W1, b1, W2, b2, y, out3, ws, None, None, None,
+                      keep, stream)
+
+    def bwd(xx=x, dyy=dy, gx=None):
+        g = list(grads)
+        if gx is not None:
+            g[0] = gx
+        B.moe_backward(cfg, xx, Wg, Wn, noise, W1, W2, b2, None, None, None, keep, dyy, *wts, *g,
+                       ws, bws, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st, det = B.moe_last_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det}) in the timed region")
+    step = [e[0].elapsed_time(e[2]) for e in ev]
+    ms = slowest_rank_ms(statistics.median(step), world, dev)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    accepted = int(keep.sum().item())
+
+    # End to end through the public calls: x and dy in from pinned host memory
+    # and dx back, every step (one buffer set; copies on the compute stream).
+    x_h, dy_h = x.cpu().pin_memory(), dy.cpu().pin_memory()
+    dx_h = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    x_d, dy_d, dx_d = torch.empty_like(x), torch.empty_like(dy), torch.empty_like(grads[0])
+
+    def step_e2e():
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        fwd(x_d)
+        bwd(x_d, dy_d, dx_d)
+        dx_h.copy_(dx_d, non_blocking=True)
+
+    for _ in range(3):
+        step_e2e()
+    torch.cuda.synchronize()
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
+    for _ in range(args.steps):
+        step_e2e()
+    b_ev.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(a_ev.elapsed_time(b_ev) / args.steps, world, dev)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return None
+    peaks, peak_kind = load_peaks()
+    # The backward's four expert GEMMs: dgrad through W2 and W1, wgrad of both,
+    # 2 * rows * d * d_ff multiply-adds each over the accepted rows.
+    bflops = 8.0 * accepted * d * dff
+    tf = bflops / (bwd_ms * 1e-3) / 1e12
+    roof = {"kernel": "moe_backward (four grouped GEMM launches plus the gate, router and "
+                      "row kernels), timed as one call",
+            "bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "peak_source": peak_kind,
+            "algorithmic_flops_per_launch": bflops, "traffic": None}
+    line = {
+        "metric": "MoE layer fwd+bwd (training step) tokens/s @1 GB300",
+        "value": job_tokens_per_s(world, T, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens and dy, N(0,1/fan_in) weights)",
+        "config": {"workload": w.name, "T": T, "d": d, "E": E, "d_ff": dff, "k": k,
+                   "loss_weights": list(wts), "seed": 0,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed between steps (256 MiB write)"},
+        "roofline": roof,
+        "stages": {"forward": {"ms": fwd_ms}, "backward": {"ms": bwd_ms},
+                   "accepted_rows": accepted},
+        "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x.numel() * x.element_size() + dy.numel() * dy.element_size(),
+                "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": (fwd_launches(w) + BWD_LAUNCHES) * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(w, inp, dy_bits, wts, BWD_CPU_SAMPLE)
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+def cpu_baseline_bwd(w: wl.Workload, inp: dict, dy_bits, wts, n_sample: int) -> dict:
+    """The oracle's backward as it stands on the host cores, on the first
+    n_sample tokens (a layer of n_sample tokens with the same weights),
+    scaled to tokens/s."""
+    import oracle
+
+    cores = 1  # orc_backward runs on one thread (its router pass uses OpenMP)
+    n = min(n_sample, w.T)
+    sub = dict(inp)
+    for key in ("x", "noise"):
+        if sub.get(key) is not None:
+            sub[key] = np.ascontiguousarray(sub[key][:n])
+    dy = wl.bf16_bits_to_f32(dy_bits[:n]).astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.backward(sub, dy, *wts)
+    t = time.perf_counter() - t0
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"the oracle's forward and backward of the first {n} tokens "
+                      f"({t:.2f} s), as a layer of {n} tokens"}
+
+
 def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int) -> dict:
     """The oracle's balanced layer on the host cores: router, softmax and the
     batchwise mask over every token, the expert loop for n_sample tokens,
@@ -1024,6 +1214,8 @@ def main():
                     help="override T (smaller cases for profiler captures)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller cases for profiler captures)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the training step (moe_forward then moe_backward)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     if args.workload in wl.HIER_WORKLOADS:
@@ -1064,6 +1256,31 @@ def main():
         w = w.with_(T=args.tokens)
     if args.experts:
         w = w.with_(E=args.experts)
+    if args.backward:
+        if args.impl == "reference":
+            rank, world, _ = dist_env()
+            if rank == 0:
+                inp = wl.generate(w, seed=0, biases=True)
+                dyb = wl.generate_dy(w, 0)
+                # each sample takes tens of seconds at the large-expert widths
+                vals = [cpu_baseline_bwd(w, inp, dyb, (0.01, 0.01, 0.01), BWD_CPU_SAMPLE)
+                        for _ in range(min(args.steps, 3))]
+                v = statistics.mean(x["value"] for x in vals)
+                print(json.dumps({
+                    "impl": "reference", "metric": "MoE layer fwd+bwd (training step) tokens/s "
+                    "@1 GB300", "value": v, "unit": "tokens/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.T / v * 1e3,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": w.name, "T": w.T, "parallelism": "host cores"},
+                    "cpu_baseline": dict(vals[-1], value=v),
+                    "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}), flush=True)
+            return
+        line = run_backward(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     line = run_reference(args, w) if args.impl == "reference" else run_ours(args, w)
     if line is not None:
         print(json.dumps(line), flush=True)

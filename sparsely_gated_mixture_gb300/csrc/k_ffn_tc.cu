@@ -337,32 +337,6 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-  return out;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
-                                                 uint32_t bar_cluster_addr, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"((uint64_t)map), "r"(bar_cluster_addr), "r"(x), "r"(y)
-      : "memory");
-}
 __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -370,15 +344,6 @@ __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t 
       "l"(a), "l"(b), "r"(kIdescPair), "r"(acc)
       : "memory");
 }
-// Arrives on the barrier at this offset in every CTA of `mask` (bit = cluster rank).
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask = 0x3) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -768,22 +768,23 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
   float *dX = ws_at<float>(bws, B.dX), *dgpart = ws_at<float>(bws, B.dgpart);
   float *dg = ws_at<float>(bws, B.dg), *dxr = ws_at<float>(bws, B.dxr);
   const long long A_rows = (long long)c.T * c.k;
+  const long long cap = host_capacity(c);  // rows per expert at most
   // 1. Padded row blocks, finite K tails, the dy rows (plain and gate-scaled).
   MOE_CUDA(launch_bwd_offsets(c.E, offset, poff, s));
   MOE_CUDA(launch_bwd_tail_zero(c, offset, xbuf, hbuf, s));
   MOE_CUDA(launch_bwd_gather(c, B.P_max, offset, poff, row_token, row_gate, dy, dY, dU, s));
   // 2. Through W2: D = dY W2^T, the gate partials <D, h> and dpre = g D [h > 0];
   //    through W1: dX = dpre W1^T.
-  BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, dY, W2, offset, poff, row_gate, hbuf, dP, dgpart};
+  BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, 0, dY, W2, offset, poff, row_gate, hbuf, dP, dgpart};
   MOE_CUDA(launch_bwd_gemm(g0, st, s));
-  BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
+  BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
              nullptr};
   MOE_CUDA(launch_bwd_gemm(g1, st, s));
   // 3. Weight gradients: dW2[e] = h^T (g dY), dW1[e] = x^T dpre; bias gradients.
-  BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, hbuf, dU, offset, poff, nullptr, nullptr,
+  BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, cap, hbuf, dU, offset, poff, nullptr, nullptr,
              dW2, nullptr};
   MOE_CUDA(launch_bwd_gemm(g2, st, s));
-  BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, xbuf, dP, offset, poff, nullptr, nullptr,
+  BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, cap, xbuf, dP, offset, poff, nullptr, nullptr,
              dW1, nullptr};
   MOE_CUDA(launch_bwd_gemm(g3, st, s));
   float *cpart = ws_at<float>(bws, B.cpart);

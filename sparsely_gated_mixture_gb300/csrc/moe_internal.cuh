@@ -228,6 +228,7 @@ constexpr int kBwdRowPad = 64;
 struct BwdGemm {
   int mode, K, N, M, E;
   long long a_rows, b_rows;
+  long long k_len;  // mode 2: rows per expert to expect (for the kernel choice)
   const void *A, *B;
   const int32_t *offset, *poff;
   const float *row_gate;

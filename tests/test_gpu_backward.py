@@ -192,8 +192,13 @@ def _check(got, ref, lim, what, norm=True):
         assert np.linalg.norm(got - ref) <= 2e-2 * nr + 1e-6, (what, np.linalg.norm(got - ref), nr)
 
 
+@pytest.mark.parametrize("variant", ["auto", "single", "pair"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_backward_matches_oracle(name):
+def test_backward_matches_oracle(name, variant, monkeypatch):
+    """variant: the expert GEMMs' kernel as the library picks it, or forced
+    to the one-CTA or the CTA-pair form."""
+    if variant != "auto":
+        monkeypatch.setenv("MOE_BWD_TC_VARIANT", variant)
     w, weights = CASES[name]
     seed = 11
     inp = wl.generate(w, seed=seed, biases=True)
