@@ -701,12 +701,19 @@ cudaError_t launch_bwd_colsum(const moe_config &c, int cols, int chunks, const i
                     cols, chunks, (const float *)part, out);
 }
 
+// Launched in plain stream order (no programmatic dependent launch): it
+// follows a join with the side stream, whose results (the router's share of
+// dx) it reads.
 cudaError_t launch_bwd_dx(const moe_config &c, const int32_t *idx, const int32_t *pos,
                           const uint8_t *keep, const int32_t *poff, const float *dX,
                           const float *dxr, const void *dy, void *dx, cudaStream_t s) {
-  return launch_pdl(k_bwd_dx, grid_for(c.T, 8), 256, 0, s, c.T, c.d, c.k, idx, pos, keep, poff,
-                    dX, dxr, static_cast<const __nv_bfloat16 *>(dy),
-                    static_cast<__nv_bfloat16 *>(dx));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(c.T, 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, k_bwd_dx, c.T, c.d, c.k, idx, pos, keep, poff, dX, dxr,
+                            static_cast<const __nv_bfloat16 *>(dy),
+                            static_cast<__nv_bfloat16 *>(dx));
 }
 
 }  // namespace moe

@@ -777,28 +777,46 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
   //    through W1: dX = dpre W1^T.
   BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, 0, dY, W2, offset, poff, row_gate, hbuf, dP, dgpart};
   MOE_CUDA(launch_bwd_gemm(g0, st, s));
+  // From here two independent branches. On the side stream (the library's,
+  // as in moe_forward; `stream` itself if none could be made): the gate's
+  // backward from the dgate partials -- <dy, U> per kept choice, the gate,
+  // load and Switch terms, the router's weight gradients and its share of dx
+  // -- and the bias column sums. Their small kernels fit beside the
+  // persistent GEMM CTAs of the other branch, which stays on `stream`.
+  SideStream *side = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  side = side_stream(side_lock);
+  cudaStream_t fs = s;
+  if (side) {
+    MOE_CUDA(cudaEventRecord(side->fork, s));
+    MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    fs = side->s;
+  }
+  MOE_CUDA(launch_bwd_dg(c, B.n_blocks2, offset, poff, row_token, dgpart, dy, b2, dg, fs));
+  r = gate_bwd_impl(c, L, B, ws, bws, x, Wg, Wnoise, noise, idx, g, kp, dg, false, w_importance,
+                    w_load, w_aux, dgate, dWg, dWnoise, dlogit_bias, dxr, fs);
+  if (r != MOE_OK) return r;
+  float *cpart = ws_at<float>(bws, B.cpart);
+  if (db2)
+    MOE_CUDA(launch_bwd_colsum(c, c.d, B.chunks, offset, poff, row_gate, dY, cpart, db2, fs));
+  if (db1)
+    MOE_CUDA(launch_bwd_colsum(c, c.d_ff, B.chunks, offset, poff, nullptr, dP, cpart, db1, fs));
+  // 3. Through W1: dX = dpre W1^T; weight gradients dW2[e] = h^T (g dY),
+  //    dW1[e] = x^T dpre.
   BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
              nullptr};
   MOE_CUDA(launch_bwd_gemm(g1, st, s));
-  // 3. Weight gradients: dW2[e] = h^T (g dY), dW1[e] = x^T dpre; bias gradients.
   BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, cap, hbuf, dU, offset, poff, nullptr, nullptr,
              dW2, nullptr};
   MOE_CUDA(launch_bwd_gemm(g2, st, s));
   BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, cap, xbuf, dP, offset, poff, nullptr, nullptr,
              dW1, nullptr};
   MOE_CUDA(launch_bwd_gemm(g3, st, s));
-  float *cpart = ws_at<float>(bws, B.cpart);
-  if (db2)
-    MOE_CUDA(launch_bwd_colsum(c, c.d, B.chunks, offset, poff, row_gate, dY, cpart, db2, s));
-  if (db1)
-    MOE_CUDA(launch_bwd_colsum(c, c.d_ff, B.chunks, offset, poff, nullptr, dP, cpart, db1, s));
-  // 4. The gate: <dy, U> per kept choice, then the gate, load and Switch terms,
-  //    the router's weight gradients and its share of dx.
-  MOE_CUDA(launch_bwd_dg(c, B.n_blocks2, offset, poff, row_token, dgpart, dy, b2, dg, s));
-  r = gate_bwd_impl(c, L, B, ws, bws, x, Wg, Wnoise, noise, idx, g, kp, dg, false, w_importance,
-                    w_load, w_aux, dgate, dWg, dWnoise, dlogit_bias, dxr, s);
-  if (r != MOE_OK) return r;
-  // 5. dx = dy + the router's share + the kept experts' rows.
+  if (side) {
+    MOE_CUDA(cudaEventRecord(side->join, side->s));
+    MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
+  }
+  // 4. dx = dy + the router's share + the kept experts' rows.
   MOE_CUDA(launch_bwd_dx(c, idx, ps, kp, poff, dX, dxr, dy, dx, s));
   return MOE_OK;
 }
