@@ -300,9 +300,11 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
  * nonzero (the backward reads its balancing totals). The call may overwrite
  * `ws` rows past the forward's last expert row; it leaves the forward's other
  * results unchanged, so it may be repeated with another dy.
- * Supported: act_dtype MOE_BF16 with d and d_ff multiples of 64 (the
- * tensor-core path); else MOE_ERR_UNSUPPORTED.
- * Inputs: dy [T,d] bf16. Outputs (fp32 unless stated): dx [T,d] bf16; dWg
+ * Every configuration moe_forward takes: bf16 layers with d and d_ff
+ * multiples of 64 run the expert GEMMs on the tensor cores, the others
+ * (fp32 layers, other widths) on the CUDA cores with fp32 row buffers.
+ * Inputs: dy [T,d] act_dtype. Outputs (fp32 unless stated): dx [T,d]
+ * act_dtype; dWg
  * [d,E]; dWnoise [d,E] (required iff Wnoise is given); dlogit_bias [E] (may
  * be NULL); dW1 [E,d,d_ff]; db1 [E,d_ff] (may be NULL); dW2 [E,d_ff,d]; db2
  * [E,d] (may be NULL); dgate [T,k] (may be NULL) = dL/dgate of each selected
@@ -328,7 +330,7 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
  * weights w_load, w_aux (these need the balancing totals of moe_aux_loss or
  * of moe_forward with aux_out3). Outputs: dWg [d,E], dWnoise [d,E] (iff
  * Wnoise), dlogit_bias [E] (may be NULL), dx_gate [T,d] (may be NULL): the
- * router's share of dx, all fp32. x [T,d] bf16; bws as for moe_backward.
+ * router's share of dx, all fp32. x [T,d] act_dtype; bws as for moe_backward.
  */
 int moe_gate_backward(const moe_config *cfg, const void *x, const float *Wg, const float *Wnoise,
                       const float *noise, const int32_t *expert_idx, const float *gate,

@@ -393,8 +393,12 @@ __global__ void __launch_bounds__(256) k_bwd_gate(const GateBwd p) {
 // the blocks of the first i tile also sum the columns of D (the bias).
 constexpr int kXtdTI = 64, kXtdTC = 32, kXtdTT = 32;
 
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f(float v) { return v; }
+
+template <typename XT>
 __global__ void __launch_bounds__(256)
-k_bwd_xtd(int T, int d, int E, int NC, int tpc, const __nv_bfloat16 *__restrict__ x,
+k_bwd_xtd(int T, int d, int E, int NC, int tpc, const XT *__restrict__ x,
           const float *__restrict__ dc, const float *__restrict__ dz, float *__restrict__ part,
           float *__restrict__ bpart) {
   pdl_wait();
@@ -409,7 +413,7 @@ k_bwd_xtd(int T, int d, int E, int NC, int tpc, const __nv_bfloat16 *__restrict_
     for (int u = threadIdx.x; u < kXtdTT * kXtdTI; u += 256) {
       const int tt = u / kXtdTI, ii = u % kXtdTI;
       const int t = tb + tt, i = i0 + ii;
-      xs[tt][ii] = (t < t_end && i < d) ? __bfloat162float(x[(size_t)t * d + i]) : 0.f;
+      xs[tt][ii] = (t < t_end && i < d) ? to_f(x[(size_t)t * d + i]) : 0.f;
     }
     for (int u = threadIdx.x; u < kXtdTT * kXtdTC; u += 256) {
       const int tt = u / kXtdTC, cc = u % kXtdTC;
@@ -531,10 +535,11 @@ k_bwd_dxr(int T, int d, int E, int NC, const float *__restrict__ dc, const float
 // chunks of 128 rows, then the chunks in order.
 constexpr int kColRows = 128;
 
+template <typename S>
 __global__ void __launch_bounds__(256)
 k_bwd_colsum(int E, int cols, int chunks, const int32_t *__restrict__ offset,
              const int32_t *__restrict__ poff, const float *__restrict__ row_gate,
-             const __nv_bfloat16 *__restrict__ src, float *__restrict__ part) {
+             const S *__restrict__ src, float *__restrict__ part) {
   pdl_wait();
   const int c = blockIdx.x * 256 + threadIdx.x, e = blockIdx.y, ch = blockIdx.z;
   if (c < cols) {
@@ -542,7 +547,7 @@ k_bwd_colsum(int E, int cols, int chunks, const int32_t *__restrict__ offset,
     const int m0 = ch * kColRows, m1 = min(rows, m0 + kColRows);
     float s = 0.f;
     for (int m = m0; m < m1; ++m) {
-      const float v = __bfloat162float(src[((size_t)poff[e] + m) * cols + c]);
+      const float v = to_f(src[((size_t)poff[e] + m) * cols + c]);
       s = row_gate ? fmaf(row_gate[offset[e] + m], v, s) : s + v;
     }
     part[((size_t)ch * E + e) * cols + c] = s;
@@ -679,8 +684,12 @@ cudaError_t launch_bwd_router(const moe_config &c, bool noisy, const void *x, co
   const int S = xtd_splits(c.T, c.d, NC);  // part holds S * d * NC, bpart S * NC floats
   const int tpc = ((c.T + S - 1) / S + kXtdTT - 1) / kXtdTT * kXtdTT;
   const dim3 g1((c.d + kXtdTI - 1) / kXtdTI, (NC + kXtdTC - 1) / kXtdTC, S);
-  cudaError_t err = launch_pdl(k_bwd_xtd, g1, 256, 0, s, c.T, c.d, c.E, NC, tpc,
-                               static_cast<const __nv_bfloat16 *>(x), dc, dz, part, bpart);
+  cudaError_t err =
+      c.act_dtype == MOE_BF16
+          ? launch_pdl(k_bwd_xtd<__nv_bfloat16>, g1, 256, 0, s, c.T, c.d, c.E, NC, tpc,
+                       static_cast<const __nv_bfloat16 *>(x), dc, dz, part, bpart)
+          : launch_pdl(k_bwd_xtd<float>, g1, 256, 0, s, c.T, c.d, c.E, NC, tpc,
+                       static_cast<const float *>(x), dc, dz, part, bpart);
   if (err != cudaSuccess) return err;
   err = launch_pdl(k_bwd_xtd_reduce, grid_for((long long)c.d * NC + NC, 256), 256, 0, s, c.d,
                    c.E, NC, S, (const float *)part, (const float *)bpart, dWg, dWn, dbias);
@@ -692,10 +701,13 @@ cudaError_t launch_bwd_router(const moe_config &c, bool noisy, const void *x, co
 
 cudaError_t launch_bwd_colsum(const moe_config &c, int cols, int chunks, const int32_t *offset,
                               const int32_t *poff, const float *row_gate, const void *src,
-                              float *part, float *out, cudaStream_t s) {
+                              bool src_f32, float *part, float *out, cudaStream_t s) {
   const dim3 g((cols + 255) / 256, c.E, chunks);
-  cudaError_t err = launch_pdl(k_bwd_colsum, g, 256, 0, s, c.E, cols, chunks, offset, poff,
-                               row_gate, static_cast<const __nv_bfloat16 *>(src), part);
+  cudaError_t err =
+      src_f32 ? launch_pdl(k_bwd_colsum<float>, g, 256, 0, s, c.E, cols, chunks, offset, poff,
+                           row_gate, static_cast<const float *>(src), part)
+              : launch_pdl(k_bwd_colsum<__nv_bfloat16>, g, 256, 0, s, c.E, cols, chunks, offset,
+                           poff, row_gate, static_cast<const __nv_bfloat16 *>(src), part);
   if (err != cudaSuccess) return err;
   return launch_pdl(k_bwd_colsum_reduce, grid_for((long long)c.E * cols, 256), 256, 0, s, c.E,
                     cols, chunks, (const float *)part, out);

@@ -287,12 +287,20 @@ struct BwdLayout {
   int n_blocks2, chunks;
 };
 
+// The expert backward runs on the tensor cores for bf16 layers whose widths
+// are multiples of 64, else on the CUDA cores (fp32 row buffers).
+static bool bwd_tc_shape(const moe_config &c) {
+  return c.act_dtype == MOE_BF16 && c.d % 64 == 0 && c.d_ff % 64 == 0;
+}
+
 static BwdLayout bwd_layout(const moe_config &cfg) {
   BwdLayout L{};
   const size_t T = cfg.T, E = cfg.E, k = cfg.k, d = cfg.d, dff = cfg.d_ff;
+  const bool tc = bwd_tc_shape(cfg);
+  const size_t rb = tc ? 2 : 4;  // bytes per element of the dY, g*dY and dpre rows
   L.P_max = (long long)T * k + (long long)kBwdRowPad * E;
   const size_t P = (size_t)L.P_max;
-  L.n_blocks2 = (int)((dff + 255) / 256);
+  L.n_blocks2 = tc ? (int)((dff + 255) / 256) : simt_dgate_blocks(cfg);
   // Router-gradient partials: sized for the larger of the clean (E columns)
   // and noisy (2E) cases, so the size does not depend on the noise arguments.
   const size_t rp_c = (size_t)xtd_splits(cfg.T, cfg.d, cfg.E) * E;
@@ -306,9 +314,9 @@ static BwdLayout bwd_layout(const moe_config &cfg) {
     return o;
   };
   L.poff = take((E + 1) * 4);
-  L.dY = take(P * d * 2);
-  L.dU = take(P * d * 2);
-  L.dP = take(P * dff * 2);
+  L.dY = take(P * d * rb);
+  L.dU = take(P * d * rb);
+  L.dP = take(P * dff * rb);
   L.dX = take(P * d * 4);
   L.dgpart = take(P * L.n_blocks2 * 4);
   L.dg = take(T * k * 4);
@@ -722,7 +730,6 @@ int moe_gate_backward(const moe_config *cfg, const void *x, const float *Wg, con
     return MOE_ERR_ARG;
   if (!isfinite(w_load) || !isfinite(w_aux)) return MOE_ERR_ARG;
   const moe_config &c = *cfg;
-  if (c.act_dtype != MOE_BF16 || c.d % 8 != 0) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(c);
   const BwdLayout B = bwd_layout(c);
   const int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
@@ -750,7 +757,8 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
     return MOE_ERR_ARG;
   if (!isfinite(w_importance) || !isfinite(w_load) || !isfinite(w_aux)) return MOE_ERR_ARG;
   const moe_config &c = *cfg;
-  if (!bwd_tc_supported(c)) return MOE_ERR_UNSUPPORTED;
+  const bool tc = bwd_tc_shape(c);
+  if (tc && !bwd_tc_supported(c)) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(c);
   const BwdLayout B = bwd_layout(c);
   cudaStream_t s = (cudaStream_t)stream;
@@ -769,14 +777,22 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
   float *dg = ws_at<float>(bws, B.dg), *dxr = ws_at<float>(bws, B.dxr);
   const long long A_rows = (long long)c.T * c.k;
   const long long cap = host_capacity(c);  // rows per expert at most
-  // 1. Padded row blocks, finite K tails, the dy rows (plain and gate-scaled).
+  // CUDA-core form (fp32 rows): the same steps, in k_bwd_simt.cu.
+  const BwdSimt sp{B.P_max, offset, poff, row_token, row_gate, dy, W1, W2, b2, xbuf, hbuf,
+                   static_cast<float *>(dY), static_cast<float *>(dU), static_cast<float *>(dP),
+                   dX, dgpart, dW1, dW2, st};
+  // 1. Padded row blocks, finite K tails, the dy rows (plain and gate-scaled);
+  // 2. through W2: D = dY W2^T, the gate partials <D, h> and dpre = g D [h > 0].
   MOE_CUDA(launch_bwd_offsets(c.E, offset, poff, s));
-  MOE_CUDA(launch_bwd_tail_zero(c, offset, xbuf, hbuf, s));
-  MOE_CUDA(launch_bwd_gather(c, B.P_max, offset, poff, row_token, row_gate, dy, dY, dU, s));
-  // 2. Through W2: D = dY W2^T, the gate partials <D, h> and dpre = g D [h > 0];
-  //    through W1: dX = dpre W1^T.
-  BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, 0, dY, W2, offset, poff, row_gate, hbuf, dP, dgpart};
-  MOE_CUDA(launch_bwd_gemm(g0, st, s));
+  if (tc) {
+    MOE_CUDA(launch_bwd_tail_zero(c, offset, xbuf, hbuf, s));
+    MOE_CUDA(launch_bwd_gather(c, B.P_max, offset, poff, row_token, row_gate, dy, dY, dU, s));
+    BwdGemm g0{0, c.d, c.d_ff, 0, c.E, B.P_max, 0, 0, dY, W2, offset, poff, row_gate, hbuf, dP,
+               dgpart};
+    MOE_CUDA(launch_bwd_gemm(g0, st, s));
+  } else {
+    MOE_CUDA(launch_bwd_simt_front(c, sp, s));
+  }
   // From here two independent branches. On the side stream (the library's,
   // as in moe_forward; `stream` itself if none could be made): the gate's
   // backward from the dgate partials -- <dy, U> per kept choice, the gate,
@@ -792,32 +808,44 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
     MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
     fs = side->s;
   }
-  MOE_CUDA(launch_bwd_dg(c, B.n_blocks2, offset, poff, row_token, dgpart, dy, b2, dg, fs));
+  if (tc)
+    MOE_CUDA(launch_bwd_dg(c, B.n_blocks2, offset, poff, row_token, dgpart, dy, b2, dg, fs));
+  else
+    MOE_CUDA(launch_bwd_simt_dg(c, sp, dg, fs));
   r = gate_bwd_impl(c, L, B, ws, bws, x, Wg, Wnoise, noise, idx, g, kp, dg, false, w_importance,
                     w_load, w_aux, dgate, dWg, dWnoise, dlogit_bias, dxr, fs);
   if (r != MOE_OK) return r;
   float *cpart = ws_at<float>(bws, B.cpart);
   if (db2)
-    MOE_CUDA(launch_bwd_colsum(c, c.d, B.chunks, offset, poff, row_gate, dY, cpart, db2, fs));
+    MOE_CUDA(launch_bwd_colsum(c, c.d, B.chunks, offset, poff, row_gate, dY, !tc, cpart, db2,
+                               fs));
   if (db1)
-    MOE_CUDA(launch_bwd_colsum(c, c.d_ff, B.chunks, offset, poff, nullptr, dP, cpart, db1, fs));
+    MOE_CUDA(launch_bwd_colsum(c, c.d_ff, B.chunks, offset, poff, nullptr, dP, !tc, cpart, db1,
+                               fs));
   // 3. Through W1: dX = dpre W1^T; weight gradients dW2[e] = h^T (g dY),
   //    dW1[e] = x^T dpre.
-  BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
-             nullptr};
-  MOE_CUDA(launch_bwd_gemm(g1, st, s));
-  BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, cap, hbuf, dU, offset, poff, nullptr, nullptr,
-             dW2, nullptr};
-  MOE_CUDA(launch_bwd_gemm(g2, st, s));
-  BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, cap, xbuf, dP, offset, poff, nullptr, nullptr,
-             dW1, nullptr};
-  MOE_CUDA(launch_bwd_gemm(g3, st, s));
+  if (tc) {
+    BwdGemm g1{1, c.d_ff, c.d, 0, c.E, B.P_max, 0, 0, dP, W1, offset, poff, nullptr, nullptr, dX,
+               nullptr};
+    MOE_CUDA(launch_bwd_gemm(g1, st, s));
+    BwdGemm g2{2, 0, c.d, c.d_ff, c.E, A_rows, B.P_max, cap, hbuf, dU, offset, poff, nullptr,
+               nullptr, dW2, nullptr};
+    MOE_CUDA(launch_bwd_gemm(g2, st, s));
+    BwdGemm g3{2, 0, c.d_ff, c.d, c.E, A_rows, B.P_max, cap, xbuf, dP, offset, poff, nullptr,
+               nullptr, dW1, nullptr};
+    MOE_CUDA(launch_bwd_gemm(g3, st, s));
+  } else {
+    MOE_CUDA(launch_bwd_simt_back(c, sp, s));
+  }
   if (side) {
     MOE_CUDA(cudaEventRecord(side->join, side->s));
     MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   }
   // 4. dx = dy + the router's share + the kept experts' rows.
-  MOE_CUDA(launch_bwd_dx(c, idx, ps, kp, poff, dX, dxr, dy, dx, s));
+  if (tc)
+    MOE_CUDA(launch_bwd_dx(c, idx, ps, kp, poff, dX, dxr, dy, dx, s));
+  else
+    MOE_CUDA(launch_bwd_simt_dx(c, sp, idx, ps, kp, dxr, dx, s));
   return MOE_OK;
 }
 

@@ -239,6 +239,26 @@ struct BwdGemm {
 bool bwd_tc_supported(const moe_config &cfg);
 cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s);
 
+// k_bwd_simt.cu: the expert backward on the CUDA cores (fp32 layers, and bf16
+// shapes the tensor-core kernels do not take); its row buffers are fp32.
+struct BwdSimt {
+  long long P_max;
+  const int32_t *offset, *poff, *row_token;
+  const float *row_gate;
+  const void *dy, *W1, *W2, *b2, *xbuf, *hbuf;
+  float *dY, *dU, *dP, *dX, *dgpart, *dW1, *dW2;
+  DeviceStatus *st;
+};
+int simt_dgate_blocks(const moe_config &c);  // column blocks of the dgate partials
+// gather and the dgrad through W2 (dpre, dgate partials)
+cudaError_t launch_bwd_simt_front(const moe_config &c, const BwdSimt &p, cudaStream_t s);
+// the dgrad through W1 and both weight gradients
+cudaError_t launch_bwd_simt_back(const moe_config &c, const BwdSimt &p, cudaStream_t s);
+cudaError_t launch_bwd_simt_dg(const moe_config &c, const BwdSimt &p, float *dg, cudaStream_t s);
+cudaError_t launch_bwd_simt_dx(const moe_config &c, const BwdSimt &p, const int32_t *idx,
+                               const int32_t *pos, const uint8_t *keep, const float *dxr,
+                               void *dx, cudaStream_t s);
+
 // k_bwd.cu: the CUDA-core kernels of the backward.
 int sm_count();  // multiprocessors of the current device (k_ffn_tc.cu)
 int xtd_splits(int T, int d, int NC);
@@ -261,13 +281,15 @@ cudaError_t launch_bwd_gate(const moe_config &c, bool noisy, bool load_on, bool 
                             const int32_t *idx, const float *gate, const uint8_t *keep,
                             const float *dg, const float *coef, float *dgate_out, float *dc,
                             float *dz, cudaStream_t s);
+// x is act_dtype (bf16 or fp32).
 cudaError_t launch_bwd_router(const moe_config &c, bool noisy, const void *x, const float *Wg,
                               const float *Wn, const float *dc, const float *dz, float *part,
                               float *bpart, float *dWg, float *dWn, float *dbias, float *dxr,
                               cudaStream_t s);
+// src rows are bf16, or fp32 when src_f32.
 cudaError_t launch_bwd_colsum(const moe_config &c, int cols, int chunks, const int32_t *offset,
                               const int32_t *poff, const float *row_gate, const void *src,
-                              float *part, float *out, cudaStream_t s);
+                              bool src_f32, float *part, float *out, cudaStream_t s);
 cudaError_t launch_bwd_dx(const moe_config &c, const int32_t *idx, const int32_t *pos,
                           const uint8_t *keep, const int32_t *poff, const float *dX,
                           const float *dxr, const void *dy, void *dx, cudaStream_t s);

@@ -166,11 +166,16 @@ def test_backward_checks_on_host(lib):
     bad = list(args)
     bad[25] = f + 16  # backward workspace not 256-byte aligned
     assert lib.moe_backward(ctypes.byref(cfg), *bad) == 1
-    f32 = B.config(64, 64, 8, 128, 2, 1.25, act_dtype=B.MOE_F32)  # fp32: no backward yet
-    assert lib.moe_backward(ctypes.byref(f32), *args) == 2
+    f32 = B.config(64, 64, 8, 128, 2, 1.25, act_dtype=B.MOE_F32)
+    assert B.moe_backward_workspace_size(f32) > B.moe_backward_workspace_size(cfg)  # fp32 rows
+    bad = list(args)
+    bad[15] = None  # dx
+    assert lib.moe_backward(ctypes.byref(f32), *bad) == 1
     #        x  Wg Wn    noise idx   gate  dgate wl      wa      dWg dWn   db    dxg   ws bws st
     gargs = [f, f, None, None, None, None, f, F(0.0), F(0.0), f, None, None, None, f, f, None]
-    assert lib.moe_gate_backward(ctypes.byref(f32), *gargs) == 2
+    bad = list(gargs)
+    bad[9] = None  # dWg
+    assert lib.moe_gate_backward(ctypes.byref(f32), *bad) == 1
     bad = list(gargs)
     bad[6] = None  # dgate
     assert lib.moe_gate_backward(ctypes.byref(cfg), *bad) == 1
