@@ -84,3 +84,19 @@ def test_reference_arm_widened_workloads(workload):
     assert rec["impl"] == "reference" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["config"]["workload"] == workload
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_training_step():
+    """bench.py --backward --impl reference: the oracle's forward and backward
+    on a bounded token sample print one well-formed JSON line."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--backward",
+           "--steps", "1", "--warmup", "1", "--workload", "noisy_top4_e16"]
+    p = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["value"] > 0
+    assert "fwd+bwd" in rec["metric"] and rec["cpu_baseline"]["kind"] == "oracle"
+    assert rec["config"]["workload"] == "noisy_top4_e16"
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
