@@ -1,6 +1,7 @@
 /*
  * moe.h -- C ABI of libmoe.so: the forward path of the sparsely-gated
- * Mixture-of-Experts layer on one NVIDIA GB300 (sm_103a).
+ * Mixture-of-Experts layer on one NVIDIA GB300 (sm_103a), its hierarchical
+ * and strictly balanced variants, and the flat layer's backward.
  *
  * The layer, as the pages state it ("Outrageously Large Neural Networks: The
  * Sparsely-Gated Mixture-of-Experts Layer", section 3.4; "Switch Transformer",
