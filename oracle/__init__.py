@@ -125,6 +125,9 @@ class Oracle:
         lib.orc_backward.argtypes = [I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, P, I,
                                      P, D, D, D, P, P, P, P, P, P, P, P, P, P, P]
         lib.orc_backward.restype = None
+        lib.orc_backward_entries.argtypes = [I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, I,
+                                             P, I, P, P, P, P, P, P]
+        lib.orc_backward_entries.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -329,6 +332,34 @@ class Oracle:
                               *[_ptr(g[n]) for n in ("dx", "dWg", "dWn", "dbias", "dW1", "db1",
                                                       "dW2", "db2", "dgate", "dc", "dz")])
         return g
+
+    def backward_entries(self, inp: dict, dy, entries):
+        """Chosen expert weight-gradient entries from their definitions, for
+        sampling a layer too large for ``backward``. entries: (kind, e, a, b)
+        with kind "dW1" (dW1[e][a][b]), "dW2" (dW2[e][a][b]), "db1" (db1[e][a])
+        or "db2" (db2[e][a]). Returns (values, sums of |terms|)."""
+        kinds = {"dW1": 0, "dW2": 1, "db1": 2, "db2": 3}
+        x = np.ascontiguousarray(inp["x"])
+        T, d = x.shape
+        Wg = _f32(inp["Wg"])
+        E = Wg.shape[1]
+        Wn, noise, bias = _f32(inp.get("Wn")), _f32(inp.get("noise")), _f32(inp.get("bias"))
+        W1 = np.ascontiguousarray(inp["W1"])
+        W2 = np.ascontiguousarray(inp["W2"])
+        d_ff = W1.shape[2]
+        b1 = None if inp.get("b1") is None else np.ascontiguousarray(inp["b1"])
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        n = len(entries)
+        kind = np.array([kinds[q[0]] for q in entries], np.int32)
+        ex, ea, eb = (np.array([q[i] for q in entries], np.int32) for i in (1, 2, 3))
+        out, absum = np.empty(n), np.empty(n)
+        self.lib.orc_backward_entries(T, d, E, d_ff, int(inp["k"]), int(inp["mode"]),
+                                      float(inp["cf"]), int(inp.get("min_cap", 1)), _ptr(x),
+                                      _dtype_code(x), _ptr(Wg), _ptr(Wn), _ptr(noise), _ptr(bias),
+                                      _ptr(W1), _ptr(b1), _ptr(W2), _dtype_code(W1), _ptr(dy), n,
+                                      _ptr(kind), _ptr(ex), _ptr(ea), _ptr(eb), _ptr(out),
+                                      _ptr(absum))
+        return out, absum
 
     # ------------------------------------------------------------ hierarchical
     def hier_select(self, idx_p, g_p, Hs, a: int, b: int, ks: int):
@@ -537,6 +568,10 @@ def loss(*a, **k):
 
 def backward(*a, **k):
     return default().backward(*a, **k)
+
+
+def backward_entries(*a, **k):
+    return default().backward_entries(*a, **k)
 
 
 def hier_select(*a, **k):

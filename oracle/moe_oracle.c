@@ -765,6 +765,76 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
   free(dH); free(dc); free(dsg); free(p);
 }
 
+/*
+ * Chosen entries of the expert weight gradients, each from its definition as
+ * a sum over the expert's kept rows (the same layer, loss and fixed choices
+ * as orc_backward; entries one by one, so a full-size layer can be sampled):
+ *   kind 0: dW1[e][a][b] = sum_r x_{t,a} dpre_{r,b}
+ *   kind 1: dW2[e][a][b] = sum_r h_{r,a} g_r dy_{t,b}
+ *   kind 2: db1[e][a]    = sum_r dpre_{r,a}
+ *   kind 3: db2[e][a]    = sum_r g_r dy_{t,a}
+ * with h_{r,f} = ReLU(x_t W1[e][:,f] + b1[e][f]) and dpre_{r,f} =
+ * g_r [pre_{r,f} > 0] (dy_t . W2[e][f,:]), over the kept assignments r =
+ * (t, j) of expert e in token order. out[n] is the entry, absum[n] the sum
+ * of the absolute values of its terms. Routing (router, selection, capacity,
+ * slots) is computed once over all T tokens.
+ * Parity: pinned against orc_backward on small layers.
+ */
+void orc_backward_entries(int T, int d, int E, int d_ff, int k, int mode, double cf, int min_cap,
+                          const void *x, int x_dtype, const float *Wg, const float *Wn,
+                          const float *noise, const float *bias, const void *W1, const void *b1,
+                          const void *W2, int w_dtype, const double *dy, int n, const int *kind,
+                          const int *ex, const int *ea, const int *eb, double *out,
+                          double *absum) {
+  const size_t TE = (size_t)T * E;
+  double *c = (double *)malloc(sizeof(double) * TE), *sg = (double *)malloc(sizeof(double) * TE);
+  double *H = (double *)malloc(sizeof(double) * TE);
+  orc_router(T, d, E, x, x_dtype, Wg, Wn, noise, bias, c, sg, H);
+  int *idx = (int *)malloc(sizeof(int) * (size_t)T * k);
+  double *gate = (double *)malloc(sizeof(double) * (size_t)T * k);
+  double *hk = (double *)malloc(sizeof(double) * T), *hk1 = (double *)malloc(sizeof(double) * T);
+  orc_select(T, E, k, mode, H, idx, gate, hk, hk1);
+  const int C = orc_capacity(T, E, k, cf, min_cap);
+  int *pos = (int *)malloc(sizeof(int) * (size_t)T * k), *cnt = (int *)malloc(sizeof(int) * E);
+  unsigned char *keep = (unsigned char *)malloc((size_t)T * k);
+  orc_slots(T, k, E, C, idx, pos, keep, cnt);
+  for (int q = 0; q < n; ++q) {
+    const int e = ex[q], a = ea[q], b = eb[q];
+    double sum = 0.0, sabs = 0.0;
+    for (int t = 0; t < T; ++t)
+      for (int j = 0; j < k; ++j) {
+        if (idx[(size_t)t * k + j] != e || !keep[(size_t)t * k + j]) continue;
+        const double g = gate[(size_t)t * k + j];
+        double term = 0.0;
+        if (kind[q] == 3) {
+          term = g * dy[(size_t)t * d + a];
+        } else {
+          /* the hidden unit f this entry needs: b for dW1, a for dW2 and db1 */
+          const int f = kind[q] == 0 ? b : a;
+          double pre = b1 ? orc_in(b1, w_dtype, (size_t)e * d_ff + f) : 0.0;
+          for (int i = 0; i < d; ++i)
+            pre += orc_in(x, x_dtype, (size_t)t * d + i) *
+                   orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f);
+          if (kind[q] == 1) {
+            term = (pre > 0.0 ? pre : 0.0) * g * dy[(size_t)t * d + b];
+          } else {
+            double dh = 0.0;
+            for (int cc = 0; cc < d; ++cc)
+              dh += dy[(size_t)t * d + cc] * orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc);
+            const double dpre = pre > 0.0 ? g * dh : 0.0;
+            term = kind[q] == 0 ? orc_in(x, x_dtype, (size_t)t * d + a) * dpre : dpre;
+          }
+        }
+        sum += term;
+        sabs += fabs(term);
+      }
+    out[q] = sum;
+    absum[q] = sabs;
+  }
+  free(c); free(sg); free(H); free(idx); free(gate); free(hk); free(hk1);
+  free(pos); free(cnt); free(keep);
+}
+
 /* Exposed for the pins: the scalar building blocks. */
 double orc_softplus_at(double z) { return orc_softplus(z); }
 double orc_phi_at(double u) { return orc_phi(u); }

@@ -843,4 +843,27 @@ def pin_backward_dgate(orc):
             np.testing.assert_allclose((g1 - g0)[sel], want, rtol=1e-6, atol=1e-9)
 
 
+
+def pin_backward_entries(orc):
+    """The entry-by-entry weight gradients (sums over the expert's kept rows)
+    equal orc_backward's on a layer with capacity drops, bf16 weights and
+    biases; the sums of |terms| bound the entries."""
+    inp, dy = _grad_case(140, 14, 6, 4, 10, 2, 0.8, TOPK, True)
+    for n in ("x", "W1", "W2", "b1", "b2"):
+        inp[n] = f32_to_bf16_bits(inp[n])
+    ref = orc.backward(inp, dy, 0.3, 0.4, 0.5)
+    rng = np.random.default_rng(141)
+    entries = []
+    for _ in range(12):
+        e = int(rng.integers(4))
+        entries += [("dW1", e, int(rng.integers(6)), int(rng.integers(10))),
+                    ("dW2", e, int(rng.integers(10)), int(rng.integers(6))),
+                    ("db1", e, int(rng.integers(10)), 0), ("db2", e, int(rng.integers(6)), 0)]
+    got, absum = orc.backward_entries(inp, dy, entries)
+    for (kind, e, a, b), v, m in zip(entries, got, absum):
+        want = ref[kind][e, a, b] if kind in ("dW1", "dW2") else ref[kind][e, a]
+        assert abs(v - want) <= 1e-12 * (1 + abs(want)), (kind, e, a, b, v, want)
+        assert abs(v) <= m * (1 + 1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
