@@ -60,7 +60,7 @@ typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t */
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_ARG = 1,         /* invalid argument (sizes, null or misaligned pointer) */
-  MOE_ERR_UNSUPPORTED = 2, /* valid but not handled by this build */
+  MOE_ERR_UNSUPPORTED = 2, /* valid but not handled by the library */
   MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed */
   MOE_ERR_NONFINITE = 4,   /* device: a logit or an output was Inf/NaN */
   MOE_ERR_TIMEOUT = 5,     /* device: a bounded wait inside a kernel ran out */

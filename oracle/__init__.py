@@ -1,4 +1,6 @@
-"""fp64 CPU oracle for the sparsely-gated Mixture-of-Experts forward path.
+"""fp64 CPU oracle for the sparsely-gated Mixture-of-Experts layer: the
+forward path, its hierarchical and strictly balanced variants, and the flat
+layer's backward.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's ``cpu_baseline`` / ``--impl reference`` legs are the only callers.

@@ -1,6 +1,7 @@
 /*
  * moe_oracle.c -- plain, slow, fp64 CPU oracle for the forward path of the
- * sparsely-gated Mixture-of-Experts layer.
+ * sparsely-gated Mixture-of-Experts layer, its hierarchical and strictly
+ * balanced variants, and the flat layer's backward.
  *
  * TEST INFRASTRUCTURE ONLY. This file is compiled into liboracle.so, which only
  * the tests, the package's smoke check and the benchmark's CPU-baseline leg
