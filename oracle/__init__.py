@@ -130,6 +130,9 @@ class Oracle:
         lib.orc_backward_entries.argtypes = [I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, I,
                                              P, I, P, P, P, P, P, P]
         lib.orc_backward_entries.restype = None
+        lib.orc_hier_backward.argtypes = [I, I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, P, P,
+                                          P, I, P, D, D, P, P, P, P, P, P, P, P, P]
+        lib.orc_hier_backward.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -438,6 +441,41 @@ class Oracle:
                     group_count=hx.pop("count"), **hx)
 
 
+    def hier_loss(self, inp: dict, dy, w_imp: float = 0.0, w_load: float = 0.0) -> float:
+        """sum <dy, y_H> + w_imp CV(Importance_H)^2 + w_load CV(Load_H)^2."""
+        fw = self.hier_forward(inp)
+        return float(np.sum(np.asarray(dy, np.float64) * fw["y"]) + w_imp * fw["out2"][0] +
+                     w_load * fw["out2"][1])
+
+    def hier_backward(self, inp: dict, dy, w_imp: float = 0.0, w_load: float = 0.0) -> dict:
+        """Gradients of ``hier_loss`` with the forward's choices fixed (OLNN
+        "Hierarchical Mixture-of-Experts"; section 3.4). Returns fp64 dx, dWp,
+        dWpn, dWs, dWsn (None without noise weights), dW1, db1, dW2, db2."""
+        x = np.ascontiguousarray(inp["x"])
+        T, d = x.shape
+        a, b, kp, ks = (int(inp[n]) for n in ("a", "b", "kp", "ks"))
+        E = a * b
+        Wp, Wpn, npn = _f32(inp["Wp"]), _f32(inp.get("Wpn")), _f32(inp.get("noise_p"))
+        Ws, Wsn, nsn = _f32(inp["Ws"]), _f32(inp.get("Wsn")), _f32(inp.get("noise_s"))
+        W1 = np.ascontiguousarray(inp["W1"])
+        W2 = np.ascontiguousarray(inp["W2"])
+        d_ff = W1.shape[2]
+        b1 = None if inp.get("b1") is None else np.ascontiguousarray(inp["b1"])
+        b2 = None if inp.get("b2") is None else np.ascontiguousarray(inp["b2"])
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        g = dict(dx=np.empty((T, d)), dWp=np.empty((d, a)),
+                 dWpn=None if Wpn is None else np.empty((d, a)), dWs=np.empty((d, E)),
+                 dWsn=None if Wsn is None else np.empty((d, E)), dW1=np.empty((E, d, d_ff)),
+                 db1=np.empty((E, d_ff)), dW2=np.empty((E, d_ff, d)), db2=np.empty((E, d)))
+        self.lib.orc_hier_backward(T, d, a, b, kp, ks, d_ff, float(inp["cf"]),
+                                   int(inp.get("min_cap", 1)), _ptr(x), _dtype_code(x), _ptr(Wp),
+                                   _ptr(Wpn), _ptr(npn), _ptr(Ws), _ptr(Wsn), _ptr(nsn), _ptr(W1),
+                                   _ptr(b1), _ptr(W2), _ptr(b2), _dtype_code(W1), _ptr(dy),
+                                   float(w_imp), float(w_load),
+                                   *[_ptr(g[n]) for n in ("dx", "dWp", "dWpn", "dWs", "dWsn", "dW1",
+                                                           "db1", "dW2", "db2")])
+        return g
+
     # ------------------------------------------------------------ strictly balanced
     def softmax_dense(self, H):
         """G_sigma = Softmax(H) over all experts, row by row (OLNN's plain
@@ -586,6 +624,14 @@ def hier_aux(*a, **k):
 
 def hier_forward(*a, **k):
     return default().hier_forward(*a, **k)
+
+
+def hier_loss(*a, **k):
+    return default().hier_loss(*a, **k)
+
+
+def hier_backward(*a, **k):
+    return default().hier_backward(*a, **k)
 
 
 def softmax_dense(*a, **k):

@@ -538,6 +538,64 @@ double orc_bal_loss(int T, int E, const double *P, const unsigned char *mask_bat
   return s;
 }
 
+/* The residual and the kept experts of a layer's backward (orc_backward's
+ * first step, shared with orc_hier_backward): dx += dy_t; for each kept
+ * choice (t, j) with expert e and gate g, dU = g dy_t, db2 += dU, dW2 +=
+ * h (x) dU, dh = W2 dU masked by pre > 0, db1 += dpre, dW1 += x (x) dpre,
+ * dx += W1 dpre, and dg[t,j] = <dy_t, U> with U = h W2 + b2. The caller
+ * zeroes the outputs. */
+static void orc_expert_bwd(int T, int d, int d_ff, int k, const void *x, int x_dtype,
+                           const int *idx, const double *gate, const unsigned char *keep,
+                           const void *W1, const void *b1, const void *W2, const void *b2,
+                           int w_dtype, const double *dy, double *dx, double *dW1, double *db1,
+                           double *dW2, double *db2, double *dg) {
+  double *pre = (double *)malloc(sizeof(double) * d_ff), *hh = (double *)malloc(sizeof(double) * d_ff);
+  double *U = (double *)malloc(sizeof(double) * d), *dpre = (double *)malloc(sizeof(double) * d_ff);
+  /* Residual and the expert path (sequential: the weight gradients sum over tokens). */
+  for (int t = 0; t < T; ++t) {
+    for (int i = 0; i < d; ++i) dx[(size_t)t * d + i] += dy[(size_t)t * d + i];
+    for (int j = 0; j < k; ++j) {
+      if (!keep[(size_t)t * k + j]) continue;
+      const int e = idx[(size_t)t * k + j];
+      const double g = gate[(size_t)t * k + j];
+      for (int f = 0; f < d_ff; ++f) pre[f] = b1 ? orc_in(b1, w_dtype, (size_t)e * d_ff + f) : 0.0;
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        for (int f = 0; f < d_ff; ++f) pre[f] += xi * orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f);
+      }
+      for (int f = 0; f < d_ff; ++f) hh[f] = pre[f] > 0.0 ? pre[f] : 0.0;
+      for (int cc = 0; cc < d; ++cc) U[cc] = b2 ? orc_in(b2, w_dtype, (size_t)e * d + cc) : 0.0;
+      for (int f = 0; f < d_ff; ++f)
+        for (int cc = 0; cc < d; ++cc) U[cc] += hh[f] * orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc);
+      double s = 0.0;
+      for (int cc = 0; cc < d; ++cc) s += dy[(size_t)t * d + cc] * U[cc];
+      dg[(size_t)t * k + j] = s;
+      /* dU = g dy_t */
+      for (int cc = 0; cc < d; ++cc) db2[(size_t)e * d + cc] += g * dy[(size_t)t * d + cc];
+      for (int f = 0; f < d_ff; ++f) {
+        double dh = 0.0;
+        for (int cc = 0; cc < d; ++cc) {
+          const double du = g * dy[(size_t)t * d + cc];
+          dW2[((size_t)e * d_ff + f) * d + cc] += hh[f] * du;
+          dh += orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc) * du;
+        }
+        dpre[f] = pre[f] > 0.0 ? dh : 0.0;
+        db1[(size_t)e * d_ff + f] += dpre[f];
+      }
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        double acc = 0.0;
+        for (int f = 0; f < d_ff; ++f) {
+          dW1[((size_t)e * d + i) * d_ff + f] += xi * dpre[f];
+          acc += orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f) * dpre[f];
+        }
+        dx[(size_t)t * d + i] += acc;
+      }
+    }
+  }
+  free(pre); free(hh); free(U); free(dpre);
+}
+
 /*
  * Backward of the layer [OLNN section 3.4, "Training the gating network":
  * plain back-propagation, gradients reach W_g through the selected softmax
@@ -622,50 +680,8 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
   memset(dW2, 0, sizeof(double) * (size_t)E * d_ff * d);
   memset(db2, 0, sizeof(double) * (size_t)E * d);
   double *dg = (double *)calloc((size_t)T * k, sizeof(double));
-  double *pre = (double *)malloc(sizeof(double) * d_ff), *hh = (double *)malloc(sizeof(double) * d_ff);
-  double *U = (double *)malloc(sizeof(double) * d), *dpre = (double *)malloc(sizeof(double) * d_ff);
-  /* Residual and the expert path (sequential: the weight gradients sum over tokens). */
-  for (int t = 0; t < T; ++t) {
-    for (int i = 0; i < d; ++i) dx[(size_t)t * d + i] += dy[(size_t)t * d + i];
-    for (int j = 0; j < k; ++j) {
-      if (!keep[(size_t)t * k + j]) continue;
-      const int e = idx[(size_t)t * k + j];
-      const double g = gate[(size_t)t * k + j];
-      for (int f = 0; f < d_ff; ++f) pre[f] = b1 ? orc_in(b1, w_dtype, (size_t)e * d_ff + f) : 0.0;
-      for (int i = 0; i < d; ++i) {
-        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
-        for (int f = 0; f < d_ff; ++f) pre[f] += xi * orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f);
-      }
-      for (int f = 0; f < d_ff; ++f) hh[f] = pre[f] > 0.0 ? pre[f] : 0.0;
-      for (int cc = 0; cc < d; ++cc) U[cc] = b2 ? orc_in(b2, w_dtype, (size_t)e * d + cc) : 0.0;
-      for (int f = 0; f < d_ff; ++f)
-        for (int cc = 0; cc < d; ++cc) U[cc] += hh[f] * orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc);
-      double s = 0.0;
-      for (int cc = 0; cc < d; ++cc) s += dy[(size_t)t * d + cc] * U[cc];
-      dg[(size_t)t * k + j] = s;
-      /* dU = g dy_t */
-      for (int cc = 0; cc < d; ++cc) db2[(size_t)e * d + cc] += g * dy[(size_t)t * d + cc];
-      for (int f = 0; f < d_ff; ++f) {
-        double dh = 0.0;
-        for (int cc = 0; cc < d; ++cc) {
-          const double du = g * dy[(size_t)t * d + cc];
-          dW2[((size_t)e * d_ff + f) * d + cc] += hh[f] * du;
-          dh += orc_in(W2, w_dtype, ((size_t)e * d_ff + f) * d + cc) * du;
-        }
-        dpre[f] = pre[f] > 0.0 ? dh : 0.0;
-        db1[(size_t)e * d_ff + f] += dpre[f];
-      }
-      for (int i = 0; i < d; ++i) {
-        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
-        double acc = 0.0;
-        for (int f = 0; f < d_ff; ++f) {
-          dW1[((size_t)e * d + i) * d_ff + f] += xi * dpre[f];
-          acc += orc_in(W1, w_dtype, ((size_t)e * d + i) * d_ff + f) * dpre[f];
-        }
-        dx[(size_t)t * d + i] += acc;
-      }
-    }
-  }
+  orc_expert_bwd(T, d, d_ff, k, x, x_dtype, idx, gate, keep, W1, b1, W2, b2, w_dtype, dy, dx, dW1,
+                 db1, dW2, db2, dg);
   /* Balancing sums and the gradients of their CV^2. */
   double *imp = (double *)malloc(sizeof(double) * E), *load = (double *)malloc(sizeof(double) * E);
   double *f = (double *)malloc(sizeof(double) * E), *pbar = (double *)malloc(sizeof(double) * E);
@@ -761,8 +777,8 @@ void orc_backward(int T, int d, int E, int d_ff, int k, int mode, double cf, int
     }
   }
   free(c); free(sg); free(H); free(zn); free(idx); free(gate); free(hk); free(hk1);
-  free(pos); free(cnt); free(keep); free(kth1); free(dg); free(pre); free(hh); free(U);
-  free(dpre); free(imp); free(load); free(f); free(pbar); free(dimp); free(dload);
+  free(pos); free(cnt); free(keep); free(kth1); free(dg);
+  free(imp); free(load); free(f); free(pbar); free(dimp); free(dload);
   free(dH); free(dc); free(dsg); free(p);
 }
 
@@ -834,6 +850,237 @@ void orc_backward_entries(int T, int d, int E, int d_ff, int k, int mode, double
   }
   free(c); free(sg); free(H); free(idx); free(gate); free(hk); free(hk1);
   free(pos); free(cnt); free(keep);
+}
+
+/* The expert of the unchosen set with the largest h (lower index on ties):
+ * the (k+1)-th pick of a row whose k picks are in chosen[0..k-1]; -1 if none. */
+static int orc_next_unchosen(const double *h, int n, const int *chosen, int k, int base) {
+  int best = -1;
+  for (int e = 0; e < n; ++e) {
+    int c = 0;
+    for (int j = 0; j < k; ++j) c |= chosen[j] == base + e;
+    if (c) continue;
+    if (best < 0 || h[e] > h[best]) best = e;
+  }
+  return best < 0 ? -1 : base + best;
+}
+
+/* d CV(v)^2 / d v_e = 2 (v_e - m) / (n m^2) - 2 var / (n m^3), scaled by w. */
+static void orc_cv2_grad(const double *v, int n, double w, double *dv) {
+  double m = 0.0, var = 0.0;
+  for (int e = 0; e < n; ++e) m += v[e];
+  m /= n;
+  for (int e = 0; e < n; ++e) var += (v[e] - m) * (v[e] - m);
+  var /= n;
+  for (int e = 0; e < n; ++e)
+    dv[e] = w * (2.0 * (v[e] - m) / (n * m * m) - 2.0 * var / (n * m * m * m));
+}
+
+/* dz = dsigma * sigmoid(z); dW += x^T dc (and x^T dz); dx += W dc + Wn dz. */
+static void orc_router_bwd(int T, int d, int E, const void *x, int x_dtype, const float *W,
+                           const float *Wn, const double *dc, const double *dz, double *dW,
+                           double *dWn, double *dx) {
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      const size_t u = (size_t)t * E + e;
+      for (int i = 0; i < d; ++i) {
+        const double xi = orc_in(x, x_dtype, (size_t)t * d + i);
+        dW[(size_t)i * E + e] += xi * dc[u];
+        dx[(size_t)t * d + i] += (double)W[(size_t)i * E + e] * dc[u];
+        if (Wn) {
+          dWn[(size_t)i * E + e] += xi * dz[u];
+          dx[(size_t)t * d + i] += (double)Wn[(size_t)i * E + e] * dz[u];
+        }
+      }
+    }
+}
+
+/*
+ * Backward of the hierarchical layer [OLNN, "Hierarchical Mixture-of-Experts":
+ * y_H = x + sum_i sum_j G_p(x)_i G_i(x)_j E_ij(x), Importance_H and Load_H;
+ * section 3.4 "Training the gating network"; the section notes that the
+ * factor Load_primary(X)_i carries the load signal to the primary gate].
+ * For an upstream gradient dy [T,d] and weights w_imp, w_load:
+ *   L = sum_t <dy_t, y_t> + w_imp CV(Importance_H)^2 + w_load CV(Load_H)^2,
+ * differentiated with the forward's choices fixed (both gates' picks,
+ * capacity drops, the ReLU pattern, the token sets X^(i) and so |X^(i)|):
+ *  - the residual and the kept experts as in orc_backward, with the product
+ *    gate G_p,i G_i,j; dL/d(product) of a selected choice = <dy, U> (kept)
+ *    plus the Importance_H term;
+ *  - the product splits into the primary gate (sum over the group's picks of
+ *    d(product) G_i,j) and the secondary gate (d(product) G_p,i), each
+ *    through its kept-set softmax Jacobian;
+ *  - Load_H[i*b+j] = Load_p[i] loadsec[i*b+j] / |X^(i)|: into the primary
+ *    load (over all tokens and the a groups, thresholds among the primary
+ *    logits) and the in-group secondary load (over X^(i), thresholds among
+ *    the group's secondary logits), each P = Phi((c - thr) / sigma) as in
+ *    orc_backward; 0 where |X^(i)| = 0;
+ *  - both routers without bias: H = c + n sigma, sigma = Softplus(z).
+ * Outputs (fp64, overwritten): dx [T,d], dWp, dWpn [d,a] (dWpn when Wpn),
+ * dWs, dWsn [d,a*b] (dWsn when Wsn), dW1 [E,d,d_ff], db1 [E,d_ff],
+ * dW2 [E,d_ff,d], db2 [E,d], E = a*b.
+ * Parity: pinned by central differences of the hierarchical forward's loss.
+ */
+void orc_hier_backward(int T, int d, int a, int b, int kp, int ks, int d_ff, double cf,
+                       int min_cap, const void *x, int x_dtype, const float *Wp,
+                       const float *Wpn, const float *noise_p, const float *Ws,
+                       const float *Wsn, const float *noise_s, const void *W1, const void *b1,
+                       const void *W2, const void *b2, int w_dtype, const double *dy,
+                       double w_imp, double w_load, double *dx, double *dWp, double *dWpn,
+                       double *dWs, double *dWsn, double *dW1, double *db1, double *dW2,
+                       double *db2) {
+  const int E = a * b, k = kp * ks;
+  const size_t TA = (size_t)T * a, TE = (size_t)T * E;
+  /* primary gate and its load */
+  double *cp = (double *)malloc(sizeof(double) * TA), *sp = (double *)malloc(sizeof(double) * TA);
+  double *Hp = (double *)malloc(sizeof(double) * TA);
+  orc_router(T, d, a, x, x_dtype, Wp, Wpn, noise_p, NULL, cp, sp, Hp);
+  int *idx_p = (int *)malloc(sizeof(int) * (size_t)T * kp);
+  double *g_p = (double *)malloc(sizeof(double) * (size_t)T * kp);
+  double *hkp = (double *)malloc(sizeof(double) * T), *hk1p = (double *)malloc(sizeof(double) * T);
+  orc_select(T, a, kp, ORC_TOPK_SOFTMAX, Hp, idx_p, g_p, hkp, hk1p);
+  double *imp_p = (double *)malloc(sizeof(double) * a), *load_p = (double *)malloc(sizeof(double) * a);
+  double o3[3];
+  orc_aux(T, a, kp, cp, sp, Hp, idx_p, g_p, hkp, hk1p, Wpn != NULL, imp_p, load_p, NULL, NULL, o3);
+  /* secondary gates, the two-level selection, capacity and slots */
+  double *cs = (double *)malloc(sizeof(double) * TE), *ss = (double *)malloc(sizeof(double) * TE);
+  double *Hs = (double *)malloc(sizeof(double) * TE);
+  orc_router(T, d, E, x, x_dtype, Ws, Wsn, noise_s, NULL, cs, ss, Hs);
+  int *idx = (int *)malloc(sizeof(int) * (size_t)T * k);
+  double *gate = (double *)malloc(sizeof(double) * (size_t)T * k);
+  double *hks = (double *)malloc(sizeof(double) * (size_t)T * kp);
+  double *hk1s = (double *)malloc(sizeof(double) * (size_t)T * kp);
+  orc_hier_select(T, a, b, kp, ks, idx_p, g_p, Hs, idx, gate, hks, hk1s);
+  const int C = orc_capacity(T, E, k, cf, min_cap);
+  int *pos = (int *)malloc(sizeof(int) * (size_t)T * k), *cnt = (int *)malloc(sizeof(int) * E);
+  unsigned char *keep = (unsigned char *)malloc((size_t)T * k);
+  orc_slots(T, k, E, C, idx, pos, keep, cnt);
+  double *imp_H = (double *)malloc(sizeof(double) * E), *loadsec = (double *)malloc(sizeof(double) * E);
+  double *load_H = (double *)malloc(sizeof(double) * E), o2[2];
+  int *gcount = (int *)malloc(sizeof(int) * a);
+  orc_hier_aux(T, a, b, kp, ks, idx_p, cs, ss, idx, gate, hks, hk1s, Wsn != NULL, load_p, imp_H,
+               loadsec, gcount, load_H, o2);
+  memset(dx, 0, sizeof(double) * (size_t)T * d);
+  memset(dWp, 0, sizeof(double) * (size_t)d * a);
+  if (dWpn) memset(dWpn, 0, sizeof(double) * (size_t)d * a);
+  memset(dWs, 0, sizeof(double) * (size_t)d * E);
+  if (dWsn) memset(dWsn, 0, sizeof(double) * (size_t)d * E);
+  memset(dW1, 0, sizeof(double) * (size_t)E * d * d_ff);
+  memset(db1, 0, sizeof(double) * (size_t)E * d_ff);
+  memset(dW2, 0, sizeof(double) * (size_t)E * d_ff * d);
+  memset(db2, 0, sizeof(double) * (size_t)E * d);
+  /* 1. residual and experts */
+  double *dg = (double *)calloc((size_t)T * k, sizeof(double));
+  orc_expert_bwd(T, d, d_ff, k, x, x_dtype, idx, gate, keep, W1, b1, W2, b2, w_dtype, dy, dx, dW1,
+                 db1, dW2, db2, dg);
+  /* 2. the losses' gradients in Importance_H and Load_H, then in the two loads */
+  double *dimp = (double *)malloc(sizeof(double) * E), *dloadH = (double *)malloc(sizeof(double) * E);
+  orc_cv2_grad(imp_H, E, w_imp, dimp);
+  orc_cv2_grad(load_H, E, w_load, dloadH);
+  double *dload_p = (double *)calloc(a, sizeof(double)), *dloadsec = (double *)calloc(E, sizeof(double));
+  for (int i = 0; i < a; ++i) {
+    if (gcount[i] == 0) continue;
+    for (int j = 0; j < b; ++j) {
+      const int e = i * b + j;
+      dload_p[i] += dloadH[e] * loadsec[e] / (double)gcount[i];
+      dloadsec[e] = dloadH[e] * load_p[i] / (double)gcount[i];
+    }
+  }
+  /* 3. the gates */
+  double *dHp = (double *)calloc(TA, sizeof(double)), *dcp = (double *)calloc(TA, sizeof(double));
+  double *dsp = (double *)calloc(TA, sizeof(double));
+  double *dHs = (double *)calloc(TE, sizeof(double)), *dcs = (double *)calloc(TE, sizeof(double));
+  double *dss = (double *)calloc(TE, sizeof(double));
+  const double rt2pi = sqrt(2.0 * acos(-1.0));
+  for (int t = 0; t < T; ++t) {
+    double dgp[kp], sumq = 0.0;
+    for (int q = 0; q < kp; ++q) {
+      const int i = idx_p[(size_t)t * kp + q];
+      const double gp = g_p[(size_t)t * kp + q];
+      const double *hs = Hs + (size_t)t * E + (size_t)i * b;
+      /* the group's secondary softmax over its ks picks, recomputed from Hs */
+      double mx = -INFINITY, z = 0.0, sg[ks], dsg[ks], sums = 0.0;
+      for (int r = 0; r < ks; ++r) {
+        const double h = hs[idx[(size_t)t * k + q * ks + r] - i * b];
+        if (h > mx) mx = h;
+      }
+      for (int r = 0; r < ks; ++r) z += exp(hs[idx[(size_t)t * k + q * ks + r] - i * b] - mx);
+      dgp[q] = 0.0;
+      for (int r = 0; r < ks; ++r) {
+        const int c = q * ks + r, e = idx[(size_t)t * k + c];
+        sg[r] = exp(hs[e - i * b] - mx) / z;
+        const double dprod = dg[(size_t)t * k + c] + dimp[e];
+        dgp[q] += dprod * sg[r];
+        dsg[r] = dprod * gp;
+        sums += sg[r] * dsg[r];
+      }
+      for (int r = 0; r < ks; ++r)
+        dHs[(size_t)t * E + idx[(size_t)t * k + q * ks + r]] += sg[r] * (dsg[r] - sums);
+      sumq += gp * dgp[q];
+      /* the in-group secondary load over X^(i) */
+      if (Wsn && ks < b) {
+        const int *picks = idx + (size_t)t * k + q * ks;
+        const int owner_out = picks[ks - 1];
+        const int owner_in = orc_next_unchosen(hs, b, picks, ks, i * b);
+        for (int j = 0; j < b; ++j) {
+          const int e = i * b + j;
+          const double s = ss[(size_t)t * E + e];
+          if (s == 0.0) continue;
+          int chosen = 0;
+          for (int r = 0; r < ks; ++r) chosen |= picks[r] == e;
+          const double thr = chosen ? hk1s[(size_t)t * kp + q] : hks[(size_t)t * kp + q];
+          const double u = (cs[(size_t)t * E + e] - thr) / s;
+          const double gl = dloadsec[e] * exp(-0.5 * u * u) / rt2pi / s;
+          dcs[(size_t)t * E + e] += gl;
+          dss[(size_t)t * E + e] -= gl * u;
+          dHs[(size_t)t * E + (chosen ? owner_in : owner_out)] -= gl;
+        }
+      }
+    }
+    for (int q = 0; q < kp; ++q)
+      dHp[(size_t)t * a + idx_p[(size_t)t * kp + q]] += g_p[(size_t)t * kp + q] * (dgp[q] - sumq);
+    /* the primary load over all tokens */
+    if (Wpn && kp < a) {
+      const int *picks = idx_p + (size_t)t * kp;
+      const int owner_out = picks[kp - 1];
+      const int owner_in = orc_next_unchosen(Hp + (size_t)t * a, a, picks, kp, 0);
+      for (int i = 0; i < a; ++i) {
+        const double s = sp[(size_t)t * a + i];
+        if (s == 0.0) continue;
+        int chosen = 0;
+        for (int q = 0; q < kp; ++q) chosen |= picks[q] == i;
+        const double thr = chosen ? hk1p[t] : hkp[t];
+        const double u = (cp[(size_t)t * a + i] - thr) / s;
+        const double gl = dload_p[i] * exp(-0.5 * u * u) / rt2pi / s;
+        dcp[(size_t)t * a + i] += gl;
+        dsp[(size_t)t * a + i] -= gl * u;
+        dHp[(size_t)t * a + (chosen ? owner_in : owner_out)] -= gl;
+      }
+    }
+  }
+  /* 4. both routers: H = c + n sigma, sigma = Softplus(z) */
+  double *dzp = (double *)calloc(TA, sizeof(double)), *dzs = (double *)calloc(TE, sizeof(double));
+  for (size_t u = 0; u < TA; ++u) {
+    dcp[u] += dHp[u];
+    if (Wpn) {
+      dsp[u] += (double)noise_p[u] * dHp[u];
+      dzp[u] = dsp[u] * -expm1(-sp[u]); /* sigmoid(z) = 1 - exp(-Softplus(z)) */
+    }
+  }
+  for (size_t u = 0; u < TE; ++u) {
+    dcs[u] += dHs[u];
+    if (Wsn) {
+      dss[u] += (double)noise_s[u] * dHs[u];
+      dzs[u] = dss[u] * -expm1(-ss[u]);
+    }
+  }
+  orc_router_bwd(T, d, a, x, x_dtype, Wp, Wpn, dcp, dzp, dWp, dWpn, dx);
+  orc_router_bwd(T, d, E, x, x_dtype, Ws, Wsn, dcs, dzs, dWs, dWsn, dx);
+  free(cp); free(sp); free(Hp); free(idx_p); free(g_p); free(hkp); free(hk1p); free(imp_p);
+  free(load_p); free(cs); free(ss); free(Hs); free(idx); free(gate); free(hks); free(hk1s);
+  free(pos); free(cnt); free(keep); free(imp_H); free(loadsec); free(load_H); free(gcount);
+  free(dg); free(dimp); free(dloadH); free(dload_p); free(dloadsec); free(dHp); free(dcp);
+  free(dsp); free(dHs); free(dcs); free(dss); free(dzp); free(dzs);
 }
 
 /* Exposed for the pins: the scalar building blocks. */

@@ -866,4 +866,74 @@ def pin_backward_entries(orc):
         assert abs(v) <= m * (1 + 1e-12)
 
 
+
+def _hier_grad_case(seed, T, d, a, b, kp, ks, d_ff, cf, noisy):
+    rng = np.random.default_rng(seed)
+    f = lambda *sh, sd=1.0: (rng.standard_normal(sh) * sd).astype(np.float32)
+    E = a * b
+    inp = dict(x=f(T, d), Wp=f(d, a, sd=1 / math.sqrt(d)), Ws=f(d, E, sd=1 / math.sqrt(d)),
+               W1=f(E, d, d_ff, sd=1 / math.sqrt(d)), W2=f(E, d_ff, d, sd=1 / math.sqrt(d_ff)),
+               b1=f(E, d_ff, sd=0.1), b2=f(E, d, sd=0.1), a=a, b=b, kp=kp, ks=ks, cf=cf,
+               min_cap=1)
+    inp["Wpn"] = f(d, a, sd=1 / math.sqrt(d)) if noisy else None
+    inp["noise_p"] = f(T, a) if noisy else None
+    inp["Wsn"] = f(d, E, sd=1 / math.sqrt(d)) if noisy else None
+    inp["noise_s"] = f(T, E) if noisy else None
+    return inp, rng.standard_normal((T, d))
+
+
+def pin_hier_backward_finite_differences(orc):
+    """The hierarchical backward equals central differences of the
+    hierarchical forward's loss (noisy, with capacity drops; clean; one
+    primary pick of two groups)."""
+    names = dict(x="dx", Wp="dWp", Wpn="dWpn", Ws="dWs", Wsn="dWsn", W1="dW1", b1="db1",
+                 W2="dW2", b2="db2")
+    cases = [((150, 12, 5, 3, 4, 2, 2, 6, 0.7, True), (0.7, 0.9)),
+             ((151, 10, 5, 3, 4, 2, 2, 6, 0.7, False), (0.5, 0.5)),
+             ((152, 12, 5, 2, 5, 1, 3, 6, 0.9, True), (0.6, 0.8))]
+    for n, (args, w) in enumerate(cases):
+        inp, dy = _hier_grad_case(*args)
+        g = orc.hier_backward(inp, dy, *w)
+        L0 = orc.hier_loss(inp, dy, *w)
+        eps = 2.0 ** -12
+        rng = np.random.default_rng(160 + n)
+        checked = skipped = 0
+        for name, gname in names.items():
+            A = inp.get(name)
+            if A is None:
+                continue
+            for _ in range(10):
+                i = tuple(int(rng.integers(0, m)) for m in A.shape)
+                v = A[i]
+                A[i] = v + np.float32(eps)
+                Lp = orc.hier_loss(inp, dy, *w)
+                A[i] = v - np.float32(eps)
+                Lm = orc.hier_loss(inp, dy, *w)
+                A[i] = v
+                up, down = (Lp - L0) / eps, (L0 - Lm) / eps
+                if abs(up - down) > 1e-3 * (abs(up) + abs(down)) + 1e-6:
+                    skipped += 1
+                    continue
+                fd = (Lp - Lm) / (2 * eps)
+                assert abs(g[gname][i] - fd) <= 1e-5 * abs(fd) + 1e-7, (n, name, i, g[gname][i], fd)
+                checked += 1
+        assert skipped <= max(2, checked // 10), (checked, skipped)
+
+
+def pin_hier_backward_one_group_is_flat(orc):
+    """One group (a = 1, kp = 1): the primary gate is the constant 1, Load_H
+    is the flat load, and the hierarchical backward equals the flat layer's
+    backward over the b experts; the primary router gets no gradient."""
+    inp, dy = _hier_grad_case(170, 11, 5, 1, 5, 1, 2, 6, 0.8, True)
+    g = orc.hier_backward(inp, dy, 0.6, 0.7)
+    flat = dict(x=inp["x"], Wg=inp["Ws"], Wn=inp["Wsn"], noise=inp["noise_s"], bias=None,
+                W1=inp["W1"], b1=inp["b1"], W2=inp["W2"], b2=inp["b2"], k=2, cf=0.8, min_cap=1,
+                mode=TOPK)
+    ref = orc.backward(flat, dy, 0.6, 0.7, 0.0)
+    for hn, fn in (("dx", "dx"), ("dWs", "dWg"), ("dWsn", "dWn"), ("dW1", "dW1"), ("db1", "db1"),
+                   ("dW2", "dW2"), ("db2", "db2")):
+        np.testing.assert_allclose(g[hn], ref[fn], rtol=1e-10, atol=1e-12, err_msg=hn)
+    assert np.all(np.abs(g["dWp"]) <= 1e-12) and np.all(np.abs(g["dWpn"]) <= 1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -80,6 +80,13 @@ MUTATIONS = {
     "bwd_aux_not_averaged": ("w_aux * 0.01 * E * f[e] / T;", "w_aux * 0.01 * E * f[e];"),
     "bwd_importance_only_kept": ("dG[j] = dg[(size_t)t * k + j] + dimp[idx[(size_t)t * k + j]];",
                                  "dG[j] = dg[(size_t)t * k + j] + (dg[(size_t)t * k + j] != 0.0 ? dimp[idx[(size_t)t * k + j]] : 0.0);"),
+    "hbwd_primary_share_unweighted": ("dgp[q] += dprod * sg[r];", "dgp[q] += dprod;"),
+    "hbwd_secondary_share_unweighted": ("dsg[r] = dprod * gp;", "dsg[r] = dprod;"),
+    "hbwd_group_load_not_normalised": ("dloadsec[e] = dloadH[e] * load_p[i] / (double)gcount[i];",
+                                       "dloadsec[e] = dloadH[e] * load_p[i];"),
+    "hbwd_primary_load_dropped": ("dload_p[i] += dloadH[e] * loadsec[e] / (double)gcount[i];", ""),
+    "hbwd_group_owner_not_offset": ("orc_next_unchosen(hs, b, picks, ks, i * b)",
+                                    "orc_next_unchosen(hs, b, picks, ks, 0)"),
 }
 
 
