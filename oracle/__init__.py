@@ -133,6 +133,9 @@ class Oracle:
         lib.orc_hier_backward.argtypes = [I, I, I, I, I, I, I, D, I, P, I, P, P, P, P, P, P, P, P, P,
                                           P, I, P, D, D, P, P, P, P, P, P, P, P, P]
         lib.orc_hier_backward.restype = None
+        lib.orc_bal_backward.argtypes = [I, I, I, I, I, I, P, I, P, P, P, P, P, P, P, I, P, D, P, P,
+                                         P, P, P, P, P]
+        lib.orc_bal_backward.restype = None
         self.lib = lib
         self.path = lib_path
 
@@ -476,6 +479,36 @@ class Oracle:
                                                            "db1", "dW2", "db2")])
         return g
 
+    def bal_loss_total(self, inp: dict, dy, w_bal: float = 0.0) -> float:
+        """sum <dy, y> + w_bal L_batchwise (the loss term only with thresholds)."""
+        return _bal_total(self, inp, dy, w_bal)
+
+    def bal_backward(self, inp: dict, dy, w_bal: float = 0.0) -> dict:
+        """Gradients of ``bal_loss_total`` with the masks fixed (OLNN, Strictly
+        Balanced Gating; section 3.4). Returns fp64 dx, dWg, dbias (None
+        without a router bias), dW1, db1, dW2, db2."""
+        x = np.ascontiguousarray(inp["x"])
+        T, d = x.shape
+        Wg = _f32(inp["Wg"])
+        E = Wg.shape[1]
+        bias, thr = _f32(inp.get("bias")), _f32(inp.get("thr"))
+        W1 = np.ascontiguousarray(inp["W1"])
+        W2 = np.ascontiguousarray(inp["W2"])
+        d_ff = W1.shape[2]
+        b1 = None if inp.get("b1") is None else np.ascontiguousarray(inp["b1"])
+        b2 = None if inp.get("b2") is None else np.ascontiguousarray(inp["b2"])
+        dy = np.ascontiguousarray(dy, dtype=np.float64)
+        g = dict(dx=np.empty((T, d)), dWg=np.empty((d, E)),
+                 dbias=None if bias is None else np.empty(E), dW1=np.empty((E, d, d_ff)),
+                 db1=np.empty((E, d_ff)), dW2=np.empty((E, d_ff, d)), db2=np.empty((E, d)))
+        self.lib.orc_bal_backward(T, d, E, d_ff, int(inp["k"]), int(inp.get("mode_bal", 0)),
+                                  _ptr(x), _dtype_code(x), _ptr(Wg), _ptr(bias), _ptr(thr),
+                                  _ptr(W1), _ptr(b1), _ptr(W2), _ptr(b2), _dtype_code(W1),
+                                  _ptr(dy), float(w_bal),
+                                  *[_ptr(g[n]) for n in ("dx", "dWg", "dbias", "dW1", "db1", "dW2",
+                                                          "db2")])
+        return g
+
     # ------------------------------------------------------------ strictly balanced
     def softmax_dense(self, H):
         """G_sigma = Softmax(H) over all experts, row by row (OLNN's plain
@@ -539,6 +572,11 @@ class Oracle:
             mb = mask if mode == 0 else self.bal_gate(P, m, None, 0)[0]
             out["loss"] = self.bal_loss(P, mb, thr)
         return out
+
+
+def _bal_total(orc, inp, dy, w_bal):
+    fw = orc.bal_forward(inp)
+    return float(np.sum(np.asarray(dy, np.float64) * fw["y"]) + w_bal * fw.get("loss", 0.0))
 
 
 def default() -> Oracle:
@@ -648,6 +686,14 @@ def bal_loss(*a, **k):
 
 def bal_forward(*a, **k):
     return default().bal_forward(*a, **k)
+
+
+def bal_backward(*a, **k):
+    return default().bal_backward(*a, **k)
+
+
+def bal_loss_total(*a, **k):
+    return default().bal_loss_total(*a, **k)
 
 
 def bal_rows(*a, **k):

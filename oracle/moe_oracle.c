@@ -1083,6 +1083,80 @@ void orc_hier_backward(int T, int d, int a, int b, int kp, int ks, int d_ff, dou
   free(dsp); free(dHs); free(dcs); free(dss); free(dzp); free(dzs);
 }
 
+/*
+ * Backward of the strictly balanced layer [OLNN, "Strictly Balanced Gating
+ * (Batchwise Mask)"; section 3.4]: for an upstream gradient dy [T,d] and
+ * weight w_bal,
+ *   L = sum_t <dy_t, y_t> + w_bal L_batchwise   (L_batchwise when thr given)
+ * with the masks held fixed (the batchwise picks, or the threshold mask in
+ * mode 1, and the masks inside L_batchwise):
+ *  - the residual and the picked experts as in orc_backward (k = E, the mask
+ *    as the keep flags), giving dG of each picked gate;
+ *  - G_i = P_i / S over the token's picks, S = sum of the picks' P: dP_i =
+ *    (dG_i - sum_l G_l dG_l) / S on the picks;
+ *  - L_batchwise adds w_bal (M_threshold - M_batchwise) to every dP;
+ *  - P = Softmax(H) over all E: dH = P (dP - <P, dP>); H = x W_g + b.
+ * Outputs (fp64, overwritten): dx [T,d], dWg [d,E], dbias [E] (when bias),
+ * dW1 [E,d,d_ff], db1 [E,d_ff], dW2 [E,d_ff,d], db2 [E,d].
+ * Parity: pinned by central differences of the balanced forward's loss.
+ */
+void orc_bal_backward(int T, int d, int E, int d_ff, int k, int mode, const void *x, int x_dtype,
+                      const float *Wg, const float *bias, const float *thr, const void *W1,
+                      const void *b1, const void *W2, const void *b2, int w_dtype,
+                      const double *dy, double w_bal, double *dx, double *dWg, double *dbias,
+                      double *dW1, double *db1, double *dW2, double *db2) {
+  const size_t TE = (size_t)T * E;
+  double *c = (double *)malloc(sizeof(double) * TE), *sg = (double *)malloc(sizeof(double) * TE);
+  double *H = (double *)malloc(sizeof(double) * TE), *P = (double *)malloc(sizeof(double) * TE);
+  orc_router(T, d, E, x, x_dtype, Wg, NULL, NULL, bias, c, sg, H);
+  orc_softmax_rows(T, E, H, P);
+  const int m = orc_bal_rows(T, k, E);
+  unsigned char *mask = (unsigned char *)malloc(TE), *mb = (unsigned char *)malloc(TE);
+  double *gate = (double *)malloc(sizeof(double) * TE), *gtmp = (double *)malloc(sizeof(double) * TE);
+  orc_bal_gate(T, E, m, mode, P, thr, mask, gate);
+  if (mode == 0) memcpy(mb, mask, TE);
+  else orc_bal_gate(T, E, m, 0, P, thr, mb, gtmp);
+  int *idx = (int *)malloc(sizeof(int) * TE);
+  for (size_t u = 0; u < TE; ++u) idx[u] = (int)(u % E);
+  memset(dx, 0, sizeof(double) * (size_t)T * d);
+  memset(dWg, 0, sizeof(double) * (size_t)d * E);
+  if (dbias) memset(dbias, 0, sizeof(double) * E);
+  memset(dW1, 0, sizeof(double) * (size_t)E * d * d_ff);
+  memset(db1, 0, sizeof(double) * (size_t)E * d_ff);
+  memset(dW2, 0, sizeof(double) * (size_t)E * d_ff * d);
+  memset(db2, 0, sizeof(double) * (size_t)E * d);
+  double *dG = (double *)calloc(TE, sizeof(double));
+  orc_expert_bwd(T, d, d_ff, E, x, x_dtype, idx, gate, mask, W1, b1, W2, b2, w_dtype, dy, dx, dW1,
+                 db1, dW2, db2, dG);
+  double *dH = (double *)malloc(sizeof(double) * TE);
+  for (int t = 0; t < T; ++t) {
+    const double *p = P + (size_t)t * E;
+    double dP[E], S = 0.0, gd = 0.0, pd = 0.0;
+    for (int i = 0; i < E; ++i)
+      if (mask[(size_t)t * E + i]) {
+        S += p[i];
+        gd += gate[(size_t)t * E + i] * dG[(size_t)t * E + i];
+      }
+    for (int i = 0; i < E; ++i) {
+      dP[i] = mask[(size_t)t * E + i] ? (dG[(size_t)t * E + i] - gd) / S : 0.0;
+      if (thr) dP[i] += w_bal * ((p[i] > (double)thr[i] ? 1.0 : 0.0) - (double)mb[(size_t)t * E + i]);
+      pd += p[i] * dP[i];
+    }
+    for (int i = 0; i < E; ++i) dH[(size_t)t * E + i] = p[i] * (dP[i] - pd);
+  }
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      const double g = dH[(size_t)t * E + e];
+      if (dbias) dbias[e] += g;
+      for (int i = 0; i < d; ++i) {
+        dWg[(size_t)i * E + e] += orc_in(x, x_dtype, (size_t)t * d + i) * g;
+        dx[(size_t)t * d + i] += (double)Wg[(size_t)i * E + e] * g;
+      }
+    }
+  free(c); free(sg); free(H); free(P); free(mask); free(mb); free(gate); free(gtmp); free(idx);
+  free(dG); free(dH);
+}
+
 /* Exposed for the pins: the scalar building blocks. */
 double orc_softplus_at(double z) { return orc_softplus(z); }
 double orc_phi_at(double u) { return orc_phi(u); }

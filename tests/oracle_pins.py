@@ -936,4 +936,45 @@ def pin_hier_backward_one_group_is_flat(orc):
     assert np.all(np.abs(g["dWp"]) <= 1e-12) and np.all(np.abs(g["dWpn"]) <= 1e-12)
 
 
+
+def pin_bal_backward_finite_differences(orc):
+    """The strictly balanced layer's backward equals central differences of
+    its forward's loss sum <dy, y> + w L_batchwise: batchwise mask with the
+    loss, the threshold mask as the gate, and every expert taking every token
+    (k = E)."""
+    names = dict(x="dx", Wg="dWg", bias="dbias", W1="dW1", b1="db1", W2="dW2", b2="db2")
+    for n, (T, E, k, mode, w) in enumerate([(12, 4, 2, 0, 0.7), (12, 4, 2, 1, 0.5),
+                                            (9, 3, 3, 0, 0.3)]):
+        rng = np.random.default_rng(180 + n)
+        f = lambda *sh, sd=1.0: (rng.standard_normal(sh) * sd).astype(np.float32)
+        d, d_ff = 5, 6
+        inp = dict(x=f(T, d), Wg=f(d, E, sd=1.5 / math.sqrt(d)), bias=f(E, sd=0.3),
+                   W1=f(E, d, d_ff, sd=1 / math.sqrt(d)), W2=f(E, d_ff, d, sd=1 / math.sqrt(d_ff)),
+                   b1=f(E, d_ff, sd=0.1), b2=f(E, d, sd=0.1), k=k, mode_bal=mode,
+                   thr=np.full(E, 1.0 / E, np.float32))
+        dy = rng.standard_normal((T, d))
+        g = orc.bal_backward(inp, dy, w)
+        L0 = orc.bal_loss_total(inp, dy, w)
+        eps = 2.0 ** -12
+        checked = skipped = 0
+        for name, gname in names.items():
+            A = inp[name]
+            for _ in range(10):
+                i = tuple(int(rng.integers(0, m)) for m in A.shape)
+                v = A[i]
+                A[i] = v + np.float32(eps)
+                Lp = orc.bal_loss_total(inp, dy, w)
+                A[i] = v - np.float32(eps)
+                Lm = orc.bal_loss_total(inp, dy, w)
+                A[i] = v
+                up, down = (Lp - L0) / eps, (L0 - Lm) / eps
+                if abs(up - down) > 1e-3 * (abs(up) + abs(down)) + 1e-6:
+                    skipped += 1
+                    continue
+                fd = (Lp - Lm) / (2 * eps)
+                assert abs(g[gname][i] - fd) <= 1e-5 * abs(fd) + 1e-7, (n, name, i, g[gname][i], fd)
+                checked += 1
+        assert skipped <= max(2, checked // 10), (checked, skipped)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

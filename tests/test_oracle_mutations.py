@@ -87,6 +87,12 @@ MUTATIONS = {
     "hbwd_primary_load_dropped": ("dload_p[i] += dloadH[e] * loadsec[e] / (double)gcount[i];", ""),
     "hbwd_group_owner_not_offset": ("orc_next_unchosen(hs, b, picks, ks, i * b)",
                                     "orc_next_unchosen(hs, b, picks, ks, 0)"),
+    "balbwd_renormalisation_ignored": ("dP[i] = mask[(size_t)t * E + i] ? (dG[(size_t)t * E + i] - gd) / S : 0.0;",
+                                       "dP[i] = mask[(size_t)t * E + i] ? dG[(size_t)t * E + i] : 0.0;"),
+    "balbwd_loss_sign": ("dP[i] += w_bal * ((p[i] > (double)thr[i] ? 1.0 : 0.0) - (double)mb[(size_t)t * E + i]);",
+                         "dP[i] += w_bal * ((double)mb[(size_t)t * E + i] - (p[i] > (double)thr[i] ? 1.0 : 0.0));"),
+    "balbwd_softmax_mean_dropped": ("dH[(size_t)t * E + i] = p[i] * (dP[i] - pd);",
+                                    "dH[(size_t)t * E + i] = p[i] * dP[i];"),
 }
 
 
