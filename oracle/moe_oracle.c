@@ -860,7 +860,7 @@ static int orc_next_unchosen(const double *h, int n, const int *chosen, int k, i
     int c = 0;
     for (int j = 0; j < k; ++j) c |= chosen[j] == base + e;
     if (c) continue;
-    if (best < 0 || h[e] > h[best]) best = e;
+    if (best < 0 || h[best] < h[e]) best = e; /* strict: the lower index stays on ties */
   }
   return best < 0 ? -1 : base + best;
 }
@@ -871,7 +871,7 @@ static void orc_cv2_grad(const double *v, int n, double w, double *dv) {
   for (int e = 0; e < n; ++e) m += v[e];
   m /= n;
   for (int e = 0; e < n; ++e) var += (v[e] - m) * (v[e] - m);
-  var /= n;
+  var = var / n; /* population variance */
   for (int e = 0; e < n; ++e)
     dv[e] = w * (2.0 * (v[e] - m) / (n * m * m) - 2.0 * var / (n * m * m * m));
 }
@@ -1028,7 +1028,8 @@ void orc_hier_backward(int T, int d, int a, int b, int kp, int ks, int d_ff, dou
           if (s == 0.0) continue;
           int chosen = 0;
           for (int r = 0; r < ks; ++r) chosen |= picks[r] == e;
-          const double thr = chosen ? hk1s[(size_t)t * kp + q] : hks[(size_t)t * kp + q];
+          const size_t tq = (size_t)t * kp + q;
+          const double thr = chosen ? hk1s[tq] : hks[tq];
           const double u = (cs[(size_t)t * E + e] - thr) / s;
           const double gl = dloadsec[e] * exp(-0.5 * u * u) / rt2pi / s;
           dcs[(size_t)t * E + e] += gl;
