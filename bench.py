@@ -957,7 +957,7 @@ def run_backward(args, w: wl.Workload):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     if w.dtype != "bf16":
-        raise SystemExit("the backward runs on bf16 layers")
+        raise SystemExit("bench.py --backward times bf16 layers")
     inp = wl.generate(w, seed=0, biases=True)
     dy_bits = wl.generate_dy(w, 0)
 

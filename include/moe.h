@@ -29,7 +29,10 @@
  *   b1, W2, b2, y, xbuf and hbuf. The router weights, router bias, noise,
  *   gates and zbuf are always fp32.
  * Errors.  A bad argument returns MOE_ERR_ARG (or MOE_ERR_UNSUPPORTED) before
- *   anything is enqueued. A failed launch returns MOE_ERR_CUDA. Conditions found
+ *   anything is enqueued. A failed launch returns MOE_ERR_CUDA; work enqueued
+ *   before the failure (on `stream` and, in moe_forward and moe_backward, on
+ *   the library's side stream) may still run, so synchronise the device before
+ *   reusing the call's buffers. Conditions found
  *   on the device -- a non-finite router logit, expert output or layer output
  *   (the Switch page raises on each), an index out of range, or a bounded wait
  *   that ran out -- are recorded in a status word inside `ws`;
