@@ -23,8 +23,10 @@
  *   default stream) and returns without synchronising. moe_forward() runs the
  *   balancing-loss finalize on a side stream of its own, forked from `stream`
  *   after the gate and joined back before it returns (so later work on
- *   `stream`, and stream capture, see one ordered forward); the side stream and
- *   its two events are created once per device on first use and kept.
+ *   `stream`, and stream capture, see one ordered forward); moe_backward forks
+ *   its gate branch onto the same side stream and joins it back before its
+ *   last kernel. The side stream and its two events are created once per
+ *   device on first use and kept.
  * Element types.  cfg->act_dtype (MOE_F32 or MOE_BF16) is the type of x, W1,
  *   b1, W2, b2, y, xbuf and hbuf. The router weights, router bias, noise,
  *   gates and zbuf are always fp32.
