@@ -93,6 +93,14 @@ MUTATIONS = {
                          "dP[i] += w_bal * ((double)mb[(size_t)t * E + i] - (p[i] > (double)thr[i] ? 1.0 : 0.0));"),
     "balbwd_softmax_mean_dropped": ("dH[(size_t)t * E + i] = p[i] * (dP[i] - pd);",
                                     "dH[(size_t)t * E + i] = p[i] * dP[i];"),
+    "load_uses_noisy_logit": ("p = orc_phi((c[(size_t)t * E + e] - thr) / s);",
+                              "p = orc_phi((H[(size_t)t * E + e] - thr) / s);"),
+    "capacity_without_k": ("double raw = floor((double)k * (double)T * cf / (double)E);",
+                           "double raw = floor((double)T * cf / (double)E);"),
+    "slot_position_inclusive": ("pos[(size_t)t * k + j] = p;", "pos[(size_t)t * k + j] = p + 1;"),
+    "residual_dropped": ("for (int i = 0; i < d; ++i) yt[i] = orc_in(x, x_dtype, (size_t)t * d + i);",
+                         "for (int i = 0; i < d; ++i) yt[i] = 0.0;"),
+    "cv2_over_mean": ("return var / (mean * mean);", "return var / mean;"),
 }
 
 
