@@ -728,7 +728,8 @@ def _finite_difference_check(orc, inp, dy, w, per_param, seed):
     """Central differences of the forward's scalar loss on sampled entries of
     every input. The forward's discrete choices (top-k, capacity, ReLU) make
     the loss piecewise smooth; an entry whose one-sided differences disagree
-    sits on a kink and is skipped (at most a few of them)."""
+    sits on a kink (or has a gradient near zero, where curvature alone
+    separates them) and is skipped: at most 3, or one in eight."""
     g = orc.backward(inp, dy, *w)
     L0 = orc.loss(inp, dy, *w)
     eps = 2.0 ** -12
@@ -753,7 +754,7 @@ def _finite_difference_check(orc, inp, dy, w, per_param, seed):
             fd = (Lp - Lm) / (2 * eps)
             assert abs(g[gname][i] - fd) <= 1e-5 * abs(fd) + 1e-7, (name, i, g[gname][i], fd)
             checked += 1
-    assert skipped <= max(2, checked // 10), (checked, skipped)
+    assert skipped <= max(3, checked // 8), (checked, skipped)
 
 
 def pin_backward_finite_differences(orc):
@@ -976,5 +977,26 @@ def pin_bal_backward_finite_differences(orc):
                 checked += 1
         assert skipped <= max(2, checked // 10), (checked, skipped)
 
+
+
+def pin_backward_varied_layers(orc):
+    """Central differences of the backward on more small layers: one expert,
+    k = E with noise, top-2 of 5 with heavy drops (cf = 0.5) and biases,
+    top-4 of 6 without noise but with a router bias, noisy Switch with drops,
+    and noisy top-1 of 2."""
+    layers = [  # (E, mode, k, T, d, d_ff, cf, noisy, router_bias, biases)
+        (1, TOPK, 1, 7, 4, 5, 1.0, True, False, True),
+        (3, TOPK, 3, 8, 4, 5, 1.0, True, True, False),
+        (5, TOPK, 2, 11, 5, 6, 0.5, True, False, True),
+        (6, TOPK, 4, 9, 4, 5, 1.0, False, True, False),
+        (4, SWITCH, 1, 10, 5, 4, 0.5, True, True, True),
+        (2, TOPK, 1, 8, 3, 7, 2.0, True, False, False),
+    ]
+    rng = np.random.default_rng(190)
+    for n, (E, mode, k, T, d, d_ff, cf, noisy, rb, biases) in enumerate(layers):
+        inp, dy = _grad_case(200 + n, T, d, E, d_ff, k, cf, mode, noisy, router_bias=rb,
+                             biases=biases)
+        w = tuple(float(v) for v in rng.uniform(0.2, 1.0, 3))
+        _finite_difference_check(orc, inp, dy, w, 6, 210 + n)
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
