@@ -3,11 +3,19 @@
 Each translation unit compiles to an object in parallel; the objects link
 into one shared library next to this file. No torch C++ headers are used, so
 the library loads with plain ctypes.
+
+An object is rebuilt unless its stamp file records the same key: a hash of
+nvcc's version banner, the architecture and flags, and the contents of the
+source and of every header it may include. So a changed flag, another nvcc or
+an object copied in from elsewhere never reuses stale code, whatever the files'
+modification times say.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
+import functools
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -38,11 +46,29 @@ def _cuda_lib_dirs(nvcc: str):
     return [d for d in dirs if os.path.isdir(d)]
 
 
-def _stale(obj: str, src: str, deps) -> bool:
-    if not os.path.exists(obj):
+@functools.lru_cache(maxsize=None)
+def _nvcc_banner(nvcc: str) -> str:
+    return subprocess.run([nvcc, "--version"], capture_output=True, text=True,
+                          check=True).stdout
+
+
+def _key(nvcc: str, cmd, src: str, deps) -> str:
+    h = hashlib.sha256()
+    h.update(_nvcc_banner(nvcc).encode())
+    h.update("\0".join(cmd).encode())
+    for p in [src, *deps]:
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(hashlib.sha256(f.read()).digest())
+    return h.hexdigest()
+
+
+def _stale(obj: str, key: str) -> bool:
+    stamp = obj + ".key"
+    if not (os.path.exists(obj) and os.path.exists(stamp)):
         return True
-    t = os.path.getmtime(obj)
-    return any(os.path.getmtime(p) > t for p in [src, *deps])
+    with open(stamp) as f:
+        return f.read().strip() != key
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
@@ -53,8 +79,10 @@ def build(verbose: bool = False, force: bool = False) -> str:
     jobs = []
     for src in srcs:
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        if force or _stale(obj, src, deps):
-            jobs.append([nvcc, *ARCH, *NVFLAGS, "-c", src, "-o", obj])
+        flags = [*ARCH, *NVFLAGS, "-c", os.path.basename(src)]
+        key = _key(nvcc, flags, src, deps)
+        if force or _stale(obj, key):
+            jobs.append(([nvcc, *ARCH, *NVFLAGS, "-c", src, "-o", obj], obj, key))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -63,15 +91,42 @@ def build(verbose: bool = False, force: bool = False) -> str:
         if r.returncode:
             raise RuntimeError("nvcc failed: " + " ".join(cmd))
 
+    def compile_one(job):
+        cmd, obj, key = job
+        stamp = obj + ".key"
+        if os.path.exists(stamp):
+            os.remove(stamp)
+        run(cmd)
+        with open(stamp, "w") as f:
+            f.write(key + "\n")
+
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
-        list(ex.map(run, jobs))
+        list(ex.map(compile_one, jobs))
     objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    if jobs or not os.path.exists(LIB):
+    # The library's key: every object's key and the link flags.
+    h = hashlib.sha256(" ".join([*ARCH, "-shared", "-cudart", "static"]).encode())
+    for o in objs:
+        with open(o + ".key") as f:
+            h.update(f.read().encode())
+    lib_key = h.hexdigest()
+    lib_stamp = os.path.join(BUILD_DIR, "libmoe.so.key")
+    if force or jobs or _stale_lib(lib_stamp, lib_key):
         libdirs = [f"-L{d}" for d in _cuda_lib_dirs(nvcc)]
         tmp = LIB + f".{os.getpid()}.tmp"
+        if os.path.exists(lib_stamp):
+            os.remove(lib_stamp)
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, *libdirs, "-cudart", "static"])
         os.replace(tmp, LIB)
+        with open(lib_stamp, "w") as f:
+            f.write(lib_key + "\n")
     return LIB
+
+
+def _stale_lib(stamp: str, key: str) -> bool:
+    if not (os.path.exists(LIB) and os.path.exists(stamp)):
+        return True
+    with open(stamp) as f:
+        return f.read().strip() != key
 
 
 if __name__ == "__main__":
