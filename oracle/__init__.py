@@ -596,6 +596,16 @@ def variant(src_path: str, out_dir: str) -> Oracle:
     return Oracle(out)
 
 
+def set_threads(n: int) -> int:
+    """Set the number of OpenMP threads the oracle's parallel loops use (its
+    arithmetic and results do not depend on it); returns the previous count.
+    Used to time the oracle on one host core beside all of them."""
+    lib = default().lib
+    prev = int(lib.omp_get_max_threads())
+    lib.omp_set_num_threads(ctypes.c_int(int(n)))
+    return prev
+
+
 def capacity(*a, **k):
     return default().capacity(*a, **k)
 
