@@ -21,12 +21,19 @@
  *   workspace `ws` of moe_workspace_size() bytes (256-byte aligned).
  * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *   default stream) and returns without synchronising. moe_forward() runs the
- *   balancing-loss finalize on a side stream of its own, forked from `stream`
- *   after the gate and joined back before it returns (so later work on
- *   `stream`, and stream capture, see one ordered forward); moe_backward forks
- *   its gate branch onto the same side stream and joins it back before its
- *   last kernel. The side stream and its two events are created once per
- *   device on first use and kept.
+ *   balancing-loss finalize on a side stream, forked from `stream` after the
+ *   gate and joined back before it returns (so later work on `stream`, and
+ *   stream capture, see one ordered forward); moe_backward forks its gate
+ *   branch onto the side stream and joins it back before its last kernel.
+ *   Each device has a pool of 8 side streams, made on the first such call
+ *   that is not under stream capture (make one call before capturing if the
+ *   captured graph should keep the overlap) and kept; each serves one caller
+ *   stream, so calls on different streams -- from different host threads,
+ *   one of them capturing a graph while another runs eagerly -- never share
+ *   a side stream. When none fits (the pool is not made yet and `stream` is
+ *   capturing; 8 other caller streams hold them; a side stream in another
+ *   capture) the call runs everything on `stream`, with the same results.
+ *   After cudaDeviceReset the next call makes a new pool.
  * Element types.  cfg->act_dtype (MOE_F32 or MOE_BF16) is the type of x, W1,
  *   b1, W2, b2, y, xbuf and hbuf. The router weights, router bias, noise,
  *   gates and zbuf are always fp32.
@@ -199,19 +206,32 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
  * it (each term rounded up to 256) and returns MOE_ERR_UNSUPPORTED, enqueuing
  * nothing, if that is more. It allocates nothing and frees nothing.
  *
- * The first call on each device looks up the array's device address
+ * The first call on each device (and again after cudaDeviceReset, or in
+ * another context) looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture. All calls share the one array: calls whose work
  * overlaps on the GPU (other streams, other host threads) race and must be
- * serialised by the caller. Device-side index errors are not reported here;
- * an expert index outside [0, E) yields pos = -1 and keep = 0 for that
- * assignment.
+ * serialised by the caller. An expert index outside [0, E) yields pos = -1
+ * and keep = 0 for that assignment and is recorded (MOE_ERR_BOUNDS, detail =
+ * the flat index t*k + j) in a status word inside the same array, which
+ * moe_noalloc_last_status() reads; each call clears it when it starts.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx, const float *gate,
                          const void *x, int32_t *pos, uint8_t *keep, int32_t *expert_count,
                          int32_t *expert_offset, void *xbuf, int32_t *row_token,
                          float *row_gate, moe_stream_t stream);
+
+/*
+ * The device-side status of the last moe_dispatch_noalloc on the current
+ * device, its counterpart of moe_last_device_status (the pages have none
+ * either): synchronises `stream` (the stream that call used), returns
+ * MOE_OK or the first error recorded since the call started (MOE_ERR_BOUNDS
+ * for an expert index outside [0, E)), writes its detail word to *detail if
+ * non-NULL, and clears it. It copies 24 bytes device-to-host into a local
+ * variable and allocates nothing.
+ */
+int moe_noalloc_last_status(moe_stream_t stream, int64_t *detail);
 
 /*
  * Hierarchical layer ("Outrageously Large Neural Networks", Hierarchical
@@ -343,6 +363,17 @@ int moe_gate_backward(const moe_config *cfg, const void *x, const float *Wg, con
                       const float *dgate, float w_load, float w_aux, float *dWg, float *dWnoise,
                       float *dlogit_bias, float *dx_gate, void *ws, void *bws,
                       moe_stream_t stream);
+
+/*
+ * Diagnostic: out[i] = Phi(u[i]) for i < n, the standard normal CDF exactly as
+ * the balancing kernels evaluate it inside the load estimator P(x, i) =
+ * Phi((c_i - kth_excluding(H, k, i)) / sigma_i) ("Outrageously Large", Eq. 9),
+ * so its accuracy can be checked on any grid. u, out [n] fp32 device arrays
+ * (n = 0: nothing is enqueued). The library's Phi is erfc(-u / sqrt 2) / 2
+ * with erfc from the Chebyshev fit of Numerical Recipes (Press et al., 2nd
+ * ed., section 6.2, "erfcc"), evaluated in fp32.
+ */
+int moe_eval_normal_cdf(const float *u, float *out, int64_t n, moe_stream_t stream);
 
 /*
  * Synchronises `stream`, returns the first device-side error recorded in `ws`

@@ -27,7 +27,8 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate"
            "moe_expert_ffn", "moe_combine", "moe_aux_loss", "moe_forward",
            "moe_last_device_status", "moe_dispatch_noalloc", "moe_hier_workspace_size",
            "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced",
-           "moe_backward_workspace_size", "moe_backward", "moe_gate_backward")
+           "moe_backward_workspace_size", "moe_backward", "moe_gate_backward",
+           "moe_noalloc_last_status", "moe_eval_normal_cdf")
 
 
 class MoEError(RuntimeError):
@@ -94,6 +95,8 @@ def lib():
             L.moe_forward.argtypes = [CP] + [P] * 17
             L.moe_last_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int64)]
             L.moe_dispatch_noalloc.argtypes = [CP] + [P] * 11
+            L.moe_noalloc_last_status.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
+            L.moe_eval_normal_cdf.argtypes = [P, P, ctypes.c_int64, P]
             HP = ctypes.POINTER(moe_hier_config)
             L.moe_hier_workspace_size.argtypes = [HP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_hier.argtypes = [HP] + [P] * 19
@@ -246,6 +249,15 @@ def moe_gate_backward(cfg, x, Wg, Wnoise, noise, expert_idx, gate, dgate, w_load
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
+def noalloc_scratch_need(cfg) -> int:
+    """Bytes of the static scratch array moe_dispatch_noalloc needs for cfg:
+    the status word, two [ceil(T*k/512), E] int32 tables and the E+1 tile
+    offsets, each rounded up to 256 bytes."""
+    r256 = lambda v: (v + 255) // 256 * 256
+    chunks = (cfg.T * cfg.k + 511) // 512
+    return 256 + 2 * r256(chunks * cfg.E * 4) + r256((cfg.E + 1) * 4)
+
+
 def moe_dispatch_noalloc(cfg, expert_idx, gate, x, pos, keep, expert_count, expert_offset, xbuf,
                          row_token, row_gate, stream=None):
     """moe_dispatch without a workspace, for callers that cannot allocate
@@ -253,10 +265,25 @@ def moe_dispatch_noalloc(cfg, expert_idx, gate, x, pos, keep, expert_count, expe
     st = lib().moe_dispatch_noalloc(ctypes.byref(cfg), _p(expert_idx), _p(gate), _p(x), _p(pos),
                                     _p(keep), _p(expert_count), _p(expert_offset), _p(xbuf),
                                     _p(row_token), _p(row_gate), _stream(stream))
-    if st == 2:
-        raise MoEError(st, "moe_dispatch_noalloc: these sizes need more scratch than the "
+    if st == 2 and noalloc_scratch_need(cfg) > NOALLOC_SCRATCH_BYTES:
+        raise MoEError(st, "moe_dispatch_noalloc: these sizes need "
+                           f"{noalloc_scratch_need(cfg)} bytes of scratch, more than the "
                            f"library's static {NOALLOC_SCRATCH_BYTES >> 20} MiB array")
     _check(st, "moe_dispatch_noalloc")
+
+
+def moe_noalloc_last_status(stream=None):
+    """Synchronise, return (status, detail) of the last moe_dispatch_noalloc
+    on the current device, and clear it."""
+    det = ctypes.c_int64()
+    st = lib().moe_noalloc_last_status(_stream(stream), ctypes.byref(det))
+    return st, det.value
+
+
+def moe_eval_normal_cdf(u, out, stream=None):
+    """out = Phi(u) as the library's balancing kernels evaluate it (fp32)."""
+    _check(lib().moe_eval_normal_cdf(_p(u), _p(out), int(u.numel()), _stream(stream)),
+           "moe_eval_normal_cdf")
 
 
 def moe_last_device_status(ws, stream=None):

@@ -1304,3 +1304,33 @@ cudaError_t launch_hier_tail(int T, int a, int b, const float2 *aux_s, const flo
 }
 
 }  // namespace moe
+
+// ----------------------------------------------------------------------------- diagnostic: Phi
+// The load estimator's normal CDF, evaluated elementwise, so that its accuracy
+// can be checked against a reference CDF on any grid.
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256)
+k_normal_cdf(long long n, const float *__restrict__ u, float *__restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    out[i] = normal_cdf(u[i]);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_eval_normal_cdf(const float *u, float *out, int64_t n, moe_stream_t stream) {
+  using namespace moe;
+  if (n < 0 || (n > 0 && (!u || !out))) return MOE_ERR_ARG;
+  if (n == 0) return MOE_OK;
+  const long long blocks = (n + 255) / 256;
+  const int grid = (int)(blocks < 4 * 152 ? blocks : 4 * 152);
+  if (launch_pdl(k_normal_cdf, grid, 256, 0, (cudaStream_t)stream, (long long)n, u, out) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -258,29 +258,44 @@ namespace moe {
 namespace {
 
 constexpr size_t kNoAllocBytes = MOE_NOALLOC_SCRATCH_BYTES;
-constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
-
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
 // Device address of the scratch array on the current device. In host code the
-// array's name is only a stand-in, so the address is looked up once per
-// device, with that device current, and cached.
+// array's name is only a stand-in, so the address is looked up with the
+// device current (cudaGetSymbolAddress), once per device and context: the
+// cache entry remembers the context it was taken in, and a call made in
+// another context -- after cudaDeviceReset, or under a context the caller
+// made current -- looks the address up again. The first lookup in a context
+// loads the library's module there.
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+struct NoAllocEntry {
+  void *ctx = nullptr, *ptr = nullptr;
+};
+NoAllocEntry g_noalloc[kNoAllocMaxDevices];
+
 int noalloc_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
+  void *ctx = current_context();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoAllocEntry &e = g_noalloc[dev];
+  if (!e.ptr || !ctx || e.ctx != ctx) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      e = NoAllocEntry{};
+      return MOE_ERR_CUDA;
+    }
+    // Re-read the context: the lookup itself may have created the primary one.
+    e.ctx = current_context();
+    e.ptr = p;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = e.ptr;
   return MOE_OK;
 }
 
@@ -328,4 +343,18 @@ extern "C" int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert
   if (launch_gather(*cfg, x, expert_offset, row_token, xbuf, st, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" int moe_noalloc_last_status(moe_stream_t stream, int64_t *detail) {
+  using namespace moe;
+  void *scratch = nullptr;
+  const int r = noalloc_scratch(&scratch);
+  if (r != MOE_OK) return r;
+  DeviceStatus h{};
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&h, scratch, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(scratch, 0, sizeof h) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = h.detail;
+  return h.code;
 }

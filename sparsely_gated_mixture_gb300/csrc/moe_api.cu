@@ -13,6 +13,23 @@ namespace moe {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+void *current_context() {
+  using GetCurrent = int (*)(void **);  // CUresult cuCtxGetCurrent(CUcontext *)
+  static const GetCurrent fn = [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<GetCurrent>(ptr);
+    cudaGetLastError();
+    return static_cast<GetCurrent>(nullptr);
+  }();
+  void *ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
 bool pdl_enabled(int cls) {
   static const unsigned mask = [] {
     const char *v = getenv("MOE_PDL_MASK");
@@ -331,37 +348,117 @@ static BwdLayout bwd_layout(const moe_config &cfg) {
   return L;
 }
 
-// One side stream (non-blocking) and a fork / join event pair per device,
-// made on first use and kept; the lock is held while a call enqueues on them,
-// so calls from several host threads do not interleave their records.
+// Side streams. moe_forward and moe_backward fork part of their work onto a
+// side stream and join it back before they return. Each device has a pool of
+// kSidePool non-blocking side streams (with a fork / join event pair each),
+// made together on the first call that is not under stream capture, and each
+// side stream serves ONE caller stream (the legacy and per-thread default
+// streams keyed by thread as well): calls on independent caller streams never
+// share a side stream, so neither serialise on it nor drag one another's work
+// into a graph being captured. A call runs everything on its own stream
+// instead (same kernels, same results) when no side stream fits: the pool is
+// not made yet and the caller is capturing, all kSidePool are taken by other
+// caller streams, or the side stream's capture state does not match the
+// caller's (idle when the caller is not capturing; idle or in the caller's
+// own capture when it is). The pool belongs to the context it was made in; a
+// call from another context (after cudaDeviceReset) makes a new one. The lock
+// is held while a call enqueues on its side stream, so calls from several
+// host threads do not interleave their records.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 constexpr int kSideMaxDevices = 64;
+constexpr int kSidePool = 8;
+struct DeviceSides {
+  void *ctx = nullptr;
+  bool made = false, failed = false;
+  int used = 0;
+  SideStream pool[kSidePool];
+  cudaStream_t owner[kSidePool] = {};
+  size_t owner_thread[kSidePool] = {};
+};
 static std::mutex g_side_mu;
-static SideStream g_side[kSideMaxDevices];
-static bool g_side_failed[kSideMaxDevices] = {};
+static DeviceSides g_side[kSideMaxDevices];
 
-static SideStream *side_stream(std::unique_lock<std::mutex> &lock) {
+// Identifies the calling thread for the default streams, which differ (per
+// thread) or are shared (legacy) without a distinct handle.
+static size_t side_thread_key(cudaStream_t caller) {
+  if (caller != cudaStreamPerThread && caller != nullptr) return 0;
+  static thread_local char tag;
+  return caller == cudaStreamPerThread ? reinterpret_cast<size_t>(&tag) : 0;
+}
+
+static SideStream *side_stream(std::unique_lock<std::mutex> &lock, cudaStream_t caller) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideMaxDevices) return nullptr;
-  lock = std::unique_lock<std::mutex>(g_side_mu);
-  SideStream &ss = g_side[dev];
-  if (!ss.s && !g_side_failed[dev]) {
-    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
-      g_side_failed[dev] = true;
-      ss = SideStream{};
-      cudaGetLastError();
-    }
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
   }
-  if (!ss.s) {
+  cudaStreamCaptureStatus cst = cudaStreamCaptureStatusNone;
+  unsigned long long cid = 0;
+  if (cudaStreamGetCaptureInfo(caller, &cst, &cid) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cst == cudaStreamCaptureStatusInvalidated) return nullptr;
+  void *ctx = current_context();
+  lock = std::unique_lock<std::mutex>(g_side_mu);
+  DeviceSides &D = g_side[dev];
+  if ((D.made || D.failed) && D.ctx != ctx) D = DeviceSides{};  // the old context's are gone
+  if (!D.made) {
+    if (D.failed || cst != cudaStreamCaptureStatusNone) {
+      lock.unlock();
+      return nullptr;
+    }
+    bool ok = true;
+    for (int i = 0; i < kSidePool && ok; ++i) {
+      SideStream &ss = D.pool[i];
+      ok = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
+    }
+    D.ctx = ctx;
+    if (!ok) {
+      cudaGetLastError();
+      for (SideStream &ss : D.pool) {
+        if (ss.join) cudaEventDestroy(ss.join);
+        if (ss.fork) cudaEventDestroy(ss.fork);
+        if (ss.s) cudaStreamDestroy(ss.s);
+        ss = SideStream{};
+      }
+      D.failed = true;
+      lock.unlock();
+      return nullptr;
+    }
+    D.made = true;
+  }
+  const size_t tkey = side_thread_key(caller);
+  int slot = -1;
+  for (int i = 0; i < D.used; ++i)
+    if (D.owner[i] == caller && D.owner_thread[i] == tkey) slot = i;
+  if (slot < 0 && D.used < kSidePool) {
+    slot = D.used++;
+    D.owner[slot] = caller;
+    D.owner_thread[slot] = tkey;
+  }
+  if (slot < 0) {
     lock.unlock();
     return nullptr;
   }
-  return &ss;
+  cudaStreamCaptureStatus sst = cudaStreamCaptureStatusNone;
+  unsigned long long sid = 0;
+  const bool side_ok =
+      cudaStreamGetCaptureInfo(D.pool[slot].s, &sst, &sid) == cudaSuccess &&
+      (sst == cudaStreamCaptureStatusNone ||
+       (sst == cudaStreamCaptureStatusActive && cst == cudaStreamCaptureStatusActive &&
+        sid == cid));
+  if (!side_ok) {
+    cudaGetLastError();
+    lock.unlock();
+    return nullptr;
+  }
+  return &D.pool[slot];
 }
 
 }  // namespace moe
@@ -503,7 +600,7 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
   SideStream *side = nullptr;
   std::unique_lock<std::mutex> side_lock;
   if (aux_out3) {
-    side = side_stream(side_lock);
+    side = side_stream(side_lock, s);
     cudaStream_t fs = s;
     if (side) {
       MOE_CUDA(cudaEventRecord(side->fork, s));
@@ -801,7 +898,7 @@ int moe_backward(const moe_config *cfg, const void *x, const float *Wg, const fl
   // persistent GEMM CTAs of the other branch, which stays on `stream`.
   SideStream *side = nullptr;
   std::unique_lock<std::mutex> side_lock;
-  side = side_stream(side_lock);
+  side = side_stream(side_lock, s);
   cudaStream_t fs = s;
   if (side) {
     MOE_CUDA(cudaEventRecord(side->fork, s));

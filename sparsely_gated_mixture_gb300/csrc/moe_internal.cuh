@@ -91,6 +91,12 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_config &cfg);
 
+// The calling thread's current CUDA context (a CUcontext, fetched through the
+// runtime's driver entry point; the library does not link libcuda), or null if
+// none is current. Host caches of per-context objects compare it to notice a
+// context that was reset or replaced.
+void *current_context();
+
 template <typename T>
 inline T *ws_at(void *ws, size_t off) {
   return reinterpret_cast<T *>(static_cast<char *>(ws) + off);

@@ -75,5 +75,48 @@ def test_noalloc_dispatch_rejects_sizes_beyond_its_scratch():
     fake = 1 << 20  # never dereferenced: the size check fails first
     st = B.lib().moe_dispatch_noalloc(ctypes.byref(cfg), *([fake] * 10), None)
     assert st == 2  # MOE_ERR_UNSUPPORTED
+    assert B.noalloc_scratch_need(cfg) > B.NOALLOC_SCRATCH_BYTES
     with pytest.raises(B.MoEError, match="static 4 MiB"):
         B.moe_dispatch_noalloc(cfg, *([fake] * 10), stream=0)
+    # Too many experts is unsupported for another reason: no scratch message.
+    wide = B.config(64, 64, 2048, 64, 2, 1.0)
+    assert B.noalloc_scratch_need(wide) <= B.NOALLOC_SCRATCH_BYTES
+    with pytest.raises(B.MoEError) as e:
+        B.moe_dispatch_noalloc(wide, *([fake] * 10), stream=0)
+    assert e.value.status == 2 and "scratch" not in str(e.value)
+
+
+@pytest.mark.gpu
+def test_noalloc_dispatch_reports_bad_expert_index():
+    """An expert index outside [0, E) is skipped by every kernel of the call
+    (pos = -1, keep = 0, no row) and recorded in the static array's status
+    word, which moe_noalloc_last_status reads back and clears; the next call
+    starts from a clear word. moe_dispatch, given the same indices, reports
+    the same error through its workspace and writes the same outputs."""
+    w = wl.WORKLOADS["noisy_top4_e16"].with_(T=300)
+    inp = wl.generate(w, seed=22)
+    d = to_device(w, inp)
+    cfg = B.config_for(w)
+    ws = workspace(cfg)
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    thr = torch.empty((w.T, 2), dtype=torch.float32, device="cuda")
+    B.moe_gate(cfg, d["x"], d["Wg"], d["Wn"], d["noise"], d["bias"], idx, gate, thr, ws)
+    assert B.moe_last_device_status(ws)[0] == 0
+    bad = idx.clone()
+    bad[57, 2] = w.E  # flat index 57 * k + 2
+    ref = _outputs(w)
+    B.moe_dispatch(cfg, bad, gate, d["x"], ref["pos"], ref["keep"], ref["count"], ref["offset"],
+                   ref["xbuf"], ref["row_token"], ref["row_gate"], ws)
+    assert B.moe_last_device_status(ws) == (6, 57 * w.k + 2)
+    got = _outputs(w)
+    B.moe_dispatch_noalloc(cfg, bad, gate, d["x"], got["pos"], got["keep"], got["count"],
+                           got["offset"], got["xbuf"], got["row_token"], got["row_gate"])
+    assert B.moe_noalloc_last_status() == (6, 57 * w.k + 2)  # MOE_ERR_BOUNDS, flat index
+    assert B.moe_noalloc_last_status() == (0, 0)  # read once, then cleared
+    _same(ref, got)
+    assert int(got["pos"][57, 2].item()) == -1 and int(got["keep"][57, 2].item()) == 0
+    good = _outputs(w)
+    B.moe_dispatch_noalloc(cfg, idx, gate, d["x"], good["pos"], good["keep"], good["count"],
+                           good["offset"], good["xbuf"], good["row_token"], good["row_gate"])
+    assert B.moe_noalloc_last_status() == (0, 0)
