@@ -742,11 +742,14 @@ def run_hier(args, w: wl.HierWorkload):
     return line
 
 
-def run_balanced(args, w: wl.Workload):
-    """Strictly balanced gating: the value is moe_forward_balanced over
-    resident inputs (median of the timed steps, L2 flushed before each); the
-    expert GEMMs are also timed through moe_expert_ffn on the same row layout
-    (m rows for every expert), interleaved."""
+def run_balanced(args, w: wl.Workload, threshold: bool = False):
+    """Strictly balanced gating: the value is moe_forward_balanced (batchwise
+    mask) or, with threshold, moe_forward_threshold (the inference-time
+    threshold mask, thresholds from wl.thresholds) over resident inputs
+    (median of the timed steps, L2 flushed before each); the expert GEMMs are
+    also timed through moe_expert_ffn on the same row layout (m rows for
+    every expert; the forward's own rows per expert for the threshold mask),
+    interleaved."""
     import torch
     import torch.distributed as dist
 
@@ -773,25 +776,50 @@ def run_balanced(args, w: wl.Workload):
     W1, W2 = to_dev(inp["W1"], True), to_dev(inp["W2"], True)
     cfg = B.config_for(w)
     T, E, d, dff = w.T, w.E, w.d, w.d_ff
-    m = max(1, min(T, (w.k * T) // E))
-    R = E * m
     z = dict(device=dev)
-    ws = torch.empty(B.moe_balanced_workspace_size(cfg), dtype=torch.uint8, **z)
-    ws_f = torch.empty(B.moe_workspace_size(cfg), dtype=torch.uint8, **z)
     y = torch.empty((T, d), dtype=act, **z)
-    offset = torch.arange(0, (E + 1) * m, m, dtype=torch.int32, **z)
-    xbuf = torch.randn((R, d), **z).to(act)
-    row_gate = torch.ones(R, dtype=torch.float32, **z)
-    hbuf = torch.empty((R, dff), dtype=act, **z)
-    zbuf = torch.empty((R, d), dtype=torch.float32, **z)
+    if threshold:
+        thr = torch.from_numpy(wl.thresholds(w)).to(dev)
+        ws = torch.empty(B.moe_threshold_workspace_size(cfg), dtype=torch.uint8, **z)
+        picks = torch.empty((T, w.k), dtype=torch.int32, **z)
+        B.moe_forward_threshold(cfg, x, Wg, None, thr, W1, None, W2, None, y, ws, picks, None,
+                                None, stream)
+        st, det = B.moe_last_device_status(ws, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {B.STATUS_NAMES[st]} ({det})")
+        counts = torch.bincount(picks[picks < E].long(), minlength=E)
+        offset = torch.cat([torch.zeros(1, dtype=torch.int64, **z), counts.cumsum(0)]).to(
+            torch.int32)
+        R = int(counts.sum().item())
+        m = R / E  # mean rows per expert (the label)
+        # the stage call's buffers: T*k rows, of which the first R are live
+        fcfg = cfg
+    else:
+        m = max(1, min(T, (w.k * T) // E))
+        R = E * m
+        ws = torch.empty(B.moe_balanced_workspace_size(cfg), dtype=torch.uint8, **z)
+        offset = torch.arange(0, (E + 1) * m, m, dtype=torch.int32, **z)
+        fcfg = cfg
+    ws_f = torch.empty(B.moe_workspace_size(fcfg), dtype=torch.uint8, **z)
+    # moe_expert_ffn's row buffers hold T*k rows (its contract: the GEMMs'
+    # tensor maps span them, and a ragged last tile reads past the live rows).
+    rows_alloc = max(R, T * fcfg.k)
+    xbuf = torch.randn((rows_alloc, d), **z).to(act)
+    row_gate = torch.ones(rows_alloc, dtype=torch.float32, **z)
+    hbuf = torch.empty((rows_alloc, dff), dtype=act, **z)
+    zbuf = torch.empty((rows_alloc, d), dtype=torch.float32, **z)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, **z)
 
     def fwd(xx=x, yy=y):
-        B.moe_forward_balanced(cfg, xx, Wg, None, None, W1, None, W2, None, yy, None, None, ws,
-                               stream)
+        if threshold:
+            B.moe_forward_threshold(cfg, xx, Wg, None, thr, W1, None, W2, None, yy, ws,
+                                    stream=stream)
+        else:
+            B.moe_forward_balanced(cfg, xx, Wg, None, None, W1, None, W2, None, yy, None, None,
+                                   ws, stream)
 
     def ffn():
-        B.moe_expert_ffn(cfg, xbuf, offset, row_gate, W1, None, W2, None, hbuf, zbuf, ws_f,
+        B.moe_expert_ffn(fcfg, xbuf, offset, row_gate, W1, None, W2, None, hbuf, zbuf, ws_f,
                          stream)
 
     for _ in range(args.warmup):
@@ -892,18 +920,26 @@ def run_balanced(args, w: wl.Workload):
     roof.update({"peak_source": peak_kind, "algorithmic_flops_per_launch": ffn_flops,
                  "algorithmic_bytes": ffn_bytes, "traffic": None})
     tc = w.dtype == "bf16" and w.d % 8 == 0
-    # router (split + tensor-core kernel), mask memset, softmax, select,
-    # token gates, gather, two GEMMs, combine
-    launches = (2 if tc else 1) + 3 + 1 + 2 + 1
+    if threshold:
+        # router (split + tensor-core kernel), threshold gate, three slot
+        # kernels, gather, two GEMMs, combine
+        launches = (2 if tc else 1) + 1 + 3 + 1 + 2 + 1
+    else:
+        # router (split + tensor-core kernel), mask memset, softmax, select,
+        # token gates, gather, two GEMMs, combine
+        launches = (2 if tc else 1) + 3 + 1 + 2 + 1
     line = {
-        "metric": "strictly balanced MoE layer fwd tokens/s @1 GB300",
+        "metric": ("threshold-mask MoE layer fwd tokens/s @1 GB300" if threshold else
+                   "strictly balanced MoE layer fwd tokens/s @1 GB300"),
         "value": job_tokens_per_s(world, T, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) tokens, N(0,1/fan_in) weights)",
         "config": {"workload": w.name, "T": T, "d": d, "E": E, "d_ff": dff, "k": w.k,
-                   "rows_per_expert": m, "gate": "batchwise mask", "seed": 0,
+                   "rows_per_expert": m,
+                   "gate": ("threshold mask, T_i = %g/E" % wl.THR_SCALE if threshold
+                            else "batchwise mask"), "seed": 0,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "flushed between steps (256 MiB write)"},
         "roofline": roof,
@@ -915,7 +951,7 @@ def run_balanced(args, w: wl.Workload):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_bal(w, inp, args.cpu_sample)
+        line["cpu_baseline"] = cpu_baseline_bal(w, inp, args.cpu_sample, threshold)
     if world > 1:
         dist.destroy_process_group()
     return line
@@ -1146,11 +1182,14 @@ def cpu_baseline_bwd(w: wl.Workload, inp: dict, dy_bits, wts, n_sample: int) -> 
                       f"({t:.2f} s), as a layer of {n} tokens"}
 
 
-def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int) -> dict:
+def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int, threshold: bool = False) -> dict:
     """The oracle's balanced layer on the host cores: router, softmax and the
-    batchwise mask over every token, the expert loop for n_sample tokens,
-    extrapolated."""
+    batchwise mask (or the threshold mask) over every token, the expert loop
+    for n_sample tokens, extrapolated."""
     import oracle
+
+    if threshold:
+        inp = dict(inp, mode_bal=1, thr=wl.thresholds(w), with_loss=False)
 
     cores = len(os.sched_getaffinity(0))
     n = min(n_sample, w.T)
@@ -1165,7 +1204,8 @@ def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int) -> dict:
     full = t_gate + t_ffn * (w.T / n)
     return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "extrapolated": True, "timed_tokens": n, "step_s": t_gate + t_all,
-            "sample": f"router, softmax and batchwise mask over all {w.T} tokens "
+            "sample": f"router, softmax and {'threshold' if threshold else 'batchwise'} mask "
+                      f"over all {w.T} tokens "
                       f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens, "
                       f"extrapolated to {w.T} tokens"}
 
@@ -1324,7 +1364,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="top2_large_experts",
                     choices=sorted(wl.WORKLOADS) + sorted(wl.HIER_WORKLOADS)
-                    + sorted(wl.BAL_WORKLOADS))
+                    + sorted(wl.BAL_WORKLOADS) + sorted(wl.THR_WORKLOADS))
     ap.add_argument("--cpu-sample", type=int, default=16,
                     help="tokens whose expert loop the oracle runs for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1344,19 +1384,23 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    if args.workload in wl.BAL_WORKLOADS:
-        w = wl.BAL_WORKLOADS[args.workload]
+    if args.workload in wl.BAL_WORKLOADS or args.workload in wl.THR_WORKLOADS:
+        thr_mode = args.workload in wl.THR_WORKLOADS
+        w = (wl.THR_WORKLOADS if thr_mode else wl.BAL_WORKLOADS)[args.workload]
         if args.tokens:
             w = w.with_(T=args.tokens)
         if args.impl == "reference":
             rank, world, _ = dist_env()
             if rank == 0:
                 inp = wl.generate(w, seed=0)
-                vals = [cpu_baseline_bal(w, inp, args.cpu_sample) for _ in range(args.steps)]
+                vals = [cpu_baseline_bal(w, inp, args.cpu_sample, thr_mode)
+                        for _ in range(args.steps)]
                 v = statistics.mean(x["value"] for x in vals)
                 print(json.dumps({
-                    "impl": "reference", "metric": "strictly balanced MoE layer fwd tokens/s "
-                    "@1 GB300", "value": v, "unit": "tokens/s", "n_gpus": world,
+                    "impl": "reference",
+                    "metric": ("threshold-mask MoE layer fwd tokens/s @1 GB300" if thr_mode else
+                               "strictly balanced MoE layer fwd tokens/s @1 GB300"),
+                    "value": v, "unit": "tokens/s", "n_gpus": world,
                     "steps": args.steps, "warmup": args.warmup,
                     "ms_per_step": statistics.mean(x["step_s"] for x in vals) * 1e3,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1366,7 +1410,7 @@ def main():
                     "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}), flush=True)
             return
-        line = run_balanced(args, w)
+        line = run_balanced(args, w, thr_mode)
         if line is not None:
             print(json.dumps(line), flush=True)
         return

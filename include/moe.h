@@ -304,6 +304,35 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
                          float *loss_out, uint32_t *mask_out, void *ws, moe_stream_t stream);
 
 /*
+ * Threshold mask, the inference-time gate of strictly balanced gating
+ * ("Outrageously Large Neural Networks", Strictly Balanced Gating: at
+ * inference examples arrive one at a time, so the batchwise mask is replaced
+ * by per-expert thresholds, M_threshold(x, T)_i = 1 iff x_i > T_i). With P =
+ * Softmax(x Wg + logit_bias) over all E experts (dense, fp32, no noise), token
+ * t picks every expert i with P[t,i] > thresholds[i] (strictly greater: P
+ * equal to T_i is not taken); a pick's gate is P renormalised over the
+ * token's own picks; y = x + sum over the picks, in expert order, of gate *
+ * E_i(x) (fp32 sum, rounded once). A token that passes no threshold keeps
+ * only the residual. No capacity: every pick is computed. Uses T, d, E, d_ff,
+ * act_dtype and k of cfg, where k (1..min(E, 16)) is the caller's bound on
+ * any token's picks, which sizes the workspace (a token's picks are fewer
+ * than 1 / min_i T_i, so k >= that bound always holds); a token with more
+ * than k picks records MOE_ERR_BOUNDS (detail = the token) and only its
+ * first k picks (in expert order) reach y. capacity_factor, min_capacity and
+ * gate_mode are not used. thresholds [E] fp32. Optional outputs (NULL to
+ * skip): expert_idx [T,k] int32, a token's picks in expert order then E;
+ * gate [T,k] fp32, their gates then 0; mask_out [T][ceil(E/32)] uint32, bit
+ * (i % 32) of word i / 32 set for every pick. The status word at the start
+ * of `ws` (moe_threshold_workspace_size bytes) is cleared first.
+ */
+int moe_threshold_workspace_size(const moe_config *cfg, size_t *bytes);
+int moe_forward_threshold(const moe_config *cfg, const void *x, const float *Wg,
+                          const float *logit_bias, const float *thresholds, const void *W1,
+                          const void *b1, const void *W2, const void *b2, void *y,
+                          int32_t *expert_idx, float *gate, uint32_t *mask_out, void *ws,
+                          moe_stream_t stream);
+
+/*
  * Backward of the flat layer ("Outrageously Large Neural Networks", section
  * 3.4, "Training the gating network": plain back-propagation, gradients reach
  * W_g through the selected softmax gates and W_noise through the smooth load

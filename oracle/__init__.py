@@ -553,7 +553,8 @@ class Oracle:
         (or the threshold mask when ``inp['mode_bal'] == 1``), the renormalised
         gates, y = x + sum over picked experts of gate * E_i(x) (no capacity:
         the mask fixes every expert's rows), and L_batchwise when thresholds
-        are given."""
+        are given (unless ``inp['with_loss']`` is false: the inference-time
+        threshold layer has no loss)."""
         x = inp["x"]
         T = x.shape[0]
         E = inp["Wg"].shape[1]
@@ -568,7 +569,7 @@ class Oracle:
         y, bad_y = self.layer_out(x, idx, gate, mask, inp["W1"], inp["W2"], inp.get("b1"),
                                   inp.get("b2"), tokens)
         out = dict(H=H, P=P, m=m, mask=mask, gate=gate, y=y, nonfinite=bad_h or bad_y)
-        if thr is not None:
+        if thr is not None and inp.get("with_loss", True):
             mb = mask if mode == 0 else self.bal_gate(P, m, None, 0)[0]
             out["loss"] = self.bal_loss(P, mb, thr)
         return out

@@ -28,7 +28,8 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate"
            "moe_last_device_status", "moe_dispatch_noalloc", "moe_hier_workspace_size",
            "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced",
            "moe_backward_workspace_size", "moe_backward", "moe_gate_backward",
-           "moe_noalloc_last_status", "moe_eval_normal_cdf")
+           "moe_noalloc_last_status", "moe_eval_normal_cdf", "moe_threshold_workspace_size",
+           "moe_forward_threshold")
 
 
 class MoEError(RuntimeError):
@@ -97,6 +98,8 @@ def lib():
             L.moe_dispatch_noalloc.argtypes = [CP] + [P] * 11
             L.moe_noalloc_last_status.argtypes = [P, ctypes.POINTER(ctypes.c_int64)]
             L.moe_eval_normal_cdf.argtypes = [P, P, ctypes.c_int64, P]
+            L.moe_threshold_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
+            L.moe_forward_threshold.argtypes = [CP] + [P] * 14
             HP = ctypes.POINTER(moe_hier_config)
             L.moe_hier_workspace_size.argtypes = [HP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_hier.argtypes = [HP] + [P] * 19
@@ -278,6 +281,23 @@ def moe_noalloc_last_status(stream=None):
     det = ctypes.c_int64()
     st = lib().moe_noalloc_last_status(_stream(stream), ctypes.byref(det))
     return st, det.value
+
+
+def moe_threshold_workspace_size(cfg) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_threshold_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_threshold_workspace_size")
+    return n.value
+
+
+def moe_forward_threshold(cfg, x, Wg, logit_bias, thresholds, W1, b1, W2, b2, y, ws,
+                          expert_idx=None, gate=None, mask_out=None, stream=None):
+    """The threshold-mask layer (inference form of strictly balanced gating)."""
+    _check(lib().moe_forward_threshold(ctypes.byref(cfg), _p(x), _p(Wg), _p(logit_bias),
+                                       _p(thresholds), _p(W1), _p(b1), _p(W2), _p(b2), _p(y),
+                                       _p(expert_idx), _p(gate), _p(mask_out), _p(ws),
+                                       _stream(stream)),
+           "moe_forward_threshold")
 
 
 def moe_eval_normal_cdf(u, out, stream=None):

@@ -346,6 +346,77 @@ __global__ void k_bal_loss(int E, const double *__restrict__ part, float *__rest
   }
 }
 
+// Threshold mask, the inference-time form of strictly balanced gating
+// ("Outrageously Large", Strictly Balanced Gating: M_threshold(x, T)_i = 1
+// iff x_i > T_i, applied to G_sigma(x) = Softmax(H), because at inference
+// examples arrive one at a time and no batch can be ranked). A warp per token:
+// P_i = exp(H_i - max) / sum_j exp(H_j - max) (the evaluation of
+// k_bal_softmax), the picks are the experts with P_i > T_i (strict), listed
+// in expert order, S = their sum of P and each pick's gate P_i / S. Choice j
+// of token t: idx[t*kmax + j] = its j-th pick, or E (no choice) past the
+// last; gate = P / S, or 0. The mask row holds bit i % 32 of word i / 32 for
+// every pick. A token with more than kmax picks records MOE_ERR_BOUNDS
+// (detail = t) and keeps its first kmax.
+__global__ void __launch_bounds__(kRowWarps * 32)
+k_thr_gate(int T, int E, int kmax, const float *__restrict__ H, const float *__restrict__ thr,
+           int32_t *__restrict__ idx, float *__restrict__ gate, uint32_t *__restrict__ mask,
+           DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float *h = H + (size_t)t * E;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) mx = fmaxf(mx, h[e]);
+  mx = warp_max(mx);
+  float se = 0.f;
+  for (int e = lane; e < E; e += 32) se += expf(h[e] - mx);
+  se = warp_sum(se);
+  const float inv = 1.f / se;
+  const unsigned below = (1u << lane) - 1u;
+  const int W = (E + 31) / 32;
+  // Pass 1: the picks' count and S, 32 experts at a time in expert order.
+  int cnt = 0;
+  float S = 0.f;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    float pv = 0.f;
+    bool take = false;
+    if (e < E) {
+      pv = expf(h[e] - mx) * inv;
+      take = pv > thr[e];
+    }
+    const unsigned b = __ballot_sync(0xffffffffu, take);
+    if (mask && lane == 0) mask[(size_t)t * W + (e0 >> 5)] = b;
+    S += warp_sum(take ? pv : 0.f);
+    cnt += __popc(b);
+  }
+  // Pass 2: each pick's choice slot and gate.
+  int base = 0;
+  for (int e0 = 0; e0 < E && base < kmax; e0 += 32) {
+    const int e = e0 + lane;
+    float pv = 0.f;
+    bool take = false;
+    if (e < E) {
+      pv = expf(h[e] - mx) * inv;
+      take = pv > thr[e];
+    }
+    const unsigned b = __ballot_sync(0xffffffffu, take);
+    const int j = base + __popc(b & below);
+    if (take && j < kmax) {
+      idx[(size_t)t * kmax + j] = e;
+      gate[(size_t)t * kmax + j] = pv / S;
+    }
+    base += __popc(b);
+  }
+  for (int j = cnt + lane; j < kmax; j += 32) {
+    idx[(size_t)t * kmax + j] = E;
+    gate[(size_t)t * kmax + j] = 0.f;
+  }
+  if (cnt > kmax && lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)t);
+}
+
 }  // namespace
 
 int balanced_m(const moe_config &c) {
@@ -380,6 +451,13 @@ cudaError_t launch_bal_combine(const moe_config &c, int m, const void *x, const 
   else
     launch_pdl(k_bal_combine<float>, grid, kRowWarps * 32, 0, s, c.T, c.d, c.E, c.k, m,
         (const float *)x, zbuf, mask, row_token, trows, npick, (float *)y, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_thr_gate(const moe_config &c, const float *H, const float *thr, int32_t *idx,
+                            float *gate, uint32_t *mask, DeviceStatus *st, cudaStream_t s) {
+  launch_pdl(k_thr_gate, (c.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s, c.T, c.E, c.k,
+      H, thr, idx, gate, mask, st);
   return cudaGetLastError();
 }
 

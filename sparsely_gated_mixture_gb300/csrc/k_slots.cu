@@ -23,8 +23,8 @@ constexpr int kScanBatch = 16;
 constexpr int kRankWarps = 8;
 
 __global__ void __launch_bounds__(kHistThreads)
-k_slot_hist(int A, int E, const int32_t *__restrict__ idx, int32_t *__restrict__ hist,
-            DeviceStatus *st) {
+k_slot_hist(int A, int E, int allow_none, const int32_t *__restrict__ idx,
+            int32_t *__restrict__ hist, DeviceStatus *st) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int32_t sh_hist[];
@@ -36,6 +36,7 @@ k_slot_hist(int A, int E, const int32_t *__restrict__ idx, int32_t *__restrict__
     int a = a0 + i;
     if (a >= A) break;
     int e = idx[a];
+    if (e == E && allow_none) continue;  // an empty choice
     if (e < 0 || e >= E) {
       record_error(st, MOE_ERR_BOUNDS, (long long)a);
       continue;
@@ -176,7 +177,7 @@ k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *_
     int e = -1;
     if (a < A) {
       e = idx[a];
-      if (e < 0 || e >= E) e = -1;  // counted as a bounds error by k_slot_hist
+      if (e < 0 || e >= E) e = -1;  // an empty choice, or a bounds error k_slot_hist counts
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int before = e >= 0 ? cnt[e] : 0;
@@ -224,10 +225,11 @@ k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *_
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
                          int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
                          int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
-                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s) {
+                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s,
+                         bool allow_none) {
   const int A = cfg.T * cfg.k;
-  launch_pdl(k_slot_hist, n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s, A, cfg.E, idx, hist,
-      st);
+  launch_pdl(k_slot_hist, n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s, A, cfg.E,
+      allow_none ? 1 : 0, idx, hist, st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   launch_pdl(k_slot_scan, (cfg.E + 31) / 32, kScanThreads, 0, s, cfg.E, C, n_chunks, kTcBM,

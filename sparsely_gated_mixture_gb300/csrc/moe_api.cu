@@ -170,7 +170,7 @@ static int ffn_impl(const moe_config &c, const void *xbuf, const int32_t *offset
 static int expert_path(const moe_config &c, const WsLayout &L, void *ws, const void *x,
                        const int32_t *idx, const float *g, int32_t *ps, uint8_t *kp,
                        const void *W1, const void *b1, const void *W2, const void *b2, void *y,
-                       DeviceStatus *st, cudaStream_t s) {
+                       DeviceStatus *st, cudaStream_t s, bool allow_none = false) {
   int32_t *offset = ws_at<int32_t>(ws, L.offset);
   int32_t *row_token = ws_at<int32_t>(ws, L.row_token);
   float *row_gate = ws_at<float>(ws, L.row_gate);
@@ -179,7 +179,7 @@ static int expert_path(const moe_config &c, const WsLayout &L, void *ws, const v
   MOE_CUDA(launch_slots(c, host_capacity(c), idx, g, ws_at<int32_t>(ws, L.hist),
                         ws_at<int32_t>(ws, L.chunk_base), ws_at<int32_t>(ws, L.count), offset,
                         ws_at<int32_t>(ws, L.mtiles), ps, kp, row_token, row_gate, L.n_chunks, st,
-                        s));
+                        s, allow_none));
   MOE_CUDA(launch_gather(c, x, offset, row_token, xbuf, st, s));
   const bool z_bf16 = forward_z_bf16(c);
   const int r = ffn_impl(c, xbuf, offset, ws_at<int32_t>(ws, L.mtiles), row_gate, W1, b1, W2,
@@ -295,6 +295,18 @@ static BalLayout bal_layout(const moe_config &cfg) {
   L.loss = take(E * 8);
   L.total = off;
   return L;
+}
+
+// ----------------------------------------------------------------------------- threshold mask
+// The inference-time gate of strictly balanced gating runs the flat expert
+// path with cfg.k choice slots per token (the caller's bound on a token's
+// picks) and no capacity: C = T, so every pick keeps its row.
+static moe_config thr_layer(const moe_config &c) {
+  moe_config r = c;
+  r.capacity_factor = (float)c.E;  // floor(k T E / E) >= T: the capacity is T
+  r.min_capacity = 1;
+  r.gate_mode = MOE_GATE_TOPK_SOFTMAX;
+  return r;
 }
 
 // ----------------------------------------------------------------------------- backward
@@ -778,6 +790,41 @@ int moe_forward_balanced(const moe_config *cfg, const void *x, const float *Wg,
   MOE_CUDA(launch_bal_combine(cr, L.m, x, zbuf, mask, row_token, trows, npick, y, st, s));
   if (loss_out) MOE_CUDA(launch_bal_loss(c.E, loss, loss_out, s));
   return MOE_OK;
+}
+
+int moe_threshold_workspace_size(const moe_config *cfg, size_t *bytes) {
+  const int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = ws_layout(thr_layer(*cfg)).total;
+  return MOE_OK;
+}
+
+int moe_forward_threshold(const moe_config *cfg, const void *x, const float *Wg,
+                          const float *logit_bias, const float *thresholds, const void *W1,
+                          const void *b1, const void *W2, const void *b2, void *y,
+                          int32_t *expert_idx, float *gate, uint32_t *mask_out, void *ws,
+                          moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(x); MOE_REQ(Wg); MOE_OPT(logit_bias); MOE_REQ(thresholds); MOE_REQ(W1); MOE_OPT(b1);
+  MOE_REQ(W2); MOE_OPT(b2); MOE_REQ(y); MOE_OPT(expert_idx); MOE_OPT(gate); MOE_OPT(mask_out);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const moe_config c = thr_layer(*cfg);
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  float *H = ws_at<float>(ws, L.H);
+  // 1. Clean router logits (this clears the status word first).
+  MOE_CUDA(launch_router(c, x, Wg, nullptr, nullptr, logit_bias, ws_at<float>(ws, L.c),
+                         ws_at<float>(ws, L.sigma), H, ws_at<char>(ws, L.bsplit), st, s));
+  // 2. P = Softmax(H), the picks P_i > T_i and their renormalised gates.
+  int32_t *idx = expert_idx ? expert_idx : ws_at<int32_t>(ws, L.idx);
+  float *g = gate ? gate : ws_at<float>(ws, L.gate);
+  MOE_CUDA(launch_thr_gate(c, H, thresholds, idx, g, mask_out, st, s));
+  // 3. Slots (token order, no capacity), gather, expert GEMMs, combine.
+  return expert_path(c, L, ws, x, idx, g, ws_at<int32_t>(ws, L.pos), ws_at<uint8_t>(ws, L.keep),
+                     W1, b1, W2, b2, y, st, s, true);
 }
 
 int moe_backward_workspace_size(const moe_config *cfg, size_t *bytes) {

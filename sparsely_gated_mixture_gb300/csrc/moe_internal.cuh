@@ -166,6 +166,12 @@ cudaError_t launch_bal_combine(const moe_config &c, int m, const void *x, const 
                                const int32_t *trows, const int32_t *npick, void *y,
                                DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_bal_loss(int E, const double *loss_part, float *out, cudaStream_t s);
+// The threshold mask (k_balanced.cu): per token the experts whose softmax gate
+// exceeds their threshold, in expert order, with gates renormalised over
+// them; idx / gate [T, c.k] with E / 0 past a token's last pick; mask
+// [T][ceil(E/32)] or null. More than c.k picks: MOE_ERR_BOUNDS.
+cudaError_t launch_thr_gate(const moe_config &c, const float *H, const float *thr, int32_t *idx,
+                            float *gate, uint32_t *mask, DeviceStatus *st, cudaStream_t s);
 
 // k_router_tc.cu, grouped form: the hierarchical layer's secondary logits for
 // the (token, primary pick) pairs only. xg holds group i's tokens in rows
@@ -194,10 +200,13 @@ cudaError_t launch_router_tc(const moe_config &cfg, const void *x, const float *
                              const RouterSelect *sel, bool *selected);
 
 // k_slots.cu: capacity, token-order slots, dispatch maps.
+// With allow_none, an expert index equal to E marks an empty choice (pos -1,
+// keep 0, no row) instead of an index error.
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
                          int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
                          int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
-                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s);
+                         float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s,
+                         bool allow_none = false);
 
 // k_rows.cu: gather of accepted token rows and the combine with the residual.
 cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,

@@ -153,6 +153,30 @@ BAL_WORKLOADS = {
     ]
 }
 
+# The threshold mask (the inference-time form of strictly balanced gating):
+# the balanced layer's shapes; k is the bound on a token's picks (the row
+# buffers' size), and every expert's threshold is THR_SCALE / E (see
+# ``thresholds``).
+THR_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("threshold_e64", T=16384, d=1024, E=64, d_ff=4096, k=16, cf=1.0, mode=TOPK,
+                 dtype="bf16", noisy=False),
+    ]
+}
+THR_SCALE = 4.0
+
+
+def thresholds(w: Workload) -> np.ndarray:
+    """Per-expert thresholds T_i of a threshold workload: the same value
+    THR_SCALE / E for every expert, a synthetic stand-in for learned
+    thresholds. With this recipe's logits (x ~ N(0, 1), W_g ~ N(0, 1/d)) about
+    two experts pass per token, the top-2 regime; since a token's softmax
+    gates sum to 1, fewer than E / THR_SCALE (16 here) can pass, so the bound
+    k = 16 always holds."""
+    return np.full(w.E, THR_SCALE / w.E, np.float32)
+
+
 _CHUNK = 1 << 24
 
 

@@ -179,3 +179,28 @@ def test_backward_checks_on_host(lib):
     bad = list(gargs)
     bad[6] = None  # dgate
     assert lib.moe_gate_backward(ctypes.byref(cfg), *bad) == 1
+
+
+def test_threshold_checks_on_host(lib):
+    cfg = B.config(64, 32, 16, 64, 4, 1.0)
+    assert B.moe_threshold_workspace_size(cfg) > 0
+    # the bound on picks sizes the row buffers
+    assert (B.moe_threshold_workspace_size(B.config(64, 32, 16, 64, 8, 1.0))
+            > B.moe_threshold_workspace_size(cfg))
+    n = ctypes.c_size_t()
+    assert lib.moe_threshold_workspace_size(ctypes.byref(B.config(64, 32, 16, 64, 17, 1.0)),
+                                            ctypes.byref(n)) == 1  # k > E
+    assert lib.moe_threshold_workspace_size(ctypes.byref(B.config(64, 32, 32, 64, 17, 1.0)),
+                                            ctypes.byref(n)) == 2  # k > 16
+    f = 1 << 20  # never dereferenced: the checks fail first
+    #       x  Wg bias  thr W1 b1    W2 b2    y  idx   gate  mask  ws stream
+    args = [f, f, None, f, f, None, f, None, f, None, None, None, f, None]
+    bad = list(args)
+    bad[3] = None  # thresholds are required
+    assert lib.moe_forward_threshold(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[11] = f + 4  # misaligned mask
+    assert lib.moe_forward_threshold(ctypes.byref(cfg), *bad) == 1
+    bad = list(args)
+    bad[12] = f + 128  # workspace not 256-byte aligned
+    assert lib.moe_forward_threshold(ctypes.byref(cfg), *bad) == 1
