@@ -17,7 +17,7 @@
  * Memory.  Every array argument is a DEVICE pointer owned by the caller, on the
  *   current CUDA device, row-major and contiguous, 16-byte aligned. The library
  *   never allocates, frees or copies host<->device (except moe_last_device_status,
- *   which reads the 24-byte status word back). Scratch space is the caller's
+ *   which reads the 32-byte status word back). Scratch space is the caller's
  *   workspace `ws` of moe_workspace_size() bytes (256-byte aligned).
  * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *   default stream) and returns without synchronising. moe_forward() runs the
@@ -228,7 +228,7 @@ int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx, const
  * either): synchronises `stream` (the stream that call used), returns
  * MOE_OK or the first error recorded since the call started (MOE_ERR_BOUNDS
  * for an expert index outside [0, E)), writes its detail word to *detail if
- * non-NULL, and clears it. It copies 24 bytes device-to-host into a local
+ * non-NULL, and clears it. It copies 32 bytes device-to-host into a local
  * variable and allocates nothing.
  */
 int moe_noalloc_last_status(moe_stream_t stream, int64_t *detail);

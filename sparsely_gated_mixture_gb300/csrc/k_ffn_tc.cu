@@ -43,6 +43,8 @@ constexpr int TMEM_COLS = 2 * BN;     // two accumulators
 
 struct Params {
   int K, N, E, n_blocks;
+  uint32_t *sched;        // [2] the CTA-pair kernel's tile counter and done count (zero at launch)
+  int dynamic;            // CTA-pair kernel: tiles from the counter (else round robin)
   const int32_t *offset;  // [E+1] packed-row offsets
   const float *row_gate;  // layer 2 only
   const __nv_bfloat16 *bias;  // [E, N] or null
@@ -329,6 +331,13 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
 // "empty" and "accumulator full" barriers; both CTAs' epilogues arrive on the
 // even CTA's "accumulator empty" barriers.
 constexpr int P_STAGES = 6;
+// Tile indices handed from the even CTA's producer to the kernel's other
+// roles, in flight at once (the producer runs at most a tile ahead of the MMA,
+// which runs at most two ahead of the epilogue).
+constexpr int kRing = 8;
+// Arrivals that free a ring slot: the even CTA's MMA issuer and four epilogue
+// warps, the odd CTA's producer and four epilogue warps.
+constexpr int kRingConsumers = 10;
 constexpr int P_BN_HALF = BN / 2;               // B columns held per CTA
 constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int P_B_BYTES = BK * P_BN_HALF * 2;   // 16 KB
@@ -336,12 +345,21 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 // kind::f16, fp32 accumulate, bf16 A/B, A K-major, B MN-major, M = 256, N = 256.
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+// The same with M = 128 (64 rows per CTA), for an expert's last row tile
+// when it holds at most 128 rows: half the MMA work of a 256-row tile. Its
+// accumulator in each CTA: TMEM lanes 0-63 hold the CTA's 64 rows for
+// columns 0-127 of the tile, lanes 64-127 the same rows for columns 128-255,
+// both at accumulator columns 0-127.
+constexpr uint32_t kIdescPairHalf = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) |
+                                    (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
+                                    ((uint32_t)(128 >> 4) << 24);
 
-__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t acc) {
+__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(kIdescPair), "r"(acc)
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
 template <int LAYER>
@@ -357,9 +375,11 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES);
   uint64_t *full = bars, *empty = bars + P_STAGES;
   uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *tfull = drain + 1, *tempty = tfull + kRing;  // the tile ring's barriers
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + kRing);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *tile_start = reinterpret_cast<int *>(tmem_slot + 2);
+  volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [kRing] tile indices
+  int *tile_start = const_cast<int *>(ring + kRing);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -374,6 +394,10 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 8);  // four epilogue warps in each CTA
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&tfull[r], 1);                // the even CTA's producer publishes
+      mbar_init(&tempty[r], kRingConsumers);  // used in the even CTA only
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -413,7 +437,9 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   const int total_tiles = tile_start[p.E];
   const int num_kb = p.K / BK;
 
-  auto locate = [&](int tile, int &e, int &pm, int &nb, int &row0, int &rows) {
+  // half: the expert's last row tile holds at most 128 rows and runs as an
+  // M = 128 tile (kIdescPairHalf), each CTA taking 64 of them.
+  auto locate = [&](int tile, int &e, int &pm, int &nb, int &row0, int &rows, bool &half) {
     int lo = 0, hi = p.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -427,6 +453,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int local = tile - tile_start[e];
     nb = local / mt;
     pm = local % mt;
+    half = pm == mt - 1 && rows - pm * 2 * BM <= BM;
   };
 
   if (warp == 0) {
@@ -434,15 +461,58 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       // --------------------------------------------------------- producer (both CTAs)
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      // Tiles: each pair's first is its index; the even CTA's producer takes
+      // every later one from the counter when it needs it, so pairs that run
+      // ahead take more tiles, and publishes it (or total_tiles: the end)
+      // through the ring to the other roles of both CTAs.
+      // The take for the next tile is issued a few k-blocks before this
+      // tile's last load, so its round trip overlaps the loads in flight.
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs) {
+      long long taken = -1;  // the next tile's take, once issued
+      int tile_rr = pair;    // round-robin order (p.dynamic == 0)
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kRing;
+        const uint32_t rph = (uint32_t)(j / kRing) & 1u;
+        int tile;
+        if (leader) {
+          if (j == 0) {
+            tile = pair;
+          } else if (p.dynamic) {
+            if (taken < 0) taken = atomicAdd(p.sched, 1u);
+            tile = (int)min(taken + n_pairs, (long long)total_tiles);
+            taken = -1;
+          } else {
+            tile_rr += n_pairs;
+            tile = min(tile_rr, total_tiles);
+          }
+          if (!mbar_wait_cl(&tempty[slot], rph ^ 1u, abort_flag, p.st, 15, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          ring[slot] = tile;
+          st_cluster_u32(mapa(smem_u32((const void *)&ring[slot]), 1), (uint32_t)tile);
+          mbar_arrive_cluster(smem_u32(&tfull[slot]));
+          mbar_arrive_cluster(mapa(smem_u32(&tfull[slot]), 1));
+        } else {
+          if (!mbar_wait_cl(&tfull[slot], rph, abort_flag, p.st, 16, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tile = ring[slot];
+          mbar_arrive_cluster(mapa(smem_u32(&tempty[slot]), 0));
+        }
+        if (tile >= total_tiles) break;
         int e, pm, nb, row0, rows;
-        locate(tile, e, pm, nb, row0, rows);
-        const int arow = row0 + pm * 2 * BM + (int)rank * BM;
+        bool half;
+        locate(tile, e, pm, nb, row0, rows, half);
+        // A half tile's CTA uses the first 64 of the 128 rows its box brings.
+        const int arow = row0 + pm * 2 * BM + (int)rank * (half ? BM / 2 : BM);
         const int ncol = nb * BN + (int)rank * P_BN_HALF;
         const int brow = e * p.K;
+        const int take_at = num_kb > 4 ? num_kb - 4 : 0;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          if (leader && p.dynamic && kb == take_at) taken = atomicAdd(p.sched, 1u);
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 11, p.wait_ns)) {
@@ -453,15 +523,24 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           if (leader) mbar_expect_tx(&full[s], 2 * P_STAGE_BYTES);
           tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kb * BK, arow);
 #pragma unroll
-          for (int j = 0; j < P_BN_HALF / 64; ++j)
-            tma_load_2d_pair(sB + s * P_B_BYTES + j * (BK * 128), &tmB, full_leader,
-                             ncol + j * 64, brow + kb * BK);
+          for (int q = 0; q < P_BN_HALF / 64; ++q)
+            tma_load_2d_pair(sB + s * P_B_BYTES + q * (BK * 128), &tmB, full_leader,
+                             ncol + q * 64, brow + kb * BK);
         }
       }
       // This CTA's copies have landed once the MMAs that read them are done.
       const uint32_t issued = it;
       for (uint32_t q = issued > (uint32_t)P_STAGES ? issued - P_STAGES : 0; q < issued; ++q)
         mbar_drain(&empty[q % P_STAGES], (q / P_STAGES) & 1u);
+      if (leader && p.dynamic) {
+        // The last pair to finish resets the counter for the next launch
+        // (every pair's last take precedes its count).
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == (uint32_t)n_pairs - 1) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
     pdl_trigger();  // all loads issued: the next kernel may be scheduled
@@ -469,11 +548,21 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     if (lane == 0 && leader) {
       // --------------------------------------------------------- MMA issuer (even CTA)
       uint32_t it = 0;
-      int local = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs, ++local) {
+      for (int local = 0; ok; ++local) {
+        const int slot = local % kRing;
+        if (!mbar_wait_cl(&tfull[slot], (uint32_t)(local / kRing) & 1u, abort_flag, p.st, 17,
+                          p.wait_ns))
+          break;
+        const int tile = ring[slot];
+        mbar_arrive_cluster(smem_u32(&tempty[slot]));
+        if (tile >= total_tiles) break;
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
+        int e, pm, nb, row0, rows;
+        bool half;
+        locate(tile, e, pm, nb, row0, rows, half);
+        const uint32_t idesc = half ? kIdescPairHalf : kIdescPair;
         if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 12, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BN);
@@ -491,7 +580,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
             const uint64_t bd = sdesc(b0 + kk * 2048, BK * 128, 1024);
-            umma_pair(tmem_d, ad, bd, (kb | kk) ? 1u : 0u);
+            umma_pair(tmem_d, ad, bd, idesc, (kb | kk) ? 1u : 0u);
           }
           umma_commit_pair(&empty[s]);
         }
@@ -508,24 +597,44 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int r_in_tile = quad * 32 + lane;
     const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
-    int local = 0;
-    for (int tile = pair; tile < total_tiles; tile += n_pairs, ++local) {
+    for (int local = 0;; ++local) {
+      const int slot = local % kRing;
+      int tile = total_tiles;
+      bool got = false;
+      if (lane == 0) {
+        got = mbar_wait_cl(&tfull[slot], (uint32_t)(local / kRing) & 1u, abort_flag, p.st, 18,
+                           p.wait_ns);
+        if (got) {
+          tile = ring[slot];
+          mbar_arrive_cluster(mapa(smem_u32(&tempty[slot]), 0));
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!got || tile >= total_tiles) break;
       int e, pm, nb, row0, rows;
-      locate(tile, e, pm, nb, row0, rows);
+      bool half;
+      locate(tile, e, pm, nb, row0, rows, half);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
       const bool ready = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], use & 1u, abort_flag,
                                                            p.st, 14, p.wait_ns));
       if (!ready) break;
       tc_fence_after();
-      const int m = pm * 2 * BM + (int)rank * BM + r_in_tile;
+      // Full tile: lane quadrant q holds rows 32q.. of this CTA's 128, all
+      // 256 columns. Half tile: quadrants 0-1 hold the CTA's 64 rows for
+      // columns 0-127, quadrants 2-3 the same rows for columns 128-255.
+      const int m = half ? pm * 2 * BM + (int)rank * (BM / 2) + (quad & 1) * 32 + lane
+                         : pm * 2 * BM + (int)rank * BM + r_in_tile;
+      const int ncol0 = nb * BN + (half ? (quad >> 1) * (BN / 2) : 0);
+      const int nchunks = half ? BN / 64 : BN / 32;
       const bool valid = m < rows;
       const size_t r = (size_t)row0 + m;
       const float g = (LAYER == 2 && valid) ? p.row_gate[r] : 1.f;
       bool bad = false;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n = nb * BN + c * 32;
+      for (int c = 0; c < nchunks; ++c) {
+        const int n = ncol0 + c * 32;
         uint32_t v[32];
         const uint32_t taddr =
             tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN + c * 32);
@@ -659,8 +768,8 @@ cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const Param
 }
 
 constexpr size_t smem_bytes_pair(int E) {
-  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5) * 8 + 8 +
-         (size_t)(E + 1) * 4;
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 +
+         (size_t)kRing * 4 + (size_t)(E + 1) * 4;
 }
 
 cudaLaunchAttribute pair_cluster_attr() {
@@ -725,14 +834,25 @@ cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const 
   return cudaLaunchKernelEx(&cfg, k_ffn_tc_pair<LAYER>, a, b, p);
 }
 
+// MOE_FFN_SCHED=static makes the CTA-pair kernel take its tiles round robin
+// instead of from the counter (read at each call; for comparisons).
+int ffn_dynamic() {
+  const char *v = getenv("MOE_FFN_SCHED");
+  return v && v[0] == 's' ? 0 : 1;
+}
+
+// MOE_FFN_TC_VARIANT=single or =pair forces one kernel (read at each call);
+// otherwise the rule in launch_ffn_tc picks per layer.
+int ffn_variant() {
+  const char *v = getenv("MOE_FFN_TC_VARIANT");
+  if (!v || !*v) return 0;
+  return v[0] == 's' ? 1 : (v[0] == 'p' ? 2 : 0);
+}
+
 // Clusters available to the CTA-pair kernel, or 0 when the one-CTA kernel must
-// run (MOE_FFN_TC_VARIANT=single asks for it; so does a device without room).
+// run (forced, or a device without room).
 int pair_clusters_for(int E) {
-  static const bool single = [] {
-    const char *v = getenv("MOE_FFN_TC_VARIANT");
-    return v && v[0] == 's';
-  }();
-  if (single || smem_bytes_pair(E) > 227 * 1024) return 0;
+  if (ffn_variant() == 1 || smem_bytes_pair(E) > 227 * 1024) return 0;
   return pair_clusters(smem_bytes_pair(E));
 }
 
@@ -753,16 +873,20 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
   if (!make_map(&ta1, xbuf, A, c.d, BM) || !make_map(&tb1, W1, (uint64_t)c.E * c.d, c.d_ff, BK) ||
       !make_map(&ta2, hbuf, A, c.d_ff, BM) || !make_map(&tb2, W2, (uint64_t)c.E * c.d_ff, c.d, BK))
     return cudaErrorInvalidValue;
-  Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, offset, row_gate,
+  uint32_t *sched = &st->gemm_next;  // gemm_next, gemm_done: adjacent words
+  const int dyn = ffn_dynamic();
+  Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, sched, dyn, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b1), hbuf, st, wait_limit_ns()};
-  Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, offset, row_gate,
+  Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, sched, dyn, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b2), zbuf, st, wait_limit_ns(), z_bf16 ? 1 : 0};
   // Per layer: the CTA pair pays off for long K and enough 256-row tiles to
   // fill several waves; otherwise the one-CTA kernel's finer tiles win.
   const long rows = (long)c.T * c.k < (long)c.E * C ? (long)c.T * c.k : (long)c.E * C;
   const int clusters = pair_clusters_for(c.E);
+  const bool force_pair = ffn_variant() == 2;
   auto pair_for = [&](int K, int N) {
-    return clusters > 0 && K >= 2048 && (rows / 256) * ((N + BN - 1) / BN) >= 4L * clusters;
+    return clusters > 0 &&
+           (force_pair || (K >= 2048 && (rows / 256) * ((N + BN - 1) / BN) >= 4L * clusters));
   };
   cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, p1, clusters, s)
                                           : launch_layer<1>(ta1, tb1, p1, s);

@@ -128,6 +128,8 @@ __global__ void k_router_split(int d, int E, int noisy, int NC, int NCP, int BNR
     st->detail = 0;
     st->slot_ticket = 0;
     st->reserved = 0;
+    st->gemm_next = 0;
+    st->gemm_done = 0;
   }
   __shared__ float tile[32][33];
   const int k0 = blockIdx.x * 32, n0 = blockIdx.y * 32;

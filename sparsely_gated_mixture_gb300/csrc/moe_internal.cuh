@@ -66,6 +66,9 @@ struct DeviceStatus {
   long long detail;
   uint32_t slot_ticket;  // blocks of the slot scan that are done (zeroed by the histogram pass)
   uint32_t reserved;
+  // The CTA-pair expert GEMM's tile scheduler: tiles handed out past each
+  // pair's first, and pairs done (the last pair resets both to zero).
+  uint32_t gemm_next, gemm_done;
 };
 
 __device__ __forceinline__ void record_error(DeviceStatus *st, int code, long long detail) {

@@ -73,6 +73,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// try_wait with acquire at cluster scope: for barriers that another CTA of the
+// cluster arrives on (release.cluster) after writing this CTA's shared memory.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (see mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity,
+                                             volatile int *abort_flag, DeviceStatus *st,
+                                             int where, unsigned long long limit_ns) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (;;) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 >= limit_ns) {
+      *abort_flag = 1;
+      record_error(st, MOE_ERR_TIMEOUT, (long long)where);
+      return false;
+    }
+    if (mbar_try_wait_cl(bar, parity)) return true;
+  }
+}
+
 // Wait used while draining after an abort: bounded, no abort check.
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer();
@@ -158,6 +187,11 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
+}
+// 32-bit store to a shared-memory word of any CTA of the cluster (an address
+// from mapa, or this CTA's own).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
                                                  uint32_t bar_cluster_addr, int x, int y) {

@@ -1,8 +1,9 @@
 """The expert FFN stage alone (moe_expert_ffn through the C ABI) against numpy
 on hand-built packed rows: ragged experts (one empty, one spanning several
 128-row tiles), an N tail that is not a multiple of the 256-column tile, and
-non-zero biases. A kernel-level check that localises GEMM faults; the layer's
-parity against the oracle is tested in test_gpu_parity.py."""
+non-zero biases; the library's kernel choice, and each of the one-CTA and
+CTA-pair kernels forced. A kernel-level check that localises GEMM faults; the
+layer's parity against the oracle is tested in test_gpu_parity.py."""
 import numpy as np
 import pytest
 import torch
@@ -17,9 +18,18 @@ def _bf16(a):
     return wl.bf16_bits_to_f32(wl.f32_to_bf16_bits(a))
 
 
+# Row counts around the 256-row tiles of the CTA-pair kernel: an expert's
+# last tile with at most 128 rows runs at M = 128 (64 rows per CTA), with
+# 129 or more at M = 256; both, and the 128 / 129 and 256 / 257 boundaries.
+PAIR_TAILS = [[40, 0, 296, 128, 129, 384, 1], [256, 257, 511, 64]]
+
+
+@pytest.mark.parametrize("variant", ["", "single", "pair"])
 @pytest.mark.parametrize("rows,d,d_ff", [([130, 0, 257], 128, 320), ([1, 128, 64], 64, 64),
-                                         ([300, 5], 256, 512)])
-def test_expert_ffn_against_numpy(rows, d, d_ff):
+                                         ([300, 5], 256, 512), (PAIR_TAILS[0], 128, 320),
+                                         (PAIR_TAILS[1], 192, 256)])
+def test_expert_ffn_against_numpy(rows, d, d_ff, variant, monkeypatch):
+    monkeypatch.setenv("MOE_FFN_TC_VARIANT", variant)
     rng = np.random.default_rng(3)
     E = len(rows)
     A = int(sum(rows)) + 7  # spare rows past the last expert
