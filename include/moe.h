@@ -234,6 +234,71 @@ int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *expert_idx, const
 int moe_noalloc_last_status(moe_stream_t stream, int64_t *detail);
 
 /*
+ * Expert parallelism ("Outrageously Large Neural Networks", Distributed
+ * Training: Solving the Shrinking Batch Problem: the experts are spread over
+ * the devices, each device gates its own share of the batch, and every token
+ * is sent to the device holding its expert and its output sent back, so each
+ * expert sees the tokens of all devices). The layer's batch is the
+ * concatenation, in rank order, of the W ranks' batches; capacity and the
+ * token-order slots are those of moe_forward over that whole batch. A rank
+ * calls, on its own T tokens (cfg->T), with E the number of all experts:
+ *   1. moe_gate (or the gate of moe_forward's stages) on its tokens;
+ *   2. moe_expert_counts: its choices per expert before capacity, and
+ *      gathers the ranks' counts into counts_all [W, E] (a collective);
+ *   3. moe_dispatch_ranked with the whole batch's capacity C: its assignment
+ *      to expert e gets the slot after every earlier rank's, so it is kept
+ *      iff base_e + pos < C with base_e the earlier ranks' count; the kept
+ *      rows are packed per expert as moe_dispatch packs them, so the rows of
+ *      the experts one rank holds are one contiguous range (an all-to-all
+ *      sends them there and the outputs back);
+ *   4. moe_expert_ffn on the rows it received, moe_combine on its own tokens
+ *      with the outputs it got back;
+ *   5. moe_aux_totals, a sum over the ranks (a collective) and
+ *      moe_aux_from_totals for the balancing losses of the whole batch.
+ * The module sparsely_gated_mixture_gb300.expert_parallel drives these.
+ */
+
+/*
+ * Choices per expert before capacity (counts [E] int32) of this rank's
+ * selection expert_idx [T,k] (an index outside [0, E) is a device-side
+ * MOE_ERR_BOUNDS and not counted).
+ */
+int moe_expert_counts(const moe_config *cfg, const int32_t *expert_idx, int32_t *expert_count,
+                      void *ws, moe_stream_t stream);
+
+/*
+ * moe_dispatch for rank `rank` of n_ranks: counts_all [n_ranks, E] int32
+ * (device) holds every rank's moe_expert_counts, capacity the whole batch's
+ * C (>= 1). pos[t,j] = this rank's exclusive count of earlier assignments to
+ * the same expert (its local position; the slot in the whole batch adds
+ * base_e); keep = pos < max(0, capacity - base_e). expert_count, expert_offset,
+ * xbuf, row_token and row_gate as in moe_dispatch (kept rows only).
+ */
+int moe_dispatch_ranked(const moe_config *cfg, int32_t capacity, const int32_t *counts_all,
+                        int32_t n_ranks, int32_t rank, const int32_t *expert_idx,
+                        const float *gate, const void *x, int32_t *pos, uint8_t *keep,
+                        int32_t *expert_count, int32_t *expert_offset, void *xbuf,
+                        int32_t *row_token, float *row_gate, void *ws, moe_stream_t stream);
+
+/*
+ * The balancing sums of the last moe_gate (or moe_forward with aux_out3) on
+ * `ws` over this rank's tokens: totals [4, E] fp32 = importance (sum of gates,
+ * Eq. 6), load (sum of P(x, e), Eq. 10), the number of tokens whose first
+ * choice is e, and the sum of Softmax(H)_e. Sums, not averages, so that
+ * ranks' totals add up to the whole batch's.
+ */
+int moe_aux_totals(const moe_config *cfg, void *ws, float *totals, moe_stream_t stream);
+
+/*
+ * The losses of moe_aux_loss (out3 [3] fp32: CV(importance)^2, CV(load)^2,
+ * the Switch loss) from totals [4, E] fp32 summed over all ranks, for a batch
+ * of T_total tokens (f and Pbar are averaged over it). ws: this rank's
+ * workspace (its status word and scratch).
+ */
+int moe_aux_from_totals(const moe_config *cfg, int64_t T_total, const float *totals,
+                        float *out3, void *ws, moe_stream_t stream);
+
+/*
  * Hierarchical layer ("Outrageously Large Neural Networks", Hierarchical
  * Mixture-of-Experts): a groups of b experts, flat expert i*b + j. A primary
  * noisy top-k gate over the a groups picks k_primary groups; in each picked

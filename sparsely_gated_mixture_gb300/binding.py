@@ -29,7 +29,8 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_gate"
            "moe_forward_hier", "moe_balanced_workspace_size", "moe_forward_balanced",
            "moe_backward_workspace_size", "moe_backward", "moe_gate_backward",
            "moe_noalloc_last_status", "moe_eval_normal_cdf", "moe_threshold_workspace_size",
-           "moe_forward_threshold")
+           "moe_forward_threshold", "moe_expert_counts", "moe_dispatch_ranked",
+           "moe_aux_totals", "moe_aux_from_totals")
 
 
 class MoEError(RuntimeError):
@@ -100,6 +101,11 @@ def lib():
             L.moe_eval_normal_cdf.argtypes = [P, P, ctypes.c_int64, P]
             L.moe_threshold_workspace_size.argtypes = [CP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_threshold.argtypes = [CP] + [P] * 14
+            I32 = ctypes.c_int32
+            L.moe_expert_counts.argtypes = [CP, P, P, P, P]
+            L.moe_dispatch_ranked.argtypes = [CP, I32, P, I32, I32] + [P] * 12
+            L.moe_aux_totals.argtypes = [CP, P, P, P]
+            L.moe_aux_from_totals.argtypes = [CP, ctypes.c_int64, P, P, P, P]
             HP = ctypes.POINTER(moe_hier_config)
             L.moe_hier_workspace_size.argtypes = [HP, ctypes.POINTER(ctypes.c_size_t)]
             L.moe_forward_hier.argtypes = [HP] + [P] * 19
@@ -297,7 +303,32 @@ def moe_forward_threshold(cfg, x, Wg, logit_bias, thresholds, W1, b1, W2, b2, y,
                                        _p(thresholds), _p(W1), _p(b1), _p(W2), _p(b2), _p(y),
                                        _p(expert_idx), _p(gate), _p(mask_out), _p(ws),
                                        _stream(stream)),
-           "moe_forward_threshold")
+           "moe_forward_threshold", "moe_expert_counts", "moe_dispatch_ranked",
+           "moe_aux_totals", "moe_aux_from_totals")
+
+
+def moe_expert_counts(cfg, expert_idx, expert_count, ws, stream=None):
+    _check(lib().moe_expert_counts(ctypes.byref(cfg), _p(expert_idx), _p(expert_count), _p(ws),
+                                   _stream(stream)), "moe_expert_counts")
+
+
+def moe_dispatch_ranked(cfg, capacity, counts_all, n_ranks, rank, expert_idx, gate, x, pos, keep,
+                        expert_count, expert_offset, xbuf, row_token, row_gate, ws, stream=None):
+    _check(lib().moe_dispatch_ranked(ctypes.byref(cfg), int(capacity), _p(counts_all),
+                                     int(n_ranks), int(rank), _p(expert_idx), _p(gate), _p(x),
+                                     _p(pos), _p(keep), _p(expert_count), _p(expert_offset),
+                                     _p(xbuf), _p(row_token), _p(row_gate), _p(ws),
+                                     _stream(stream)), "moe_dispatch_ranked")
+
+
+def moe_aux_totals(cfg, ws, totals, stream=None):
+    _check(lib().moe_aux_totals(ctypes.byref(cfg), _p(ws), _p(totals), _stream(stream)),
+           "moe_aux_totals")
+
+
+def moe_aux_from_totals(cfg, T_total, totals, out3, ws, stream=None):
+    _check(lib().moe_aux_from_totals(ctypes.byref(cfg), int(T_total), _p(totals), _p(out3),
+                                     _p(ws), _stream(stream)), "moe_aux_from_totals")
 
 
 def moe_eval_normal_cdf(u, out, stream=None):

@@ -806,12 +806,14 @@ __device__ void block_sum_ff(ff (&v)[N], ff *sh) {
 __device__ __forceinline__ void store_expert_totals(int T, int E, int e, int q, ff tot,
                                                     float2 *__restrict__ aux,
                                                     float *__restrict__ importance,
-                                                    float *__restrict__ load) {
+                                                    float *__restrict__ load,
+                                                    float *__restrict__ raw) {
   const ff v = q >= 2 ? d_to_ff(ff_to_d(tot) / T) : tot;
   aux[(size_t)q * E + e] = make_float2(v.hi, v.lo);
   const float f32 = (float)ff_to_d(tot);
   if (q == 0 && importance) importance[e] = f32;
   if (q == 1 && load) load[e] = f32;
+  if (raw) raw[(size_t)q * E + e] = f32;
 }
 
 // Run by every block of a finalize launch once its aux entries are written:
@@ -861,7 +863,7 @@ __device__ void finish_aux(int E, const float2 *__restrict__ aux, float *__restr
 __global__ void __launch_bounds__(kFinThreads)
 k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float2 *__restrict__ aux,
                float *__restrict__ importance, float *__restrict__ load,
-               float *__restrict__ out3, DeviceStatus *st) {
+               float *__restrict__ out3, DeviceStatus *st, float *__restrict__ raw) {
   pdl_wait();
   pdl_trigger();
   __shared__ ff sh[kFinThreads];
@@ -874,7 +876,7 @@ k_aux_finalize(int T, int E, int nb, const float *__restrict__ partials, float2 
   }
   block_sum_ff<4>(tot, sh);
   if (threadIdx.x < 4) store_expert_totals(T, E, e, threadIdx.x, tot[threadIdx.x], aux,
-                                           importance, load);
+                                           importance, load, raw);
   finish_aux(E, aux, out3, st, sh);
 }
 
@@ -888,7 +890,8 @@ constexpr int kFinBatch = 16;
 __global__ void __launch_bounds__(kFinColThreads)
 k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
                     float2 *__restrict__ aux, float *__restrict__ importance,
-                    float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st) {
+                    float *__restrict__ load, float *__restrict__ out3, DeviceStatus *st,
+                    float *__restrict__ raw) {
   pdl_wait();
   pdl_trigger();
   __shared__ ff sh[kFinColThreads];
@@ -915,7 +918,7 @@ k_aux_finalize_cols(int T, int E, int nb, const float *__restrict__ partials,
     ff tot{0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < NW; ++w) tot = ff_add(tot, sh[w * 32 + lane]);
-    store_expert_totals(T, E, e, q, tot, aux, importance, load);
+    store_expert_totals(T, E, e, q, tot, aux, importance, load, raw);
   }
   __syncthreads();
   finish_aux(E, aux, out3, st, sh);
@@ -1240,14 +1243,14 @@ cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c,
 
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
                                 float *out3, float *importance, float *load, float2 *aux_vec,
-                                DeviceStatus *st, cudaStream_t s) {
+                                DeviceStatus *st, cudaStream_t s, float *raw_totals) {
   // E <= 256: a block per expert; beyond: the column form.
   if (cfg.E <= 256)
     launch_pdl_c(kPdlFinalize, k_aux_finalize, cfg.E, kFinThreads, 0, s, cfg.T, cfg.E, n_blocks,
-        partials, aux_vec, importance, load, out3, st);
+        partials, aux_vec, importance, load, out3, st, raw_totals);
   else
     launch_pdl_c(kPdlFinalize, k_aux_finalize_cols, dim3((cfg.E + 31) / 32, 4), kFinColThreads, 0,
-        s, cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st);
+        s, cfg.T, cfg.E, n_blocks, partials, aux_vec, importance, load, out3, st, raw_totals);
   return cudaGetLastError();
 }
 

@@ -82,10 +82,18 @@ __device__ int block_exclusive_scan(int v, int *sh_warp, int *total) {
 // each warp its base; the warp then writes its chunks' bases. The block that
 // finishes last (a ticket in the status word) scans min(n_e, C) and the tile
 // counts over all experts, kScanThreads at a time, into offset and mtiles.
+//
+// Ranked form (counts_all given: the per-expert choice counts [W, E] of the W
+// ranks whose batches, in rank order, make up the layer's batch): this rank's
+// assignments to expert e come after base_e = sum over earlier ranks of their
+// counts, so the capacity left to this rank is cap_e = max(0, C - base_e);
+// the last block writes it to ecap, and the kept rows per expert are
+// min(n_e, cap_e).
 __global__ void __launch_bounds__(kScanThreads)
 k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
             int32_t *__restrict__ count, int32_t *__restrict__ offset,
-            int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist, DeviceStatus *st) {
+            int32_t *__restrict__ mtiles, const int32_t *__restrict__ hist, DeviceStatus *st,
+            const int32_t *__restrict__ counts_all, int rank, int32_t *__restrict__ ecap) {
   pdl_wait();
   pdl_trigger();
   constexpr int NW = kScanThreads / 32;
@@ -129,7 +137,14 @@ k_slot_scan(int E, int C, int n_chunks, int bm, int32_t *__restrict__ hist_base,
   int carry_rows = 0, carry_tiles = 0;
   for (int e0 = 0; e0 < E; e0 += kScanThreads) {
     const int ee = e0 + threadIdx.x;
-    const int kept = ee < E ? min(cnt[ee], C) : 0;
+    int capv = C;
+    if (counts_all && ee < E) {
+      long long base = 0;
+      for (int r = 0; r < rank; ++r) base += counts_all[(size_t)r * E + ee];
+      capv = base >= C ? 0 : (int)(C - base);
+      ecap[ee] = capv;
+    }
+    const int kept = ee < E ? min(cnt[ee], capv) : 0;
     const int tiles = (kept + bm - 1) / bm;
     int tot_rows, tot_tiles;
     const int off = block_exclusive_scan(kept, sh_warp, &tot_rows);
@@ -158,7 +173,7 @@ __global__ void __launch_bounds__(kRankWarps * 32)
 k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *__restrict__ gate,
             const int32_t *__restrict__ hist_base, const int32_t *__restrict__ offset,
             int32_t *__restrict__ pos, uint8_t *__restrict__ keep, int32_t *__restrict__ row_token,
-            float *__restrict__ row_gate) {
+            float *__restrict__ row_gate, const int32_t *__restrict__ ecap) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ int32_t sh_cnt[];  // [kRankWarps][E]
@@ -210,7 +225,7 @@ k_slot_rank(int A, int E, int C, const int32_t *__restrict__ idx, const float *_
     }
     const int p = hist_base[(size_t)chunk * E + e] + cnt[e] + rk[r];
     pos[a] = p;
-    const bool kp = p < C;
+    const bool kp = p < (ecap ? ecap[e] : C);
     keep[a] = kp ? 1 : 0;
     if (kp) {
       const int row = offset[e] + p;
@@ -226,16 +241,19 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
                          int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
                          int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
                          float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s,
-                         bool allow_none) {
+                         bool allow_none, const SlotRanks *ranks) {
   const int A = cfg.T * cfg.k;
   launch_pdl(k_slot_hist, n_chunks, kHistThreads, cfg.E * sizeof(int32_t), s, A, cfg.E,
       allow_none ? 1 : 0, idx, hist, st);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  const int32_t *counts_all = ranks ? ranks->counts_all : nullptr;
+  int32_t *ecap = ranks ? ranks->ecap : nullptr;
   launch_pdl(k_slot_scan, (cfg.E + 31) / 32, kScanThreads, 0, s, cfg.E, C, n_chunks, kTcBM,
-      chunk_base, count, offset, mtiles, hist, st);
+      chunk_base, count, offset, mtiles, hist, st, counts_all, ranks ? ranks->rank : 0, ecap);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (!pos) return cudaSuccess;  // counts only
   size_t smem = (size_t)kRankWarps * cfg.E * sizeof(int32_t);
   if (smem > 48 * 1024) {
     err = cudaFuncSetAttribute(k_slot_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -243,7 +261,7 @@ cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const
     if (err != cudaSuccess) return err;
   }
   launch_pdl(k_slot_rank, n_chunks, kRankWarps * 32, smem, s, A, cfg.E, C, idx, gate, chunk_base,
-      offset, pos, keep, row_token, row_gate);
+      offset, pos, keep, row_token, row_gate, (const int32_t *)ecap);
   return cudaGetLastError();
 }
 

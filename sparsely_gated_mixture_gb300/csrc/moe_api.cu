@@ -62,6 +62,8 @@ WsLayout ws_layout(const moe_config &cfg) {
   L.count = take(E * 4);
   L.offset = take((E + 1) * 4);
   L.mtiles = take((E + 1) * 4);
+  L.ecap = take(E * 4);
+  L.out3s = take(16);
   L.partials = take((size_t)L.n_aux_blocks * 4 * E * 4);
   L.aux_vec = take(4 * E * 8);
   L.idx = take(A * 4);
@@ -629,6 +631,76 @@ int moe_forward(const moe_config *cfg, const void *x, const float *Wg, const flo
     MOE_CUDA(cudaEventRecord(side->join, side->s));
     MOE_CUDA(cudaStreamWaitEvent(s, side->join, 0));
   }
+  return MOE_OK;
+}
+
+int moe_expert_counts(const moe_config *cfg, const int32_t *expert_idx, int32_t *expert_count,
+                      void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(expert_idx); MOE_REQ(expert_count);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  const WsLayout L = ws_layout(c);
+  MOE_CUDA(launch_slots(c, host_capacity(c), expert_idx, nullptr, ws_at<int32_t>(ws, L.hist),
+                        ws_at<int32_t>(ws, L.chunk_base), expert_count,
+                        ws_at<int32_t>(ws, L.offset), ws_at<int32_t>(ws, L.mtiles), nullptr,
+                        nullptr, nullptr, nullptr, L.n_chunks, ws_at<DeviceStatus>(ws, L.status),
+                        (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_dispatch_ranked(const moe_config *cfg, int32_t capacity, const int32_t *counts_all,
+                        int32_t n_ranks, int32_t rank, const int32_t *expert_idx,
+                        const float *gate, const void *x, int32_t *pos, uint8_t *keep,
+                        int32_t *expert_count, int32_t *expert_offset, void *xbuf,
+                        int32_t *row_token, float *row_gate, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (capacity < 1 || n_ranks < 1 || rank < 0 || rank >= n_ranks) return MOE_ERR_ARG;
+  MOE_REQ(counts_all); MOE_REQ(expert_idx); MOE_REQ(gate); MOE_REQ(x); MOE_REQ(pos);
+  MOE_REQ(keep); MOE_REQ(expert_count); MOE_REQ(expert_offset); MOE_REQ(xbuf);
+  MOE_REQ(row_token); MOE_REQ(row_gate);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const moe_config &c = *cfg;
+  const WsLayout L = ws_layout(c);
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceStatus *st = ws_at<DeviceStatus>(ws, L.status);
+  const SlotRanks ranks{counts_all, rank, ws_at<int32_t>(ws, L.ecap)};
+  MOE_CUDA(launch_slots(c, capacity, expert_idx, gate, ws_at<int32_t>(ws, L.hist),
+                        ws_at<int32_t>(ws, L.chunk_base), expert_count, expert_offset,
+                        ws_at<int32_t>(ws, L.mtiles), pos, keep, row_token, row_gate, L.n_chunks,
+                        st, s, false, &ranks));
+  MOE_CUDA(launch_gather(c, x, expert_offset, row_token, xbuf, st, s));
+  return MOE_OK;
+}
+
+int moe_aux_totals(const moe_config *cfg, void *ws, float *totals, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  MOE_REQ(totals);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  MOE_CUDA(launch_aux_finalize(*cfg, ws_at<float>(ws, L.partials), L.n_aux_blocks,
+                               ws_at<float>(ws, L.out3s), nullptr, nullptr,
+                               ws_at<float2>(ws, L.aux_vec), ws_at<DeviceStatus>(ws, L.status),
+                               (cudaStream_t)stream, totals));
+  return MOE_OK;
+}
+
+int moe_aux_from_totals(const moe_config *cfg, int64_t T_total, const float *totals,
+                        float *out3, void *ws, moe_stream_t stream) {
+  int r = check_cfg(cfg);
+  if (r != MOE_OK) return r;
+  if (T_total < 1 || T_total > 0x7fffffffLL) return MOE_ERR_ARG;
+  MOE_REQ(totals); MOE_REQ(out3);
+  if (!ws || !aligned(ws, 256)) return MOE_ERR_ARG;
+  const WsLayout L = ws_layout(*cfg);
+  moe_config whole = *cfg;
+  whole.T = (int32_t)T_total;  // f and Pbar are averages over the whole batch
+  MOE_CUDA(launch_aux_finalize(whole, totals, 1, out3, nullptr, nullptr,
+                               ws_at<float2>(ws, L.aux_vec), ws_at<DeviceStatus>(ws, L.status),
+                               (cudaStream_t)stream));
   return MOE_OK;
 }
 

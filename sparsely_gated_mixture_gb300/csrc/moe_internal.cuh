@@ -84,6 +84,8 @@ struct WsLayout {
   size_t bsplit;                          // router weights as three bf16 pieces (tensor-core router)
   size_t hist, chunk_base;                // slot pass: per-chunk per-expert counts and bases
   size_t count, offset, mtiles;           // per-expert totals, row offsets, GEMM tile prefix
+  size_t ecap;                            // ranked dispatch: capacity left to this rank per expert
+  size_t out3s;                           // scratch losses of moe_aux_totals
   size_t partials, aux_vec;               // balancing partial sums and final vectors
   size_t idx, gate, thr, pos, keep;       // moe_forward's own copies of the gate / slot outputs
   size_t row_token, row_gate;             // moe_forward's dispatch maps
@@ -133,9 +135,11 @@ cudaError_t launch_aux_partials(const moe_config &cfg, bool noisy, const float *
                                 const float *sigma, const float *H, const float *rowstat,
                                 const int32_t *idx, const float *gate, const float *thr,
                                 float *partials, int n_blocks, cudaStream_t s);
+// raw_totals [4][E] or null: the summed partial rows (importance, load, first
+// choices, sum of Softmax(H)) in fp32 before any division by T.
 cudaError_t launch_aux_finalize(const moe_config &cfg, const float *partials, int n_blocks,
                                 float *out3, float *importance, float *load, float2 *aux_vec,
-                                DeviceStatus *st, cudaStream_t s);
+                                DeviceStatus *st, cudaStream_t s, float *raw_totals = nullptr);
 int aux_rows(int T, int E);  // partial rows of the balancing sums
 // Selection and balancing partials in one kernel (E <= 256).
 cudaError_t launch_select_aux(const moe_config &cfg, bool noisy, const float *c, const float *sigma,
@@ -204,12 +208,21 @@ cudaError_t launch_router_tc(const moe_config &cfg, const void *x, const float *
 
 // k_slots.cu: capacity, token-order slots, dispatch maps.
 // With allow_none, an expert index equal to E marks an empty choice (pos -1,
-// keep 0, no row) instead of an index error.
+// keep 0, no row) instead of an index error. With ranks, this rank's
+// assignments follow those of the earlier ranks (counts_all [W, E] device,
+// rank in 0..W-1): the capacity left to it per expert, max(0, C - the earlier
+// ranks' count), is written to ecap [E] and decides keep. With pos null only
+// the counts (and offsets) are computed.
+struct SlotRanks {
+  const int32_t *counts_all;
+  int rank;
+  int32_t *ecap;
+};
 cudaError_t launch_slots(const moe_config &cfg, int C, const int32_t *idx, const float *gate,
                          int32_t *hist, int32_t *chunk_base, int32_t *count, int32_t *offset,
                          int32_t *mtiles, int32_t *pos, uint8_t *keep, int32_t *row_token,
                          float *row_gate, int n_chunks, DeviceStatus *st, cudaStream_t s,
-                         bool allow_none = false);
+                         bool allow_none = false, const SlotRanks *ranks = nullptr);
 
 // k_rows.cu: gather of accepted token rows and the combine with the residual.
 cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *offset,
