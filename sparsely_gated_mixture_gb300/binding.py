@@ -303,8 +303,7 @@ def moe_forward_threshold(cfg, x, Wg, logit_bias, thresholds, W1, b1, W2, b2, y,
                                        _p(thresholds), _p(W1), _p(b1), _p(W2), _p(b2), _p(y),
                                        _p(expert_idx), _p(gate), _p(mask_out), _p(ws),
                                        _stream(stream)),
-           "moe_forward_threshold", "moe_expert_counts", "moe_dispatch_ranked",
-           "moe_aux_totals", "moe_aux_from_totals")
+           "moe_forward_threshold")
 
 
 def moe_expert_counts(cfg, expert_idx, expert_count, ws, stream=None):

@@ -43,6 +43,53 @@ k_gather(int A, int k, int nvec, const V *__restrict__ x, const int32_t *__restr
   for (; v < nvec; v += 32) dst[v] = src[v];
 }
 
+// Gather for short rows (at most 32 * VPL 16-byte vectors): each warp moves
+// RPW consecutive packed rows, their tokens and the row count read side by
+// side, then every row's vectors loaded before any is stored, so a warp has
+// RPW * VPL loads in flight instead of one row's worth.
+template <int RPW, int VPL>
+__global__ void __launch_bounds__(kRowWarps * 32)
+k_gather_short(int A, int k, int nvec, const uint4 *__restrict__ x,
+               const int32_t *__restrict__ offset_end, const int32_t *__restrict__ row_token,
+               uint4 *__restrict__ xbuf, DeviceStatus *st) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int r0 = (blockIdx.x * kRowWarps + (threadIdx.x >> 5)) * RPW;
+  if (r0 >= A) return;
+  const int end = min(*offset_end, A);
+  int a_l = -1;
+  if (lane < RPW && r0 + lane < A) a_l = row_token[r0 + lane];
+  uint4 v[RPW][VPL];
+  int tok[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const int a = __shfl_sync(0xffffffffu, a_l, i);
+    const bool live = r0 + i < end;
+    const bool ok = live && a >= 0 && a < A;
+    if (live && !ok && lane == 0) record_error(st, MOE_ERR_BOUNDS, (long long)(r0 + i));
+    tok[i] = ok ? a / k : -1;
+    if (tok[i] >= 0) {
+      const uint4 *src = x + (size_t)tok[i] * nvec;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int c = lane + 32 * j;
+        if (c < nvec) v[i][j] = src[c];
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    if (tok[i] < 0) continue;
+    uint4 *dst = xbuf + (size_t)(r0 + i) * nvec;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int c = lane + 32 * j;
+      if (c < nvec) dst[c] = v[i][j];
+    }
+  }
+}
+
 template <typename T>
 struct Act;
 template <>
@@ -242,7 +289,21 @@ cudaError_t launch_gather(const moe_config &cfg, const void *x, const int32_t *o
   const size_t row_bytes = (size_t)cfg.d * elem_bytes(cfg.act_dtype);
   dim3 grid((A + kRowWarps - 1) / kRowWarps);
   const int32_t *end = offset + cfg.E;
-  if (row_bytes % 16 == 0) {
+  const int nv16 = (int)(row_bytes / 16);
+  constexpr int kRpw = 4;
+  const dim3 grid_s((A + kRowWarps * kRpw - 1) / (kRowWarps * kRpw));
+  if (row_bytes % 16 == 0 && nv16 <= 64) {
+    if (nv16 <= 32)
+      launch_pdl(k_gather_short<kRpw, 1>, grid_s, kRowWarps * 32, 0, s, A, cfg.k, nv16,
+          (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
+    else
+      launch_pdl(k_gather_short<kRpw, 2>, grid_s, kRowWarps * 32, 0, s, A, cfg.k, nv16,
+          (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
+  } else if (row_bytes % 16 == 0 && nv16 <= 128) {
+    launch_pdl(k_gather_short<2, 4>, dim3((A + kRowWarps * 2 - 1) / (kRowWarps * 2)),
+        kRowWarps * 32, 0, s, A, cfg.k, nv16, (const uint4 *)x, end, row_token, (uint4 *)xbuf,
+        st);
+  } else if (row_bytes % 16 == 0) {
     launch_pdl(k_gather<uint4>, grid, kRowWarps * 32, 0, s, A, cfg.k, (int)(row_bytes / 16),
         (const uint4 *)x, end, row_token, (uint4 *)xbuf, st);
   } else if (row_bytes % 4 == 0) {
