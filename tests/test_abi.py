@@ -213,12 +213,15 @@ def test_python_wrappers_reach_the_library(lib):
     f = 1 << 20  # never dereferenced: the checks fail first
     cfg = B.config(64, 32, 16, 64, 4, 1.0)
     cases = [
-        (lambda: B.moe_forward_threshold(cfg, f, f, None, None, f, None, f, None, f, f), 1),
-        (lambda: B.moe_expert_counts(cfg, None, f, f), 1),
-        (lambda: B.moe_dispatch_ranked(cfg, 0, f, 2, 0, f, f, f, f, f, f, f, f, f, f, f), 1),
-        (lambda: B.moe_dispatch_ranked(cfg, 10, f, 2, 2, f, f, f, f, f, f, f, f, f, f, f), 1),
-        (lambda: B.moe_aux_totals(cfg, f + 16, f), 1),
-        (lambda: B.moe_aux_from_totals(cfg, 0, f, f, f), 1),
+        (lambda: B.moe_forward_threshold(cfg, f, f, None, None, f, None, f, None, f, f,
+                                         stream=0), 1),
+        (lambda: B.moe_expert_counts(cfg, None, f, f, stream=0), 1),
+        (lambda: B.moe_dispatch_ranked(cfg, 0, f, 2, 0, f, f, f, f, f, f, f, f, f, f, f,
+                                       stream=0), 1),
+        (lambda: B.moe_dispatch_ranked(cfg, 10, f, 2, 2, f, f, f, f, f, f, f, f, f, f, f,
+                                       stream=0), 1),
+        (lambda: B.moe_aux_totals(cfg, f + 16, f, stream=0), 1),
+        (lambda: B.moe_aux_from_totals(cfg, 0, f, f, f, stream=0), 1),
     ]
     for call, status in cases:
         with pytest.raises(B.MoEError) as e:
