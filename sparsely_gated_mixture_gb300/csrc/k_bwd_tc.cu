@@ -63,7 +63,15 @@ struct BParams {
   float *dgpart;  // mode 0: [padded rows, n_blocks]
   DeviceStatus *st;
   unsigned long long wait_ns;
+  uint32_t *sched;  // [2] the CTA-pair kernel's tile counter and done count (zero at launch)
+  int dynamic;      // CTA-pair kernel: tiles from the counter (else round robin)
 };
+
+// The CTA-pair kernel's tile ring, as in the forward expert GEMM: tile
+// indices from the even CTA's producer to the MMA issuer, both CTAs'
+// epilogue warps and the odd CTA's producer (ten arrivals free a slot).
+constexpr int kRing = 8;
+constexpr int kRingConsumers = 10;
 
 // kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M = 128,
 // N = 256; bits 15 / 16 select MN-major A / B.
@@ -472,9 +480,11 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES);
   uint64_t *full = bars, *empty = bars + P_STAGES;
   uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *tfull = drain + 1, *tempty = tfull + kRing;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + kRing);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *tile_start = reinterpret_cast<int *>(tmem_slot + 2);
+  volatile int *ring = reinterpret_cast<volatile int *>(tmem_slot + 2);
+  int *tile_start = const_cast<int *>(ring + kRing);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -489,6 +499,10 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 8);
+    }
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&tfull[r], 1);
+      mbar_init(&tempty[r], kRingConsumers);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -530,11 +544,49 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       // --------------------------------------------------------- producer (both CTAs)
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      // Tiles: each pair's first is its index, every later one taken from the
+      // counter by the even CTA's producer (the take issued a few k-blocks
+      // before the current tile's last load) and published through the ring.
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs) {
+      long long taken = -1;
+      int tile_rr = pair;
+      for (int j = 0; ok; ++j) {
+        const int slot = j % kRing;
+        const uint32_t rph = (uint32_t)(j / kRing) & 1u;
+        int tile;
+        if (leader) {
+          if (j == 0) {
+            tile = pair;
+          } else if (p.dynamic) {
+            if (taken < 0) taken = atomicAdd(p.sched, 1u);
+            tile = (int)min(taken + n_pairs, (long long)total_tiles);
+            taken = -1;
+          } else {
+            tile_rr += n_pairs;
+            tile = min(tile_rr, total_tiles);
+          }
+          if (!mbar_wait_cl(&tempty[slot], rph ^ 1u, abort_flag, p.st, 45, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          ring[slot] = tile;
+          st_cluster_u32(mapa(smem_u32((const void *)&ring[slot]), 1), (uint32_t)tile);
+          mbar_arrive_cluster(smem_u32(&tfull[slot]));
+          mbar_arrive_cluster(mapa(smem_u32(&tfull[slot]), 1));
+        } else {
+          if (!mbar_wait_cl(&tfull[slot], rph, abort_flag, p.st, 46, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tile = ring[slot];
+          mbar_arrive_cluster(mapa(smem_u32(&tempty[slot]), 0));
+        }
+        if (tile >= total_tiles) break;
         const BTile t = locate_pair<MODE>(p, tile_start, tile);
+        const int take_at = t.num_kb > 4 ? t.num_kb - 4 : 0;
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
+          if (leader && p.dynamic && kb == take_at) taken = atomicAdd(p.sched, 1u);
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 41, p.wait_ns)) {
@@ -553,19 +605,27 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int mcol = t.mb * 2 * BM + (int)rank * BM;
             const int ncol = t.nb * BN + (int)rank * (BN / 2);
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j)
-              tma_load_2d_pair(sA + s * P_A_BYTES + j * (BK * 128), &tmA, full_leader,
-                               mcol + j * 64, arow);
+            for (int q = 0; q < BM / 64; ++q)
+              tma_load_2d_pair(sA + s * P_A_BYTES + q * (BK * 128), &tmA, full_leader,
+                               mcol + q * 64, arow);
 #pragma unroll
-            for (int j = 0; j < (BN / 2) / 64; ++j)
-              tma_load_2d_pair(sB + s * P_B_BYTES + j * (BK * 128), &tmB, full_leader,
-                               ncol + j * 64, brow);
+            for (int q = 0; q < (BN / 2) / 64; ++q)
+              tma_load_2d_pair(sB + s * P_B_BYTES + q * (BK * 128), &tmB, full_leader,
+                               ncol + q * 64, brow);
           }
         }
       }
       const uint32_t issued = it;
       for (uint32_t q = issued > (uint32_t)P_STAGES ? issued - P_STAGES : 0; q < issued; ++q)
         mbar_drain(&empty[q % P_STAGES], (q / P_STAGES) & 1u);
+      if (leader && p.dynamic) {
+        // The last pair to finish resets the counter for the next launch.
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == (uint32_t)n_pairs - 1) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
     pdl_trigger();
@@ -573,9 +633,15 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     if (lane == 0 && leader) {
       // --------------------------------------------------------- MMA issuer (even CTA)
       uint32_t it = 0;
-      int local = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < total_tiles; tile += n_pairs, ++local) {
+      for (int local = 0; ok; ++local) {
+        const int slot = local % kRing;
+        if (!mbar_wait_cl(&tfull[slot], (uint32_t)(local / kRing) & 1u, abort_flag, p.st, 47,
+                          p.wait_ns))
+          break;
+        const int tile = ring[slot];
+        mbar_arrive_cluster(smem_u32(&tempty[slot]));
+        if (tile >= total_tiles) break;
         const BTile t = locate_pair<MODE>(p, tile_start, tile);
         const int buf = local & 1;
         const uint32_t use = (uint32_t)(local >> 1);
@@ -619,8 +685,21 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int r_in_tile = quad * 32 + lane;
     const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
-    int local = 0;
-    for (int tile = pair; tile < total_tiles; tile += n_pairs, ++local) {
+    for (int local = 0;; ++local) {
+      const int slot = local % kRing;
+      int tile = total_tiles;
+      bool got = false;
+      if (lane == 0) {
+        got = mbar_wait_cl(&tfull[slot], (uint32_t)(local / kRing) & 1u, abort_flag, p.st, 48,
+                           p.wait_ns);
+        if (got) {
+          tile = ring[slot];
+          mbar_arrive_cluster(mapa(smem_u32(&tempty[slot]), 0));
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (!got || tile >= total_tiles) break;
       const BTile t = locate_pair<MODE>(p, tile_start, tile);
       const int buf = local & 1;
       const uint32_t use = (uint32_t)(local >> 1);
@@ -648,8 +727,8 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 }
 
 constexpr size_t bwd_smem_bytes_pair(int E) {
-  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5) * 8 + 8 +
-         (size_t)(E + 1) * 4;
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 +
+         (size_t)kRing * 4 + (size_t)(E + 1) * 4;
 }
 
 constexpr size_t bwd_smem_bytes(int E) {
@@ -777,6 +856,11 @@ cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) 
   p.dgpart = g.dgpart;
   p.st = st;
   p.wait_ns = wait_limit_ns();
+  p.sched = &st->gemm_next;  // gemm_next, gemm_done: adjacent words
+  {
+    const char *v = getenv("MOE_FFN_SCHED");  // =static: round robin (for comparisons)
+    p.dynamic = v && v[0] == 's' ? 0 : 1;
+  }
   const long long nb = (g.N + BN - 1) / BN;
   if (g.mode == 2) {
     // A: the forward's packed rows [a_rows, M]; B: padded rows [b_rows, N].
