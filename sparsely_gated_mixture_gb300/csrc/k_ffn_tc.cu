@@ -45,6 +45,7 @@ struct Params {
   int K, N, E, n_blocks;
   uint32_t *sched;        // [2] the CTA-pair kernel's tile counter and done count (zero at launch)
   int dynamic;            // CTA-pair kernel: tiles from the counter (else round robin)
+  int half_tiles;         // CTA-pair kernel: short last row tiles at M = 128
   const int32_t *offset;  // [E+1] packed-row offsets
   const float *row_gate;  // layer 2 only
   const __nv_bfloat16 *bias;  // [E, N] or null
@@ -453,7 +454,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int local = tile - tile_start[e];
     nb = local / mt;
     pm = local % mt;
-    half = pm == mt - 1 && rows - pm * 2 * BM <= BM;
+    half = p.half_tiles && pm == mt - 1 && rows - pm * 2 * BM <= BM;
   };
 
   if (warp == 0) {
@@ -875,9 +876,12 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
     return cudaErrorInvalidValue;
   uint32_t *sched = &st->gemm_next;  // gemm_next, gemm_done: adjacent words
   const int dyn = ffn_dynamic();
-  Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, sched, dyn, offset, row_gate,
+  // MOE_FFN_HALF=0 runs every row tile at M = 256 (read at each call; for comparisons).
+  const char *hv = getenv("MOE_FFN_HALF");
+  const int half = hv && hv[0] == '0' ? 0 : 1;
+  Params p1{c.d, c.d_ff, c.E, (c.d_ff + BN - 1) / BN, sched, dyn, half, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b1), hbuf, st, wait_limit_ns()};
-  Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, sched, dyn, offset, row_gate,
+  Params p2{c.d_ff, c.d, c.E, (c.d + BN - 1) / BN, sched, dyn, half, offset, row_gate,
             static_cast<const __nv_bfloat16 *>(b2), zbuf, st, wait_limit_ns(), z_bf16 ? 1 : 0};
   // Per layer: the CTA pair pays off for long K and enough 256-row tiles to
   // fill several waves; otherwise the one-CTA kernel's finer tiles win.
