@@ -1184,54 +1184,55 @@ def cpu_baseline_bwd(w: wl.Workload, inp: dict, dy_bits, wts, n_sample: int) -> 
 
 def cpu_baseline_bal(w: wl.Workload, inp: dict, n_sample: int, threshold: bool = False) -> dict:
     """The oracle's balanced layer on the host cores: router, softmax and the
-    batchwise mask (or the threshold mask) over every token, the expert loop
-    for n_sample tokens, extrapolated."""
+    batchwise mask (or the threshold mask) over every token, then the expert
+    loop, timed on its own, for n_sample evenly spaced tokens; the layer's
+    tokens/s extrapolates the expert loop to T."""
     import oracle
 
     if threshold:
         inp = dict(inp, mode_bal=1, thr=wl.thresholds(w), with_loss=False)
-
     cores = len(os.sched_getaffinity(0))
     n = min(n_sample, w.T)
     tokens = np.linspace(0, w.T - 1, n).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.bal_forward(inp, tokens=tokens[:0])
+    ref = oracle.bal_forward(inp, tokens=tokens[:0])
     t_gate = time.perf_counter() - t0
+    idx = np.tile(np.arange(w.E, dtype=np.int32), (w.T, 1))
     t0 = time.perf_counter()
-    oracle.bal_forward(inp, tokens=tokens)
-    t_all = time.perf_counter() - t0
-    t_ffn = max(t_all - t_gate, 1e-9)
+    oracle.layer_out(inp["x"], idx, ref["gate"], ref["mask"], inp["W1"], inp["W2"],
+                     inp.get("b1"), inp.get("b2"), tokens)
+    t_ffn = time.perf_counter() - t0
     full = t_gate + t_ffn * (w.T / n)
     return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "extrapolated": True, "timed_tokens": n, "step_s": t_gate + t_all,
+            "extrapolated": True, "timed_tokens": n, "step_s": t_gate + t_ffn,
             "sample": f"router, softmax and {'threshold' if threshold else 'batchwise'} mask "
-                      f"over all {w.T} tokens "
-                      f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens, "
-                      f"extrapolated to {w.T} tokens"}
+                      f"over all {w.T} tokens ({t_gate:.2f} s) and the expert loop over {n} "
+                      f"evenly spaced tokens ({t_ffn:.3f} s), extrapolated to {w.T} tokens"}
 
 
 def cpu_baseline_hier(w: wl.HierWorkload, inp: dict, n_sample: int) -> dict:
     """The oracle's hierarchical layer on the host cores: both gates, the
-    two-level selection, slots and losses over every token, the expert loop
-    for n_sample tokens, extrapolated."""
+    two-level selection, slots and losses over every token, then the expert
+    loop, timed on its own, for n_sample evenly spaced tokens; the layer's
+    tokens/s extrapolates the expert loop to T."""
     import oracle
 
     cores = len(os.sched_getaffinity(0))
     n = min(n_sample, w.T)
     tokens = np.linspace(0, w.T - 1, n).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.hier_forward(inp, tokens=tokens[:0])
+    ref = oracle.hier_forward(inp, tokens=tokens[:0])
     t_gate = time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle.hier_forward(inp, tokens=tokens)
-    t_all = time.perf_counter() - t0
-    t_ffn = max(t_all - t_gate, 1e-9)
+    oracle.layer_out(inp["x"], ref["idx"], ref["gate"], ref["keep"], inp["W1"], inp["W2"],
+                     inp.get("b1"), inp.get("b2"), tokens)
+    t_ffn = time.perf_counter() - t0
     full = t_gate + t_ffn * (w.T / n)
     return {"value": w.T / full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "extrapolated": True, "timed_tokens": n, "step_s": t_gate + t_all,
+            "extrapolated": True, "timed_tokens": n, "step_s": t_gate + t_ffn,
             "sample": f"gates, selection, slots and losses over all {w.T} tokens "
-                      f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens, "
-                      f"extrapolated to {w.T} tokens"}
+                      f"({t_gate:.2f} s) and the expert loop over {n} evenly spaced tokens "
+                      f"({t_ffn:.3f} s), extrapolated to {w.T} tokens"}
 
 
 # ----------------------------------------------------------------------------- oracle timing
