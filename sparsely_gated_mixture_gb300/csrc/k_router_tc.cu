@@ -254,47 +254,51 @@ __device__ __forceinline__ void load_noise8(const RParams &p, int t, int e0, flo
   }
 }
 
+// The biases of experts e0 .. e0+n-1 (n <= 16; zero past E, past n or
+// without a bias) for an epilogue unit; every lane loads the same values.
+__device__ __forceinline__ void load_bias_n(const RParams &p, int e0, int n, float (&b)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) b[j] = (p.bias && j < n && e0 + j < p.E) ? p.bias[e0 + j] : 0.f;
+}
+
 // One unit of the TMA-store epilogue with the noise term: experts e0 .. e0+7
 // of tokens t0 .. t0+31 (lane l = token t0 + l). cv holds the clean logits and
-// zv the noise logits on entry; both are overwritten (c, then sigma, then H),
-// each [32 x 8] tile written to shared memory as soon as it is ready.
+// zv the noise logits on entry, bu the unit's biases; c, sigma and H are
+// computed in registers, then (once this warp's previous stores have read its
+// staging tiles) written as three [32 x 8] tiles and stored by TMA.
 // With fused selection, row points at this lane's token row in the shared
 // row buffers (c, sigma and H planes, plane stride ps floats); else null.
 __device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtensorMap *mc,
                                                   const CUtensorMap *ms, const CUtensorMap *mh,
                                                   int t0, int e0, float *cv, float *zv,
-                                                  const float *nz, float *stg, float *row,
-                                                  int ps) {
+                                                  const float *nz, const float *bu, float *stg,
+                                                  float *row, int ps) {
   const int lane = threadIdx.x & 31;
   float *sc = stg, *ss = stg + 256, *sh = stg + 512;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
-  tile_row_store8(sc, lane, cv);
-  if (row) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (e0 + j < p.E) row[ps + e0 + j] = cv[j];
-  }
+  float h[8];
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
+    if (p.bias) cv[j] += bu[j];
     zv[j] = softplus_r(zv[j]);
-    cv[j] = fmaf(nz[j], zv[j], cv[j]);
+    h[j] = fmaf(nz[j], zv[j], cv[j]);
+    bad |= e0 + j < p.E && !isfinite(h[j]);
   }
-  tile_row_store8(ss, lane, zv);
-  tile_row_store8(sh, lane, cv);
   if (row) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (e0 + j < p.E) {
-        row[e0 + j] = cv[j];
+        row[e0 + j] = h[j];
+        row[ps + e0 + j] = cv[j];
         row[2 * ps + e0 + j] = zv[j];
       }
   }
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
   if (bad && t0 + lane < p.T) record_error(p.st, MOE_ERR_NONFINITE, (long long)(t0 + lane));
+  if (lane == 0) bulk_wait_read_all();  // the last unit's stores have read the tiles
+  __syncwarp();
+  tile_row_store8(sc, lane, cv);
+  tile_row_store8(ss, lane, zv);
+  tile_row_store8(sh, lane, h);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
@@ -308,27 +312,42 @@ __device__ __forceinline__ void router_unit_noisy(const RParams &p, const CUtens
 // One unit without the noise term: H = c for experts e0 .. e0+15, one
 // [32 x 16] tile.
 __device__ __forceinline__ void router_unit_clean(const RParams &p, const CUtensorMap *mh, int t0,
-                                                  int e0, float *cv, float *stg, float *row) {
+                                                  int e0, float *cv, const float *bu, float *stg,
+                                                  float *row) {
   const int lane = threadIdx.x & 31;
+  bool bad = false;
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (p.bias && e0 + j < p.E) cv[j] += p.bias[e0 + j];
-  tile_row_store(stg, lane, cv);
+  for (int j = 0; j < 16; ++j) {
+    if (p.bias) cv[j] += bu[j];
+    bad |= e0 + j < p.E && !isfinite(cv[j]);
+  }
   if (row) {
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (e0 + j < p.E) row[e0 + j] = cv[j];
   }
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) bad |= e0 + j < p.E && !isfinite(cv[j]);
   if (bad && t0 + lane < p.T) record_error(p.st, MOE_ERR_NONFINITE, (long long)(t0 + lane));
+  if (lane == 0) bulk_wait_read_all();  // the last unit's stores have read the tile
+  __syncwarp();
+  tile_row_store(stg, lane, cv);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
     tma_store_2d(mh, stg, e0, t0);
     bulk_commit();
   }
+}
+
+// The 16 accumulator columns u*16 .. of a tile for this lane's token: column
+// j is hi[j] + (mid[j] + lo[j]) from the three BNR-wide sections.
+template <int BNR>
+__device__ __forceinline__ void unit_columns(uint32_t lane_addr, int u, float (&v)[16]) {
+  uint32_t r[48];
+  tmem_ld16x3(lane_addr + (uint32_t)(u * 16), lane_addr + (uint32_t)(BNR + u * 16),
+              lane_addr + (uint32_t)(2 * BNR + u * 16), r);
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = __uint_as_float(r[j]) + (__uint_as_float(r[16 + j]) + __uint_as_float(r[32 + j]));
 }
 
 // ----------------------------------------------------------------------------- fused selection
@@ -719,16 +738,10 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               }
             }
           }
-          uint32_t vh[16], vm[16], vl[16];
-          tmem_ld16(lane_addr + (uint32_t)(u * 16), vh);
-          tmem_ld16(lane_addr + (uint32_t)(BNR + u * 16), vm);
-          tmem_ld16(lane_addr + (uint32_t)(2 * BNR + u * 16), vl);
+          float bu[16];  // issued before the TMEM loads, so their latencies overlap
+          load_bias_n(p, eb + u * epu, epu, bu);
           float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            v[j] = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
-          if (lane == 0) bulk_wait_read_all();  // the last unit's stores have read the tiles
-          __syncwarp();
+          unit_columns<BNR>(lane_addr, u, v);
           if (p.noisy) {
             float cv[8], zv[8];
 #pragma unroll
@@ -736,10 +749,10 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
               cv[j] = v[2 * j];
               zv[j] = v[2 * j + 1];
             }
-            router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg, row,
+            router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, bu, stg, row,
                               fs.ps);
           } else {
-            router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg, row);
+            router_unit_clean(p, &tmH, t0, eb + u * epu, v, bu, stg, row);
           }
         }
         tc_fence_before();
@@ -806,6 +819,276 @@ k_router_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ----------------------------------------------------------------------------- CTA-pair form
+// The unfused router with tcgen05.mma.cta_group::2, for many column blocks
+// (large E). A cluster of two CTAs on two SMs computes a 256-token x
+// BNR-column tile: each CTA loads its own 128 token rows of x and half of the
+// three pieces' 3*BNR B rows (the even CTA rows 0 .. 3*BNR/2 - 1 of the
+// block, the odd CTA the rest), 28 KB per 64-deep K step instead of the
+// one-CTA form's 40 KB for the same work per SM. The even CTA issues the MMAs
+// (M = 256, N = 3*BNR); each CTA's token rows land in its own TMEM with the
+// one-CTA form's column layout (hi, mid, lo sections), and each CTA's eight
+// epilogue warps run the TMA-store epilogue on its rows. The odd CTA's TMA
+// completions are counted on the even CTA's "full" barriers, the MMA commits
+// arrive (multicast) on both CTAs' "empty" and "accumulator full" barriers,
+// and both CTAs' epilogue warps arrive on the even CTA's "accumulator empty"
+// barriers. Tiles go round robin over the pairs.
+//
+// The noise draws of a tile (this CTA's 128 tokens x BNR/2 experts, fp32)
+// come into shared memory by TMA, issued by the producer after the tile's
+// operand loads, into one of two buffers: the epilogue reads them from there
+// instead of loading them from HBM a unit ahead, a latency it could not hide.
+template <int BNR>
+struct RPCfg {
+  static constexpr int NB = 3 * BNR;
+  static constexpr int B_ROWS = NB / 2;                  // B rows held per CTA
+  static constexpr int A_BYTES = RBM * RBK * 2;          // 16 KB
+  static constexpr int B_BYTES = B_ROWS * RBK * 2;       // 12 KB at BNR = 64
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int NZ_COLS = BNR / 2;                // experts per tile (noise term)
+  static constexpr int NZ_BYTES = RBM * NZ_COLS * 4;     // 16 KB at BNR = 64
+  static constexpr int FIT = (227 * 1024 - 1024 - 2 * NZ_BYTES - EPI_BYTES - 512) / STAGE;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int TMEM_COLS = RCfg<BNR>::TMEM_COLS;
+  // kind::f16: fp32 accumulate, bf16 A and B, both K-major, M = 256, N = 3*BNR.
+  static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                                    ((uint32_t)(NB >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE + 2 * NZ_BYTES + EPI_BYTES +
+                                 (2 * STAGES + 9) * 8 + 8;
+  static_assert(NZ_COLS * 4 == 128, "one 128-byte swizzled row of noise per token");
+  static_assert(B_ROWS % 8 == 0 && STAGE % 1024 == 0, "swizzle atoms");
+  static_assert(STAGES >= 4, "pipeline depth");
+};
+
+__device__ __forceinline__ void umma_rp(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// Noise draws of token row r (0..127) of a tile, experts u*8 .. u*8+7 of the
+// tile's 32, from a [128 x 32] fp32 buffer in the 128-byte swizzle (16-byte
+// chunk q of row r at chunk q ^ (r & 7)).
+__device__ __forceinline__ void noise_from_smem(const float *buf, int r, int u, float *nz) {
+  const float4 *row = reinterpret_cast<const float4 *>(buf + r * 32);
+  const float4 a = row[(2 * u) ^ (r & 7)], b = row[(2 * u + 1) ^ (r & 7)];
+  nz[0] = a.x; nz[1] = a.y; nz[2] = a.z; nz[3] = a.w;
+  nz[4] = b.x; nz[5] = b.y; nz[6] = b.z; nz[7] = b.w;
+}
+
+// tmB's box is RPCfg::B_ROWS rows; tmN the noise [T, E] fp32, box [128 tokens
+// x BNR/2 experts], 128-byte swizzle (unused without the noise term); tmC,
+// tmS, tmH as for k_router_tc (the TMA-store epilogue only).
+template <int BNR>
+__global__ void __launch_bounds__(kRThreads, 1)
+k_router_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmN, const __grid_constant__ CUtensorMap tmC,
+                 const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmH,
+                 const RParams p) {
+  using C = RPCfg<BNR>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  float *nzbuf = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE);  // [2][128][32]
+  float *staging = reinterpret_cast<float *>(smem + C::STAGES * C::STAGE + 2 * C::NZ_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE + 2 * C::NZ_BYTES +
+                                                EPI_BYTES);
+  uint64_t *full = bars, *empty = bars + C::STAGES;
+  uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
+  uint64_t *nz_full = drain + 1, *nz_empty = nz_full + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(nz_empty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);   // the even CTA's expect_tx arrival
+      mbar_init(&empty[s], 1);  // one multicast commit per use
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * kREpiWarps);  // both CTAs' epilogue warps
+      mbar_init(&nz_full[b], 1);                 // this CTA's expect_tx arrival
+      mbar_init(&nz_empty[b], kREpiWarps);       // this CTA's epilogue warps
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  pdl_wait();  // the split weights come from the kernel before
+  pdl_trigger();
+  const uint32_t tmem_base = *tmem_slot;
+  const int m_blocks = (p.T + 2 * RBM - 1) / (2 * RBM);
+  const int total = m_blocks * p.n_blocks;
+  const int num_kb = (p.d + RBK - 1) / RBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- producer (both CTAs)
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+      if (p.noisy) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmN) : "memory");
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += n_pairs, ++local) {
+        const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+        const int arow = mb * 2 * RBM + (int)rank * RBM;
+        const int brow = nb * C::NB + (int)rank * C::B_ROWS;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.st, 25, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = mapa(smem_u32(&full[s]), 0);
+          if (leader) mbar_expect_tx(&full[s], 2 * C::STAGE);
+          uint8_t *st = smem + s * C::STAGE;
+          tma_load_2d_pair(st, &tmA, full_leader, kb * RBK, arow);
+          tma_load_2d_pair(st + C::A_BYTES, &tmB, full_leader, kb * RBK, brow);
+        }
+        if (ok && p.noisy) {
+          // The tile's noise, once the epilogue is done with this buffer's
+          // previous tile (two tiles back).
+          const int nbuf = local & 1;
+          const uint32_t use = (uint32_t)(local >> 1);
+          if (!mbar_wait(&nz_empty[nbuf], (use & 1u) ^ 1u, abort_flag, p.st, 29, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&nz_full[nbuf], C::NZ_BYTES);
+          tma_load_2d(nzbuf + nbuf * (C::NZ_BYTES / 4), &tmN, &nz_full[nbuf], nb * C::NZ_COLS,
+                      arow);
+        }
+      }
+      // This CTA's copies have landed once the MMAs that read them are done,
+      // and its noise once the epilogue has read it.
+      const uint32_t issued = it;
+      for (uint32_t q = issued > (uint32_t)C::STAGES ? issued - C::STAGES : 0; q < issued; ++q)
+        mbar_drain(&empty[q % C::STAGES], (q / C::STAGES) & 1u);
+      if (p.noisy)
+        for (int q = local > 2 ? local - 2 : 0; q < local; ++q)
+          mbar_drain(&nz_full[q & 1], (uint32_t)(q >> 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ----------------------------------------------------------- MMA issuer (even CTA)
+      uint32_t it = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = pair; ok && tile < total; tile += n_pairs, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = (uint32_t)(local >> 1);
+        if (!mbar_wait(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag, p.st, 26, p.wait_ns)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * C::NB);
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (it / C::STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, p.st, 27, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < RBK / 16; ++kk) {
+            const uint64_t ad = sdesc(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc(a0 + C::A_BYTES + kk * 32, 16, 1024);
+            umma_rp(tmem_d, ad, bd, C::IDESC, (kb | kk) ? 1u : 0u);
+          }
+          umma_commit_pair(&empty[s]);
+        }
+        if (ok) umma_commit_pair(&acc_full[buf]);
+      }
+      umma_commit_pair(drain, 0x1);
+      mbar_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;        // TMEM lanes 32*quad .. 32*quad+31
+    const int sub = (warp - 2) >> 2;  // this warp's units: sub, sub+2, ...
+    const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
+    const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
+    float *stg = staging + (size_t)(warp - 2) * kEpiWarpFloats;
+    const int epu = p.noisy ? 8 : 16;  // experts per unit
+    const int r = quad * 32 + lane;    // this lane's token row in the tile
+    int local = 0;
+    for (int tile = pair; tile < total; tile += n_pairs, ++local) {
+      const int mb = tile / p.n_blocks, nb = tile % p.n_blocks;
+      const int buf = local & 1;
+      const uint32_t use = (uint32_t)(local >> 1);
+      bool ready = mbar_wait(&acc_full[buf], use & 1u, abort_flag, p.st, 28, p.wait_ns);
+      if (p.noisy) ready = ready && mbar_wait(&nz_full[buf], use & 1u, abort_flag, p.st, 30,
+                                              p.wait_ns);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      const int t0 = mb * 2 * RBM + (int)rank * RBM + quad * 32;
+      const uint32_t lane_addr =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * C::NB);
+      const int ncols = min(p.NC - nb * BNR, BNR);
+      const int nunits = (ncols + 15) / 16;
+      const int eb = p.noisy ? (nb * BNR) >> 1 : nb * BNR;  // first expert of the block
+      const float *nzt = nzbuf + buf * (C::NZ_BYTES / 4);
+#pragma unroll 1
+      for (int u = sub; u < nunits; u += 2) {
+        float bu[16];  // issued before the TMEM loads, so their latencies overlap
+        load_bias_n(p, eb + u * epu, epu, bu);
+        float nz[8];
+        if (p.noisy) noise_from_smem(nzt, r, u, nz);
+        float v[16];
+        unit_columns<BNR>(lane_addr, u, v);
+        if (p.noisy) {
+          float cv[8], zv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            cv[j] = v[2 * j];
+            zv[j] = v[2 * j + 1];
+          }
+          router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, bu, stg, nullptr,
+                            0);
+        } else {
+          router_unit_clean(p, &tmH, t0, eb + u * epu, v, bu, stg, nullptr);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_remote(buf ? acc_empty_leader1 : acc_empty_leader0);
+        if (p.noisy) mbar_arrive(&nz_empty[buf]);
+      }
+    }
+  }
+  if (warp >= 2 && lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
+  tc_fence_before();
+  cluster_sync_all();  // every MMA reading either CTA's memory and every TMEM read are done
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(C::TMEM_COLS)
                  : "memory");
   }
@@ -1008,16 +1291,9 @@ k_router_grp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       for (int u = sub; u < nunits; u += 2) {
         float nz[8];
         if (p.noisy) load_noise8_g(p, t, (size_t)gi * p.E + eb + u * 8, nz);
-        uint32_t vh[16], vm[16], vl[16];
-        tmem_ld16(lane_addr + (uint32_t)(u * 16), vh);
-        tmem_ld16(lane_addr + (uint32_t)(BNR + u * 16), vm);
-        tmem_ld16(lane_addr + (uint32_t)(2 * BNR + u * 16), vl);
+        const float bu[16] = {};  // no router bias in the grouped form
         float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          v[j] = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+        unit_columns<BNR>(lane_addr, u, v);
         if (p.noisy) {
           float cv[8], zv[8];
 #pragma unroll
@@ -1025,9 +1301,10 @@ k_router_grp(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             cv[j] = v[2 * j];
             zv[j] = v[2 * j + 1];
           }
-          router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, stg, nullptr, 0);
+          router_unit_noisy(p, &tmC, &tmS, &tmH, t0, eb + u * epu, cv, zv, nz, bu, stg, nullptr,
+                            0);
         } else {
-          router_unit_clean(p, &tmH, t0, eb + u * epu, v, stg, nullptr);
+          router_unit_clean(p, &tmH, t0, eb + u * epu, v, bu, stg, nullptr);
         }
       }
       tc_fence_before();
@@ -1062,6 +1339,84 @@ bool make_out_map(CUtensorMap *m, float *base, int T, int E, bool noisy) {
             CU_TENSOR_MAP_INTERLEAVE_NONE,
             noisy ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MOE_ROUTER_PAIR=0 keeps the one-CTA form, =1 takes the CTA-pair form
+// wherever it applies (read at each call; for comparisons and tests);
+// otherwise the pair form runs where there are at least four 128-row tiles per
+// SM over two or more column blocks.
+bool use_pair(int tiles, int n_blocks) {
+  const char *v = getenv("MOE_ROUTER_PAIR");
+  if (v && v[0] == '0') return false;
+  if (n_blocks < 2) return false;
+  if (v && v[0] == '1') return true;
+  return tiles >= 4 * sm_count();
+}
+
+cudaLaunchAttribute router_cluster_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 2;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  return a;
+}
+
+// Clusters of two that can be resident at once for the CTA-pair form (0 if
+// none); one shared-memory size, so looked up once.
+int pair_router_clusters() {
+  static const int n = [] {
+    const size_t smem = RPCfg<64>::SMEM;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sm_count() / 2));
+    cfg.blockDim = dim3(kRThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1] = {router_cluster_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int m = 0;
+    if (cudaFuncSetAttribute(k_router_tc_pair<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&m, k_router_tc_pair<64>, &cfg) != cudaSuccess)
+      m = 0;
+    return m;
+  }();
+  return n;
+}
+
+// 2-D fp32 tensor [T, E] (E % 4 == 0): the noise draws, box [128 tokens, 32
+// experts] in the 128-byte swizzle, for the CTA-pair form's epilogue.
+bool make_noise_map(CUtensorMap *m, const float *base, int T, int E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)E * 4};
+  cuuint32_t box[2] = {32u, (cuuint32_t)RBM};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BNR>
+cudaError_t launch_router_pair(const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &tn,
+                               const CUtensorMap &tc, const CUtensorMap &ts, const CUtensorMap &th,
+                               const RParams &p, int clusters, cudaStream_t s) {
+  const size_t smem = RPCfg<BNR>::SMEM;
+  cudaError_t err = cudaFuncSetAttribute(k_router_tc_pair<BNR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2] = {router_cluster_attr(), {}};
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_router_tc_pair<BNR>, ta, tb, tn, tc, ts, th, p);
 }
 
 template <int BNR>
@@ -1101,8 +1456,23 @@ cudaError_t run(const moe_config &c, const void *x, const float *Wg, const float
             wait_limit_ns(), fuse ? 1 : 0, c.k, c.gate_mode,
             fuse ? sel->idx : nullptr, fuse ? sel->gate : nullptr, fuse ? sel->thr : nullptr,
             fuse ? sel->rowstat : nullptr, fuse ? sel->partials : nullptr};
-  const size_t smem = RCfg<BNR>::SMEM;
   const int tiles = ((c.T + RBM - 1) / RBM) * n_blocks;
+  if constexpr (BNR == 64) {
+    if (!fuse && tma_out && use_pair(tiles, n_blocks)) {
+      const int clusters = pair_router_clusters();
+      CUtensorMap tbp, tn = ta;  // tn: unused without the noise term
+      if (clusters > 0 &&
+          make_map(&tbp, bsplit, (uint64_t)3 * NCP, (uint64_t)c.d, RPCfg<BNR>::B_ROWS) &&
+          (!noisy || ((uintptr_t)noise % 16 == 0 && make_noise_map(&tn, noise, c.T, c.E)))) {
+        const int pair_tiles = ((c.T + 2 * RBM - 1) / (2 * RBM)) * n_blocks;
+        const int n = pair_tiles < clusters ? pair_tiles : clusters;
+        err = launch_router_pair<BNR>(ta, tbp, tn, tc, ts, th, p, n, s);
+        if (err == cudaSuccess && selected) *selected = false;
+        return err;
+      }
+    }
+  }
+  const size_t smem = RCfg<BNR>::SMEM;
   const int grid = fuse || tiles < sm_count() ? tiles : sm_count();
   const int kmf = !fuse ? 0 : c.k <= 2 ? 2 : c.k <= 4 ? 4 : kFuseMaxK;
   auto kernel = kmf == 0 ? k_router_tc<BNR, 0>
