@@ -413,6 +413,10 @@ constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int P_B_BYTES = BK * (BN / 2) * 2;    // 16 KB
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+// Weight-gradient epilogue staging: per epilogue warp two [32 rows x 32
+// columns] fp32 tiles (4 KB each) in the 128-byte swizzle.
+constexpr int P_STG_TILE = 32 * 32;  // floats
+constexpr int P_STG_BYTES = 4 * 2 * P_STG_TILE * 4;
 
 template <int MODE>
 __host__ __device__ constexpr uint32_t bwd_idesc_pair() {
@@ -467,17 +471,62 @@ __device__ __forceinline__ BTile locate_pair(const BParams &p, const int *start,
   return t;
 }
 
+// The weight-gradient epilogue of the CTA-pair kernel: this warp's 32 rows
+// m0 .. m0+31 of expert e's dW tile, 32 columns at a time from TMEM into one
+// of the warp's two staging tiles, then out by a TMA store into dW viewed as
+// [E, M, N] (tmO), which drops rows past M and columns past N. The per-lane
+// row stores of the other modes send 32 rows' 16-byte pieces per instruction;
+// here each store writes whole 128-byte row segments, and the fp32 output
+// (4 bytes per product of a K = rows-per-expert reduction) no longer holds
+// the tensor pipe back. cnt counts this warp's staged chunks (buffer parity).
+__device__ __forceinline__ void epilogue_wgrad_tma(const BParams &p, const BTile &t, int m0,
+                                                   uint32_t lane_addr, float *stg,
+                                                   const CUtensorMap *tmO, uint32_t &cnt) {
+  const int lane = threadIdx.x & 31;
+  bool bad = false;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int n = t.nb * BN + c * 32;
+    uint32_t v[32];
+    tmem_ld32(lane_addr + (uint32_t)(c * 32), v);  // warp-collective
+    if (n >= p.N) continue;
+    float *buf = stg + (cnt & 1u) * P_STG_TILE;
+    if (lane == 0) bulk_wait_read_but1();  // this buffer's previous store has read it
+    __syncwarp();
+    float4 *row = reinterpret_cast<float4 *>(buf + lane * 32);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 f = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      bad |= !isfinite(f.x) || !isfinite(f.y) || !isfinite(f.z) || !isfinite(f.w);
+      row[q ^ (lane & 7)] = f;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmO, buf, n, m0, t.e);
+      bulk_commit();
+    }
+    ++cnt;
+  }
+  if (bad && m0 + lane < p.M) record_error(p.st, MOE_ERR_NONFINITE, (long long)(m0 + lane));
+}
+
+// tmO: mode 2's output dW as [E, M, N] fp32, box [1, 32, 32], 128-byte
+// swizzle (unused in modes 0 and 1).
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const BParams p) {
+              const __grid_constant__ CUtensorMap tmO, const BParams p) {
   pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + P_STAGES * P_A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES);
+  float *stg_all = reinterpret_cast<float *>(sB + P_STAGES * P_B_BYTES);  // mode 2 only
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES +
+                                                (MODE == 2 ? P_STG_BYTES : 0));
   uint64_t *full = bars, *empty = bars + P_STAGES;
   uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
   uint64_t *tfull = drain + 1, *tempty = tfull + kRing;
@@ -685,6 +734,8 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int r_in_tile = quad * 32 + lane;
     const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
+    float *stg = stg_all + (size_t)(warp - 2) * 2 * P_STG_TILE;  // mode 2
+    uint32_t stg_cnt = 0;
     for (int local = 0;; ++local) {
       const int slot = local % kRing;
       int tile = total_tiles;
@@ -708,12 +759,17 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (!ready) break;
       tc_fence_after();
       const int m = t.mb * 2 * BM + (int)rank * BM + r_in_tile;
-      epilogue_rows<MODE>(p, t, m, tmem_base + ((uint32_t)(quad * 32) << 16) +
-                                       (uint32_t)(buf * BN));
+      const uint32_t lane_addr =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(buf * BN);
+      if constexpr (MODE == 2)
+        epilogue_wgrad_tma(p, t, m - lane, lane_addr, stg, &tmO, stg_cnt);
+      else
+        epilogue_rows<MODE>(p, t, m, lane_addr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
+    if (MODE == 2 && lane == 0) bulk_wait_all();  // this warp's dW stores are complete
     pdl_trigger();
   }
   tc_fence_before();
@@ -726,9 +782,9 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
 }
 
-constexpr size_t bwd_smem_bytes_pair(int E) {
-  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 +
-         (size_t)kRing * 4 + (size_t)(E + 1) * 4;
+constexpr size_t bwd_smem_bytes_pair(int E, int mode) {
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (mode == 2 ? P_STG_BYTES : 0) +
+         (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 + (size_t)kRing * 4 + (size_t)(E + 1) * 4;
 }
 
 constexpr size_t bwd_smem_bytes(int E) {
@@ -779,9 +835,9 @@ int pair_clusters_bwd(size_t smem) {
 }
 
 template <int MODE>
-cudaError_t launch_mode_pair(const CUtensorMap &a, const CUtensorMap &b, const BParams &p,
-                             int clusters, cudaStream_t s) {
-  const size_t smem = bwd_smem_bytes_pair(p.E);
+cudaError_t launch_mode_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                             const BParams &p, int clusters, cudaStream_t s) {
+  const size_t smem = bwd_smem_bytes_pair(p.E, MODE);
   cudaError_t err = cudaFuncSetAttribute(
       k_bwd_tc_pair<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -795,7 +851,7 @@ cudaError_t launch_mode_pair(const CUtensorMap &a, const CUtensorMap &b, const B
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled(kPdlGemm) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_bwd_tc_pair<MODE>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, k_bwd_tc_pair<MODE>, a, b, o, p);
 }
 
 template <int MODE>
@@ -809,7 +865,21 @@ cudaError_t launch_mode(const CUtensorMap &a, const CUtensorMap &b, const BParam
   return cudaGetLastError();
 }
 
-// 2-D bf16 tensor [rows, cols], box [box_rows, 64 cols], 128B swizzle (make_map).
+// 3-D fp32 tensor [E, M, N] (N % 4 == 0): the weight gradient, box [1, 32
+// rows, 32 columns] in the 128-byte swizzle, for the CTA-pair kernel's TMA
+// stores (rows past M and columns past N of a box are not written).
+bool make_out_map3(CUtensorMap *m, float *base, int E, int M, int N) {
+  auto fn = encode_fn();
+  if (!fn || N % 4 != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)N * 4, (cuuint64_t)M * N * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 
 }  // namespace
 
@@ -831,8 +901,8 @@ static int bwd_variant() {
 template <int MODE>
 static int pick_pair(const BwdGemm &g, long long k_len, long long tiles) {
   const int force = bwd_variant();
-  if (force == 1 || bwd_smem_bytes_pair(g.E) > 227 * 1024) return 0;
-  const int clusters = pair_clusters_bwd<MODE>(bwd_smem_bytes_pair(g.E));
+  if (force == 1 || bwd_smem_bytes_pair(g.E, MODE) > 227 * 1024) return 0;
+  const int clusters = pair_clusters_bwd<MODE>(bwd_smem_bytes_pair(g.E, MODE));
   if (clusters <= 0) return 0;
   if (force == 2) return clusters;
   return (k_len >= 1024 && tiles >= 4LL * clusters) ? clusters : 0;
@@ -868,7 +938,11 @@ cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) 
         !make_map(&tb, g.B, (uint64_t)g.b_rows, (uint64_t)g.N, 64))
       return cudaErrorInvalidValue;
     const int cl = pick_pair<2>(g, g.k_len, (long long)g.E * ((g.M + 255) / 256) * nb);
-    return cl > 0 ? launch_mode_pair<2>(ta, tb, p, cl, s) : launch_mode<2>(ta, tb, p, s);
+    CUtensorMap to;
+    if (cl > 0 && (uintptr_t)g.out % 16 == 0 &&
+        make_out_map3(&to, static_cast<float *>(g.out), g.E, g.M, g.N))
+      return launch_mode_pair<2>(ta, tb, to, p, cl, s);
+    return launch_mode<2>(ta, tb, p, s);
   }
   // A: padded rows [a_rows, K]; B: the weight as [E*N rows, K] (the pair
   // kernel loads half of a tile's 256 B rows per CTA).
@@ -878,8 +952,8 @@ cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) 
       !make_map(&tb, g.B, (uint64_t)g.E * g.N, (uint64_t)g.K, cl > 0 ? BN / 2 : BN))
     return cudaErrorInvalidValue;
   if (cl > 0)
-    return g.mode == 0 ? launch_mode_pair<0>(ta, tb, p, cl, s)
-                       : launch_mode_pair<1>(ta, tb, p, cl, s);
+    return g.mode == 0 ? launch_mode_pair<0>(ta, tb, ta, p, cl, s)
+                       : launch_mode_pair<1>(ta, tb, ta, p, cl, s);
   return g.mode == 0 ? launch_mode<0>(ta, tb, p, s) : launch_mode<1>(ta, tb, p, s);
 }
 

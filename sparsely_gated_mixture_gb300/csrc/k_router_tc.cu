@@ -71,27 +71,6 @@ __device__ __forceinline__ float softplus_r(float z) {
   return fmaxf(z, 0.0f) + 2.f * sv * q;
 }
 
-// TMA store of a shared-memory tile, and the bulk-group bookkeeping around it.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x,
-                                             int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   (uint64_t)map),
-               "r"(smem_u32(src)), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Row l of a [32 x 8] fp32 tile in the 32-byte swizzle of the TMA store:
 // 16-byte chunk q of row l sits at chunk q ^ ((l >> 2) & 1).
 __device__ __forceinline__ void tile_row_store8(float *tile, int l, const float *v) {
