@@ -53,6 +53,7 @@ struct Params {
   DeviceStatus *st;
   unsigned long long wait_ns;  // bounded-wait limit
   int z_bf16;                  // layer 2 writes Z in bf16
+  int tma_out;                 // CTA-pair kernel: whole 32-row groups leave by TMA store
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -343,6 +344,51 @@ constexpr int P_BN_HALF = BN / 2;               // B columns held per CTA
 constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int P_B_BYTES = BK * P_BN_HALF * 2;   // 16 KB
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+// Epilogue staging of the CTA-pair kernel: per epilogue warp two 4 KB tiles,
+// each [32 rows x 32 columns] of the output (fp32 in the 128-byte swizzle,
+// bf16 in the 64-byte swizzle).
+constexpr int P_STG_TILE = 32 * 32;  // floats
+constexpr int P_STG_BYTES = 4 * 2 * P_STG_TILE * 4;
+
+// One warp's 32 output rows x 32 columns, staged and sent by one TMA store at
+// column n, packed row r0 (tmO: the output [rows, N], box [32 rows, 32
+// columns]). The per-lane row stores send 32 rows' 16-byte pieces per
+// instruction and cost the GEMM 5-7% of its time; a TMA store writes whole row
+// segments. buf is the warp's staging tile for this chunk; before it is
+// written, the store that last read it (two chunks back) must have read it.
+__device__ __forceinline__ void stage_store_bf16(const CUtensorMap *tmO, float *buf,
+                                                 const uint32_t (&packed)[16], int n, int r0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_but1();
+  __syncwarp();
+  uint4 *row = reinterpret_cast<uint4 *>(buf) + lane * 4;  // 64-byte rows
+  const int x = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    row[q ^ x] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, buf, n, r0);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void stage_store_f32(const CUtensorMap *tmO, float *buf,
+                                                const float (&f)[32], int n, int r0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_but1();
+  __syncwarp();
+  float4 *row = reinterpret_cast<float4 *>(buf) + lane * 8;  // 128-byte rows
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    row[q ^ (lane & 7)] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, buf, n, r0);
+    bulk_commit();
+  }
+}
 // kind::f16, fp32 accumulate, bf16 A/B, A K-major, B MN-major, M = 256, N = 256.
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
@@ -366,14 +412,15 @@ __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint64_t a, uint64_t 
 template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const Params p) {
+              const __grid_constant__ CUtensorMap tmO, const Params p) {
   pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + P_STAGES * P_A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES);
+  float *stg_all = reinterpret_cast<float *>(sB + P_STAGES * P_B_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES + P_STG_BYTES);
   uint64_t *full = bars, *empty = bars + P_STAGES;
   uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
   uint64_t *tfull = drain + 1, *tempty = tfull + kRing;  // the tile ring's barriers
@@ -598,6 +645,8 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int r_in_tile = quad * 32 + lane;
     const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
+    float *stg = stg_all + (size_t)(warp - 2) * 2 * P_STG_TILE;  // this warp's two tiles
+    uint32_t stg_cnt = 0;                                         // chunks staged so far
     for (int local = 0;; ++local) {
       const int slot = local % kRing;
       int tile = total_tiles;
@@ -632,6 +681,10 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const bool valid = m < rows;
       const size_t r = (size_t)row0 + m;
       const float g = (LAYER == 2 && valid) ? p.row_gate[r] : 1.f;
+      // The warp's 32 rows all belong to this expert: they leave by TMA store
+      // (a partial group would spill into the next expert's rows).
+      const bool tma_rows = p.tma_out && m - lane + 32 <= rows;
+      const int r0 = row0 + m - lane;
       bool bad = false;
 #pragma unroll 1
       for (int c = 0; c < nchunks; ++c) {
@@ -647,8 +700,8 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           f[j] = __uint_as_float(v[j]);
           if (p.bias) f[j] += __bfloat162float(p.bias[(size_t)e * p.N + n + j]);
         }
+        float *sbuf = stg + (stg_cnt & 1u) * P_STG_TILE;
         if (LAYER == 1) {
-          __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -656,10 +709,16 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 __floats2bfloat162_rn(fmaxf(f[2 * j], 0.f), fmaxf(f[2 * j + 1], 0.f));
             packed[j] = *reinterpret_cast<uint32_t *>(&h2);
           }
+          if (tma_rows) {
+            stage_store_bf16(&tmO, sbuf, packed, n, r0);
+            ++stg_cnt;
+          } else {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<uint4 *>(o)[q] =
-                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                           packed[4 * q + 2], packed[4 * q + 3]);
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -667,17 +726,25 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             bad |= !isfinite(f[j]);
           }
           if (p.z_bf16) {
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
               packed[j] = *reinterpret_cast<uint32_t *>(&h2);
             }
+            if (tma_rows) {
+              stage_store_bf16(&tmO, sbuf, packed, n, r0);
+              ++stg_cnt;
+            } else {
+              __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
-                                                           packed[4 * q + 2], packed[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                             packed[4 * q + 2], packed[4 * q + 3]);
+            }
+          } else if (tma_rows) {
+            stage_store_f32(&tmO, sbuf, f, n, r0);
+            ++stg_cnt;
           } else {
             float *o = static_cast<float *>(p.out) + r * p.N + n;
 #pragma unroll
@@ -692,6 +759,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
     pdl_trigger();
   }
   tc_fence_before();
@@ -753,6 +821,23 @@ int sm_count() {
 
 namespace {
 
+// 2-D tensor [rows, cols] (cols % 8 == 0, 16-byte-aligned base) of bf16 or
+// fp32: an expert GEMM's output, box [32 rows, 32 columns] in the 64-byte
+// (bf16) or 128-byte (fp32) swizzle, for the CTA-pair kernel's TMA stores.
+bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, bool f32) {
+  auto fn = encode_fn();
+  if (!fn || (uintptr_t)base % 16 != 0 || cols % 8 != 0) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr size_t smem_bytes(int E) {
   return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 8 + (size_t)(E + 1) * 4;
 }
@@ -769,8 +854,8 @@ cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const Param
 }
 
 constexpr size_t smem_bytes_pair(int E) {
-  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 +
-         (size_t)kRing * 4 + (size_t)(E + 1) * 4;
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_STG_BYTES +
+         (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 + (size_t)kRing * 4 + (size_t)(E + 1) * 4;
 }
 
 cudaLaunchAttribute pair_cluster_attr() {
@@ -816,8 +901,8 @@ int pair_clusters(size_t smem) {
 }
 
 template <int LAYER>
-cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const Params &p,
-                              int clusters, cudaStream_t s) {
+cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                              const Params &p, int clusters, cudaStream_t s) {
   const size_t smem = smem_bytes_pair(p.E);
   cudaError_t err = cudaFuncSetAttribute(
       k_ffn_tc_pair<LAYER>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -832,7 +917,7 @@ cudaError_t launch_layer_pair(const CUtensorMap &a, const CUtensorMap &b, const 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled(kPdlGemm) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k_ffn_tc_pair<LAYER>, a, b, p);
+  return cudaLaunchKernelEx(&cfg, k_ffn_tc_pair<LAYER>, a, b, o, p);
 }
 
 // MOE_FFN_SCHED=static makes the CTA-pair kernel take its tiles round robin
@@ -892,10 +977,16 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
     return clusters > 0 &&
            (force_pair || (K >= 2048 && (rows / 256) * ((N + BN - 1) / BN) >= 4L * clusters));
   };
-  cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, p1, clusters, s)
+  // The CTA-pair kernel's output maps (H, then Z): box [32 rows, 32 columns].
+  CUtensorMap to1, to2;
+  p1.tma_out = make_rows_map(&to1, hbuf, A, c.d_ff, false) ? 1 : 0;
+  p2.tma_out = make_rows_map(&to2, zbuf, A, c.d, !z_bf16) ? 1 : 0;
+  if (!p1.tma_out) to1 = ta1;  // unused
+  if (!p2.tma_out) to2 = ta2;
+  cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, to1, p1, clusters, s)
                                           : launch_layer<1>(ta1, tb1, p1, s);
   if (err != cudaSuccess) return err;
-  return pair_for(c.d_ff, c.d) ? launch_layer_pair<2>(ta2, tb2, p2, clusters, s)
+  return pair_for(c.d_ff, c.d) ? launch_layer_pair<2>(ta2, tb2, to2, p2, clusters, s)
                                : launch_layer<2>(ta2, tb2, p2, s);
 }
 
