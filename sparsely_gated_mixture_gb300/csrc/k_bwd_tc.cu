@@ -65,6 +65,7 @@ struct BParams {
   unsigned long long wait_ns;
   uint32_t *sched;  // [2] the CTA-pair kernel's tile counter and done count (zero at launch)
   int dynamic;      // CTA-pair kernel: tiles from the counter (else round robin)
+  int tma_out;      // CTA-pair kernel, modes 0 and 1: 32-row groups leave by TMA store
 };
 
 // The CTA-pair kernel's tile ring, as in the forward expert GEMM: tile
@@ -146,13 +147,24 @@ __device__ __forceinline__ BTile locate(const BParams &p, const int *start, int 
 
 // One lane's row m of a finished tile: 32 accumulator columns at a time from
 // TMEM (lane_addr: this warp's lanes, this accumulator), stored as the mode
-// asks. Warp-collective (every lane loads).
+// asks. Warp-collective (every lane loads). Modes 0 and 1 in the CTA-pair
+// kernel pass stg (the warp's two staging tiles), tmO (the output [padded
+// rows, N]) and cnt: the warp's 32 rows, inside the expert's padded block
+// (its size is a multiple of 64), then leave by TMA store, mode 1's pad rows
+// included (zero, as dpre's pad rows are).
 template <int MODE>
 __device__ __forceinline__ void epilogue_rows(const BParams &p, const BTile &t, int m,
-                                              uint32_t lane_addr) {
+                                              uint32_t lane_addr, float *stg = nullptr,
+                                              const CUtensorMap *tmO = nullptr,
+                                              uint32_t *cnt = nullptr) {
+  const int m0 = m - (int)(threadIdx.x & 31);  // the warp's first row
+  const bool tma = MODE != 2 && stg != nullptr && m0 + 32 <= t.prows;
   // Rows this lane writes: mode 0 every padded row of the expert (pad rows
-  // as zero), mode 1 the real rows, mode 2 the output rows m < M.
-  const bool valid = MODE == 0 ? m < t.prows : (MODE == 1 ? m < t.rows : m < p.M);
+  // as zero), mode 1 the real rows (every padded row through TMA), mode 2 the
+  // output rows m < M.
+  const bool valid = MODE == 0 ? m < t.prows
+                     : MODE == 1 ? (tma || m < t.rows)
+                                 : m < p.M;
   const bool real = m < t.rows;
   const size_t pr = (size_t)t.prow0 + m;
   const size_t q = (size_t)p.offset[t.e] + m;
@@ -196,11 +208,17 @@ __device__ __forceinline__ void epilogue_rows(const BParams &p, const BTile &t, 
         __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
         packed[j] = *reinterpret_cast<uint32_t *>(&b2);
       }
-      uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + pr * p.N + n);
+      if (tma) {
+        stage_store_bf16(tmO, stg + (*cnt & 1u) * 1024, packed, n, t.prow0 + m0);
+        ++*cnt;
+      } else {
+        uint4 *o =
+            reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + pr * p.N + n);
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        o[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
-                          packed[4 * w + 3]);
+        for (int w = 0; w < 4; ++w)
+          o[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
+                            packed[4 * w + 3]);
+      }
     } else {
       float f[32];
 #pragma unroll
@@ -208,13 +226,18 @@ __device__ __forceinline__ void epilogue_rows(const BParams &p, const BTile &t, 
         f[j] = __uint_as_float(v[j]);
         bad |= !isfinite(f[j]);
       }
-      float *o = MODE == 1
-                     ? static_cast<float *>(p.out) + pr * p.N + n
-                     : static_cast<float *>(p.out) + ((size_t)t.e * p.M + m) * p.N + n;
+      if (tma) {
+        stage_store_f32(tmO, stg + (*cnt & 1u) * 1024, f, n, t.prow0 + m0);
+        ++*cnt;
+      } else {
+        float *o = MODE == 1
+                       ? static_cast<float *>(p.out) + pr * p.N + n
+                       : static_cast<float *>(p.out) + ((size_t)t.e * p.M + m) * p.N + n;
 #pragma unroll
-      for (int w = 0; w < 8; ++w)
-        reinterpret_cast<float4 *>(o)[w] =
-            make_float4(f[4 * w], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+        for (int w = 0; w < 8; ++w)
+          reinterpret_cast<float4 *>(o)[w] =
+              make_float4(f[4 * w], f[4 * w + 1], f[4 * w + 2], f[4 * w + 3]);
+      }
     }
   }
   if (MODE == 0 && valid) p.dgpart[pr * p.n_blocks + t.nb] = part;
@@ -513,7 +536,8 @@ __device__ __forceinline__ void epilogue_wgrad_tma(const BParams &p, const BTile
 }
 
 // tmO: mode 2's output dW as [E, M, N] fp32, box [1, 32, 32], 128-byte
-// swizzle (unused in modes 0 and 1).
+// swizzle; modes 0 and 1: the output [padded rows, N] (bf16 / fp32), box [32,
+// 32], when p.tma_out is set.
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -524,9 +548,8 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + P_STAGES * P_A_BYTES;
-  float *stg_all = reinterpret_cast<float *>(sB + P_STAGES * P_B_BYTES);  // mode 2 only
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES +
-                                                (MODE == 2 ? P_STG_BYTES : 0));
+  float *stg_all = reinterpret_cast<float *>(sB + P_STAGES * P_B_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + P_STAGES * P_B_BYTES + P_STG_BYTES);
   uint64_t *full = bars, *empty = bars + P_STAGES;
   uint64_t *acc_full = bars + 2 * P_STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
   uint64_t *tfull = drain + 1, *tempty = tfull + kRing;
@@ -734,7 +757,7 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const int r_in_tile = quad * 32 + lane;
     const uint32_t acc_empty_leader0 = mapa(smem_u32(&acc_empty[0]), 0);
     const uint32_t acc_empty_leader1 = mapa(smem_u32(&acc_empty[1]), 0);
-    float *stg = stg_all + (size_t)(warp - 2) * 2 * P_STG_TILE;  // mode 2
+    float *stg = stg_all + (size_t)(warp - 2) * 2 * P_STG_TILE;  // this warp's two tiles
     uint32_t stg_cnt = 0;
     for (int local = 0;; ++local) {
       const int slot = local % kRing;
@@ -764,12 +787,12 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if constexpr (MODE == 2)
         epilogue_wgrad_tma(p, t, m - lane, lane_addr, stg, &tmO, stg_cnt);
       else
-        epilogue_rows<MODE>(p, t, m, lane_addr);
+        epilogue_rows<MODE>(p, t, m, lane_addr, p.tma_out ? stg : nullptr, &tmO, &stg_cnt);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
-    if (MODE == 2 && lane == 0) bulk_wait_all();  // this warp's dW stores are complete
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
     pdl_trigger();
   }
   tc_fence_before();
@@ -783,7 +806,8 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 }
 
 constexpr size_t bwd_smem_bytes_pair(int E, int mode) {
-  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + (mode == 2 ? P_STG_BYTES : 0) +
+  (void)mode;
+  return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_STG_BYTES +
          (2 * P_STAGES + 5 + 2 * kRing) * 8 + 8 + (size_t)kRing * 4 + (size_t)(E + 1) * 4;
 }
 
@@ -951,9 +975,12 @@ cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) 
   if (!make_map(&ta, g.A, (uint64_t)g.a_rows, (uint64_t)g.K, BM) ||
       !make_map(&tb, g.B, (uint64_t)g.E * g.N, (uint64_t)g.K, cl > 0 ? BN / 2 : BN))
     return cudaErrorInvalidValue;
-  if (cl > 0)
-    return g.mode == 0 ? launch_mode_pair<0>(ta, tb, ta, p, cl, s)
-                       : launch_mode_pair<1>(ta, tb, ta, p, cl, s);
+  if (cl > 0) {
+    CUtensorMap to = ta;  // unused unless p.tma_out
+    p.tma_out = make_rows_map(&to, g.out, (uint64_t)g.a_rows, (uint64_t)g.N, g.mode == 1) ? 1 : 0;
+    return g.mode == 0 ? launch_mode_pair<0>(ta, tb, to, p, cl, s)
+                       : launch_mode_pair<1>(ta, tb, to, p, cl, s);
+  }
   return g.mode == 0 ? launch_mode<0>(ta, tb, p, s) : launch_mode<1>(ta, tb, p, s);
 }
 

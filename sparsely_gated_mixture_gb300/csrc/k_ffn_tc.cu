@@ -350,45 +350,6 @@ constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_STG_TILE = 32 * 32;  // floats
 constexpr int P_STG_BYTES = 4 * 2 * P_STG_TILE * 4;
 
-// One warp's 32 output rows x 32 columns, staged and sent by one TMA store at
-// column n, packed row r0 (tmO: the output [rows, N], box [32 rows, 32
-// columns]). The per-lane row stores send 32 rows' 16-byte pieces per
-// instruction and cost the GEMM 5-7% of its time; a TMA store writes whole row
-// segments. buf is the warp's staging tile for this chunk; before it is
-// written, the store that last read it (two chunks back) must have read it.
-__device__ __forceinline__ void stage_store_bf16(const CUtensorMap *tmO, float *buf,
-                                                 const uint32_t (&packed)[16], int n, int r0) {
-  const int lane = threadIdx.x & 31;
-  if (lane == 0) bulk_wait_read_but1();
-  __syncwarp();
-  uint4 *row = reinterpret_cast<uint4 *>(buf) + lane * 4;  // 64-byte rows
-  const int x = (lane >> 1) & 3;
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    row[q ^ x] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_2d(tmO, buf, n, r0);
-    bulk_commit();
-  }
-}
-__device__ __forceinline__ void stage_store_f32(const CUtensorMap *tmO, float *buf,
-                                                const float (&f)[32], int n, int r0) {
-  const int lane = threadIdx.x & 31;
-  if (lane == 0) bulk_wait_read_but1();
-  __syncwarp();
-  float4 *row = reinterpret_cast<float4 *>(buf) + lane * 8;  // 128-byte rows
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    row[q ^ (lane & 7)] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_2d(tmO, buf, n, r0);
-    bulk_commit();
-  }
-}
 // kind::f16, fp32 accumulate, bf16 A/B, A K-major, B MN-major, M = 256, N = 256.
 constexpr uint32_t kIdescPair = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                                 ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
@@ -803,6 +764,23 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
+// 2-D tensor [rows, cols] (cols % 8 == 0, 16-byte-aligned base) of bf16 or
+// fp32: an expert GEMM's output, box [32 rows, 32 columns] in the 64-byte
+// (bf16) or 128-byte (fp32) swizzle, for the CTA-pair kernel's TMA stores.
+bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, bool f32) {
+  auto fn = encode_fn();
+  if (!fn || (uintptr_t)base % 16 != 0 || cols % 8 != 0) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 unsigned long long wait_limit_ns() {
   const char *v = getenv("MOE_WAIT_LIMIT_NS");
   if (v && *v) return strtoull(v, nullptr, 10);
@@ -820,23 +798,6 @@ int sm_count() {
 }
 
 namespace {
-
-// 2-D tensor [rows, cols] (cols % 8 == 0, 16-byte-aligned base) of bf16 or
-// fp32: an expert GEMM's output, box [32 rows, 32 columns] in the 64-byte
-// (bf16) or 128-byte (fp32) swizzle, for the CTA-pair kernel's TMA stores.
-bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, bool f32) {
-  auto fn = encode_fn();
-  if (!fn || (uintptr_t)base % 16 != 0 || cols % 8 != 0) return false;
-  const uint64_t es = f32 ? 4 : 2;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * es};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base,
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 constexpr size_t smem_bytes(int E) {
   return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 8 + (size_t)(E + 1) * 4;

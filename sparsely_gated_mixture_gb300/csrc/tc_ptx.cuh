@@ -15,6 +15,10 @@ namespace moe {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box [box_rows, 64 cols], 128B swizzle.
 bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 2-D bf16 or fp32 tensor [rows, cols] (cols % 8 == 0, 16-byte-aligned base), box
+// [32 rows, 32 columns], 64-byte (bf16) or 128-byte (fp32) swizzle: a GEMM's
+// output for stage_store_bf16 / stage_store_f32. False if it cannot be made.
+bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, bool f32);
 int sm_count();
 // Limit of every bounded mbarrier wait, in ns: MOE_WAIT_LIMIT_NS if set (read
 // at each launch, so a test can shorten it to force the timeout path), else 2 s.
@@ -226,6 +230,48 @@ __device__ __forceinline__ void tmem_ld16x3(uint32_t a0, uint32_t a1, uint32_t a
         "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47])
       : "r"(a0), "r"(a1), "r"(a2)
       : "memory");
+}
+
+// One warp's 32 output rows x 32 columns of a GEMM epilogue (lane l holds row
+// l), staged in shared memory and sent by one TMA store at column n, row r0
+// (tmO: the output [rows, N], box [32 rows, 32 columns]; bf16 in the 64-byte
+// swizzle, fp32 in the 128-byte swizzle). Per-lane row stores send 32 rows'
+// 16-byte pieces per instruction; a TMA store writes whole row segments. buf
+// (4 KB, 1024-byte aligned) is one of the warp's two staging tiles, used in
+// turn: before it is written, the store that last read it (two chunks back)
+// must have read it.
+__device__ __forceinline__ void stage_store_bf16(const CUtensorMap *tmO, float *buf,
+                                                 const uint32_t (&packed)[16], int n, int r0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_but1();
+  __syncwarp();
+  uint4 *row = reinterpret_cast<uint4 *>(buf) + lane * 4;  // 64-byte rows
+  const int x = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    row[q ^ x] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, buf, n, r0);
+    bulk_commit();
+  }
+}
+__device__ __forceinline__ void stage_store_f32(const CUtensorMap *tmO, float *buf,
+                                                const float (&f)[32], int n, int r0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_but1();
+  __syncwarp();
+  float4 *row = reinterpret_cast<float4 *>(buf) + lane * 8;  // 128-byte rows
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    row[q ^ (lane & 7)] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, buf, n, r0);
+    bulk_commit();
+  }
 }
 
 // ----------------------------------------------------------------------------- CTA pairs
