@@ -40,6 +40,10 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BK * BN * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;     // two accumulators
+// One-CTA kernel's epilogue staging for bf16 output: per epilogue warp two
+// 2 KB [32 rows x 32 columns] tiles (64-byte swizzle).
+constexpr int STG_TILE = 32 * 32 / 2;  // 2 KB, counted in floats
+constexpr int STG_BYTES = 4 * 2 * STG_TILE * 4;
 
 struct Params {
   int K, N, E, n_blocks;
@@ -90,10 +94,12 @@ struct TileMap {
   }
 };
 
+// tmO: the bf16 output [rows, N], box [32 rows, 32 columns], 64-byte swizzle,
+// used when p.tma_out is set (layer 1, and layer 2 with Z in bf16).
 template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-         const Params p) {
+         const __grid_constant__ CUtensorMap tmO, const Params p) {
   pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128B-swizzle atoms.
@@ -101,7 +107,8 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  float *stg_all = reinterpret_cast<float *>(sB + STAGES * B_BYTES);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES + STG_BYTES);
   uint64_t *full = bars, *empty = bars + STAGES;
   uint64_t *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 2, *drain = acc_empty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -236,6 +243,9 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     // ----------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     const int r_in_tile = quad * 32 + lane;
+    float *stg = stg_all + (size_t)(warp - 2) * 2 * STG_TILE;  // this warp's two tiles
+    uint32_t stg_cnt = 0;
+    const bool out_bf16 = LAYER == 1 || p.z_bf16;
     int local = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
       int e, mb, nb, row0, rows;
@@ -251,6 +261,10 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       const bool valid = m < rows;
       const size_t r = (size_t)row0 + m;
       const float g = (LAYER == 2 && valid) ? p.row_gate[r] : 1.f;
+      // bf16 output of a warp whose 32 rows all belong to this expert leaves
+      // by TMA store (a partial group would spill into the next expert's rows).
+      const bool tma_rows = p.tma_out && out_bf16 && m - lane + 32 <= rows;
+      const int r0 = row0 + m - lane;
       bool bad = false;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -266,18 +280,24 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
           f[j] = __uint_as_float(v[j]);
           if (p.bias) f[j] += __bfloat162float(p.bias[(size_t)e * p.N + n + j]);
         }
+        float *sbuf = stg + (stg_cnt & 1u) * STG_TILE;
         if (LAYER == 1) {
-          __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
           uint32_t packed[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             __nv_bfloat162 h2 = __floats2bfloat162_rn(fmaxf(f[2 * j], 0.f), fmaxf(f[2 * j + 1], 0.f));
             packed[j] = *reinterpret_cast<uint32_t *>(&h2);
           }
+          if (tma_rows) {
+            stage_store_bf16(&tmO, sbuf, packed, n, r0);
+            ++stg_cnt;
+          } else {
+            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            reinterpret_cast<uint4 *>(o)[q] =
-                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                           packed[4 * q + 2], packed[4 * q + 3]);
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -285,17 +305,22 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
             bad |= !isfinite(f[j]);
           }
           if (p.z_bf16) {
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
               packed[j] = *reinterpret_cast<uint32_t *>(&h2);
             }
+            if (tma_rows) {
+              stage_store_bf16(&tmO, sbuf, packed, n, r0);
+              ++stg_cnt;
+            } else {
+              __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + r * p.N + n;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
-                                                           packed[4 * q + 2], packed[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
+                                                             packed[4 * q + 2], packed[4 * q + 3]);
+            }
           } else {
             float *o = static_cast<float *>(p.out) + r * p.N + n;
 #pragma unroll
@@ -310,6 +335,7 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
     pdl_trigger();
   }
   tc_fence_before();
@@ -800,17 +826,18 @@ int sm_count() {
 namespace {
 
 constexpr size_t smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + (2 * STAGES + 5) * 8 + 8 + (size_t)(E + 1) * 4;
+  return 1024 + (size_t)STAGES * STAGE_BYTES + STG_BYTES + (2 * STAGES + 5) * 8 + 8 +
+         (size_t)(E + 1) * 4;
 }
 
 template <int LAYER>
-cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const Params &p,
-                         cudaStream_t s) {
+cudaError_t launch_layer(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &o,
+                         const Params &p, cudaStream_t s) {
   const size_t smem = smem_bytes(p.E);
   cudaError_t err = cudaFuncSetAttribute(k_ffn_tc<LAYER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  launch_pdl_c(kPdlGemm, k_ffn_tc<LAYER>, sm_count(), kThreads, smem, s, a, b, p);
+  launch_pdl_c(kPdlGemm, k_ffn_tc<LAYER>, sm_count(), kThreads, smem, s, a, b, o, p);
   return cudaGetLastError();
 }
 
@@ -945,10 +972,10 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
   if (!p1.tma_out) to1 = ta1;  // unused
   if (!p2.tma_out) to2 = ta2;
   cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, to1, p1, clusters, s)
-                                          : launch_layer<1>(ta1, tb1, p1, s);
+                                          : launch_layer<1>(ta1, tb1, to1, p1, s);
   if (err != cudaSuccess) return err;
   return pair_for(c.d_ff, c.d) ? launch_layer_pair<2>(ta2, tb2, to2, p2, clusters, s)
-                               : launch_layer<2>(ta2, tb2, p2, s);
+                               : launch_layer<2>(ta2, tb2, to2, p2, s);
 }
 
 }  // namespace moe
