@@ -790,7 +790,7 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         epilogue_rows<MODE>(p, t, m, lane_addr, p.tma_out ? stg : nullptr, &tmO, &stg_cnt);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
+      if (lane == 0) mbar_arrive_remote(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
     if (lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
     pdl_trigger();

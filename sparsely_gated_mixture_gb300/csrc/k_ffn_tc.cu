@@ -744,7 +744,7 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (bad) record_error(p.st, MOE_ERR_NONFINITE, (long long)r);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? acc_empty_leader1 : acc_empty_leader0);
+      if (lane == 0) mbar_arrive_remote(buf ? acc_empty_leader1 : acc_empty_leader0);
     }
     if (lane == 0) bulk_wait_all();  // this warp's TMA stores are complete
     pdl_trigger();
