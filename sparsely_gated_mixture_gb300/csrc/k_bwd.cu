@@ -446,6 +446,85 @@ k_bwd_xtd(int T, int d, int E, int NC, int tpc, const XT *__restrict__ x,
   pdl_trigger();
 }
 
+// The same partials for a narrow router (NC = E or 2E columns, NC <= 32, E a
+// multiple of 4, bf16 x), together with the router's share of dx, in one
+// pass. Thread i of block (256-feature tile, token chunk) owns feature i: per
+// step of TT tokens it loads its x[t][i] for all TT tokens at once (the
+// block's loads of a token are 512 contiguous bytes, and TT of them are in
+// flight per thread), the block stages the TT rows of D in shared memory, and
+// the thread adds x[t][i] D[t][col] to its NC sums and (with dxr) stores
+// dxr[t][i] = sum_col D[t][col] W'[col][i] from W' values held in registers.
+// The tiled kernels above take 64 x 32 output tiles with K = the tokens;
+// at NC = 16 half their threads computed zero columns, and dxr went through
+// a second pass over D.
+constexpr int kNarrowNC = 32;
+constexpr int kNarrowFeat = 256;  // features per block
+
+template <int NCM, int TT>  // NCM >= NC, a multiple of 4; TT tokens per step
+__global__ void __launch_bounds__(256)
+k_bwd_router_narrow(int T, int d, int E, int NC, int tpc, const __nv_bfloat16 *__restrict__ x,
+                    const float *__restrict__ dc, const float *__restrict__ dz,
+                    const float *__restrict__ Wg, const float *__restrict__ Wn,
+                    float *__restrict__ part, float *__restrict__ bpart,
+                    float *__restrict__ dxr) {
+  pdl_wait();
+  __shared__ __align__(16) float Ds[TT][NCM];
+  const int i = blockIdx.x * kNarrowFeat + threadIdx.x, sidx = blockIdx.y;
+  const int t_begin = sidx * tpc, t_end = min(T, t_begin + tpc);
+  const bool feat = i < d;
+  float w[NCM], acc[NCM];
+#pragma unroll
+  for (int c = 0; c < NCM; ++c) {
+    acc[c] = 0.f;
+    w[c] = 0.f;
+    if (dxr && feat && c < NC) w[c] = c < E ? Wg[(size_t)i * E + c] : Wn[(size_t)i * E + c - E];
+  }
+  const bool bcol = blockIdx.x == 0 && (int)threadIdx.x < NC;  // the bias column sums
+  float bsum = 0.f;
+  for (int tb = t_begin; tb < t_end; tb += TT) {
+    const int nt = min(TT, t_end - tb);
+    float xv[TT];
+#pragma unroll
+    for (int u = 0; u < TT; ++u)
+      xv[u] = (feat && u < nt) ? __bfloat162float(x[(size_t)(tb + u) * d + i]) : 0.f;
+    __syncthreads();  // the previous step's rows of D are no longer read
+    for (int q = threadIdx.x; q < TT * NCM; q += blockDim.x) {
+      const int u = q / NCM, c = q - u * NCM;
+      float v = 0.f;
+      if (u < nt && c < NC)
+        v = c < E ? dc[(size_t)(tb + u) * E + c] : dz[(size_t)(tb + u) * E + c - E];
+      Ds[u][c] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < TT; ++u) {
+      float D[NCM];
+#pragma unroll
+      for (int q = 0; q < NCM / 4; ++q) {
+        const float4 v = reinterpret_cast<const float4 *>(Ds[u])[q];
+        D[4 * q] = v.x;
+        D[4 * q + 1] = v.y;
+        D[4 * q + 2] = v.z;
+        D[4 * q + 3] = v.w;
+      }
+      float r = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCM; ++c) {
+        acc[c] = fmaf(xv[u], D[c], acc[c]);
+        r = fmaf(D[c], w[c], r);
+      }
+      if (dxr && feat && u < nt) dxr[(size_t)(tb + u) * d + i] = r;
+      if (bcol) bsum += Ds[u][threadIdx.x];
+    }
+  }
+  if (feat)
+#pragma unroll
+    for (int c = 0; c < NCM; ++c)
+      if (c < NC) part[((size_t)sidx * d + i) * NC + c] = acc[c];
+  if (bcol) bpart[(size_t)sidx * NC + threadIdx.x] = bsum;
+  pdl_trigger();
+}
+
 // Sum the partials over the token chunks in order: dWg [d,E], dWn [d,E], dbias [E].
 __global__ void k_bwd_xtd_reduce(int d, int E, int NC, int S, const float *__restrict__ part,
                                  const float *__restrict__ bpart, float *__restrict__ dWg,
@@ -618,8 +697,14 @@ int grid_for(long long work, int per_block) {
 
 }  // namespace
 
+// Token chunks of the router's weight-gradient partials: about four blocks
+// per SM for whichever kernel runs (the narrow one for NC <= 32 columns, one
+// block per 256 features; the tiled one per 64 x 32 tile).
 int xtd_splits(int T, int d, int NC) {
-  const long long tiles = (long long)((d + kXtdTI - 1) / kXtdTI) * ((NC + kXtdTC - 1) / kXtdTC);
+  const long long tiles =
+      NC <= kNarrowNC
+          ? (long long)((d + kNarrowFeat - 1) / kNarrowFeat)
+          : (long long)((d + kXtdTI - 1) / kXtdTI) * ((NC + kXtdTC - 1) / kXtdTC);
   long long S = (4LL * sm_count() + tiles - 1) / tiles;
   const long long maxS = (T + kXtdTT - 1) / kXtdTT;
   if (S > maxS) S = maxS;
@@ -683,6 +768,20 @@ cudaError_t launch_bwd_router(const moe_config &c, bool noisy, const void *x, co
   const int NC = noisy ? 2 * c.E : c.E;
   const int S = xtd_splits(c.T, c.d, NC);  // part holds S * d * NC, bpart S * NC floats
   const int tpc = ((c.T + S - 1) / S + kXtdTT - 1) / kXtdTT * kXtdTT;
+  if (c.act_dtype == MOE_BF16 && NC <= kNarrowNC && c.E % 4 == 0) {
+    // One pass for the weight gradients' partials and the share of dx.
+    const dim3 gn((c.d + kNarrowFeat - 1) / kNarrowFeat, S);
+    cudaError_t err =
+        NC <= 16 ? launch_pdl(k_bwd_router_narrow<16, 32>, gn, 256, 0, s, c.T, c.d, c.E, NC, tpc,
+                              static_cast<const __nv_bfloat16 *>(x), dc, dz, Wg, Wn, part, bpart,
+                              dxr)
+                 : launch_pdl(k_bwd_router_narrow<kNarrowNC, 16>, gn, 256, 0, s, c.T, c.d, c.E,
+                              NC, tpc, static_cast<const __nv_bfloat16 *>(x), dc, dz, Wg, Wn,
+                              part, bpart, dxr);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_bwd_xtd_reduce, grid_for((long long)c.d * NC + NC, 256), 256, 0, s, c.d,
+                      c.E, NC, S, (const float *)part, (const float *)bpart, dWg, dWn, dbias);
+  }
   const dim3 g1((c.d + kXtdTI - 1) / kXtdTI, (NC + kXtdTC - 1) / kXtdTC, S);
   cudaError_t err =
       c.act_dtype == MOE_BF16
