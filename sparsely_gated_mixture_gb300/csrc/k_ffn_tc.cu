@@ -57,7 +57,8 @@ struct Params {
   DeviceStatus *st;
   unsigned long long wait_ns;  // bounded-wait limit
   int z_bf16;                  // layer 2 writes Z in bf16
-  int tma_out;                 // CTA-pair kernel: whole 32-row groups leave by TMA store
+  int tma_out;                 // whole 32-row groups of the output leave by TMA store
+                               // (the one-CTA kernel: bf16 output only)
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
