@@ -45,7 +45,7 @@ NOMINAL_HBM_GBS = 8000.0  # the part's nominal HBM3e rate, reported beside the m
 # hash was re-keyed once, when the cluster PTX wrappers moved unchanged from
 # k_ffn_tc.cu into tc_ptx.cuh (ptxas reports the same registers, spills and
 # shared memory for every FFN kernel before and after the move).
-FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4113976064, "source": "6324699bfe56680b"}}
+FFN_TRAFFIC = {"top2_large_experts": {"bytes": 4113976064, "source": "747f294c0679d9fb"}}
 
 
 class nvtx:
@@ -78,12 +78,12 @@ class nvtx:
 
 
 def _code_only(src: str) -> str:
-    """CUDA source without its comments and blank-line layout, so that a
-    comment edit keeps a traffic record that the code still matches."""
+    """CUDA source without its comments, blank lines and indentation, so that
+    a comment edit keeps a traffic record that the code still matches."""
     import re
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
-    return "\n".join(l.rstrip() for l in src.splitlines() if l.strip())
+    return "\n".join(l.strip() for l in src.splitlines() if l.strip())
 
 
 def ffn_source_hash() -> str:

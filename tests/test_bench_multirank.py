@@ -100,3 +100,17 @@ def test_reference_arm_training_step():
     assert "fwd+bwd" in rec["metric"] and rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["config"]["workload"] == "noisy_top4_e16"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_record_keys_on_code_not_comments():
+    """The measured expert-GEMM traffic is reported only for the kernel code
+    it was captured on: comment and blank-line edits keep the key, a code
+    edit changes it, and the recorded key is the current source's."""
+    src = "// note\nint f(int a) {  // why\n  /* more\n text */ return a + 1;\n}\n\n"
+    same = "int f(int a) {\n\n  return a + 1;   // other words\n}\n"
+    other = "int f(int a) {\n  return a + 2;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    rec = bench.FFN_TRAFFIC["top2_large_experts"]
+    assert rec["source"] == bench.ffn_source_hash()
+    assert bench.measured_traffic(bench.wl.WORKLOADS["top2_large_experts"]) == rec["bytes"]
