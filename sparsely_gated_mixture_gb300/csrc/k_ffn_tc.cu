@@ -40,8 +40,9 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BK * BN * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;     // two accumulators
-// One-CTA kernel's epilogue staging for bf16 output: per epilogue warp two
-// 2 KB [32 rows x 32 columns] tiles (64-byte swizzle).
+// One-CTA kernel's epilogue staging: per epilogue warp two 2 KB tiles, each
+// [32 rows x 32 columns] of bf16 output or [32 x 16] of fp32 (64-byte rows,
+// 64-byte swizzle).
 constexpr int STG_TILE = 32 * 32 / 2;  // 2 KB, counted in floats
 constexpr int STG_BYTES = 4 * 2 * STG_TILE * 4;
 
@@ -58,7 +59,6 @@ struct Params {
   unsigned long long wait_ns;  // bounded-wait limit
   int z_bf16;                  // layer 2 writes Z in bf16
   int tma_out;                 // whole 32-row groups of the output leave by TMA store
-                               // (the one-CTA kernel: bf16 output only)
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -95,8 +95,9 @@ struct TileMap {
   }
 };
 
-// tmO: the bf16 output [rows, N], box [32 rows, 32 columns], 64-byte swizzle,
-// used when p.tma_out is set (layer 1, and layer 2 with Z in bf16).
+// tmO: the output [rows, N] when p.tma_out is set: bf16 with a [32 rows, 32
+// columns] box, or fp32 (layer 2's Z) with a [32 rows, 16 columns] box, both
+// in the 64-byte swizzle.
 template <int LAYER>
 __global__ void __launch_bounds__(kThreads, 1)
 k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -246,7 +247,6 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
     const int r_in_tile = quad * 32 + lane;
     float *stg = stg_all + (size_t)(warp - 2) * 2 * STG_TILE;  // this warp's two tiles
     uint32_t stg_cnt = 0;
-    const bool out_bf16 = LAYER == 1 || p.z_bf16;
     int local = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++local) {
       int e, mb, nb, row0, rows;
@@ -262,9 +262,9 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
       const bool valid = m < rows;
       const size_t r = (size_t)row0 + m;
       const float g = (LAYER == 2 && valid) ? p.row_gate[r] : 1.f;
-      // bf16 output of a warp whose 32 rows all belong to this expert leaves
-      // by TMA store (a partial group would spill into the next expert's rows).
-      const bool tma_rows = p.tma_out && out_bf16 && m - lane + 32 <= rows;
+      // The output of a warp whose 32 rows all belong to this expert leaves by
+      // TMA store (a partial group would spill into the next expert's rows).
+      const bool tma_rows = p.tma_out && m - lane + 32 <= rows;
       const int r0 = row0 + m - lane;
       bool bad = false;
 #pragma unroll 1
@@ -322,6 +322,12 @@ k_ffn_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtens
                 reinterpret_cast<uint4 *>(o)[q] = make_uint4(packed[4 * q], packed[4 * q + 1],
                                                              packed[4 * q + 2], packed[4 * q + 3]);
             }
+          } else if (tma_rows) {
+            // fp32: the chunk's two 16-column halves, one staging tile each
+            stage_store_f32x16(&tmO, sbuf, f, n, r0);
+            ++stg_cnt;
+            stage_store_f32x16(&tmO, stg + (stg_cnt & 1u) * STG_TILE, f + 16, n + 16, r0);
+            ++stg_cnt;
           } else {
             float *o = static_cast<float *>(p.out) + r * p.N + n;
 #pragma unroll
@@ -808,6 +814,18 @@ bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, boo
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_rows_map16(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn || (uintptr_t)base % 16 != 0 || cols % 8 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 unsigned long long wait_limit_ns() {
   const char *v = getenv("MOE_WAIT_LIMIT_NS");
   if (v && *v) return strtoull(v, nullptr, 10);
@@ -967,16 +985,25 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
            (force_pair || (K >= 2048 && (rows / 256) * ((N + BN - 1) / BN) >= 4L * clusters));
   };
   // The CTA-pair kernel's output maps (H, then Z): box [32 rows, 32 columns].
-  CUtensorMap to1, to2;
+  // The one-CTA kernel stores fp32 Z in 16-column boxes (its staging tiles
+  // are 2 KB).
+  CUtensorMap to1, to2, to2s;
   p1.tma_out = make_rows_map(&to1, hbuf, A, c.d_ff, false) ? 1 : 0;
   p2.tma_out = make_rows_map(&to2, zbuf, A, c.d, !z_bf16) ? 1 : 0;
   if (!p1.tma_out) to1 = ta1;  // unused
   if (!p2.tma_out) to2 = ta2;
+  Params p2s = p2;
+  if (z_bf16) {
+    to2s = to2;
+  } else {
+    p2s.tma_out = make_rows_map16(&to2s, zbuf, A, c.d) ? 1 : 0;
+    if (!p2s.tma_out) to2s = ta2;
+  }
   cudaError_t err = pair_for(c.d, c.d_ff) ? launch_layer_pair<1>(ta1, tb1, to1, p1, clusters, s)
                                           : launch_layer<1>(ta1, tb1, to1, p1, s);
   if (err != cudaSuccess) return err;
   return pair_for(c.d_ff, c.d) ? launch_layer_pair<2>(ta2, tb2, to2, p2, clusters, s)
-                               : launch_layer<2>(ta2, tb2, to2, p2, s);
+                               : launch_layer<2>(ta2, tb2, to2s, p2s, s);
 }
 
 }  // namespace moe

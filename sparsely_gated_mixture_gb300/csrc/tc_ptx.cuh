@@ -19,6 +19,9 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, ui
 // [32 rows, 32 columns], 64-byte (bf16) or 128-byte (fp32) swizzle: a GEMM's
 // output for stage_store_bf16 / stage_store_f32. False if it cannot be made.
 bool make_rows_map(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols, bool f32);
+// The same for fp32 with a [32 rows, 16 columns] box (64-byte rows, 64-byte
+// swizzle), for stage_store_f32x16.
+bool make_rows_map16(CUtensorMap *m, void *base, uint64_t rows, uint64_t cols);
 int sm_count();
 // Limit of every bounded mbarrier wait, in ns: MOE_WAIT_LIMIT_NS if set (read
 // at each launch, so a test can shorten it to force the timeout path), else 2 s.
@@ -266,6 +269,26 @@ __device__ __forceinline__ void stage_store_f32(const CUtensorMap *tmO, float *b
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     row[q ^ (lane & 7)] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmO, buf, n, r0);
+    bulk_commit();
+  }
+}
+
+// The same for 16 fp32 columns (64-byte rows in the 64-byte swizzle, the
+// [32 x 16] box of make_rows_map16): f points at this lane's 16 values.
+__device__ __forceinline__ void stage_store_f32x16(const CUtensorMap *tmO, float *buf,
+                                                   const float *f, int n, int r0) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) bulk_wait_read_but1();
+  __syncwarp();
+  float4 *row = reinterpret_cast<float4 *>(buf) + lane * 4;  // 64-byte rows
+  const int x = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    row[q ^ x] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
