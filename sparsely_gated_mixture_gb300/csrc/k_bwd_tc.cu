@@ -66,6 +66,7 @@ struct BParams {
   uint32_t *sched;  // [2] the CTA-pair kernel's tile counter and done count (zero at launch)
   int dynamic;      // CTA-pair kernel: tiles from the counter (else round robin)
   int tma_out;      // CTA-pair kernel, modes 0 and 1: 32-row groups leave by TMA store
+  int snake;        // CTA-pair kernel: 1 = odd waves of tiles run K backwards, 2 = all do
 };
 
 // The CTA-pair kernel's tile ring, as in the forward expert GEMM: tile
@@ -657,6 +658,9 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (tile >= total_tiles) break;
         const BTile t = locate_pair<MODE>(p, tile_start, tile);
         const int take_at = t.num_kb > 4 ? t.num_kb - 4 : 0;
+        // Odd waves of tiles walk K from the end, starting on the blocks the
+        // wave before read last (still in L2); the order is fixed per tile.
+        const bool rev = p.snake == 2 || (p.snake == 1 && ((tile / n_pairs) & 1));
         for (int kb = 0; kb < t.num_kb; ++kb, ++it) {
           if (leader && p.dynamic && kb == take_at) taken = atomicAdd(p.sched, 1u);
           const int s = it % P_STAGES;
@@ -665,15 +669,16 @@ k_bwd_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             ok = false;
             break;
           }
+          const int kx = (rev ? t.num_kb - 1 - kb : kb) * BK;
           const uint32_t full_leader = mapa(smem_u32(&full[s]), 0);
           if (leader) mbar_expect_tx(&full[s], 2 * P_STAGE_BYTES);
           if (MODE != 2) {
-            tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kb * BK,
+            tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kx,
                              t.prow0 + t.mb * 2 * BM + (int)rank * BM);
-            tma_load_2d_pair(sB + s * P_B_BYTES, &tmB, full_leader, kb * BK,
+            tma_load_2d_pair(sB + s * P_B_BYTES, &tmB, full_leader, kx,
                              t.e * p.N + t.nb * BN + (int)rank * (BN / 2));
           } else {
-            const int arow = p.offset[t.e] + kb * BK, brow = t.prow0 + kb * BK;
+            const int arow = p.offset[t.e] + kx, brow = t.prow0 + kx;
             const int mcol = t.mb * 2 * BM + (int)rank * BM;
             const int ncol = t.nb * BN + (int)rank * (BN / 2);
 #pragma unroll
@@ -954,6 +959,9 @@ cudaError_t launch_bwd_gemm(const BwdGemm &g, DeviceStatus *st, cudaStream_t s) 
   {
     const char *v = getenv("MOE_FFN_SCHED");  // =static: round robin (for comparisons)
     p.dynamic = v && v[0] == 's' ? 0 : 1;
+    // =0: every tile's K forward, =all: every tile's backwards (comparisons, tests)
+    const char *sv = getenv("MOE_FFN_SNAKE");
+    p.snake = !sv || !*sv ? 1 : (sv[0] == '0' ? 0 : (sv[0] == 'a' ? 2 : 1));
   }
   const long long nb = (g.N + BN - 1) / BN;
   if (g.mode == 2) {

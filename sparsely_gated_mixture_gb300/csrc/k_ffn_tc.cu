@@ -59,6 +59,8 @@ struct Params {
   unsigned long long wait_ns;  // bounded-wait limit
   int z_bf16;                  // layer 2 writes Z in bf16
   int tma_out;                 // whole 32-row groups of the output leave by TMA store
+  int snake;                   // CTA-pair kernel: 1 = odd waves of tiles run K backwards,
+                               // 2 = every tile does (0 = none)
 };
 
 // Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, A K-major,
@@ -553,6 +555,12 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int ncol = nb * BN + (int)rank * P_BN_HALF;
         const int brow = e * p.K;
         const int take_at = num_kb > 4 ? num_kb - 4 : 0;
+        // Tiles of odd waves (tile / pairs) walk K from the end: their first
+        // K blocks are the ones the wave before read last, so the operand
+        // rows and stripes the two waves share are still in L2. The sum's
+        // order is fixed by the tile, so results do not depend on which
+        // pair takes it.
+        const bool rev = p.snake == 2 || (p.snake == 1 && ((tile / n_pairs) & 1));
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           if (leader && p.dynamic && kb == take_at) taken = atomicAdd(p.sched, 1u);
           const int s = it % P_STAGES;
@@ -561,13 +569,14 @@ k_ffn_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             ok = false;
             break;
           }
+          const int kx = (rev ? num_kb - 1 - kb : kb) * BK;
           const uint32_t full_leader = mapa(smem_u32(&full[s]), 0);
           if (leader) mbar_expect_tx(&full[s], 2 * P_STAGE_BYTES);
-          tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kb * BK, arow);
+          tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, full_leader, kx, arow);
 #pragma unroll
           for (int q = 0; q < P_BN_HALF / 64; ++q)
             tma_load_2d_pair(sB + s * P_B_BYTES + q * (BK * 128), &tmB, full_leader,
-                             ncol + q * 64, brow + kb * BK);
+                             ncol + q * 64, brow + kx);
         }
       }
       // This CTA's copies have landed once the MMAs that read them are done.
@@ -934,6 +943,15 @@ int ffn_dynamic() {
   return v && v[0] == 's' ? 0 : 1;
 }
 
+// MOE_FFN_SNAKE=0 keeps every CTA-pair tile's K order forward, =all runs
+// every tile backwards (read at each call; for comparisons and tests);
+// otherwise odd waves run backwards.
+int ffn_snake() {
+  const char *v = getenv("MOE_FFN_SNAKE");
+  if (!v || !*v) return 1;
+  return v[0] == '0' ? 0 : (v[0] == 'a' ? 2 : 1);
+}
+
 // MOE_FFN_TC_VARIANT=single or =pair forces one kernel (read at each call);
 // otherwise the rule in launch_ffn_tc picks per layer.
 int ffn_variant() {
@@ -992,6 +1010,7 @@ cudaError_t launch_ffn_tc(const moe_config &c, int C, const void *xbuf, const in
   p2.tma_out = make_rows_map(&to2, zbuf, A, c.d, !z_bf16) ? 1 : 0;
   if (!p1.tma_out) to1 = ta1;  // unused
   if (!p2.tma_out) to2 = ta2;
+  p1.snake = p2.snake = ffn_snake();
   Params p2s = p2;
   if (z_bf16) {
     to2s = to2;

@@ -212,15 +212,19 @@ def _check(got, ref, lim, what, norm=True):
         assert np.linalg.norm(got - ref) <= 2e-2 * nr + 1e-6, (what, np.linalg.norm(got - ref), nr)
 
 
-@pytest.mark.parametrize("variant", ["auto", "single", "pair"])
+@pytest.mark.parametrize("variant", ["auto", "single", "pair", "pair_k_backwards"])
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_backward_matches_oracle(name, variant, monkeypatch):
     """variant: the expert GEMMs' kernel as the library picks it, or forced
-    to the one-CTA or the CTA-pair form."""
+    to the one-CTA or the CTA-pair form; pair_k_backwards also makes every
+    CTA-pair tile walk K from its last block (by default only the odd waves
+    of tiles do, which these small layers never reach)."""
     if variant != "auto":
         if name in SIMT:
             pytest.skip("the CUDA-core expert backward has one form")
-        monkeypatch.setenv("MOE_BWD_TC_VARIANT", variant)
+        monkeypatch.setenv("MOE_BWD_TC_VARIANT", variant.split("_")[0])
+        if variant == "pair_k_backwards":
+            monkeypatch.setenv("MOE_FFN_SNAKE", "all")
     w, weights = CASES[name]
     seed = 11
     inp = wl.generate(w, seed=seed, biases=True)

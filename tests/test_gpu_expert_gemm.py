@@ -24,10 +24,12 @@ def _bf16(a):
 PAIR_TAILS = [[40, 0, 296, 128, 129, 384, 1], [256, 257, 511, 64]]
 
 
+SHAPES = [([130, 0, 257], 128, 320), ([1, 128, 64], 64, 64), ([300, 5], 256, 512),
+          (PAIR_TAILS[0], 128, 320), (PAIR_TAILS[1], 192, 256)]
+
+
 @pytest.mark.parametrize("variant", ["", "single", "pair"])
-@pytest.mark.parametrize("rows,d,d_ff", [([130, 0, 257], 128, 320), ([1, 128, 64], 64, 64),
-                                         ([300, 5], 256, 512), (PAIR_TAILS[0], 128, 320),
-                                         (PAIR_TAILS[1], 192, 256)])
+@pytest.mark.parametrize("rows,d,d_ff", SHAPES)
 def test_expert_ffn_against_numpy(rows, d, d_ff, variant, monkeypatch):
     monkeypatch.setenv("MOE_FFN_TC_VARIANT", variant)
     rng = np.random.default_rng(3)
@@ -64,3 +66,13 @@ def test_expert_ffn_against_numpy(rows, d, d_ff, variant, monkeypatch):
         Zref = g[r0:r1, None] * (H[r0:r1] @ W2[e].astype(np.float64) + b2[e])
         err = np.abs(Z[r0:r1] - Zref)
         assert np.all(err <= 1e-3 * (1 + np.abs(Zref))), f"layer 2 expert {e}: {err.max():.3e}"
+
+
+@pytest.mark.parametrize("rows,d,d_ff", SHAPES)
+def test_pair_kernel_k_backwards(rows, d, d_ff, monkeypatch):
+    """The CTA-pair kernel with every tile walking K from its last block
+    (MOE_FFN_SNAKE=all). By default only the odd waves of tiles do, which
+    these small layers (fewer tiles than pairs) never reach; the full-size
+    layers of test_gpu_parity.py run both directions."""
+    monkeypatch.setenv("MOE_FFN_SNAKE", "all")
+    test_expert_ffn_against_numpy(rows, d, d_ff, "pair", monkeypatch)
